@@ -1,0 +1,401 @@
+"""Float64 CPU oracle of the SpargeAttn two-stage sparse attention forward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may import this module.  The CUDA library never calls it, and it shares
+no code with the CUDA library.
+
+Sources (page titles of the SpargeAttn material, cited by section):
+  [abstract]  "SpargeAttention: Accurate and Training-free Sparse Attention Accelerating Any
+              Model Inference" (paper abstract page) -- two-stage online filter: stage 1
+              predicts the attention map so some matrix multiplications are skipped; stage 2
+              is an online softmax-aware filter that skips further updates.
+  [summary]   same title (paper summary page), method paragraph -- blocks with high internal
+              similarity are compressed, non-similar blocks are always computed, the second
+              filter works at GPU-warp level, Hilbert-curve reordering for visual tokens.
+  [overview]  "SpargeAttn: accelerate LLM inference without training" -- plug-and-play API
+              ``f(q, k, v, topk=0.5, is_causal=False)``, drop-in for scaled_dot_product_attention,
+              per-head block mask of shape (B, H, ceil(N/128), ceil(N/64)), fixed 128x64 blocks,
+              topk in (0, 1], lower is sparser.
+  [readme-cn] "SpargeAttention" (Chinese README): custom block-sparse mask API; the mask is made
+              of 0 and 1 with 1 meaning the block is kept; topk=0.5 keeps the top 50% of the
+              attention weights.
+
+Where the pages leave a step open, the reading taken is stated at the function that takes it.
+Every function computes in float64 on inputs that are the bf16 values upcast exactly.
+
+Parity status: pool_sim, pooled_scores, topk_select, predict_mask, block_sparse_attn,
+sparge_attn, the Hilbert orderings and the token permutation are pinned by the tests
+(closed forms, brute force, library routines, textbook curves).  The 8-bit path has no
+oracle of its own rounding: it is checked only by tolerance against block_sparse_attn.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Tuple
+
+import numpy as np
+
+QBLK = 128       # query tokens per block  [overview: "128x64 block granularity"]
+KBLK = 64        # key tokens per block
+WARP_ROWS = 32   # rows whose P.V update is skipped together  [summary: "at the GPU warp level"]
+
+
+def n_blocks(N: int, blk: int) -> int:
+    return -(-N // blk)
+
+
+def default_scale(d: int) -> float:
+    """Softmax scale 1/sqrt(d): the SDPA default, implied by the drop-in-replacement claim
+    [overview, "Using the plug-and-play API"].  Reading: the pooled scores use the same scale."""
+    return 1.0 / math.sqrt(d)
+
+
+# ---------------------------------------------------------------------------------------------
+# Stage 1a: block mean pooling and intra-block self-similarity
+# ---------------------------------------------------------------------------------------------
+def pool_sim(x: np.ndarray, blk: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Mean of each block of ``blk`` tokens and its self-similarity.
+
+    [summary, method paragraph] stage 1 compresses token blocks that show high internal
+    similarity.  Reading of "internal similarity": the mean cosine similarity over all ordered
+    pairs (a, b) of tokens in the block, the pairs a == b included.  That mean equals
+    ||(1/n) sum_a x_a/||x_a|| ||^2, which is what is computed here; a token of zero norm
+    contributes a zero unit vector.  A partial tail block uses its valid tokens only.
+
+    x: (B, H, N, d) float64.  Returns mu (B, H, nb, d) and s (B, H, nb)."""
+    B, H, N, d = x.shape
+    nb = n_blocks(N, blk)
+    mu = np.zeros((B, H, nb, d))
+    s = np.zeros((B, H, nb))
+    for i in range(nb):
+        xb = x[:, :, i * blk:min(N, (i + 1) * blk), :]
+        n = xb.shape[2]
+        mu[:, :, i, :] = xb.sum(axis=2) / n
+        nrm = np.sqrt((xb * xb).sum(axis=-1, keepdims=True))
+        unit = np.divide(xb, nrm, out=np.zeros_like(xb), where=nrm > 0)
+        h = unit.sum(axis=2) / n
+        s[:, :, i] = (h * h).sum(axis=-1)
+    return mu, s
+
+
+# ---------------------------------------------------------------------------------------------
+# Stage 1b: pooled score map, row softmax, cumulative top-k, always-keep
+# ---------------------------------------------------------------------------------------------
+def block_valid(nqb: int, nkb: int, causal: bool) -> np.ndarray:
+    """(nqb, nkb) bool: a 128x64 tile is valid unless causal attention hides all of it.
+    Tile (i, j) holds some visible element iff 64*j <= 128*i + 127."""
+    i = np.arange(nqb)[:, None]
+    j = np.arange(nkb)[None, :]
+    if not causal:
+        return np.ones((nqb, nkb), dtype=bool)
+    return KBLK * j <= QBLK * i + (QBLK - 1)
+
+
+def pooled_scores(muQ: np.ndarray, muK: np.ndarray, causal: bool, scale: float) -> np.ndarray:
+    """S_hat[b, h, i, j] = scale * muQ[b, h, i] . muK[b, h // G, j], -inf on invalid tiles.
+
+    [abstract] stage 1 predicts the attention map from a compressed form of Q and K; the
+    compressed tokens are the block means.  G = Hq / Hkv (reading: query heads share the pooled
+    keys of their key/value head, as grouped-query attention shares K and V)."""
+    B, Hq, nqb, d = muQ.shape
+    Hkv, nkb = muK.shape[1], muK.shape[2]
+    G = Hq // Hkv
+    S = np.empty((B, Hq, nqb, nkb))
+    for b in range(B):
+        for h in range(Hq):
+            S[b, h] = scale * (muQ[b, h] @ muK[b, h // G].T)
+    S[:, :, ~block_valid(nqb, nkb, causal)] = -np.inf
+    return S
+
+
+def row_softmax(S: np.ndarray) -> np.ndarray:
+    """Softmax over the last axis, -inf entries get probability 0."""
+    m = S.max(axis=-1, keepdims=True)
+    e = np.exp(S - m)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def topk_select(p: np.ndarray, valid: np.ndarray, topk: float) -> np.ndarray:
+    """Keep set of one row of block probabilities.
+
+    [overview, FAQ] topk lies in (0, 1]; lower means sparser.  [readme-cn, quick start]
+    topk = 0.5 keeps the top 50% of the attention weights.  Reading: order the valid blocks by
+    (probability descending, index ascending) and keep the shortest prefix whose cumulative
+    probability reaches topk; topk >= 1 keeps every valid block; at least one block is kept.
+
+    p: (nkb,) probabilities, valid: (nkb,) bool with at least one True.  Returns bool (nkb,)."""
+    keep = np.zeros(p.shape[0], dtype=bool)
+    if topk >= 1.0:
+        keep[valid] = True
+        return keep
+    vj = np.nonzero(valid)[0]
+    order = vj[np.lexsort((vj, -p[vj]))]
+    c = np.cumsum(p[order])
+    hit = np.nonzero(c >= topk)[0]
+    kstar = (hit[0] + 1) if hit.size else order.size
+    keep[order[:kstar]] = True
+    return keep
+
+
+def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal: bool,
+                 scale: float = None) -> Dict[str, np.ndarray]:
+    """Stage 1 of SpargeAttn: the (B, Hq, ceil(N/128), ceil(N/64)) uint8 block mask.
+
+    [overview, "Strengths"] mask shape and 128x64 granularity; [readme-cn, custom mask] 1 = keep.
+    [summary, method paragraph] non-similar blocks are always computed.  Reading of that rule:
+    after top-k, a query block i with s_Q < theta keeps every valid key block of its row, and a
+    key block j with s_K < theta is kept in every valid row of every query head that shares its
+    key/value head.  The softmax is taken over all valid blocks, similar or not.  Comparisons
+    with theta are strict.
+
+    q: (B, Hq, N, d), k: (B, Hkv, N, d) float64."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    if scale is None:
+        scale = default_scale(d)
+    muQ, sQ = pool_sim(q, QBLK)
+    muK, sK = pool_sim(k, KBLK)
+    S = pooled_scores(muQ, muK, causal, scale)
+    P = row_softmax(S)
+    nqb, nkb = S.shape[2], S.shape[3]
+    valid = block_valid(nqb, nkb, causal)
+    mask = np.zeros((B, Hq, nqb, nkb), dtype=np.uint8)
+    for b in range(B):
+        for h in range(Hq):
+            colkeep = sK[b, h // G] < theta
+            for i in range(nqb):
+                keep = topk_select(P[b, h, i], valid[i], topk)
+                if sQ[b, h, i] < theta:
+                    keep |= valid[i]
+                keep |= colkeep & valid[i]
+                mask[b, h, i] = keep
+    return dict(mask=mask, muQ=muQ, sQ=sQ, muK=muK, sK=sK, S=S, P=P)
+
+
+def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal: bool,
+                  eps: float = 1e-3) -> np.ndarray:
+    """Rows whose mask no rounding within ``eps`` can change (the bit-exact comparison set).
+
+    A row is decisive when its query similarity is farther than eps from theta and either it
+    keeps every block because s_Q < theta, or (i) the cumulative sum at the cut and the one
+    before it are farther than eps from topk, (ii) the probability gap at the cut exceeds eps,
+    and (iii) every valid key block similarity is farther than eps from theta."""
+    P, sQ, sK = pred["P"], pred["sQ"], pred["sK"]
+    B, Hq, nqb, nkb = P.shape
+    G = Hq // sK.shape[1]
+    valid = block_valid(nqb, nkb, causal)
+    out = np.zeros((B, Hq, nqb), dtype=bool)
+    for b in range(B):
+        for h in range(Hq):
+            kd = np.abs(sK[b, h // G] - theta) > eps
+            for i in range(nqb):
+                if abs(sQ[b, h, i] - theta) <= eps:
+                    continue
+                if sQ[b, h, i] < theta:
+                    out[b, h, i] = True
+                    continue
+                if not np.all(kd[valid[i]]):
+                    continue
+                if topk >= 1.0:
+                    out[b, h, i] = True
+                    continue
+                p = P[b, h, i]
+                vj = np.nonzero(valid[i])[0]
+                order = vj[np.lexsort((vj, -p[vj]))]
+                ps = p[order]
+                c = np.cumsum(ps)
+                hit = np.nonzero(c >= topk)[0]
+                kstar = (hit[0] + 1) if hit.size else order.size
+                c_at = c[kstar - 1]
+                c_before = c[kstar - 2] if kstar >= 2 else 0.0
+                gap = ps[kstar - 1] - (ps[kstar] if kstar < ps.size else 0.0)
+                if abs(c_at - topk) > eps and abs(topk - c_before) > eps and gap > eps:
+                    out[b, h, i] = True
+    return out
+
+
+# ---------------------------------------------------------------------------------------------
+# Stage 2: block-sparse flash attention with the lambda warp filter
+# ---------------------------------------------------------------------------------------------
+def block_sparse_attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask, lam: float,
+                      causal: bool, scale: float = None, group: int = WARP_ROWS,
+                      return_stats: bool = False, qblocks=None):
+    """Stage 2 of SpargeAttn, step by step as an online-softmax attention over kept tiles.
+
+    [abstract] only the tiles the mask keeps are multiplied; the second-stage online
+    softmax-aware filter skips further updates.  [summary] the filter acts at warp level.
+    Reading of the filter: rows are grouped 32 at a time (one warp's rows); the key tiles of a
+    query block are visited in ascending order; for tile j the group skips its P.V update when
+    for every row r of the group m_local[r] - m_new[r] < lam (m_local the row max over tile j,
+    m_new the running max after tile j; a row with m_local = -inf or m_new = -inf counts as
+    trailing).  The running max and the row sum l are updated even for a skipped group; only
+    P.V is left out.  lam = -inf disables the filter.  A row with no visible kept key outputs 0.
+
+    mask: (B, Hq, nqb, nkb) uint8 or None (all ones).  Tiles above the causal diagonal are never
+    visited.  ``qblocks`` optionally restricts the work to a list of (b, h, i) query blocks (the
+    other rows of O stay 0).  Returns O (B, Hq, N, d) float64 (and statistics when asked)."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    if scale is None:
+        scale = default_scale(d)
+    nqb, nkb = n_blocks(N, QBLK), n_blocks(N, KBLK)
+    valid = block_valid(nqb, nkb, causal)
+    O = np.zeros((B, Hq, N, d))
+    kept_tiles = 0
+    skipped_group_tiles = 0
+    pv_tiles = 0
+    if qblocks is None:
+        qblocks = [(b, h, i) for b in range(B) for h in range(Hq) for i in range(nqb)]
+    for b, h, i in qblocks:
+        Kh, Vh = k[b, h // G], v[b, h // G]
+        r0, r1 = i * QBLK, min(N, (i + 1) * QBLK)
+        nr = r1 - r0
+        Qi = q[b, h, r0:r1]
+        grp = np.arange(nr) // group
+        ngrp = grp[-1] + 1
+        m = np.full(nr, -np.inf)
+        l = np.zeros(nr)
+        acc = np.zeros((nr, d))
+        rows = np.arange(r0, r1)
+        kept = np.ones(nkb, bool) if mask is None else (mask[b, h, i] != 0)
+        for j in np.nonzero(kept & valid[i])[0]:
+            c0, c1 = j * KBLK, min(N, (j + 1) * KBLK)
+            kept_tiles += 1
+            S = scale * (Qi @ Kh[c0:c1].T)
+            if causal:
+                S = np.where(np.arange(c0, c1)[None, :] > rows[:, None], -np.inf, S)
+            m_loc = S.max(axis=1)
+            m_new = np.maximum(m, m_loc)
+            with np.errstate(invalid="ignore"):
+                trailing = np.isneginf(m_loc) | np.isneginf(m_new) | ((m_loc - m_new) < lam)
+            skip_g = np.array([trailing[grp == g].all() for g in range(ngrp)])
+            skipped_group_tiles += int(skip_g.sum())
+            fin = ~np.isneginf(m_new)
+            m_ref = np.where(fin, m_new, 0.0)
+            alpha = np.where(fin, np.exp(m - m_ref), 1.0)
+            Pm = np.where(fin[:, None], np.exp(S - m_ref[:, None]), 0.0)
+            l = alpha * l + Pm.sum(axis=1)
+            upd = Pm @ Vh[c0:c1]
+            upd[skip_g[grp]] = 0.0
+            if not skip_g.all():
+                pv_tiles += 1
+            acc = alpha[:, None] * acc + upd
+            m = m_new
+        O[b, h, r0:r1] = np.divide(acc, l[:, None], out=np.zeros_like(acc), where=l[:, None] > 0)
+    if return_stats:
+        return O, dict(kept_tiles=kept_tiles, skipped_group_tiles=skipped_group_tiles, pv_tiles=pv_tiles)
+    return O
+
+
+def sparge_attn(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: float = -math.inf,
+                scale: float = None, return_all: bool = False):
+    """The plug-and-play call [overview, "Using the plug-and-play API"]: stage 1 mask, then
+    stage 2 attention.  Reading: theta defaults to 0.5 and lambda to -inf (no second filter),
+    since the plug-and-play call takes neither."""
+    pred = predict_mask(q, k, topk, theta, causal, scale)
+    O = block_sparse_attn(q, k, v, pred["mask"], lam, causal, scale)
+    if return_all:
+        return O, pred
+    return O
+
+
+# ---------------------------------------------------------------------------------------------
+# Hilbert-curve token order for image and video tokens  [summary, method paragraph]
+# ---------------------------------------------------------------------------------------------
+def hilbert_index_2d(x: int, y: int, order: int) -> int:
+    """Position of cell (x, y) on the order-``order`` Hilbert curve over a 2^order square.
+
+    The curve starts at (0, 0) and ends at (2^order - 1, 0).  Written from the recursive
+    definition: the square splits into quadrants visited lower-left, upper-left, upper-right,
+    lower-right; the lower-left copy is mirrored about the main diagonal and the lower-right
+    copy about the anti-diagonal so that the pieces join end to end."""
+    idx = 0
+    for lev in range(order, 0, -1):
+        h = 1 << (lev - 1)
+        if x < h and y < h:
+            qd, x, y = 0, y, x
+        elif x < h:
+            qd, x, y = 1, x, y - h
+        elif y >= h:
+            qd, x, y = 2, x - h, y - h
+        else:
+            qd, x, y = 3, h - 1 - y, h - 1 - (x - h)
+        idx += qd * h * h
+    return idx
+
+
+def hilbert_index_3d(coords, bits: int) -> int:
+    """Position of a point on the 3-D Hilbert curve of a 2^bits cube (J. Skilling, "Programming
+    the Hilbert curve", AIP Conf. Proc. 707, 2004: transform the axes to the 'transposed' index,
+    then read its bits most significant first, axis 0 first).  coords = (a0, a1, a2)."""
+    X = [int(c) for c in coords]
+    n = len(X)
+    top = 1 << (bits - 1)
+    qb = top
+    while qb > 1:
+        low = qb - 1
+        for a in range(n):
+            if X[a] & qb:
+                X[0] ^= low
+            else:
+                t = (X[0] ^ X[a]) & low
+                X[0] ^= t
+                X[a] ^= t
+        qb >>= 1
+    for a in range(1, n):
+        X[a] ^= X[a - 1]
+    t = 0
+    qb = top
+    while qb > 1:
+        if X[n - 1] & qb:
+            t ^= qb - 1
+        qb >>= 1
+    for a in range(n):
+        X[a] ^= t
+    idx = 0
+    for bit in range(bits - 1, -1, -1):
+        for a in range(n):
+            idx = (idx << 1) | ((X[a] >> bit) & 1)
+    return idx
+
+
+def _order_for(*extent) -> int:
+    o = 0
+    while (1 << o) < max(extent):
+        o += 1
+    return max(o, 1)
+
+
+def hilbert_perm_2d(n_prefix: int, H: int, W: int) -> np.ndarray:
+    """Gather permutation pi (int32, length n_prefix + H*W): new position t takes old token pi[t].
+    Text tokens stay first and in order; image token (r, c), stored row-major after the prefix,
+    is placed by its Hilbert index with x = c, y = r on the smallest 2^k square covering the grid
+    (points outside the grid are skipped)."""
+    k = _order_for(H, W)
+    keys = np.array([hilbert_index_2d(c, r, k) for r in range(H) for c in range(W)], dtype=np.int64)
+    order = np.argsort(keys, kind="stable")
+    return np.concatenate([np.arange(n_prefix), n_prefix + order]).astype(np.int32)
+
+
+def hilbert_perm_3d(n_prefix: int, T: int, H: int, W: int) -> np.ndarray:
+    """As hilbert_perm_2d for a (T, H, W) video grid stored (t, r, c) row-major, ordered by the
+    3-D Hilbert index of (t, r, c) on the smallest 2^k cube covering the grid."""
+    k = _order_for(T, H, W)
+    keys = np.array([hilbert_index_3d((t, r, c), k) for t in range(T) for r in range(H) for c in range(W)],
+                    dtype=np.int64)
+    order = np.argsort(keys, kind="stable")
+    return np.concatenate([np.arange(n_prefix), n_prefix + order]).astype(np.int32)
+
+
+def permute_tokens(x: np.ndarray, perm: np.ndarray) -> np.ndarray:
+    """y[:, :, t] = x[:, :, perm[t]]."""
+    return x[:, :, perm, :]
+
+
+def unpermute_tokens(y: np.ndarray, perm: np.ndarray) -> np.ndarray:
+    """Inverse of permute_tokens: x[:, :, perm[t]] = y[:, :, t]."""
+    x = np.empty_like(y)
+    x[:, :, perm, :] = y
+    return x
