@@ -1,0 +1,246 @@
+"""GB300 (sm_103a) SpargeAttn: two-stage sparse attention forward behind a C ABI.
+
+Thin Python binding over ``libsparge.so`` (see include/sparge.h for the contract of every
+call).  This module only marshals arguments: torch provides device memory and the current CUDA
+stream, every step of the computation runs in the library's CUDA kernels.  There is no CPU
+path: if the library is missing or no CUDA device is present the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsparge.so")
+
+SPARGE_OK = 0
+SPARGE_ERR_INVALID_ARG = -1
+SPARGE_ERR_UNSUPPORTED = -2
+SPARGE_ERR_WORKSPACE_TOO_SMALL = -3
+SPARGE_ERR_CUDA = -4
+SPARGE_ERR_DEVICE_TIMEOUT = -5
+SPARGE_BF16 = 1
+SPARGE_PRECISION_BF16 = 0
+SPARGE_PRECISION_Q8 = 1
+SPARGE_OP_PREDICT_MASK = 1
+SPARGE_OP_BLOCK_SPARSE_ATTN = 2
+SPARGE_OP_ATTN = 3
+QBLK, KBLK = 128, 64
+
+
+class SpargeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__("sparge error %d: %s" % (code, msg))
+        self.code = code
+
+
+class sparge_tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("pad_", ctypes.c_int32),
+                ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64), ("d", ctypes.c_int64),
+                ("stride_b", ctypes.c_int64), ("stride_h", ctypes.c_int64), ("stride_n", ctypes.c_int64)]
+
+
+class sparge_params(ctypes.Structure):
+    _fields_ = [("theta", ctypes.c_float), ("lambda_", ctypes.c_float), ("scale", ctypes.c_float),
+                ("precision", ctypes.c_int32), ("stats", ctypes.c_void_p)]
+
+
+_lib = None
+
+EXPORTS = {
+    "sparge_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] + [ctypes.c_int64] * 5),
+    "sparge_predict_mask": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_float,
+                                           ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                           ctypes.c_void_p]),
+    "sparge_block_sparse_attn": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "sparge_attn": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_int,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "sparge_attn_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_size_t, ctypes.c_void_p]),
+    "sparge_permute_tokens": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "sparge_unpermute_tokens": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "sparge_hilbert_perm_2d": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "sparge_hilbert_perm_3d": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "sparge_last_error": (ctypes.c_char_p, []),
+    "sparge_get_device_status": (ctypes.c_int, [ctypes.c_void_p]),
+}
+
+
+def lib():
+    """Load libsparge.so (built by ``free_block_sparse_gb300.build``); raise if it is absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libsparge.so is not built (%s); run free_block_sparse_gb300.build.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in EXPORTS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != SPARGE_OK:
+        raise SpargeError(rc, lib().sparge_last_error().decode())
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream():
+    torch = _torch()
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _desc(t) -> sparge_tensor:
+    torch = _torch()
+    if not (isinstance(t, torch.Tensor) and t.is_cuda):
+        raise TypeError("expected a CUDA tensor")
+    if t.dtype != torch.bfloat16 or t.dim() != 4 or t.stride(-1) != 1:
+        raise TypeError("expected a bf16 (B, H, N, d) tensor with contiguous last dim")
+    B, H, N, d = t.shape
+    sb, sh, sn, _ = t.stride()
+    return sparge_tensor(t.data_ptr(), SPARGE_BF16, 0, B, H, N, d, sb, sh, sn)
+
+
+def workspace_bytes(op: int, B: int, Hq: int, Hkv: int, N: int, d: int) -> int:
+    return int(lib().sparge_workspace_bytes(op, B, Hq, Hkv, N, d))
+
+
+def n_blocks(N: int):
+    return -(-N // QBLK), -(-N // KBLK)
+
+
+def _workspace(op, q, k, ws):
+    torch = _torch()
+    B, Hq, N, d = q.shape
+    need = workspace_bytes(op, B, Hq, k.shape[1], N, d)
+    if ws is None:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    return ws
+
+
+def predict_mask(q, k, topk: float, theta: float = 0.5, causal: bool = False, ws=None, mask=None):
+    """Stage 1: the (B, Hq, ceil(N/128), ceil(N/64)) uint8 block mask."""
+    torch = _torch()
+    B, Hq, N, d = q.shape
+    nqb, nkb = n_blocks(N)
+    if mask is None:
+        mask = torch.empty((B, Hq, nqb, nkb), dtype=torch.uint8, device=q.device)
+    ws = _workspace(SPARGE_OP_PREDICT_MASK, q, k, ws)
+    dq, dk = _desc(q), _desc(k)
+    _check(lib().sparge_predict_mask(ctypes.byref(dq), ctypes.byref(dk), float(topk), float(theta), int(causal),
+                                     mask.data_ptr(), ws.data_ptr(), ws.numel(), _stream()))
+    return mask
+
+
+def predict_ws_views(ws, B, Hq, Hkv, N, d):
+    """Views of the stage-1 workspace after predict_mask: muQ (B,Hq,nqb,d), sQ (B,Hq,nqb),
+    muK (B,Hkv,nkb,d) and sK (B,Hkv,nkb), following the layout the library writes (fp32,
+    regions 256-byte aligned, pooled keys stored d-major with the key-block axis padded to 4)."""
+    torch = _torch()
+    nqb, nkb = n_blocks(N)
+    nkb_pad = -(-nkb // 4) * 4
+    f = ws.view(torch.float32) if ws.dtype == torch.uint8 else ws
+
+    def take(off, n):
+        return f[off // 4: off // 4 + n], off + ((4 * n + 255) // 256) * 256
+
+    off = 0
+    muQ, off = take(off, B * Hq * nqb * d)
+    sQ, off = take(off, B * Hq * nqb)
+    muKt, off = take(off, B * Hkv * d * nkb_pad)
+    sK, off = take(off, B * Hkv * nkb_pad)
+    return (muQ.view(B, Hq, nqb, d), sQ.view(B, Hq, nqb),
+            muKt.view(B, Hkv, d, nkb_pad)[..., :nkb].transpose(2, 3), sK.view(B, Hkv, nkb_pad)[..., :nkb])
+
+
+def block_sparse_attn(q, k, v, mask=None, lam: float = -math.inf, causal: bool = False, out=None, stats=None,
+                      precision: int = SPARGE_PRECISION_BF16):
+    """Stage 2: attention over the kept 128x64 tiles with the lambda warp filter."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(q)
+    dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
+    mp = 0 if mask is None else mask.data_ptr()
+    sp = 0 if stats is None else stats.data_ptr()
+    _check(lib().sparge_block_sparse_attn(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), mp, float(lam),
+                                          int(causal), int(precision), ctypes.byref(do), None, 0, sp, _stream()))
+    return out
+
+
+def sparge_attn(q, k, v, topk: float = 0.5, causal: bool = False, out=None, ws=None):
+    """The plug-and-play call: predicted mask (theta 0.5) then block-sparse attention."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(q)
+    ws = _workspace(SPARGE_OP_ATTN, q, k, ws)
+    dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
+    _check(lib().sparge_attn(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), float(topk), int(causal),
+                             ctypes.byref(do), ws.data_ptr(), ws.numel(), _stream()))
+    return out
+
+
+def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: float = -math.inf,
+                   scale: float = 0.0, precision: int = SPARGE_PRECISION_BF16, stats=None, mask_out=None,
+                   out=None, ws=None):
+    """sparge_attn with explicit theta, lambda, scale, counters and an optional mask output."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(q)
+    ws = _workspace(SPARGE_OP_ATTN, q, k, ws)
+    p = sparge_params(float(theta), float(lam), float(scale), int(precision),
+                      0 if stats is None else stats.data_ptr())
+    dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
+    mp = 0 if mask_out is None else mask_out.data_ptr()
+    _check(lib().sparge_attn_ex(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), float(topk), int(causal),
+                                ctypes.byref(p), ctypes.byref(do), mp, ws.data_ptr(), ws.numel(), _stream()))
+    return out
+
+
+def permute_tokens(x, perm, out=None):
+    """y[:, :, t] = x[:, :, perm[t]] (perm: int32 CUDA tensor)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(x)
+    dx, dy = _desc(x), _desc(out)
+    _check(lib().sparge_permute_tokens(ctypes.byref(dx), perm.data_ptr(), ctypes.byref(dy), _stream()))
+    return out
+
+
+def unpermute_tokens(x, perm, out=None):
+    """y[:, :, perm[t]] = x[:, :, t]."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(x)
+    dx, dy = _desc(x), _desc(out)
+    _check(lib().sparge_unpermute_tokens(ctypes.byref(dx), perm.data_ptr(), ctypes.byref(dy), _stream()))
+    return out
+
+
+def hilbert_perm_2d(n_prefix: int, H: int, W: int) -> np.ndarray:
+    out = np.empty(n_prefix + H * W, dtype=np.int32)
+    _check(lib().sparge_hilbert_perm_2d(n_prefix, H, W, out.ctypes.data))
+    return out
+
+
+def hilbert_perm_3d(n_prefix: int, T: int, H: int, W: int) -> np.ndarray:
+    out = np.empty(n_prefix + T * H * W, dtype=np.int32)
+    _check(lib().sparge_hilbert_perm_3d(n_prefix, T, H, W, out.ctypes.data))
+    return out
+
+
+def device_status() -> int:
+    """Reads and clears the library's device status word (0 = fine)."""
+    return int(lib().sparge_get_device_status(_stream()))

@@ -1,0 +1,310 @@
+// C-ABI layer of libsparge: argument validation, workspace layout, TMA descriptor creation,
+// the device status word and kernel launches.  Every entry point is declared (and its
+// arguments documented) in include/sparge.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sparge.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace sparge;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char *where) {
+  return fail(SPARGE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+// One status word per process in device memory (a __device__ variable, not an allocation);
+// kernels record a timed-out bounded wait there.
+__device__ int g_status_word = 0;
+
+int *status_ptr() {
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+  return static_cast<int *>(p);
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int check_tensor(const sparge_tensor *t, const char *name, View *v) {
+  if (!t) return fail(SPARGE_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!t->data) return fail(SPARGE_ERR_INVALID_ARG, "%s->data is NULL", name);
+  if (t->dtype != SPARGE_BF16) return fail(SPARGE_ERR_UNSUPPORTED, "%s: only bf16 is supported", name);
+  if (t->d != 64 && t->d != 128) return fail(SPARGE_ERR_UNSUPPORTED, "%s: head dim %lld not in {64,128}", name, (long long)t->d);
+  if (t->B < 0 || t->H <= 0 || t->N < 0)
+    return fail(SPARGE_ERR_INVALID_ARG, "%s: bad shape B=%lld H=%lld N=%lld", name, (long long)t->B,
+                (long long)t->H, (long long)t->N);
+  if (t->N > (int64_t(1) << 30) || t->B * t->H > (int64_t(1) << 24))
+    return fail(SPARGE_ERR_UNSUPPORTED, "%s: shape too large", name);
+  if ((reinterpret_cast<uintptr_t>(t->data) & 15u) != 0)
+    return fail(SPARGE_ERR_INVALID_ARG, "%s: data not 16-byte aligned", name);
+  int64_t sb = t->stride_b, sh = t->stride_h, sn = t->stride_n;
+  // strides of unit dimensions do not matter; give them a harmless legal value
+  if (t->N == 1) sn = t->d;
+  if (t->H == 1) sh = sn * (t->N > 0 ? t->N : 1);
+  if (t->B == 1) sb = sh * t->H;
+  if (sn < t->d || sh <= 0 || sb <= 0 || sn % 8 || sh % 8 || sb % 8)
+    return fail(SPARGE_ERR_INVALID_ARG, "%s: strides (%lld,%lld,%lld) must be positive multiples of 8 with stride_n >= d",
+                name, (long long)t->stride_b, (long long)t->stride_h, (long long)t->stride_n);
+  *v = View{t->data, t->B, t->H, t->N, t->d, sb, sh, sn};
+  return SPARGE_OK;
+}
+
+int check_qk(const View &q, const View &k) {
+  if (k.B != q.B || k.N != q.N || k.d != q.d)
+    return fail(SPARGE_ERR_INVALID_ARG, "q and k disagree in B, N or d");
+  if (q.H % k.H != 0) return fail(SPARGE_ERR_UNSUPPORTED, "Hq=%lld not a multiple of Hkv=%lld", (long long)q.H, (long long)k.H);
+  return SPARGE_OK;
+}
+
+typedef CUresult (*encode_fn_t)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+encode_fn_t get_encode() {
+  static encode_fn_t fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<encode_fn_t>(p);
+  });
+  return fn;
+}
+
+int make_map(CUtensorMap *m, const View &v, int box_rows, const char *name) {
+  encode_fn_t enc = get_encode();
+  if (!enc) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[4] = {(cuuint64_t)v.d, (cuuint64_t)v.N, (cuuint64_t)v.H, (cuuint64_t)v.B};
+  cuuint64_t strides[3] = {(cuuint64_t)v.sn * 2, (cuuint64_t)v.sh * 2, (cuuint64_t)v.sb * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(v.data), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+  return SPARGE_OK;
+}
+
+int check_topk_theta(float topk, float theta) {
+  if (!(topk > 0.f && topk <= 1.f)) return fail(SPARGE_ERR_INVALID_ARG, "topk=%g not in (0, 1]", (double)topk);
+  if (!std::isfinite(theta)) return fail(SPARGE_ERR_INVALID_ARG, "theta must be finite");
+  return SPARGE_OK;
+}
+
+int check_lambda(float lambda) {
+  if (std::isnan(lambda) || lambda > 0.f) return fail(SPARGE_ERR_INVALID_ARG, "lambda=%g must be <= 0 or -inf", (double)lambda);
+  return SPARGE_OK;
+}
+
+int predict_impl(const View &q, const View &k, float topk, float theta, int causal, float scale, uint8_t *mask,
+                 void *ws, size_t ws_bytes, cudaStream_t s) {
+  if (!mask) return fail(SPARGE_ERR_INVALID_ARG, "mask is NULL");
+  if (q.N > 131072) return fail(SPARGE_ERR_UNSUPPORTED, "mask prediction supports N <= 131072 (got %lld)", (long long)q.N);
+  const size_t need = predict_ws_bytes(q.B, q.H, k.H, q.N, q.d);
+  if (need && (!ws || ws_bytes < need))
+    return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
+  if (q.B == 0 || q.N == 0) return SPARGE_OK;
+  PredictWs pw = predict_ws_carve(ws, q.B, q.H, k.H, q.N, q.d);
+  cudaError_t e = launch_pool_sim(q, k, pw, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pool_sim launch");
+  e = launch_score_select(pw, (int)q.B, (int)q.H, (int)k.H, (int)q.N, (int)q.d, topk, theta, causal, scale, mask, s);
+  if (e != cudaSuccess) return cuda_fail(e, "score_select launch");
+  return SPARGE_OK;
+}
+
+int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, float lambda, int causal, float scale,
+              int precision, sparge_tensor *o, unsigned long long *stats, cudaStream_t s) {
+  if (precision != SPARGE_PRECISION_BF16) return fail(SPARGE_ERR_UNSUPPORTED, "precision %d not supported", precision);
+  View ov;
+  int rc = check_tensor(o, "o", &ov);
+  if (rc) return rc;
+  if (v.B != q.B || v.N != q.N || v.d != q.d || v.H != k.H) return fail(SPARGE_ERR_INVALID_ARG, "v disagrees with q/k");
+  if (ov.B != q.B || ov.N != q.N || ov.d != q.d || ov.H != q.H) return fail(SPARGE_ERR_INVALID_ARG, "o disagrees with q");
+  if (q.B == 0 || q.N == 0) return SPARGE_OK;
+  AttnLaunch l;
+  memset(&l, 0, sizeof(l));
+  if ((rc = make_map(&l.tq, q, 128, "q"))) return rc;
+  if ((rc = make_map(&l.tk, k, 64, "k"))) return rc;
+  if ((rc = make_map(&l.tv, v, 64, "v"))) return rc;
+  l.mask = mask;
+  l.o = o->data;
+  l.o_sb = ov.sb; l.o_sh = ov.sh; l.o_sn = ov.sn;
+  l.B = (int)q.B; l.Hq = (int)q.H; l.Hkv = (int)k.H; l.N = (int)q.N; l.d = (int)q.d;
+  l.causal = causal ? 1 : 0;
+  l.scale = scale;
+  l.lambda = lambda;
+  l.stats = stats;
+  l.status = status_ptr();
+  cudaError_t e = launch_bsattn(l, s);
+  if (e != cudaSuccess) return cuda_fail(e, "bsattn launch");
+  return SPARGE_OK;
+}
+
+}  // namespace
+
+namespace sparge {
+
+size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
+  const int64_t nqb = cdiv(N, QBLK), nkb = cdiv(N, KBLK), nkb_pad = cdiv(nkb, 4) * 4;
+  size_t s = 0;
+  s += align256(sizeof(float) * B * Hq * nqb * d);
+  s += align256(sizeof(float) * B * Hq * nqb);
+  s += align256(sizeof(float) * B * Hkv * d * nkb_pad);
+  s += align256(sizeof(float) * B * Hkv * nkb_pad);
+  return s;
+}
+
+PredictWs predict_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
+  const int64_t nqb = cdiv(N, QBLK), nkb = cdiv(N, KBLK), nkb_pad = cdiv(nkb, 4) * 4;
+  char *p = static_cast<char *>(ws);
+  PredictWs w;
+  w.muQ = reinterpret_cast<float *>(p);
+  p += align256(sizeof(float) * B * Hq * nqb * d);
+  w.sQ = reinterpret_cast<float *>(p);
+  p += align256(sizeof(float) * B * Hq * nqb);
+  w.muKt = reinterpret_cast<float *>(p);
+  p += align256(sizeof(float) * B * Hkv * d * nkb_pad);
+  w.sK = reinterpret_cast<float *>(p);
+  w.nkb_pad = nkb_pad;
+  return w;
+}
+
+}  // namespace sparge
+
+extern "C" {
+
+size_t sparge_workspace_bytes(int op, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || (d != 64 && d != 128)) return 0;
+  switch (op) {
+    case SPARGE_OP_PREDICT_MASK:
+      return predict_ws_bytes(B, Hq, Hkv, N, d);
+    case SPARGE_OP_ATTN:
+      return predict_ws_bytes(B, Hq, Hkv, N, d) + align256((size_t)B * Hq * cdiv(N, QBLK) * cdiv(N, KBLK));
+    default:
+      return 0;
+  }
+}
+
+const char *sparge_last_error(void) { return g_last_error; }
+
+int sparge_predict_mask(const sparge_tensor *q, const sparge_tensor *k, float topk, float theta, int is_causal,
+                        uint8_t *mask, void *ws, size_t ws_bytes, sparge_stream_t stream) {
+  g_last_error[0] = 0;
+  View qv, kv;
+  int rc;
+  if ((rc = check_tensor(q, "q", &qv)) || (rc = check_tensor(k, "k", &kv)) || (rc = check_qk(qv, kv))) return rc;
+  if ((rc = check_topk_theta(topk, theta))) return rc;
+  return predict_impl(qv, kv, topk, theta, is_causal, 1.f / sqrtf((float)qv.d), mask, ws, ws_bytes,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v,
+                             const uint8_t *mask, float lambda, int is_causal, int precision, sparge_tensor *o,
+                             void *ws, size_t ws_bytes, unsigned long long *stats, sparge_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  g_last_error[0] = 0;
+  View qv, kv, vv;
+  int rc;
+  if ((rc = check_tensor(q, "q", &qv)) || (rc = check_tensor(k, "k", &kv)) || (rc = check_tensor(v, "v", &vv)) ||
+      (rc = check_qk(qv, kv)))
+    return rc;
+  if ((rc = check_lambda(lambda))) return rc;
+  return attn_impl(qv, kv, vv, mask, lambda, is_causal, 1.f / sqrtf((float)qv.d), precision, o, stats,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,
+                   const sparge_params *p, sparge_tensor *o, uint8_t *mask_out, void *ws, size_t ws_bytes,
+                   sparge_stream_t stream) {
+  g_last_error[0] = 0;
+  if (!p) return fail(SPARGE_ERR_INVALID_ARG, "params is NULL");
+  View qv, kv, vv;
+  int rc;
+  if ((rc = check_tensor(q, "q", &qv)) || (rc = check_tensor(k, "k", &kv)) || (rc = check_tensor(v, "v", &vv)) ||
+      (rc = check_qk(qv, kv)))
+    return rc;
+  if ((rc = check_topk_theta(topk, p->theta)) || (rc = check_lambda(p->lambda))) return rc;
+  if (std::isnan(p->scale) || p->scale < 0.f || std::isinf(p->scale))
+    return fail(SPARGE_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)qv.d);
+  const size_t need_pred = predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, qv.d);
+  const size_t mask_bytes = (size_t)qv.B * qv.H * cdiv(qv.N, QBLK) * cdiv(qv.N, KBLK);
+  const size_t need = need_pred + (mask_out ? 0 : align256(mask_bytes));
+  if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
+  uint8_t *mask = mask_out ? mask_out : static_cast<uint8_t *>(ws) + need_pred;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s))) return rc;
+  return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, s);
+}
+
+int sparge_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,
+                sparge_tensor *o, void *ws, size_t ws_bytes, sparge_stream_t stream) {
+  sparge_params p;
+  p.theta = 0.5f;
+  p.lambda = -INFINITY;
+  p.scale = 0.f;
+  p.precision = SPARGE_PRECISION_BF16;
+  p.stats = nullptr;
+  return sparge_attn_ex(q, k, v, topk, is_causal, &p, o, nullptr, ws, ws_bytes, stream);
+}
+
+static int permute_common(const sparge_tensor *x, const int32_t *perm, sparge_tensor *y, bool inverse,
+                          sparge_stream_t stream) {
+  g_last_error[0] = 0;
+  View xv, yv;
+  int rc;
+  if ((rc = check_tensor(x, "x", &xv)) || (rc = check_tensor(y, "y", &yv))) return rc;
+  if (!perm) return fail(SPARGE_ERR_INVALID_ARG, "perm is NULL");
+  if (xv.B != yv.B || xv.H != yv.H || xv.N != yv.N || xv.d != yv.d) return fail(SPARGE_ERR_INVALID_ARG, "x and y shapes differ");
+  if (x->data == y->data) return fail(SPARGE_ERR_INVALID_ARG, "x and y must not overlap");
+  cudaError_t e = launch_permute(xv, perm, y->data, yv.sb, yv.sh, yv.sn, inverse, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+  return SPARGE_OK;
+}
+
+int sparge_permute_tokens(const sparge_tensor *x, const int32_t *perm, sparge_tensor *y, sparge_stream_t stream) {
+  return permute_common(x, perm, y, false, stream);
+}
+
+int sparge_unpermute_tokens(const sparge_tensor *x, const int32_t *perm, sparge_tensor *y, sparge_stream_t stream) {
+  return permute_common(x, perm, y, true, stream);
+}
+
+int sparge_get_device_status(sparge_stream_t stream) {
+  g_last_error[0] = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int host = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&host, g_status_word, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (host != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_status_word, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    return fail(host, "a device-side wait timed out");
+  }
+  return SPARGE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,452 @@
+// Stage 2: block-sparse flash attention with the lambda warp filter, on tcgen05 tensor cores.
+//
+// SpargeAttention abstract: only the kept tiles of the predicted map are multiplied, and an
+// online softmax-aware filter skips further updates; summary page: that filter works at GPU
+// warp level; Chinese README: arbitrary per-head block masks of 128x64 tiles.
+//
+// One CTA computes one 128-row query block of one head.  Warp roles (192 threads):
+//   warps 0-3  softmax + epilogue; warp w owns TMEM lanes 32w..32w+31, i.e. rows 32w.. of the
+//              block, one row per thread (the 32-row group of the lambda filter).
+//   warp 4     producer: TMA loads of the Q block once, then of only the kept K/V tiles into a
+//              STAGES-deep shared-memory ring.
+//   warp 5     MMA issuer: S_t = Q K_t^T into one of two TMEM score buffers, O += P_t V_t with P_t
+//              read back from TMEM (bf16, written over S_t) and V_t from shared memory.
+// TMEM columns: O at [0, D), score buffers at [128, 192) and [192, 256) (D = 128) or [64, 128)
+// and [128, 192) (D = 64); 256 columns are allocated, so two CTAs can share an SM.
+//
+// Online softmax per row in the log2 domain.  The exponent reference m_ref is moved only when
+// the running maximum exceeds it by more than 8 (P <= 2^8 before the move), so O is rescaled
+// in TMEM only then; O and l share the reference so O / l is exact.  The lambda filter compares
+// each row's tile maximum with its true running maximum; a warp whose 32 rows all trail writes
+// P = 0 (its row sums still include the tile) and the P.V product is not issued when all four
+// warps trail.
+#include <cfloat>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sparge {
+namespace {
+
+constexpr int NTHREADS = 192;
+constexpr int RESCALE_LOG2 = 8;
+
+struct AttnArgs {
+  const uint8_t *mask;
+  __nv_bfloat16 *o;
+  int64_t o_sb, o_sh, o_sn;
+  int B, Hq, Hkv, G, N, nqb, nkb, causal;
+  float scale_log2, lam_log2;
+  unsigned long long *stats;
+  int *status;
+};
+
+// Warp-collective walk over the kept, valid key blocks of one mask row in ascending order.
+struct KeptScan {
+  const uint8_t *row;
+  int n, base;
+  uint32_t bits;
+  __device__ void init(const uint8_t *r, int n_valid) {
+    row = r;
+    n = n_valid;
+    base = -32;
+    bits = 0u;
+  }
+  __device__ int next(int lane) {
+    while (bits == 0u) {
+      base += 32;
+      if (base >= n) return -1;
+      const int j = base + lane;
+      const bool k = j < n && (row == nullptr || row[j] != 0);
+      bits = __ballot_sync(0xffffffffu, k);
+    }
+    const int l = __ffs(bits) - 1;
+    bits &= bits - 1u;
+    return base + l;
+  }
+};
+
+__device__ __forceinline__ int count_kept(const uint8_t *row, int n, int lane) {
+  if (row == nullptr) return n;
+  int cnt = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int j = base + lane;
+    cnt += __popc(__ballot_sync(0xffffffffu, j < n && row[j] != 0));
+  }
+  return cnt;
+}
+
+template <int D, int STAGES>
+struct Smem {
+  static constexpr int QCH = D / 64;                     // 64-column chunks of a row
+  static constexpr uint32_t Q_BYTES = QCH * 128 * 128;   // 128 rows x 128 B per chunk
+  static constexpr uint32_t KV_CHUNK = 64 * 128;         // 64 rows x 128 B
+  static constexpr uint32_t K_BYTES = QCH * KV_CHUNK;
+  static constexpr uint32_t STAGE_BYTES = 2 * K_BYTES;   // K then V
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_KV = Q_BYTES;
+  static constexpr uint32_t OFF_CTRL = OFF_KV + STAGES * STAGE_BYTES;
+  static constexpr uint32_t CTRL_BYTES = 256;
+  static constexpr uint32_t TOTAL = OFF_CTRL + CTRL_BYTES + 1024;  // + alignment slack
+};
+
+struct Ctrl {
+  uint64_t q_full;
+  uint64_t kv_full[4];
+  uint64_t kv_empty[4];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done;
+  uint64_t mma_done;
+  uint64_t final_bar;
+  uint32_t tmem_base;
+  int abort;
+  int pv_any;
+  uint8_t skip[2][4];
+};
+
+template <int D, int STAGES>
+__global__ void __launch_bounds__(NTHREADS, 2)
+    bsattn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const AttnArgs a) {
+  using L = Smem<D, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctrl &cs = *reinterpret_cast<Ctrl *>(smem + L::OFF_CTRL);
+  volatile int *abort = &cs.abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // work item: (b, kvh) outermost so concurrently resident CTAs share K/V in L2; within it the
+  // query blocks go from last to first (most causal work first), heads of a group adjacent.
+  const int per_bk = a.nqb * a.G;
+  const int bk = blockIdx.x / per_bk, rem = blockIdx.x % per_bk;
+  const int b = bk / a.Hkv, kvh = bk % a.Hkv;
+  const int i = a.nqb - 1 - rem / a.G;
+  const int h = kvh * a.G + rem % a.G;
+  const int n_valid = a.causal ? min(a.nkb, 2 * i + 2) : a.nkb;
+  const uint8_t *mrow = a.mask ? a.mask + ((static_cast<int64_t>(b) * a.Hq + h) * a.nqb + i) * a.nkb : nullptr;
+
+  constexpr int SCOL0 = (D == 128) ? 128 : 64;
+  constexpr uint32_t TMEM_COLS = 256;
+  constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false);
+  constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, true);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&cs.q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&cs.kv_full[s], 1);
+      mbar_init(&cs.kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&cs.s_full[s], 1);
+      mbar_init(&cs.p_full[s], 128);
+    }
+    mbar_init(&cs.o_done, 1);
+    mbar_init(&cs.mma_done, 1);
+    mbar_init(&cs.final_bar, 1);
+    cs.abort = 0;
+    cs.pv_any = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&cs.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = cs.tmem_base;
+
+  const int T = count_kept(mrow, n_valid, lane);  // warp-uniform, same in every warp
+
+  const uint32_t sQ = smem_u32(smem + L::OFF_Q);
+  const uint32_t sKV = smem_u32(smem + L::OFF_KV);
+
+  if (warp == 4) {
+    // ------------------------------------ producer ------------------------------------
+    if (T > 0) {
+      if (lane == 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+        mbar_arrive_expect_tx(&cs.q_full, L::Q_BYTES);
+        for (int c = 0; c < L::QCH; ++c)
+          tma_load_4d(smem + L::OFF_Q + c * 16384, &tq, &cs.q_full, 64 * c, QBLK * i, h, b);
+      }
+      KeptScan ks;
+      ks.init(mrow, n_valid);
+      for (int t = 0;; ++t) {
+        const int j = ks.next(lane);
+        if (j < 0) break;
+        const int st = t % STAGES;
+        if (!mbar_wait(&cs.kv_empty[st], ((t / STAGES) & 1) ^ 1, abort, a.status)) break;
+        if (lane == 0) {
+          uint8_t *kdst = smem + L::OFF_KV + st * L::STAGE_BYTES;
+          uint8_t *vdst = kdst + L::K_BYTES;
+          mbar_arrive_expect_tx(&cs.kv_full[st], L::STAGE_BYTES);
+          for (int c = 0; c < L::QCH; ++c) {
+            tma_load_4d(kdst + c * L::KV_CHUNK, &tk, &cs.kv_full[st], 64 * c, KBLK * j, kvh, b);
+            tma_load_4d(vdst + c * L::KV_CHUNK, &tv, &cs.kv_full[st], 64 * c, KBLK * j, kvh, b);
+          }
+        }
+        __syncwarp();
+      }
+      if (*abort) {  // let copies already in flight land before the CTA exits
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------ MMA issuer ------------------------------------
+    int pv_count = 0;
+    if (T > 0) {
+      bool ok = mbar_wait(&cs.q_full, 0, abort, a.status);
+      tc_fence_after();
+      auto issue_s = [&](int u) -> bool {
+        const int st = u % STAGES;
+        if (!mbar_wait(&cs.kv_full[st], (u / STAGES) & 1, abort, a.status)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t kaddr = sKV + st * L::STAGE_BYTES;
+          const uint32_t dS = tmem + SCOL0 + (u & 1) * 64;
+#pragma unroll
+          for (int s = 0; s < D / 16; ++s) {
+            const uint64_t da = smem_desc_sw128(sQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+            const uint64_t db = smem_desc_sw128(kaddr + (s >> 2) * L::KV_CHUNK + (s & 3) * 32, 16, 1024);
+            mma_bf16_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
+          }
+          mma_commit(&cs.s_full[u & 1]);
+        }
+        __syncwarp();
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      uint32_t pv_issued = 0;
+      for (int t = 0; ok && t < T; ++t) {
+        if (t + 1 < T && !issue_s(t + 1)) break;
+        if (!mbar_wait(&cs.p_full[t & 1], (t >> 1) & 1, abort, a.status)) break;
+        tc_fence_after();
+        const bool all_skip = cs.skip[t & 1][0] && cs.skip[t & 1][1] && cs.skip[t & 1][2] && cs.skip[t & 1][3];
+        const int st = t % STAGES;
+        if (lane == 0) {
+          if (!all_skip) {
+            const uint32_t vaddr = sKV + st * L::STAGE_BYTES + L::K_BYTES;
+            const uint32_t aP = tmem + SCOL0 + (t & 1) * 64;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              const uint64_t db = smem_desc_sw128(vaddr + s * 2048, L::KV_CHUNK, 1024);
+              mma_bf16_ts(tmem, aP + s * 8, db, IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
+            }
+            pv_issued = 1;
+            ++pv_count;
+          }
+          mma_commit(&cs.kv_empty[st]);
+          mma_commit(&cs.o_done);
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        cs.pv_any = static_cast<int>(pv_issued);
+        mbar_arrive(&cs.mma_done);
+      }
+    }
+    if (lane == 0) {
+      if (T > 0) {
+        mma_commit(&cs.final_bar);  // completes once every MMA above has finished
+        mbar_wait(&cs.final_bar, 0, abort, a.status);
+      }
+      if (a.stats) {
+        atomicAdd(a.stats + 0, static_cast<unsigned long long>(T));
+        atomicAdd(a.stats + 1, static_cast<unsigned long long>(pv_count));
+        atomicAdd(a.stats + 3, static_cast<unsigned long long>(n_valid));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------ softmax warps ------------------------------------
+    const int r = warp * 32 + lane;
+    const int row_g = QBLK * i + r;
+    const bool row_ok = row_g < a.N;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
+    int nskip = 0;
+    KeptScan ks;
+    ks.init(mrow, n_valid);
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int j = ks.next(lane);
+      const int buf = t & 1;
+      if (!mbar_wait(&cs.s_full[buf], (t >> 1) & 1, abort, a.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sc = tl + SCOL0 + buf * 64;
+      float x[64];
+      {
+        uint32_t r0[16], r1[16], r2[16], r3[16];
+        tmem_ld16(sc, r0);
+        tmem_ld16(sc + 16, r1);
+        tmem_ld16(sc + 32, r2);
+        tmem_ld16(sc + 48, r3);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          x[c] = __uint_as_float(r0[c]);
+          x[16 + c] = __uint_as_float(r1[c]);
+          x[32 + c] = __uint_as_float(r2[c]);
+          x[48 + c] = __uint_as_float(r3[c]);
+        }
+      }
+      const bool edge = (a.causal && KBLK * j + KBLK - 1 > QBLK * i) || (KBLK * j + KBLK > a.N);
+      float mloc = -INFINITY;
+      if (!row_ok) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = -INFINITY;
+      } else if (edge) {
+        const int lim_causal = a.causal ? row_g - KBLK * j : 1 << 30;  // cols c > lim are hidden
+        const int lim_tail = a.N - 1 - KBLK * j;
+        const int lim = min(lim_causal, lim_tail);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          x[c] = (c > lim) ? -INFINITY : x[c] * a.scale_log2;
+          mloc = fmaxf(mloc, x[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          x[c] *= a.scale_log2;
+          mloc = fmaxf(mloc, x[c]);
+        }
+      }
+      const float m_new = fmaxf(m_run, mloc);
+      const bool trailing = !row_ok || mloc == -INFINITY || m_new == -INFINITY || (mloc - m_new < a.lam_log2);
+      const bool wskip = __all_sync(0xffffffffu, trailing);
+      const bool resc = m_new > m_ref + static_cast<float>(RESCALE_LOG2);
+      const float alpha = resc ? fast_exp2(m_ref - m_new) : 1.f;
+      if (__any_sync(0xffffffffu, resc) && t > 0) {
+        // O must hold P_{t-1} V_{t-1} before it is rescaled
+        if (!mbar_wait(&cs.o_done, (t - 1) & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int q = 0; q < D / 16; ++q) {
+          uint32_t rr[16];
+          tmem_ld16(tl + 16 * q, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
+          tmem_st16(tl + 16 * q, rr);
+        }
+      }
+      if (resc) m_ref = m_new;
+      m_run = m_new;
+      l *= alpha;
+      float rs = 0.f;
+      uint32_t pk[32];
+      const bool live = m_ref != -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = live ? fast_exp2(x[2 * c] - m_ref) : 0.f;
+        const float p1 = live ? fast_exp2(x[2 * c + 1] - m_ref) : 0.f;
+        rs += p0 + p1;
+        pk[c] = wskip ? 0u : pack_bf16x2(p0, p1);
+      }
+      l += rs;
+      {
+        uint32_t rr[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) rr[c] = pk[c];
+        tmem_st16(sc, rr);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) rr[c] = pk[16 + c];
+        tmem_st16(sc + 16, rr);
+      }
+      tmem_st_wait();
+      if (lane == 0) cs.skip[buf][warp] = wskip ? 1 : 0;
+      nskip += wskip ? 1 : 0;
+      tc_fence_before();
+      mbar_arrive(&cs.p_full[buf]);
+    }
+    // ------------------------------------ epilogue ------------------------------------
+    bool have_o = false;
+    if (T > 0 && ok) {
+      ok = mbar_wait(&cs.o_done, (T - 1) & 1, abort, a.status) && mbar_wait(&cs.mma_done, 0, abort, a.status);
+      tc_fence_after();
+      have_o = ok && cs.pv_any != 0;
+    }
+    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    __nv_bfloat16 *orow = a.o + b * a.o_sb + h * a.o_sh + static_cast<int64_t>(row_g) * a.o_sn;
+#pragma unroll 1
+    for (int q = 0; q < D / 16; ++q) {
+      uint32_t rr[16];
+      if (have_o) {
+        tmem_ld16(tl + 16 * q, rr);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) rr[c] = 0u;
+      }
+      uint4 o0, o1;
+      o0.x = pack_bf16x2(__uint_as_float(rr[0]) * inv_l, __uint_as_float(rr[1]) * inv_l);
+      o0.y = pack_bf16x2(__uint_as_float(rr[2]) * inv_l, __uint_as_float(rr[3]) * inv_l);
+      o0.z = pack_bf16x2(__uint_as_float(rr[4]) * inv_l, __uint_as_float(rr[5]) * inv_l);
+      o0.w = pack_bf16x2(__uint_as_float(rr[6]) * inv_l, __uint_as_float(rr[7]) * inv_l);
+      o1.x = pack_bf16x2(__uint_as_float(rr[8]) * inv_l, __uint_as_float(rr[9]) * inv_l);
+      o1.y = pack_bf16x2(__uint_as_float(rr[10]) * inv_l, __uint_as_float(rr[11]) * inv_l);
+      o1.z = pack_bf16x2(__uint_as_float(rr[12]) * inv_l, __uint_as_float(rr[13]) * inv_l);
+      o1.w = pack_bf16x2(__uint_as_float(rr[14]) * inv_l, __uint_as_float(rr[15]) * inv_l);
+      if (row_ok) {
+        *reinterpret_cast<uint4 *>(orow + 16 * q) = o0;
+        *reinterpret_cast<uint4 *>(orow + 16 * q + 8) = o1;
+      }
+    }
+    if (a.stats && lane == 0 && nskip) atomicAdd(a.stats + 2, static_cast<unsigned long long>(nskip));
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+template <int D, int STAGES>
+cudaError_t launch_t(const AttnLaunch &l, const AttnArgs &a, cudaStream_t st) {
+  const uint32_t smem = Smem<D, STAGES>::TOTAL;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(bsattn_kernel<D, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t grid = static_cast<int64_t>(a.B) * a.Hq * a.nqb;
+  bsattn_kernel<D, STAGES><<<static_cast<unsigned>(grid), NTHREADS, smem, st>>>(l.tq, l.tk, l.tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
+  AttnArgs a;
+  a.mask = l.mask;
+  a.o = static_cast<__nv_bfloat16 *>(l.o);
+  a.o_sb = l.o_sb; a.o_sh = l.o_sh; a.o_sn = l.o_sn;
+  a.B = l.B; a.Hq = l.Hq; a.Hkv = l.Hkv; a.G = l.Hq / l.Hkv; a.N = l.N;
+  a.nqb = (l.N + QBLK - 1) / QBLK;
+  a.nkb = (l.N + KBLK - 1) / KBLK;
+  a.causal = l.causal;
+  const float LOG2E = 1.4426950408889634f;
+  a.scale_log2 = l.scale * LOG2E;
+  a.lam_log2 = (l.lambda == -INFINITY) ? -INFINITY : l.lambda * LOG2E;
+  a.stats = l.stats;
+  a.status = l.status;
+  if (static_cast<int64_t>(a.B) * a.Hq * a.nqb == 0) return cudaSuccess;
+  return l.d == 128 ? launch_t<128, 2>(l, a, st) : launch_t<64, 4>(l, a, st);
+}
+
+}  // namespace sparge

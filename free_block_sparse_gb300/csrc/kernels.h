@@ -1,0 +1,52 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sparge {
+
+struct View {  // a validated bf16 (B, H, N, d) tensor, strides in elements
+  const void *data;
+  int64_t B, H, N, d;
+  int64_t sb, sh, sn;
+};
+
+// Stage-1 workspace (fp32).  Pooled key means are stored d-major, muKt[b][kvh][k][nkb_pad],
+// so the score kernel reads rows of key blocks with contiguous vector loads.
+struct PredictWs {
+  float *muQ;   // [B][Hq][nqb][d]
+  float *sQ;    // [B][Hq][nqb]
+  float *muKt;  // [B][Hkv][d][nkb_pad]
+  float *sK;    // [B][Hkv][nkb_pad]
+  int64_t nkb_pad;
+};
+
+size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
+PredictWs predict_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
+
+cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, cudaStream_t st);
+
+cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int N, int d, float topk,
+                                float theta, int causal, float scale, uint8_t *mask, cudaStream_t st);
+
+struct AttnLaunch {
+  CUtensorMap tq, tk, tv;  // 4-D maps (d, N, H, B), 128-byte swizzle, boxes 64 x 128 (Q) / 64 x 64 (K, V)
+  const uint8_t *mask;     // (B, Hq, nqb, nkb) or nullptr
+  void *o;
+  int64_t o_sb, o_sh, o_sn;
+  int B, Hq, Hkv, N, d;
+  int causal;
+  float scale;
+  float lambda;
+  unsigned long long *stats;
+  int *status;
+};
+
+cudaError_t launch_bsattn(const AttnLaunch &a, cudaStream_t st);
+
+cudaError_t launch_permute(const View &x, const int32_t *perm, void *y, int64_t ysb, int64_t ysh, int64_t ysn,
+                           bool inverse, cudaStream_t st);
+
+}  // namespace sparge

@@ -1,0 +1,180 @@
+/*
+ * sparge.h -- C ABI of the GB300 (sm_103a) SpargeAttn sparse-attention forward.
+ *
+ * The method (SpargeAttention: Accurate and Training-free Sparse Attention Accelerating Any
+ * Model Inference, abstract and summary pages) is a two-stage online filter:
+ *   stage 1 predicts a 128x64 block mask from mean-pooled Q/K blocks (sparge_predict_mask);
+ *   stage 2 runs flash attention over the kept tiles only, and inside its online softmax
+ *   skips a warp's P.V update when its row maxima trail the running maxima by more than
+ *   lambda (sparge_block_sparse_attn).
+ * sparge_attn chains the two, as the plug-and-play call of the SpargeAttn overview page
+ * ("Using the plug-and-play API": attn(q, k, v, topk=0.5, is_causal=False)).
+ *
+ * Conventions shared by every call
+ *   - Tensors are bf16 in (B, H, N, d) order ("HND"), described by sparge_tensor.  The d axis
+ *     must be contiguous; stride_n, stride_h and stride_b are in elements and must be
+ *     multiples of 8 (16 bytes); data must be 16-byte aligned.  d is 64 or 128.
+ *   - K and V may have fewer heads than Q (grouped-query attention): Hq % Hkv == 0 and query
+ *     head h reads key/value head h / (Hq / Hkv).
+ *   - The block mask is uint8, contiguous, shape (B, Hq, ceil(N/128), ceil(N/64)); 1 keeps
+ *     the 128x64 tile, 0 drops it (SpargeAttention Chinese README, custom block-sparse mask).
+ *   - Every pointer except the *_host ones is a device pointer.  The caller owns every buffer
+ *     (inputs, outputs, mask, workspace); the library allocates no device memory.  All work
+ *     is enqueued asynchronously on the caller's stream; no call synchronises except
+ *     sparge_get_device_status.
+ *   - Every call returns SPARGE_OK (0) or a negative status; sparge_last_error() then gives a
+ *     message (thread-local).  Arguments are validated on the host before anything is
+ *     enqueued, so a failed validation leaves the outputs untouched.
+ *   - Device-side waits are bounded; a wait that runs out records SPARGE_ERR_DEVICE_TIMEOUT in
+ *     a device status word that sparge_get_device_status reads.
+ */
+#ifndef SPARGE_H
+#define SPARGE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *sparge_stream_t; /* the same handle type as cudaStream_t */
+
+enum sparge_status {
+  SPARGE_OK = 0,
+  SPARGE_ERR_INVALID_ARG = -1,        /* null pointer, bad shape/stride, topk/theta/lambda out of range */
+  SPARGE_ERR_UNSUPPORTED = -2,        /* d not in {64,128}, dtype not bf16, Hq % Hkv != 0, N too large */
+  SPARGE_ERR_WORKSPACE_TOO_SMALL = -3,
+  SPARGE_ERR_CUDA = -4,               /* a CUDA runtime/driver call or a launch failed */
+  SPARGE_ERR_DEVICE_TIMEOUT = -5      /* a bounded device-side wait ran out */
+};
+
+enum sparge_dtype { SPARGE_BF16 = 1 };
+
+enum sparge_precision {
+  SPARGE_PRECISION_BF16 = 0,          /* bf16 tensor-core products, fp32 accumulation */
+  SPARGE_PRECISION_Q8 = 1             /* 8-bit path (reserved; currently SPARGE_ERR_UNSUPPORTED) */
+};
+
+enum sparge_op {
+  SPARGE_OP_PREDICT_MASK = 1,
+  SPARGE_OP_BLOCK_SPARSE_ATTN = 2,
+  SPARGE_OP_ATTN = 3
+};
+
+/* A strided bf16 tensor of logical shape (B, H, N, d); data is a device pointer. */
+typedef struct sparge_tensor {
+  void *data;
+  int32_t dtype; /* SPARGE_BF16 */
+  int32_t pad_;
+  int64_t B, H, N, d;
+  int64_t stride_b, stride_h, stride_n; /* in elements */
+} sparge_tensor;
+
+/* Counters the attention kernel can add to (device memory, 4 x uint64, caller-zeroed):
+ *   [0] kept tiles visited, [1] tiles whose P.V product was issued,
+ *   [2] (32-row group, tile) pairs whose P.V update the lambda filter skipped,
+ *   [3] valid tiles (tiles not wholly above the causal diagonal). */
+typedef struct sparge_params {
+  float theta;   /* similarity threshold; blocks with self-similarity < theta are always kept */
+  float lambda;  /* <= 0 or -INFINITY (filter off) */
+  float scale;   /* softmax scale; 0 means 1/sqrt(d) */
+  int32_t precision;            /* enum sparge_precision */
+  unsigned long long *stats;    /* optional device pointer to 4 counters, or NULL */
+} sparge_params;
+
+/*
+ * Workspace bytes needed by an op for the given shape (0 if the op needs none).
+ * SPARGE_OP_PREDICT_MASK: pooled means and similarities (fp32).
+ * SPARGE_OP_ATTN: the above plus the uint8 mask.
+ * SPARGE_OP_BLOCK_SPARSE_ATTN: 0.
+ */
+size_t sparge_workspace_bytes(int op, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
+
+/*
+ * Stage 1, mask prediction (SpargeAttention summary page, method paragraph: blocks with high
+ * internal similarity are compressed, non-similar blocks always computed; abstract: the
+ * attention map is predicted so that some matrix multiplications are skipped).
+ *   For each 128-token query block and 64-token key block: the mean over its valid tokens and
+ *   its self-similarity s = mean pairwise cosine = ||mean of unit tokens||^2.  Then per query
+ *   head and query block i: pooled scores scale * muQ_i . muK_j over the valid key blocks
+ *   (causal: 64 j <= 128 i + 127), a row softmax, and the shortest prefix of blocks in
+ *   (probability desc, index asc) order whose cumulative probability reaches topk (all valid
+ *   blocks when topk >= 1).  The row is then OR-ed with every valid block if s_Q(i) < theta,
+ *   and with block j if s_K(j) < theta (per key/value head).
+ * q: (B,Hq,N,d), k: (B,Hkv,N,d).  topk in (0,1]; theta finite.  mask: device, (B,Hq,nqb,nkb).
+ * ws/ws_bytes: device workspace of at least sparge_workspace_bytes(SPARGE_OP_PREDICT_MASK,...).
+ * Supports N <= 131072 (nkb <= 2048).
+ */
+int sparge_predict_mask(const sparge_tensor *q, const sparge_tensor *k, float topk, float theta,
+                        int is_causal, uint8_t *mask, void *ws, size_t ws_bytes,
+                        sparge_stream_t stream);
+
+/*
+ * Stage 2, block-sparse attention (SpargeAttention abstract: the second-stage online
+ * softmax-aware filter; summary: it works at GPU-warp level; Chinese README: custom mask API).
+ *   O = softmax(scale * Q K^T) V restricted to the kept tiles, visited in ascending key-block
+ *   order with an online softmax.  Rows are grouped 32 per warp; for each kept tile a group
+ *   leaves out its P.V update when every row's tile maximum trails its running maximum by more
+ *   than |lambda| (the running maximum and the row sum are still updated).  Rows with no
+ *   visible kept key output 0.  mask may be NULL (every tile kept).  Tiles wholly above the
+ *   causal diagonal are never visited, whatever the mask says.
+ * lambda <= 0 or -INFINITY; precision SPARGE_PRECISION_BF16.  o: (B,Hq,N,d) bf16 output.
+ * ws may be NULL (ws_bytes 0).  stats: optional counters (see sparge_params), may be NULL.
+ */
+int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k,
+                             const sparge_tensor *v, const uint8_t *mask, float lambda,
+                             int is_causal, int precision, sparge_tensor *o, void *ws,
+                             size_t ws_bytes, unsigned long long *stats, sparge_stream_t stream);
+
+/*
+ * The plug-and-play call: sparge_predict_mask with theta = 0.5, then sparge_block_sparse_attn
+ * with lambda = -INFINITY, scale 1/sqrt(d).  ws: sparge_workspace_bytes(SPARGE_OP_ATTN, ...).
+ */
+int sparge_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v,
+                float topk, int is_causal, sparge_tensor *o, void *ws, size_t ws_bytes,
+                sparge_stream_t stream);
+
+/*
+ * sparge_attn with every parameter explicit (theta, lambda, scale, precision, counters).
+ * mask_out: optional device buffer (B,Hq,nqb,nkb) that receives the predicted mask; when
+ * NULL the mask lives in the workspace.
+ */
+int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v,
+                   float topk, int is_causal, const sparge_params *params, sparge_tensor *o,
+                   uint8_t *mask_out, void *ws, size_t ws_bytes, sparge_stream_t stream);
+
+/*
+ * Hilbert-curve token order (SpargeAttention summary page: a space-filling Hilbert-curve
+ * reordering improves token locality and sparsity for visual tasks).
+ * perm (device, int32, length N): y[:, :, t, :] = x[:, :, perm[t], :] (permute) and
+ * y[:, :, perm[t], :] = x[:, :, t, :] (unpermute).  x and y have the same shape; they must
+ * not overlap.  perm must be a permutation of 0..N-1 (not checked on the device).
+ */
+int sparge_permute_tokens(const sparge_tensor *x, const int32_t *perm, sparge_tensor *y,
+                          sparge_stream_t stream);
+int sparge_unpermute_tokens(const sparge_tensor *x, const int32_t *perm, sparge_tensor *y,
+                            sparge_stream_t stream);
+
+/*
+ * Host-side builders of the gather permutation (integer only, host memory, length
+ * n_prefix + H*W or n_prefix + T*H*W).  Text tokens 0..n_prefix-1 stay in place; grid tokens
+ * (stored row-major after the prefix) are ordered by their index on the Hilbert curve of the
+ * smallest power-of-two square (2-D, x = column, y = row, curve from (0,0) to (2^k-1,0)) or
+ * cube (3-D, Skilling's transpose construction on (t, row, column)) covering the grid.
+ */
+int sparge_hilbert_perm_2d(int n_prefix, int H, int W, int32_t *perm_host);
+int sparge_hilbert_perm_3d(int n_prefix, int T, int H, int W, int32_t *perm_host);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *sparge_last_error(void);
+
+/* Reads and clears the device status word after synchronising the stream: SPARGE_OK or
+ * SPARGE_ERR_DEVICE_TIMEOUT (or SPARGE_ERR_CUDA if the read itself failed). */
+int sparge_get_device_status(sparge_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARGE_H */

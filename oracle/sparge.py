@@ -173,14 +173,38 @@ def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal
     return dict(mask=mask, muQ=muQ, sQ=sQ, muK=muK, sK=sK, S=S, P=P)
 
 
-def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal: bool,
-                  eps: float = 1e-3) -> np.ndarray:
-    """Rows whose mask no rounding within ``eps`` can change (the bit-exact comparison set).
+def row_decisive(p: np.ndarray, valid: np.ndarray, sq: float, sk: np.ndarray, topk: float, theta: float,
+                 eps: float = 1e-3) -> bool:
+    """Whether no rounding within ``eps`` can change one mask row (the bit-exact comparison set).
 
     A row is decisive when its query similarity is farther than eps from theta and either it
     keeps every block because s_Q < theta, or (i) the cumulative sum at the cut and the one
     before it are farther than eps from topk, (ii) the probability gap at the cut exceeds eps,
-    and (iii) every valid key block similarity is farther than eps from theta."""
+    and (iii) every valid key block similarity is farther than eps from theta.
+    p: row probabilities (nkb,), valid: bool (nkb,), sq: s_Q of the row, sk: s_K (nkb,)."""
+    if abs(sq - theta) <= eps:
+        return False
+    if sq < theta:
+        return True
+    if not np.all(np.abs(sk[valid] - theta) > eps):
+        return False
+    if topk >= 1.0:
+        return True
+    vj = np.nonzero(valid)[0]
+    order = vj[np.lexsort((vj, -p[vj]))]
+    ps = p[order]
+    c = np.cumsum(ps)
+    hit = np.nonzero(c >= topk)[0]
+    kstar = (hit[0] + 1) if hit.size else order.size
+    c_at = c[kstar - 1]
+    c_before = c[kstar - 2] if kstar >= 2 else 0.0
+    gap = ps[kstar - 1] - (ps[kstar] if kstar < ps.size else 0.0)
+    return bool(abs(c_at - topk) > eps and abs(topk - c_before) > eps and gap > eps)
+
+
+def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal: bool,
+                  eps: float = 1e-3) -> np.ndarray:
+    """row_decisive for every row of a predict_mask result: bool (B, Hq, nqb)."""
     P, sQ, sK = pred["P"], pred["sQ"], pred["sK"]
     B, Hq, nqb, nkb = P.shape
     G = Hq // sK.shape[1]
@@ -188,36 +212,79 @@ def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal
     out = np.zeros((B, Hq, nqb), dtype=bool)
     for b in range(B):
         for h in range(Hq):
-            kd = np.abs(sK[b, h // G] - theta) > eps
             for i in range(nqb):
-                if abs(sQ[b, h, i] - theta) <= eps:
-                    continue
-                if sQ[b, h, i] < theta:
-                    out[b, h, i] = True
-                    continue
-                if not np.all(kd[valid[i]]):
-                    continue
-                if topk >= 1.0:
-                    out[b, h, i] = True
-                    continue
-                p = P[b, h, i]
-                vj = np.nonzero(valid[i])[0]
-                order = vj[np.lexsort((vj, -p[vj]))]
-                ps = p[order]
-                c = np.cumsum(ps)
-                hit = np.nonzero(c >= topk)[0]
-                kstar = (hit[0] + 1) if hit.size else order.size
-                c_at = c[kstar - 1]
-                c_before = c[kstar - 2] if kstar >= 2 else 0.0
-                gap = ps[kstar - 1] - (ps[kstar] if kstar < ps.size else 0.0)
-                if abs(c_at - topk) > eps and abs(topk - c_before) > eps and gap > eps:
-                    out[b, h, i] = True
+                out[b, h, i] = row_decisive(P[b, h, i], valid[i], sQ[b, h, i], sK[b, h // G], topk, theta, eps)
     return out
+
+
+def predict_mask_row(q_block: np.ndarray, k_head: np.ndarray, i: int, topk: float, theta: float,
+                     causal: bool, scale: float = None) -> Dict[str, np.ndarray]:
+    """predict_mask for a single query block: q_block (n_i, d) the tokens of query block i,
+    k_head (N, d) every key of its key/value head.  Same steps as predict_mask, for checking
+    rows of workloads too large to run whole.  Returns mask (nkb,) uint8, P (nkb,), sQ (float),
+    sK (nkb,), valid (nkb,) bool."""
+    N, d = k_head.shape
+    if scale is None:
+        scale = default_scale(d)
+    muq, sq = pool_sim(q_block[None, None], QBLK)
+    muk, sk = pool_sim(k_head[None, None], KBLK)
+    nkb = muk.shape[2]
+    valid = block_valid(i + 1, nkb, causal)[i]
+    s = scale * (muk[0, 0] @ muq[0, 0, 0])
+    s[~valid] = -np.inf
+    p = row_softmax(s)
+    keep = topk_select(p, valid, topk)
+    if sq[0, 0, 0] < theta:
+        keep |= valid
+    keep |= (sk[0, 0] < theta) & valid
+    return dict(mask=keep.astype(np.uint8), P=p, sQ=float(sq[0, 0, 0]), sK=sk[0, 0], valid=valid)
 
 
 # ---------------------------------------------------------------------------------------------
 # Stage 2: block-sparse flash attention with the lambda warp filter
 # ---------------------------------------------------------------------------------------------
+def attn_qblock(Qi: np.ndarray, Kh: np.ndarray, Vh: np.ndarray, i: int, kept, lam: float, causal: bool,
+                scale: float, group: int = WARP_ROWS):
+    """The rows of one query block: Qi (n_i, d), Kh/Vh (N, d) of its key/value head, kept the
+    ascending key-block indices to visit (already restricted to valid tiles).  Returns the
+    output rows (n_i, d) and (kept tiles, skipped group-tiles, tiles with a P.V update)."""
+    N, d = Kh.shape
+    r0 = i * QBLK
+    nr = Qi.shape[0]
+    grp = np.arange(nr) // group
+    ngrp = grp[-1] + 1
+    m = np.full(nr, -np.inf)
+    l = np.zeros(nr)
+    acc = np.zeros((nr, d))
+    rows = np.arange(r0, r0 + nr)
+    n_skip = n_pv = n_tiles = 0
+    for j in kept:
+        c0, c1 = j * KBLK, min(N, (j + 1) * KBLK)
+        n_tiles += 1
+        S = scale * (Qi @ Kh[c0:c1].T)
+        if causal:
+            S = np.where(np.arange(c0, c1)[None, :] > rows[:, None], -np.inf, S)
+        m_loc = S.max(axis=1)
+        m_new = np.maximum(m, m_loc)
+        with np.errstate(invalid="ignore"):
+            trailing = np.isneginf(m_loc) | np.isneginf(m_new) | ((m_loc - m_new) < lam)
+        skip_g = np.array([trailing[grp == g].all() for g in range(ngrp)])
+        n_skip += int(skip_g.sum())
+        fin = ~np.isneginf(m_new)
+        m_ref = np.where(fin, m_new, 0.0)
+        alpha = np.where(fin, np.exp(m - m_ref), 1.0)
+        Pm = np.where(fin[:, None], np.exp(S - m_ref[:, None]), 0.0)
+        l = alpha * l + Pm.sum(axis=1)
+        upd = Pm @ Vh[c0:c1]
+        upd[skip_g[grp]] = 0.0
+        if not skip_g.all():
+            n_pv += 1
+        acc = alpha[:, None] * acc + upd
+        m = m_new
+    out = np.divide(acc, l[:, None], out=np.zeros_like(acc), where=l[:, None] > 0)
+    return out, (n_tiles, n_skip, n_pv)
+
+
 def block_sparse_attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask, lam: float,
                       causal: bool, scale: float = None, group: int = WARP_ROWS,
                       return_stats: bool = False, qblocks=None):
@@ -243,49 +310,18 @@ def block_sparse_attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask, lam: fl
     nqb, nkb = n_blocks(N, QBLK), n_blocks(N, KBLK)
     valid = block_valid(nqb, nkb, causal)
     O = np.zeros((B, Hq, N, d))
-    kept_tiles = 0
-    skipped_group_tiles = 0
-    pv_tiles = 0
+    tot = np.zeros(3, dtype=np.int64)
     if qblocks is None:
         qblocks = [(b, h, i) for b in range(B) for h in range(Hq) for i in range(nqb)]
     for b, h, i in qblocks:
-        Kh, Vh = k[b, h // G], v[b, h // G]
         r0, r1 = i * QBLK, min(N, (i + 1) * QBLK)
-        nr = r1 - r0
-        Qi = q[b, h, r0:r1]
-        grp = np.arange(nr) // group
-        ngrp = grp[-1] + 1
-        m = np.full(nr, -np.inf)
-        l = np.zeros(nr)
-        acc = np.zeros((nr, d))
-        rows = np.arange(r0, r1)
         kept = np.ones(nkb, bool) if mask is None else (mask[b, h, i] != 0)
-        for j in np.nonzero(kept & valid[i])[0]:
-            c0, c1 = j * KBLK, min(N, (j + 1) * KBLK)
-            kept_tiles += 1
-            S = scale * (Qi @ Kh[c0:c1].T)
-            if causal:
-                S = np.where(np.arange(c0, c1)[None, :] > rows[:, None], -np.inf, S)
-            m_loc = S.max(axis=1)
-            m_new = np.maximum(m, m_loc)
-            with np.errstate(invalid="ignore"):
-                trailing = np.isneginf(m_loc) | np.isneginf(m_new) | ((m_loc - m_new) < lam)
-            skip_g = np.array([trailing[grp == g].all() for g in range(ngrp)])
-            skipped_group_tiles += int(skip_g.sum())
-            fin = ~np.isneginf(m_new)
-            m_ref = np.where(fin, m_new, 0.0)
-            alpha = np.where(fin, np.exp(m - m_ref), 1.0)
-            Pm = np.where(fin[:, None], np.exp(S - m_ref[:, None]), 0.0)
-            l = alpha * l + Pm.sum(axis=1)
-            upd = Pm @ Vh[c0:c1]
-            upd[skip_g[grp]] = 0.0
-            if not skip_g.all():
-                pv_tiles += 1
-            acc = alpha[:, None] * acc + upd
-            m = m_new
-        O[b, h, r0:r1] = np.divide(acc, l[:, None], out=np.zeros_like(acc), where=l[:, None] > 0)
+        js = np.nonzero(kept & valid[i])[0]
+        O[b, h, r0:r1], st = attn_qblock(q[b, h, r0:r1], k[b, h // G], v[b, h // G], i, js, lam, causal,
+                                         scale, group)
+        tot += st
     if return_stats:
-        return O, dict(kept_tiles=kept_tiles, skipped_group_tiles=skipped_group_tiles, pv_tiles=pv_tiles)
+        return O, dict(kept_tiles=int(tot[0]), skipped_group_tiles=int(tot[1]), pv_tiles=int(tot[2]))
     return O
 
 

@@ -1,0 +1,151 @@
+"""The C-ABI library without a GPU: it loads, exports every call include/sparge.h declares,
+and its host-only parts (workspace sizes, argument validation that fails before any CUDA call,
+Hilbert permutation builders) behave as documented."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import free_block_sparse_gb300 as fbs
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fbs.LIB_PATH):
+        from free_block_sparse_gb300 import build
+        build.build()
+    return fbs.lib()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(sparge_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "sparge_attn" in names and "sparge_predict_mask" in names and "sparge_block_sparse_attn" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert names <= set(fbs.EXPORTS)
+
+
+def test_workspace_bytes(lib):
+    B, Hq, Hkv, N, d = 1, 32, 8, 131072, 128
+    nqb, nkb = 1024, 2048
+    pred = fbs.workspace_bytes(fbs.SPARGE_OP_PREDICT_MASK, B, Hq, Hkv, N, d)
+    assert pred >= 4 * (Hq * nqb * d + Hq * nqb + Hkv * d * nkb + Hkv * nkb)
+    full = fbs.workspace_bytes(fbs.SPARGE_OP_ATTN, B, Hq, Hkv, N, d)
+    assert full >= pred + Hq * nqb * nkb
+    assert fbs.workspace_bytes(fbs.SPARGE_OP_BLOCK_SPARSE_ATTN, B, Hq, Hkv, N, d) == 0
+    assert fbs.workspace_bytes(fbs.SPARGE_OP_ATTN, B, Hq, Hkv, N, 96) == 0
+
+
+def _t(ptr=0x1000, B=1, H=2, N=256, d=64, dtype=fbs.SPARGE_BF16, sb=None, sh=None, sn=None):
+    sn = d if sn is None else sn
+    sh = N * sn if sh is None else sh
+    sb = H * sh if sb is None else sb
+    return fbs.sparge_tensor(ptr, dtype, 0, B, H, N, d, sb, sh, sn)
+
+
+@pytest.mark.parametrize("case,code", [
+    ("null_q", fbs.SPARGE_ERR_INVALID_ARG),
+    ("bad_d", fbs.SPARGE_ERR_UNSUPPORTED),
+    ("bad_dtype", fbs.SPARGE_ERR_UNSUPPORTED),
+    ("gqa_ratio", fbs.SPARGE_ERR_UNSUPPORTED),
+    ("topk_zero", fbs.SPARGE_ERR_INVALID_ARG),
+    ("topk_nan", fbs.SPARGE_ERR_INVALID_ARG),
+    ("topk_big", fbs.SPARGE_ERR_INVALID_ARG),
+    ("theta_nan", fbs.SPARGE_ERR_INVALID_ARG),
+    ("stride", fbs.SPARGE_ERR_INVALID_ARG),
+    ("misaligned", fbs.SPARGE_ERR_INVALID_ARG),
+    ("null_mask", fbs.SPARGE_ERR_INVALID_ARG),
+    ("small_ws", fbs.SPARGE_ERR_WORKSPACE_TOO_SMALL),
+    ("too_long", fbs.SPARGE_ERR_UNSUPPORTED),
+])
+def test_predict_mask_rejects_bad_arguments(lib, case, code):
+    q, k = _t(), _t()
+    topk, theta, mask, ws, wsb = 0.5, 0.5, 0x2000, 0x3000, 1 << 30
+    if case == "null_q":
+        rc = lib.sparge_predict_mask(None, ctypes.byref(k), topk, theta, 0, mask, ws, wsb, None)
+        assert rc == code and b"NULL" in lib.sparge_last_error()
+        return
+    if case == "bad_d":
+        q, k = _t(d=96), _t(d=96)
+    elif case == "bad_dtype":
+        q = _t(dtype=7)
+    elif case == "gqa_ratio":
+        q, k = _t(H=3), _t(H=2)
+    elif case == "topk_zero":
+        topk = 0.0
+    elif case == "topk_nan":
+        topk = math.nan
+    elif case == "topk_big":
+        topk = 1.5
+    elif case == "theta_nan":
+        theta = math.nan
+    elif case == "stride":
+        q = _t(sn=65)
+    elif case == "misaligned":
+        q = _t(ptr=0x1002)
+    elif case == "null_mask":
+        mask = None
+    elif case == "small_ws":
+        wsb = 16
+    elif case == "too_long":
+        q, k = _t(N=131073), _t(N=131073)
+    rc = lib.sparge_predict_mask(ctypes.byref(q), ctypes.byref(k), topk, theta, 0, mask, ws, wsb, None)
+    assert rc == code, lib.sparge_last_error()
+    assert lib.sparge_last_error()
+
+
+@pytest.mark.parametrize("lam", [0.5, math.nan])
+def test_attention_rejects_bad_lambda(lib, lam):
+    q = _t()
+    rc = lib.sparge_block_sparse_attn(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), None, lam, 0, 0,
+                                      ctypes.byref(q), None, 0, None, None)
+    assert rc == fbs.SPARGE_ERR_INVALID_ARG
+
+
+def test_attention_rejects_mismatched_output(lib):
+    q, o = _t(), _t(H=4)
+    rc = lib.sparge_block_sparse_attn(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), None, -math.inf, 0, 0,
+                                      ctypes.byref(o), None, 0, None, None)
+    assert rc == fbs.SPARGE_ERR_INVALID_ARG
+    rc = lib.sparge_block_sparse_attn(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), None, -math.inf, 0,
+                                      fbs.SPARGE_PRECISION_Q8, ctypes.byref(q), None, 0, None, None)
+    assert rc == fbs.SPARGE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("n_prefix,H,W", [(0, 1, 1), (5, 8, 8), (512, 64, 64), (3, 7, 13), (0, 30, 45)])
+def test_hilbert_2d_matches_oracle(lib, n_prefix, H, W):
+    np.testing.assert_array_equal(fbs.hilbert_perm_2d(n_prefix, H, W), oracle.hilbert_perm_2d(n_prefix, H, W))
+
+
+@pytest.mark.parametrize("n_prefix,T,H,W", [(0, 2, 2, 2), (3, 3, 5, 6), (0, 8, 8, 8), (226, 13, 30, 45)])
+def test_hilbert_3d_matches_oracle(lib, n_prefix, T, H, W):
+    np.testing.assert_array_equal(fbs.hilbert_perm_3d(n_prefix, T, H, W),
+                                  oracle.hilbert_perm_3d(n_prefix, T, H, W))
+
+
+def test_hilbert_rejects_bad_arguments(lib):
+    assert lib.sparge_hilbert_perm_2d(0, 0, 4, None) == fbs.SPARGE_ERR_INVALID_ARG
+    assert lib.sparge_hilbert_perm_3d(-1, 2, 2, 2, None) == fbs.SPARGE_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        fbs.sparge_attn(x, x, x)
