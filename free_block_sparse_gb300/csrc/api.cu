@@ -44,7 +44,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int check_tensor(const sparge_tensor *t, const char *name, View *v) {
   if (!t) return fail(SPARGE_ERR_INVALID_ARG, "%s is NULL", name);
-  if (!t->data) return fail(SPARGE_ERR_INVALID_ARG, "%s->data is NULL", name);
+  if (!t->data && t->B * t->H * t->N != 0) return fail(SPARGE_ERR_INVALID_ARG, "%s->data is NULL", name);
   if (t->dtype != SPARGE_BF16) return fail(SPARGE_ERR_UNSUPPORTED, "%s: only bf16 is supported", name);
   if (t->d != 64 && t->d != 128) return fail(SPARGE_ERR_UNSUPPORTED, "%s: head dim %lld not in {64,128}", name, (long long)t->d);
   if (t->B < 0 || t->H <= 0 || t->N < 0)

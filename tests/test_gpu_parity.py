@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle on the same seeded
+inputs.  Masks bit-exact on decisive rows; bf16 outputs given the same mask at cosine >= 0.9999
+and max-abs error <= 1e-2; pooled statistics at fp32 tolerance; permutations bit-exact."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import free_block_sparse_gb300 as fbs
+import oracle
+import workloads as W
+from gpu_util import COS_MIN, MAXABS, cos_maxabs, dev_bf16, f64, host_f64
+
+pytestmark = pytest.mark.gpu
+
+# small members of each workload family: several tiles and a ragged tail where the family has one
+SMALL = {
+    "tiny": dict(name="tiny"),
+    "llama": dict(name="llama32k", N=4096 + 200, Hq=8, Hkv=2),
+    "flux": dict(name="flux", Hq=4, Hkv=4),
+    "cogvideox": dict(name="cogvideox", Hq=2, Hkv=2, grid=(5, 30, 45)),
+}
+
+
+def make(key):
+    spec = dict(SMALL[key])
+    return W.make_config(spec.pop("name"), **spec)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fbs.lib()
+    assert torch.cuda.is_available()
+    yield
+    torch.cuda.synchronize()
+    assert fbs.device_status() == 0
+
+
+# ------------------------------------------------------------------------------------------------
+# stage 1
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("key", list(SMALL))
+def test_pool_sim_matches_oracle(key):
+    w = make(key)
+    q, k = dev_bf16(w.q), dev_bf16(w.k)
+    ws = torch.zeros(fbs.workspace_bytes(fbs.SPARGE_OP_PREDICT_MASK, w.B, w.Hq, w.Hkv, w.N, w.d),
+                     dtype=torch.uint8, device="cuda")
+    fbs.predict_mask(q, k, w.topk, w.theta, w.causal, ws=ws)
+    torch.cuda.synchronize()
+    muQ, sQ, muK, sK = (t.cpu().numpy().astype(np.float64) for t in fbs.predict_ws_views(ws, w.B, w.Hq, w.Hkv, w.N, w.d))
+    rmuQ, rsQ = oracle.pool_sim(f64(w.q), 128)
+    rmuK, rsK = oracle.pool_sim(f64(w.k), 64)
+    np.testing.assert_allclose(muQ, rmuQ, rtol=1e-5, atol=2e-6)
+    np.testing.assert_allclose(muK, rmuK, rtol=1e-5, atol=2e-6)
+    np.testing.assert_allclose(sQ, rsQ, rtol=1e-5, atol=2e-6)
+    np.testing.assert_allclose(sK, rsK, rtol=1e-5, atol=2e-6)
+
+
+def check_mask(w, gm, topk=None, theta=None):
+    topk = w.topk if topk is None else topk
+    theta = w.theta if theta is None else theta
+    pred = oracle.predict_mask(f64(w.q), f64(w.k), topk, theta, w.causal)
+    dec = oracle.decisive_rows(pred, topk, theta, w.causal)
+    valid = oracle.block_valid(w.nqb, w.nkb, w.causal)
+    assert not gm[:, :, ~valid].any(), "mask keeps tiles above the causal diagonal"
+    assert (gm.sum(axis=-1) >= 1).all(), "a row keeps no block"
+    assert dec.mean() > 0.5, "too few decisive rows to be a meaningful check"
+    bad = np.nonzero((gm != pred["mask"]).any(axis=-1) & dec)
+    assert bad[0].size == 0, "mask differs on decisive rows %s" % (list(zip(*bad))[:5],)
+    return pred, dec
+
+
+@pytest.mark.parametrize("key", list(SMALL))
+def test_mask_matches_oracle_on_decisive_rows(key):
+    w = make(key)
+    gm = fbs.predict_mask(dev_bf16(w.q), dev_bf16(w.k), w.topk, w.theta, w.causal).cpu().numpy()
+    check_mask(w, gm)
+
+
+@pytest.mark.parametrize("topk,theta", [(0.05, 0.5), (0.3, 0.3), (0.9, 0.0), (1.0, 0.5), (0.5, 2.0)])
+def test_mask_topk_theta_sweep(topk, theta):
+    w = make("llama")
+    gm = fbs.predict_mask(dev_bf16(w.q), dev_bf16(w.k), topk, theta, w.causal).cpu().numpy()
+    check_mask(w, gm, topk, theta)
+    if topk >= 1.0 or theta > 1.0:
+        assert (gm == oracle.block_valid(w.nqb, w.nkb, True)[None, None]).all()
+
+
+# ------------------------------------------------------------------------------------------------
+# stage 2
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N,Hq,Hkv", [(128, 1, 1), (1000, 4, 1), (777, 2, 2)])
+def test_dense_attention_all_ones(causal, d, N, Hq, Hkv):
+    qu, ku, vu = W.random_qkv(21, 1, Hq, Hkv, N, d)
+    out = fbs.block_sparse_attn(dev_bf16(qu), dev_bf16(ku), dev_bf16(vu), None, -math.inf, causal)
+    ref = oracle.block_sparse_attn(f64(qu), f64(ku), f64(vu), None, -math.inf, causal)
+    cos, err = cos_maxabs(host_f64(out), ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_random_mask_attention(causal, d):
+    N, Hq, Hkv = 1500, 4, 2
+    qu, ku, vu = W.random_qkv(22, 2, Hq, Hkv, N, d)
+    mask = W.random_mask(23, 2, Hq, N, p=0.3, force_diag=False)
+    mask[0, 0, 3] = 0                               # an empty row: output 0
+    out = fbs.block_sparse_attn(dev_bf16(qu), dev_bf16(ku), dev_bf16(vu), torch.from_numpy(mask).cuda(),
+                                -math.inf, causal)
+    ref = oracle.block_sparse_attn(f64(qu), f64(ku), f64(vu), mask, -math.inf, causal)
+    got = host_f64(out)
+    cos, err = cos_maxabs(got, ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
+    assert (got[0, 0, 3 * 128:4 * 128] == 0).all()
+
+
+@pytest.mark.parametrize("lam", [-12.0, -8.0, -4.0])
+def test_lambda_filter_matches_oracle(lam):
+    w = make("llama")
+    q, k, v = dev_bf16(w.q), dev_bf16(w.k), dev_bf16(w.v)
+    stats = torch.zeros(4, dtype=torch.int64, device="cuda")
+    out = fbs.block_sparse_attn(q, k, v, None, lam, True, stats=stats)
+    ref, st = oracle.block_sparse_attn(f64(w.q), f64(w.k), f64(w.v), None, lam, True, return_stats=True)
+    cos, err = cos_maxabs(host_f64(out), ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
+    s = stats.cpu().numpy()
+    assert s[0] == st["kept_tiles"]
+    assert abs(int(s[2]) - st["skipped_group_tiles"]) <= max(2, st["skipped_group_tiles"] // 1000)
+    assert abs(int(s[1]) - st["pv_tiles"]) <= max(2, st["pv_tiles"] // 1000)
+    if lam >= -8.0:
+        assert s[2] > 0
+
+
+def test_strided_inputs():
+    """Q/K/V as views into one packed (B, N, 3, H, d) buffer: head and token strides differ
+    from the contiguous ones."""
+    B, N, H, d = 1, 700, 2, 64
+    qu, ku, vu = W.random_qkv(24, B, H, H, N, d)
+    packed = torch.empty((B, N, 3, H, d), dtype=torch.bfloat16, device="cuda")
+    for s, u in enumerate((qu, ku, vu)):
+        packed[:, :, s] = dev_bf16(u).transpose(1, 2)
+    q, k, v = (packed[:, :, s].transpose(1, 2) for s in range(3))
+    assert q.stride(2) == 3 * H * d
+    out_full = torch.zeros((B, H, N, 2 * d), dtype=torch.bfloat16, device="cuda")
+    out = out_full[..., :d]
+    fbs.block_sparse_attn(q, k, v, None, -math.inf, False, out=out)
+    ref = oracle.block_sparse_attn(f64(qu), f64(ku), f64(vu), None, -math.inf, False)
+    cos, err = cos_maxabs(host_f64(out), ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
+    assert (out_full[..., d:] == 0).all()
+
+
+# ------------------------------------------------------------------------------------------------
+# the whole path
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("key", ["tiny", "llama"])
+def test_sparge_attn_end_to_end(key):
+    w = make(key)
+    q, k, v = dev_bf16(w.q), dev_bf16(w.k), dev_bf16(w.v)
+    mask = torch.empty((w.B, w.Hq, w.nqb, w.nkb), dtype=torch.uint8, device="cuda")
+    lam = w.lam if key == "llama" else -math.inf
+    out = fbs.sparge_attn_ex(q, k, v, w.topk, w.causal, theta=w.theta, lam=lam, mask_out=mask)
+    gm = mask.cpu().numpy()
+    check_mask(w, gm)
+    ref = oracle.block_sparse_attn(f64(w.q), f64(w.k), f64(w.v), gm, lam, w.causal)
+    cos, err = cos_maxabs(host_f64(out), ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
+    # the plug-and-play call is the same computation with theta 0.5, lambda -inf
+    out2 = fbs.sparge_attn(q, k, v, w.topk, w.causal)
+    if w.theta == 0.5 and lam == -math.inf:
+        assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("key", ["flux", "cogvideox"])
+def test_hilbert_pipeline(key):
+    w = make(key)
+    perm_np = (fbs.hilbert_perm_2d(w.n_prefix, *w.grid) if len(w.grid) == 2
+               else fbs.hilbert_perm_3d(w.n_prefix, *w.grid))
+    perm = torch.from_numpy(perm_np).cuda()
+    q, k, v = dev_bf16(w.q), dev_bf16(w.k), dev_bf16(w.v)
+    pq, pk, pv = (fbs.permute_tokens(t, perm) for t in (q, k, v))
+    for dev_t, host_t in ((pq, w.q), (pk, w.k), (pv, w.v)):
+        assert np.array_equal(dev_t.cpu().view(torch.int16).numpy().view(np.uint16), host_t[:, :, perm_np])
+    mask = torch.empty((w.B, w.Hq, w.nqb, w.nkb), dtype=torch.uint8, device="cuda")
+    po = fbs.sparge_attn_ex(pq, pk, pv, w.topk, w.causal, theta=w.theta, mask_out=mask)
+    out = fbs.unpermute_tokens(po, perm)
+    assert torch.equal(fbs.permute_tokens(out, perm), po)
+    gm = mask.cpu().numpy()
+    wp = W.Workload(**{**w.__dict__})
+    wp.q, wp.k, wp.v = w.q[:, :, perm_np], w.k[:, :, perm_np], w.v[:, :, perm_np]
+    check_mask(wp, gm)
+    ref = oracle.unpermute_tokens(
+        oracle.block_sparse_attn(f64(wp.q), f64(wp.k), f64(wp.v), gm, -math.inf, w.causal), perm_np)
+    cos, err = cos_maxabs(host_f64(out), ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
+
+
+def test_empty_and_degenerate_shapes():
+    for N in (1, 63, 64, 65, 127, 129):
+        qu, ku, vu = W.random_qkv(25, 1, 2, 1, N, 128)
+        q, k, v = dev_bf16(qu), dev_bf16(ku), dev_bf16(vu)
+        out = fbs.sparge_attn(q, k, v, 0.5, True)
+        mask = fbs.predict_mask(q, k, 0.5, 0.5, True)
+        ref = oracle.block_sparse_attn(f64(qu), f64(ku), f64(vu), mask.cpu().numpy(), -math.inf, True)
+        cos, err = cos_maxabs(host_f64(out), ref)
+        assert cos >= COS_MIN and err <= MAXABS, (N, cos, err)
+    z = torch.zeros((0, 2, 128, 64), dtype=torch.bfloat16, device="cuda")
+    fbs.sparge_attn(z, z, z, 0.5, False)
+    torch.cuda.synchronize()
