@@ -4,7 +4,8 @@ pooled scores + softmax + cumulative top-k) followed by block-sparse attention w
 filter, on the Llama-3.1-8B-like causal prefill at 128K tokens (B=1, 32 query heads, 8 KV heads,
 d=128, topk 0.5, theta 0.5, lambda -8; synthetic bf16 inputs).
 
-One step = one sparge_attn_ex call (three kernel launches) over inputs resident in HBM.
+One step = mask prediction then block-sparse attention (four kernel launches: pooling, score/select,
+V to f16, attention) over inputs resident in HBM.
 Prints one JSON line.  ``--impl reference`` times the float64 CPU oracle instead, on a bounded
 sample of the same workload.  Under torchrun every rank runs its own full replica (weak scaling,
 no collective on the data path); timings are reduced with a max over ranks.
@@ -161,6 +162,10 @@ def run_ours(args, rank, world, local_rank):
     o = torch.empty_like(q)
     mask = torch.empty((w.B, w.Hq, w.nqb, w.nkb), dtype=torch.uint8, device=dev)
     ws = torch.empty(fbs.workspace_bytes(fbs.SPARGE_OP_ATTN, w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8, device=dev)
+    ws_pred = torch.empty(fbs.workspace_bytes(fbs.SPARGE_OP_PREDICT_MASK, w.B, w.Hq, w.Hkv, w.N, w.d),
+                          dtype=torch.uint8, device=dev)
+    ws_attn = torch.empty(fbs.workspace_bytes(fbs.SPARGE_OP_BLOCK_SPARSE_ATTN, w.B, w.Hq, w.Hkv, w.N, w.d),
+                          dtype=torch.uint8, device=dev)
     stats = torch.zeros(4, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -172,9 +177,9 @@ def run_ours(args, rank, world, local_rank):
     assert fbs.device_status() == 0
 
     def step():
-        fbs.predict_mask(q, k, w.topk, w.theta, w.causal, ws=ws, mask=mask)
+        fbs.predict_mask(q, k, w.topk, w.theta, w.causal, ws=ws_pred, mask=mask)
         ev_mid.record(stream)
-        fbs.block_sparse_attn(q, k, v, mask, w.lam, w.causal, out=o)
+        fbs.block_sparse_attn(q, k, v, mask, w.lam, w.causal, out=o, ws=ws_attn)
 
     ev_mid = torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
@@ -192,9 +197,9 @@ def run_ours(args, rank, world, local_rank):
     e2 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for s in range(args.steps):
         e0[s].record(stream)
-        fbs.predict_mask(q, k, w.topk, w.theta, w.causal, ws=ws, mask=mask)
+        fbs.predict_mask(q, k, w.topk, w.theta, w.causal, ws=ws_pred, mask=mask)
         e1[s].record(stream)
-        fbs.block_sparse_attn(q, k, v, mask, w.lam, w.causal, out=o)
+        fbs.block_sparse_attn(q, k, v, mask, w.lam, w.causal, out=o, ws=ws_attn)
         e2[s].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -279,7 +284,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(world * dense / e2e_t / 1e12, 2), "unit": "dense-equiv TOPS",
                 "h2d_bytes_per_step": int(w.q.nbytes + w.k.nbytes + w.v.nbytes),
                 "d2h_bytes_per_step": int(o.numel() * 2)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

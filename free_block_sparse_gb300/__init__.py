@@ -167,16 +167,18 @@ def predict_ws_views(ws, B, Hq, Hkv, N, d):
 
 
 def block_sparse_attn(q, k, v, mask=None, lam: float = -math.inf, causal: bool = False, out=None, stats=None,
-                      precision: int = SPARGE_PRECISION_BF16):
+                      precision: int = SPARGE_PRECISION_BF16, ws=None):
     """Stage 2: attention over the kept 128x64 tiles with the lambda warp filter."""
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
+    ws = _workspace(SPARGE_OP_BLOCK_SPARSE_ATTN, q, k, ws)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     mp = 0 if mask is None else mask.data_ptr()
     sp = 0 if stats is None else stats.data_ptr()
     _check(lib().sparge_block_sparse_attn(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), mp, float(lam),
-                                          int(causal), int(precision), ctypes.byref(do), None, 0, sp, _stream()))
+                                          int(causal), int(precision), ctypes.byref(do), ws.data_ptr(), ws.numel(),
+                                          sp, _stream()))
     return out
 
 

@@ -90,14 +90,15 @@ encode_fn_t get_encode() {
   return fn;
 }
 
-int make_map(CUtensorMap *m, const View &v, int box_rows, const char *name) {
+int make_map(CUtensorMap *m, const View &v, int box_rows, const char *name,
+             CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   encode_fn_t enc = get_encode();
   if (!enc) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   cuuint64_t dims[4] = {(cuuint64_t)v.d, (cuuint64_t)v.N, (cuuint64_t)v.H, (cuuint64_t)v.B};
   cuuint64_t strides[3] = {(cuuint64_t)v.sn * 2, (cuuint64_t)v.sh * 2, (cuuint64_t)v.sb * 2};
   cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(v.data), dims, strides, box, es,
+  CUresult r = enc(m, dt, 4, const_cast<void *>(v.data), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
@@ -131,20 +132,31 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
   return SPARGE_OK;
 }
 
+size_t v16_bytes(int64_t B, int64_t Hkv, int64_t N, int64_t d) { return align256((size_t)B * Hkv * N * d * 2); }
+
+// ws: at least v16_bytes(...) for the f16 copy of V
 int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, float lambda, int causal, float scale,
-              int precision, sparge_tensor *o, unsigned long long *stats, cudaStream_t s) {
+              int precision, sparge_tensor *o, unsigned long long *stats, void *ws, size_t ws_bytes,
+              cudaStream_t s) {
   if (precision != SPARGE_PRECISION_BF16) return fail(SPARGE_ERR_UNSUPPORTED, "precision %d not supported", precision);
   View ov;
   int rc = check_tensor(o, "o", &ov);
   if (rc) return rc;
   if (v.B != q.B || v.N != q.N || v.d != q.d || v.H != k.H) return fail(SPARGE_ERR_INVALID_ARG, "v disagrees with q/k");
   if (ov.B != q.B || ov.N != q.N || ov.d != q.d || ov.H != q.H) return fail(SPARGE_ERR_INVALID_ARG, "o disagrees with q");
+  const size_t need = v16_bytes(v.B, v.H, v.N, v.d);
+  if (ws_bytes < need || (need && !ws))
+    return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(SPARGE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   if (q.B == 0 || q.N == 0) return SPARGE_OK;
+  cudaError_t e = launch_convert_v_f16(v, ws, s);
+  if (e != cudaSuccess) return cuda_fail(e, "convert_v launch");
+  View v16{ws, v.B, v.H, v.N, v.d, v.H * v.N * v.d, v.N * v.d, v.d};
   AttnLaunch l;
   memset(&l, 0, sizeof(l));
   if ((rc = make_map(&l.tq, q, 128, "q"))) return rc;
   if ((rc = make_map(&l.tk, k, 64, "k"))) return rc;
-  if ((rc = make_map(&l.tv, v, 64, "v"))) return rc;
+  if ((rc = make_map(&l.tv, v16, 64, "v", CU_TENSOR_MAP_DATA_TYPE_FLOAT16))) return rc;
   l.mask = mask;
   l.o = o->data;
   l.o_sb = ov.sb; l.o_sh = ov.sh; l.o_sn = ov.sn;
@@ -154,7 +166,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   l.lambda = lambda;
   l.stats = stats;
   l.status = status_ptr();
-  cudaError_t e = launch_bsattn(l, s);
+  e = launch_bsattn(l, s);
   if (e != cudaSuccess) return cuda_fail(e, "bsattn launch");
   return SPARGE_OK;
 }
@@ -197,8 +209,11 @@ size_t sparge_workspace_bytes(int op, int64_t B, int64_t Hq, int64_t Hkv, int64_
   switch (op) {
     case SPARGE_OP_PREDICT_MASK:
       return predict_ws_bytes(B, Hq, Hkv, N, d);
+    case SPARGE_OP_BLOCK_SPARSE_ATTN:
+      return v16_bytes(B, Hkv, N, d);
     case SPARGE_OP_ATTN:
-      return predict_ws_bytes(B, Hq, Hkv, N, d) + align256((size_t)B * Hq * cdiv(N, QBLK) * cdiv(N, KBLK));
+      return predict_ws_bytes(B, Hq, Hkv, N, d) + align256((size_t)B * Hq * cdiv(N, QBLK) * cdiv(N, KBLK)) +
+             v16_bytes(B, Hkv, N, d);
     default:
       return 0;
   }
@@ -220,8 +235,6 @@ int sparge_predict_mask(const sparge_tensor *q, const sparge_tensor *k, float to
 int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v,
                              const uint8_t *mask, float lambda, int is_causal, int precision, sparge_tensor *o,
                              void *ws, size_t ws_bytes, unsigned long long *stats, sparge_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   g_last_error[0] = 0;
   View qv, kv, vv;
   int rc;
@@ -229,8 +242,8 @@ int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k, con
       (rc = check_qk(qv, kv)))
     return rc;
   if ((rc = check_lambda(lambda))) return rc;
-  return attn_impl(qv, kv, vv, mask, lambda, is_causal, 1.f / sqrtf((float)qv.d), precision, o, stats,
-                   reinterpret_cast<cudaStream_t>(stream));
+  return attn_impl(qv, kv, vv, mask, lambda, is_causal, 1.f / sqrtf((float)qv.d), precision, o, stats, ws,
+                   ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,
@@ -248,13 +261,15 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
     return fail(SPARGE_ERR_INVALID_ARG, "scale must be finite and >= 0");
   const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)qv.d);
   const size_t need_pred = predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, qv.d);
-  const size_t mask_bytes = (size_t)qv.B * qv.H * cdiv(qv.N, QBLK) * cdiv(qv.N, KBLK);
-  const size_t need = need_pred + (mask_out ? 0 : align256(mask_bytes));
+  const size_t mask_bytes = mask_out ? 0 : align256((size_t)qv.B * qv.H * cdiv(qv.N, QBLK) * cdiv(qv.N, KBLK));
+  const size_t need_v = v16_bytes(vv.B, vv.H, vv.N, vv.d);
+  const size_t need = need_pred + mask_bytes + need_v;
   if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   uint8_t *mask = mask_out ? mask_out : static_cast<uint8_t *>(ws) + need_pred;
+  void *ws_v = static_cast<uint8_t *>(ws) + need_pred + mask_bytes;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s))) return rc;
-  return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, s);
+  return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws_v, need_v, s);
 }
 
 int sparge_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,

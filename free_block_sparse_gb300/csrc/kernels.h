@@ -32,7 +32,8 @@ cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int
                                 float theta, int causal, float scale, uint8_t *mask, cudaStream_t st);
 
 struct AttnLaunch {
-  CUtensorMap tq, tk, tv;  // 4-D maps (d, N, H, B), 128-byte swizzle, boxes 64 x 128 (Q) / 64 x 64 (K, V)
+  CUtensorMap tq, tk, tv;  // 4-D maps (d, N, H, B), 128-byte swizzle, boxes 64 x 128 (Q) / 64 x 64 (K, V);
+                           // Q, K bf16, V the f16 copy
   const uint8_t *mask;     // (B, Hq, nqb, nkb) or nullptr
   void *o;
   int64_t o_sb, o_sh, o_sn;
@@ -45,6 +46,8 @@ struct AttnLaunch {
 };
 
 cudaError_t launch_bsattn(const AttnLaunch &a, cudaStream_t st);
+
+cudaError_t launch_convert_v_f16(const View &v, void *v16, cudaStream_t st);
 
 cudaError_t launch_permute(const View &x, const int32_t *perm, void *y, int64_t ysb, int64_t ysh, int64_t ysn,
                            bool inverse, cudaStream_t st);

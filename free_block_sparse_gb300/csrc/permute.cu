@@ -1,3 +1,5 @@
+// Layout kernels: token permutation along the Hilbert curve, and the f16 copy of V.
+//
 // Token permutation along the Hilbert curve and its inverse (SpargeAttention summary page: a
 // space-filling Hilbert-curve reordering improves token locality and sparsity for visual
 // tasks).  y[:, :, t] = x[:, :, perm[t]] (gather) or y[:, :, perm[t]] = x[:, :, t] (scatter).
@@ -5,6 +7,8 @@
 // a grid-stride loop over all (b, h, t) rows.
 #include "common.cuh"
 #include "kernels.h"
+
+#include <cuda_fp16.h>
 
 namespace sparge {
 namespace {
@@ -39,7 +43,45 @@ __global__ void __launch_bounds__(256) permute_kernel(PermArgs a) {
   }
 }
 
+// V (bf16, any legal strides) -> contiguous f16 copy for the P.V product of the attention kernel.
+// cvt.rn.satfinite: exact for |v| <= 65504 (every bf16 value in f16 range keeps its 8 significant
+// bits), larger magnitudes saturate.
+__global__ void __launch_bounds__(256) convert_v_f16_kernel(const __nv_bfloat16 *x, int64_t sb, int64_t sh,
+                                                             int64_t sn, __half *y, int H, int N, int d,
+                                                             int64_t nvec) {
+  const int vpr = d / 8;  // 16-byte vectors per row
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < nvec;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int part = static_cast<int>(e % vpr);
+    const int64_t r = e / vpr;
+    const int t = static_cast<int>(r % N);
+    const int64_t bh = r / N;
+    const int h = static_cast<int>(bh % H), b = static_cast<int>(bh / H);
+    const uint4 v = ld_stream_v4(x + b * sb + h * sh + static_cast<int64_t>(t) * sn + part * 8);
+    uint4 o;
+    o.x = pack_f16x2(bf16lo(v.x), bf16hi(v.x));
+    o.y = pack_f16x2(bf16lo(v.y), bf16hi(v.y));
+    o.z = pack_f16x2(bf16lo(v.z), bf16hi(v.z));
+    o.w = pack_f16x2(bf16lo(v.w), bf16hi(v.w));
+    *reinterpret_cast<uint4 *>(y + e * 8) = o;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_convert_v_f16(const View &v, void *v16, cudaStream_t st) {
+  const int64_t nvec = v.B * v.H * v.N * (v.d / 8);
+  if (nvec == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (nvec + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
+  convert_v_f16_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16 *>(v.data), v.sb, v.sh, v.sn, static_cast<__half *>(v16),
+      static_cast<int>(v.H), static_cast<int>(v.N), static_cast<int>(v.d), nvec);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_permute(const View &x, const int32_t *perm, void *y, int64_t ysb, int64_t ysh, int64_t ysn,
                            bool inverse, cudaStream_t st) {

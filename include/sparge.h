@@ -86,8 +86,9 @@ typedef struct sparge_params {
 /*
  * Workspace bytes needed by an op for the given shape (0 if the op needs none).
  * SPARGE_OP_PREDICT_MASK: pooled means and similarities (fp32).
- * SPARGE_OP_ATTN: the above plus the uint8 mask.
- * SPARGE_OP_BLOCK_SPARSE_ATTN: 0.
+ * SPARGE_OP_BLOCK_SPARSE_ATTN: an f16 copy of V.
+ * SPARGE_OP_ATTN: all of the above plus the uint8 mask.
+ * Returns 0 for an unknown op or an unsupported shape.
  */
 size_t sparge_workspace_bytes(int op, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
 
@@ -120,7 +121,12 @@ int sparge_predict_mask(const sparge_tensor *q, const sparge_tensor *k, float to
  *   visible kept key output 0.  mask may be NULL (every tile kept).  Tiles wholly above the
  *   causal diagonal are never visited, whatever the mask says.
  * lambda <= 0 or -INFINITY; precision SPARGE_PRECISION_BF16.  o: (B,Hq,N,d) bf16 output.
- * ws may be NULL (ws_bytes 0).  stats: optional counters (see sparge_params), may be NULL.
+ * Q.K^T runs on bf16 operands; P.V runs on f16 operands (P in [0, 256], V copied to f16 into the
+ * workspace first: exact for |v| <= 65504, larger magnitudes saturate), both with fp32
+ * accumulation.
+ * ws: 256-byte aligned device workspace of at least
+ * sparge_workspace_bytes(SPARGE_OP_BLOCK_SPARSE_ATTN, ...) bytes (the f16 copy of V).
+ * stats: optional counters (see sparge_params), may be NULL.
  */
 int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k,
                              const sparge_tensor *v, const uint8_t *mask, float lambda,

@@ -47,8 +47,9 @@ def test_workspace_bytes(lib):
     pred = fbs.workspace_bytes(fbs.SPARGE_OP_PREDICT_MASK, B, Hq, Hkv, N, d)
     assert pred >= 4 * (Hq * nqb * d + Hq * nqb + Hkv * d * nkb + Hkv * nkb)
     full = fbs.workspace_bytes(fbs.SPARGE_OP_ATTN, B, Hq, Hkv, N, d)
-    assert full >= pred + Hq * nqb * nkb
-    assert fbs.workspace_bytes(fbs.SPARGE_OP_BLOCK_SPARSE_ATTN, B, Hq, Hkv, N, d) == 0
+    attn = fbs.workspace_bytes(fbs.SPARGE_OP_BLOCK_SPARSE_ATTN, B, Hq, Hkv, N, d)
+    assert attn >= 2 * B * Hkv * N * d
+    assert full >= pred + Hq * nqb * nkb + attn
     assert fbs.workspace_bytes(fbs.SPARGE_OP_ATTN, B, Hq, Hkv, N, 96) == 0
 
 
