@@ -68,6 +68,8 @@ EXPORTS = {
     "sparge_unpermute_tokens": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "sparge_hilbert_perm_2d": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "sparge_hilbert_perm_3d": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "sparge_predict_mask_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_float,
+                                                   ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "sparge_last_error": (ctypes.c_char_p, []),
     "sparge_get_device_status": (ctypes.c_int, [ctypes.c_void_p]),
 }

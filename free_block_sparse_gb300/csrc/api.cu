@@ -175,6 +175,21 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
 
 namespace sparge {
 
+int validate_predict_args(const sparge_tensor *q, const sparge_tensor *k, float topk, float theta, View *qv,
+                          View *kv) {
+  g_last_error[0] = 0;
+  int rc;
+  if ((rc = check_tensor(q, "q", qv)) || (rc = check_tensor(k, "k", kv)) || (rc = check_qk(*qv, *kv))) return rc;
+  return check_topk_theta(topk, theta);
+}
+
+int run_predict(const View &q, const View &k, float topk, float theta, int causal, uint8_t *mask, void *ws,
+                size_t ws_bytes, cudaStream_t s) {
+  return predict_impl(q, k, topk, theta, causal, 1.f / sqrtf((float)q.d), mask, ws, ws_bytes, s);
+}
+
+int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
 size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
   const int64_t nqb = cdiv(N, QBLK), nkb = cdiv(N, KBLK), nkb_pad = cdiv(nkb, 4) * 4;
   size_t s = 0;

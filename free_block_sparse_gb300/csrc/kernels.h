@@ -26,6 +26,16 @@ struct PredictWs {
 size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
 PredictWs predict_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
 
+}  // namespace sparge
+struct sparge_tensor;
+namespace sparge {
+// Host-side pieces of the C-ABI layer (api.cu) that other entry points reuse.
+int validate_predict_args(const ::sparge_tensor *q, const ::sparge_tensor *k, float topk, float theta, View *qv,
+                          View *kv);
+int run_predict(const View &q, const View &k, float topk, float theta, int causal, uint8_t *mask, void *ws,
+                size_t ws_bytes, cudaStream_t s);
+int report_error(int code, const char *msg);
+
 cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, cudaStream_t st);
 
 cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int N, int d, float topk,

@@ -172,6 +172,24 @@ int sparge_unpermute_tokens(const sparge_tensor *x, const int32_t *perm, sparge_
 int sparge_hilbert_perm_2d(int n_prefix, int H, int W, int32_t *perm_host);
 int sparge_hilbert_perm_3d(int n_prefix, int T, int H, int W, int32_t *perm_host);
 
+/*
+ * Mask prediction without any device allocation, for callers that cannot call cudaMalloc (a
+ * plug-in inside a host application whose allocator already holds the device memory it hands
+ * out; a latency-critical loop that cannot afford the device synchronisation cudaMalloc and
+ * cudaFree may cause).  The paper has no counterpart: this is a packaging variant of
+ * sparge_predict_mask, with the same arguments minus the workspace and the same result.
+ * The scratch (pooled means and similarities) is a fixed 8 MiB array in device memory that every
+ * GPU loading the library holds until the process exits; a shape whose scratch
+ * (sparge_workspace_bytes(SPARGE_OP_PREDICT_MASK, ...)) exceeds 8 MiB is rejected with
+ * SPARGE_ERR_UNSUPPORTED before anything is enqueued.  The first call on a device looks up the
+ * array's device address with that device current; make that first call before any stream
+ * capture.  All calls on a device share the array and it keeps the last call's contents (no
+ * part of it needs to start at zero): calls that can overlap on the GPU (different streams, no
+ * ordering between them) race on it and must be serialised by the caller.
+ */
+int sparge_predict_mask_noalloc(const sparge_tensor *q, const sparge_tensor *k, float topk, float theta,
+                                int is_causal, uint8_t *mask, sparge_stream_t stream);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char *sparge_last_error(void);
 
