@@ -4,8 +4,9 @@ pooled scores + softmax + cumulative top-k) followed by block-sparse attention w
 filter, on the Llama-3.1-8B-like causal prefill at 128K tokens (B=1, 32 query heads, 8 KV heads,
 d=128, topk 0.5, theta 0.5, lambda -8; synthetic bf16 inputs).
 
-One step = mask prediction then block-sparse attention (four kernel launches: pooling, score/select,
-V to f16, attention) over inputs resident in HBM.
+One step = one sparge_attn_ex call (four kernel launches: pooling, score/select, V to f16,
+attention) over inputs resident in HBM; CUDA events recorded by the library around each kernel
+give the per-kernel times.
 Prints one JSON line.  ``--impl reference`` times the float64 CPU oracle instead, on a bounded
 sample of the same workload.  Under torchrun every rank runs its own full replica (weak scaling,
 no collective on the data path); timings are reduced with a max over ranks.
@@ -162,10 +163,6 @@ def run_ours(args, rank, world, local_rank):
     o = torch.empty_like(q)
     mask = torch.empty((w.B, w.Hq, w.nqb, w.nkb), dtype=torch.uint8, device=dev)
     ws = torch.empty(fbs.workspace_bytes(fbs.SPARGE_OP_ATTN, w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8, device=dev)
-    ws_pred = torch.empty(fbs.workspace_bytes(fbs.SPARGE_OP_PREDICT_MASK, w.B, w.Hq, w.Hkv, w.N, w.d),
-                          dtype=torch.uint8, device=dev)
-    ws_attn = torch.empty(fbs.workspace_bytes(fbs.SPARGE_OP_BLOCK_SPARSE_ATTN, w.B, w.Hq, w.Hkv, w.N, w.d),
-                          dtype=torch.uint8, device=dev)
     stats = torch.zeros(4, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -176,12 +173,15 @@ def run_ours(args, rank, world, local_rank):
     kept, pv, skipped, valid = (int(x) for x in stats.cpu().tolist())
     assert fbs.device_status() == 0
 
-    def step():
-        fbs.predict_mask(q, k, w.topk, w.theta, w.causal, ws=ws_pred, mask=mask)
-        ev_mid.record(stream)
-        fbs.block_sparse_attn(q, k, v, mask, w.lam, w.causal, out=o, ws=ws_attn)
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
 
-    ev_mid = torch.cuda.Event(enable_timing=True)
+    def step(events=None):
+        fbs.sparge_attn_ex(q, k, v, w.topk, w.causal, theta=w.theta, lam=w.lam, mask_out=mask, out=o, ws=ws,
+                           events=events)
+
+    for evs in ev_sets:   # create every event once (torch creates events on first record)
+        for ev in evs:
+            ev.record(stream)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -191,23 +191,17 @@ def run_ours(args, rank, world, local_rank):
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.5)
-    t_pred, t_attn, t_step = [], [], []
-    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e2 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for s in range(args.steps):
-        e0[s].record(stream)
-        fbs.predict_mask(q, k, w.topk, w.theta, w.causal, ws=ws_pred, mask=mask)
-        e1[s].record(stream)
-        fbs.block_sparse_attn(q, k, v, mask, w.lam, w.causal, out=o, ws=ws_attn)
-        e2[s].record(stream)
+        step(ev_sets[s])
     torch.cuda.synchronize()
     clk = clocks.stop()
-    for s in range(args.steps):
-        t_pred.append(e0[s].elapsed_time(e1[s]) / 1e3)
-        t_attn.append(e1[s].elapsed_time(e2[s]) / 1e3)
-        t_step.append(e0[s].elapsed_time(e2[s]) / 1e3)
-    total = e0[0].elapsed_time(e2[-1]) / 1e3
+    # per step: [0] before pooling, [1] after pooling, [2] after score/select, [3] after V copy, [4] after attention
+    t_pool = [e[0].elapsed_time(e[1]) / 1e3 for e in ev_sets]
+    t_sel = [e[1].elapsed_time(e[2]) / 1e3 for e in ev_sets]
+    t_conv = [e[2].elapsed_time(e[3]) / 1e3 for e in ev_sets]
+    t_attn = [e[3].elapsed_time(e[4]) / 1e3 for e in ev_sets]
+    t_pred = [a + b for a, b in zip(t_pool, t_sel)]
+    total = ev_sets[0][0].elapsed_time(ev_sets[-1][4]) / 1e3
     if dist:
         tt = torch.tensor([total], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -243,8 +237,8 @@ def run_ours(args, rank, world, local_rank):
     dense = w.dense_flops()
     ms_step = total / args.steps * 1e3
     value = world * dense * args.steps / total / 1e12
-    t_attn_avg = sum(t_attn) / len(t_attn)
-    t_pred_avg = sum(t_pred) / len(t_pred)
+    avg = lambda xs: sum(xs) / len(xs)
+    t_attn_avg, t_pred_avg = avg(t_attn), avg(t_pred)
     tile_flops = 2.0 * 128 * 64 * w.d
     executed = (kept + pv) * tile_flops
     attn_tflops = executed / t_attn_avg / 1e12
@@ -271,6 +265,8 @@ def run_ours(args, rank, world, local_rank):
                    "causal": w.causal, "topk": w.topk, "theta": w.theta, "lambda": w.lam,
                    "l2": "inputs larger than L2 (Q+K+V %.2f GB), no flush" % ((w.q.nbytes + w.k.nbytes + w.v.nbytes) / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "kernels_ms": {"pool_sim": round(avg(t_pool) * 1e3, 4), "score_select": round(avg(t_sel) * 1e3, 4),
+                       "convert_v_f16": round(avg(t_conv) * 1e3, 4), "bsattn": round(t_attn_avg * 1e3, 4)},
         "attn": {"ms": round(t_attn_avg * 1e3, 4), "dense_equiv_tops": round(dense / t_attn_avg / 1e12, 2),
                  "executed_tflops": round(attn_tflops, 2), "pct_tensor_peak": round(100 * attn_tflops / peak_tc, 2),
                  "kept_tiles": kept, "valid_tiles": valid, "sparsity": round(1 - kept / max(valid, 1), 4),

@@ -46,7 +46,7 @@ class sparge_tensor(ctypes.Structure):
 
 class sparge_params(ctypes.Structure):
     _fields_ = [("theta", ctypes.c_float), ("lambda_", ctypes.c_float), ("scale", ctypes.c_float),
-                ("precision", ctypes.c_int32), ("stats", ctypes.c_void_p)]
+                ("precision", ctypes.c_int32), ("stats", ctypes.c_void_p), ("timing_events", ctypes.c_void_p)]
 
 
 _lib = None
@@ -198,14 +198,23 @@ def sparge_attn(q, k, v, topk: float = 0.5, causal: bool = False, out=None, ws=N
 
 def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: float = -math.inf,
                    scale: float = 0.0, precision: int = SPARGE_PRECISION_BF16, stats=None, mask_out=None,
-                   out=None, ws=None):
-    """sparge_attn with explicit theta, lambda, scale, counters and an optional mask output."""
+                   out=None, ws=None, events=None):
+    """sparge_attn with explicit theta, lambda, scale, counters, an optional mask output and
+    optional timing events (5 torch.cuda.Event, recorded around the four kernels)."""
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
     ws = _workspace(SPARGE_OP_ATTN, q, k, ws)
+    evp = None
+    if events is not None:
+        assert len(events) == 5
+        for ev in events:
+            if not ev.cuda_event:
+                ev.record()   # torch creates the event on its first record
+        evp = (ctypes.c_void_p * 5)(*[ev.cuda_event for ev in events])
     p = sparge_params(float(theta), float(lam), float(scale), int(precision),
-                      0 if stats is None else stats.data_ptr())
+                      0 if stats is None else stats.data_ptr(),
+                      ctypes.cast(evp, ctypes.c_void_p) if evp is not None else None)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     mp = 0 if mask_out is None else mask_out.data_ptr()
     _check(lib().sparge_attn_ex(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), float(topk), int(causal),

@@ -50,7 +50,7 @@ int check_tensor(const sparge_tensor *t, const char *name, View *v) {
   if (t->B < 0 || t->H <= 0 || t->N < 0)
     return fail(SPARGE_ERR_INVALID_ARG, "%s: bad shape B=%lld H=%lld N=%lld", name, (long long)t->B,
                 (long long)t->H, (long long)t->N);
-  if (t->N > (int64_t(1) << 30) || t->B * t->H > (int64_t(1) << 24))
+  if (t->N > (int64_t(1) << 30) || t->B * t->H > (int64_t(1) << 24) || t->B > 65535 || t->H > 65535)
     return fail(SPARGE_ERR_UNSUPPORTED, "%s: shape too large", name);
   if ((reinterpret_cast<uintptr_t>(t->data) & 15u) != 0)
     return fail(SPARGE_ERR_INVALID_ARG, "%s: data not 16-byte aligned", name);
@@ -116,8 +116,15 @@ int check_lambda(float lambda) {
   return SPARGE_OK;
 }
 
+// Records timing event `idx` of `ev` (an array of 5 cudaEvent_t, or nullptr) on stream s.
+int record_event(void *const *ev, int idx, cudaStream_t s) {
+  if (!ev || !ev[idx]) return SPARGE_OK;
+  cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(ev[idx]), s);
+  return e == cudaSuccess ? SPARGE_OK : cuda_fail(e, "timing event record");
+}
+
 int predict_impl(const View &q, const View &k, float topk, float theta, int causal, float scale, uint8_t *mask,
-                 void *ws, size_t ws_bytes, cudaStream_t s) {
+                 void *ws, size_t ws_bytes, cudaStream_t s, void *const *ev = nullptr) {
   if (!mask) return fail(SPARGE_ERR_INVALID_ARG, "mask is NULL");
   if (q.N > 131072) return fail(SPARGE_ERR_UNSUPPORTED, "mask prediction supports N <= 131072 (got %lld)", (long long)q.N);
   const size_t need = predict_ws_bytes(q.B, q.H, k.H, q.N, q.d);
@@ -125,11 +132,14 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
     return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   if (q.B == 0 || q.N == 0) return SPARGE_OK;
   PredictWs pw = predict_ws_carve(ws, q.B, q.H, k.H, q.N, q.d);
+  int rc;
+  if ((rc = record_event(ev, 0, s))) return rc;
   cudaError_t e = launch_pool_sim(q, k, pw, s);
   if (e != cudaSuccess) return cuda_fail(e, "pool_sim launch");
+  if ((rc = record_event(ev, 1, s))) return rc;
   e = launch_score_select(pw, (int)q.B, (int)q.H, (int)k.H, (int)q.N, (int)q.d, topk, theta, causal, scale, mask, s);
   if (e != cudaSuccess) return cuda_fail(e, "score_select launch");
-  return SPARGE_OK;
+  return record_event(ev, 2, s);
 }
 
 size_t v16_bytes(int64_t B, int64_t Hkv, int64_t N, int64_t d) { return align256((size_t)B * Hkv * N * d * 2); }
@@ -137,7 +147,7 @@ size_t v16_bytes(int64_t B, int64_t Hkv, int64_t N, int64_t d) { return align256
 // ws: at least v16_bytes(...) for the f16 copy of V
 int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, float lambda, int causal, float scale,
               int precision, sparge_tensor *o, unsigned long long *stats, void *ws, size_t ws_bytes,
-              cudaStream_t s) {
+              cudaStream_t s, void *const *ev = nullptr) {
   if (precision != SPARGE_PRECISION_BF16) return fail(SPARGE_ERR_UNSUPPORTED, "precision %d not supported", precision);
   View ov;
   int rc = check_tensor(o, "o", &ov);
@@ -151,6 +161,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   if (q.B == 0 || q.N == 0) return SPARGE_OK;
   cudaError_t e = launch_convert_v_f16(v, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "convert_v launch");
+  if ((rc = record_event(ev, 3, s))) return rc;
   View v16{ws, v.B, v.H, v.N, v.d, v.H * v.N * v.d, v.N * v.d, v.d};
   AttnLaunch l;
   memset(&l, 0, sizeof(l));
@@ -168,7 +179,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   l.status = status_ptr();
   e = launch_bsattn(l, s);
   if (e != cudaSuccess) return cuda_fail(e, "bsattn launch");
-  return SPARGE_OK;
+  return record_event(ev, 4, s);
 }
 
 }  // namespace
@@ -283,8 +294,10 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   uint8_t *mask = mask_out ? mask_out : static_cast<uint8_t *>(ws) + need_pred;
   void *ws_v = static_cast<uint8_t *>(ws) + need_pred + mask_bytes;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s))) return rc;
-  return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws_v, need_v, s);
+  if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s, p->timing_events)))
+    return rc;
+  return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws_v, need_v, s,
+                   p->timing_events);
 }
 
 int sparge_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,
@@ -295,6 +308,7 @@ int sparge_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_ten
   p.scale = 0.f;
   p.precision = SPARGE_PRECISION_BF16;
   p.stats = nullptr;
+  p.timing_events = nullptr;
   return sparge_attn_ex(q, k, v, topk, is_causal, &p, o, nullptr, ws, ws_bytes, stream);
 }
 

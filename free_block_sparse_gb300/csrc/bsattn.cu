@@ -287,43 +287,33 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
       tc_fence_after();
       const uint32_t sc = tl + SCOL0 + buf * 64;
-      float x[64];
+      float x[64];  // raw scores Q.K^T of this row; hidden columns become -inf
       {
-        uint32_t r0[16], r1[16], r2[16], r3[16];
-        tmem_ld16(sc, r0);
-        tmem_ld16(sc + 16, r1);
-        tmem_ld16(sc + 32, r2);
-        tmem_ld16(sc + 48, r3);
+        uint32_t r0[32], r1[32];
+        tmem_ld32(sc, r0);
+        tmem_ld32(sc + 32, r1);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < 32; ++c) {
           x[c] = __uint_as_float(r0[c]);
-          x[16 + c] = __uint_as_float(r1[c]);
-          x[32 + c] = __uint_as_float(r2[c]);
-          x[48 + c] = __uint_as_float(r3[c]);
+          x[32 + c] = __uint_as_float(r1[c]);
         }
       }
       const bool edge = (a.causal && KBLK * j + KBLK - 1 > QBLK * i) || (KBLK * j + KBLK > a.N);
-      float mloc = -INFINITY;
       if (!row_ok) {
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = -INFINITY;
       } else if (edge) {
         const int lim_causal = a.causal ? row_g - KBLK * j : 1 << 30;  // cols c > lim are hidden
-        const int lim_tail = a.N - 1 - KBLK * j;
-        const int lim = min(lim_causal, lim_tail);
+        const int lim = min(lim_causal, a.N - 1 - KBLK * j);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          x[c] = (c > lim) ? -INFINITY : x[c] * a.scale_log2;
-          mloc = fmaxf(mloc, x[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          x[c] *= a.scale_log2;
-          mloc = fmaxf(mloc, x[c]);
-        }
+        for (int c = 0; c < 64; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
       }
+      float mraw = fmax3(x[0], x[1], x[2]);
+#pragma unroll
+      for (int c = 3; c < 63; c += 2) mraw = fmax3(mraw, x[c], x[c + 1]);
+      mraw = fmaxf(mraw, x[63]);
+      const float mloc = mraw * a.scale_log2;  // the scale is positive: max commutes with it
       const float m_new = fmaxf(m_run, mloc);
       const bool trailing = !row_ok || mloc == -INFINITY || m_new == -INFINITY || (mloc - m_new < a.lam_log2);
       const bool wskip = __all_sync(0xffffffffu, trailing);
@@ -336,38 +326,58 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           break;
         }
         tc_fence_after();
+        const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll 1
-        for (int q = 0; q < D / 16; ++q) {
-          uint32_t rr[16];
-          tmem_ld16(tl + 16 * q, rr);
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t rr[32];
+          tmem_ld32(tl + 32 * q, rr);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 16; ++c) rr[c] = __float_as_uint(__uint_as_float(rr[c]) * alpha);
-          tmem_st16(tl + 16 * q, rr);
+          for (int c = 0; c < 16; ++c) {
+            const float2 o2 = fmul2(make_float2(__uint_as_float(rr[2 * c]), __uint_as_float(rr[2 * c + 1])), al2);
+            rr[2 * c] = __float_as_uint(o2.x);
+            rr[2 * c + 1] = __float_as_uint(o2.y);
+          }
+          uint32_t lo[16], hi[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            lo[c] = rr[c];
+            hi[c] = rr[16 + c];
+          }
+          tmem_st16(tl + 32 * q, lo);
+          tmem_st16(tl + 32 * q + 16, hi);
         }
       }
       if (resc) m_ref = m_new;
       m_run = m_new;
       l *= alpha;
-      float rs = 0.f;
+      // P = 2^(x * scale_log2 - m_ref); a row whose reference is still -inf has only hidden columns
+      const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nr2 = make_float2(nref, nref);
+      float2 rs2 = make_float2(0.f, 0.f);
       uint32_t pk[32];
-      const bool live = m_ref != -INFINITY;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = live ? fast_exp2(x[2 * c] - m_ref) : 0.f;
-        const float p1 = live ? fast_exp2(x[2 * c + 1] - m_ref) : 0.f;
-        rs += p0 + p1;
-        pk[c] = wskip ? 0u : pack_f16x2(p0, p1);
+        const float2 e2 = ffma2(make_float2(x[2 * c], x[2 * c + 1]), sc2, nr2);
+        const float2 p2 = make_float2(fast_exp2(e2.x), fast_exp2(e2.y));
+        rs2 = fadd2(rs2, p2);
+        pk[c] = pack_f16x2(p2.x, p2.y);
       }
-      l += rs;
+      l += rs2.x + rs2.y;
       {
-        uint32_t rr[16];
+        uint32_t lo[16], hi[16];
+        if (wskip) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) rr[c] = pk[c];
-        tmem_st16(sc, rr);
+          for (int c = 0; c < 16; ++c) lo[c] = hi[c] = 0u;
+        } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) rr[c] = pk[16 + c];
-        tmem_st16(sc + 16, rr);
+          for (int c = 0; c < 16; ++c) {
+            lo[c] = pk[c];
+            hi[c] = pk[16 + c];
+          }
+        }
+        tmem_st16(sc, lo);
+        tmem_st16(sc + 16, hi);
       }
       tmem_st_wait();
       if (lane == 0) cs.skip[buf][warp] = wskip ? 1 : 0;

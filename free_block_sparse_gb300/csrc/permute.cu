@@ -45,41 +45,50 @@ __global__ void __launch_bounds__(256) permute_kernel(PermArgs a) {
 
 // V (bf16, any legal strides) -> contiguous f16 copy for the P.V product of the attention kernel.
 // cvt.rn.satfinite: exact for |v| <= 65504 (every bf16 value in f16 range keeps its 8 significant
-// bits), larger magnitudes saturate.
+// bits), larger magnitudes saturate.  Grid (token chunks, H, B); each thread moves 16 bytes per
+// step with streaming loads, two independent vectors in flight.
+template <int D>
 __global__ void __launch_bounds__(256) convert_v_f16_kernel(const __nv_bfloat16 *x, int64_t sb, int64_t sh,
-                                                             int64_t sn, __half *y, int H, int N, int d,
-                                                             int64_t nvec) {
-  const int vpr = d / 8;  // 16-byte vectors per row
-  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < nvec;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int part = static_cast<int>(e % vpr);
-    const int64_t r = e / vpr;
-    const int t = static_cast<int>(r % N);
-    const int64_t bh = r / N;
-    const int h = static_cast<int>(bh % H), b = static_cast<int>(bh / H);
-    const uint4 v = ld_stream_v4(x + b * sb + h * sh + static_cast<int64_t>(t) * sn + part * 8);
-    uint4 o;
-    o.x = pack_f16x2(bf16lo(v.x), bf16hi(v.x));
-    o.y = pack_f16x2(bf16lo(v.y), bf16hi(v.y));
-    o.z = pack_f16x2(bf16lo(v.z), bf16hi(v.z));
-    o.w = pack_f16x2(bf16lo(v.w), bf16hi(v.w));
-    *reinterpret_cast<uint4 *>(y + e * 8) = o;
+                                                             int64_t sn, __half *y, int N) {
+  constexpr int VPR = D / 8;                 // 16-byte vectors per token row
+  constexpr int ROWS = 2 * 256 / VPR;        // token rows per CTA
+  const int h = blockIdx.y, b = blockIdx.z, H = gridDim.y;
+  const __nv_bfloat16 *xb = x + b * sb + h * sh;
+  __half *yb = y + (static_cast<int64_t>(b) * H + h) * N * D;
+  const int t0 = blockIdx.x * ROWS;
+  uint4 v[2];
+  int t[2], part[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int e = threadIdx.x + u * 256;
+    t[u] = t0 + e / VPR;
+    part[u] = e % VPR;
+    if (t[u] < N) v[u] = ld_stream_v4(xb + static_cast<int64_t>(t[u]) * sn + part[u] * 8);
+  }
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    if (t[u] < N) {
+      uint4 o;
+      o.x = pack_f16x2(bf16lo(v[u].x), bf16hi(v[u].x));
+      o.y = pack_f16x2(bf16lo(v[u].y), bf16hi(v[u].y));
+      o.z = pack_f16x2(bf16lo(v[u].z), bf16hi(v[u].z));
+      o.w = pack_f16x2(bf16lo(v[u].w), bf16hi(v[u].w));
+      *reinterpret_cast<uint4 *>(yb + static_cast<int64_t>(t[u]) * D + part[u] * 8) = o;
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t launch_convert_v_f16(const View &v, void *v16, cudaStream_t st) {
-  const int64_t nvec = v.B * v.H * v.N * (v.d / 8);
-  if (nvec == 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (nvec + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
-  convert_v_f16_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16 *>(v.data), v.sb, v.sh, v.sn, static_cast<__half *>(v16),
-      static_cast<int>(v.H), static_cast<int>(v.N), static_cast<int>(v.d), nvec);
+  if (v.B * v.H * v.N == 0) return cudaSuccess;
+  const int rows = 2 * 256 / static_cast<int>(v.d / 8);
+  dim3 grid(static_cast<unsigned>((v.N + rows - 1) / rows), static_cast<unsigned>(v.H), static_cast<unsigned>(v.B));
+  const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(v.data);
+  if (v.d == 128)
+    convert_v_f16_kernel<128><<<grid, 256, 0, st>>>(x, v.sb, v.sh, v.sn, static_cast<__half *>(v16), (int)v.N);
+  else
+    convert_v_f16_kernel<64><<<grid, 256, 0, st>>>(x, v.sb, v.sh, v.sn, static_cast<__half *>(v16), (int)v.N);
   return cudaGetLastError();
 }
 
