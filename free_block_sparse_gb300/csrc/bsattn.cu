@@ -44,40 +44,42 @@ struct AttnArgs {
   int *status;
 };
 
-// Warp-collective walk over the kept, valid key blocks of one mask row in ascending order.
+// Warp-collective walk over the kept, valid key blocks of one mask row in ascending order, run
+// by the producer warp only: windows of 512 candidates, 16 per lane loaded as independent bytes,
+// then lowest lane / lowest bit first.  Returns -1 after the last kept block.
 struct KeptScan {
   const uint8_t *row;
-  int n, base;
-  uint32_t bits;
+  int n, base, t;
+  uint32_t bits;  // this lane's 16 flags of the current window
   __device__ void init(const uint8_t *r, int n_valid) {
     row = r;
     n = n_valid;
-    base = -32;
+    base = -512;
+    t = 0;
     bits = 0u;
   }
   __device__ int next(int lane) {
-    while (bits == 0u) {
-      base += 32;
+    if (row == nullptr) return t < n ? t++ : -1;
+    for (;;) {
+      const uint32_t any = __ballot_sync(0xffffffffu, bits != 0u);
+      if (any) {
+        const int l = __ffs(any) - 1;
+        const uint32_t lb = __shfl_sync(0xffffffffu, bits, l);
+        if (lane == l) bits &= bits - 1u;
+        return base + 16 * l + (__ffs(lb) - 1);
+      }
+      base += 512;
       if (base >= n) return -1;
-      const int j = base + lane;
-      const bool k = j < n && (row == nullptr || row[j] != 0);
-      bits = __ballot_sync(0xffffffffu, k);
+      uint32_t f = 0u;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int j = base + 16 * lane + c;
+        if (j < n && __ldg(row + j) != 0) f |= 1u << c;
+      }
+      bits = f;
     }
-    const int l = __ffs(bits) - 1;
-    bits &= bits - 1u;
-    return base + l;
   }
 };
-
-__device__ __forceinline__ int count_kept(const uint8_t *row, int n, int lane) {
-  if (row == nullptr) return n;
-  int cnt = 0;
-  for (int base = 0; base < n; base += 32) {
-    const int j = base + lane;
-    cnt += __popc(__ballot_sync(0xffffffffu, j < n && row[j] != 0));
-  }
-  return cnt;
-}
 
 template <int D, int STAGES>
 struct Smem {
@@ -103,6 +105,7 @@ struct Ctrl {
   uint64_t mma_done;
   uint64_t final_bar;
   uint32_t tmem_base;
+  int jtile[4];  // key block held by each K/V stage; -1 marks the end of the row
   int abort;
   int pv_any;
   uint8_t skip[2][4];
@@ -161,30 +164,32 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   tc_fence_after();
   const uint32_t tmem = cs.tmem_base;
 
-  const int T = count_kept(mrow, n_valid, lane);  // warp-uniform, same in every warp
-
   const uint32_t sQ = smem_u32(smem + L::OFF_Q);
   const uint32_t sKV = smem_u32(smem + L::OFF_KV);
 
   if (warp == 4) {
     // ------------------------------------ producer ------------------------------------
-    if (T > 0) {
+    // Loads Q with the first kept tile, then every kept K/V tile; after the last one it fills the
+    // next stage with the end mark (jtile = -1, a plain arrive without data).
+    KeptScan ks;
+    ks.init(mrow, n_valid);
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+    }
+    for (int t = 0;; ++t) {
+      const int j = ks.next(lane);
+      const int st = t % STAGES;
+      if (!mbar_wait(&cs.kv_empty[st], ((t / STAGES) & 1) ^ 1, abort, a.status)) break;
       if (lane == 0) {
-        prefetch_tmap(&tq);
-        prefetch_tmap(&tk);
-        prefetch_tmap(&tv);
-        mbar_arrive_expect_tx(&cs.q_full, L::Q_BYTES);
-        for (int c = 0; c < L::QCH; ++c)
-          tma_load_4d(smem + L::OFF_Q + c * 16384, &tq, &cs.q_full, 64 * c, QBLK * i, h, b);
-      }
-      KeptScan ks;
-      ks.init(mrow, n_valid);
-      for (int t = 0;; ++t) {
-        const int j = ks.next(lane);
-        if (j < 0) break;
-        const int st = t % STAGES;
-        if (!mbar_wait(&cs.kv_empty[st], ((t / STAGES) & 1) ^ 1, abort, a.status)) break;
-        if (lane == 0) {
+        cs.jtile[st] = j;
+        if (j >= 0) {
+          if (t == 0) {
+            mbar_arrive_expect_tx(&cs.q_full, L::Q_BYTES);
+            for (int c = 0; c < L::QCH; ++c)
+              tma_load_4d(smem + L::OFF_Q + c * 16384, &tq, &cs.q_full, 64 * c, QBLK * i, h, b);
+          }
           uint8_t *kdst = smem + L::OFF_KV + st * L::STAGE_BYTES;
           uint8_t *vdst = kdst + L::K_BYTES;
           mbar_arrive_expect_tx(&cs.kv_full[st], L::STAGE_BYTES);
@@ -192,44 +197,51 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             tma_load_4d(kdst + c * L::KV_CHUNK, &tk, &cs.kv_full[st], 64 * c, KBLK * j, kvh, b);
             tma_load_4d(vdst + c * L::KV_CHUNK, &tv, &cs.kv_full[st], 64 * c, KBLK * j, kvh, b);
           }
+        } else {
+          mbar_arrive(&cs.kv_full[st]);
         }
-        __syncwarp();
       }
-      if (*abort) {  // let copies already in flight land before the CTA exits
-        const uint64_t t0 = global_timer_ns();
-        while (global_timer_ns() - t0 < 1000000ull) {
-        }
+      __syncwarp();
+      if (j < 0) break;
+    }
+    if (*abort) {  // let copies already in flight land before the CTA exits
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 1000000ull) {
       }
     }
   } else if (warp == 5) {
     // ------------------------------------ MMA issuer ------------------------------------
-    int pv_count = 0;
-    if (T > 0) {
-      bool ok = mbar_wait(&cs.q_full, 0, abort, a.status);
+    int pv_count = 0, T = 0;
+    // next_tile(u): waits for stage u % STAGES and returns its key block (-1 = end of row)
+    auto next_tile = [&](int u) -> int {
+      const int st = u % STAGES;
+      if (!mbar_wait(&cs.kv_full[st], (u / STAGES) & 1, abort, a.status)) return -2;
       tc_fence_after();
-      auto issue_s = [&](int u) -> bool {
-        const int st = u % STAGES;
-        if (!mbar_wait(&cs.kv_full[st], (u / STAGES) & 1, abort, a.status)) return false;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t kaddr = sKV + st * L::STAGE_BYTES;
-          const uint32_t dS = tmem + SCOL0 + (u & 1) * 64;
+      return cs.jtile[st];
+    };
+    auto issue_s = [&](int u) {
+      if (lane == 0) {
+        const uint32_t kaddr = sKV + (u % STAGES) * L::STAGE_BYTES;
+        const uint32_t dS = tmem + SCOL0 + (u & 1) * 64;
 #pragma unroll
-          for (int s = 0; s < D / 16; ++s) {
-            const uint64_t da = smem_desc_sw128(sQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
-            const uint64_t db = smem_desc_sw128(kaddr + (s >> 2) * L::KV_CHUNK + (s & 3) * 32, 16, 1024);
-            mma_bf16_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
-          }
-          mma_commit(&cs.s_full[u & 1]);
+        for (int s = 0; s < D / 16; ++s) {
+          const uint64_t da = smem_desc_sw128(sQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+          const uint64_t db = smem_desc_sw128(kaddr + (s >> 2) * L::KV_CHUNK + (s & 3) * 32, 16, 1024);
+          mma_bf16_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
         }
-        __syncwarp();
-        return true;
-      };
-      if (ok) ok = issue_s(0);
+        mma_commit(&cs.s_full[u & 1]);
+      }
+      __syncwarp();
+    };
+    int jn = next_tile(0);
+    if (jn >= 0 && mbar_wait(&cs.q_full, 0, abort, a.status)) {
+      tc_fence_after();
+      issue_s(0);
       uint32_t pv_issued = 0;
-      for (int t = 0; ok && t < T; ++t) {
-        if (t + 1 < T && !issue_s(t + 1)) break;
-        if (!mbar_wait(&cs.p_full[t & 1], (t >> 1) & 1, abort, a.status)) break;
+      for (int t = 0;; ++t) {
+        jn = next_tile(t + 1);
+        if (jn >= 0) issue_s(t + 1);
+        if (jn == -2 || !mbar_wait(&cs.p_full[t & 1], (t >> 1) & 1, abort, a.status)) break;
         tc_fence_after();
         const bool all_skip = cs.skip[t & 1][0] && cs.skip[t & 1][1] && cs.skip[t & 1][2] && cs.skip[t & 1][3];
         const int st = t % STAGES;
@@ -249,6 +261,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           mma_commit(&cs.o_done);
         }
         __syncwarp();
+        T = t + 1;
+        if (jn < 0) break;
       }
       if (lane == 0) {
         cs.pv_any = static_cast<int>(pv_issued);
@@ -274,12 +288,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const bool row_ok = row_g < a.N;
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
-    int nskip = 0;
-    KeptScan ks;
-    ks.init(mrow, n_valid);
+    int nskip = 0, T = 0;
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const int j = ks.next(lane);
+    for (int t = 0;; ++t) {
+      const int st = t % STAGES;
+      if (!mbar_wait(&cs.kv_full[st], (t / STAGES) & 1, abort, a.status)) {
+        ok = false;
+        break;
+      }
+      const int j = cs.jtile[st];
+      if (j < 0) break;
+      T = t + 1;
       const int buf = t & 1;
       if (!mbar_wait(&cs.s_full[buf], (t >> 1) & 1, abort, a.status)) {
         ok = false;

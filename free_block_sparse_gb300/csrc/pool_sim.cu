@@ -5,7 +5,7 @@
 // the valid tokens and s = ||(1/n) sum_a x_a / ||x_a|| ||^2, the mean cosine similarity over
 // all ordered token pairs of the block (pairs a == b included).  A zero token contributes a
 // zero unit vector.  Memory-bound: one pass over Q and K with 16-byte streaming loads, fp32
-// accumulation, warp-shuffle reductions; every load of a CTA is issued before any arithmetic.
+// accumulation (packed pair arithmetic), warp-shuffle reductions.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -20,129 +20,156 @@ struct PoolArgs {
   PredictWs ws;
 };
 
+struct BlockRef {
+  const __nv_bfloat16 *base;  // first token row of the block
+  int64_t sn;                  // token stride (elements)
+  int n;                       // valid tokens
+  int steps;                   // CTA load steps covering the block
+  float *mu;                   // where the mean goes (stride mu_stride between dims)
+  int64_t mu_stride;
+  float *s;                    // where the similarity goes
+};
+
+template <int TPS>
+__device__ __forceinline__ BlockRef block_ref(const PoolArgs &a, int64_t bid, int D) {
+  BlockRef r;
+  if (bid < a.nq_total) {
+    const int i = static_cast<int>(bid % a.nqb);
+    const int64_t bh = bid / a.nqb;
+    const int h = static_cast<int>(bh % a.Hq), b = static_cast<int>(bh / a.Hq);
+    r.base = a.q + b * a.q_sb + h * a.q_sh + static_cast<int64_t>(i) * QBLK * a.q_sn;
+    r.sn = a.q_sn;
+    r.n = min(QBLK, a.N - i * QBLK);
+    r.steps = QBLK / TPS;
+    r.mu = a.ws.muQ + ((static_cast<int64_t>(b) * a.Hq + h) * a.nqb + i) * D;
+    r.mu_stride = 1;
+    r.s = a.ws.sQ + (static_cast<int64_t>(b) * a.Hq + h) * a.nqb + i;
+  } else {
+    bid -= a.nq_total;
+    const int j = static_cast<int>(bid % a.nkb);
+    const int64_t bh = bid / a.nkb;
+    const int h = static_cast<int>(bh % a.Hkv), b = static_cast<int>(bh / a.Hkv);
+    r.base = a.k + b * a.k_sb + h * a.k_sh + static_cast<int64_t>(j) * KBLK * a.k_sn;
+    r.sn = a.k_sn;
+    r.n = min(KBLK, a.N - j * KBLK);
+    r.steps = KBLK / TPS;
+    r.mu = a.ws.muKt + (static_cast<int64_t>(b) * a.Hkv + h) * D * a.ws.nkb_pad + j;
+    r.mu_stride = a.ws.nkb_pad;
+    r.s = a.ws.sK + (static_cast<int64_t>(b) * a.Hkv + h) * a.ws.nkb_pad + j;
+  }
+  return r;
+}
+
+// Persistent CTAs walk the blocks (all query blocks, then all key blocks) with a stride of the
+// grid size.  Each thread keeps the 16-byte vectors of the next block in flight (registers)
+// while it reduces the current one, so the loads of a CTA overlap its arithmetic.
 template <int D>
-__global__ void __launch_bounds__(256) pool_sim_kernel(PoolArgs a) {
+__global__ void __launch_bounds__(256, (D == 128 ? 2 : 3)) pool_sim_kernel(PoolArgs a) {
   constexpr int LPT = D / 8;        // lanes per token, 8 bf16 (16 bytes) per lane
   constexpr int TPW = 32 / LPT;     // tokens per warp per step
   constexpr int TPS = 8 * TPW;      // tokens per CTA step
   constexpr int MAXSTEPS = QBLK / TPS;
 
-  __shared__ float red[8][2][D];
-  __shared__ float red_s[D / 32];
+  __shared__ float red[2][8][2][D];  // double-buffered per-warp partial sums (x and unit x)
 
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / LPT, part = lane % LPT;
+  const int64_t total = a.nq_total + static_cast<int64_t>(a.B) * a.Hkv * a.nkb;
+
+  auto load = [&](const BlockRef &r, uint4 (&v)[MAXSTEPS]) {
+#pragma unroll
+    for (int st = 0; st < MAXSTEPS; ++st) {
+      const int t = st * TPS + w * TPW + sub;
+      v[st] = make_uint4(0, 0, 0, 0);
+      if (st < r.steps && t < r.n) v[st] = ld_stream_v4(r.base + t * r.sn + part * 8);
+    }
+  };
 
   int64_t bid = blockIdx.x;
-  const bool isQ = bid < a.nq_total;
-  const __nv_bfloat16 *base;
-  int blk, tok0, b, h, blkidx;
-  if (isQ) {
-    blkidx = static_cast<int>(bid % a.nqb);
-    int64_t bh = bid / a.nqb;
-    h = static_cast<int>(bh % a.Hq);
-    b = static_cast<int>(bh / a.Hq);
-    base = a.q + b * a.q_sb + h * a.q_sh;
-    blk = QBLK;
-    tok0 = blkidx * QBLK;
-  } else {
-    bid -= a.nq_total;
-    blkidx = static_cast<int>(bid % a.nkb);
-    int64_t bh = bid / a.nkb;
-    h = static_cast<int>(bh % a.Hkv);
-    b = static_cast<int>(bh / a.Hkv);
-    base = a.k + b * a.k_sb + h * a.k_sh;
-    blk = KBLK;
-    tok0 = blkidx * KBLK;
-  }
-  const int64_t sn = isQ ? a.q_sn : a.k_sn;
-  const int n = min(blk, a.N - tok0);
-  const int steps = blk / TPS;
-
-  uint4 v[MAXSTEPS];
+  if (bid >= total) return;
+  BlockRef cur = block_ref<TPS>(a, bid, D);
+  uint4 vc[MAXSTEPS], vn[MAXSTEPS];
+  load(cur, vc);
+  for (int it = 0; bid < total; ++it) {
+    const int64_t nbid = bid + gridDim.x;
+    BlockRef nxt = cur;
+    if (nbid < total) {
+      nxt = block_ref<TPS>(a, nbid, D);
+      load(nxt, vn);
+    }
+    float2 sx2[4], sh2[4];
 #pragma unroll
-  for (int s = 0; s < MAXSTEPS; ++s) {
-    const int t = s * TPS + w * TPW + sub;
-    v[s] = make_uint4(0, 0, 0, 0);
-    if (s < steps && t < n) v[s] = ld_stream_v4(base + (tok0 + t) * sn + part * 8);
-  }
-
-  float sx[8], sh[8];
+    for (int c = 0; c < 4; ++c) sx2[c] = sh2[c] = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int c = 0; c < 8; ++c) sx[c] = sh[c] = 0.f;
-
+    for (int st = 0; st < MAXSTEPS; ++st) {
+      if (st < cur.steps) {
+        const uint32_t wd[4] = {vc[st].x, vc[st].y, vc[st].z, vc[st].w};
+        float2 x2[4];
 #pragma unroll
-  for (int s = 0; s < MAXSTEPS; ++s) {
-    if (s < steps) {
-      const uint32_t wd[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
-      float x[8];
+        for (int c = 0; c < 4; ++c) x2[c] = make_float2(bf16lo(wd[c]), bf16hi(wd[c]));
+        float2 n2 = fmul2(x2[0], x2[0]);
+#pragma unroll
+        for (int c = 1; c < 4; ++c) n2 = ffma2(x2[c], x2[c], n2);
+        float nn = n2.x + n2.y;
+#pragma unroll
+        for (int off = LPT / 2; off > 0; off >>= 1) nn += __shfl_xor_sync(0xffffffffu, nn, off);
+        const float inv = nn > 0.f ? rsqrtf(nn) : 0.f;
+        const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          sx2[c] = fadd2(sx2[c], x2[c]);
+          sh2[c] = ffma2(x2[c], inv2, sh2[c]);
+        }
+      }
+    }
+    // sum over the token slots of the warp: lanes with the same `part`
+#pragma unroll
+    for (int off = LPT; off < 32; off <<= 1) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        x[2 * c] = bf16lo(wd[c]);
-        x[2 * c + 1] = bf16hi(wd[c]);
-      }
-      float n2 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) n2 = fmaf(x[c], x[c], n2);
-#pragma unroll
-      for (int off = LPT / 2; off > 0; off >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, off);
-      const float inv = n2 > 0.f ? rsqrtf(n2) : 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        sx[c] += x[c];
-        sh[c] = fmaf(x[c], inv, sh[c]);
+        sx2[c].x += __shfl_xor_sync(0xffffffffu, sx2[c].x, off);
+        sx2[c].y += __shfl_xor_sync(0xffffffffu, sx2[c].y, off);
+        sh2[c].x += __shfl_xor_sync(0xffffffffu, sh2[c].x, off);
+        sh2[c].y += __shfl_xor_sync(0xffffffffu, sh2[c].y, off);
       }
     }
-  }
-  // sum over the token slots of the warp: lanes with the same `part`
+    float(*rb)[2][D] = red[it & 1];
+    if (sub == 0) {
 #pragma unroll
-  for (int off = LPT; off < 32; off <<= 1) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      sx[c] += __shfl_xor_sync(0xffffffffu, sx[c], off);
-      sh[c] += __shfl_xor_sync(0xffffffffu, sh[c], off);
+      for (int c = 0; c < 4; ++c) {
+        rb[w][0][part * 8 + 2 * c] = sx2[c].x;
+        rb[w][0][part * 8 + 2 * c + 1] = sx2[c].y;
+        rb[w][1][part * 8 + 2 * c] = sh2[c].x;
+        rb[w][1][part * 8 + 2 * c + 1] = sh2[c].y;
+      }
     }
-  }
-  if (sub == 0) {
+    __syncthreads();
+    if (w == 0) {
+      // warp 0 finishes the block while the other warps go on with the next one; the partial
+      // sums alternate between two buffers, so the next barrier orders the reuse.
+      const float invn = 1.f / static_cast<float>(cur.n);
+      float hsq = 0.f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      red[w][0][part * 8 + c] = sx[c];
-      red[w][1][part * 8 + c] = sh[c];
+      for (int dd = 0; dd < D / 32; ++dd) {
+        const int dim = lane + 32 * dd;
+        float mx = 0.f, hx = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < 8; ++ww) {
+          mx += rb[ww][0][dim];
+          hx += rb[ww][1][dim];
+        }
+        hx *= invn;
+        hsq = fmaf(hx, hx, hsq);
+        cur.mu[dim * cur.mu_stride] = mx * invn;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) hsq += __shfl_xor_sync(0xffffffffu, hsq, off);
+      if (lane == 0) *cur.s = hsq;
     }
-  }
-  __syncthreads();
-  const int t = threadIdx.x;
-  float hsq = 0.f;
-  const float invn = 1.f / static_cast<float>(n);
-  if (t < D) {
-    float mx = 0.f, hx = 0.f;
+    cur = nxt;
 #pragma unroll
-    for (int ww = 0; ww < 8; ++ww) {
-      mx += red[ww][0][t];
-      hx += red[ww][1][t];
-    }
-    mx *= invn;
-    hx *= invn;
-    hsq = hx * hx;
-    if (isQ)
-      a.ws.muQ[((static_cast<int64_t>(b) * a.Hq + h) * a.nqb + blkidx) * D + t] = mx;
-    else
-      a.ws.muKt[((static_cast<int64_t>(b) * a.Hkv + h) * D + t) * a.ws.nkb_pad + blkidx] = mx;
-  }
-  if (t < D) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) hsq += __shfl_xor_sync(0xffffffffu, hsq, off);
-    if (lane == 0) red_s[w] = hsq;
-  }
-  __syncthreads();
-  if (t == 0) {
-    float s = 0.f;
-#pragma unroll
-    for (int ww = 0; ww < D / 32; ++ww) s += red_s[ww];
-    if (isQ)
-      a.ws.sQ[(static_cast<int64_t>(b) * a.Hq + h) * a.nqb + blkidx] = s;
-    else
-      a.ws.sK[(static_cast<int64_t>(b) * a.Hkv + h) * a.ws.nkb_pad + blkidx] = s;
+    for (int st = 0; st < MAXSTEPS; ++st) vc[st] = vn[st];
+    bid = nbid;
   }
 }
 
@@ -160,12 +187,17 @@ cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, c
   a.nkb = (a.N + KBLK - 1) / KBLK;
   a.nq_total = static_cast<int64_t>(a.B) * a.Hq * a.nqb;
   a.ws = ws;
-  const int64_t grid = a.nq_total + static_cast<int64_t>(a.B) * a.Hkv * a.nkb;
-  if (grid == 0) return cudaSuccess;
+  const int64_t total = a.nq_total + static_cast<int64_t>(a.B) * a.Hkv * a.nkb;
+  if (total == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * (q.d == 128 ? 2 : 3);  // resident CTAs
+  const unsigned grid = static_cast<unsigned>(total < cap ? total : cap);
   if (q.d == 128)
-    pool_sim_kernel<128><<<static_cast<unsigned>(grid), 256, 0, st>>>(a);
+    pool_sim_kernel<128><<<grid, 256, 0, st>>>(a);
   else
-    pool_sim_kernel<64><<<static_cast<unsigned>(grid), 256, 0, st>>>(a);
+    pool_sim_kernel<64><<<grid, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
