@@ -33,6 +33,9 @@ namespace {
 
 constexpr int NTHREADS = 192;
 constexpr int RESCALE_LOG2 = 8;
+#ifndef EXP_POLY_EVERY
+#define EXP_POLY_EVERY 1000  // pairs c with c % EXP_POLY_EVERY == EXP_POLY_EVERY - 1 use the FMA-pipe exp2 (off: MUFU is not the limit)
+#endif
 
 struct AttnArgs {
   const uint8_t *mask;
@@ -378,7 +381,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float2 e2 = ffma2(make_float2(x[2 * c], x[2 * c + 1]), sc2, nr2);
-        const float2 p2 = make_float2(fast_exp2(e2.x), fast_exp2(e2.y));
+        // every EXP_POLY_EVERY-th pair goes to the FMA pipe so the MUFU unit is not the bottleneck
+        const float2 p2 = (c % EXP_POLY_EVERY == EXP_POLY_EVERY - 1) ? exp2_poly2(e2)
+                                                                      : make_float2(fast_exp2(e2.x), fast_exp2(e2.y));
         rs2 = fadd2(rs2, p2);
         pk[c] = pack_f16x2(p2.x, p2.y);
       }
