@@ -7,8 +7,10 @@
 // One CTA computes one 128-row query block of one head.  Warp roles (192 threads):
 //   warps 0-3  softmax + epilogue; warp w owns TMEM lanes 32w..32w+31, i.e. rows 32w.. of the
 //              block, one row per thread (the 32-row group of the lambda filter).
-//   warp 4     producer: TMA loads of the Q block once, then of only the kept K/V tiles into a
-//              STAGES-deep shared-memory ring.
+//   warp 4     producer: TMA loads of the Q block once, then of only the kept tiles: K into a
+//              KST-deep ring that is freed as soon as Q.K^T of a tile completes (so K runs well
+//              ahead), V into a VST-deep ring freed when P.V completes; the key-block index of
+//              each tile goes to the softmax warps through a small ring of its own.
 //   warp 5     MMA issuer: S_t = Q K_t^T (bf16) into one of two TMEM score buffers, O += P_t V_t
 //              (f16) with P_t read back from TMEM (written over S_t) and V_t from shared memory.
 // P and V enter the second product as f16 (V converted once from bf16 by convert_v_f16 before
@@ -84,43 +86,52 @@ struct KeptScan {
   }
 };
 
-template <int D, int STAGES>
+template <int D, int KST, int VST>
 struct Smem {
   static constexpr int QCH = D / 64;                     // 64-column chunks of a row
   static constexpr uint32_t Q_BYTES = QCH * 128 * 128;   // 128 rows x 128 B per chunk
   static constexpr uint32_t KV_CHUNK = 64 * 128;         // 64 rows x 128 B
-  static constexpr uint32_t K_BYTES = QCH * KV_CHUNK;
-  static constexpr uint32_t STAGE_BYTES = 2 * K_BYTES;   // K then V
+  static constexpr uint32_t T_BYTES = QCH * KV_CHUNK;    // one K (or V) tile
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_KV = Q_BYTES;
-  static constexpr uint32_t OFF_CTRL = OFF_KV + STAGES * STAGE_BYTES;
-  static constexpr uint32_t CTRL_BYTES = 256;
-  static constexpr uint32_t TOTAL = OFF_CTRL + CTRL_BYTES + 1024;  // + alignment slack
+  static constexpr uint32_t OFF_K = Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + KST * T_BYTES;
+  static constexpr uint32_t OFF_CTRL = OFF_V + VST * T_BYTES;
+  static constexpr uint32_t CTRL_BYTES = 512;
+  static constexpr uint32_t TOTAL = OFF_CTRL + CTRL_BYTES;
 };
+
+constexpr int JRING = 8;  // key-block indices handed from the producer to the softmax warps
 
 struct Ctrl {
   uint64_t q_full;
-  uint64_t kv_full[4];
-  uint64_t kv_empty[4];
+  uint64_t k_full[4], k_empty[4];    // K ring: filled by TMA, freed when Q.K^T of the tile completes
+  uint64_t v_full[4], v_empty[4];    // V ring: filled by TMA, freed when P.V of the tile completes
+  uint64_t j_full[JRING], j_empty[JRING];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done;
   uint64_t mma_done;
   uint64_t final_bar;
   uint32_t tmem_base;
-  int jtile[4];  // key block held by each K/V stage; -1 marks the end of the row
+  int jring[JRING];  // key block of tile t at t % JRING; -1 marks the end of the row
+  int jk[4];         // key block of the tile in each K stage (-1: end of the row)
   int abort;
   int pv_any;
   uint8_t skip[2][4];
 };
+static_assert(sizeof(Ctrl) <= 512, "control block");
 
-template <int D, int STAGES>
+template <int D, int KST, int VST>
 __global__ void __launch_bounds__(NTHREADS, 2)
     bsattn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const AttnArgs a) {
-  using L = Smem<D, STAGES>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using L = Smem<D, KST, VST>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // the 128-byte swizzle of TMA and of the MMA descriptors assumes 1024-byte aligned tiles
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) record_status(a.status, -4 /* SPARGE_ERR_CUDA */);
+    return;
+  }
   Ctrl &cs = *reinterpret_cast<Ctrl *>(smem + L::OFF_CTRL);
   volatile int *abort = &cs.abort;
 
@@ -143,9 +154,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 
   if (threadIdx.x == 0) {
     mbar_init(&cs.q_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&cs.kv_full[s], 1);
-      mbar_init(&cs.kv_empty[s], 1);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(&cs.k_full[s], 1);
+      mbar_init(&cs.k_empty[s], 1);
+    }
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(&cs.v_full[s], 1);
+      mbar_init(&cs.v_empty[s], 1);
+    }
+    for (int s = 0; s < JRING; ++s) {
+      mbar_init(&cs.j_full[s], 1);
+      mbar_init(&cs.j_empty[s], 4);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&cs.s_full[s], 1);
@@ -168,12 +187,15 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   const uint32_t tmem = cs.tmem_base;
 
   const uint32_t sQ = smem_u32(smem + L::OFF_Q);
-  const uint32_t sKV = smem_u32(smem + L::OFF_KV);
+  const uint32_t sK = smem_u32(smem + L::OFF_K);
+  const uint32_t sV = smem_u32(smem + L::OFF_V);
 
   if (warp == 4) {
     // ------------------------------------ producer ------------------------------------
-    // Loads Q with the first kept tile, then every kept K/V tile; after the last one it fills the
-    // next stage with the end mark (jtile = -1, a plain arrive without data).
+    // For tile t: the key block index into the j ring, K_t into the K ring (Q with the first
+    // tile), then V_{t-1} into the V ring, so K runs up to KST tiles ahead of Q.K^T while V
+    // follows P.V.  After the last tile the next K stage and j slot get the end mark (-1, a plain
+    // arrive without data).
     KeptScan ks;
     ks.init(mrow, n_valid);
     if (lane == 0) {
@@ -181,30 +203,43 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
     }
+    int jprev = -1;
     for (int t = 0;; ++t) {
       const int j = ks.next(lane);
-      const int st = t % STAGES;
-      if (!mbar_wait(&cs.kv_empty[st], ((t / STAGES) & 1) ^ 1, abort, a.status)) break;
+      const int kst = t % KST, js = t % JRING;
+      if (!mbar_wait(&cs.k_empty[kst], ((t / KST) & 1) ^ 1, abort, a.status)) break;
+      if (!mbar_wait(&cs.j_empty[js], ((t / JRING) & 1) ^ 1, abort, a.status)) break;
       if (lane == 0) {
-        cs.jtile[st] = j;
+        cs.jring[js] = j;
+        mbar_arrive(&cs.j_full[js]);
+        cs.jk[kst] = j;
         if (j >= 0) {
           if (t == 0) {
             mbar_arrive_expect_tx(&cs.q_full, L::Q_BYTES);
             for (int c = 0; c < L::QCH; ++c)
               tma_load_4d(smem + L::OFF_Q + c * 16384, &tq, &cs.q_full, 64 * c, QBLK * i, h, b);
           }
-          uint8_t *kdst = smem + L::OFF_KV + st * L::STAGE_BYTES;
-          uint8_t *vdst = kdst + L::K_BYTES;
-          mbar_arrive_expect_tx(&cs.kv_full[st], L::STAGE_BYTES);
-          for (int c = 0; c < L::QCH; ++c) {
-            tma_load_4d(kdst + c * L::KV_CHUNK, &tk, &cs.kv_full[st], 64 * c, KBLK * j, kvh, b);
-            tma_load_4d(vdst + c * L::KV_CHUNK, &tv, &cs.kv_full[st], 64 * c, KBLK * j, kvh, b);
-          }
+          uint8_t *kdst = smem + L::OFF_K + kst * L::T_BYTES;
+          mbar_arrive_expect_tx(&cs.k_full[kst], L::T_BYTES);
+          for (int c = 0; c < L::QCH; ++c)
+            tma_load_4d(kdst + c * L::KV_CHUNK, &tk, &cs.k_full[kst], 64 * c, KBLK * j, kvh, b);
         } else {
-          mbar_arrive(&cs.kv_full[st]);
+          mbar_arrive(&cs.k_full[kst]);
         }
       }
       __syncwarp();
+      if (jprev >= 0) {
+        const int u = t - 1, vst = u % VST;
+        if (!mbar_wait(&cs.v_empty[vst], ((u / VST) & 1) ^ 1, abort, a.status)) break;
+        if (lane == 0) {
+          uint8_t *vdst = smem + L::OFF_V + vst * L::T_BYTES;
+          mbar_arrive_expect_tx(&cs.v_full[vst], L::T_BYTES);
+          for (int c = 0; c < L::QCH; ++c)
+            tma_load_4d(vdst + c * L::KV_CHUNK, &tv, &cs.v_full[vst], 64 * c, KBLK * jprev, kvh, b);
+        }
+        __syncwarp();
+      }
+      jprev = j;
       if (j < 0) break;
     }
     if (*abort) {  // let copies already in flight land before the CTA exits
@@ -215,16 +250,16 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   } else if (warp == 5) {
     // ------------------------------------ MMA issuer ------------------------------------
     int pv_count = 0, T = 0;
-    // next_tile(u): waits for stage u % STAGES and returns its key block (-1 = end of row)
+    // next_tile(u): waits for K stage u % KST and returns its key block (-1 = end of row)
     auto next_tile = [&](int u) -> int {
-      const int st = u % STAGES;
-      if (!mbar_wait(&cs.kv_full[st], (u / STAGES) & 1, abort, a.status)) return -2;
+      const int st = u % KST;
+      if (!mbar_wait(&cs.k_full[st], (u / KST) & 1, abort, a.status)) return -2;
       tc_fence_after();
-      return cs.jtile[st];
+      return cs.jk[st];
     };
     auto issue_s = [&](int u) {
       if (lane == 0) {
-        const uint32_t kaddr = sKV + (u % STAGES) * L::STAGE_BYTES;
+        const uint32_t kaddr = sK + (u % KST) * L::T_BYTES;
         const uint32_t dS = tmem + SCOL0 + (u & 1) * 64;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
@@ -233,6 +268,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           mma_bf16_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
         }
         mma_commit(&cs.s_full[u & 1]);
+        mma_commit(&cs.k_empty[u % KST]);  // the K stage is free once this product completes
       }
       __syncwarp();
     };
@@ -245,12 +281,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         jn = next_tile(t + 1);
         if (jn >= 0) issue_s(t + 1);
         if (jn == -2 || !mbar_wait(&cs.p_full[t & 1], (t >> 1) & 1, abort, a.status)) break;
+        const int vst = t % VST;
+        if (!mbar_wait(&cs.v_full[vst], (t / VST) & 1, abort, a.status)) break;
         tc_fence_after();
         const bool all_skip = cs.skip[t & 1][0] && cs.skip[t & 1][1] && cs.skip[t & 1][2] && cs.skip[t & 1][3];
-        const int st = t % STAGES;
         if (lane == 0) {
           if (!all_skip) {
-            const uint32_t vaddr = sKV + st * L::STAGE_BYTES + L::K_BYTES;
+            const uint32_t vaddr = sV + vst * L::T_BYTES;
             const uint32_t aP = tmem + SCOL0 + (t & 1) * 64;
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
@@ -260,7 +297,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             pv_issued = 1;
             ++pv_count;
           }
-          mma_commit(&cs.kv_empty[st]);
+          mma_commit(&cs.v_empty[vst]);
           mma_commit(&cs.o_done);
         }
         __syncwarp();
@@ -294,12 +331,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     int nskip = 0, T = 0;
     bool ok = true;
     for (int t = 0;; ++t) {
-      const int st = t % STAGES;
-      if (!mbar_wait(&cs.kv_full[st], (t / STAGES) & 1, abort, a.status)) {
+      const int js = t % JRING;
+      if (!mbar_wait(&cs.j_full[js], (t / JRING) & 1, abort, a.status)) {
         ok = false;
         break;
       }
-      const int j = cs.jtile[st];
+      const int j = cs.jring[js];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cs.j_empty[js]);
       if (j < 0) break;
       T = t + 1;
       const int buf = t & 1;
@@ -451,18 +490,18 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int D, int STAGES>
+template <int D, int KST, int VST>
 cudaError_t launch_t(const AttnLaunch &l, const AttnArgs &a, cudaStream_t st) {
-  const uint32_t smem = Smem<D, STAGES>::TOTAL;
+  const uint32_t smem = Smem<D, KST, VST>::TOTAL;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bsattn_kernel<D, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(bsattn_kernel<D, KST, VST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int64_t grid = static_cast<int64_t>(a.B) * a.Hq * a.nqb;
-  bsattn_kernel<D, STAGES><<<static_cast<unsigned>(grid), NTHREADS, smem, st>>>(l.tq, l.tk, l.tv, a);
+  bsattn_kernel<D, KST, VST><<<static_cast<unsigned>(grid), NTHREADS, smem, st>>>(l.tq, l.tk, l.tv, a);
   return cudaGetLastError();
 }
 
@@ -483,7 +522,7 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
   a.stats = l.stats;
   a.status = l.status;
   if (static_cast<int64_t>(a.B) * a.Hq * a.nqb == 0) return cudaSuccess;
-  return l.d == 128 ? launch_t<128, 2>(l, a, st) : launch_t<64, 4>(l, a, st);
+  return l.d == 128 ? launch_t<128, 3, 2>(l, a, st) : launch_t<64, 4, 3>(l, a, st);
 }
 
 }  // namespace sparge
