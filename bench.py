@@ -274,7 +274,7 @@ def run_ours(args, rank, world, local_rank):
                  "lambda_skip_fraction": round(skipped / max(4 * kept, 1), 4)},
         "mask_pred": {"ms": round(t_pred_avg * 1e3, 4), "gbs": round(pred_gbs, 1),
                       "pct_hbm": round(100 * pred_gbs / hbm, 2), "bytes": pred_bytes},
-        "roofline": {"bound": "tensor", "kernel": "bsattn_kernel<128,2>", "achieved": round(attn_tflops, 2),
+        "roofline": {"bound": "tensor", "kernel": "bsattn_kernel<128,3,2>", "achieved": round(attn_tflops, 2),
                      "peak": peak_tc, "unit": "TFLOP/s", "frac": round(attn_tflops / peak_tc, 4),
                      "peak_source": "bf16_tflops_sustained " + tag, "traffic": None},
         "e2e": {"value": round(world * dense / e2e_t / 1e12, 2), "unit": "dense-equiv TOPS",
