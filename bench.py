@@ -4,8 +4,8 @@ pooled scores + softmax + cumulative top-k) followed by block-sparse attention w
 filter, on the Llama-3.1-8B-like causal prefill at 128K tokens (B=1, 32 query heads, 8 KV heads,
 d=128, topk 0.5, theta 0.5, lambda -8; synthetic bf16 inputs).
 
-One step = one sparge_attn_ex call (four kernel launches: pooling, score/select, V to f16,
-attention) over inputs resident in HBM; CUDA events recorded by the library around each kernel
+One step = one sparge_attn_ex call (five kernel launches: pooling, pooled-score GEMM, selection,
+V to f16, attention) over inputs resident in HBM; CUDA events recorded by the library around each kernel
 give the per-kernel times.
 Prints one JSON line.  ``--impl reference`` times the float64 CPU oracle instead, on a bounded
 sample of the same workload.  Under torchrun every rank runs its own full replica (weak scaling,
@@ -173,7 +173,7 @@ def run_ours(args, rank, world, local_rank):
     kept, pv, skipped, valid = (int(x) for x in stats.cpu().tolist())
     assert fbs.device_status() == 0
 
-    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
 
     def step(events=None):
         fbs.sparge_attn_ex(q, k, v, w.topk, w.causal, theta=w.theta, lam=w.lam, mask_out=mask, out=o, ws=ws,
@@ -195,13 +195,15 @@ def run_ours(args, rank, world, local_rank):
         step(ev_sets[s])
     torch.cuda.synchronize()
     clk = clocks.stop()
-    # per step: [0] before pooling, [1] after pooling, [2] after score/select, [3] after V copy, [4] after attention
+    # per step: [0] before pooling, [1] after pooling, [2] after the score GEMM, [3] after selection,
+    # [4] after the V copy, [5] after attention
     t_pool = [e[0].elapsed_time(e[1]) / 1e3 for e in ev_sets]
-    t_sel = [e[1].elapsed_time(e[2]) / 1e3 for e in ev_sets]
-    t_conv = [e[2].elapsed_time(e[3]) / 1e3 for e in ev_sets]
-    t_attn = [e[3].elapsed_time(e[4]) / 1e3 for e in ev_sets]
-    t_pred = [a + b for a, b in zip(t_pool, t_sel)]
-    total = ev_sets[0][0].elapsed_time(ev_sets[-1][4]) / 1e3
+    t_gemm = [e[1].elapsed_time(e[2]) / 1e3 for e in ev_sets]
+    t_sel = [e[2].elapsed_time(e[3]) / 1e3 for e in ev_sets]
+    t_conv = [e[3].elapsed_time(e[4]) / 1e3 for e in ev_sets]
+    t_attn = [e[4].elapsed_time(e[5]) / 1e3 for e in ev_sets]
+    t_pred = [a + b + c for a, b, c in zip(t_pool, t_gemm, t_sel)]
+    total = ev_sets[0][0].elapsed_time(ev_sets[-1][5]) / 1e3
     if dist:
         tt = torch.tensor([total], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -265,7 +267,8 @@ def run_ours(args, rank, world, local_rank):
                    "causal": w.causal, "topk": w.topk, "theta": w.theta, "lambda": w.lam,
                    "l2": "inputs larger than L2 (Q+K+V %.2f GB), no flush" % ((w.q.nbytes + w.k.nbytes + w.v.nbytes) / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "kernels_ms": {"pool_sim": round(avg(t_pool) * 1e3, 4), "score_select": round(avg(t_sel) * 1e3, 4),
+        "kernels_ms": {"pool_sim": round(avg(t_pool) * 1e3, 4), "score_gemm": round(avg(t_gemm) * 1e3, 4),
+                       "score_select": round(avg(t_sel) * 1e3, 4),
                        "convert_v_f16": round(avg(t_conv) * 1e3, 4), "bsattn": round(t_attn_avg * 1e3, 4)},
         "attn": {"ms": round(t_attn_avg * 1e3, 4), "dense_equiv_tops": round(dense / t_attn_avg / 1e12, 2),
                  "executed_tflops": round(attn_tflops, 2), "pct_tensor_peak": round(100 * attn_tflops / peak_tc, 2),
@@ -280,7 +283,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(world * dense / e2e_t / 1e12, 2), "unit": "dense-equiv TOPS",
                 "h2d_bytes_per_step": int(w.q.nbytes + w.k.nbytes + w.v.nbytes),
                 "d2h_bytes_per_step": int(o.numel() * 2)},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 5 * args.steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -149,23 +149,30 @@ def predict_mask(q, k, topk: float, theta: float = 0.5, causal: bool = False, ws
 
 def predict_ws_views(ws, B, Hq, Hkv, N, d):
     """Views of the stage-1 workspace after predict_mask: muQ (B,Hq,nqb,d), sQ (B,Hq,nqb),
-    muK (B,Hkv,nkb,d) and sK (B,Hkv,nkb), following the layout the library writes (fp32,
-    regions 256-byte aligned, pooled keys stored d-major with the key-block axis padded to 4)."""
+    muK (B,Hkv,nkb,d), sK (B,Hkv,nkb) and the scaled pooled scores S (B,Hq,nqb,nkb), following
+    the layout the library writes (regions 256-byte aligned; fp32 except the bf16 hi/lo copies of
+    the means, which are skipped here)."""
     torch = _torch()
     nqb, nkb = n_blocks(N)
     nkb_pad = -(-nkb // 4) * 4
-    f = ws.view(torch.float32) if ws.dtype == torch.uint8 else ws
+    u8 = ws if ws.dtype == torch.uint8 else ws.view(torch.uint8)
 
-    def take(off, n):
-        return f[off // 4: off // 4 + n], off + ((4 * n + 255) // 256) * 256
+    def take(off, nbytes):
+        return u8[off:off + nbytes], off + ((nbytes + 255) // 256) * 256
 
     off = 0
-    muQ, off = take(off, B * Hq * nqb * d)
-    sQ, off = take(off, B * Hq * nqb)
-    muKt, off = take(off, B * Hkv * d * nkb_pad)
-    sK, off = take(off, B * Hkv * nkb_pad)
-    return (muQ.view(B, Hq, nqb, d), sQ.view(B, Hq, nqb),
-            muKt.view(B, Hkv, d, nkb_pad)[..., :nkb].transpose(2, 3), sK.view(B, Hkv, nkb_pad)[..., :nkb])
+    muQ, off = take(off, 4 * B * Hq * nqb * d)
+    sQ, off = take(off, 4 * B * Hq * nqb)
+    muK, off = take(off, 4 * B * Hkv * nkb * d)
+    sK, off = take(off, 4 * B * Hkv * nkb_pad)
+    _, off = take(off, 2 * B * Hq * nqb * d)
+    _, off = take(off, 2 * B * Hq * nqb * d)
+    _, off = take(off, 2 * B * Hkv * nkb * d)
+    _, off = take(off, 2 * B * Hkv * nkb * d)
+    S, off = take(off, 4 * B * Hq * nqb * nkb_pad)
+    f = lambda t: t.view(torch.float32)
+    return (f(muQ).view(B, Hq, nqb, d), f(sQ).view(B, Hq, nqb), f(muK).view(B, Hkv, nkb, d),
+            f(sK).view(B, Hkv, nkb_pad)[..., :nkb], f(S).view(B, Hq, nqb, nkb_pad)[..., :nkb])
 
 
 def block_sparse_attn(q, k, v, mask=None, lam: float = -math.inf, causal: bool = False, out=None, stats=None,
@@ -200,18 +207,18 @@ def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: 
                    scale: float = 0.0, precision: int = SPARGE_PRECISION_BF16, stats=None, mask_out=None,
                    out=None, ws=None, events=None):
     """sparge_attn with explicit theta, lambda, scale, counters, an optional mask output and
-    optional timing events (5 torch.cuda.Event, recorded around the four kernels)."""
+    optional timing events (6 torch.cuda.Event, recorded around the five kernels)."""
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
     ws = _workspace(SPARGE_OP_ATTN, q, k, ws)
     evp = None
     if events is not None:
-        assert len(events) == 5
+        assert len(events) == 6
         for ev in events:
             if not ev.cuda_event:
                 ev.record()   # torch creates the event on its first record
-        evp = (ctypes.c_void_p * 5)(*[ev.cuda_event for ev in events])
+        evp = (ctypes.c_void_p * 6)(*[ev.cuda_event for ev in events])
     p = sparge_params(float(theta), float(lam), float(scale), int(precision),
                       0 if stats is None else stats.data_ptr(),
                       ctypes.cast(evp, ctypes.c_void_p) if evp is not None else None)

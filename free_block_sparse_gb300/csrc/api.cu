@@ -105,6 +105,20 @@ int make_map(CUtensorMap *m, const View &v, int box_rows, const char *name,
   return SPARGE_OK;
 }
 
+// 3-D map over a contiguous bf16 array [planes][rows][d], box 64 columns x 128 rows, 128-byte swizzle.
+int make_map3(CUtensorMap *m, void *base, int64_t d, int64_t rows, int64_t planes, const char *name) {
+  encode_fn_t enc = get_encode();
+  if (!enc) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)(rows * d * 2)};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+  return SPARGE_OK;
+}
+
 int check_topk_theta(float topk, float theta) {
   if (!(topk > 0.f && topk <= 1.f)) return fail(SPARGE_ERR_INVALID_ARG, "topk=%g not in (0, 1]", (double)topk);
   if (!std::isfinite(theta)) return fail(SPARGE_ERR_INVALID_ARG, "theta must be finite");
@@ -116,7 +130,7 @@ int check_lambda(float lambda) {
   return SPARGE_OK;
 }
 
-// Records timing event `idx` of `ev` (an array of 5 cudaEvent_t, or nullptr) on stream s.
+// Records timing event `idx` of `ev` (an array of 6 cudaEvent_t, or nullptr) on stream s.
 int record_event(void *const *ev, int idx, cudaStream_t s) {
   if (!ev || !ev[idx]) return SPARGE_OK;
   cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(ev[idx]), s);
@@ -137,9 +151,25 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
   cudaError_t e = launch_pool_sim(q, k, pw, s);
   if (e != cudaSuccess) return cuda_fail(e, "pool_sim launch");
   if ((rc = record_event(ev, 1, s))) return rc;
-  e = launch_score_select(pw, (int)q.B, (int)q.H, (int)k.H, (int)q.N, (int)q.d, topk, theta, causal, scale, mask, s);
+  {
+    ScoreGemmLaunch g;
+    memset(&g, 0, sizeof(g));
+    const int64_t nqb = cdiv(q.N, QBLK), nkb = cdiv(q.N, KBLK);
+    if ((rc = make_map3(&g.qhi, pw.qhi, q.d, nqb, q.B * q.H, "qhi")) || (rc = make_map3(&g.qlo, pw.qlo, q.d, nqb, q.B * q.H, "qlo")) ||
+        (rc = make_map3(&g.khi, pw.khi, q.d, nkb, q.B * k.H, "khi")) || (rc = make_map3(&g.klo, pw.klo, q.d, nkb, q.B * k.H, "klo")))
+      return rc;
+    g.S = pw.S;
+    g.nkb_pad = pw.nkb_pad;
+    g.B = (int)q.B; g.Hq = (int)q.H; g.Hkv = (int)k.H; g.N = (int)q.N; g.d = (int)q.d; g.causal = causal;
+    g.scale = scale;
+    g.status = status_ptr();
+    e = launch_score_gemm(g, s);
+    if (e != cudaSuccess) return cuda_fail(e, "score_gemm launch");
+    if ((rc = record_event(ev, 2, s))) return rc;
+  }
+  e = launch_score_select(pw, (int)q.B, (int)q.H, (int)k.H, (int)q.N, (int)q.d, topk, theta, causal, mask, s);
   if (e != cudaSuccess) return cuda_fail(e, "score_select launch");
-  return record_event(ev, 2, s);
+  return record_event(ev, 3, s);
 }
 
 size_t v16_bytes(int64_t B, int64_t Hkv, int64_t N, int64_t d) { return align256((size_t)B * Hkv * N * d * 2); }
@@ -161,7 +191,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   if (q.B == 0 || q.N == 0) return SPARGE_OK;
   cudaError_t e = launch_convert_v_f16(v, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "convert_v launch");
-  if ((rc = record_event(ev, 3, s))) return rc;
+  if ((rc = record_event(ev, 4, s))) return rc;
   View v16{ws, v.B, v.H, v.N, v.d, v.H * v.N * v.d, v.N * v.d, v.d};
   AttnLaunch l;
   memset(&l, 0, sizeof(l));
@@ -179,7 +209,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   l.status = status_ptr();
   e = launch_bsattn(l, s);
   if (e != cudaSuccess) return cuda_fail(e, "bsattn launch");
-  return record_event(ev, 4, s);
+  return record_event(ev, 5, s);
 }
 
 }  // namespace
@@ -204,10 +234,13 @@ int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
 size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
   const int64_t nqb = cdiv(N, QBLK), nkb = cdiv(N, KBLK), nkb_pad = cdiv(nkb, 4) * 4;
   size_t s = 0;
-  s += align256(sizeof(float) * B * Hq * nqb * d);
-  s += align256(sizeof(float) * B * Hq * nqb);
-  s += align256(sizeof(float) * B * Hkv * d * nkb_pad);
-  s += align256(sizeof(float) * B * Hkv * nkb_pad);
+  s += align256(sizeof(float) * B * Hq * nqb * d);      // muQ
+  s += align256(sizeof(float) * B * Hq * nqb);          // sQ
+  s += align256(sizeof(float) * B * Hkv * nkb * d);     // muK
+  s += align256(sizeof(float) * B * Hkv * nkb_pad);     // sK
+  s += 2 * align256(2 * B * Hq * nqb * d);              // qhi, qlo
+  s += 2 * align256(2 * B * Hkv * nkb * d);             // khi, klo
+  s += align256(sizeof(float) * B * Hq * nqb * nkb_pad);  // S
   return s;
 }
 
@@ -215,13 +248,20 @@ PredictWs predict_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t
   const int64_t nqb = cdiv(N, QBLK), nkb = cdiv(N, KBLK), nkb_pad = cdiv(nkb, 4) * 4;
   char *p = static_cast<char *>(ws);
   PredictWs w;
-  w.muQ = reinterpret_cast<float *>(p);
-  p += align256(sizeof(float) * B * Hq * nqb * d);
-  w.sQ = reinterpret_cast<float *>(p);
-  p += align256(sizeof(float) * B * Hq * nqb);
-  w.muKt = reinterpret_cast<float *>(p);
-  p += align256(sizeof(float) * B * Hkv * d * nkb_pad);
-  w.sK = reinterpret_cast<float *>(p);
+  auto take = [&](size_t bytes) {
+    char *r = p;
+    p += align256(bytes);
+    return r;
+  };
+  w.muQ = reinterpret_cast<float *>(take(sizeof(float) * B * Hq * nqb * d));
+  w.sQ = reinterpret_cast<float *>(take(sizeof(float) * B * Hq * nqb));
+  w.muK = reinterpret_cast<float *>(take(sizeof(float) * B * Hkv * nkb * d));
+  w.sK = reinterpret_cast<float *>(take(sizeof(float) * B * Hkv * nkb_pad));
+  w.qhi = reinterpret_cast<uint16_t *>(take(2 * B * Hq * nqb * d));
+  w.qlo = reinterpret_cast<uint16_t *>(take(2 * B * Hq * nqb * d));
+  w.khi = reinterpret_cast<uint16_t *>(take(2 * B * Hkv * nkb * d));
+  w.klo = reinterpret_cast<uint16_t *>(take(2 * B * Hkv * nkb * d));
+  w.S = reinterpret_cast<float *>(take(sizeof(float) * B * Hq * nqb * nkb_pad));
   w.nkb_pad = nkb_pad;
   return w;
 }

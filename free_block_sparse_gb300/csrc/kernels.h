@@ -13,13 +13,17 @@ struct View {  // a validated bf16 (B, H, N, d) tensor, strides in elements
   int64_t sb, sh, sn;
 };
 
-// Stage-1 workspace (fp32).  Pooled key means are stored d-major, muKt[b][kvh][k][nkb_pad],
-// so the score kernel reads rows of key blocks with contiguous vector loads.
+// Stage-1 workspace.  fp32 block means and similarities, the means again as bf16 hi/lo pairs
+// (mu ~= hi + lo, about 16 significant bits) for the tensor-core score product, and the scaled
+// pooled scores S, one fp32 row of nkb_pad entries per query block.
 struct PredictWs {
-  float *muQ;   // [B][Hq][nqb][d]
-  float *sQ;    // [B][Hq][nqb]
-  float *muKt;  // [B][Hkv][d][nkb_pad]
-  float *sK;    // [B][Hkv][nkb_pad]
+  float *muQ;       // [B][Hq][nqb][d]
+  float *sQ;        // [B][Hq][nqb]
+  float *muK;       // [B][Hkv][nkb][d]
+  float *sK;        // [B][Hkv][nkb_pad]
+  uint16_t *qhi, *qlo;  // bf16 [B][Hq][nqb][d]
+  uint16_t *khi, *klo;  // bf16 [B][Hkv][nkb][d]
+  float *S;         // [B][Hq][nqb][nkb_pad]
   int64_t nkb_pad;
 };
 
@@ -38,8 +42,22 @@ int report_error(int code, const char *msg);
 
 cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, cudaStream_t st);
 
+// Pooled scores S = scale * muQ . muK^T on tcgen05 (bf16 hi/lo split, three products), for the
+// valid (causal) key blocks of every query block.  The four maps cover qhi, qlo (3-D: d, nqb,
+// B*Hq; box 64 x 128) and khi, klo (d, nkb, B*Hkv; box 64 x 128).
+struct ScoreGemmLaunch {
+  CUtensorMap qhi, qlo, khi, klo;
+  float *S;
+  int64_t nkb_pad;
+  int B, Hq, Hkv, N, d, causal;
+  float scale;
+  int *status;
+};
+cudaError_t launch_score_gemm(const ScoreGemmLaunch &l, cudaStream_t st);
+
+// Row softmax, cumulative top-k and the always-keep rule on S: writes the uint8 mask.
 cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int N, int d, float topk,
-                                float theta, int causal, float scale, uint8_t *mask, cudaStream_t st);
+                                float theta, int causal, uint8_t *mask, cudaStream_t st);
 
 struct AttnLaunch {
   CUtensorMap tq, tk, tv;  // 4-D maps (d, N, H, B), 128-byte swizzle, boxes 64 x 128 (Q) / 64 x 64 (K, V);

@@ -25,8 +25,8 @@ struct BlockRef {
   int64_t sn;                  // token stride (elements)
   int n;                       // valid tokens
   int steps;                   // CTA load steps covering the block
-  float *mu;                   // where the mean goes (stride mu_stride between dims)
-  int64_t mu_stride;
+  float *mu;                   // where the mean goes (d contiguous floats)
+  uint16_t *hi, *lo;           // where its bf16 hi/lo split goes
   float *s;                    // where the similarity goes
 };
 
@@ -41,9 +41,11 @@ __device__ __forceinline__ BlockRef block_ref(const PoolArgs &a, int64_t bid, in
     r.sn = a.q_sn;
     r.n = min(QBLK, a.N - i * QBLK);
     r.steps = QBLK / TPS;
-    r.mu = a.ws.muQ + ((static_cast<int64_t>(b) * a.Hq + h) * a.nqb + i) * D;
-    r.mu_stride = 1;
-    r.s = a.ws.sQ + (static_cast<int64_t>(b) * a.Hq + h) * a.nqb + i;
+    const int64_t row = (static_cast<int64_t>(b) * a.Hq + h) * a.nqb + i;
+    r.mu = a.ws.muQ + row * D;
+    r.hi = a.ws.qhi + row * D;
+    r.lo = a.ws.qlo + row * D;
+    r.s = a.ws.sQ + row;
   } else {
     bid -= a.nq_total;
     const int j = static_cast<int>(bid % a.nkb);
@@ -53,8 +55,10 @@ __device__ __forceinline__ BlockRef block_ref(const PoolArgs &a, int64_t bid, in
     r.sn = a.k_sn;
     r.n = min(KBLK, a.N - j * KBLK);
     r.steps = KBLK / TPS;
-    r.mu = a.ws.muKt + (static_cast<int64_t>(b) * a.Hkv + h) * D * a.ws.nkb_pad + j;
-    r.mu_stride = a.ws.nkb_pad;
+    const int64_t row = (static_cast<int64_t>(b) * a.Hkv + h) * a.nkb + j;
+    r.mu = a.ws.muK + row * D;
+    r.hi = a.ws.khi + row * D;
+    r.lo = a.ws.klo + row * D;
     r.s = a.ws.sK + (static_cast<int64_t>(b) * a.Hkv + h) * a.ws.nkb_pad + j;
   }
   return r;
@@ -71,6 +75,7 @@ __global__ void __launch_bounds__(256, (D == 128 ? 2 : 3)) pool_sim_kernel(PoolA
   constexpr int MAXSTEPS = QBLK / TPS;
 
   __shared__ float red[2][8][2][D];  // double-buffered per-warp partial sums (x and unit x)
+  __shared__ float red_s[2][8];      // per-warp partial sums of squares of the mean unit vector
 
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / LPT, part = lane % LPT;
@@ -90,7 +95,9 @@ __global__ void __launch_bounds__(256, (D == 128 ? 2 : 3)) pool_sim_kernel(PoolA
   BlockRef cur = block_ref<TPS>(a, bid, D);
   uint4 vc[MAXSTEPS], vn[MAXSTEPS];
   load(cur, vc);
-  for (int it = 0; bid < total; ++it) {
+  float *prev_s = nullptr;
+  int it = 0;
+  for (; bid < total; ++it) {
     const int64_t nbid = bid + gridDim.x;
     BlockRef nxt = cur;
     if (nbid < total) {
@@ -144,14 +151,21 @@ __global__ void __launch_bounds__(256, (D == 128 ? 2 : 3)) pool_sim_kernel(PoolA
       }
     }
     __syncthreads();
-    if (w == 0) {
-      // warp 0 finishes the block while the other warps go on with the next one; the partial
-      // sums alternate between two buffers, so the next barrier orders the reuse.
+    // the similarity of the previous block: its eight per-warp partial sums of squares
+    if (threadIdx.x == 0 && prev_s) {
+      float sprev = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < 8; ++ww) sprev += red_s[(it - 1) & 1][ww];
+      *prev_s = sprev;
+    }
+    // every warp finishes D/8 dimensions of this block (the partial sums alternate between two
+    // buffers, so the next barrier orders their reuse)
+    {
+      constexpr int DPW = D / 8;
       const float invn = 1.f / static_cast<float>(cur.n);
       float hsq = 0.f;
-#pragma unroll
-      for (int dd = 0; dd < D / 32; ++dd) {
-        const int dim = lane + 32 * dd;
+      if (lane < DPW) {
+        const int dim = w * DPW + lane;
         float mx = 0.f, hx = 0.f;
 #pragma unroll
         for (int ww = 0; ww < 8; ++ww) {
@@ -159,17 +173,29 @@ __global__ void __launch_bounds__(256, (D == 128 ? 2 : 3)) pool_sim_kernel(PoolA
           hx += rb[ww][1][dim];
         }
         hx *= invn;
-        hsq = fmaf(hx, hx, hsq);
-        cur.mu[dim * cur.mu_stride] = mx * invn;
+        hsq = hx * hx;
+        const float mean = mx * invn;
+        cur.mu[dim] = mean;
+        const __nv_bfloat16 hb = __float2bfloat16_rn(mean);
+        cur.hi[dim] = __bfloat16_as_ushort(hb);
+        cur.lo[dim] = __bfloat16_as_ushort(__float2bfloat16_rn(mean - __bfloat162float(hb)));
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) hsq += __shfl_xor_sync(0xffffffffu, hsq, off);
-      if (lane == 0) *cur.s = hsq;
+      for (int off = DPW / 2; off > 0; off >>= 1) hsq += __shfl_xor_sync(0xffffffffu, hsq, off);
+      if (lane == 0) red_s[it & 1][w] = hsq;
     }
+    prev_s = cur.s;
     cur = nxt;
 #pragma unroll
     for (int st = 0; st < MAXSTEPS; ++st) vc[st] = vn[st];
     bid = nbid;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && prev_s) {
+    float sprev = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < 8; ++ww) sprev += red_s[(it - 1) & 1][ww];
+    *prev_s = sprev;
   }
 }
 

@@ -1,0 +1,215 @@
+// Stage 1b, part 1: the pooled score map S = scale * muQ . muK^T (SpargeAttention abstract: the
+// attention map is predicted from a compressed Q and K).  A batched GEMM per head on tcgen05:
+// M = 128 query blocks, N = 128 key blocks per chunk, K = d.  The fp32 means are carried as bf16
+// hi/lo pairs and multiplied as hi.hi + hi.lo + lo.hi with fp32 accumulation, which keeps about
+// 16 significant bits (relative error ~1e-5, far inside the 1e-3 decision margins of the mask).
+// Only chunks holding valid (causal) key blocks are computed.  One CTA per (128 query blocks,
+// head); warp 4 loads operands by TMA (Q once, K chunks into a 2-stage ring), warp 5 issues the
+// MMAs into two TMEM accumulators, warps 0-3 move each finished accumulator row to S.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sparge {
+namespace {
+
+constexpr int GROWS = 128;  // query blocks per CTA (MMA M)
+constexpr int GCOLS = 128;  // key blocks per chunk (MMA N)
+
+struct GemmArgs {
+  float *S;
+  int64_t nkb_pad;
+  int B, Hq, Hkv, G, nqb, nkb, causal, ngroups;
+  float scale;
+  int *status;
+};
+
+template <int D>
+struct GL {
+  static constexpr int KCH = D / 64;                     // 64-wide k chunks (128-byte rows)
+  static constexpr uint32_t OP_BYTES = KCH * 128 * 128;  // one 128-row bf16 operand
+  static constexpr uint32_t OFF_QHI = 0;
+  static constexpr uint32_t OFF_QLO = OP_BYTES;
+  static constexpr uint32_t OFF_K = 2 * OP_BYTES;        // stage s: hi at OFF_K + 2 s OP_BYTES, lo after it
+  static constexpr int KST = 2;
+  static constexpr uint32_t OFF_CTRL = OFF_K + KST * 2 * OP_BYTES;
+  static constexpr uint32_t TOTAL = OFF_CTRL + 256;
+};
+
+struct GCtrl {
+  uint64_t q_full;
+  uint64_t k_full[2], k_empty[2];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t final_bar;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    score_gemm_kernel(const __grid_constant__ CUtensorMap tqh, const __grid_constant__ CUtensorMap tql,
+                      const __grid_constant__ CUtensorMap tkh, const __grid_constant__ CUtensorMap tkl,
+                      const GemmArgs a) {
+  using L = GL<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) record_status(a.status, -4 /* SPARGE_ERR_CUDA */);
+    return;
+  }
+  GCtrl &cs = *reinterpret_cast<GCtrl *>(smem + L::OFF_CTRL);
+  volatile int *abort = &cs.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int group = a.ngroups - 1 - static_cast<int>(blockIdx.y);  // longest causal rows first
+  const int bh = blockIdx.x, b = bh / a.Hq, h = bh % a.Hq, kvh = h / a.G;
+  const int i0 = group * GROWS;
+  const int ilast = min(i0 + GROWS - 1, a.nqb - 1);
+  const int ncols = a.causal ? min(a.nkb, 2 * ilast + 2) : a.nkb;
+  const int nch = (ncols + GCOLS - 1) / GCOLS;
+  constexpr uint32_t IDESC = idesc_f32acc(128, GCOLS, FMT_BF16, false);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&cs.q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&cs.k_full[s], 1);
+      mbar_init(&cs.k_empty[s], 1);
+      mbar_init(&cs.acc_full[s], 1);
+      mbar_init(&cs.acc_empty[s], 128);
+    }
+    mbar_init(&cs.final_bar, 1);
+    cs.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&cs.tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = cs.tmem_base;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&cs.q_full, 2 * L::OP_BYTES);
+      for (int c = 0; c < L::KCH; ++c) {
+        tma_load_3d(smem + L::OFF_QHI + c * 16384, &tqh, &cs.q_full, 64 * c, i0, bh);
+        tma_load_3d(smem + L::OFF_QLO + c * 16384, &tql, &cs.q_full, 64 * c, i0, bh);
+      }
+      for (int ch = 0; ch < nch; ++ch) {
+        const int st = ch % L::KST;
+        if (!mbar_wait(&cs.k_empty[st], ((ch / L::KST) & 1) ^ 1, abort, a.status)) break;
+        uint8_t *kh = smem + L::OFF_K + st * 2 * L::OP_BYTES;
+        uint8_t *kl = kh + L::OP_BYTES;
+        mbar_arrive_expect_tx(&cs.k_full[st], 2 * L::OP_BYTES);
+        for (int c = 0; c < L::KCH; ++c) {
+          tma_load_3d(kh + c * 16384, &tkh, &cs.k_full[st], 64 * c, GCOLS * ch, b * a.Hkv + kvh);
+          tma_load_3d(kl + c * 16384, &tkl, &cs.k_full[st], 64 * c, GCOLS * ch, b * a.Hkv + kvh);
+        }
+      }
+      if (*abort) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0 && nch > 0 && mbar_wait(&cs.q_full, 0, abort, a.status)) {
+      tc_fence_after();
+      const uint32_t qh = smem_u32(smem + L::OFF_QHI), ql = smem_u32(smem + L::OFF_QLO);
+      for (int ch = 0; ch < nch; ++ch) {
+        const int st = ch % L::KST, ab = ch & 1;
+        if (!mbar_wait(&cs.k_full[st], (ch / L::KST) & 1, abort, a.status)) break;
+        if (!mbar_wait(&cs.acc_empty[ab], ((ch >> 1) & 1) ^ 1, abort, a.status)) break;
+        tc_fence_after();
+        const uint32_t kh = smem_u32(smem + L::OFF_K + st * 2 * L::OP_BYTES), kl = kh + L::OP_BYTES;
+        const uint32_t acc = tmem + ab * GCOLS;
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+          const uint64_t dqh = smem_desc_sw128(qh + off, 16, 1024), dql = smem_desc_sw128(ql + off, 16, 1024);
+          const uint64_t dkh = smem_desc_sw128(kh + off, 16, 1024), dkl = smem_desc_sw128(kl + off, 16, 1024);
+          mma_bf16_ss(acc, dqh, dkh, IDESC, s > 0 ? 1u : 0u);
+          mma_bf16_ss(acc, dqh, dkl, IDESC, 1u);
+          mma_bf16_ss(acc, dql, dkh, IDESC, 1u);
+        }
+        mma_commit(&cs.k_empty[st]);
+        mma_commit(&cs.acc_full[ab]);
+      }
+      mma_commit(&cs.final_bar);
+      mbar_wait(&cs.final_bar, 0, abort, a.status);
+    }
+    __syncwarp();
+  } else {
+    const int r = warp * 32 + lane;
+    const int i = i0 + r;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float *srow = a.S + ((static_cast<int64_t>(b) * a.Hq + h) * a.nqb + (i < a.nqb ? i : 0)) * a.nkb_pad;
+    for (int ch = 0; ch < nch; ++ch) {
+      const int ab = ch & 1;
+      if (!mbar_wait(&cs.acc_full[ab], (ch >> 1) & 1, abort, a.status)) break;
+      tc_fence_after();
+      uint32_t v[4][32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld32(tl + ab * GCOLS + 32 * q, v[q]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&cs.acc_empty[ab]);
+      if (i < a.nqb) {
+        const int j0 = GCOLS * ch;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const int j = j0 + 32 * q + c;
+            if (j < a.nkb_pad) {
+              float4 o;
+              o.x = __uint_as_float(v[q][c]) * a.scale;
+              o.y = __uint_as_float(v[q][c + 1]) * a.scale;
+              o.z = __uint_as_float(v[q][c + 2]) * a.scale;
+              o.w = __uint_as_float(v[q][c + 3]) * a.scale;
+              *reinterpret_cast<float4 *>(srow + j) = o;
+            }
+          }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 256);
+}
+
+template <int D>
+cudaError_t launch_d(const ScoreGemmLaunch &l, const GemmArgs &a, cudaStream_t st) {
+  const uint32_t smem = GL<D>::TOTAL;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(score_gemm_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(static_cast<unsigned>(a.B * a.Hq), static_cast<unsigned>(a.ngroups));
+  score_gemm_kernel<D><<<grid, 192, smem, st>>>(l.qhi, l.qlo, l.khi, l.klo, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_score_gemm(const ScoreGemmLaunch &l, cudaStream_t st) {
+  GemmArgs a;
+  a.S = l.S;
+  a.nkb_pad = l.nkb_pad;
+  a.B = l.B; a.Hq = l.Hq; a.Hkv = l.Hkv; a.G = l.Hq / l.Hkv;
+  a.nqb = (l.N + QBLK - 1) / QBLK;
+  a.nkb = (l.N + KBLK - 1) / KBLK;
+  a.causal = l.causal;
+  a.ngroups = (a.nqb + GROWS - 1) / GROWS;
+  a.scale = l.scale;
+  a.status = l.status;
+  if (static_cast<int64_t>(a.B) * a.Hq * a.ngroups == 0) return cudaSuccess;
+  return l.d == 128 ? launch_d<128>(l, a, st) : launch_d<64>(l, a, st);
+}
+
+}  // namespace sparge

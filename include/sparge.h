@@ -81,9 +81,9 @@ typedef struct sparge_params {
   float scale;   /* softmax scale; 0 means 1/sqrt(d) */
   int32_t precision;            /* enum sparge_precision */
   unsigned long long *stats;    /* optional device pointer to 4 counters, or NULL */
-  void *const *timing_events;   /* optional: 5 cudaEvent_t handles recorded on the stream before the
-                                   pooling kernel and after the pooling, score/select, V-copy and
-                                   attention kernels (for per-kernel timing), or NULL */
+  void *const *timing_events;   /* optional: 6 cudaEvent_t handles recorded on the stream before the
+                                   pooling kernel and after the pooling, pooled-score, selection,
+                                   V-copy and attention kernels (for per-kernel timing), or NULL */
 } sparge_params;
 
 /*

@@ -48,13 +48,17 @@ def test_pool_sim_matches_oracle(key):
                      dtype=torch.uint8, device="cuda")
     fbs.predict_mask(q, k, w.topk, w.theta, w.causal, ws=ws)
     torch.cuda.synchronize()
-    muQ, sQ, muK, sK = (t.cpu().numpy().astype(np.float64) for t in fbs.predict_ws_views(ws, w.B, w.Hq, w.Hkv, w.N, w.d))
+    muQ, sQ, muK, sK, S = (t.cpu().numpy().astype(np.float64) for t in fbs.predict_ws_views(ws, w.B, w.Hq, w.Hkv, w.N, w.d))
     rmuQ, rsQ = oracle.pool_sim(f64(w.q), 128)
     rmuK, rsK = oracle.pool_sim(f64(w.k), 64)
     np.testing.assert_allclose(muQ, rmuQ, rtol=1e-5, atol=2e-6)
     np.testing.assert_allclose(muK, rmuK, rtol=1e-5, atol=2e-6)
     np.testing.assert_allclose(sQ, rsQ, rtol=1e-5, atol=2e-6)
     np.testing.assert_allclose(sK, rsK, rtol=1e-5, atol=2e-6)
+    # pooled scores on the valid tiles: tensor-core product of bf16 hi/lo splits, ~1e-5 relative
+    rS = oracle.pooled_scores(rmuQ, rmuK, w.causal, oracle.default_scale(w.d))
+    valid = np.isfinite(rS)
+    np.testing.assert_allclose(S[valid], rS[valid], rtol=1e-4, atol=2e-4)
 
 
 def check_mask(w, gm, topk=None, theta=None):
