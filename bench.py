@@ -141,6 +141,24 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------------
+# multi-rank bookkeeping (each rank runs its own replica; no collective on the data path)
+# ------------------------------------------------------------------------------------------------
+def max_over_ranks(seconds: float, dist=None, device=None) -> float:
+    """The slowest rank's timed-region length (the job is done when every replica is done)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, dense_flops_per_step: float, steps: int, seconds: float) -> float:
+    """Whole-job dense-equivalent TOPS: every rank processed `steps` full steps in `seconds`."""
+    return world * dense_flops_per_step * steps / seconds / 1e12
+
+
+# ------------------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------------------
 def run_ours(args, rank, world, local_rank):
@@ -204,10 +222,7 @@ def run_ours(args, rank, world, local_rank):
     t_attn = [e[4].elapsed_time(e[5]) / 1e3 for e in ev_sets]
     t_pred = [a + b + c for a, b, c in zip(t_pool, t_gemm, t_sel)]
     total = ev_sets[0][0].elapsed_time(ev_sets[-1][5]) / 1e3
-    if dist:
-        tt = torch.tensor([total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total = float(tt.item())
+    total = max_over_ranks(total, dist, dev)
     assert fbs.device_status() == 0
 
     # end to end through the public call: pinned host inputs copied in, output copied back
@@ -238,7 +253,7 @@ def run_ours(args, rank, world, local_rank):
 
     dense = w.dense_flops()
     ms_step = total / args.steps * 1e3
-    value = world * dense * args.steps / total / 1e12
+    value = job_value(world, dense, args.steps, total)
     avg = lambda xs: sum(xs) / len(xs)
     t_attn_avg, t_pred_avg = avg(t_attn), avg(t_pred)
     tile_flops = 2.0 * 128 * 64 * w.d

@@ -70,6 +70,7 @@ EXPORTS = {
     "sparge_hilbert_perm_3d": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "sparge_predict_mask_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_float,
                                                    ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "sparge_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
     "sparge_last_error": (ctypes.c_char_p, []),
     "sparge_get_device_status": (ctypes.c_int, [ctypes.c_void_p]),
 }
@@ -259,6 +260,11 @@ def hilbert_perm_3d(n_prefix: int, T: int, H: int, W: int) -> np.ndarray:
     out = np.empty(n_prefix + T * H * W, dtype=np.int32)
     _check(lib().sparge_hilbert_perm_3d(n_prefix, T, H, W, out.ctypes.data))
     return out
+
+
+def selftest_bounded_wait(limit_ns: int = 50_000_000):
+    """Enqueue the library's bounded-wait self test (a wait that is made to run out)."""
+    _check(lib().sparge_selftest_bounded_wait(int(limit_ns), _stream()))
 
 
 def device_status() -> int:

@@ -33,6 +33,20 @@ int cuda_fail(cudaError_t e, const char *where) {
 // kernels record a timed-out bounded wait there.
 __device__ int g_status_word = 0;
 
+// One thread waits on an mbarrier that nothing arrives on, through the same bounded wait the
+// attention and score kernels use; the wait runs out after limit_ns and records a timeout.
+__global__ void bounded_wait_probe_kernel(int *status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status, limit_ns);
+}
+
 int *status_ptr() {
   void *p = nullptr;
   if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
@@ -372,6 +386,17 @@ int sparge_permute_tokens(const sparge_tensor *x, const int32_t *perm, sparge_te
 
 int sparge_unpermute_tokens(const sparge_tensor *x, const int32_t *perm, sparge_tensor *y, sparge_stream_t stream) {
   return permute_common(x, perm, y, true, stream);
+}
+
+int sparge_selftest_bounded_wait(int64_t limit_ns, sparge_stream_t stream) {
+  g_last_error[0] = 0;
+  if (limit_ns < 1000000) limit_ns = 1000000;
+  if (limit_ns > 1000000000) limit_ns = 1000000000;
+  int *st = status_ptr();
+  if (!st) return fail(SPARGE_ERR_CUDA, "device status word unavailable");
+  bounded_wait_probe_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(st, (uint64_t)limit_ns);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SPARGE_OK : cuda_fail(e, "bounded wait probe launch");
 }
 
 int sparge_get_device_status(sparge_stream_t stream) {

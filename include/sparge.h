@@ -193,6 +193,15 @@ int sparge_hilbert_perm_3d(int n_prefix, int T, int H, int W, int32_t *perm_host
 int sparge_predict_mask_noalloc(const sparge_tensor *q, const sparge_tensor *k, float topk, float theta,
                                 int is_causal, uint8_t *mask, sparge_stream_t stream);
 
+/*
+ * Failure-detection test support.  Enqueues a one-thread kernel whose mbarrier wait gets no
+ * arrival: the wait gives up after limit_ns (clamped to [1 ms, 1 s]) exactly like the bounded
+ * waits of the library's kernels and records SPARGE_ERR_DEVICE_TIMEOUT in the device status word,
+ * which sparge_get_device_status then reports (and clears).  Nothing faults or hangs; the context
+ * stays usable.  No passage of the method corresponds to it.
+ */
+int sparge_selftest_bounded_wait(int64_t limit_ns, sparge_stream_t stream);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char *sparge_last_error(void);
 
