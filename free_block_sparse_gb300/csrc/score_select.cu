@@ -86,6 +86,9 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
   const bool keep_all = a.topk >= 1.f || a.sQ[row] < a.theta;
   float vstar = 0.f;
   uint64_t tiekeep = 0;
+  bool sorted = false;          // threshold found by sorting the crossing bin:
+  float et = 0.f;               //   keep e > et, or e == et with index <= jt
+  int jt = -1;
   if (!keep_all) {
     const float target = a.topk * Z;
     // bins of width 2^(sh-23) in log2 units over the bit pattern distance from 1.0f
@@ -134,7 +137,50 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
       const int nc = __shfl_sync(0xffffffffu, off, 31);
       off -= cnt;
       __syncwarp();
-      if (nc <= CMAX) {
+      if (nc <= 32) {
+        // one candidate per lane: sort by (e desc, index asc), then the first prefix reaching target
+#pragma unroll
+        for (int c = 0; c < VPL; ++c) {
+          const uint32_t u = __float_as_uint(e[c]);
+          if (e[c] > 0.f && u >= lo && u < hi) {
+            H[off] = e[c];
+            H[32 + off] = __int_as_float(lane + 32 * c);
+            ++off;
+          }
+        }
+        __syncwarp();
+        float ce = lane < nc ? H[lane] : -1.f;
+        int cj = lane < nc ? __float_as_int(H[32 + lane]) : 0x7fffffff;
+#pragma unroll
+        for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+          for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+            const float oe = __shfl_xor_sync(0xffffffffu, ce, jj);
+            const int oj = __shfl_xor_sync(0xffffffffu, cj, jj);
+            const bool mine_first = ce > oe || (ce == oe && cj < oj);
+            const bool take_first = ((lane & jj) == 0) == ((lane & kk) == 0);
+            if (mine_first != take_first) {
+              ce = oe;
+              cj = oj;
+            }
+          }
+        }
+        float ps = ce > 0.f ? ce : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float v = __shfl_up_sync(0xffffffffu, ps, o);
+          if (lane >= o) ps += v;
+        }
+        const float above = __shfl_sync(0xffffffffu, cum - mass, bstar);
+        const uint32_t reach = __ballot_sync(0xffffffffu, lane < nc && above + ps >= target);
+        if (reach) {
+          const int kstar = __ffs(reach) - 1;
+          et = __shfl_sync(0xffffffffu, ce, kstar);
+          jt = __shfl_sync(0xffffffffu, cj, kstar);
+          sorted = true;
+          lo = hi - 1u;  // resolved
+        }
+      } else if (nc <= CMAX) {
 #pragma unroll
         for (int c = 0; c < VPL; ++c) {
           const uint32_t u = __float_as_uint(e[c]);
@@ -173,6 +219,9 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
       }
     }
     vstar = __uint_as_float(lo);
+  }
+  if (!keep_all && !sorted) {
+    const float target = a.topk * Z;
     // elements equal to v*: keep them in ascending key-block order until the mass reaches target
     int nties = 0;
     float abovev = 0.f;
@@ -206,7 +255,11 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
     const int j = lane + 32 * c;
     if (j < a.nkb) {
       bool keep = false;
-      if (j < nvalid) keep = keep_all || e[c] > vstar || ((tiekeep >> c) & 1ull) || sKrow[j] < a.theta;
+      if (j < nvalid) {
+        const bool topk_keep = sorted ? (e[c] > et || (e[c] == et && j <= jt))
+                                      : (e[c] > vstar || ((tiekeep >> c) & 1ull));
+        keep = keep_all || topk_keep || sKrow[j] < a.theta;
+      }
       mrow[j] = keep ? 1 : 0;
     }
   }
