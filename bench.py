@@ -171,7 +171,7 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     peaks = load_peaks()
-    w = W.make_config(args.config)
+    w = make_workload(args)
     dev = torch.device("cuda", local_rank)
 
     def to_dev(u16):
@@ -312,10 +312,17 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line))
 
 
+def make_workload(args):
+    if args.heads:
+        hq, hkv = (int(x) for x in args.heads.split(","))
+        return W.make_config(args.config, Hq=hq, Hkv=hkv)
+    return W.make_config(args.config)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    w = W.make_config(args.config)
+    w = make_workload(args)
     for _ in range(args.warmup):
         oracle_sample(w, 2, 1)
     vals, walls = [], []
@@ -350,6 +357,8 @@ def main():
     ap.add_argument("--cpu-blocks", type=int, default=64)
     ap.add_argument("--cpu-workers", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", default=None,
+                    help="Hq,Hkv override (smaller cases of a workload for profiling; not a bench line)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

@@ -162,9 +162,7 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
   PredictWs pw = predict_ws_carve(ws, q.B, q.H, k.H, q.N, q.d);
   int rc;
   if ((rc = record_event(ev, 0, s))) return rc;
-  CUtensorMap tq, tk;
-  if ((rc = make_map(&tq, q, 128, "q")) || (rc = make_map(&tk, k, 64, "k"))) return rc;
-  cudaError_t e = launch_pool_sim(q, k, tq, tk, pw, status_ptr(), s);
+  cudaError_t e = launch_pool_sim(q, k, pw, s);
   if (e != cudaSuccess) return cuda_fail(e, "pool_sim launch");
   if ((rc = record_event(ev, 1, s))) return rc;
   {

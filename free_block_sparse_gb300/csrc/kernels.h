@@ -40,9 +40,7 @@ int run_predict(const View &q, const View &k, float topk, float theta, int causa
                 size_t ws_bytes, cudaStream_t s);
 int report_error(int code, const char *msg);
 
-// tq / tk: 4-D maps over Q and K as for the attention kernel (box 64 x 128 rows / 64 x 64 rows).
-cudaError_t launch_pool_sim(const View &q, const View &k, const CUtensorMap &tq, const CUtensorMap &tk,
-                            const PredictWs &ws, int *status, cudaStream_t st);
+cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, cudaStream_t st);
 
 // Pooled scores S = scale * muQ . muK^T on tcgen05 (bf16 hi/lo split, three products), for the
 // valid (causal) key blocks of every query block.  The four maps cover qhi, qlo (3-D: d, nqb,

@@ -4,10 +4,10 @@
 // For each 128-token query block and 64-token key block this kernel produces the fp32 mean of
 // the valid tokens and s = ||(1/n) sum_a x_a / ||x_a|| ||^2, the mean cosine similarity over
 // all ordered token pairs of the block (pairs a == b included).  A zero token contributes a
-// zero unit vector.  Memory-bound: one pass over Q and K.  One persistent CTA per SM: a producer
-// warp streams blocks by TMA into a deep shared-memory ring (so enough bytes are in flight to keep
-// HBM busy), eight consumer warps reduce each block from shared memory with fp32 (packed pair)
-// arithmetic and warp shuffles, then split the finishing work of the block among themselves.
+// zero unit vector.  Memory-bound: one pass over Q and K.  One warp per block, no block-level
+// barriers: each lane keeps eight 16-byte loads in flight in a rolling register buffer while it
+// accumulates, so many warps per SM keep enough bytes in flight to hold HBM busy; fp32 (packed
+// pair) arithmetic, warp-shuffle reductions, vector stores of the results.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -15,130 +15,67 @@ namespace sparge {
 namespace {
 
 struct PoolArgs {
+  const __nv_bfloat16 *q, *k;
+  int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn;
   int B, Hq, Hkv, N, nqb, nkb;
   int64_t nq_total, total;
   PredictWs ws;
-  int *status;
 };
+
+constexpr int INFLIGHT = 8;  // 16-byte loads in flight per lane
 
 template <int D>
-struct PL {
-  static constexpr int NST = D == 128 ? 6 : 10;         // ring stages
-  static constexpr uint32_t STAGE = QBLK * D * 2;        // room for one query block
-  static constexpr uint32_t OFF_RED = NST * STAGE;       // [8 warps][2][D] partial sums
-  static constexpr uint32_t OFF_REDS = OFF_RED + 8 * 2 * D * 4;
-  static constexpr uint32_t OFF_CTRL = OFF_REDS + 64;
-  static constexpr uint32_t TOTAL = OFF_CTRL + 256;
-};
-
-struct PCtrl {
-  uint64_t full[10], empty[10];
-  int abort;
-};
-
-struct BlockRef {
-  bool isQ;
-  int b, h, idx;  // batch, head, block index within the head
-  int n;          // valid tokens
-};
-
-__device__ __forceinline__ BlockRef block_ref(const PoolArgs &a, int64_t bid) {
-  BlockRef r;
-  r.isQ = bid < a.nq_total;
-  if (r.isQ) {
-    r.idx = static_cast<int>(bid % a.nqb);
-    const int64_t bh = bid / a.nqb;
-    r.h = static_cast<int>(bh % a.Hq);
-    r.b = static_cast<int>(bh / a.Hq);
-    r.n = min(QBLK, a.N - r.idx * QBLK);
-  } else {
-    bid -= a.nq_total;
-    r.idx = static_cast<int>(bid % a.nkb);
-    const int64_t bh = bid / a.nkb;
-    r.h = static_cast<int>(bh % a.Hkv);
-    r.b = static_cast<int>(bh / a.Hkv);
-    r.n = min(KBLK, a.N - r.idx * KBLK);
-  }
-  return r;
-}
-
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-template <int D>
-__global__ void __launch_bounds__(288, 1)
-    pool_sim_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const PoolArgs a) {
-  using L = PL<D>;
+__global__ void __launch_bounds__(128, 5) pool_sim_kernel(PoolArgs a) {
   constexpr int LPT = D / 8;     // lanes per token, 8 bf16 (16 bytes) per lane
-  constexpr int TPW = 32 / LPT;  // tokens per warp per step
-  constexpr int TPS = 8 * TPW;   // tokens per step of the 8 consumer warps
-  constexpr int NBOX = D / 64;   // 64-column boxes per token row
-  extern __shared__ __align__(1024) uint8_t smem[];
-  if (smem_u32(smem) & 1023u) {
-    if (threadIdx.x == 0) record_status(a.status, -4 /* SPARGE_ERR_CUDA */);
-    return;
-  }
-  PCtrl &cs = *reinterpret_cast<PCtrl *>(smem + L::OFF_CTRL);
-  float(*red)[2][D] = reinterpret_cast<float(*)[2][D]>(smem + L::OFF_RED);
-  float *red_s = reinterpret_cast<float *>(smem + L::OFF_REDS);
-  volatile int *abort = &cs.abort;
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int st = 0; st < L::NST; ++st) {
-      mbar_init(&cs.full[st], 1);
-      mbar_init(&cs.empty[st], 1);
-    }
-    cs.abort = 0;
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  if (w == 8) {
-    // ------------------------------- producer: TMA into the ring -------------------------------
-    if (lane == 0) {
-      prefetch_tmap(&tq);
-      prefetch_tmap(&tk);
-      int k = 0;
-      for (int64_t bid = blockIdx.x; bid < a.total; bid += gridDim.x, ++k) {
-        const int st = k % L::NST;
-        if (!mbar_wait(&cs.empty[st], ((k / L::NST) & 1) ^ 1, abort, a.status)) break;
-        const BlockRef r = block_ref(a, bid);
-        const int rows = r.isQ ? QBLK : KBLK;
-        uint8_t *dst = smem + st * L::STAGE;
-        mbar_arrive_expect_tx(&cs.full[st], static_cast<uint32_t>(rows * D * 2));
-        for (int bx = 0; bx < NBOX; ++bx)
-          tma_load_4d(dst + bx * rows * 128, r.isQ ? &tq : &tk, &cs.full[st], 64 * bx, rows * r.idx, r.h, r.b);
-      }
-      if (*abort) {
-        const uint64_t t0 = global_timer_ns();
-        while (global_timer_ns() - t0 < 1000000ull) {
-        }
-      }
-    }
-    return;
-  }
-
-  // ------------------------------- consumers: 8 warps -------------------------------
+  constexpr int TPW = 32 / LPT;  // tokens per warp-wide load
+  const int lane = threadIdx.x & 31;
   const int sub = lane / LPT, part = lane % LPT;
-  const int bx = part >> 3, chunk = part & 7;
-  int k = 0;
-  for (int64_t bid = blockIdx.x; bid < a.total; bid += gridDim.x, ++k) {
-    const int st = k % L::NST;
-    // after a timeout the wait returns at once and the data is stale, but every consumer warp
-    // still takes part in the barriers below, so none of them can hang
-    mbar_wait(&cs.full[st], (k / L::NST) & 1, abort, a.status);
-    const BlockRef r = block_ref(a, bid);
-    const int rows = r.isQ ? QBLK : KBLK;
-    const uint8_t *src = smem + st * L::STAGE + bx * rows * 128;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t bid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; bid < a.total;
+       bid += nwarps) {
+    // ---- which block ----
+    const bool isQ = bid < a.nq_total;
+    int b, h, idx, n, rows;
+    const __nv_bfloat16 *base;
+    int64_t sn, row;
+    if (isQ) {
+      idx = static_cast<int>(bid % a.nqb);
+      const int64_t bh = bid / a.nqb;
+      h = static_cast<int>(bh % a.Hq);
+      b = static_cast<int>(bh / a.Hq);
+      rows = QBLK;
+      sn = a.q_sn;
+      base = a.q + b * a.q_sb + h * a.q_sh + static_cast<int64_t>(idx) * QBLK * sn;
+      row = (static_cast<int64_t>(b) * a.Hq + h) * a.nqb + idx;
+    } else {
+      const int64_t kb = bid - a.nq_total;
+      idx = static_cast<int>(kb % a.nkb);
+      const int64_t bh = kb / a.nkb;
+      h = static_cast<int>(bh % a.Hkv);
+      b = static_cast<int>(bh / a.Hkv);
+      rows = KBLK;
+      sn = a.k_sn;
+      base = a.k + b * a.k_sb + h * a.k_sh + static_cast<int64_t>(idx) * KBLK * sn;
+      row = (static_cast<int64_t>(b) * a.Hkv + h) * a.nkb + idx;
+    }
+    n = min(rows, a.N - idx * rows);
+    const int steps = rows / TPW;  // warp-wide loads covering the block (a multiple of INFLIGHT)
+    const __nv_bfloat16 *p = base + sub * sn + part * 8;
+    auto load = [&](int s) {
+      const int t = s * TPW + sub;
+      return (t < n) ? ld_stream_v4(p + static_cast<int64_t>(s) * TPW * sn) : make_uint4(0, 0, 0, 0);
+    };
+    uint4 buf[INFLIGHT];
+#pragma unroll
+    for (int u = 0; u < INFLIGHT; ++u) buf[u] = load(u);
     float2 sx2[4], sh2[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) sx2[c] = sh2[c] = make_float2(0.f, 0.f);
+    for (int s0 = 0; s0 < steps; s0 += INFLIGHT) {
 #pragma unroll
-    for (int step = 0; step < QBLK / TPS; ++step) {
-      const int t = step * TPS + w * TPW + sub;
-      if (t < rows) {  // rows past the valid tokens were zero-filled by TMA and add nothing
-        const uint4 v = *reinterpret_cast<const uint4 *>(src + t * 128 + ((chunk ^ (t & 7)) << 4));
+      for (int u = 0; u < INFLIGHT; ++u) {
+        const uint4 v = buf[u];
+        if (s0 + INFLIGHT + u < steps) buf[u] = load(s0 + INFLIGHT + u);
         const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
         float2 x2[4];
 #pragma unroll
@@ -158,6 +95,7 @@ __global__ void __launch_bounds__(288, 1)
         }
       }
     }
+    // sum over the token slots of the warp (lanes with the same part)
 #pragma unroll
     for (int off = LPT; off < 32; off <<= 1) {
 #pragma unroll
@@ -168,83 +106,51 @@ __global__ void __launch_bounds__(288, 1)
         sh2[c].y += __shfl_xor_sync(0xffffffffu, sh2[c].y, off);
       }
     }
-    if (sub == 0) {
+    const float invn = 1.f / static_cast<float>(n);
+    float hsq = 0.f;
+    if (sub == 0) {  // lanes 0..LPT-1 own dims 8 part .. 8 part + 7
+      float mean[8];
+      uint32_t hi[4], lo[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        red[w][0][part * 8 + 2 * c] = sx2[c].x;
-        red[w][0][part * 8 + 2 * c + 1] = sx2[c].y;
-        red[w][1][part * 8 + 2 * c] = sh2[c].x;
-        red[w][1][part * 8 + 2 * c + 1] = sh2[c].y;
-      }
-    }
-    consumer_sync();
-    if (threadIdx.x == 0) mbar_arrive(&cs.empty[st]);  // every consumer is done with this stage
-    {
-      constexpr int DPW = D / 8;
-      const float invn = 1.f / static_cast<float>(r.n);
-      float hsq = 0.f;
-      if (lane < DPW) {
-        const int dim = w * DPW + lane;
-        float mx = 0.f, hx = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < 8; ++ww) {
-          mx += red[ww][0][dim];
-          hx += red[ww][1][dim];
-        }
-        hx *= invn;
-        hsq = hx * hx;
-        const float mean = mx * invn;
-        const int64_t row = r.isQ ? (static_cast<int64_t>(r.b) * a.Hq + r.h) * a.nqb + r.idx
-                                  : (static_cast<int64_t>(r.b) * a.Hkv + r.h) * a.nkb + r.idx;
-        float *mu = (r.isQ ? a.ws.muQ : a.ws.muK) + row * D;
-        uint16_t *hi = (r.isQ ? a.ws.qhi : a.ws.khi) + row * D;
-        uint16_t *lo = (r.isQ ? a.ws.qlo : a.ws.klo) + row * D;
-        mu[dim] = mean;
-        const __nv_bfloat16 hb = __float2bfloat16_rn(mean);
-        hi[dim] = __bfloat16_as_ushort(hb);
-        lo[dim] = __bfloat16_as_ushort(__float2bfloat16_rn(mean - __bfloat162float(hb)));
+        mean[2 * c] = sx2[c].x * invn;
+        mean[2 * c + 1] = sx2[c].y * invn;
+        const float h0 = sh2[c].x * invn, h1 = sh2[c].y * invn;
+        hsq = fmaf(h0, h0, fmaf(h1, h1, hsq));
       }
 #pragma unroll
-      for (int off = DPW / 2; off > 0; off >>= 1) hsq += __shfl_xor_sync(0xffffffffu, hsq, off);
-      if (lane == 0) red_s[w] = hsq;
+      for (int c = 0; c < 4; ++c) {
+        const __nv_bfloat16 a0 = __float2bfloat16_rn(mean[2 * c]), a1 = __float2bfloat16_rn(mean[2 * c + 1]);
+        const __nv_bfloat16 b0 = __float2bfloat16_rn(mean[2 * c] - __bfloat162float(a0));
+        const __nv_bfloat16 b1 = __float2bfloat16_rn(mean[2 * c + 1] - __bfloat162float(a1));
+        hi[c] = static_cast<uint32_t>(__bfloat16_as_ushort(a0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(a1)) << 16);
+        lo[c] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b1)) << 16);
+      }
+      float *mu = (isQ ? a.ws.muQ : a.ws.muK) + row * D + part * 8;
+      *reinterpret_cast<float4 *>(mu) = make_float4(mean[0], mean[1], mean[2], mean[3]);
+      *reinterpret_cast<float4 *>(mu + 4) = make_float4(mean[4], mean[5], mean[6], mean[7]);
+      *reinterpret_cast<uint4 *>((isQ ? a.ws.qhi : a.ws.khi) + row * D + part * 8) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4 *>((isQ ? a.ws.qlo : a.ws.klo) + row * D + part * 8) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    consumer_sync();
-    if (threadIdx.x == 0) {
-      float sv = 0.f;
 #pragma unroll
-      for (int ww = 0; ww < 8; ++ww) sv += red_s[ww];
-      if (r.isQ)
-        a.ws.sQ[(static_cast<int64_t>(r.b) * a.Hq + r.h) * a.nqb + r.idx] = sv;
+    for (int off = 16; off > 0; off >>= 1) hsq += __shfl_xor_sync(0xffffffffu, hsq, off);
+    if (lane == 0) {
+      if (isQ)
+        a.ws.sQ[row] = hsq;
       else
-        a.ws.sK[(static_cast<int64_t>(r.b) * a.Hkv + r.h) * a.ws.nkb_pad + r.idx] = sv;
+        a.ws.sK[(static_cast<int64_t>(b) * a.Hkv + h) * a.ws.nkb_pad + idx] = hsq;
     }
   }
-}
-
-template <int D>
-cudaError_t launch_d(const CUtensorMap &tq, const CUtensorMap &tk, const PoolArgs &a, cudaStream_t st) {
-  const uint32_t smem = PL<D>::TOTAL;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(pool_sim_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t cap = sms > 0 ? sms : 152;  // one persistent CTA per SM
-  const unsigned grid = static_cast<unsigned>(a.total < cap ? a.total : cap);
-  pool_sim_kernel<D><<<grid, 288, smem, st>>>(tq, tk, a);
-  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_pool_sim(const View &q, const View &k, const CUtensorMap &tq, const CUtensorMap &tk,
-                            const PredictWs &ws, int *status, cudaStream_t st) {
+cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, cudaStream_t st) {
   PoolArgs a;
+  a.q = static_cast<const __nv_bfloat16 *>(q.data);
+  a.k = static_cast<const __nv_bfloat16 *>(k.data);
+  a.q_sb = q.sb; a.q_sh = q.sh; a.q_sn = q.sn;
+  a.k_sb = k.sb; a.k_sh = k.sh; a.k_sn = k.sn;
   a.B = static_cast<int>(q.B); a.Hq = static_cast<int>(q.H); a.Hkv = static_cast<int>(k.H);
   a.N = static_cast<int>(q.N);
   a.nqb = (a.N + QBLK - 1) / QBLK;
@@ -252,9 +158,18 @@ cudaError_t launch_pool_sim(const View &q, const View &k, const CUtensorMap &tq,
   a.nq_total = static_cast<int64_t>(a.B) * a.Hq * a.nqb;
   a.total = a.nq_total + static_cast<int64_t>(a.B) * a.Hkv * a.nkb;
   a.ws = ws;
-  a.status = status;
   if (a.total == 0) return cudaSuccess;
-  return q.d == 128 ? launch_d<128>(tq, tk, a, st) : launch_d<64>(tq, tk, a, st);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (a.total + 3) / 4;
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 5;  // 5 resident CTAs of 4 warps per SM
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  if (q.d == 128)
+    pool_sim_kernel<128><<<grid, 128, 0, st>>>(a);
+  else
+    pool_sim_kernel<64><<<grid, 128, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace sparge
