@@ -23,7 +23,6 @@ namespace {
 
 constexpr int WARPS = 8;
 constexpr int NBIN = 32;
-constexpr int CMAX = 256;  // candidates handled by the compact search (8 per lane)
 
 struct SelArgs {
   const float *S;
@@ -91,37 +90,58 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
   int jt = -1;
   if (!keep_all) {
     const float target = a.topk * Z;
-    // bins of width 2^(sh-23) in log2 units over the bit pattern distance from 1.0f
+    // Level 0: bins of width 2^sh bit patterns (2^(sh-23) log2 units) below 1.0f, wide enough that
+    // 32 of them reach the bound past which no element can be v*.  Each further level splits the
+    // crossing bin of the previous one into 32 sub-bins.  All levels use one formula:
+    // bin = (hi - 1 - bits(e)) >> shift for e in [lo, hi).
     const float r2 = log2f(static_cast<float>(nvalid) / (1.f - a.topk)) + 0.1f;
-    int sh = 16;
-    while (static_cast<float>(NBIN) * exp2f(static_cast<float>(sh - 23)) < r2) ++sh;
-#pragma unroll
-    for (int k = 0; k < NBIN; ++k) H[k * 32 + lane] = 0.f;
-    __syncwarp();
-#pragma unroll
-    for (int c = 0; c < VPL; ++c) {
-      const uint32_t bin = (0x3F800000u - __float_as_uint(e[c])) >> sh;
-      if (e[c] > 0.f && bin < NBIN) H[bin * 32 + lane] += e[c];  // lane-private column: no conflicts
-    }
-    __syncwarp();
-    float mass = 0.f;  // lane = bin
-#pragma unroll
-    for (int k = 0; k < 32; ++k) mass += H[lane * 32 + ((k + lane) & 31)];
-    float cum = mass;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float o = __shfl_up_sync(0xffffffffu, cum, off);
-      if (lane >= off) cum += o;
-    }
-    const uint32_t hit = __ballot_sync(0xffffffffu, cum >= target);
+    int shift = 16;
+    while (static_cast<float>(NBIN) * exp2f(static_cast<float>(shift - 23)) < r2) ++shift;
     uint32_t lo = 1u, hi = 0x3F800001u;  // bit patterns: mass(e >= lo) >= target > mass(e >= hi)
-    if (hit) {
+    float above = 0.f;                   // mass of the elements >= hi
+    int nc = 0x7fffffff;                 // elements in [lo, hi)
+    for (int level = 0; level < 3 && nc > 32 && shift >= 0; ++level) {
+#pragma unroll
+      for (int k = 0; k < NBIN; ++k) H[k * 32 + lane] = 0.f;
+      __syncwarp();
+      const uint32_t top = hi - 1u;
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) {
+        const uint32_t u = __float_as_uint(e[c]);
+        const uint32_t bin = (top - u) >> shift;
+        if (e[c] > 0.f && u >= lo && u < hi && bin < NBIN) H[bin * 32 + lane] += e[c];  // lane-private column
+      }
+      __syncwarp();
+      float mass = 0.f;  // lane = bin
+#pragma unroll
+      for (int k = 0; k < 32; ++k) mass += H[lane * 32 + ((k + lane) & 31)];
+      float cum = mass;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, cum, off);
+        if (lane >= off) cum += o;
+      }
+      const uint32_t hit = __ballot_sync(0xffffffffu, above + cum >= target);
+      if (!hit) break;  // rounding left the crossing outside the bins: resolve [lo, hi) below
       const int bstar = __ffs(hit) - 1;
-      const uint32_t top = 0x3F800000u - (static_cast<uint32_t>(bstar) << sh) + 1u;
-      const uint32_t width = 1u << sh;
-      hi = top;
-      lo = (top > width) ? top - width : 1u;
-      // compact the elements of the crossing bin
+      const uint32_t nhi = top + 1u - (static_cast<uint32_t>(bstar) << shift);
+      const uint32_t width = 1u << shift;
+      const uint32_t nlo = (nhi > lo + width) ? nhi - width : lo;
+      above += __shfl_sync(0xffffffffu, cum - mass, bstar);
+      hi = nhi;
+      lo = nlo;
+      int cnt = 0;
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) {
+        const uint32_t u = __float_as_uint(e[c]);
+        cnt += (e[c] > 0.f && u >= lo && u < hi) ? 1 : 0;
+      }
+      nc = warp_sum_i(cnt);
+      shift -= 5;
+      __syncwarp();
+    }
+    if (nc <= 32) {
+      // one candidate per lane: sort by (e desc, index asc), then the first prefix reaching target
       int cnt = 0;
 #pragma unroll
       for (int c = 0; c < VPL; ++c) {
@@ -134,78 +154,50 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
         const int v = __shfl_up_sync(0xffffffffu, off, o);
         if (lane >= o) off += v;
       }
-      const int nc = __shfl_sync(0xffffffffu, off, 31);
       off -= cnt;
       __syncwarp();
-      if (nc <= 32) {
-        // one candidate per lane: sort by (e desc, index asc), then the first prefix reaching target
 #pragma unroll
-        for (int c = 0; c < VPL; ++c) {
-          const uint32_t u = __float_as_uint(e[c]);
-          if (e[c] > 0.f && u >= lo && u < hi) {
-            H[off] = e[c];
-            H[32 + off] = __int_as_float(lane + 32 * c);
-            ++off;
-          }
-        }
-        __syncwarp();
-        float ce = lane < nc ? H[lane] : -1.f;
-        int cj = lane < nc ? __float_as_int(H[32 + lane]) : 0x7fffffff;
-#pragma unroll
-        for (int kk = 2; kk <= 32; kk <<= 1) {
-#pragma unroll
-          for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-            const float oe = __shfl_xor_sync(0xffffffffu, ce, jj);
-            const int oj = __shfl_xor_sync(0xffffffffu, cj, jj);
-            const bool mine_first = ce > oe || (ce == oe && cj < oj);
-            const bool take_first = ((lane & jj) == 0) == ((lane & kk) == 0);
-            if (mine_first != take_first) {
-              ce = oe;
-              cj = oj;
-            }
-          }
-        }
-        float ps = ce > 0.f ? ce : 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float v = __shfl_up_sync(0xffffffffu, ps, o);
-          if (lane >= o) ps += v;
-        }
-        const float above = __shfl_sync(0xffffffffu, cum - mass, bstar);
-        const uint32_t reach = __ballot_sync(0xffffffffu, lane < nc && above + ps >= target);
-        if (reach) {
-          const int kstar = __ffs(reach) - 1;
-          et = __shfl_sync(0xffffffffu, ce, kstar);
-          jt = __shfl_sync(0xffffffffu, cj, kstar);
-          sorted = true;
-          lo = hi - 1u;  // resolved
-        }
-      } else if (nc <= CMAX) {
-#pragma unroll
-        for (int c = 0; c < VPL; ++c) {
-          const uint32_t u = __float_as_uint(e[c]);
-          if (e[c] > 0.f && u >= lo && u < hi) H[off++] = e[c];
-        }
-        __syncwarp();
-        float ce[CMAX / 32];
-#pragma unroll
-        for (int k = 0; k < CMAX / 32; ++k) ce[k] = (lane + 32 * k < nc) ? H[lane + 32 * k] : 0.f;
-        const float above = __shfl_sync(0xffffffffu, cum - mass, bstar);
-        while (hi - lo > 1u) {
-          const uint32_t mid = lo + ((hi - lo) >> 1);
-          const float tv = __uint_as_float(mid);
-          float part = 0.f;
-#pragma unroll
-          for (int k = 0; k < CMAX / 32; ++k) part += (ce[k] >= tv) ? ce[k] : 0.f;
-          if (above + warp_sum(part) >= target)
-            lo = mid;
-          else
-            hi = mid;
+      for (int c = 0; c < VPL; ++c) {
+        const uint32_t u = __float_as_uint(e[c]);
+        if (e[c] > 0.f && u >= lo && u < hi) {
+          H[off] = e[c];
+          H[32 + off] = __int_as_float(lane + 32 * c);
+          ++off;
         }
       }
+      __syncwarp();
+      float ce = lane < nc ? H[lane] : -1.f;
+      int cj = lane < nc ? __float_as_int(H[32 + lane]) : 0x7fffffff;
+#pragma unroll
+      for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+          const float oe = __shfl_xor_sync(0xffffffffu, ce, jj);
+          const int oj = __shfl_xor_sync(0xffffffffu, cj, jj);
+          const bool mine_first = ce > oe || (ce == oe && cj < oj);
+          const bool take_first = ((lane & jj) == 0) == ((lane & kk) == 0);
+          if (mine_first != take_first) {
+            ce = oe;
+            cj = oj;
+          }
+        }
+      }
+      float ps = ce > 0.f ? ce : 0.f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float v = __shfl_up_sync(0xffffffffu, ps, o);
+        if (lane >= o) ps += v;
+      }
+      const uint32_t reach = __ballot_sync(0xffffffffu, lane < nc && above + ps >= target);
+      if (reach) {
+        const int kstar = __ffs(reach) - 1;
+        et = __shfl_sync(0xffffffffu, ce, kstar);
+        jt = __shfl_sync(0xffffffffu, cj, kstar);
+        sorted = true;
+      }
     }
-    if (hi - lo > 1u) {
-      // many candidates (or no crossing bin): bisection over every element in [lo, hi)
+    if (!sorted) {
+      // bisection over every element in [lo, hi) (rare: many equal-looking values or rounding)
       while (hi - lo > 1u) {
         const uint32_t mid = lo + ((hi - lo) >> 1);
         const float tv = __uint_as_float(mid);
@@ -217,8 +209,8 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
         else
           hi = mid;
       }
+      vstar = __uint_as_float(lo);
     }
-    vstar = __uint_as_float(lo);
   }
   if (!keep_all && !sorted) {
     const float target = a.topk * Z;
