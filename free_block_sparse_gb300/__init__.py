@@ -26,9 +26,12 @@ SPARGE_ERR_DEVICE_TIMEOUT = -5
 SPARGE_BF16 = 1
 SPARGE_PRECISION_BF16 = 0
 SPARGE_PRECISION_Q8 = 1
+SPARGE_PRECISION_Q8_FP8PV = 2
 SPARGE_OP_PREDICT_MASK = 1
 SPARGE_OP_BLOCK_SPARSE_ATTN = 2
 SPARGE_OP_ATTN = 3
+SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 = 4
+SPARGE_OP_ATTN_Q8 = 5
 QBLK, KBLK = 128, 64
 
 
@@ -176,13 +179,46 @@ def predict_ws_views(ws, B, Hq, Hkv, N, d):
             f(sK).view(B, Hkv, nkb_pad)[..., :nkb], f(S).view(B, Hq, nqb, nkb_pad)[..., :nkb])
 
 
+def q8_ws_views(ws, B, Hq, Hkv, N, d):
+    """Views of the 8-bit attention workspace after block_sparse_attn with an 8-bit precision: q8
+    (B,Hq,N,d) and k8 (B,Hkv,N,d) e4m3 codes (uint8), v8 (B,Hkv,d,npad) channel-major e4m3 codes
+    (meaningful after SPARGE_PRECISION_Q8_FP8PV), sq (B,Hq,nqb), sk (B,Hkv,nkb), kmean (B,Hkv,d),
+    sv (B,Hkv,d), following the layout the library writes (regions 256-byte aligned)."""
+    torch = _torch()
+    nqb, nkb = n_blocks(N)
+    npad = -(-N // 64) * 64
+    u8 = ws if ws.dtype == torch.uint8 else ws.view(torch.uint8)
+
+    def take(off, nbytes):
+        return u8[off:off + nbytes], off + ((nbytes + 255) // 256) * 256
+
+    off = 0
+    q8, off = take(off, B * Hq * N * d)
+    k8, off = take(off, B * Hkv * N * d)
+    v8, _ = take(off, B * Hkv * d * npad)
+    _, off = take(off, max(B * Hkv * d * npad, 2 * B * Hkv * N * d))
+    sq, off = take(off, 4 * B * Hq * nqb)
+    sk, off = take(off, 4 * B * Hkv * nkb)
+    km, off = take(off, 4 * B * Hkv * d)
+    sv, off = take(off, 4 * B * Hkv * d)
+    f = lambda t: t.view(torch.float32)
+    return dict(q8=q8.view(B, Hq, N, d), k8=k8.view(B, Hkv, N, d), v8=v8.view(B, Hkv, d, npad),
+                sq=f(sq).view(B, Hq, nqb), sk=f(sk).view(B, Hkv, nkb), kmean=f(km).view(B, Hkv, d),
+                sv=f(sv).view(B, Hkv, d))
+
+
 def block_sparse_attn(q, k, v, mask=None, lam: float = -math.inf, causal: bool = False, out=None, stats=None,
                       precision: int = SPARGE_PRECISION_BF16, ws=None):
-    """Stage 2: attention over the kept 128x64 tiles with the lambda warp filter."""
+    """Stage 2: attention over the kept 128x64 tiles with the lambda warp filter.
+    precision SPARGE_PRECISION_Q8 (e4m3 Q.K^T, f16 P.V) or SPARGE_PRECISION_Q8_FP8PV (both
+    products e4m3) runs the 8-bit path (d = 128); its workspace then holds the quantised copies
+    and scales (see q8_ws_views)."""
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
-    ws = _workspace(SPARGE_OP_BLOCK_SPARSE_ATTN, q, k, ws)
+    op = SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 if precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV) \
+        else SPARGE_OP_BLOCK_SPARSE_ATTN
+    ws = _workspace(op, q, k, ws)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     mp = 0 if mask is None else mask.data_ptr()
     sp = 0 if stats is None else stats.data_ptr()
@@ -212,7 +248,8 @@ def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: 
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
-    ws = _workspace(SPARGE_OP_ATTN, q, k, ws)
+    q8 = precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV)
+    ws = _workspace(SPARGE_OP_ATTN_Q8 if q8 else SPARGE_OP_ATTN, q, k, ws)
     evp = None
     if events is not None:
         assert len(events) == 6

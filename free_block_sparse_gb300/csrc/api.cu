@@ -133,6 +133,23 @@ int make_map3(CUtensorMap *m, void *base, int64_t d, int64_t rows, int64_t plane
   return SPARGE_OK;
 }
 
+// 4-D map over a byte array (e4m3 codes): dims and byte strides innermost first, box
+// box0 x box1, the given swizzle.
+int make_map_u8(CUtensorMap *m, void *base, const int64_t dims_[4], const int64_t strides_[3], int box0, int box1,
+                CUtensorMapSwizzle swz, const char *name) {
+  encode_fn_t enc = get_encode();
+  if (!enc) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[4], strides[3];
+  for (int i = 0; i < 4; ++i) dims[i] = (cuuint64_t)dims_[i];
+  for (int i = 0; i < 3; ++i) strides[i] = (cuuint64_t)strides_[i];
+  cuuint32_t box[4] = {(cuuint32_t)box0, (cuuint32_t)box1, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+  return SPARGE_OK;
+}
+
 int check_topk_theta(float topk, float theta) {
   if (!(topk > 0.f && topk <= 1.f)) return fail(SPARGE_ERR_INVALID_ARG, "topk=%g not in (0, 1]", (double)topk);
   if (!std::isfinite(theta)) return fail(SPARGE_ERR_INVALID_ARG, "theta must be finite");
@@ -188,30 +205,65 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
 
 size_t v16_bytes(int64_t B, int64_t Hkv, int64_t N, int64_t d) { return align256((size_t)B * Hkv * N * d * 2); }
 
-// ws: at least v16_bytes(...) for the f16 copy of V
+// Attention workspace for a precision: the f16 copy of V, or the 8-bit copies and scales.
+bool is_q8(int precision) { return precision == SPARGE_PRECISION_Q8 || precision == SPARGE_PRECISION_Q8_FP8PV; }
+
+size_t attn_ws_bytes(int precision, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
+  if (is_q8(precision)) return d == 128 ? q8_ws_bytes(B, Hq, Hkv, N, d) : 0;
+  return v16_bytes(B, Hkv, N, d);
+}
+
 int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, float lambda, int causal, float scale,
               int precision, sparge_tensor *o, unsigned long long *stats, void *ws, size_t ws_bytes,
               cudaStream_t s, void *const *ev = nullptr) {
-  if (precision != SPARGE_PRECISION_BF16) return fail(SPARGE_ERR_UNSUPPORTED, "precision %d not supported", precision);
+  if (precision != SPARGE_PRECISION_BF16 && !is_q8(precision))
+    return fail(SPARGE_ERR_UNSUPPORTED, "precision %d not supported", precision);
+  const bool q8 = is_q8(precision), pv8 = precision == SPARGE_PRECISION_Q8_FP8PV;
+  if (q8 && q.d != 128) return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path needs d = 128 (got %lld)", (long long)q.d);
+  if (q8 && q.N > 65535LL * 64) return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path supports N <= %lld", 65535LL * 64);
   View ov;
   int rc = check_tensor(o, "o", &ov);
   if (rc) return rc;
   if (v.B != q.B || v.N != q.N || v.d != q.d || v.H != k.H) return fail(SPARGE_ERR_INVALID_ARG, "v disagrees with q/k");
   if (ov.B != q.B || ov.N != q.N || ov.d != q.d || ov.H != q.H) return fail(SPARGE_ERR_INVALID_ARG, "o disagrees with q");
-  const size_t need = v16_bytes(v.B, v.H, v.N, v.d);
+  const size_t need = attn_ws_bytes(precision, q.B, q.H, k.H, q.N, q.d);
   if (ws_bytes < need || (need && !ws))
     return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(SPARGE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   if (q.B == 0 || q.N == 0) return SPARGE_OK;
-  cudaError_t e = launch_convert_v_f16(v, ws, s);
-  if (e != cudaSuccess) return cuda_fail(e, "convert_v launch");
-  if ((rc = record_event(ev, 4, s))) return rc;
-  View v16{ws, v.B, v.H, v.N, v.d, v.H * v.N * v.d, v.N * v.d, v.d};
   AttnLaunch l;
   memset(&l, 0, sizeof(l));
-  if ((rc = make_map(&l.tq, q, 128, "q"))) return rc;
-  if ((rc = make_map(&l.tk, k, 64, "k"))) return rc;
-  if ((rc = make_map(&l.tv, v16, 64, "v", CU_TENSOR_MAP_DATA_TYPE_FLOAT16))) return rc;
+  if (q8) {
+    const Q8Ws w = q8_ws_carve(ws, q.B, q.H, k.H, q.N, q.d);
+    cudaError_t e = launch_q8_prep(q, k, v, w, pv8, s);
+    if (e != cudaSuccess) return cuda_fail(e, "8-bit quantisation launch");
+    if (!pv8 && (e = launch_convert_v_f16(v, w.v8, s)) != cudaSuccess) return cuda_fail(e, "convert_v launch");
+    if ((rc = record_event(ev, 4, s))) return rc;
+    const int64_t d = q.d, N = q.N, npad = cdiv(N, 64) * 64;
+    const int64_t qd[4] = {d, N, q.H, q.B}, qs[3] = {d, N * d, q.H * N * d};
+    const int64_t kd[4] = {d, N, k.H, k.B}, ks[3] = {d, N * d, k.H * N * d};
+    const int64_t vd[4] = {npad, d, k.H, k.B}, vs[3] = {npad, d * npad, k.H * d * npad};
+    if ((rc = make_map_u8(&l.tq, w.q8, qd, qs, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, "q8")) ||
+        (rc = make_map_u8(&l.tk, w.k8, kd, ks, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B, "k8")) ||
+        (pv8 && (rc = make_map_u8(&l.tv, w.v8, vd, vs, 64, (int)d, CU_TENSOR_MAP_SWIZZLE_64B, "v8"))))
+      return rc;
+    if (!pv8) {
+      View v16{w.v8, v.B, v.H, v.N, v.d, v.H * v.N * v.d, v.N * v.d, v.d};
+      if ((rc = make_map(&l.tv, v16, 64, "v", CU_TENSOR_MAP_DATA_TYPE_FLOAT16))) return rc;
+    }
+    l.q8 = pv8 ? 2 : 1;
+    l.sq = w.sq;
+    l.sk = w.sk;
+    l.sv = w.sv;
+  } else {
+    cudaError_t e = launch_convert_v_f16(v, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "convert_v launch");
+    if ((rc = record_event(ev, 4, s))) return rc;
+    View v16{ws, v.B, v.H, v.N, v.d, v.H * v.N * v.d, v.N * v.d, v.d};
+    if ((rc = make_map(&l.tq, q, 128, "q"))) return rc;
+    if ((rc = make_map(&l.tk, k, 64, "k"))) return rc;
+    if ((rc = make_map(&l.tv, v16, 64, "v", CU_TENSOR_MAP_DATA_TYPE_FLOAT16))) return rc;
+  }
   l.mask = mask;
   l.o = o->data;
   l.o_sb = ov.sb; l.o_sh = ov.sh; l.o_sn = ov.sn;
@@ -221,7 +273,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   l.lambda = lambda;
   l.stats = stats;
   l.status = status_ptr();
-  e = launch_bsattn(l, s);
+  cudaError_t e = launch_bsattn(l, s);
   if (e != cudaSuccess) return cuda_fail(e, "bsattn launch");
   return record_event(ev, 5, s);
 }
@@ -294,6 +346,12 @@ size_t sparge_workspace_bytes(int op, int64_t B, int64_t Hq, int64_t Hkv, int64_
     case SPARGE_OP_ATTN:
       return predict_ws_bytes(B, Hq, Hkv, N, d) + align256((size_t)B * Hq * cdiv(N, QBLK) * cdiv(N, KBLK)) +
              v16_bytes(B, Hkv, N, d);
+    case SPARGE_OP_BLOCK_SPARSE_ATTN_Q8:
+      return attn_ws_bytes(SPARGE_PRECISION_Q8, B, Hq, Hkv, N, d);
+    case SPARGE_OP_ATTN_Q8:
+      if (d != 128) return 0;
+      return predict_ws_bytes(B, Hq, Hkv, N, d) + align256((size_t)B * Hq * cdiv(N, QBLK) * cdiv(N, KBLK)) +
+             attn_ws_bytes(SPARGE_PRECISION_Q8, B, Hq, Hkv, N, d);
     default:
       return 0;
   }
@@ -342,7 +400,9 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)qv.d);
   const size_t need_pred = predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, qv.d);
   const size_t mask_bytes = mask_out ? 0 : align256((size_t)qv.B * qv.H * cdiv(qv.N, QBLK) * cdiv(qv.N, KBLK));
-  const size_t need_v = v16_bytes(vv.B, vv.H, vv.N, vv.d);
+  if (is_q8(p->precision) && qv.d != 128)
+    return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path needs d = 128 (got %lld)", (long long)qv.d);
+  const size_t need_v = attn_ws_bytes(p->precision, qv.B, qv.H, kv.H, qv.N, qv.d);
   const size_t need = need_pred + mask_bytes + need_v;
   if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   uint8_t *mask = mask_out ? mask_out : static_cast<uint8_t *>(ws) + need_pred;

@@ -34,7 +34,8 @@ namespace sparge {
 namespace {
 
 constexpr int NTHREADS = 192;
-constexpr int RESCALE_LOG2 = 8;
+constexpr int RESCALE_LOG2 = 8;   // bf16 path: O is rescaled when the running max passes m_ref + 8
+constexpr int RESCALE_LOG2_P8 = 4;  // e4m3 P: P = 2^(x - m_ref + 4) <= 256 < 448 (e4m3 maximum)
 #ifndef EXP_POLY_EVERY
 #define EXP_POLY_EVERY 1000  // pairs c with c % EXP_POLY_EVERY == EXP_POLY_EVERY - 1 use the FMA-pipe exp2 (off: MUFU is not the limit)
 #endif
@@ -47,6 +48,7 @@ struct AttnArgs {
   float scale_log2, lam_log2;
   unsigned long long *stats;
   int *status;
+  const float *sq, *sk, *sv;  // 8-bit path: scales of the Q blocks, K blocks and V channels
 };
 
 // Warp-collective walk over the kept, valid key blocks of one mask row in ascending order, run
@@ -86,16 +88,24 @@ struct KeptScan {
   }
 };
 
-template <int D, int KST, int VST>
+// Operand precisions: Q.K^T on bf16 or e4m3 (QK8) operands, P.V on f16 or e4m3 (PV8) operands.
+// Shared memory of one CTA.  Q and K tiles are rows of D elements in 128-byte chunks (bf16: D / 64
+// chunks; e4m3: one chunk for D = 128).  A V tile is 64 keys x D channels, either key-major f16
+// (MN-major operand, 128-byte chunks of 64 channels) or channel-major e4m3 with 64-byte rows
+// (K-major operand, 64-byte swizzle).
+template <int D, int KST, int VST, bool QK8, bool PV8>
 struct Smem {
-  static constexpr int QCH = D / 64;                     // 64-column chunks of a row
+  static constexpr int EB = QK8 ? 1 : 2;                 // bytes per element of Q and K
+  static constexpr int QCH = D * EB / 128;               // 128-byte chunks of a Q or K row
+  static constexpr int VCH = D * (PV8 ? 1 : 2) / 128;    // 128 bytes of V row data per chunk
   static constexpr uint32_t Q_BYTES = QCH * 128 * 128;   // 128 rows x 128 B per chunk
   static constexpr uint32_t KV_CHUNK = 64 * 128;         // 64 rows x 128 B
-  static constexpr uint32_t T_BYTES = QCH * KV_CHUNK;    // one K (or V) tile
+  static constexpr uint32_t K_BYTES = QCH * KV_CHUNK;    // one K tile
+  static constexpr uint32_t V_BYTES = VCH * KV_CHUNK;    // one V tile
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = Q_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + KST * T_BYTES;
-  static constexpr uint32_t OFF_CTRL = OFF_V + VST * T_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + KST * K_BYTES;
+  static constexpr uint32_t OFF_CTRL = OFF_V + VST * V_BYTES;
   static constexpr uint32_t CTRL_BYTES = 512;
   static constexpr uint32_t TOTAL = OFF_CTRL + CTRL_BYTES;
 };
@@ -121,11 +131,12 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= 512, "control block");
 
-template <int D, int KST, int VST>
+template <int D, int KST, int VST, bool QK8, bool PV8>
 __global__ void __launch_bounds__(NTHREADS, 2)
     bsattn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const AttnArgs a) {
-  using L = Smem<D, KST, VST>;
+  using L = Smem<D, KST, VST, QK8, PV8>;
+  static_assert((!QK8 && !PV8) || D == 128, "the 8-bit operands cover d = 128");
   extern __shared__ __align__(1024) uint8_t smem[];
   // the 128-byte swizzle of TMA and of the MMA descriptors assumes 1024-byte aligned tiles
   if (smem_u32(smem) & 1023u) {
@@ -149,8 +160,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 
   constexpr int SCOL0 = (D == 128) ? 128 : 64;
   constexpr uint32_t TMEM_COLS = 256;
-  constexpr uint32_t IDESC_S = idesc_f32acc(128, 64, FMT_BF16, false);
-  constexpr uint32_t IDESC_PV = idesc_f32acc(128, D, FMT_F16, true);
+  constexpr uint32_t IDESC_S = QK8 ? idesc_f32acc(128, 64, FMT_E4M3, false) : idesc_f32acc(128, 64, FMT_BF16, false);
+  constexpr uint32_t IDESC_PV = PV8 ? idesc_f32acc(128, D, FMT_E4M3, false) : idesc_f32acc(128, D, FMT_F16, true);
+  constexpr int KSTEPS = D * L::EB / 32;  // 32 bytes of the contraction per MMA: K = 16 (bf16) or 32 (e4m3)
 
   if (threadIdx.x == 0) {
     mbar_init(&cs.q_full, 1);
@@ -217,12 +229,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           if (t == 0) {
             mbar_arrive_expect_tx(&cs.q_full, L::Q_BYTES);
             for (int c = 0; c < L::QCH; ++c)
-              tma_load_4d(smem + L::OFF_Q + c * 16384, &tq, &cs.q_full, 64 * c, QBLK * i, h, b);
+              tma_load_4d(smem + L::OFF_Q + c * 16384, &tq, &cs.q_full, (128 / L::EB) * c, QBLK * i, h, b);
           }
-          uint8_t *kdst = smem + L::OFF_K + kst * L::T_BYTES;
-          mbar_arrive_expect_tx(&cs.k_full[kst], L::T_BYTES);
+          uint8_t *kdst = smem + L::OFF_K + kst * L::K_BYTES;
+          mbar_arrive_expect_tx(&cs.k_full[kst], L::K_BYTES);
           for (int c = 0; c < L::QCH; ++c)
-            tma_load_4d(kdst + c * L::KV_CHUNK, &tk, &cs.k_full[kst], 64 * c, KBLK * j, kvh, b);
+            tma_load_4d(kdst + c * L::KV_CHUNK, &tk, &cs.k_full[kst], (128 / L::EB) * c, KBLK * j, kvh, b);
         } else {
           mbar_arrive(&cs.k_full[kst]);
         }
@@ -232,10 +244,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         const int u = t - 1, vst = u % VST;
         if (!mbar_wait(&cs.v_empty[vst], ((u / VST) & 1) ^ 1, abort, a.status)) break;
         if (lane == 0) {
-          uint8_t *vdst = smem + L::OFF_V + vst * L::T_BYTES;
-          mbar_arrive_expect_tx(&cs.v_full[vst], L::T_BYTES);
-          for (int c = 0; c < L::QCH; ++c)
-            tma_load_4d(vdst + c * L::KV_CHUNK, &tv, &cs.v_full[vst], 64 * c, KBLK * jprev, kvh, b);
+          uint8_t *vdst = smem + L::OFF_V + vst * L::V_BYTES;
+          mbar_arrive_expect_tx(&cs.v_full[vst], L::V_BYTES);
+          if constexpr (PV8) {
+            tma_load_4d(vdst, &tv, &cs.v_full[vst], KBLK * jprev, 0, kvh, b);  // [D channels][64 keys]
+          } else {
+            for (int c = 0; c < L::VCH; ++c)
+              tma_load_4d(vdst + c * L::KV_CHUNK, &tv, &cs.v_full[vst], 64 * c, KBLK * jprev, kvh, b);
+          }
         }
         __syncwarp();
       }
@@ -259,13 +275,16 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     };
     auto issue_s = [&](int u) {
       if (lane == 0) {
-        const uint32_t kaddr = sK + (u % KST) * L::T_BYTES;
+        const uint32_t kaddr = sK + (u % KST) * L::K_BYTES;
         const uint32_t dS = tmem + SCOL0 + (u & 1) * 64;
 #pragma unroll
-        for (int s = 0; s < D / 16; ++s) {
+        for (int s = 0; s < KSTEPS; ++s) {
           const uint64_t da = smem_desc_sw128(sQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
           const uint64_t db = smem_desc_sw128(kaddr + (s >> 2) * L::KV_CHUNK + (s & 3) * 32, 16, 1024);
-          mma_bf16_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
+          if constexpr (QK8)
+            mma_f8_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
+          else
+            mma_bf16_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
         }
         mma_commit(&cs.s_full[u & 1]);
         mma_commit(&cs.k_empty[u % KST]);  // the K stage is free once this product completes
@@ -287,12 +306,21 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         const bool all_skip = cs.skip[t & 1][0] && cs.skip[t & 1][1] && cs.skip[t & 1][2] && cs.skip[t & 1][3];
         if (lane == 0) {
           if (!all_skip) {
-            const uint32_t vaddr = sV + vst * L::T_BYTES;
+            const uint32_t vaddr = sV + vst * L::V_BYTES;
             const uint32_t aP = tmem + SCOL0 + (t & 1) * 64;
+            if constexpr (PV8) {
+              // P: 4 e4m3 per TMEM column, 8 columns per 32 keys; V tile rows of 64 keys
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              const uint64_t db = smem_desc_sw128(vaddr + s * 2048, L::KV_CHUNK, 1024);
-              mma_bf16_ts(tmem, aP + s * 8, db, IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
+              for (int s = 0; s < 2; ++s) {
+                const uint64_t db = smem_desc_sw64(vaddr + s * 32, 512);
+                mma_f8_ts(tmem, aP + s * 8, db, IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
+              }
+            } else {
+#pragma unroll
+              for (int s = 0; s < 4; ++s) {
+                const uint64_t db = smem_desc_sw128(vaddr + s * 2048, L::KV_CHUNK, 1024);
+                mma_bf16_ts(tmem, aP + s * 8, db, IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
+              }
             }
             pv_issued = 1;
             ++pv_count;
@@ -330,6 +358,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
     int nskip = 0, T = 0;
     bool ok = true;
+    constexpr float RESC = static_cast<float>(PV8 ? RESCALE_LOG2_P8 : RESCALE_LOG2);
+    constexpr float POFF = PV8 ? static_cast<float>(8 - RESCALE_LOG2_P8) : 0.f;  // exponent offset of P
+    float sq_blk = 1.f;
+    const float *skrow = nullptr;
+    if constexpr (QK8) {
+      sq_blk = a.sq[(static_cast<int64_t>(b) * a.Hq + h) * a.nqb + i];
+      skrow = a.sk + (static_cast<int64_t>(b) * a.Hkv + kvh) * a.nkb;
+    }
     for (int t = 0;; ++t) {
       const int js = t % JRING;
       if (!mbar_wait(&cs.j_full[js], (t / JRING) & 1, abort, a.status)) {
@@ -374,11 +410,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
       for (int c = 3; c < 63; c += 2) mraw = fmax3(mraw, x[c], x[c + 1]);
       mraw = fmaxf(mraw, x[63]);
-      const float mloc = mraw * a.scale_log2;  // the scale is positive: max commutes with it
+      // score multiplier of this tile (8-bit path: times the Q block and K block scales)
+      const float tsc = QK8 ? a.scale_log2 * sq_blk * __ldg(skrow + j) : a.scale_log2;
+      const float mloc = mraw * tsc;  // the multiplier is positive: max commutes with it
       const float m_new = fmaxf(m_run, mloc);
       const bool trailing = !row_ok || mloc == -INFINITY || m_new == -INFINITY || (mloc - m_new < a.lam_log2);
       const bool wskip = __all_sync(0xffffffffu, trailing);
-      const bool resc = m_new > m_ref + static_cast<float>(RESCALE_LOG2);
+      const bool resc = m_new > m_ref + RESC;
       const float alpha = resc ? fast_exp2(m_ref - m_new) : 1.f;
       if (__any_sync(0xffffffffu, resc) && t > 0) {
         // O must hold P_{t-1} V_{t-1} before it is rescaled
@@ -413,8 +451,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       m_run = m_new;
       l *= alpha;
       // P = 2^(x * scale_log2 - m_ref); a row whose reference is still -inf has only hidden columns
-      const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nr2 = make_float2(nref, nref);
+      const float nref = (m_ref == -INFINITY) ? 0.f : POFF - m_ref;
+      const float2 sc2 = make_float2(tsc, tsc), nr2 = make_float2(nref, nref);
       float2 rs2 = make_float2(0.f, 0.f);
       uint32_t pk[32];
 #pragma unroll
@@ -424,10 +462,15 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         const float2 p2 = (c % EXP_POLY_EVERY == EXP_POLY_EVERY - 1) ? exp2_poly2(e2)
                                                                       : make_float2(fast_exp2(e2.x), fast_exp2(e2.y));
         rs2 = fadd2(rs2, p2);
-        pk[c] = pack_f16x2(p2.x, p2.y);
+        pk[c] = PV8 ? pack_e4m3x2(p2.x, p2.y) : pack_f16x2(p2.x, p2.y);
       }
       l += rs2.x + rs2.y;
-      {
+      if constexpr (PV8) {
+        uint32_t w[16];  // 4 e4m3 per column, keys in order
+#pragma unroll
+        for (int c = 0; c < 16; ++c) w[c] = wskip ? 0u : (pk[2 * c] | (pk[2 * c + 1] << 16));
+        tmem_st16(sc, w);
+      } else {
         uint32_t lo[16], hi[16];
         if (wskip) {
 #pragma unroll
@@ -456,6 +499,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       have_o = ok && cs.pv_any != 0;
     }
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    const float *svrow = PV8 ? a.sv + (static_cast<int64_t>(b) * a.Hkv + kvh) * D : nullptr;
     __nv_bfloat16 *orow = a.o + b * a.o_sb + h * a.o_sh + static_cast<int64_t>(row_g) * a.o_sn;
 #pragma unroll 1
     for (int q = 0; q < D / 16; ++q) {
@@ -466,6 +510,16 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       } else {
 #pragma unroll
         for (int c = 0; c < 16; ++c) rr[c] = 0u;
+      }
+      if constexpr (PV8) {  // undo the per-channel V scale
+#pragma unroll
+        for (int c = 0; c < 16; c += 4) {
+          const float4 s4 = __ldg(reinterpret_cast<const float4 *>(svrow + 16 * q + c));
+          rr[c] = __float_as_uint(__uint_as_float(rr[c]) * s4.x);
+          rr[c + 1] = __float_as_uint(__uint_as_float(rr[c + 1]) * s4.y);
+          rr[c + 2] = __float_as_uint(__uint_as_float(rr[c + 2]) * s4.z);
+          rr[c + 3] = __float_as_uint(__uint_as_float(rr[c + 3]) * s4.w);
+        }
       }
       uint4 o0, o1;
       o0.x = pack_bf16x2(__uint_as_float(rr[0]) * inv_l, __uint_as_float(rr[1]) * inv_l);
@@ -490,18 +544,18 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int D, int KST, int VST>
+template <int D, int KST, int VST, bool QK8, bool PV8>
 cudaError_t launch_t(const AttnLaunch &l, const AttnArgs &a, cudaStream_t st) {
-  const uint32_t smem = Smem<D, KST, VST>::TOTAL;
+  const uint32_t smem = Smem<D, KST, VST, QK8, PV8>::TOTAL;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bsattn_kernel<D, KST, VST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(bsattn_kernel<D, KST, VST, QK8, PV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int64_t grid = static_cast<int64_t>(a.B) * a.Hq * a.nqb;
-  bsattn_kernel<D, KST, VST><<<static_cast<unsigned>(grid), NTHREADS, smem, st>>>(l.tq, l.tk, l.tv, a);
+  bsattn_kernel<D, KST, VST, QK8, PV8><<<static_cast<unsigned>(grid), NTHREADS, smem, st>>>(l.tq, l.tk, l.tv, a);
   return cudaGetLastError();
 }
 
@@ -521,8 +575,14 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
   a.lam_log2 = (l.lambda == -INFINITY) ? -INFINITY : l.lambda * LOG2E;
   a.stats = l.stats;
   a.status = l.status;
+  a.sq = l.sq;
+  a.sk = l.sk;
+  a.sv = l.sv;
   if (static_cast<int64_t>(a.B) * a.Hq * a.nqb == 0) return cudaSuccess;
-  return l.d == 128 ? launch_t<128, 3, 2>(l, a, st) : launch_t<64, 4, 3>(l, a, st);
+  if (l.q8 != 0 && l.d != 128) return cudaErrorInvalidValue;
+  if (l.q8 == 2) return launch_t<128, 4, 3, true, true>(l, a, st);
+  if (l.q8 == 1) return launch_t<128, 4, 2, true, false>(l, a, st);
+  return l.d == 128 ? launch_t<128, 3, 2, false, false>(l, a, st) : launch_t<64, 4, 3, false, false>(l, a, st);
 }
 
 }  // namespace sparge

@@ -71,11 +71,32 @@ struct AttnLaunch {
   float lambda;
   unsigned long long *stats;
   int *status;
+  int q8;                  // 0: bf16 Q.K^T, f16 P.V; 1: e4m3 Q.K^T (maps over the e4m3 copies, scales sq, sk),
+                           // f16 P.V; 2: as 1 with e4m3 P.V (channel-major e4m3 V, scales sv)
+  const float *sq, *sk, *sv;
 };
 
 cudaError_t launch_bsattn(const AttnLaunch &a, cudaStream_t st);
 
 cudaError_t launch_convert_v_f16(const View &v, void *v16, cudaStream_t st);
+
+// 8-bit path: e4m3 copies of Q, K - mean(K) and V with their scales (all contiguous).
+struct Q8Ws {
+  uint8_t *q8;      // [B][Hq][N][d]
+  uint8_t *k8;      // [B][Hkv][N][d]
+  uint8_t *v8;      // e4m3 P.V: [B][Hkv][d][npad] channel-major, npad = N rounded up to 64 (tail zero);
+                    // f16 P.V: the f16 copy of V, [B][Hkv][N][d]
+  float *sq;        // [B][Hq][nqb]   per 128-token query block
+  float *sk;        // [B][Hkv][nkb]  per 64-token key block
+  float *kmean;     // [B][Hkv][d]
+  float *sv;        // [B][Hkv][d]    per channel
+  float *partial;   // [B*Hkv][chunks][2][d]
+};
+size_t q8_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
+Q8Ws q8_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
+// K mean, V channel scales, e4m3 Q and K - mean with their block scales; with quant_v also the
+// channel-major e4m3 V (otherwise v8 is left to the caller).
+cudaError_t launch_q8_prep(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v, cudaStream_t st);
 
 cudaError_t launch_permute(const View &x, const int32_t *perm, void *y, int64_t ysb, int64_t ysh, int64_t ysn,
                            bool inverse, cudaStream_t st);

@@ -1,0 +1,238 @@
+// Quantisation for the 8-bit attention path (SpargeAttention overview page: SpargeAttn builds on
+// SageAttention's 8-bit quantisation and outlier smoothing; abstract: "sparse and quantized
+// attention").
+//
+//   K is smoothed by its per-(batch, KV head) token mean, K~ = K - mean_t K (a per-row constant
+//   shift of the scores, which the row softmax ignores), then Q and K~ are quantised to FP8 e4m3
+//   with one scale per 128-token query block and per 64-token key block (scale = max|x| / 448,
+//   round to nearest even, saturating); V is quantised to e4m3 with one scale per channel
+//   (max over the head's tokens), stored channel-major.  INT8 tensor-core products (tcgen05 kind::i8) are not available
+//   on sm_103a, so Q.K^T also runs in e4m3 (kind::f8f6f4).
+//
+// Kernels: per-chunk partial sums of K and maxima of |V| per (batch, KV head, channel); their
+// reduction into the K mean and the V scales; one warp per query / key block for Q and K~
+// (block maximum, then quantise); a tiled transpose for V.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sparge {
+namespace {
+
+constexpr int CHUNK = 2048;    // tokens per partial of the K mean / V maximum
+constexpr float E4M3_MAX = 448.f;
+
+// grid (B*Hkv, chunks); 256 threads: 16 lanes per token (d = 128) or 8 (d = 64), 8 dims per lane
+template <int D>
+__global__ void __launch_bounds__(256) kv_partials_kernel(const __nv_bfloat16 *k, int64_t ksb, int64_t ksh,
+                                                          int64_t ksn, const __nv_bfloat16 *v, int64_t vsb,
+                                                          int64_t vsh, int64_t vsn, int Hkv, int N,
+                                                          float *part) {
+  constexpr int LPT = D / 8, TPW = 32 / LPT, TPS = 8 * TPW;
+  __shared__ float red[8][2][D];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane / LPT, p = lane % LPT;
+  const int bh = blockIdx.x, b = bh / Hkv, h = bh % Hkv;
+  const int t0 = blockIdx.y * CHUNK, t1 = min(N, t0 + CHUNK);
+  float s[8], mx[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) s[c] = mx[c] = 0.f;
+  for (int t = t0 + w * TPW + sub; t < t1; t += TPS) {
+    const uint4 kv = ld_stream_v4(k + b * ksb + h * ksh + static_cast<int64_t>(t) * ksn + p * 8);
+    const uint4 vv = ld_stream_v4(v + b * vsb + h * vsh + static_cast<int64_t>(t) * vsn + p * 8);
+    const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      s[2 * c] += bf16lo(kw[c]);
+      s[2 * c + 1] += bf16hi(kw[c]);
+      mx[2 * c] = fmaxf(mx[2 * c], fabsf(bf16lo(vw[c])));
+      mx[2 * c + 1] = fmaxf(mx[2 * c + 1], fabsf(bf16hi(vw[c])));
+    }
+  }
+#pragma unroll
+  for (int off = LPT; off < 32; off <<= 1)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      s[c] += __shfl_xor_sync(0xffffffffu, s[c], off);
+      mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
+    }
+  if (sub == 0)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      red[w][0][p * 8 + c] = s[c];
+      red[w][1][p * 8 + c] = mx[c];
+    }
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float ss = 0.f, mm = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < 8; ++ww) {
+      ss += red[ww][0][threadIdx.x];
+      mm = fmaxf(mm, red[ww][1][threadIdx.x]);
+    }
+    float *dst = part + (static_cast<int64_t>(bh) * gridDim.y + blockIdx.y) * 2 * D;
+    dst[threadIdx.x] = ss;
+    dst[D + threadIdx.x] = mm;
+  }
+}
+
+// grid B*Hkv, D threads: K mean and V scale per channel
+template <int D>
+__global__ void kv_finish_kernel(const float *part, int nchunks, int N, float *kmean, float *sv) {
+  const int bh = blockIdx.x, c = threadIdx.x;
+  float ss = 0.f, mm = 0.f;
+  for (int k = 0; k < nchunks; ++k) {
+    const float *src = part + (static_cast<int64_t>(bh) * nchunks + k) * 2 * D;
+    ss += src[c];
+    mm = fmaxf(mm, src[D + c]);
+  }
+  kmean[static_cast<int64_t>(bh) * D + c] = ss / static_cast<float>(N);
+  sv[static_cast<int64_t>(bh) * D + c] = mm > 0.f ? mm / E4M3_MAX : 1.f;
+}
+
+// One warp per block of `blk` tokens: x (minus the per-channel mean when given) -> e4m3 with one
+// scale for the block.  out is contiguous [B][H][N][D] bytes; scale[(b H + h) nblk + blockidx].
+template <int D>
+__global__ void __launch_bounds__(256) quant_block_kernel(const __nv_bfloat16 *x, int64_t sb, int64_t sh,
+                                                          int64_t sn, int H, int N, int blk, int nblk,
+                                                          const float *mean, uint8_t *out, float *scale,
+                                                          int64_t nblocks) {
+  constexpr int LPT = D / 8, TPW = 32 / LPT;
+  const int lane = threadIdx.x & 31, sub = lane / LPT, p = lane % LPT;
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (wid >= nblocks) return;
+  const int bi = static_cast<int>(wid % nblk);
+  const int64_t bh = wid / nblk;
+  const int h = static_cast<int>(bh % H), b = static_cast<int>(bh / H);
+  const int t0 = bi * blk, t1 = min(N, t0 + blk);
+  float mu[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) mu[c] = mean ? mean[bh * D + p * 8 + c] : 0.f;
+  const __nv_bfloat16 *base = x + b * sb + h * sh;
+  float m = 0.f;
+  for (int t = t0 + sub; t < t1; t += TPW) {
+    const uint4 v = ld_stream_v4(base + static_cast<int64_t>(t) * sn + p * 8);
+    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      m = fmaxf(m, fmaxf(fabsf(bf16lo(wd[c]) - mu[2 * c]), fabsf(bf16hi(wd[c]) - mu[2 * c + 1])));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const float s = m > 0.f ? m / E4M3_MAX : 1.f;
+  const float inv = 1.f / s;
+  if (lane == 0) scale[wid] = s;
+  uint8_t *obase = out + (static_cast<int64_t>(b) * H + h) * static_cast<int64_t>(N) * D;
+  for (int t = t0 + sub; t < t1; t += TPW) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(base + static_cast<int64_t>(t) * sn + p * 8);
+    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      f[2 * c] = (bf16lo(wd[c]) - mu[2 * c]) * inv;
+      f[2 * c + 1] = (bf16hi(wd[c]) - mu[2 * c + 1]) * inv;
+    }
+    uint2 o;
+    o.x = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+    o.y = pack_e4m3x4(f[4], f[5], f[6], f[7]);
+    *reinterpret_cast<uint2 *>(obase + static_cast<int64_t>(t) * D + p * 8) = o;
+  }
+}
+
+// V -> e4m3 with a scale per (batch, KV head, channel), written channel-major: out is
+// [B][Hkv][D][npad] bytes (npad = N rounded up to 64, the tail zero), so that a 64-key tile is a
+// K-major operand of P.V.  grid (B*Hkv, npad / 64), 256 threads; each CTA transposes one tile of
+// 64 keys through shared memory.
+template <int D>
+__global__ void __launch_bounds__(256) quant_vt_kernel(const __nv_bfloat16 *v, int64_t sb, int64_t sh, int64_t sn,
+                                                       int H, int N, int npad, const float *sv, uint8_t *out) {
+  constexpr int VPR = D / 8;  // 16-byte input vectors per token
+  __shared__ __align__(16) uint8_t tile[D][64];
+  const int bh = blockIdx.x, b = bh / H, h = bh % H;
+  const int t0 = blockIdx.y * 64;
+  const __nv_bfloat16 *base = v + b * sb + h * sh;
+  for (int e = threadIdx.x; e < 64 * VPR; e += blockDim.x) {
+    const int tt = e / VPR, p = e % VPR, t = t0 + tt;
+    uint8_t q[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (t < N) {
+      const uint4 x = ld_stream_v4(base + static_cast<int64_t>(t) * sn + p * 8);
+      const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+      const float *s = sv + static_cast<int64_t>(bh) * D + p * 8;
+      const uint32_t w0 = pack_e4m3x4(bf16lo(wd[0]) / s[0], bf16hi(wd[0]) / s[1], bf16lo(wd[1]) / s[2],
+                                      bf16hi(wd[1]) / s[3]);
+      const uint32_t w1 = pack_e4m3x4(bf16lo(wd[2]) / s[4], bf16hi(wd[2]) / s[5], bf16lo(wd[3]) / s[6],
+                                      bf16hi(wd[3]) / s[7]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        q[c] = static_cast<uint8_t>(w0 >> (8 * c));
+        q[4 + c] = static_cast<uint8_t>(w1 >> (8 * c));
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) tile[p * 8 + c][tt] = q[c];
+  }
+  __syncthreads();
+  uint8_t *obase = out + static_cast<int64_t>(bh) * D * npad + t0;
+  for (int e = threadIdx.x; e < D * 4; e += blockDim.x) {
+    const int ch = e >> 2, part = e & 3;
+    *reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(ch) * npad + 16 * part) =
+        *reinterpret_cast<const uint4 *>(&tile[ch][16 * part]);
+  }
+}
+
+template <int D>
+cudaError_t run(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v, cudaStream_t st) {
+  const int B = static_cast<int>(q.B), Hq = static_cast<int>(q.H), Hkv = static_cast<int>(k.H);
+  const int N = static_cast<int>(q.N);
+  const int nchunks = (N + CHUNK - 1) / CHUNK;
+  kv_partials_kernel<D><<<dim3(B * Hkv, nchunks), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16 *>(k.data), k.sb, k.sh, k.sn, static_cast<const __nv_bfloat16 *>(v.data),
+      v.sb, v.sh, v.sn, Hkv, N, w.partial);
+  kv_finish_kernel<D><<<B * Hkv, D, 0, st>>>(w.partial, nchunks, N, w.kmean, w.sv);
+  const int nqb = (N + QBLK - 1) / QBLK, nkb = (N + KBLK - 1) / KBLK;
+  const int64_t nq = static_cast<int64_t>(B) * Hq * nqb, nk = static_cast<int64_t>(B) * Hkv * nkb;
+  quant_block_kernel<D><<<static_cast<unsigned>((nq + 7) / 8), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16 *>(q.data), q.sb, q.sh, q.sn, Hq, N, QBLK, nqb, nullptr, w.q8, w.sq, nq);
+  quant_block_kernel<D><<<static_cast<unsigned>((nk + 7) / 8), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16 *>(k.data), k.sb, k.sh, k.sn, Hkv, N, KBLK, nkb, w.kmean, w.k8, w.sk, nk);
+  const int npad = (N + 63) / 64 * 64;
+  if (quant_v)
+    quant_vt_kernel<D><<<dim3(B * Hkv, npad / 64), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(v.data), v.sb, v.sh,
+                                                              v.sn, Hkv, N, npad, w.sv, w.v8);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t q8_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const int64_t nqb = (N + QBLK - 1) / QBLK, nkb = (N + KBLK - 1) / KBLK, nch = (N + CHUNK - 1) / CHUNK;
+  const int64_t npad = (N + 63) / 64 * 64;
+  const int64_t vbytes = std::max(B * Hkv * d * npad, 2 * B * Hkv * N * d);  // e4m3 V^T or the f16 copy
+  return al(B * Hq * N * d) + al(B * Hkv * N * d) + al(vbytes) + al(4 * B * Hq * nqb) + al(4 * B * Hkv * nkb) +
+         2 * al(4 * B * Hkv * d) + al(4 * B * Hkv * nch * 2 * d);
+}
+
+Q8Ws q8_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const int64_t nqb = (N + QBLK - 1) / QBLK, nkb = (N + KBLK - 1) / KBLK;
+  const int64_t npad = (N + 63) / 64 * 64;
+  char *p = static_cast<char *>(ws);
+  Q8Ws w;
+  w.q8 = reinterpret_cast<uint8_t *>(p); p += al(B * Hq * N * d);
+  w.k8 = reinterpret_cast<uint8_t *>(p); p += al(B * Hkv * N * d);
+  w.v8 = reinterpret_cast<uint8_t *>(p); p += al(std::max(B * Hkv * d * npad, 2 * B * Hkv * N * d));
+  w.sq = reinterpret_cast<float *>(p); p += al(4 * B * Hq * nqb);
+  w.sk = reinterpret_cast<float *>(p); p += al(4 * B * Hkv * nkb);
+  w.kmean = reinterpret_cast<float *>(p); p += al(4 * B * Hkv * d);
+  w.sv = reinterpret_cast<float *>(p); p += al(4 * B * Hkv * d);
+  w.partial = reinterpret_cast<float *>(p);
+  return w;
+}
+
+cudaError_t launch_q8_prep(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v, cudaStream_t st) {
+  if (q.B * q.N == 0) return cudaSuccess;
+  return q.d == 128 ? run<128>(q, k, v, w, quant_v, st) : run<64>(q, k, v, w, quant_v, st);
+}
+
+}  // namespace sparge

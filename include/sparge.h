@@ -53,13 +53,16 @@ enum sparge_dtype { SPARGE_BF16 = 1 };
 
 enum sparge_precision {
   SPARGE_PRECISION_BF16 = 0,          /* bf16 tensor-core products, fp32 accumulation */
-  SPARGE_PRECISION_Q8 = 1             /* 8-bit path (reserved; currently SPARGE_ERR_UNSUPPORTED) */
+  SPARGE_PRECISION_Q8 = 1,            /* 8-bit Q.K^T (e4m3, K smoothed), f16 P.V; d = 128 */
+  SPARGE_PRECISION_Q8_FP8PV = 2       /* 8-bit Q.K^T and P.V (both e4m3); d = 128 */
 };
 
 enum sparge_op {
   SPARGE_OP_PREDICT_MASK = 1,
   SPARGE_OP_BLOCK_SPARSE_ATTN = 2,
-  SPARGE_OP_ATTN = 3
+  SPARGE_OP_ATTN = 3,
+  SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 = 4, /* sparge_block_sparse_attn with an 8-bit precision */
+  SPARGE_OP_ATTN_Q8 = 5               /* sparge_attn_ex with an 8-bit precision */
 };
 
 /* A strided bf16 tensor of logical shape (B, H, N, d); data is a device pointer. */
@@ -83,7 +86,7 @@ typedef struct sparge_params {
   unsigned long long *stats;    /* optional device pointer to 4 counters, or NULL */
   void *const *timing_events;   /* optional: 6 cudaEvent_t handles recorded on the stream before the
                                    pooling kernel and after the pooling, pooled-score, selection,
-                                   V-copy and attention kernels (for per-kernel timing), or NULL */
+                                   V-copy (8-bit path: quantisation) and attention kernels (for per-kernel timing), or NULL */
 } sparge_params;
 
 /*
@@ -91,6 +94,10 @@ typedef struct sparge_params {
  * SPARGE_OP_PREDICT_MASK: pooled means and similarities (fp32).
  * SPARGE_OP_BLOCK_SPARSE_ATTN: an f16 copy of V.
  * SPARGE_OP_ATTN: all of the above plus the uint8 mask.
+ * SPARGE_OP_BLOCK_SPARSE_ATTN_Q8: e4m3 copies of Q and K - mean(K), room for either V copy (f16,
+ *   or e4m3 channel-major with the keys padded to a multiple of 64) and the fp32 scales;
+ *   SPARGE_OP_ATTN_Q8: that plus the mask-prediction workspace and the mask.  Both return 0
+ *   unless d = 128.
  * Returns 0 for an unknown op or an unsupported shape.
  */
 size_t sparge_workspace_bytes(int op, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
@@ -123,12 +130,23 @@ int sparge_predict_mask(const sparge_tensor *q, const sparge_tensor *k, float to
  *   than |lambda| (the running maximum and the row sum are still updated).  Rows with no
  *   visible kept key output 0.  mask may be NULL (every tile kept).  Tiles wholly above the
  *   causal diagonal are never visited, whatever the mask says.
- * lambda <= 0 or -INFINITY; precision SPARGE_PRECISION_BF16.  o: (B,Hq,N,d) bf16 output.
- * Q.K^T runs on bf16 operands; P.V runs on f16 operands (P in [0, 256], V copied to f16 into the
- * workspace first: exact for |v| <= 65504, larger magnitudes saturate), both with fp32
- * accumulation.
- * ws: 256-byte aligned device workspace of at least
+ * lambda <= 0 or -INFINITY.  o: (B,Hq,N,d) bf16 output.
+ * precision SPARGE_PRECISION_BF16: Q.K^T runs on bf16 operands; P.V runs on f16 operands (P in
+ * [0, 256], V copied to f16 into the workspace first: exact for |v| <= 65504, larger magnitudes
+ * saturate), both with fp32 accumulation.  ws: 256-byte aligned device workspace of at least
  * sparge_workspace_bytes(SPARGE_OP_BLOCK_SPARSE_ATTN, ...) bytes (the f16 copy of V).
+ * precision SPARGE_PRECISION_Q8 and SPARGE_PRECISION_Q8_FP8PV (d = 128 only, else
+ * SPARGE_ERR_UNSUPPORTED; SpargeAttention overview page: built on SageAttention's 8-bit
+ * quantisation with outlier smoothing): K is smoothed by its per-(batch, KV head) token mean (a
+ * per-row shift of the scores that the softmax ignores); Q and K - mean are quantised to FP8
+ * e4m3 with one scale per 128-token query block and per 64-token key block (scale = max|x| /
+ * 448, round to nearest even) and Q.K^T runs as e4m3 x e4m3 with fp32 accumulation.  INT8
+ * Q.K^T (tcgen05 kind::i8) is not available on sm_103a, hence e4m3, whose 3-bit mantissa
+ * leaves a larger score error than INT8 would.  SPARGE_PRECISION_Q8 keeps P.V on f16 operands
+ * as above; SPARGE_PRECISION_Q8_FP8PV also quantises V to e4m3 with one scale per channel and
+ * P to e4m3 (P <= 256) and runs P.V as e4m3 x e4m3 (faster tensor work, about twice the output
+ * error).  ws: 256-byte aligned, at least sparge_workspace_bytes(SPARGE_OP_BLOCK_SPARSE_ATTN_Q8,
+ * ...) bytes (both 8-bit precisions); it holds the quantised copies after the call.
  * stats: optional counters (see sparge_params), may be NULL.
  */
 int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k,
@@ -146,6 +164,7 @@ int sparge_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_ten
 
 /*
  * sparge_attn with every parameter explicit (theta, lambda, scale, precision, counters).
+ * ws: sparge_workspace_bytes(SPARGE_OP_ATTN, ...) bytes, or SPARGE_OP_ATTN_Q8 for the 8-bit path.
  * mask_out: optional device buffer (B,Hq,nqb,nkb) that receives the predicted mask; when
  * NULL the mask lives in the workspace.
  */

@@ -51,6 +51,12 @@ def test_workspace_bytes(lib):
     assert attn >= 2 * B * Hkv * N * d
     assert full >= pred + Hq * nqb * nkb + attn
     assert fbs.workspace_bytes(fbs.SPARGE_OP_ATTN, B, Hq, Hkv, N, 96) == 0
+    # 8-bit path: e4m3 copies of Q, K and V (V keys padded to 64) plus fp32 scales; d = 128 only
+    q8 = fbs.workspace_bytes(fbs.SPARGE_OP_BLOCK_SPARSE_ATTN_Q8, B, Hq, Hkv, N, d)
+    assert q8 >= B * (Hq + 2 * Hkv) * N * d + 4 * B * (Hq * nqb + Hkv * nkb + 2 * Hkv * d)
+    assert fbs.workspace_bytes(fbs.SPARGE_OP_ATTN_Q8, B, Hq, Hkv, N, d) >= pred + Hq * nqb * nkb + q8
+    assert fbs.workspace_bytes(fbs.SPARGE_OP_BLOCK_SPARSE_ATTN_Q8, B, Hq, Hkv, N, 64) == 0
+    assert fbs.workspace_bytes(fbs.SPARGE_OP_ATTN_Q8, B, Hq, Hkv, N, 64) == 0
 
 
 def _t(ptr=0x1000, B=1, H=2, N=256, d=64, dtype=fbs.SPARGE_BF16, sb=None, sh=None, sn=None):
