@@ -14,6 +14,7 @@ no collective on the data path); timings are reduced with a max over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -46,13 +47,16 @@ def load_peaks():
 # CPU oracle sample (reference arm and cpu_baseline)
 # ------------------------------------------------------------------------------------------------
 def _oracle_sample_job(args):
-    q_blocks, k_head, v_head, idx, N, d, topk, theta, lam, causal = args
+    q_blocks, k_head, v_head, idx, N, d, topk, theta, lam, causal, mask_rows = args
     import oracle as O
     t0 = time.perf_counter()
     rows = 0
-    for qb, i in zip(q_blocks, idx):
-        pr = O.predict_mask_row(qb, k_head, i, topk, theta, causal)
-        kept = np.nonzero(pr["mask"])[0]
+    for n, (qb, i) in enumerate(zip(q_blocks, idx)):
+        if mask_rows is None:   # predicted mask row, then attention
+            pr = O.predict_mask_row(qb, k_head, i, topk, theta, causal)
+            kept = np.nonzero(pr["mask"])[0]
+        else:                   # the workload's own mask row
+            kept = np.nonzero(mask_rows[n])[0]
         O.attn_qblock(qb, k_head, v_head, i, kept, lam, causal, O.default_scale(d))
         rows += qb.shape[0]
     return time.perf_counter() - t0, rows
@@ -75,7 +79,8 @@ def oracle_sample(w, n_blocks_sample: int, workers: int):
         if len(part) == 0:
             continue
         qbs = [W.bf16_to_f64(w.q[0, 0, i * 128:min(N, i * 128 + 128)]) for i in part]
-        jobs.append((qbs, kh, vh, list(part), N, d, w.topk, w.theta, w.lam, w.causal))
+        mrows = None if w.mask is None else [w.mask[0, 0, i] for i in part]
+        jobs.append((qbs, kh, vh, list(part), N, d, w.topk, w.theta, w.lam, w.causal, mrows))
     ctx = mp.get_context("spawn")
     t0 = time.perf_counter()
     with ctx.Pool(len(jobs)) as pool:
@@ -83,8 +88,9 @@ def oracle_sample(w, n_blocks_sample: int, workers: int):
     wall = time.perf_counter() - t0
     rows = sum(r for _, r in res)
     tops = 4.0 * rows * N * d / wall / 1e12
-    desc = ("%d query blocks (%d rows) of head 0 spread over the sequence, mask row + attention each, "
-            "%d processes x 1 BLAS thread, key/value head pooled per process" % (n_blocks_sample, rows, len(jobs)))
+    what = "mask row + attention each" if w.mask is None else "attention over the workload's mask row each"
+    desc = ("%d query blocks (%d rows) of head 0 spread over the sequence, %s, "
+            "%d processes x 1 BLAS thread, key/value head pooled per process" % (n_blocks_sample, rows, what, len(jobs)))
     return tops, wall, desc, len(jobs)
 
 
@@ -161,6 +167,35 @@ def job_value(world: int, dense_flops_per_step: float, steps: int, seconds: floa
 # ------------------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------------------
+PRECISIONS = {  # name: (C enum, dtype label, Q.K^T peak ratio to bf16, P.V peak ratio to bf16)
+    "bf16": (0, "bf16", 1.0, 1.0),
+    "q8": (1, "e4m3 Q.K^T + f16 P.V", 2.0, 1.0),
+    "fp8pv": (2, "e4m3", 2.0, 2.0),
+}
+
+
+def profile_traffic(w, precision):
+    """DRAM bytes of one full attention launch from the committed ncu capture of the same kernel
+    (4 of the 32 query heads, scaled by 8), or None when the workload differs or the kernel source
+    has changed since the capture."""
+    if w.name != "llama128k" or precision != "bf16" or (w.Hq, w.Hkv) != (32, 8):
+        return None
+    src = b"".join(open(os.path.join(ROOT, "free_block_sparse_gb300", "csrc", f), "rb").read()
+                   for f in ("bsattn.cu", "common.cuh"))
+    sha = hashlib.sha256(src).hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", "bsattn_llama128k_h4.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.startswith("- "):
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source sha256 (bsattn.cu + common.cuh)") != sha:
+        return None
+    return int(fields["traffic per full launch (bytes)"])
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import free_block_sparse_gb300 as fbs
@@ -179,14 +214,28 @@ def run_ours(args, rank, world, local_rank):
 
     q, k, v = to_dev(w.q), to_dev(w.k), to_dev(w.v)
     o = torch.empty_like(q)
-    mask = torch.empty((w.B, w.Hq, w.nqb, w.nkb), dtype=torch.uint8, device=dev)
-    ws = torch.empty(fbs.workspace_bytes(fbs.SPARGE_OP_ATTN, w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8, device=dev)
+    prec, dtype_label, r_s, r_pv = PRECISIONS[args.precision]
+    given_mask = w.mask is not None   # the custom-mask workload: the block-sparse call on its own mask
+    lam = w.lam if args.lam is None else args.lam
+    if given_mask:
+        mask = torch.from_numpy(w.mask).to(dev)
+        op = fbs.SPARGE_OP_BLOCK_SPARSE_ATTN if prec == 0 else fbs.SPARGE_OP_BLOCK_SPARSE_ATTN_Q8
+    else:
+        mask = torch.empty((w.B, w.Hq, w.nqb, w.nkb), dtype=torch.uint8, device=dev)
+        op = fbs.SPARGE_OP_ATTN if prec == 0 else fbs.SPARGE_OP_ATTN_Q8
+    ws = torch.empty(fbs.workspace_bytes(op, w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8, device=dev)
     stats = torch.zeros(4, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream()
 
+    def call(qq, kk, vv, events=None, counters=None):
+        if given_mask:
+            fbs.block_sparse_attn(qq, kk, vv, mask, lam, w.causal, out=o, ws=ws, precision=prec, stats=counters)
+        else:
+            fbs.sparge_attn_ex(qq, kk, vv, w.topk, w.causal, theta=w.theta, lam=lam, mask_out=mask, out=o, ws=ws,
+                               precision=prec, events=events, stats=counters)
+
     # one run with counters for the executed-work figures (same inputs -> same mask every step)
-    fbs.sparge_attn_ex(q, k, v, w.topk, w.causal, theta=w.theta, lam=w.lam, stats=stats, mask_out=mask,
-                       out=o, ws=ws)
+    call(q, k, v, counters=stats)
     torch.cuda.synchronize()
     kept, pv, skipped, valid = (int(x) for x in stats.cpu().tolist())
     assert fbs.device_status() == 0
@@ -194,8 +243,13 @@ def run_ours(args, rank, world, local_rank):
     ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
 
     def step(events=None):
-        fbs.sparge_attn_ex(q, k, v, w.topk, w.causal, theta=w.theta, lam=w.lam, mask_out=mask, out=o, ws=ws,
-                           events=events)
+        if given_mask and events is not None:   # the block-sparse call records no inner events
+            events[0].record(stream)
+            call(q, k, v)
+            for e in events[1:]:
+                e.record(stream)
+        else:
+            call(q, k, v, events=events)
 
     for evs in ev_sets:   # create every event once (torch creates events on first record)
         for ev in evs:
@@ -214,7 +268,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clk = clocks.stop()
     # per step: [0] before pooling, [1] after pooling, [2] after the score GEMM, [3] after selection,
-    # [4] after the V copy, [5] after attention
+    # [4] after the V copy (8-bit: quantisation), [5] after attention.  With the workload's own
+    # mask there is no prediction and [0]..[5] bracket the whole block-sparse call.
     t_pool = [e[0].elapsed_time(e[1]) / 1e3 for e in ev_sets]
     t_gemm = [e[1].elapsed_time(e[2]) / 1e3 for e in ev_sets]
     t_sel = [e[2].elapsed_time(e[3]) / 1e3 for e in ev_sets]
@@ -236,7 +291,7 @@ def run_ours(args, rank, world, local_rank):
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
-        fbs.sparge_attn_ex(dq, dk, dv, w.topk, w.causal, theta=w.theta, lam=w.lam, out=o, ws=ws, mask_out=mask)
+        call(dq, dk, dv)
         ho.copy_(o, non_blocking=True)
 
     e2e_steps = max(2, min(args.steps, 5))
@@ -259,9 +314,13 @@ def run_ours(args, rank, world, local_rank):
     tile_flops = 2.0 * 128 * 64 * w.d
     executed = (kept + pv) * tile_flops
     attn_tflops = executed / t_attn_avg / 1e12
-    peak_tc = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    peak_bf16 = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    # the peak of the executed mix: Q.K^T work at r_s x and P.V work at r_pv x the bf16 rate
+    # (e4m3 = 2 x bf16, the nominal dense ratio 4.5 / 2.25 PFLOP/s)
+    peak_tc = executed / (kept * tile_flops / (r_s * peak_bf16) + pv * tile_flops / (r_pv * peak_bf16)) \
+        if kept else peak_bf16
     pred_bytes = (w.q.nbytes + w.k.nbytes + mask.numel())
-    pred_gbs = pred_bytes / t_pred_avg / 1e9
+    pred_gbs = pred_bytes / t_pred_avg / 1e9 if t_pred_avg > 0 else 0.0
     hbm = float(peaks["hbm_gbs"])
     tag = "of measured" if peaks.get("source") == "measured" else "of fallback"
 
@@ -276,29 +335,34 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded, bf16; Llama-like rotary structure with attention sink)",
+        "dtype": dtype_label,
+        "data": "synthetic (seeded, bf16; %s)" % W.DATA_DESCRIPTIONS[w.name],
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
-                   "causal": w.causal, "topk": w.topk, "theta": w.theta, "lambda": w.lam,
+                   "causal": w.causal, "topk": w.topk, "theta": w.theta, "lambda": lam,
+                   "mask": "the workload's Bernoulli(0.25) tile mask" if given_mask else "predicted",
                    "l2": "inputs larger than L2 (Q+K+V %.2f GB), no flush" % ((w.q.nbytes + w.k.nbytes + w.v.nbytes) / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "kernels_ms": {"pool_sim": round(avg(t_pool) * 1e3, 4), "score_gemm": round(avg(t_gemm) * 1e3, 4),
-                       "score_select": round(avg(t_sel) * 1e3, 4),
-                       "convert_v_f16": round(avg(t_conv) * 1e3, 4), "bsattn": round(t_attn_avg * 1e3, 4)},
+        "kernels_ms": ({"block_sparse_call": round(avg(t_pool) * 1e3, 4)} if given_mask else
+                       {"pool_sim": round(avg(t_pool) * 1e3, 4), "score_gemm": round(avg(t_gemm) * 1e3, 4),
+                        "score_select": round(avg(t_sel) * 1e3, 4),
+                        "attn_prep": round(avg(t_conv) * 1e3, 4), "bsattn": round(t_attn_avg * 1e3, 4)}),
         "attn": {"ms": round(t_attn_avg * 1e3, 4), "dense_equiv_tops": round(dense / t_attn_avg / 1e12, 2),
                  "executed_tflops": round(attn_tflops, 2), "pct_tensor_peak": round(100 * attn_tflops / peak_tc, 2),
                  "kept_tiles": kept, "valid_tiles": valid, "sparsity": round(1 - kept / max(valid, 1), 4),
                  "pv_tiles": pv, "lambda_skipped_warp_tiles": skipped,
                  "lambda_skip_fraction": round(skipped / max(4 * kept, 1), 4)},
-        "mask_pred": {"ms": round(t_pred_avg * 1e3, 4), "gbs": round(pred_gbs, 1),
-                      "pct_hbm": round(100 * pred_gbs / hbm, 2), "bytes": pred_bytes},
-        "roofline": {"bound": "tensor", "kernel": "bsattn_kernel<128,3,2>", "achieved": round(attn_tflops, 2),
-                     "peak": peak_tc, "unit": "TFLOP/s", "frac": round(attn_tflops / peak_tc, 4),
-                     "peak_source": "bf16_tflops_sustained " + tag, "traffic": None},
+        "mask_pred": None if given_mask else {"ms": round(t_pred_avg * 1e3, 4), "gbs": round(pred_gbs, 1),
+                                              "pct_hbm": round(100 * pred_gbs / hbm, 2), "bytes": pred_bytes},
+        "roofline": {"bound": "tensor", "kernel": KERNEL_NAMES[(args.precision, w.d)], "achieved": round(attn_tflops, 2),
+                     "peak": round(peak_tc, 1), "unit": "TFLOP/s", "frac": round(attn_tflops / peak_tc, 4),
+                     "peak_source": ("bf16_tflops_sustained " + tag +
+                                     ("" if args.precision == "bf16" else
+                                      ", e4m3 products at 2x (nominal 4.5 / 2.25 PFLOP/s), weighted by the executed mix")),
+                     "traffic": profile_traffic(w, args.precision)},
         "e2e": {"value": round(world * dense / e2e_t / 1e12, 2), "unit": "dense-equiv TOPS",
                 "h2d_bytes_per_step": int(w.q.nbytes + w.k.nbytes + w.v.nbytes),
                 "d2h_bytes_per_step": int(o.numel() * 2)},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP[(args.precision, given_mask)] * args.steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -310,6 +374,15 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line))
+
+
+KERNEL_NAMES = {("bf16", 128): "bsattn_kernel<128,3,2,0,0>", ("bf16", 64): "bsattn_kernel<64,4,3,0,0>",
+                ("q8", 128): "bsattn_kernel<128,4,2,1,0>", ("fp8pv", 128): "bsattn_kernel<128,4,3,1,1>"}
+# kernels per step: prediction (pool_sim, score_gemm, score_select) unless the mask is given, then
+# the V copy (bf16) or the quantisation (K/V partial sums, their reduction, Q, K, and the V copy or
+# the V quantisation), then the attention kernel
+LAUNCHES_PER_STEP = {("bf16", False): 5, ("bf16", True): 2, ("q8", False): 9, ("q8", True): 6,
+                     ("fp8pv", False): 9, ("fp8pv", True): 6}
 
 
 def make_workload(args):
@@ -354,9 +427,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="llama128k", choices=list(W.CONFIG_NAMES))
-    ap.add_argument("--cpu-blocks", type=int, default=64)
+    ap.add_argument("--cpu-blocks", type=int, default=384)
     ap.add_argument("--cpu-workers", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--precision", default="bf16", choices=list(PRECISIONS),
+                    help="bf16, q8 (e4m3 Q.K^T, f16 P.V) or fp8pv (both products e4m3); 8-bit needs d = 128")
+    ap.add_argument("--lam", type=float, default=None, help="lambda override (default: the workload's)")
     ap.add_argument("--heads", default=None,
                     help="Hq,Hkv override (smaller cases of a workload for profiling; not a bench line)")
     args = ap.parse_args()

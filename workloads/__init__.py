@@ -189,6 +189,16 @@ def _bernoulli_mask(rng, B, H, N, p=0.25):
 # --------------------------------------------------------------------------
 CONFIG_NAMES = ("tiny", "flux", "cogvideox", "llama32k", "llama128k", "custom")
 
+# one line per workload on how its tokens are drawn (for reports)
+DATA_DESCRIPTIONS = {
+    "tiny": "per-block mean N(0,1) plus N(0,0.3) token noise",
+    "flux": "text prefix N(0,1) plus a 2-D Gaussian random field image grid with N(0,0.2) noise",
+    "cogvideox": "text prefix N(0,1) plus a 3-D smooth Gaussian field video grid with N(0,0.2) noise",
+    "llama32k": "Llama-like rotary structure with attention sink",
+    "llama128k": "Llama-like rotary structure with attention sink",
+    "custom": "i.i.d. N(0,1) Q/K/V with a Bernoulli(0.25) tile mask, diagonal tiles on",
+}
+
 
 def describe(name: str, **over) -> Workload:
     """Shape and settings of a named workload without drawing its tensors."""
