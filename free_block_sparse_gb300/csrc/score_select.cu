@@ -3,17 +3,21 @@
 // computed; overview page "Strengths": mask of shape (B, H, ceil(N/128), ceil(N/64)); Chinese
 // README quick start: topk = 0.5 keeps the top 50% of the attention weights).
 //
-// One warp per mask row, the row's valid scores in registers (lane l holds key blocks l, l+32,
-// ...; the register count per lane is chosen per row from its number of valid blocks).  With
-// e_j = exp(s_j - max) and Z = sum e_j, the kept set is the shortest prefix, in (e desc, index
-// asc) order, whose mass reaches topk * Z.  The cut is found without sorting the row: a 32-bin
-// histogram of the mass over the bit pattern of e (bins ordered by value, per-lane private
-// columns in shared memory, no shared counters) finds the bin holding the cut; that bin is split
-// again into 32 sub-bins (after the few elements inside it have been compacted into a short
-// list) until at most 32 remain, which one warp-wide bitonic sort orders exactly.  Elements more
-// than log2(n / (1 - topk)) + 0.1 below the maximum (in log2 units) never reach the cut (the
-// elements from the cut down carry more than (1 - topk) Z, so the cut value is at least
-// (1 - topk) Z / n >= (1 - topk) / n), so they stay out of the histogram.
+// One warp per mask row.  Lane l handles the key blocks 128 t + 4 l .. 128 t + 4 l + 3 of each
+// 128-block stretch t, so every global and shared access is 16 bytes per lane and the mask goes
+// out as 32-bit words.  The row lives in shared memory: pass 1 copies the scores there and takes
+// the maximum; pass 2 replaces them by e_j = exp(s_j - max), sums Z, and builds a 32-bin
+// histogram of the mass over the bit pattern of e (bins ordered by value, lane-private columns,
+// no shared counters).  With the kept set defined as the shortest prefix, in (e desc, index asc)
+// order, whose mass reaches topk * Z, the bin where the cumulative mass first reaches the target
+// holds the cut.  Its elements are compacted into a short list (ballot offsets); further 32-bin
+// levels split the list until at most 32 remain, which one warp-wide bitonic sort orders
+// exactly.  Elements more than log2(n / (1 - topk)) + 0.1 below the maximum (in log2 units) never
+// reach the cut (the elements from the cut down carry more than (1 - topk) Z, so the cut value is
+// at least (1 - topk) Z / n >= (1 - topk) / n), so they stay out of the histogram.  A bisection
+// over the whole row, with an index-ordered tie rule, covers the rare rows the levels cannot
+// split (many equal values, or rounding).  The last pass writes the mask: kept by the cut, or the
+// whole row when s_Q < theta, or the column when s_K < theta; causally hidden blocks are 0.
 #include <cfloat>
 
 #include "common.cuh"
@@ -22,7 +26,7 @@
 namespace sparge {
 namespace {
 
-constexpr int WARPS = 8;
+constexpr int WARPS = 4;
 constexpr int NBIN = 32;
 constexpr int CMAX = 256;  // crossing-bin elements compacted into the short list (8 per lane)
 
@@ -31,7 +35,7 @@ struct SelArgs {
   const float *sQ, *sK;
   uint8_t *mask;
   int64_t nkb_pad, rows;
-  int Hq, Hkv, G, nqb, nkb, causal;
+  int Hq, Hkv, G, nqb, nkb, causal, ew;  // ew: floats of a warp's row buffer (nkb rounded up to 128)
   float topk, theta;
 };
 
@@ -54,6 +58,9 @@ __device__ __forceinline__ bool in_range(float x, uint32_t lo, uint32_t hi) {
   const uint32_t u = __float_as_uint(x);
   return x > 0.f && u >= lo && u < hi;
 }
+__device__ __forceinline__ float comp(const float4 &v, int u) {
+  return u == 0 ? v.x : (u == 1 ? v.y : (u == 2 ? v.z : v.w));
+}
 
 // The search state: bit patterns [lo, hi) hold the cut (mass(e >= lo) >= target > mass(e >= hi)),
 // `above` is the mass of the elements >= hi, `nc` the number of elements in [lo, hi).
@@ -63,20 +70,25 @@ struct Cut {
   int nc, shift;
 };
 
-// One histogram level over the elements of x inside [lo, hi): 32 bins of 2^shift patterns from
-// hi - 1 down; narrows the state to the bin where the cumulative mass first reaches target.
-// Returns false (state unchanged) if rounding left no bin reaching it.
-template <int V>
-__device__ __forceinline__ bool hist_level(const float (&x)[V], float *H, int lane, float target, Cut &st) {
+__device__ __forceinline__ void hist_zero(float *H, int lane) {
 #pragma unroll
   for (int k = 0; k < NBIN; ++k) H[k * 32 + lane] = 0.f;
   __syncwarp();
-  const uint32_t top = st.hi - 1u;
-#pragma unroll
-  for (int c = 0; c < V; ++c) {
-    const uint32_t bin = (top - __float_as_uint(x[c])) >> st.shift;
-    if (in_range(x[c], st.lo, st.hi) && bin < NBIN) H[bin * 32 + lane] += x[c];  // lane-private column
-  }
+}
+// 32 bins of 2^shift patterns from hi - 1 down; lane-private column
+__device__ __forceinline__ void hist_add(float *H, int lane, float x, const Cut &st) {
+  const uint32_t bin = (st.hi - 1u - __float_as_uint(x)) >> st.shift;
+  if (in_range(x, st.lo, st.hi) && bin < NBIN) H[bin * 32 + lane] += x;
+}
+__device__ __forceinline__ void hist_add4(float *H, int lane, const float4 &v, const Cut &st) {
+  hist_add(H, lane, v.x, st);
+  hist_add(H, lane, v.y, st);
+  hist_add(H, lane, v.z, st);
+  hist_add(H, lane, v.w, st);
+}
+// Narrows the state to the bin where the cumulative mass first reaches target (st.nc is left for
+// the caller to recount).  Returns false (state unchanged) if rounding left no bin reaching it.
+__device__ __forceinline__ bool hist_pick(float *H, int lane, float target, Cut &st) {
   __syncwarp();
   float mass = 0.f;  // lane = bin
 #pragma unroll
@@ -96,237 +108,279 @@ __device__ __forceinline__ bool hist_level(const float (&x)[V], float *H, int la
   st.lo = (nhi > st.lo + width) ? nhi - width : st.lo;
   st.hi = nhi;
   st.above += __shfl_sync(0xffffffffu, cum - mass, bstar);
-  int cnt = 0;
-#pragma unroll
-  for (int c = 0; c < V; ++c) cnt += in_range(x[c], st.lo, st.hi) ? 1 : 0;
-  st.nc = warp_sum_i(cnt);
   st.shift -= 5;
   return true;
 }
 
-// Exclusive prefix over lanes of per-lane counts.
-__device__ __forceinline__ int lane_offset(int cnt, int lane) {
-  int off = cnt;
+// Appends the elements of e (4 per lane, key blocks j0 .. j0 + 3) inside [lo, hi) to the short
+// list Lv/Lj at slots n, n + 1, ... (any order; slots >= CMAX are dropped); returns the new count.
+__device__ __forceinline__ int list_append(const float4 &e, int j0, const Cut &st, float *Lv, int *Lj, int n,
+                                           int lane) {
+  bool f[4];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, off, o);
-    if (lane >= o) off += v;
+  for (int u = 0; u < 4; ++u) f[u] = in_range(comp(e, u), st.lo, st.hi);
+  if (!__any_sync(0xffffffffu, f[0] || f[1] || f[2] || f[3])) return n;
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint32_t bb = __ballot_sync(0xffffffffu, f[u]);
+    const int slot = n + __popc(bb & lt);
+    if (f[u] && slot < CMAX) {
+      Lv[slot] = comp(e, u);
+      Lj[slot] = j0 + u;
+    }
+    n += __popc(bb);
   }
-  return off - cnt;
+  return n;
 }
 
-template <int V>
-__device__ __forceinline__ void select_row(const SelArgs &a, float *H, int lane, int64_t row, int nvalid,
-                                           const float *srow, const float *sKrow) {
-  constexpr float LOG2E = 1.4426950408889634f;
-  float e[V];
-  float m = -FLT_MAX;
-#pragma unroll
-  for (int c = 0; c < V; ++c) {
-    const int j = lane + 32 * c;
-    e[c] = (j < nvalid) ? srow[j] : -FLT_MAX;
-    m = fmaxf(m, e[c]);
-  }
-  m = warp_max(m);
-  float zl = 0.f;
-#pragma unroll
-  for (int c = 0; c < V; ++c) {
-    const int j = lane + 32 * c;
-    e[c] = (j < nvalid) ? exp2f((e[c] - m) * LOG2E) : 0.f;
-    zl += e[c];
-  }
-  const float Z = warp_sum(zl);
-  const bool keep_all = a.topk >= 1.f || a.sQ[row] < a.theta;
-  bool sorted = false;  // cut found by the sort: keep e > et, or e == et with index <= jt
-  float et = 0.f, vstar = 0.f;
-  int jt = -1;
-  uint64_t tiekeep = 0;
-  if (!keep_all) {
-    const float target = a.topk * Z;
-    const float r2 = log2f(static_cast<float>(nvalid) / (1.f - a.topk)) + 0.1f;
-    Cut st;
-    st.lo = 1u;
-    st.hi = 0x3F800001u;
-    st.above = 0.f;
-    st.nc = 0x7fffffff;
-    st.shift = 16;
-    while (static_cast<float>(NBIN) * exp2f(static_cast<float>(st.shift - 23)) < r2) ++st.shift;
-    bool ok = hist_level(e, H, lane, target, st);
-    // the short list: crossing-bin elements with their key-block indices
-    float ce[CMAX / 32];
-    int cj[CMAX / 32];
-    bool compact = false;
-    if (ok && st.nc > 32 && st.nc <= CMAX) {
-      int cnt = 0;
-#pragma unroll
-      for (int c = 0; c < V; ++c) cnt += in_range(e[c], st.lo, st.hi) ? 1 : 0;
-      int off = lane_offset(cnt, lane);
-#pragma unroll
-      for (int c = 0; c < V; ++c)
-        if (in_range(e[c], st.lo, st.hi)) {
-          H[off] = e[c];
-          H[CMAX + off] = __int_as_float(lane + 32 * c);
-          ++off;
-        }
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < CMAX / 32; ++k) {
-        const int idx = lane + 32 * k;
-        ce[k] = idx < st.nc ? H[idx] : 0.f;
-        cj[k] = idx < st.nc ? __float_as_int(H[CMAX + idx]) : 0x7fffffff;
-      }
-      __syncwarp();
-      compact = true;
-      for (int lev = 0; lev < 3 && ok && st.nc > 32 && st.shift >= 0; ++lev) ok = hist_level(ce, H, lane, target, st);
-    } else {
-      for (int lev = 0; lev < 2 && ok && st.nc > 32 && st.shift >= 0; ++lev) ok = hist_level(e, H, lane, target, st);
-    }
-    if (ok && st.nc <= 32) {
-      // one candidate per lane, sorted by (e desc, index asc); the first prefix reaching target
-      float x = -1.f;
-      int xj = 0x7fffffff;
-      int cnt = 0;
-      if (compact) {
-#pragma unroll
-        for (int k = 0; k < CMAX / 32; ++k) cnt += in_range(ce[k], st.lo, st.hi) ? 1 : 0;
-      } else {
-#pragma unroll
-        for (int c = 0; c < V; ++c) cnt += in_range(e[c], st.lo, st.hi) ? 1 : 0;
-      }
-      int off = lane_offset(cnt, lane);
-      if (compact) {
-#pragma unroll
-        for (int k = 0; k < CMAX / 32; ++k)
-          if (in_range(ce[k], st.lo, st.hi)) {
-            H[off] = ce[k];
-            H[32 + off] = __int_as_float(cj[k]);
-            ++off;
-          }
-      } else {
-#pragma unroll
-        for (int c = 0; c < V; ++c)
-          if (in_range(e[c], st.lo, st.hi)) {
-            H[off] = e[c];
-            H[32 + off] = __int_as_float(lane + 32 * c);
-            ++off;
-          }
-      }
-      __syncwarp();
-      if (lane < st.nc) {
-        x = H[lane];
-        xj = __float_as_int(H[32 + lane]);
-      }
-      __syncwarp();
-#pragma unroll
-      for (int kk = 2; kk <= 32; kk <<= 1) {
-#pragma unroll
-        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-          const float oe = __shfl_xor_sync(0xffffffffu, x, jj);
-          const int oj = __shfl_xor_sync(0xffffffffu, xj, jj);
-          const bool mine_first = x > oe || (x == oe && xj < oj);
-          const bool take_first = ((lane & jj) == 0) == ((lane & kk) == 0);
-          if (mine_first != take_first) {
-            x = oe;
-            xj = oj;
-          }
-        }
-      }
-      float ps = x > 0.f ? x : 0.f;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float v = __shfl_up_sync(0xffffffffu, ps, o);
-        if (lane >= o) ps += v;
-      }
-      const uint32_t reach = __ballot_sync(0xffffffffu, lane < st.nc && st.above + ps >= target);
-      if (reach) {
-        const int kstar = __ffs(reach) - 1;
-        et = __shfl_sync(0xffffffffu, x, kstar);
-        jt = __shfl_sync(0xffffffffu, xj, kstar);
-        sorted = true;
-      }
-    }
-    if (!sorted) {
-      // bisection over every element in [lo, hi) (rare: many equal values, or rounding)
-      uint32_t lo = ok ? st.lo : 1u, hi = ok ? st.hi : 0x3F800001u;
-      while (hi - lo > 1u) {
-        const uint32_t mid = lo + ((hi - lo) >> 1);
-        const float tv = __uint_as_float(mid);
-        float part = 0.f;
-#pragma unroll
-        for (int c = 0; c < V; ++c) part += (e[c] >= tv) ? e[c] : 0.f;
-        if (warp_sum(part) >= target)
-          lo = mid;
-        else
-          hi = mid;
-      }
-      vstar = __uint_as_float(lo);
-      // elements equal to v*: keep them in ascending key-block order until the mass reaches target
-      float abovev = 0.f;
-      int nties = 0;
-#pragma unroll
-      for (int c = 0; c < V; ++c) {
-        abovev += (e[c] > vstar) ? e[c] : 0.f;
-        nties += (e[c] == vstar && (lane + 32 * c) < nvalid) ? 1 : 0;
-      }
-      nties = warp_sum_i(nties);
-      float cumv = warp_sum(abovev);
-      if (nties > 0) {
-#pragma unroll
-        for (int c = 0; c < V; ++c) {
-          uint32_t bal = __ballot_sync(0xffffffffu, e[c] == vstar && (lane + 32 * c) < nvalid);
-          while (bal != 0u && cumv < target) {
-            const int l = __ffs(bal) - 1;
-            if (lane == l) tiekeep |= (1ull << c);
-            cumv += vstar;
-            bal &= bal - 1u;
-          }
-        }
-      }
-    }
-  }
-  uint8_t *mrow = a.mask + row * a.nkb;
-#pragma unroll
-  for (int c = 0; c < V; ++c) {
-    const int j = lane + 32 * c;
-    if (j < nvalid) {
-      const bool topk_keep =
-          sorted ? (e[c] > et || (e[c] == et && j <= jt)) : (e[c] > vstar || ((tiekeep >> c) & 1ull));
-      mrow[j] = (keep_all || topk_keep || sKrow[j] < a.theta) ? 1 : 0;
-    }
-  }
-  for (int j = nvalid + lane; j < a.nkb; j += 32) mrow[j] = 0;  // causally hidden blocks
-}
-
-template <int VMAX>
 __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
-  __shared__ float hist[WARPS][NBIN * 32];  // per warp: [bin][lane]; reused for the short lists
+  extern __shared__ __align__(16) float sel_smem[];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * WARPS + w;
   if (row >= a.rows) return;
+  float *E = sel_smem + static_cast<int64_t>(w) * (a.ew + NBIN * 32 + 2 * CMAX);  // the row
+  float *H = E + a.ew;                           // histogram [bin][lane]
+  float *Lv = H + NBIN * 32;                     // short list: values
+  int *Lj = reinterpret_cast<int *>(Lv + CMAX);  // and key-block indices
+  float4 *E4 = reinterpret_cast<float4 *>(E);
+
   const int i = static_cast<int>(row % a.nqb);
   const int64_t bh = row / a.nqb;
   const int h = static_cast<int>(bh % a.Hq), b = static_cast<int>(bh / a.Hq);
   const int kvh = h / a.G;
   const int nvalid = a.causal ? min(a.nkb, 2 * i + 2) : a.nkb;
+  const int nit = (nvalid + 127) >> 7;
   const float *srow = a.S + row * a.nkb_pad;
   const float *sKrow = a.sK + (static_cast<int64_t>(b) * a.Hkv + kvh) * a.nkb_pad;
-  // the fewest registers per lane that cover this row's valid blocks
-  if (VMAX == 8 || nvalid <= 256) {
-    select_row<8>(a, hist[w], lane, row, nvalid, srow, sKrow);
-  } else if (VMAX == 16 || nvalid <= 512) {
-    select_row<(VMAX >= 16 ? 16 : 8)>(a, hist[w], lane, row, nvalid, srow, sKrow);
-  } else if (VMAX == 32 || nvalid <= 1024) {
-    select_row<(VMAX >= 32 ? 32 : 8)>(a, hist[w], lane, row, nvalid, srow, sKrow);
-  } else {
-    select_row<VMAX>(a, hist[w], lane, row, nvalid, srow, sKrow);
-  }
-}
+  constexpr float LOG2E = 1.4426950408889634f;
 
-template <int VPL>
-cudaError_t launch_t(const SelArgs &a, cudaStream_t st) {
-  const int64_t grid = (a.rows + WARPS - 1) / WARPS;
-  score_select_kernel<VPL><<<static_cast<unsigned>(grid), WARPS * 32, 0, st>>>(a);
-  return cudaGetLastError();
+  // pass 1: scores into shared memory (-FLT_MAX past the valid blocks), row maximum
+  float m = -FLT_MAX;
+  for (int t = 0; t < nit; ++t) {
+    const int j0 = 128 * t + 4 * lane;
+    float4 v = make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+    if (j0 < nvalid) {
+      v = __ldg(reinterpret_cast<const float4 *>(srow + j0));
+      if (j0 + 1 >= nvalid) v.y = -FLT_MAX;
+      if (j0 + 2 >= nvalid) v.z = -FLT_MAX;
+      if (j0 + 3 >= nvalid) v.w = -FLT_MAX;
+    }
+    E4[32 * t + lane] = v;
+    m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+  }
+  m = warp_max(m);
+
+  const bool keep_all = a.topk >= 1.f || a.sQ[row] < a.theta;
+  Cut st;
+  st.lo = 1u;
+  st.hi = 0x3F800001u;  // e <= 1: the maximum gives exactly 1
+  st.above = 0.f;
+  st.nc = 0x7fffffff;
+  st.shift = 16;
+  if (!keep_all) {
+    const float r2 = log2f(static_cast<float>(nvalid) / (1.f - a.topk)) + 0.1f;
+    while (static_cast<float>(NBIN) * exp2f(static_cast<float>(st.shift - 23)) < r2) ++st.shift;
+    hist_zero(H, lane);
+  }
+  // pass 2: e = exp(s - max) in place (0 past the valid blocks), Z, first histogram level
+  float zl = 0.f;
+  for (int t = 0; t < nit; ++t) {
+    float4 v = E4[32 * t + lane];
+    v.x = exp2f((v.x - m) * LOG2E);
+    v.y = exp2f((v.y - m) * LOG2E);
+    v.z = exp2f((v.z - m) * LOG2E);
+    v.w = exp2f((v.w - m) * LOG2E);
+    E4[32 * t + lane] = v;
+    zl += (v.x + v.y) + (v.z + v.w);
+    if (!keep_all) hist_add4(H, lane, v, st);
+  }
+  const float Z = warp_sum(zl);
+
+  // the cut: keep e > et, or e == et with index <= jt
+  float et = 2.f;
+  int jt = -1;
+  if (!keep_all) {
+    const float target = a.topk * Z;
+    bool ok = hist_pick(H, lane, target, st);
+    bool listed = false;
+    // compact the crossing bin; while it does not fit the short list, split it over the row
+    while (ok) {
+      int n = 0;
+      for (int t = 0; t < nit; ++t) n = list_append(E4[32 * t + lane], 128 * t + 4 * lane, st, Lv, Lj, n, lane);
+      st.nc = n;
+      if (n <= CMAX) {
+        listed = true;
+        break;
+      }
+      if (st.shift < 0) break;
+      hist_zero(H, lane);
+      for (int t = 0; t < nit; ++t) hist_add4(H, lane, E4[32 * t + lane], st);
+      ok = hist_pick(H, lane, target, st);
+    }
+    bool sorted = false;
+    if (listed) {
+      __syncwarp();
+      float ce[CMAX / 32];
+      int cj[CMAX / 32];
+#pragma unroll
+      for (int k = 0; k < CMAX / 32; ++k) {
+        const int idx = lane + 32 * k;
+        ce[k] = idx < st.nc ? Lv[idx] : 0.f;
+        cj[k] = idx < st.nc ? Lj[idx] : 0x7fffffff;
+      }
+      __syncwarp();
+      // split the list in registers until at most 32 candidates remain
+      while (ok && st.nc > 32 && st.shift >= 0) {
+        hist_zero(H, lane);
+#pragma unroll
+        for (int k = 0; k < CMAX / 32; ++k) hist_add(H, lane, ce[k], st);
+        ok = hist_pick(H, lane, target, st);
+        if (ok) {
+          int cnt = 0;
+#pragma unroll
+          for (int k = 0; k < CMAX / 32; ++k) cnt += in_range(ce[k], st.lo, st.hi) ? 1 : 0;
+          st.nc = warp_sum_i(cnt);
+        }
+      }
+      if (ok && st.nc <= 32) {
+        // one candidate per lane, sorted by (e desc, index asc); the first prefix reaching target
+        int n = 0;
+        const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int k = 0; k < CMAX / 32; ++k) {
+          const bool f = in_range(ce[k], st.lo, st.hi);
+          const uint32_t bb = __ballot_sync(0xffffffffu, f);
+          if (f) {
+            Lv[n + __popc(bb & lt)] = ce[k];
+            Lj[n + __popc(bb & lt)] = cj[k];
+          }
+          n += __popc(bb);
+        }
+        __syncwarp();
+        float x = -1.f;
+        int xj = 0x7fffffff;
+        if (lane < st.nc) {
+          x = Lv[lane];
+          xj = Lj[lane];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+          for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+            const float oe = __shfl_xor_sync(0xffffffffu, x, jj);
+            const int oj = __shfl_xor_sync(0xffffffffu, xj, jj);
+            const bool mine_first = x > oe || (x == oe && xj < oj);
+            const bool take_first = ((lane & jj) == 0) == ((lane & kk) == 0);
+            if (mine_first != take_first) {
+              x = oe;
+              xj = oj;
+            }
+          }
+        }
+        float ps = x > 0.f ? x : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float v = __shfl_up_sync(0xffffffffu, ps, o);
+          if (lane >= o) ps += v;
+        }
+        const uint32_t reach = __ballot_sync(0xffffffffu, lane < st.nc && st.above + ps >= target);
+        if (reach) {
+          const int kstar = __ffs(reach) - 1;
+          et = __shfl_sync(0xffffffffu, x, kstar);
+          jt = __shfl_sync(0xffffffffu, xj, kstar);
+          sorted = true;
+        }
+      }
+    }
+    if (!sorted) {
+      // bisection over the whole row for v* = the largest value with mass(e >= v*) >= target
+      uint32_t lo = 1u, hi = 0x3F800001u;
+      while (hi - lo > 1u) {
+        const uint32_t mid = lo + ((hi - lo) >> 1);
+        const float tv = __uint_as_float(mid);
+        float part = 0.f;
+        for (int t = 0; t < nit; ++t) {
+          const float4 v = E4[32 * t + lane];
+          part += (v.x >= tv ? v.x : 0.f) + (v.y >= tv ? v.y : 0.f) + (v.z >= tv ? v.z : 0.f) +
+                  (v.w >= tv ? v.w : 0.f);
+        }
+        if (warp_sum(part) >= target)
+          lo = mid;
+        else
+          hi = mid;
+      }
+      et = __uint_as_float(lo);
+      // elements equal to v* are kept in ascending key-block order until the mass reaches target
+      float above = 0.f;
+      for (int t = 0; t < nit; ++t) {
+        const float4 v = E4[32 * t + lane];
+        above += (v.x > et ? v.x : 0.f) + (v.y > et ? v.y : 0.f) + (v.z > et ? v.z : 0.f) + (v.w > et ? v.w : 0.f);
+      }
+      float cum = warp_sum(above);
+      jt = -1;
+      for (int t = 0; t < nit && cum < target; ++t) {
+        const float4 v = E4[32 * t + lane];
+        const int j0 = 128 * t + 4 * lane;
+        int mine = 0;  // ties held by this lane
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mine += (comp(v, u) == et && j0 + u < nvalid) ? 1 : 0;
+        int upto = mine;  // ties of this stretch up to and including this lane (index order)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int x = __shfl_up_sync(0xffffffffu, upto, o);
+          if (lane >= o) upto += x;
+        }
+        const int total = __shfl_sync(0xffffffffu, upto, 31);
+        // ties still needed to bring the mass to target
+        const int take = max(1, static_cast<int>(ceilf((target - cum) / et)));
+        if (take <= total) {
+          const int first = upto - mine;  // ties before this lane
+          int jsel = -1;
+          if (take > first && take <= upto) {
+            int c = first;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (comp(v, u) == et && j0 + u < nvalid && ++c == take) jsel = j0 + u;
+          }
+          jt = __reduce_max_sync(0xffffffffu, jsel);
+          cum = target;
+        } else {
+          cum += et * static_cast<float>(total);
+          jt = 128 * t + 127;  // every tie of this stretch is kept
+        }
+      }
+    }
+  }
+
+  // the mask row: 4 key blocks per lane, 32-bit stores when the rows are 4-byte aligned
+  uint8_t *mrow = a.mask + row * a.nkb;
+  const int nall = (a.nkb + 127) >> 7;
+  const bool words = (a.nkb & 3) == 0 && (reinterpret_cast<uintptr_t>(a.mask) & 3u) == 0;
+  for (int t = 0; t < nall; ++t) {
+    const int j0 = 128 * t + 4 * lane;
+    if (j0 >= a.nkb) continue;
+    uint32_t word = 0u;
+    if (j0 < nvalid) {
+      const float4 v = E4[32 * t + lane];
+      const float4 sk = __ldg(reinterpret_cast<const float4 *>(sKrow + j0));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u;
+        const float e = comp(v, u);
+        const bool keep = j < nvalid && (keep_all || e > et || (e == et && j <= jt) || comp(sk, u) < a.theta);
+        word |= (keep ? 1u : 0u) << (8 * u);
+      }
+    }
+    if (words) {
+      *reinterpret_cast<uint32_t *>(mrow + j0) = word;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (j0 + u < a.nkb) mrow[j0 + u] = static_cast<uint8_t>(word >> (8 * u));
+    }
+  }
 }
 
 }  // namespace
@@ -343,15 +397,19 @@ cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int
   a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv;
   a.nqb = (N + QBLK - 1) / QBLK;
   a.nkb = (N + KBLK - 1) / KBLK;
+  a.ew = (a.nkb + 127) / 128 * 128;
   a.causal = causal;
   a.rows = static_cast<int64_t>(B) * Hq * a.nqb;
   a.topk = topk;
   a.theta = theta;
   if (a.rows == 0) return cudaSuccess;
-  if (a.nkb <= 256) return launch_t<8>(a, st);
-  if (a.nkb <= 512) return launch_t<16>(a, st);
-  if (a.nkb <= 1024) return launch_t<32>(a, st);
-  return launch_t<64>(a, st);
+  const size_t smem = static_cast<size_t>(WARPS) * (a.ew + NBIN * 32 + 2 * CMAX) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(score_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int64_t grid = (a.rows + WARPS - 1) / WARPS;
+  score_select_kernel<<<static_cast<unsigned>(grid), WARPS * 32, smem, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace sparge

@@ -82,6 +82,25 @@ def test_mask_matches_oracle_on_decisive_rows(key):
     check_mask(w, gm)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_mask_equal_scores_keep_lowest_indices(causal):
+    """Every key block identical, so each row's pooled scores are all equal: the cut falls among
+    ties, which the (probability desc, index asc) order resolves to the lowest indices.  300 key
+    blocks make rows with up to 32, up to 256 and more than 256 tied candidates (the sort, the
+    split-list and the whole-row tie paths)."""
+    B, Hq, Hkv, N, d = 1, 2, 1, 300 * 64, 64
+    qu, ku, _ = W.random_qkv(26, B, Hq, Hkv, N, d)
+    ku = np.broadcast_to(ku[:, :, :1, :], ku.shape).copy()
+    topk, theta = 0.331, 0.0      # 0.331 n is never an integer for n <= 300; theta 0 keeps nothing extra
+    gm = fbs.predict_mask(dev_bf16(qu), dev_bf16(ku), topk, theta, causal).cpu().numpy()
+    pred = oracle.predict_mask(f64(qu), f64(ku), topk, theta, causal)
+    assert np.array_equal(gm, pred["mask"])
+    nvalid = pred["mask"].shape[-1] if not causal else None
+    if nvalid:
+        assert (gm.sum(axis=-1) == math.ceil(topk * nvalid)).all()
+        assert gm[..., :math.ceil(topk * nvalid)].all()
+
+
 @pytest.mark.parametrize("topk,theta", [(0.05, 0.5), (0.3, 0.3), (0.9, 0.0), (1.0, 0.5), (0.5, 2.0)])
 def test_mask_topk_theta_sweep(topk, theta):
     w = make("llama")
