@@ -150,6 +150,21 @@ int make_map_u8(CUtensorMap *m, void *base, const int64_t dims_[4], const int64_
   return SPARGE_OK;
 }
 
+// 3-D map over the fp32 pooled scores [planes][rows][nkb_pad] for TMA stores: box 32 columns
+// (128 bytes) x 128 rows, 128-byte swizzle.
+int make_map_s(CUtensorMap *m, float *base, int64_t nkb_pad, int64_t rows, int64_t planes) {
+  encode_fn_t enc = get_encode();
+  if (!enc) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[3] = {(cuuint64_t)nkb_pad, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)nkb_pad * 4, (cuuint64_t)(rows * nkb_pad * 4)};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled(S) failed with %d", (int)r);
+  return SPARGE_OK;
+}
+
 int check_topk_theta(float topk, float theta) {
   if (!(topk > 0.f && topk <= 1.f)) return fail(SPARGE_ERR_INVALID_ARG, "topk=%g not in (0, 1]", (double)topk);
   if (!std::isfinite(theta)) return fail(SPARGE_ERR_INVALID_ARG, "theta must be finite");
@@ -172,6 +187,8 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
                  void *ws, size_t ws_bytes, cudaStream_t s, void *const *ev = nullptr) {
   if (!mask) return fail(SPARGE_ERR_INVALID_ARG, "mask is NULL");
   if (q.N > 131072) return fail(SPARGE_ERR_UNSUPPORTED, "mask prediction supports N <= 131072 (got %lld)", (long long)q.N);
+  if (q.B * q.H * cdiv(q.N, QBLK) > 0x7fffffffLL)
+    return fail(SPARGE_ERR_UNSUPPORTED, "mask prediction supports at most 2^31 - 1 mask rows");
   const size_t need = predict_ws_bytes(q.B, q.H, k.H, q.N, q.d);
   if (need && (!ws || ws_bytes < need))
     return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
@@ -187,9 +204,10 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
     memset(&g, 0, sizeof(g));
     const int64_t nqb = cdiv(q.N, QBLK), nkb = cdiv(q.N, KBLK);
     if ((rc = make_map3(&g.qhi, pw.qhi, q.d, nqb, q.B * q.H, "qhi")) || (rc = make_map3(&g.qlo, pw.qlo, q.d, nqb, q.B * q.H, "qlo")) ||
-        (rc = make_map3(&g.khi, pw.khi, q.d, nkb, q.B * k.H, "khi")) || (rc = make_map3(&g.klo, pw.klo, q.d, nkb, q.B * k.H, "klo")))
+        (rc = make_map3(&g.khi, pw.khi, q.d, nkb, q.B * k.H, "khi")) || (rc = make_map3(&g.klo, pw.klo, q.d, nkb, q.B * k.H, "klo")) ||
+        (rc = make_map_s(&g.ts, pw.S, pw.nkb_pad, nqb, q.B * q.H)))
       return rc;
-    g.S = pw.S;
+    g.Smax = pw.Smax;
     g.nkb_pad = pw.nkb_pad;
     g.B = (int)q.B; g.Hq = (int)q.H; g.Hkv = (int)k.H; g.N = (int)q.N; g.d = (int)q.d; g.causal = causal;
     g.scale = scale;
@@ -307,6 +325,7 @@ size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d
   s += 2 * align256(2 * B * Hq * nqb * d);              // qhi, qlo
   s += 2 * align256(2 * B * Hkv * nkb * d);             // khi, klo
   s += align256(sizeof(float) * B * Hq * nqb * nkb_pad);  // S
+  s += align256(sizeof(float) * B * Hq * nqb);          // Smax
   return s;
 }
 
@@ -328,6 +347,7 @@ PredictWs predict_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t
   w.khi = reinterpret_cast<uint16_t *>(take(2 * B * Hkv * nkb * d));
   w.klo = reinterpret_cast<uint16_t *>(take(2 * B * Hkv * nkb * d));
   w.S = reinterpret_cast<float *>(take(sizeof(float) * B * Hq * nqb * nkb_pad));
+  w.Smax = reinterpret_cast<float *>(take(sizeof(float) * B * Hq * nqb));
   w.nkb_pad = nkb_pad;
   return w;
 }

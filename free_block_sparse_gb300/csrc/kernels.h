@@ -24,6 +24,7 @@ struct PredictWs {
   uint16_t *qhi, *qlo;  // bf16 [B][Hq][nqb][d]
   uint16_t *khi, *klo;  // bf16 [B][Hkv][nkb][d]
   float *S;         // [B][Hq][nqb][nkb_pad]
+  float *Smax;      // [B][Hq][nqb] maximum of each S row over its valid key blocks
   int64_t nkb_pad;
 };
 
@@ -47,7 +48,8 @@ cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, c
 // B*Hq; box 64 x 128) and khi, klo (d, nkb, B*Hkv; box 64 x 128).
 struct ScoreGemmLaunch {
   CUtensorMap qhi, qlo, khi, klo;
-  float *S;
+  CUtensorMap ts;  // 3-D map over S (nkb_pad, nqb, B*Hq) fp32, box 32 x 128, 128-byte swizzle
+  float *Smax;     // [B][Hq][nqb] row maxima over the valid key blocks
   int64_t nkb_pad;
   int B, Hq, Hkv, N, d, causal;
   float scale;

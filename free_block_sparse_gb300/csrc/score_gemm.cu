@@ -5,7 +5,12 @@
 // 16 significant bits (relative error ~1e-5, far inside the 1e-3 decision margins of the mask).
 // Only chunks holding valid (causal) key blocks are computed.  One CTA per (128 query blocks,
 // head); warp 4 loads operands by TMA (Q once, K chunks into a 2-stage ring), warp 5 issues the
-// MMAs into two TMEM accumulators, warps 0-3 move each finished accumulator row to S.
+// MMAs into two TMEM accumulators, warps 0-3 move each finished accumulator to S: each thread
+// owns one row, scales it, keeps the maximum over the row's valid key blocks, and writes it in
+// 32-column quarters into the K stage the chunk's MMAs have just finished with (128-byte
+// swizzle), from where one thread stores the quarters to S by TMA (whole 128-byte lines instead
+// of one 16-byte piece per row per instruction).  The stage goes back to the producer once the
+// stores have read it.  The row maxima go to Smax for the selection.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -16,7 +21,7 @@ constexpr int GROWS = 128;  // query blocks per CTA (MMA M)
 constexpr int GCOLS = 128;  // key blocks per chunk (MMA N)
 
 struct GemmArgs {
-  float *S;
+  float *Smax;
   int64_t nkb_pad;
   int B, Hq, Hkv, G, nqb, nkb, causal, ngroups;
   float scale;
@@ -31,7 +36,10 @@ struct GL {
   static constexpr uint32_t OFF_QLO = OP_BYTES;
   static constexpr uint32_t OFF_K = 2 * OP_BYTES;        // stage s: hi at OFF_K + 2 s OP_BYTES, lo after it
   static constexpr int KST = 2;
-  static constexpr uint32_t OFF_CTRL = OFF_K + KST * 2 * OP_BYTES;
+  static constexpr uint32_t STAGE_BYTES = 2 * OP_BYTES;  // K hi + lo; reused to stage S quarters
+  static constexpr int QPR = STAGE_BYTES / 16384 < 4 ? STAGE_BYTES / 16384 : 4;  // 16 KB quarters per round
+  static constexpr int ROUNDS = 4 / QPR;
+  static constexpr uint32_t OFF_CTRL = OFF_K + KST * STAGE_BYTES;
   static constexpr uint32_t TOTAL = OFF_CTRL + 256;
 };
 
@@ -48,7 +56,7 @@ template <int D>
 __global__ void __launch_bounds__(192, 1)
     score_gemm_kernel(const __grid_constant__ CUtensorMap tqh, const __grid_constant__ CUtensorMap tql,
                       const __grid_constant__ CUtensorMap tkh, const __grid_constant__ CUtensorMap tkl,
-                      const GemmArgs a) {
+                      const __grid_constant__ CUtensorMap ts, const GemmArgs a) {
   using L = GL<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
@@ -71,7 +79,7 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(&cs.q_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&cs.k_full[s], 1);
-      mbar_init(&cs.k_empty[s], 1);
+      mbar_init(&cs.k_empty[s], 2);  // the chunk's MMAs, and the S stores out of the stage
       mbar_init(&cs.acc_full[s], 1);
       mbar_init(&cs.acc_empty[s], 128);
     }
@@ -143,36 +151,63 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     const int r = warp * 32 + lane;
     const int i = i0 + r;
+    const int nv = (i < a.nqb) ? (a.causal ? min(a.nkb, 2 * i + 2) : a.nkb) : 0;  // valid key blocks
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float *srow = a.S + ((static_cast<int64_t>(b) * a.Hq + h) * a.nqb + (i < a.nqb ? i : 0)) * a.nkb_pad;
+    float rmax = -3.402823466e38f;
     for (int ch = 0; ch < nch; ++ch) {
-      const int ab = ch & 1;
-      if (!mbar_wait(&cs.acc_full[ab], (ch >> 1) & 1, abort, a.status)) break;
+      const int ab = ch & 1, st = ch % L::KST;
+      // all 128 epilogue threads leave together if any wait gave up (they meet at named barriers)
+      const bool ok = mbar_wait(&cs.acc_full[ab], (ch >> 1) & 1, abort, a.status);
+      if (bar_red_or(1, 128, !ok)) break;
       tc_fence_after();
-      uint32_t v[4][32];
+      uint8_t *stage = smem + L::OFF_K + st * L::STAGE_BYTES;  // free: the chunk's MMAs are done
+      for (int rd = 0; rd < L::ROUNDS; ++rd) {
+        if (rd > 0) {  // the previous round's stores must have read the stage
+          if (threadIdx.x == 0) bulk_wait_read_all();
+          bar_sync(1, 128);
+        }
+#pragma unroll 1
+        for (int qq = 0; qq < L::QPR; ++qq) {
+          const int q = rd * L::QPR + qq;
+          uint32_t v[32];
+          tmem_ld32(tl + ab * GCOLS + 32 * q, v);
+          tmem_ld_wait();
+          const int j0 = GCOLS * ch + 32 * q;
+          uint8_t *row = stage + qq * 16384 + r * 128;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld32(tl + ab * GCOLS + 32 * q, v[q]);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&cs.acc_empty[ab]);
-      if (i < a.nqb) {
-        const int j0 = GCOLS * ch;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            const int j = j0 + 32 * q + c;
-            if (j < a.nkb_pad) {
-              float4 o;
-              o.x = __uint_as_float(v[q][c]) * a.scale;
-              o.y = __uint_as_float(v[q][c + 1]) * a.scale;
-              o.z = __uint_as_float(v[q][c + 2]) * a.scale;
-              o.w = __uint_as_float(v[q][c + 3]) * a.scale;
-              *reinterpret_cast<float4 *>(srow + j) = o;
-            }
+          for (int c = 0; c < 8; ++c) {
+            float4 o;
+            o.x = __uint_as_float(v[4 * c]) * a.scale;
+            o.y = __uint_as_float(v[4 * c + 1]) * a.scale;
+            o.z = __uint_as_float(v[4 * c + 2]) * a.scale;
+            o.w = __uint_as_float(v[4 * c + 3]) * a.scale;
+            const int j = j0 + 4 * c;
+            if (j < nv) rmax = fmaxf(rmax, o.x);
+            if (j + 1 < nv) rmax = fmaxf(rmax, o.y);
+            if (j + 2 < nv) rmax = fmaxf(rmax, o.z);
+            if (j + 3 < nv) rmax = fmaxf(rmax, o.w);
+            *reinterpret_cast<float4 *>(row + ((c ^ (r & 7)) << 4)) = o;
           }
+        }
+        if (rd == L::ROUNDS - 1) {  // this thread's TMEM reads of the accumulator are done
+          tc_fence_before();
+          mbar_arrive(&cs.acc_empty[ab]);
+        }
+        fence_proxy_async_smem();
+        bar_sync(1, 128);
+        if (threadIdx.x == 0) {
+          for (int qq = 0; qq < L::QPR; ++qq)
+            tma_store_3d(&ts, stage + qq * 16384, GCOLS * ch + 32 * (rd * L::QPR + qq), i0, bh);
+          bulk_commit();
+        }
+      }
+      if (threadIdx.x == 0) {  // the stage returns to the producer once the stores have read it
+        bulk_wait_read_all();
+        mbar_arrive(&cs.k_empty[st]);
       }
     }
+    if (threadIdx.x == 0) bulk_wait_all();
+    if (i < a.nqb) a.Smax[static_cast<int64_t>(bh) * a.nqb + i] = rmax;
   }
   tc_fence_before();
   __syncthreads();
@@ -191,7 +226,7 @@ cudaError_t launch_d(const ScoreGemmLaunch &l, const GemmArgs &a, cudaStream_t s
     attr_set = true;
   }
   dim3 grid(static_cast<unsigned>(a.B * a.Hq), static_cast<unsigned>(a.ngroups));
-  score_gemm_kernel<D><<<grid, 192, smem, st>>>(l.qhi, l.qlo, l.khi, l.klo, a);
+  score_gemm_kernel<D><<<grid, 192, smem, st>>>(l.qhi, l.qlo, l.khi, l.klo, l.ts, a);
   return cudaGetLastError();
 }
 
@@ -199,7 +234,7 @@ cudaError_t launch_d(const ScoreGemmLaunch &l, const GemmArgs &a, cudaStream_t s
 
 cudaError_t launch_score_gemm(const ScoreGemmLaunch &l, cudaStream_t st) {
   GemmArgs a;
-  a.S = l.S;
+  a.Smax = l.Smax;
   a.nkb_pad = l.nkb_pad;
   a.B = l.B; a.Hq = l.Hq; a.Hkv = l.Hkv; a.G = l.Hq / l.Hkv;
   a.nqb = (l.N + QBLK - 1) / QBLK;

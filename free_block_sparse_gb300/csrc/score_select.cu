@@ -4,11 +4,12 @@
 // README quick start: topk = 0.5 keeps the top 50% of the attention weights).
 //
 // One warp per mask row.  Lane l handles the key blocks 128 t + 4 l .. 128 t + 4 l + 3 of each
-// 128-block stretch t, so every global and shared access is 16 bytes per lane and the mask goes
-// out as 32-bit words.  The row lives in shared memory: pass 1 copies the scores there and takes
-// the maximum; pass 2 replaces them by e_j = exp(s_j - max), sums Z, and builds a 32-bin
-// histogram of the mass over the bit pattern of e (bins ordered by value, lane-private columns,
-// no shared counters).  With the kept set defined as the shortest prefix, in (e desc, index asc)
+// 128-block stretch t, so every global access is 16 bytes per lane and the mask goes out as
+// 32-bit words.  The row maximum comes from the score kernel; every pass re-reads the row (from
+// L2 after the first) and recomputes e_j = exp(s_j - max) with the same expression, so no row
+// buffer limits how many warps an SM holds.  The first pass sums Z and builds a 32-bin
+// histogram of the mass over the bit pattern of e (bins ordered by value, lane-private columns in
+// shared memory, no shared counters).  With the kept set defined as the shortest prefix, in (e desc, index asc)
 // order, whose mass reaches topk * Z, the bin where the cumulative mass first reaches the target
 // holds the cut.  Its elements are compacted into a short list (ballot offsets); further 32-bin
 // levels split the list until at most 32 remain, which one warp-wide bitonic sort orders
@@ -26,27 +27,42 @@
 namespace sparge {
 namespace {
 
-constexpr int WARPS = 4;
+constexpr int WARPS = 8;
 constexpr int NBIN = 32;
 constexpr int CMAX = 256;  // crossing-bin elements compacted into the short list (8 per lane)
 
 struct SelArgs {
-  const float *S;
+  const float *S, *Smax;
   const float *sQ, *sK;
   uint8_t *mask;
   int64_t nkb_pad, rows;
-  int Hq, Hkv, G, nqb, nkb, causal, ew;  // ew: floats of a warp's row buffer (nkb rounded up to 128)
+  int Hq, Hkv, G, nqb, nkb, causal;
   float topk, theta;
 };
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+// e of the key blocks j0 .. j0 + 3 of a row (0 past the valid blocks); every pass uses this one
+// expression, so the values agree bit for bit between passes.  s - max is exact zero for the
+// maximum, and the hardware exponential is clamped at 1, so e <= 1 always.
+__device__ __forceinline__ float4 load_e(const float *srow, int j0, int nvalid, float negm) {
+  float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (j0 < nvalid) {
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(srow + j0));
+    const float2 l2 = make_float2(LOG2E, LOG2E), nm = make_float2(negm, negm);
+    const float2 a = fmul2(fadd2(make_float2(v.x, v.y), nm), l2);
+    const float2 b = fmul2(fadd2(make_float2(v.z, v.w), nm), l2);
+    e.x = fminf(fast_exp2(a.x), 1.f);
+    e.y = j0 + 1 < nvalid ? fminf(fast_exp2(a.y), 1.f) : 0.f;
+    e.z = j0 + 2 < nvalid ? fminf(fast_exp2(b.x), 1.f) : 0.f;
+    e.w = j0 + 3 < nvalid ? fminf(fast_exp2(b.y), 1.f) : 0.f;
+  }
+  return e;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
   return v;
 }
 __device__ __forceinline__ int warp_sum_i(int v) {
@@ -54,9 +70,9 @@ __device__ __forceinline__ int warp_sum_i(int v) {
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   return v;
 }
+// x (>= 0) has a bit pattern in [lo, hi); lo >= 1, so x = 0 is never inside
 __device__ __forceinline__ bool in_range(float x, uint32_t lo, uint32_t hi) {
-  const uint32_t u = __float_as_uint(x);
-  return x > 0.f && u >= lo && u < hi;
+  return __float_as_uint(x) - lo < hi - lo;
 }
 __device__ __forceinline__ float comp(const float4 &v, int u) {
   return u == 0 ? v.x : (u == 1 ? v.y : (u == 2 ? v.z : v.w));
@@ -75,16 +91,21 @@ __device__ __forceinline__ void hist_zero(float *H, int lane) {
   for (int k = 0; k < NBIN; ++k) H[k * 32 + lane] = 0.f;
   __syncwarp();
 }
-// 32 bins of 2^shift patterns from hi - 1 down; lane-private column
-__device__ __forceinline__ void hist_add(float *H, int lane, float x, const Cut &st) {
-  const uint32_t bin = (st.hi - 1u - __float_as_uint(x)) >> st.shift;
-  if (in_range(x, st.lo, st.hi) && bin < NBIN) H[bin * 32 + lane] += x;
+// 32 bins of 2^shift patterns from hi - 1 down, lane-private column.  With d = hi - 1 - bits, x
+// is in [lo, hi) and in one of the 32 bins exactly when d < lim = min(hi - lo, 32 << shift).
+__device__ __forceinline__ uint32_t hist_lim(const Cut &st) {
+  const uint32_t w = st.hi - st.lo, b = static_cast<uint32_t>(NBIN) << st.shift;
+  return w < b ? w : b;
 }
-__device__ __forceinline__ void hist_add4(float *H, int lane, const float4 &v, const Cut &st) {
-  hist_add(H, lane, v.x, st);
-  hist_add(H, lane, v.y, st);
-  hist_add(H, lane, v.z, st);
-  hist_add(H, lane, v.w, st);
+__device__ __forceinline__ void hist_add(float *H, int lane, float x, const Cut &st, uint32_t lim) {
+  const uint32_t d = st.hi - 1u - __float_as_uint(x);
+  if (d < lim) H[(d >> st.shift) * 32 + lane] += x;
+}
+__device__ __forceinline__ void hist_add4(float *H, int lane, const float4 &v, const Cut &st, uint32_t lim) {
+  hist_add(H, lane, v.x, st, lim);
+  hist_add(H, lane, v.y, st, lim);
+  hist_add(H, lane, v.z, st, lim);
+  hist_add(H, lane, v.w, st, lim);
 }
 // Narrows the state to the bin where the cumulative mass first reaches target (st.nc is left for
 // the caller to recount).  Returns false (state unchanged) if rounding left no bin reaching it.
@@ -134,42 +155,26 @@ __device__ __forceinline__ int list_append(const float4 &e, int j0, const Cut &s
   return n;
 }
 
-__global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
-  extern __shared__ __align__(16) float sel_smem[];
+__global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) {
+  __shared__ float sel_smem[WARPS][NBIN * 32 + 2 * CMAX];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * WARPS + w;
-  if (row >= a.rows) return;
-  float *E = sel_smem + static_cast<int64_t>(w) * (a.ew + NBIN * 32 + 2 * CMAX);  // the row
-  float *H = E + a.ew;                           // histogram [bin][lane]
+  // 32-bit row arithmetic (the host keeps rows below 2^31): the divisions below are per row
+  const uint32_t row = blockIdx.x * WARPS + w;
+  if (row >= static_cast<uint32_t>(a.rows)) return;
+  float *H = sel_smem[w];                        // histogram [bin][lane]
   float *Lv = H + NBIN * 32;                     // short list: values
   int *Lj = reinterpret_cast<int *>(Lv + CMAX);  // and key-block indices
-  float4 *E4 = reinterpret_cast<float4 *>(E);
 
-  const int i = static_cast<int>(row % a.nqb);
-  const int64_t bh = row / a.nqb;
-  const int h = static_cast<int>(bh % a.Hq), b = static_cast<int>(bh / a.Hq);
+  const uint32_t bh = row / static_cast<uint32_t>(a.nqb);
+  const int i = static_cast<int>(row - bh * static_cast<uint32_t>(a.nqb));
+  const uint32_t b = bh / static_cast<uint32_t>(a.Hq);
+  const int h = static_cast<int>(bh - b * static_cast<uint32_t>(a.Hq));
   const int kvh = h / a.G;
   const int nvalid = a.causal ? min(a.nkb, 2 * i + 2) : a.nkb;
   const int nit = (nvalid + 127) >> 7;
-  const float *srow = a.S + row * a.nkb_pad;
+  const float *srow = a.S + static_cast<int64_t>(row) * a.nkb_pad;
   const float *sKrow = a.sK + (static_cast<int64_t>(b) * a.Hkv + kvh) * a.nkb_pad;
-  constexpr float LOG2E = 1.4426950408889634f;
-
-  // pass 1: scores into shared memory (-FLT_MAX past the valid blocks), row maximum
-  float m = -FLT_MAX;
-  for (int t = 0; t < nit; ++t) {
-    const int j0 = 128 * t + 4 * lane;
-    float4 v = make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
-    if (j0 < nvalid) {
-      v = __ldg(reinterpret_cast<const float4 *>(srow + j0));
-      if (j0 + 1 >= nvalid) v.y = -FLT_MAX;
-      if (j0 + 2 >= nvalid) v.z = -FLT_MAX;
-      if (j0 + 3 >= nvalid) v.w = -FLT_MAX;
-    }
-    E4[32 * t + lane] = v;
-    m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-  }
-  m = warp_max(m);
+  const float negm = -a.Smax[row];
 
   const bool keep_all = a.topk >= 1.f || a.sQ[row] < a.theta;
   Cut st;
@@ -183,19 +188,15 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
     while (static_cast<float>(NBIN) * exp2f(static_cast<float>(st.shift - 23)) < r2) ++st.shift;
     hist_zero(H, lane);
   }
-  // pass 2: e = exp(s - max) in place (0 past the valid blocks), Z, first histogram level
-  float zl = 0.f;
+  // first pass: Z and the first histogram level
+  float2 z2 = make_float2(0.f, 0.f);
+  const uint32_t lim1 = hist_lim(st);
   for (int t = 0; t < nit; ++t) {
-    float4 v = E4[32 * t + lane];
-    v.x = exp2f((v.x - m) * LOG2E);
-    v.y = exp2f((v.y - m) * LOG2E);
-    v.z = exp2f((v.z - m) * LOG2E);
-    v.w = exp2f((v.w - m) * LOG2E);
-    E4[32 * t + lane] = v;
-    zl += (v.x + v.y) + (v.z + v.w);
-    if (!keep_all) hist_add4(H, lane, v, st);
+    const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm);
+    z2 = fadd2(z2, fadd2(make_float2(v.x, v.y), make_float2(v.z, v.w)));
+    if (!keep_all) hist_add4(H, lane, v, st, lim1);
   }
-  const float Z = warp_sum(zl);
+  const float Z = warp_sum(z2.x + z2.y);
 
   // the cut: keep e > et, or e == et with index <= jt
   float et = 2.f;
@@ -207,7 +208,10 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
     // compact the crossing bin; while it does not fit the short list, split it over the row
     while (ok) {
       int n = 0;
-      for (int t = 0; t < nit; ++t) n = list_append(E4[32 * t + lane], 128 * t + 4 * lane, st, Lv, Lj, n, lane);
+      for (int t = 0; t < nit; ++t) {
+        const int j0 = 128 * t + 4 * lane;
+        n = list_append(load_e(srow, j0, nvalid, negm), j0, st, Lv, Lj, n, lane);
+      }
       st.nc = n;
       if (n <= CMAX) {
         listed = true;
@@ -215,7 +219,8 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
       }
       if (st.shift < 0) break;
       hist_zero(H, lane);
-      for (int t = 0; t < nit; ++t) hist_add4(H, lane, E4[32 * t + lane], st);
+      const uint32_t lim = hist_lim(st);
+      for (int t = 0; t < nit; ++t) hist_add4(H, lane, load_e(srow, 128 * t + 4 * lane, nvalid, negm), st, lim);
       ok = hist_pick(H, lane, target, st);
     }
     bool sorted = false;
@@ -233,8 +238,9 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
       // split the list in registers until at most 32 candidates remain
       while (ok && st.nc > 32 && st.shift >= 0) {
         hist_zero(H, lane);
+        const uint32_t lim = hist_lim(st);
 #pragma unroll
-        for (int k = 0; k < CMAX / 32; ++k) hist_add(H, lane, ce[k], st);
+        for (int k = 0; k < CMAX / 32; ++k) hist_add(H, lane, ce[k], st, lim);
         ok = hist_pick(H, lane, target, st);
         if (ok) {
           int cnt = 0;
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
         const float tv = __uint_as_float(mid);
         float part = 0.f;
         for (int t = 0; t < nit; ++t) {
-          const float4 v = E4[32 * t + lane];
+          const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm);
           part += (v.x >= tv ? v.x : 0.f) + (v.y >= tv ? v.y : 0.f) + (v.z >= tv ? v.z : 0.f) +
                   (v.w >= tv ? v.w : 0.f);
         }
@@ -315,14 +321,14 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
       // elements equal to v* are kept in ascending key-block order until the mass reaches target
       float above = 0.f;
       for (int t = 0; t < nit; ++t) {
-        const float4 v = E4[32 * t + lane];
+        const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm);
         above += (v.x > et ? v.x : 0.f) + (v.y > et ? v.y : 0.f) + (v.z > et ? v.z : 0.f) + (v.w > et ? v.w : 0.f);
       }
       float cum = warp_sum(above);
       jt = -1;
       for (int t = 0; t < nit && cum < target; ++t) {
-        const float4 v = E4[32 * t + lane];
         const int j0 = 128 * t + 4 * lane;
+        const float4 v = load_e(srow, j0, nvalid, negm);
         int mine = 0;  // ties held by this lane
 #pragma unroll
         for (int u = 0; u < 4; ++u) mine += (comp(v, u) == et && j0 + u < nvalid) ? 1 : 0;
@@ -354,16 +360,15 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
     }
   }
 
-  // the mask row: 4 key blocks per lane, 32-bit stores when the rows are 4-byte aligned
-  uint8_t *mrow = a.mask + row * a.nkb;
-  const int nall = (a.nkb + 127) >> 7;
+  // the mask row: 4 key blocks per lane, 32-bit stores when the rows are 4-byte aligned; the
+  // causally hidden part of the row is zero-filled
+  uint8_t *mrow = a.mask + static_cast<int64_t>(row) * a.nkb;
   const bool words = (a.nkb & 3) == 0 && (reinterpret_cast<uintptr_t>(a.mask) & 3u) == 0;
-  for (int t = 0; t < nall; ++t) {
+  for (int t = 0; t < nit; ++t) {
     const int j0 = 128 * t + 4 * lane;
-    if (j0 >= a.nkb) continue;
     uint32_t word = 0u;
     if (j0 < nvalid) {
-      const float4 v = E4[32 * t + lane];
+      const float4 v = load_e(srow, j0, nvalid, negm);
       const float4 sk = __ldg(reinterpret_cast<const float4 *>(sKrow + j0));
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -373,12 +378,25 @@ __global__ void __launch_bounds__(WARPS * 32) score_select_kernel(SelArgs a) {
         word |= (keep ? 1u : 0u) << (8 * u);
       }
     }
+    if (j0 >= a.nkb) continue;
     if (words) {
       *reinterpret_cast<uint32_t *>(mrow + j0) = word;
     } else {
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         if (j0 + u < a.nkb) mrow[j0 + u] = static_cast<uint8_t>(word >> (8 * u));
+    }
+  }
+  const int nall = (a.nkb + 127) >> 7;
+  for (int t = nit; t < nall; ++t) {
+    const int j0 = 128 * t + 4 * lane;
+    if (j0 >= a.nkb) continue;
+    if (words) {
+      *reinterpret_cast<uint32_t *>(mrow + j0) = 0u;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (j0 + u < a.nkb) mrow[j0 + u] = 0;
     }
   }
 }
@@ -390,6 +408,7 @@ cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int
   (void)d;
   SelArgs a;
   a.S = ws.S;
+  a.Smax = ws.Smax;
   a.sQ = ws.sQ;
   a.sK = ws.sK;
   a.mask = mask;
@@ -397,18 +416,14 @@ cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int
   a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv;
   a.nqb = (N + QBLK - 1) / QBLK;
   a.nkb = (N + KBLK - 1) / KBLK;
-  a.ew = (a.nkb + 127) / 128 * 128;
   a.causal = causal;
   a.rows = static_cast<int64_t>(B) * Hq * a.nqb;
   a.topk = topk;
   a.theta = theta;
   if (a.rows == 0) return cudaSuccess;
-  const size_t smem = static_cast<size_t>(WARPS) * (a.ew + NBIN * 32 + 2 * CMAX) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(score_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  if (a.rows > 0x7fffffffLL) return cudaErrorInvalidValue;  // the kernel indexes rows in 32 bits
   const int64_t grid = (a.rows + WARPS - 1) / WARPS;
-  score_select_kernel<<<static_cast<unsigned>(grid), WARPS * 32, smem, st>>>(a);
+  score_select_kernel<<<static_cast<unsigned>(grid), WARPS * 32, 0, st>>>(a);
   return cudaGetLastError();
 }
 
