@@ -62,6 +62,9 @@ EXPORTS = {
     "sparge_block_sparse_attn": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                 ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "sparge_block_sparse_attn_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_size_t, ctypes.c_void_p]),
     "sparge_attn": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_int,
                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "sparge_attn_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_int,
@@ -240,16 +243,9 @@ def sparge_attn(q, k, v, topk: float = 0.5, causal: bool = False, out=None, ws=N
     return out
 
 
-def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: float = -math.inf,
-                   scale: float = 0.0, precision: int = SPARGE_PRECISION_BF16, stats=None, mask_out=None,
-                   out=None, ws=None, events=None):
-    """sparge_attn with explicit theta, lambda, scale, counters, an optional mask output and
-    optional timing events (6 torch.cuda.Event, recorded around the five kernels)."""
-    torch = _torch()
-    if out is None:
-        out = torch.empty_like(q)
-    q8 = precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV)
-    ws = _workspace(SPARGE_OP_ATTN_Q8 if q8 else SPARGE_OP_ATTN, q, k, ws)
+def _params(theta, lam, scale, precision, stats, events):
+    """A sparge_params; `events` (6 torch.cuda.Event or None) are passed as cudaEvent_t handles.
+    The handle array is kept on the returned struct so it outlives the call."""
     evp = None
     if events is not None:
         assert len(events) == 6
@@ -260,6 +256,39 @@ def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: 
     p = sparge_params(float(theta), float(lam), float(scale), int(precision),
                       0 if stats is None else stats.data_ptr(),
                       ctypes.cast(evp, ctypes.c_void_p) if evp is not None else None)
+    p._evp = evp
+    return p
+
+
+def block_sparse_attn_ex(q, k, v, mask=None, causal: bool = False, lam: float = -math.inf, scale: float = 0.0,
+                         precision: int = SPARGE_PRECISION_BF16, stats=None, out=None, ws=None, events=None):
+    """block_sparse_attn with an explicit scale and optional timing events (6 torch.cuda.Event:
+    [0] before the V copy or quantisation, [4] after it, [5] after the attention kernel)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(q)
+    op = SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 if precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV) \
+        else SPARGE_OP_BLOCK_SPARSE_ATTN
+    ws = _workspace(op, q, k, ws)
+    p = _params(0.5, lam, scale, precision, stats, events)
+    dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
+    mp = 0 if mask is None else mask.data_ptr()
+    _check(lib().sparge_block_sparse_attn_ex(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), mp, int(causal),
+                                             ctypes.byref(p), ctypes.byref(do), ws.data_ptr(), ws.numel(), _stream()))
+    return out
+
+
+def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: float = -math.inf,
+                   scale: float = 0.0, precision: int = SPARGE_PRECISION_BF16, stats=None, mask_out=None,
+                   out=None, ws=None, events=None):
+    """sparge_attn with explicit theta, lambda, scale, counters, an optional mask output and
+    optional timing events (6 torch.cuda.Event, recorded around the five kernels)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(q)
+    q8 = precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV)
+    ws = _workspace(SPARGE_OP_ATTN_Q8 if q8 else SPARGE_OP_ATTN, q, k, ws)
+    p = _params(theta, lam, scale, precision, stats, events)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     mp = 0 if mask_out is None else mask_out.data_ptr()
     _check(lib().sparge_attn_ex(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), float(topk), int(causal),

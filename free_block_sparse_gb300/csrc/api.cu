@@ -404,6 +404,26 @@ int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k, con
                    ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int sparge_block_sparse_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v,
+                                const uint8_t *mask, int is_causal, const sparge_params *p, sparge_tensor *o, void *ws,
+                                size_t ws_bytes, sparge_stream_t stream) {
+  g_last_error[0] = 0;
+  if (!p) return fail(SPARGE_ERR_INVALID_ARG, "params is NULL");
+  View qv, kv, vv;
+  int rc;
+  if ((rc = check_tensor(q, "q", &qv)) || (rc = check_tensor(k, "k", &kv)) || (rc = check_tensor(v, "v", &vv)) ||
+      (rc = check_qk(qv, kv)))
+    return rc;
+  if ((rc = check_lambda(p->lambda))) return rc;
+  if (std::isnan(p->scale) || p->scale < 0.f || std::isinf(p->scale))
+    return fail(SPARGE_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)qv.d);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = record_event(p->timing_events, 0, s))) return rc;
+  return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws, ws_bytes, s,
+                   p->timing_events);
+}
+
 int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,
                    const sparge_params *p, sparge_tensor *o, uint8_t *mask_out, void *ws, size_t ws_bytes,
                    sparge_stream_t stream) {

@@ -155,6 +155,16 @@ int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k,
                              size_t ws_bytes, unsigned long long *stats, sparge_stream_t stream);
 
 /*
+ * sparge_block_sparse_attn with its parameters in a sparge_params (theta is unused): lambda,
+ * scale (0 means 1/sqrt(d)), precision, counters, and timing events; of the six events, [0] is
+ * recorded before the V copy or quantisation, [4] after it and [5] after the attention kernel
+ * ([1]-[3] are left alone).  Same workspace and errors as sparge_block_sparse_attn.
+ */
+int sparge_block_sparse_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v,
+                                const uint8_t *mask, int is_causal, const sparge_params *params,
+                                sparge_tensor *o, void *ws, size_t ws_bytes, sparge_stream_t stream);
+
+/*
  * The plug-and-play call: sparge_predict_mask with theta = 0.5, then sparge_block_sparse_attn
  * with lambda = -INFINITY, scale 1/sqrt(d).  ws: sparge_workspace_bytes(SPARGE_OP_ATTN, ...).
  */

@@ -125,6 +125,26 @@ def test_attention_rejects_bad_lambda(lib, lam):
     assert rc == fbs.SPARGE_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("case", ["null_params", "bad_lambda", "neg_scale", "inf_scale", "q8_d64"])
+def test_block_sparse_ex_rejects_bad_parameters(lib, case):
+    q = _t()
+    p = fbs.sparge_params(0.5, -math.inf, 0.0, fbs.SPARGE_PRECISION_BF16, 0, None)
+    code = fbs.SPARGE_ERR_INVALID_ARG
+    if case == "bad_lambda":
+        p.lambda_ = 1.0
+    elif case == "neg_scale":
+        p.scale = -1.0
+    elif case == "inf_scale":
+        p.scale = math.inf
+    elif case == "q8_d64":
+        p.precision = fbs.SPARGE_PRECISION_Q8
+        code = fbs.SPARGE_ERR_UNSUPPORTED
+    pp = None if case == "null_params" else ctypes.byref(p)
+    rc = lib.sparge_block_sparse_attn_ex(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), None, 0, pp,
+                                         ctypes.byref(q), None, 0, None)
+    assert rc == code, lib.sparge_last_error()
+
+
 def test_attention_rejects_mismatched_output(lib):
     q, o = _t(), _t(H=4)
     rc = lib.sparge_block_sparse_attn(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), None, -math.inf, 0, 0,

@@ -233,3 +233,21 @@ def test_empty_and_degenerate_shapes():
     z = torch.zeros((0, 2, 128, 64), dtype=torch.bfloat16, device="cuda")
     fbs.sparge_attn(z, z, z, 0.5, False)
     torch.cuda.synchronize()
+
+
+def test_block_sparse_ex_matches_and_times():
+    """The _ex call with scale 0 is the plain call (bit-identical); an explicit scale is the
+    oracle's scale; its six events bracket the V copy and the attention kernel."""
+    N, Hq, Hkv, d = 900, 2, 1, 128
+    qu, ku, vu = W.random_qkv(27, 1, Hq, Hkv, N, d)
+    q, k, v = dev_bf16(qu), dev_bf16(ku), dev_bf16(vu)
+    base = fbs.block_sparse_attn(q, k, v, None, -math.inf, True)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    ex = fbs.block_sparse_attn_ex(q, k, v, None, True, events=evs)
+    torch.cuda.synchronize()
+    assert torch.equal(base, ex)
+    assert evs[0].elapsed_time(evs[4]) >= 0 and evs[4].elapsed_time(evs[5]) > 0
+    out = fbs.block_sparse_attn_ex(q, k, v, None, True, scale=0.05)
+    ref = oracle.block_sparse_attn(f64(qu), f64(ku), f64(vu), None, -math.inf, True, scale=0.05)
+    cos, err = cos_maxabs(host_f64(out), ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
