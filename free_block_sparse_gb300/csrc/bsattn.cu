@@ -547,13 +547,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 template <int D, int KST, int VST, bool QK8, bool PV8>
 cudaError_t launch_t(const AttnLaunch &l, const AttnArgs &a, cudaStream_t st) {
   const uint32_t smem = Smem<D, KST, VST, QK8, PV8>::TOTAL;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bsattn_kernel<D, KST, VST, QK8, PV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};
+  if (cudaError_t e = set_smem_limit_once(bsattn_kernel<D, KST, VST, QK8, PV8>, static_cast<int>(smem), smem_set); e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(a.B) * a.Hq * a.nqb;
   bsattn_kernel<D, KST, VST, QK8, PV8><<<static_cast<unsigned>(grid), NTHREADS, smem, st>>>(l.tq, l.tk, l.tv, a);
   return cudaGetLastError();

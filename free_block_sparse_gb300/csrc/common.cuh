@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -79,6 +80,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
       }
     }
   }
+}
+
+// Raises a kernel's dynamic shared-memory limit on the current device the first time the kernel
+// runs there (the attribute is per device); `done` holds one bit per device id below 64.
+template <typename Kernel>
+inline cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<unsigned long long> &done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit != 0ull && (done.load(std::memory_order_acquire) & bit) != 0ull) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0ull) done.fetch_or(bit, std::memory_order_release);
+  return e;
 }
 
 // ------------------------------------------------------------------------------------------

@@ -218,13 +218,8 @@ __global__ void __launch_bounds__(192, 1)
 template <int D>
 cudaError_t launch_d(const ScoreGemmLaunch &l, const GemmArgs &a, cudaStream_t st) {
   const uint32_t smem = GL<D>::TOTAL;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(score_gemm_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};
+  if (cudaError_t e = set_smem_limit_once(score_gemm_kernel<D>, static_cast<int>(smem), smem_set); e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.B * a.Hq), static_cast<unsigned>(a.ngroups));
   score_gemm_kernel<D><<<grid, 192, smem, st>>>(l.qhi, l.qlo, l.khi, l.klo, l.ts, a);
   return cudaGetLastError();
