@@ -196,6 +196,43 @@ def profile_traffic(w, precision):
     return int(fields["traffic per full launch (bytes)"])
 
 
+def measure_permute(steps, warmup, dev, peaks):
+    """The Hilbert token order of the video-like workload's shape (B 1, H 30, N 17776 = 226 text
+    + 13 x 30 x 45 grid tokens, d 64): one step permutes q, k and v into curve order and
+    unpermutes the output (four launches); eight 68 MB tensors, 546 MB in all, more than L2.
+    Algorithmic bytes: each launch reads and writes every token row once (the 71 KB
+    permutation is not counted)."""
+    import torch
+    import free_block_sparse_gb300 as fbs
+    wd = W.describe("cogvideox")
+    perm = torch.from_numpy(fbs.hilbert_perm_3d(wd.n_prefix, *wd.grid)).to(dev)
+    g = torch.Generator(device=dev).manual_seed(11)
+    xs = [torch.randn((wd.B, wd.Hq, wd.N, wd.d), generator=g, device=dev).to(torch.bfloat16) for _ in range(4)]
+    ys = [torch.empty_like(x) for x in xs]
+
+    def step():
+        for i in range(3):
+            fbs.permute_tokens(xs[i], perm, out=ys[i])
+        fbs.unpermute_tokens(xs[3], perm, out=ys[3])
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    assert fbs.device_status() == 0
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    nbytes = 4 * 2 * xs[0].numel() * 2
+    gbs = nbytes / t / 1e9
+    return {"workload": "cogvideox-like shape, q/k/v into Hilbert order + output back (B1 H30 N17776 d64)",
+            "launches_per_step": 4, "ms": round(t * 1e3, 4), "bytes_per_step": nbytes, "gbs": round(gbs, 1),
+            "pct_hbm": round(100 * gbs / float(peaks["hbm_gbs"]), 2)}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import free_block_sparse_gb300 as fbs
@@ -388,6 +425,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": LAUNCHES_PER_STEP[(args.precision, given_mask)] * args.steps,
         "clocks": clk,
     }
+    line["permute"] = measure_permute(max(args.steps, 10), args.warmup, dev, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         tops, wall, desc, ncores = oracle_sample(w, args.cpu_blocks, min(args.cpu_workers, os.cpu_count() or 1))
         line["cpu_baseline"] = {"value": round(tops, 6), "unit": "dense-equiv TOPS", "cores": ncores,
@@ -458,11 +496,18 @@ def main():
     ap.add_argument("--lam", type=float, default=None, help="lambda override (default: the workload's)")
     ap.add_argument("--heads", default=None,
                     help="Hq,Hkv override (smaller cases of a workload for profiling; not a bench line)")
+    ap.add_argument("--permute-only", action="store_true",
+                    help="time only the Hilbert permute step (for profiling; not a bench line)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
-    if args.impl == "reference":
+    if args.permute_only:
+        import torch
+        torch.cuda.set_device(local_rank)
+        print(json.dumps({"permute": measure_permute(max(args.steps, 10), args.warmup,
+                                                     torch.device("cuda", local_rank), load_peaks())}))
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local_rank)

@@ -475,7 +475,8 @@ static int permute_common(const sparge_tensor *x, const int32_t *perm, sparge_te
   if (!perm) return fail(SPARGE_ERR_INVALID_ARG, "perm is NULL");
   if (xv.B != yv.B || xv.H != yv.H || xv.N != yv.N || xv.d != yv.d) return fail(SPARGE_ERR_INVALID_ARG, "x and y shapes differ");
   if (x->data == y->data) return fail(SPARGE_ERR_INVALID_ARG, "x and y must not overlap");
-  cudaError_t e = launch_permute(xv, perm, y->data, yv.sb, yv.sh, yv.sn, inverse, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_permute(xv, perm, y->data, yv.sb, yv.sh, yv.sn, inverse, status_ptr(),
+                                 reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
   return SPARGE_OK;
 }
@@ -511,7 +512,8 @@ int sparge_get_device_status(sparge_stream_t stream) {
     e = cudaMemcpyToSymbolAsync(g_status_word, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "status clear");
-    return fail(host, "a device-side wait timed out");
+    return fail(host, host == SPARGE_ERR_DEVICE_TIMEOUT ? "a device-side wait timed out"
+                                                        : "a kernel skipped a permutation entry outside 0..N-1");
   }
   return SPARGE_OK;
 }

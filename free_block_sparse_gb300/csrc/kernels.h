@@ -101,6 +101,6 @@ Q8Ws q8_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_
 cudaError_t launch_q8_prep(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v, cudaStream_t st);
 
 cudaError_t launch_permute(const View &x, const int32_t *perm, void *y, int64_t ysb, int64_t ysh, int64_t ysn,
-                           bool inverse, cudaStream_t st);
+                           bool inverse, int *status, cudaStream_t st);
 
 }  // namespace sparge

@@ -3,8 +3,7 @@
 // Token permutation along the Hilbert curve and its inverse (SpargeAttention summary page: a
 // space-filling Hilbert-curve reordering improves token locality and sparsity for visual
 // tasks).  y[:, :, t] = x[:, :, perm[t]] (gather) or y[:, :, perm[t]] = x[:, :, t] (scatter).
-// A pure row copy: each group of d/8 lanes moves one token row with 16-byte loads and stores;
-// a grid-stride loop over all (b, h, t) rows.
+// A pure row copy: each group of d/8 lanes moves one token row with 16-byte loads and stores.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -20,27 +19,45 @@ struct PermArgs {
   int64_t xsb, xsh, xsn, ysb, ysh, ysn;
   int B, H, N;
   int inverse;
+  int *status;
 };
+
+// Grid (token chunks, H, B), 256 threads; each thread moves U 16-byte pieces of token rows, all
+// U loads issued before the first store, so each SM keeps many bytes in flight; 32-bit index
+// arithmetic within a head.  A perm entry outside 0..N-1 is never used as an address: its row is
+// skipped and the device status word records SPARGE_ERR_INVALID_ARG.
+constexpr int PERM_U = 4;
 
 template <int D>
 __global__ void __launch_bounds__(256) permute_kernel(PermArgs a) {
-  constexpr int LPT = D / 8;
-  constexpr int RPW = 32 / LPT;  // rows per warp per step
-  const int lane = threadIdx.x & 31;
-  const int sub = lane / LPT, part = lane % LPT;
-  const int64_t rows = static_cast<int64_t>(a.B) * a.H * a.N;
-  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t r = warp0 * RPW + sub; r < rows; r += nwarps * RPW) {
-    const int t = static_cast<int>(r % a.N);
-    const int64_t bh = r / a.N;
-    const int h = static_cast<int>(bh % a.H), b = static_cast<int>(bh / a.H);
-    const int p = __ldg(a.perm + t);
-    const int src = a.inverse ? t : p;
-    const int dst = a.inverse ? p : t;
-    const uint4 v = ld_stream_v4(a.x + b * a.xsb + h * a.xsh + static_cast<int64_t>(src) * a.xsn + part * 8);
-    *reinterpret_cast<uint4 *>(a.y + b * a.ysb + h * a.ysh + static_cast<int64_t>(dst) * a.ysn + part * 8) = v;
+  constexpr int VPR = D / 8;                 // 16-byte pieces per token row
+  constexpr int ROWS = PERM_U * 256 / VPR;   // token rows per CTA
+  const int h = blockIdx.y, b = blockIdx.z;
+  const __nv_bfloat16 *xb = a.x + b * a.xsb + h * a.xsh;
+  __nv_bfloat16 *yb = a.y + b * a.ysb + h * a.ysh;
+  const int t0 = blockIdx.x * ROWS;
+  uint4 v[PERM_U];
+  int dst[PERM_U], part[PERM_U];
+#pragma unroll
+  for (int u = 0; u < PERM_U; ++u) {
+    const int e = threadIdx.x + u * 256;
+    const int t = t0 + e / VPR;
+    part[u] = e % VPR;
+    dst[u] = -1;
+    if (t < a.N) {
+      const int p = __ldg(a.perm + t);
+      if (static_cast<unsigned>(p) >= static_cast<unsigned>(a.N)) {  // not a token index: skip the row
+        if (part[u] == 0) record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
+        continue;
+      }
+      const int src = a.inverse ? t : p;
+      dst[u] = a.inverse ? p : t;
+      v[u] = ld_stream_v4(xb + static_cast<int64_t>(src) * a.xsn + part[u] * 8);
+    }
   }
+#pragma unroll
+  for (int u = 0; u < PERM_U; ++u)
+    if (dst[u] >= 0) *reinterpret_cast<uint4 *>(yb + static_cast<int64_t>(dst[u]) * a.ysn + part[u] * 8) = v[u];
 }
 
 // V (bf16, any legal strides) -> contiguous f16 copy for the P.V product of the attention kernel.
@@ -93,7 +110,7 @@ cudaError_t launch_convert_v_f16(const View &v, void *v16, cudaStream_t st) {
 }
 
 cudaError_t launch_permute(const View &x, const int32_t *perm, void *y, int64_t ysb, int64_t ysh, int64_t ysn,
-                           bool inverse, cudaStream_t st) {
+                           bool inverse, int *status, cudaStream_t st) {
   PermArgs a;
   a.x = static_cast<const __nv_bfloat16 *>(x.data);
   a.y = static_cast<__nv_bfloat16 *>(y);
@@ -102,15 +119,10 @@ cudaError_t launch_permute(const View &x, const int32_t *perm, void *y, int64_t 
   a.ysb = ysb; a.ysh = ysh; a.ysn = ysn;
   a.B = static_cast<int>(x.B); a.H = static_cast<int>(x.H); a.N = static_cast<int>(x.N);
   a.inverse = inverse ? 1 : 0;
-  const int64_t rows = x.B * x.H * x.N;
-  if (rows == 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int rpb = 8 * (32 / (static_cast<int>(x.d) / 8));  // rows per CTA per step
-  int64_t want = (rows + rpb - 1) / rpb;
-  int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;  // 8 resident CTAs of 256 threads per SM
-  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  a.status = status;
+  if (x.B * x.H * x.N == 0) return cudaSuccess;
+  const int rows = PERM_U * 256 / static_cast<int>(x.d / 8);
+  dim3 grid(static_cast<unsigned>((x.N + rows - 1) / rows), static_cast<unsigned>(x.H), static_cast<unsigned>(x.B));
   if (x.d == 128)
     permute_kernel<128><<<grid, 256, 0, st>>>(a);
   else

@@ -187,7 +187,11 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
  * reordering improves token locality and sparsity for visual tasks).
  * perm (device, int32, length N): y[:, :, t, :] = x[:, :, perm[t], :] (permute) and
  * y[:, :, perm[t], :] = x[:, :, t, :] (unpermute).  x and y have the same shape; they must
- * not overlap.  perm must be a permutation of 0..N-1 (not checked on the device).
+ * not overlap.  perm should be a permutation of 0..N-1.  An entry outside 0..N-1 is never used
+ * as an address: its token row is skipped (left unwritten in y) and the kernel records
+ * SPARGE_ERR_INVALID_ARG in the device status word (read by sparge_get_device_status).  Entries
+ * in range that repeat leave some rows of y unwritten (permute) or written more than once
+ * (unpermute, last writer unspecified).
  */
 int sparge_permute_tokens(const sparge_tensor *x, const int32_t *perm, sparge_tensor *y,
                           sparge_stream_t stream);
@@ -234,8 +238,10 @@ int sparge_selftest_bounded_wait(int64_t limit_ns, sparge_stream_t stream);
 /* Message of the last failed call on this thread ("" if none). */
 const char *sparge_last_error(void);
 
-/* Reads and clears the device status word after synchronising the stream: SPARGE_OK or
- * SPARGE_ERR_DEVICE_TIMEOUT (or SPARGE_ERR_CUDA if the read itself failed). */
+/* Reads and clears the device status word after synchronising the stream: SPARGE_OK,
+ * SPARGE_ERR_DEVICE_TIMEOUT (a bounded wait ran out), SPARGE_ERR_INVALID_ARG (a permutation entry
+ * outside 0..N-1 was skipped), or SPARGE_ERR_CUDA if the read itself failed.  The first code
+ * recorded since the last read is kept. */
 int sparge_get_device_status(sparge_stream_t stream);
 
 #ifdef __cplusplus

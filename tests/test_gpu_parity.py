@@ -221,6 +221,63 @@ def test_hilbert_pipeline(key):
     assert cos >= COS_MIN and err <= MAXABS, (cos, err)
 
 
+@pytest.mark.parametrize("d,N", [(64, 1000), (128, 777), (128, 4096 + 33)])
+def test_permute_strided_ragged(d, N):
+    """Gather and scatter bit-exact against numpy on strided views (token stride 2d, heads
+    interleaved) with N not a multiple of the kernel's row chunk."""
+    rng = np.random.Generator(np.random.PCG64(N + d))
+    B, H = 2, 3
+    perm_np = rng.permutation(N).astype(np.int32)
+    perm = torch.from_numpy(perm_np).cuda()
+    base = torch.randn((B, N, H, 2 * d), generator=torch.Generator().manual_seed(N), dtype=torch.float32)
+    x = base.to(torch.bfloat16).cuda().permute(0, 2, 1, 3)[..., :d]     # (B, H, N, d), stride_n = 2 H d
+    yb = torch.zeros((B, H, N, 2 * d), dtype=torch.bfloat16, device="cuda")
+    y = yb[..., d:]                                                     # stride_n = 2 d, offset d
+    fbs.permute_tokens(x, perm, out=y)
+    xn = x.float().cpu().numpy()
+    np.testing.assert_array_equal(y.float().cpu().numpy(), xn[:, :, perm_np])
+    assert not yb[..., :d].any()                                        # nothing written outside y
+    z = torch.empty_like(x)
+    fbs.unpermute_tokens(y, perm, out=z)
+    np.testing.assert_array_equal(z.float().cpu().numpy(), xn)
+    assert fbs.device_status() == fbs.SPARGE_OK
+
+
+def test_permute_skips_entries_out_of_range():
+    """Entries outside 0..N-1 are never used as addresses: their rows are left as they were and
+    the device status word reports SPARGE_ERR_INVALID_ARG once; the next valid call is clean."""
+    N, d = 300, 64
+    rng = np.random.Generator(np.random.PCG64(5))
+    perm_np = rng.permutation(N).astype(np.int32)
+    bad = [3, 150, 299]
+    perm_np[bad[0]], perm_np[bad[1]], perm_np[bad[2]] = -1, N, 1 << 30
+    perm = torch.from_numpy(perm_np).cuda()
+    x = torch.randn((1, 2, N, d), generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).cuda()
+    sentinel = torch.full_like(x, 7.0)
+    y = sentinel.clone()
+    torch.cuda.synchronize()
+    assert fbs.device_status() == fbs.SPARGE_OK
+    fbs.permute_tokens(x, perm, out=y)
+    torch.cuda.synchronize()
+    assert fbs.device_status() == fbs.SPARGE_ERR_INVALID_ARG
+    assert b"permutation entry" in fbs.lib().sparge_last_error()
+    assert fbs.device_status() == fbs.SPARGE_OK                 # reading clears the word
+    good = np.setdiff1d(np.arange(N), bad)
+    xn, yn = x.float().cpu().numpy(), y.float().cpu().numpy()
+    np.testing.assert_array_equal(yn[:, :, good], xn[:, :, perm_np[good]])
+    assert (yn[:, :, bad] == 7.0).all()
+    z = sentinel.clone()
+    fbs.unpermute_tokens(x, perm, out=z)
+    torch.cuda.synchronize()
+    assert fbs.device_status() == fbs.SPARGE_ERR_INVALID_ARG
+    zn = z.float().cpu().numpy()
+    np.testing.assert_array_equal(zn[:, :, perm_np[good]], xn[:, :, good])
+    untouched = np.setdiff1d(np.arange(N), perm_np[good])
+    assert (zn[:, :, untouched] == 7.0).all()
+    fbs.permute_tokens(x, torch.arange(N, dtype=torch.int32, device="cuda"), out=y)
+    assert torch.equal(y, x) and fbs.device_status() == fbs.SPARGE_OK
+
+
 def test_empty_and_degenerate_shapes():
     for N in (1, 63, 64, 65, 127, 129):
         qu, ku, vu = W.random_qkv(25, 1, 2, 1, N, 128)
