@@ -9,9 +9,9 @@
 //   (max over the head's tokens), stored channel-major.  INT8 tensor-core products (tcgen05 kind::i8) are not available
 //   on sm_103a, so Q.K^T also runs in e4m3 (kind::f8f6f4).
 //
-// Kernels: per-chunk partial sums of K and maxima of |V| per (batch, KV head, channel); their
-// reduction into the K mean and the V scales; one warp per query / key block for Q and K~
-// (block maximum, then quantise); a tiled transpose for V.
+// Kernels: per-chunk partial sums of K (and maxima of |V| when V is quantised) per (batch, KV
+// head, channel); their reduction into the K mean and the V scales; one CTA per query / key block
+// for Q and K~ (block maximum, then quantise, the block held in registers); a tiled transpose for V.
 #include <algorithm>
 
 #include "common.cuh"
@@ -23,8 +23,11 @@ namespace {
 constexpr int CHUNK = 2048;    // tokens per partial of the K mean / V maximum
 constexpr float E4M3_MAX = 448.f;
 
-// grid (B*Hkv, chunks); 256 threads: 16 lanes per token (d = 128) or 8 (d = 64), 8 dims per lane
-template <int D>
+// grid (B*Hkv, chunks); 256 threads: 16 lanes per token (d = 128) or 8 (d = 64), 8 dims per lane;
+// each lane loads U tokens (of K, and of V when its scales are wanted) before it accumulates.
+constexpr int U = 4;
+
+template <int D, bool WITH_V>
 __global__ void __launch_bounds__(256) kv_partials_kernel(const __nv_bfloat16 *k, int64_t ksb, int64_t ksh,
                                                           int64_t ksn, const __nv_bfloat16 *v, int64_t vsb,
                                                           int64_t vsh, int64_t vsn, int Hkv, int N,
@@ -34,19 +37,33 @@ __global__ void __launch_bounds__(256) kv_partials_kernel(const __nv_bfloat16 *k
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane / LPT, p = lane % LPT;
   const int bh = blockIdx.x, b = bh / Hkv, h = bh % Hkv;
   const int t0 = blockIdx.y * CHUNK, t1 = min(N, t0 + CHUNK);
+  const __nv_bfloat16 *kb = k + b * ksb + h * ksh + p * 8, *vb = v + b * vsb + h * vsh + p * 8;
   float s[8], mx[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) s[c] = mx[c] = 0.f;
-  for (int t = t0 + w * TPW + sub; t < t1; t += TPS) {
-    const uint4 kv = ld_stream_v4(k + b * ksb + h * ksh + static_cast<int64_t>(t) * ksn + p * 8);
-    const uint4 vv = ld_stream_v4(v + b * vsb + h * vsh + static_cast<int64_t>(t) * vsn + p * 8);
-    const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
+  for (int t = t0 + w * TPW + sub; t < t1; t += U * TPS) {
+    uint4 kx[U], vx[U];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      s[2 * c] += bf16lo(kw[c]);
-      s[2 * c + 1] += bf16hi(kw[c]);
-      mx[2 * c] = fmaxf(mx[2 * c], fabsf(bf16lo(vw[c])));
-      mx[2 * c + 1] = fmaxf(mx[2 * c + 1], fabsf(bf16hi(vw[c])));
+    for (int u = 0; u < U; ++u) {
+      const int tt = t + u * TPS;
+      kx[u] = vx[u] = make_uint4(0, 0, 0, 0);  // zeros add nothing to the sum or the maximum
+      if (tt < t1) {
+        kx[u] = ld_stream_v4(kb + static_cast<int64_t>(tt) * ksn);
+        if (WITH_V) vx[u] = ld_stream_v4(vb + static_cast<int64_t>(tt) * vsn);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t kw[4] = {kx[u].x, kx[u].y, kx[u].z, kx[u].w}, vw[4] = {vx[u].x, vx[u].y, vx[u].z, vx[u].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        s[2 * c] += bf16lo(kw[c]);
+        s[2 * c + 1] += bf16hi(kw[c]);
+        if (WITH_V) {
+          mx[2 * c] = fmaxf(mx[2 * c], fabsf(bf16lo(vw[c])));
+          mx[2 * c + 1] = fmaxf(mx[2 * c + 1], fabsf(bf16hi(vw[c])));
+        }
+      }
     }
   }
 #pragma unroll
@@ -76,9 +93,9 @@ __global__ void __launch_bounds__(256) kv_partials_kernel(const __nv_bfloat16 *k
   }
 }
 
-// grid B*Hkv, D threads: K mean and V scale per channel
+// grid B*Hkv, D threads: K mean and (with_v) V scale per channel
 template <int D>
-__global__ void kv_finish_kernel(const float *part, int nchunks, int N, float *kmean, float *sv) {
+__global__ void kv_finish_kernel(const float *part, int nchunks, int N, int with_v, float *kmean, float *sv) {
   const int bh = blockIdx.x, c = threadIdx.x;
   float ss = 0.f, mm = 0.f;
   for (int k = 0; k < nchunks; ++k) {
@@ -87,45 +104,59 @@ __global__ void kv_finish_kernel(const float *part, int nchunks, int N, float *k
     mm = fmaxf(mm, src[D + c]);
   }
   kmean[static_cast<int64_t>(bh) * D + c] = ss / static_cast<float>(N);
-  sv[static_cast<int64_t>(bh) * D + c] = mm > 0.f ? mm / E4M3_MAX : 1.f;
+  if (with_v) sv[static_cast<int64_t>(bh) * D + c] = mm > 0.f ? mm / E4M3_MAX : 1.f;
 }
 
-// One warp per block of `blk` tokens: x (minus the per-channel mean when given) -> e4m3 with one
-// scale for the block.  out is contiguous [B][H][N][D] bytes; scale[(b H + h) nblk + blockidx].
-template <int D>
+// One CTA of 256 threads per block of ROWS tokens, held in registers between the two steps (one
+// read of the block): the block maximum of |x - mean| (mean per channel when given, else 0), the
+// scale max / 448, then the e4m3 codes.  Grid: one CTA per (b h, block), x = bh * nblk + block.
+// out is contiguous [B][H][N][D] bytes; scale[bh * nblk + block].
+template <int D, int ROWS>
 __global__ void __launch_bounds__(256) quant_block_kernel(const __nv_bfloat16 *x, int64_t sb, int64_t sh,
-                                                          int64_t sn, int H, int N, int blk, int nblk,
-                                                          const float *mean, uint8_t *out, float *scale,
-                                                          int64_t nblocks) {
-  constexpr int LPT = D / 8, TPW = 32 / LPT;
-  const int lane = threadIdx.x & 31, sub = lane / LPT, p = lane % LPT;
-  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (wid >= nblocks) return;
-  const int bi = static_cast<int>(wid % nblk);
-  const int64_t bh = wid / nblk;
-  const int h = static_cast<int>(bh % H), b = static_cast<int>(bh / H);
-  const int t0 = bi * blk, t1 = min(N, t0 + blk);
+                                                          int64_t sn, int H, int N, int nblk,
+                                                          const float *mean, uint8_t *out, float *scale) {
+  constexpr int LPT = D / 8, TPC = 256 / LPT;  // tokens per CTA-wide load
+  constexpr int STEPS = ROWS / TPC;
+  __shared__ float red[8];
+  const int bi = static_cast<int>(blockIdx.x % static_cast<unsigned>(nblk));
+  const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(nblk));
+  const int h = bh % H, b = bh / H;
+  const int tok = threadIdx.x / LPT, p = threadIdx.x % LPT;
+  const int t0 = bi * ROWS;
   float mu[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) mu[c] = mean ? mean[bh * D + p * 8 + c] : 0.f;
-  const __nv_bfloat16 *base = x + b * sb + h * sh;
+  for (int c = 0; c < 8; ++c) mu[c] = mean ? mean[static_cast<int64_t>(bh) * D + p * 8 + c] : 0.f;
+  const __nv_bfloat16 *base = x + b * sb + h * sh + p * 8;
+  uint4 xv[STEPS];
+#pragma unroll
+  for (int s = 0; s < STEPS; ++s) {
+    const int t = t0 + s * TPC + tok;
+    xv[s] = t < N ? ld_stream_v4(base + static_cast<int64_t>(t) * sn) : make_uint4(0, 0, 0, 0);
+  }
   float m = 0.f;
-  for (int t = t0 + sub; t < t1; t += TPW) {
-    const uint4 v = ld_stream_v4(base + static_cast<int64_t>(t) * sn + p * 8);
-    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int s = 0; s < STEPS; ++s) {
+    if (t0 + s * TPC + tok >= N) continue;  // rows past N do not count (0 - mean would)
+    const uint32_t wd[4] = {xv[s].x, xv[s].y, xv[s].z, xv[s].w};
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       m = fmaxf(m, fmaxf(fabsf(bf16lo(wd[c]) - mu[2 * c]), fabsf(bf16hi(wd[c]) - mu[2 * c + 1])));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  const float s = m > 0.f ? m / E4M3_MAX : 1.f;
-  const float inv = 1.f / s;
-  if (lane == 0) scale[wid] = s;
-  uint8_t *obase = out + (static_cast<int64_t>(b) * H + h) * static_cast<int64_t>(N) * D;
-  for (int t = t0 + sub; t < t1; t += TPW) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(base + static_cast<int64_t>(t) * sn + p * 8);
-    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < 8; ++w) m = fmaxf(m, red[w]);
+  const float sc = m > 0.f ? m / E4M3_MAX : 1.f;
+  const float inv = 1.f / sc;
+  if (threadIdx.x == 0) scale[blockIdx.x] = sc;
+  uint8_t *obase = out + static_cast<int64_t>(bh) * N * D + p * 8;
+#pragma unroll
+  for (int s = 0; s < STEPS; ++s) {
+    const int t = t0 + s * TPC + tok;
+    if (t >= N) continue;
+    const uint32_t wd[4] = {xv[s].x, xv[s].y, xv[s].z, xv[s].w};
     float f[8];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -135,48 +166,58 @@ __global__ void __launch_bounds__(256) quant_block_kernel(const __nv_bfloat16 *x
     uint2 o;
     o.x = pack_e4m3x4(f[0], f[1], f[2], f[3]);
     o.y = pack_e4m3x4(f[4], f[5], f[6], f[7]);
-    *reinterpret_cast<uint2 *>(obase + static_cast<int64_t>(t) * D + p * 8) = o;
+    *reinterpret_cast<uint2 *>(obase + static_cast<int64_t>(t) * D) = o;
   }
 }
 
 // V -> e4m3 with a scale per (batch, KV head, channel), written channel-major: out is
 // [B][Hkv][D][npad] bytes (npad = N rounded up to 64, the tail zero), so that a 64-key tile is a
-// K-major operand of P.V.  grid (B*Hkv, npad / 64), 256 threads; each CTA transposes one tile of
-// 64 keys through shared memory.
+// K-major operand of P.V.  grid (B*Hkv, npad / 64), 256 threads.  Each CTA quantises one tile of
+// 64 keys into shared memory token-major (coalesced 16-byte loads, all issued first; 8-byte
+// stores), then each of D * 2 threads gathers 32 keys of one channel and writes them as two
+// 16-byte pieces (one whole 32-byte sector).
 template <int D>
 __global__ void __launch_bounds__(256) quant_vt_kernel(const __nv_bfloat16 *v, int64_t sb, int64_t sh, int64_t sn,
                                                        int H, int N, int npad, const float *sv, uint8_t *out) {
-  constexpr int VPR = D / 8;  // 16-byte input vectors per token
-  __shared__ __align__(16) uint8_t tile[D][64];
+  constexpr int VPR = D / 8;           // 16-byte input pieces per token
+  constexpr int TPC = 256 / VPR;       // tokens per CTA-wide load
+  constexpr int STEPS = 64 / TPC;
+  __shared__ __align__(16) uint8_t tile[64][D];  // token-major codes
   const int bh = blockIdx.x, b = bh / H, h = bh % H;
   const int t0 = blockIdx.y * 64;
-  const __nv_bfloat16 *base = v + b * sb + h * sh;
-  for (int e = threadIdx.x; e < 64 * VPR; e += blockDim.x) {
-    const int tt = e / VPR, p = e % VPR, t = t0 + tt;
-    uint8_t q[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (t < N) {
-      const uint4 x = ld_stream_v4(base + static_cast<int64_t>(t) * sn + p * 8);
-      const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
-      const float *s = sv + static_cast<int64_t>(bh) * D + p * 8;
-      const uint32_t w0 = pack_e4m3x4(bf16lo(wd[0]) / s[0], bf16hi(wd[0]) / s[1], bf16lo(wd[1]) / s[2],
-                                      bf16hi(wd[1]) / s[3]);
-      const uint32_t w1 = pack_e4m3x4(bf16lo(wd[2]) / s[4], bf16hi(wd[2]) / s[5], bf16lo(wd[3]) / s[6],
-                                      bf16hi(wd[3]) / s[7]);
+  const int tok = threadIdx.x / VPR, p = threadIdx.x % VPR;
+  const __nv_bfloat16 *base = v + b * sb + h * sh + p * 8;
+  float inv[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        q[c] = static_cast<uint8_t>(w0 >> (8 * c));
-        q[4 + c] = static_cast<uint8_t>(w1 >> (8 * c));
-      }
-    }
+  for (int c = 0; c < 8; ++c) inv[c] = 1.f / sv[static_cast<int64_t>(bh) * D + p * 8 + c];
+  uint4 xv[STEPS];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) tile[p * 8 + c][tt] = q[c];
+  for (int s = 0; s < STEPS; ++s) {
+    const int t = t0 + s * TPC + tok;
+    xv[s] = t < N ? ld_stream_v4(base + static_cast<int64_t>(t) * sn) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int s = 0; s < STEPS; ++s) {
+    const uint32_t wd[4] = {xv[s].x, xv[s].y, xv[s].z, xv[s].w};
+    uint2 o;
+    o.x = pack_e4m3x4(bf16lo(wd[0]) * inv[0], bf16hi(wd[0]) * inv[1], bf16lo(wd[1]) * inv[2], bf16hi(wd[1]) * inv[3]);
+    o.y = pack_e4m3x4(bf16lo(wd[2]) * inv[4], bf16hi(wd[2]) * inv[5], bf16lo(wd[3]) * inv[6], bf16hi(wd[3]) * inv[7]);
+    *reinterpret_cast<uint2 *>(&tile[s * TPC + tok][p * 8]) = o;  // zero codes past N
   }
   __syncthreads();
   uint8_t *obase = out + static_cast<int64_t>(bh) * D * npad + t0;
-  for (int e = threadIdx.x; e < D * 4; e += blockDim.x) {
-    const int ch = e >> 2, part = e & 3;
-    *reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(ch) * npad + 16 * part) =
-        *reinterpret_cast<const uint4 *>(&tile[ch][16 * part]);
+  for (int e = threadIdx.x; e < D * 2; e += 256) {
+    const int ch = e % D, half = e / D;  // keys 32 half .. 32 half + 31 of channel ch
+    uint32_t wv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = 32 * half + 4 * j;
+      wv[j] = static_cast<uint32_t>(tile[r][ch]) | (static_cast<uint32_t>(tile[r + 1][ch]) << 8) |
+              (static_cast<uint32_t>(tile[r + 2][ch]) << 16) | (static_cast<uint32_t>(tile[r + 3][ch]) << 24);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(ch) * npad + 32 * half);
+    dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
   }
 }
 
@@ -185,20 +226,22 @@ cudaError_t run(const View &q, const View &k, const View &v, const Q8Ws &w, bool
   const int B = static_cast<int>(q.B), Hq = static_cast<int>(q.H), Hkv = static_cast<int>(k.H);
   const int N = static_cast<int>(q.N);
   const int nchunks = (N + CHUNK - 1) / CHUNK;
-  kv_partials_kernel<D><<<dim3(B * Hkv, nchunks), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16 *>(k.data), k.sb, k.sh, k.sn, static_cast<const __nv_bfloat16 *>(v.data),
-      v.sb, v.sh, v.sn, Hkv, N, w.partial);
-  kv_finish_kernel<D><<<B * Hkv, D, 0, st>>>(w.partial, nchunks, N, w.kmean, w.sv);
+  const dim3 pgrid(B * Hkv, nchunks);
+  const __nv_bfloat16 *kp = static_cast<const __nv_bfloat16 *>(k.data), *vp = static_cast<const __nv_bfloat16 *>(v.data);
+  if (quant_v)
+    kv_partials_kernel<D, true><<<pgrid, 256, 0, st>>>(kp, k.sb, k.sh, k.sn, vp, v.sb, v.sh, v.sn, Hkv, N, w.partial);
+  else
+    kv_partials_kernel<D, false><<<pgrid, 256, 0, st>>>(kp, k.sb, k.sh, k.sn, vp, v.sb, v.sh, v.sn, Hkv, N, w.partial);
+  kv_finish_kernel<D><<<B * Hkv, D, 0, st>>>(w.partial, nchunks, N, quant_v ? 1 : 0, w.kmean, w.sv);
   const int nqb = (N + QBLK - 1) / QBLK, nkb = (N + KBLK - 1) / KBLK;
   const int64_t nq = static_cast<int64_t>(B) * Hq * nqb, nk = static_cast<int64_t>(B) * Hkv * nkb;
-  quant_block_kernel<D><<<static_cast<unsigned>((nq + 7) / 8), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16 *>(q.data), q.sb, q.sh, q.sn, Hq, N, QBLK, nqb, nullptr, w.q8, w.sq, nq);
-  quant_block_kernel<D><<<static_cast<unsigned>((nk + 7) / 8), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16 *>(k.data), k.sb, k.sh, k.sn, Hkv, N, KBLK, nkb, w.kmean, w.k8, w.sk, nk);
+  quant_block_kernel<D, QBLK><<<static_cast<unsigned>(nq), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16 *>(q.data), q.sb, q.sh, q.sn, Hq, N, nqb, nullptr, w.q8, w.sq);
+  quant_block_kernel<D, KBLK><<<static_cast<unsigned>(nk), 256, 0, st>>>(kp, k.sb, k.sh, k.sn, Hkv, N, nkb, w.kmean,
+                                                                          w.k8, w.sk);
   const int npad = (N + 63) / 64 * 64;
   if (quant_v)
-    quant_vt_kernel<D><<<dim3(B * Hkv, npad / 64), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(v.data), v.sb, v.sh,
-                                                              v.sn, Hkv, N, npad, w.sv, w.v8);
+    quant_vt_kernel<D><<<dim3(B * Hkv, npad / 64), 256, 0, st>>>(vp, v.sb, v.sh, v.sn, Hkv, N, npad, w.sv, w.v8);
   return cudaGetLastError();
 }
 
