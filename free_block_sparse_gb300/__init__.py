@@ -49,7 +49,9 @@ class sparge_tensor(ctypes.Structure):
 
 class sparge_params(ctypes.Structure):
     _fields_ = [("theta", ctypes.c_float), ("lambda_", ctypes.c_float), ("scale", ctypes.c_float),
-                ("precision", ctypes.c_int32), ("stats", ctypes.c_void_p), ("timing_events", ctypes.c_void_p)]
+                ("precision", ctypes.c_int32), ("stats", ctypes.c_void_p), ("timing_events", ctypes.c_void_p),
+                ("topk_per_head", ctypes.c_void_p), ("theta_per_head", ctypes.c_void_p),
+                ("lambda_per_head", ctypes.c_void_p)]
 
 
 _lib = None
@@ -59,6 +61,9 @@ EXPORTS = {
     "sparge_predict_mask": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_float,
                                            ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                            ctypes.c_void_p]),
+    "sparge_predict_mask_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_int,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                              ctypes.c_void_p]),
     "sparge_block_sparse_attn": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                 ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
@@ -154,6 +159,22 @@ def predict_mask(q, k, topk: float, theta: float = 0.5, causal: bool = False, ws
     return mask
 
 
+def predict_mask_ex(q, k, topk: float, causal: bool = False, theta: float = 0.5, scale: float = 0.0,
+                    topk_per_head=None, theta_per_head=None, ws=None, mask=None, events=None):
+    """predict_mask with an explicit pooled-score scale, optional per-query-head topk and theta
+    (float32 CUDA tensors of Hq entries) and optional timing events ([0]-[3] are recorded)."""
+    torch = _torch()
+    B, Hq, N, _ = q.shape
+    if mask is None:
+        mask = torch.empty((B, Hq, -(-N // 128), -(-N // 64)), dtype=torch.uint8, device=q.device)
+    ws = _workspace(SPARGE_OP_PREDICT_MASK, q, k, ws)
+    p = _params(theta, -math.inf, scale, SPARGE_PRECISION_BF16, None, events, topk_per_head, theta_per_head)
+    dq, dk = _desc(q), _desc(k)
+    _check(lib().sparge_predict_mask_ex(ctypes.byref(dq), ctypes.byref(dk), float(topk), int(causal), ctypes.byref(p),
+                                        mask.data_ptr(), ws.data_ptr(), ws.numel(), _stream()))
+    return mask
+
+
 def predict_ws_views(ws, B, Hq, Hkv, N, d):
     """Views of the stage-1 workspace after predict_mask: muQ (B,Hq,nqb,d), sQ (B,Hq,nqb),
     muK (B,Hkv,nkb,d), sK (B,Hkv,nkb) and the scaled pooled scores S (B,Hq,nqb,nkb), following
@@ -243,9 +264,21 @@ def sparge_attn(q, k, v, topk: float = 0.5, causal: bool = False, out=None, ws=N
     return out
 
 
-def _params(theta, lam, scale, precision, stats, events):
+def _head_array(x, name):
+    """A per-head parameter array as a device pointer (0 for None); x is a float32 CUDA tensor."""
+    if x is None:
+        return 0
+    torch = _torch()
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32 and x.dim() == 1
+            and x.is_contiguous()):
+        raise TypeError("%s must be a contiguous float32 CUDA tensor of Hq entries" % name)
+    return x.data_ptr()
+
+
+def _params(theta, lam, scale, precision, stats, events, topk_h=None, theta_h=None, lam_h=None):
     """A sparge_params; `events` (6 torch.cuda.Event or None) are passed as cudaEvent_t handles.
-    The handle array is kept on the returned struct so it outlives the call."""
+    The handle array is kept on the returned struct so it outlives the call.  topk_h, theta_h and
+    lam_h are optional per-query-head float32 CUDA tensors."""
     evp = None
     if events is not None:
         assert len(events) == 6
@@ -255,22 +288,27 @@ def _params(theta, lam, scale, precision, stats, events):
         evp = (ctypes.c_void_p * 6)(*[ev.cuda_event for ev in events])
     p = sparge_params(float(theta), float(lam), float(scale), int(precision),
                       0 if stats is None else stats.data_ptr(),
-                      ctypes.cast(evp, ctypes.c_void_p) if evp is not None else None)
+                      ctypes.cast(evp, ctypes.c_void_p) if evp is not None else None,
+                      _head_array(topk_h, "topk_per_head"), _head_array(theta_h, "theta_per_head"),
+                      _head_array(lam_h, "lambda_per_head"))
     p._evp = evp
+    p._arrays = (topk_h, theta_h, lam_h)
     return p
 
 
 def block_sparse_attn_ex(q, k, v, mask=None, causal: bool = False, lam: float = -math.inf, scale: float = 0.0,
-                         precision: int = SPARGE_PRECISION_BF16, stats=None, out=None, ws=None, events=None):
-    """block_sparse_attn with an explicit scale and optional timing events (6 torch.cuda.Event:
-    [0] before the V copy or quantisation, [4] after it, [5] after the attention kernel)."""
+                         precision: int = SPARGE_PRECISION_BF16, stats=None, out=None, ws=None, events=None,
+                         lambda_per_head=None):
+    """block_sparse_attn with an explicit scale, optional timing events (6 torch.cuda.Event:
+    [0] before the V copy or quantisation, [4] after it, [5] after the attention kernel) and an
+    optional per-query-head lambda (float32 CUDA tensor of Hq entries)."""
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
     op = SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 if precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV) \
         else SPARGE_OP_BLOCK_SPARSE_ATTN
     ws = _workspace(op, q, k, ws)
-    p = _params(0.5, lam, scale, precision, stats, events)
+    p = _params(0.5, lam, scale, precision, stats, events, lam_h=lambda_per_head)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     mp = 0 if mask is None else mask.data_ptr()
     _check(lib().sparge_block_sparse_attn_ex(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), mp, int(causal),
@@ -280,15 +318,16 @@ def block_sparse_attn_ex(q, k, v, mask=None, causal: bool = False, lam: float = 
 
 def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: float = -math.inf,
                    scale: float = 0.0, precision: int = SPARGE_PRECISION_BF16, stats=None, mask_out=None,
-                   out=None, ws=None, events=None):
-    """sparge_attn with explicit theta, lambda, scale, counters, an optional mask output and
-    optional timing events (6 torch.cuda.Event, recorded around the five kernels)."""
+                   out=None, ws=None, events=None, topk_per_head=None, theta_per_head=None, lambda_per_head=None):
+    """sparge_attn with explicit theta, lambda, scale, counters, an optional mask output,
+    optional timing events (6 torch.cuda.Event, recorded around the five kernels) and optional
+    per-query-head topk, theta and lambda (float32 CUDA tensors of Hq entries)."""
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
     q8 = precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV)
     ws = _workspace(SPARGE_OP_ATTN_Q8 if q8 else SPARGE_OP_ATTN, q, k, ws)
-    p = _params(theta, lam, scale, precision, stats, events)
+    p = _params(theta, lam, scale, precision, stats, events, topk_per_head, theta_per_head, lambda_per_head)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     mp = 0 if mask_out is None else mask_out.data_ptr()
     _check(lib().sparge_attn_ex(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), float(topk), int(causal),

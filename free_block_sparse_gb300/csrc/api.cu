@@ -183,8 +183,13 @@ int record_event(void *const *ev, int idx, cudaStream_t s) {
   return e == cudaSuccess ? SPARGE_OK : cuda_fail(e, "timing event record");
 }
 
+// Per-query-head parameter arrays of a sparge_params (device pointers, each may be null).
+struct HeadParams {
+  const float *topk = nullptr, *theta = nullptr, *lambda = nullptr;
+};
+
 int predict_impl(const View &q, const View &k, float topk, float theta, int causal, float scale, uint8_t *mask,
-                 void *ws, size_t ws_bytes, cudaStream_t s, void *const *ev = nullptr) {
+                 void *ws, size_t ws_bytes, cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {}) {
   if (!mask) return fail(SPARGE_ERR_INVALID_ARG, "mask is NULL");
   if (q.N > 131072) return fail(SPARGE_ERR_UNSUPPORTED, "mask prediction supports N <= 131072 (got %lld)", (long long)q.N);
   if (q.B * q.H * cdiv(q.N, QBLK) > 0x7fffffffLL)
@@ -216,7 +221,8 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
     if (e != cudaSuccess) return cuda_fail(e, "score_gemm launch");
     if ((rc = record_event(ev, 2, s))) return rc;
   }
-  e = launch_score_select(pw, (int)q.B, (int)q.H, (int)k.H, (int)q.N, (int)q.d, topk, theta, causal, mask, s);
+  e = launch_score_select(pw, (int)q.B, (int)q.H, (int)k.H, (int)q.N, (int)q.d, topk, theta, causal, mask, hp.topk,
+                          hp.theta, status_ptr(), s);
   if (e != cudaSuccess) return cuda_fail(e, "score_select launch");
   return record_event(ev, 3, s);
 }
@@ -233,7 +239,7 @@ size_t attn_ws_bytes(int precision, int64_t B, int64_t Hq, int64_t Hkv, int64_t 
 
 int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, float lambda, int causal, float scale,
               int precision, sparge_tensor *o, unsigned long long *stats, void *ws, size_t ws_bytes,
-              cudaStream_t s, void *const *ev = nullptr) {
+              cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {}) {
   if (precision != SPARGE_PRECISION_BF16 && !is_q8(precision))
     return fail(SPARGE_ERR_UNSUPPORTED, "precision %d not supported", precision);
   const bool q8 = is_q8(precision), pv8 = precision == SPARGE_PRECISION_Q8_FP8PV;
@@ -289,6 +295,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   l.causal = causal ? 1 : 0;
   l.scale = scale;
   l.lambda = lambda;
+  l.lambda_h = hp.lambda;
   l.stats = stats;
   l.status = status_ptr();
   cudaError_t e = launch_bsattn(l, s);
@@ -390,6 +397,24 @@ int sparge_predict_mask(const sparge_tensor *q, const sparge_tensor *k, float to
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
+int sparge_predict_mask_ex(const sparge_tensor *q, const sparge_tensor *k, float topk, int is_causal,
+                           const sparge_params *p, uint8_t *mask, void *ws, size_t ws_bytes, sparge_stream_t stream) {
+  g_last_error[0] = 0;
+  if (!p) return fail(SPARGE_ERR_INVALID_ARG, "params is NULL");
+  View qv, kv;
+  int rc;
+  if ((rc = check_tensor(q, "q", &qv)) || (rc = check_tensor(k, "k", &kv)) || (rc = check_qk(qv, kv))) return rc;
+  if ((rc = check_topk_theta(topk, p->theta))) return rc;
+  if (std::isnan(p->scale) || p->scale < 0.f || std::isinf(p->scale))
+    return fail(SPARGE_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)qv.d);
+  HeadParams hp;
+  hp.topk = p->topk_per_head;
+  hp.theta = p->theta_per_head;
+  return predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, ws_bytes,
+                      reinterpret_cast<cudaStream_t>(stream), p->timing_events, hp);
+}
+
 int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v,
                              const uint8_t *mask, float lambda, int is_causal, int precision, sparge_tensor *o,
                              void *ws, size_t ws_bytes, unsigned long long *stats, sparge_stream_t stream) {
@@ -420,8 +445,10 @@ int sparge_block_sparse_attn_ex(const sparge_tensor *q, const sparge_tensor *k, 
   const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)qv.d);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = record_event(p->timing_events, 0, s))) return rc;
+  HeadParams hp;
+  hp.lambda = p->lambda_per_head;
   return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws, ws_bytes, s,
-                   p->timing_events);
+                   p->timing_events, hp);
 }
 
 int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,
@@ -448,15 +475,20 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   uint8_t *mask = mask_out ? mask_out : static_cast<uint8_t *>(ws) + need_pred;
   void *ws_v = static_cast<uint8_t *>(ws) + need_pred + mask_bytes;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s, p->timing_events)))
+  HeadParams hp;
+  hp.topk = p->topk_per_head;
+  hp.theta = p->theta_per_head;
+  hp.lambda = p->lambda_per_head;
+  if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s, p->timing_events, hp)))
     return rc;
   return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws_v, need_v, s,
-                   p->timing_events);
+                   p->timing_events, hp);
 }
 
 int sparge_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,
                 sparge_tensor *o, void *ws, size_t ws_bytes, sparge_stream_t stream) {
   sparge_params p;
+  memset(&p, 0, sizeof(p));  // every optional pointer null
   p.theta = 0.5f;
   p.lambda = -INFINITY;
   p.scale = 0.f;

@@ -46,6 +46,7 @@ struct AttnArgs {
   int64_t o_sb, o_sh, o_sn;
   int B, Hq, Hkv, G, N, nqb, nkb, causal;
   float scale_log2, lam_log2;
+  const float *lam_h;  // lambda per query head (natural-log units), or nullptr
   unsigned long long *stats;
   int *status;
   const float *sq, *sk, *sv;  // 8-bit path: scales of the Q blocks, K blocks and V channels
@@ -360,6 +361,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     bool ok = true;
     constexpr float RESC = static_cast<float>(PV8 ? RESCALE_LOG2_P8 : RESCALE_LOG2);
     constexpr float POFF = PV8 ? static_cast<float>(8 - RESCALE_LOG2_P8) : 0.f;  // exponent offset of P
+    // this head's filter threshold in log2 units; a bad per-head entry turns the filter off
+    float lam_log2 = a.lam_log2;
+    if (a.lam_h) {
+      const float lh = a.lam_h[h];
+      const bool good = lh <= 0.f;  // false for NaN and for lambda > 0
+      lam_log2 = (!good || lh == -INFINITY) ? -INFINITY : lh * 1.4426950408889634f;
+      if (!good && r == 0) record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
+    }
     float sq_blk = 1.f;
     const float *skrow = nullptr;
     if constexpr (QK8) {
@@ -414,7 +423,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       const float tsc = QK8 ? a.scale_log2 * sq_blk * __ldg(skrow + j) : a.scale_log2;
       const float mloc = mraw * tsc;  // the multiplier is positive: max commutes with it
       const float m_new = fmaxf(m_run, mloc);
-      const bool trailing = !row_ok || mloc == -INFINITY || m_new == -INFINITY || (mloc - m_new < a.lam_log2);
+      const bool trailing = !row_ok || mloc == -INFINITY || m_new == -INFINITY || (mloc - m_new < lam_log2);
       const bool wskip = __all_sync(0xffffffffu, trailing);
       const bool resc = m_new > m_ref + RESC;
       const float alpha = resc ? fast_exp2(m_ref - m_new) : 1.f;
@@ -568,6 +577,7 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
   const float LOG2E = 1.4426950408889634f;
   a.scale_log2 = l.scale * LOG2E;
   a.lam_log2 = (l.lambda == -INFINITY) ? -INFINITY : l.lambda * LOG2E;
+  a.lam_h = l.lambda_h;
   a.stats = l.stats;
   a.status = l.status;
   a.sq = l.sq;

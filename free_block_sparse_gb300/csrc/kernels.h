@@ -57,9 +57,12 @@ struct ScoreGemmLaunch {
 };
 cudaError_t launch_score_gemm(const ScoreGemmLaunch &l, cudaStream_t st);
 
-// Row softmax, cumulative top-k and the always-keep rule on S: writes the uint8 mask.
+// Row softmax, cumulative top-k and the always-keep rule on S: writes the uint8 mask.  topk_h and
+// theta_h (device, Hq floats, or nullptr) override topk and theta per query head; a bad entry is
+// recorded in *status and its head keeps every valid block.
 cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int N, int d, float topk,
-                                float theta, int causal, uint8_t *mask, cudaStream_t st);
+                                float theta, int causal, uint8_t *mask, const float *topk_h, const float *theta_h,
+                                int *status, cudaStream_t st);
 
 struct AttnLaunch {
   CUtensorMap tq, tk, tv;  // 4-D maps (d, N, H, B), 128-byte swizzle, boxes 64 x 128 (Q) / 64 x 64 (K, V);
@@ -71,6 +74,7 @@ struct AttnLaunch {
   int causal;
   float scale;
   float lambda;
+  const float *lambda_h;   // per query head (device, Hq floats) or nullptr; a bad entry turns the filter off
   unsigned long long *stats;
   int *status;
   int q8;                  // 0: bf16 Q.K^T, f16 P.V; 1: e4m3 Q.K^T (maps over the e4m3 copies, scales sq, sk),

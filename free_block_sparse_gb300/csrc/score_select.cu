@@ -38,6 +38,8 @@ struct SelArgs {
   int64_t nkb_pad, rows;
   int Hq, Hkv, G, nqb, nkb, causal;
   float topk, theta;
+  const float *topk_h, *theta_h;  // per query head, or nullptr
+  int *status;
 };
 
 constexpr float LOG2E = 1.4426950408889634f;
@@ -175,8 +177,20 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
   const float *srow = a.S + static_cast<int64_t>(row) * a.nkb_pad;
   const float *sKrow = a.sK + (static_cast<int64_t>(b) * a.Hkv + kvh) * a.nkb_pad;
   const float negm = -a.Smax[row];
+  // this head's parameters; an entry out of range keeps every valid block of the head
+  float topk = a.topk, theta = a.theta;
+  bool bad = false;
+  if (a.topk_h) {
+    const float t = a.topk_h[h];
+    if (t > 0.f && t <= 1.f) topk = t; else { topk = 1.f; bad = true; }
+  }
+  if (a.theta_h) {
+    const float th = a.theta_h[h];
+    if (isfinite(th)) theta = th; else { theta = INFINITY; bad = true; }
+  }
+  if (bad && lane == 0) record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
 
-  const bool keep_all = a.topk >= 1.f || a.sQ[row] < a.theta;
+  const bool keep_all = topk >= 1.f || a.sQ[row] < theta;
   Cut st;
   st.lo = 1u;
   st.hi = 0x3F800001u;  // e <= 1: the maximum gives exactly 1
@@ -184,7 +198,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
   st.nc = 0x7fffffff;
   st.shift = 16;
   if (!keep_all) {
-    const float r2 = log2f(static_cast<float>(nvalid) / (1.f - a.topk)) + 0.1f;
+    const float r2 = log2f(static_cast<float>(nvalid) / (1.f - topk)) + 0.1f;
     while (static_cast<float>(NBIN) * exp2f(static_cast<float>(st.shift - 23)) < r2) ++st.shift;
     hist_zero(H, lane);
   }
@@ -202,7 +216,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
   float et = 2.f;
   int jt = -1;
   if (!keep_all) {
-    const float target = a.topk * Z;
+    const float target = topk * Z;
     bool ok = hist_pick(H, lane, target, st);
     bool listed = false;
     // compact the crossing bin; while it does not fit the short list, split it over the row
@@ -374,7 +388,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
       for (int u = 0; u < 4; ++u) {
         const int j = j0 + u;
         const float e = comp(v, u);
-        const bool keep = j < nvalid && (keep_all || e > et || (e == et && j <= jt) || comp(sk, u) < a.theta);
+        const bool keep = j < nvalid && (keep_all || e > et || (e == et && j <= jt) || comp(sk, u) < theta);
         word |= (keep ? 1u : 0u) << (8 * u);
       }
     }
@@ -404,7 +418,8 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
 }  // namespace
 
 cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int N, int d, float topk,
-                                float theta, int causal, uint8_t *mask, cudaStream_t st) {
+                                float theta, int causal, uint8_t *mask, const float *topk_h, const float *theta_h,
+                                int *status, cudaStream_t st) {
   (void)d;
   SelArgs a;
   a.S = ws.S;
@@ -420,6 +435,9 @@ cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int
   a.rows = static_cast<int64_t>(B) * Hq * a.nqb;
   a.topk = topk;
   a.theta = theta;
+  a.topk_h = topk_h;
+  a.theta_h = theta_h;
+  a.status = status;
   if (a.rows == 0) return cudaSuccess;
   if (a.rows > 0x7fffffffLL) return cudaErrorInvalidValue;  // the kernel indexes rows in 32 bits
   const int64_t grid = (a.rows + WARPS - 1) / WARPS;

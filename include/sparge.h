@@ -74,7 +74,9 @@ typedef struct sparge_tensor {
   int64_t stride_b, stride_h, stride_n; /* in elements */
 } sparge_tensor;
 
-/* Counters the attention kernel can add to (device memory, 4 x uint64, caller-zeroed):
+/* Zero-initialise a sparge_params before setting its fields (sparge_params p = {0};): every
+ * optional pointer must be NULL unless it is meant to be used.
+ * Counters the attention kernel can add to (device memory, 4 x uint64, caller-zeroed):
  *   [0] kept tiles visited, [1] tiles whose P.V product was issued,
  *   [2] (32-row group, tile) pairs whose P.V update the lambda filter skipped,
  *   [3] valid tiles (tiles not wholly above the causal diagonal). */
@@ -87,6 +89,18 @@ typedef struct sparge_params {
   void *const *timing_events;   /* optional: 6 cudaEvent_t handles recorded on the stream before the
                                    pooling kernel and after the pooling, pooled-score, selection,
                                    V-copy (8-bit path: quantisation) and attention kernels (for per-kernel timing), or NULL */
+  /* Optional per-query-head parameters (the tuned mode of the SpargeAttn overview page, where
+   * every head of every layer has its own thresholds): device arrays of Hq floats, or NULL.
+   * When given, entry h replaces the scalar for query head h: topk_per_head in the mask rows of
+   * head h (the topk argument otherwise), theta_per_head in its always-keep rules (both the
+   * row rule on s_Q and the column rule on s_K), lambda_per_head in its attention rows.  The
+   * entries are read on the device; an entry out of range (topk outside (0, 1], a theta that is
+   * not finite, a lambda that is NaN or > 0) records SPARGE_ERR_INVALID_ARG in the device status
+   * word and that head runs with every valid block kept (bad topk or theta) or with the filter
+   * off (bad lambda). */
+  const float *topk_per_head;
+  const float *theta_per_head;
+  const float *lambda_per_head;
 } sparge_params;
 
 /*
@@ -122,6 +136,17 @@ int sparge_predict_mask(const sparge_tensor *q, const sparge_tensor *k, float to
                         sparge_stream_t stream);
 
 /*
+ * sparge_predict_mask with its parameters in a sparge_params: theta, scale (0 means 1/sqrt(d);
+ * the pooled scores are scale * muQ . muK), topk_per_head and theta_per_head, and timing events
+ * [0]-[3] (before pooling, after pooling, after the pooled scores, after the selection).  lambda,
+ * precision, stats and lambda_per_head are unused.  Same workspace and errors as
+ * sparge_predict_mask.
+ */
+int sparge_predict_mask_ex(const sparge_tensor *q, const sparge_tensor *k, float topk, int is_causal,
+                           const sparge_params *params, uint8_t *mask, void *ws, size_t ws_bytes,
+                           sparge_stream_t stream);
+
+/*
  * Stage 2, block-sparse attention (SpargeAttention abstract: the second-stage online
  * softmax-aware filter; summary: it works at GPU-warp level; Chinese README: custom mask API).
  *   O = softmax(scale * Q K^T) V restricted to the kept tiles, visited in ascending key-block
@@ -155,10 +180,11 @@ int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k,
                              size_t ws_bytes, unsigned long long *stats, sparge_stream_t stream);
 
 /*
- * sparge_block_sparse_attn with its parameters in a sparge_params (theta is unused): lambda,
- * scale (0 means 1/sqrt(d)), precision, counters, and timing events; of the six events, [0] is
- * recorded before the V copy or quantisation, [4] after it and [5] after the attention kernel
- * ([1]-[3] are left alone).  Same workspace and errors as sparge_block_sparse_attn.
+ * sparge_block_sparse_attn with its parameters in a sparge_params (theta, topk_per_head and
+ * theta_per_head are unused): lambda or lambda_per_head, scale (0 means 1/sqrt(d)), precision,
+ * counters, and timing events; of the six events, [0] is recorded before the V copy or
+ * quantisation, [4] after it and [5] after the attention kernel ([1]-[3] are left alone).  Same
+ * workspace and errors as sparge_block_sparse_attn.
  */
 int sparge_block_sparse_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v,
                                 const uint8_t *mask, int is_causal, const sparge_params *params,
@@ -173,7 +199,8 @@ int sparge_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_ten
                 sparge_stream_t stream);
 
 /*
- * sparge_attn with every parameter explicit (theta, lambda, scale, precision, counters).
+ * sparge_attn with every parameter explicit (theta, lambda, scale, precision, counters, and the
+ * optional per-head topk, theta and lambda arrays).
  * ws: sparge_workspace_bytes(SPARGE_OP_ATTN, ...) bytes, or SPARGE_OP_ATTN_Q8 for the 8-bit path.
  * mask_out: optional device buffer (B,Hq,nqb,nkb) that receives the predicted mask; when
  * NULL the mask lives in the workspace.

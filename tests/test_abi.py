@@ -41,6 +41,49 @@ def test_exports_every_declared_symbol(lib):
     assert names <= set(fbs.EXPORTS)
 
 
+def test_struct_layouts_match_the_header(tmp_path):
+    """The binding's ctypes structs have the sizes and field offsets the C compiler gives the
+    header's structs."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "layout.c"
+    src.write_text(
+        "#include <stdio.h>\n#include <stddef.h>\n#include \"sparge.h\"\n"
+        "int main(void) {\n"
+        "  printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(sparge_params), offsetof(sparge_params, stats),\n"
+        "         offsetof(sparge_params, timing_events), offsetof(sparge_params, topk_per_head),\n"
+        "         offsetof(sparge_params, theta_per_head), offsetof(sparge_params, lambda_per_head));\n"
+        "  printf(\"%zu %zu %zu\\n\", sizeof(sparge_tensor), offsetof(sparge_tensor, B),\n"
+        "         offsetof(sparge_tensor, stride_n));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    P, T = fbs.sparge_params, fbs.sparge_tensor
+    want = [ctypes.sizeof(P), P.stats.offset, P.timing_events.offset, P.topk_per_head.offset,
+            P.theta_per_head.offset, P.lambda_per_head.offset, ctypes.sizeof(T), T.B.offset, T.stride_n.offset]
+    assert got == want
+
+
+@pytest.mark.parametrize("case", ["null_params", "bad_topk", "bad_theta", "neg_scale"])
+def test_predict_mask_ex_rejects_bad_parameters(lib, case):
+    q = _t()
+    p = fbs.sparge_params(0.5, -math.inf, 0.0, fbs.SPARGE_PRECISION_BF16, 0, None)
+    topk = 0.5
+    if case == "bad_topk":
+        topk = 1.5
+    elif case == "bad_theta":
+        p.theta = math.nan
+    elif case == "neg_scale":
+        p.scale = -1.0
+    pp = None if case == "null_params" else ctypes.byref(p)
+    rc = lib.sparge_predict_mask_ex(ctypes.byref(q), ctypes.byref(q), topk, 0, pp, None, None, 0, None)
+    assert rc == fbs.SPARGE_ERR_INVALID_ARG, lib.sparge_last_error()
+
+
 def test_workspace_bytes(lib):
     B, Hq, Hkv, N, d = 1, 32, 8, 131072, 128
     nqb, nkb = 1024, 2048
