@@ -263,15 +263,30 @@ def run_ours(args, rank, world, local_rank):
     ws = torch.empty(fbs.workspace_bytes(op, w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8, device=dev)
     stats = torch.zeros(4, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream()
+    # image / video workloads run in Hilbert token order, inside the call (sparge_params.token_order):
+    # the call copies Q and K in that order, gathers V while converting it and writes each output
+    # row back to its original position
+    perm = None
+    if w.grid is not None:
+        perm_np = (fbs.hilbert_perm_2d(w.n_prefix, *w.grid) if len(w.grid) == 2
+                   else fbs.hilbert_perm_3d(w.n_prefix, *w.grid))
+        perm = torch.from_numpy(perm_np).to(dev)
+        ws = torch.empty(fbs.workspace_bytes(op | fbs.SPARGE_OP_TOKEN_ORDER, w.B, w.Hq, w.Hkv, w.N, w.d),
+                         dtype=torch.uint8, device=dev)
 
-    def call(qq, kk, vv, events=None, counters=None, oo=None):
+    def call(qq, kk, vv, events=None, counters=None, oo=None, outer=None):
+        """One step through the public call; `outer` (2 events) brackets the whole call."""
         oo = o if oo is None else oo
+        if outer is not None:
+            outer[0].record(stream)
         if given_mask:
             fbs.block_sparse_attn_ex(qq, kk, vv, mask, w.causal, lam=lam, out=oo, ws=ws, precision=prec,
-                                     stats=counters, events=events)
+                                     stats=counters, events=events, token_order=perm)
         else:
             fbs.sparge_attn_ex(qq, kk, vv, w.topk, w.causal, theta=w.theta, lam=lam, mask_out=mask, out=oo, ws=ws,
-                               precision=prec, events=events, stats=counters)
+                               precision=prec, events=events, stats=counters, token_order=perm)
+        if outer is not None:
+            outer[1].record(stream)
 
     # one run with counters for the executed-work figures (same inputs -> same mask every step)
     call(q, k, v, counters=stats)
@@ -279,10 +294,13 @@ def run_ours(args, rank, world, local_rank):
     kept, pv, skipped, valid = (int(x) for x in stats.cpu().tolist())
     assert fbs.device_status() == 0
 
-    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    # inputs smaller than twice L2 (129 MB): flush L2 between steps and sum the steps' own spans
+    in_bytes = w.q.nbytes + w.k.nbytes + w.v.nbytes
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if in_bytes < 2 * 129e6 else None
 
     def step(events=None):
-        call(q, k, v, events=events)
+        call(q, k, v, events=None if events is None else events[:6], outer=None if events is None else events[6:])
 
     for evs in ev_sets:   # create every event once (torch creates events on first record)
         for ev in evs:
@@ -297,6 +315,8 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.5)
     for s in range(args.steps):
+        if flush is not None:
+            flush.zero_()    # evict the previous step's data from L2 (outside the step's own span)
         step(ev_sets[s])
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -309,7 +329,13 @@ def run_ours(args, rank, world, local_rank):
     t_conv = [e[0 if given_mask else 3].elapsed_time(e[4]) / 1e3 for e in ev_sets]
     t_attn = [e[4].elapsed_time(e[5]) / 1e3 for e in ev_sets]
     t_pred = [0.0 if given_mask else a + b + c for a, b, c in zip(t_pool, t_gemm, t_sel)]
-    total = ev_sets[0][0].elapsed_time(ev_sets[-1][5]) / 1e3
+    # [6] before the call and [7] after it: with a token order, [6]-[0] holds the ordered copies of Q and K
+    t_perm = [e[6].elapsed_time(e[0]) / 1e3 + e[5].elapsed_time(e[7]) / 1e3 for e in ev_sets] if perm is not None else None
+    first, last = 6, 7
+    if flush is None:
+        total = ev_sets[0][first].elapsed_time(ev_sets[-1][last]) / 1e3
+    else:
+        total = sum(e[first].elapsed_time(e[last]) for e in ev_sets) / 1e3
     total = max_over_ranks(total, dist, dev)
     assert fbs.device_status() == 0
 
@@ -384,6 +410,13 @@ def run_ours(args, rank, world, local_rank):
     hbm = float(peaks["hbm_gbs"])
     tag = "of measured" if peaks.get("source") == "measured" else "of fallback"
 
+    kernels_ms = ({"attn_prep": round(avg(t_conv) * 1e3, 4), "bsattn": round(t_attn_avg * 1e3, 4)} if given_mask else
+                  {"pool_sim": round(avg(t_pool) * 1e3, 4), "score_gemm": round(avg(t_gemm) * 1e3, 4),
+                   "score_select": round(avg(t_sel) * 1e3, 4),
+                   "attn_prep": round(avg(t_conv) * 1e3, 4), "bsattn": round(t_attn_avg * 1e3, 4)})
+    if t_perm is not None:
+        kernels_ms["hilbert_order_qk_copies"] = round(avg(t_perm) * 1e3, 4)
+
     line = {
         "metric": "dense-equiv attention TOPS and % tensor peak at 128K causal; mask-pred GB/s",
         "value": round(value, 2),
@@ -400,12 +433,10 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
                    "causal": w.causal, "topk": w.topk, "theta": w.theta, "lambda": lam,
                    "mask": "the workload's Bernoulli(0.25) tile mask" if given_mask else "predicted",
-                   "l2": "inputs larger than L2 (Q+K+V %.2f GB), no flush" % ((w.q.nbytes + w.k.nbytes + w.v.nbytes) / 1e9),
+                   "l2": ("inputs larger than L2 (Q+K+V %.2f GB), no flush" % (in_bytes / 1e9) if flush is None else
+                          "Q+K+V %.3f GB: L2 flushed (256 MB write) before every step, steps timed apart" % (in_bytes / 1e9)),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "kernels_ms": ({"attn_prep": round(avg(t_conv) * 1e3, 4), "bsattn": round(t_attn_avg * 1e3, 4)} if given_mask else
-                       {"pool_sim": round(avg(t_pool) * 1e3, 4), "score_gemm": round(avg(t_gemm) * 1e3, 4),
-                        "score_select": round(avg(t_sel) * 1e3, 4),
-                        "attn_prep": round(avg(t_conv) * 1e3, 4), "bsattn": round(t_attn_avg * 1e3, 4)}),
+        "kernels_ms": kernels_ms,
         "attn": {"ms": round(t_attn_avg * 1e3, 4), "dense_equiv_tops": round(dense / t_attn_avg / 1e12, 2),
                  "executed_tflops": round(attn_tflops, 2), "pct_tensor_peak": round(100 * attn_tflops / peak_tc, 2),
                  "kept_tiles": kept, "valid_tiles": valid, "sparsity": round(1 - kept / max(valid, 1), 4),
@@ -422,7 +453,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(world * dense / e2e_t / 1e12, 2), "unit": "dense-equiv TOPS",
                 "h2d_bytes_per_step": int(w.q.nbytes + w.k.nbytes + w.v.nbytes),
                 "d2h_bytes_per_step": int(o.numel() * 2)},
-        "gpu_launches": LAUNCHES_PER_STEP[(args.precision, given_mask)] * args.steps,
+        "gpu_launches": (LAUNCHES_PER_STEP[(args.precision, given_mask)] + (2 if perm is not None else 0)) * args.steps,
         "clocks": clk,
     }
     line["permute"] = measure_permute(max(args.steps, 10), args.warmup, dev, peaks)

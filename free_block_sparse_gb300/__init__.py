@@ -32,6 +32,7 @@ SPARGE_OP_BLOCK_SPARSE_ATTN = 2
 SPARGE_OP_ATTN = 3
 SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 = 4
 SPARGE_OP_ATTN_Q8 = 5
+SPARGE_OP_TOKEN_ORDER = 0x100  # flag OR-ed into an op: room for token-ordered copies of Q and K
 QBLK, KBLK = 128, 64
 
 
@@ -51,7 +52,7 @@ class sparge_params(ctypes.Structure):
     _fields_ = [("theta", ctypes.c_float), ("lambda_", ctypes.c_float), ("scale", ctypes.c_float),
                 ("precision", ctypes.c_int32), ("stats", ctypes.c_void_p), ("timing_events", ctypes.c_void_p),
                 ("topk_per_head", ctypes.c_void_p), ("theta_per_head", ctypes.c_void_p),
-                ("lambda_per_head", ctypes.c_void_p)]
+                ("lambda_per_head", ctypes.c_void_p), ("token_order", ctypes.c_void_p)]
 
 
 _lib = None
@@ -160,15 +161,18 @@ def predict_mask(q, k, topk: float, theta: float = 0.5, causal: bool = False, ws
 
 
 def predict_mask_ex(q, k, topk: float, causal: bool = False, theta: float = 0.5, scale: float = 0.0,
-                    topk_per_head=None, theta_per_head=None, ws=None, mask=None, events=None):
+                    topk_per_head=None, theta_per_head=None, ws=None, mask=None, events=None, token_order=None):
     """predict_mask with an explicit pooled-score scale, optional per-query-head topk and theta
-    (float32 CUDA tensors of Hq entries) and optional timing events ([0]-[3] are recorded)."""
+    (float32 CUDA tensors of Hq entries), optional timing events ([0]-[3] are recorded) and an
+    optional token order (int32 CUDA tensor of N entries; the mask refers to the reordered
+    sequence)."""
     torch = _torch()
     B, Hq, N, _ = q.shape
     if mask is None:
         mask = torch.empty((B, Hq, -(-N // 128), -(-N // 64)), dtype=torch.uint8, device=q.device)
-    ws = _workspace(SPARGE_OP_PREDICT_MASK, q, k, ws)
-    p = _params(theta, -math.inf, scale, SPARGE_PRECISION_BF16, None, events, topk_per_head, theta_per_head)
+    ws = _workspace(SPARGE_OP_PREDICT_MASK | (SPARGE_OP_TOKEN_ORDER if token_order is not None else 0), q, k, ws)
+    p = _params(theta, -math.inf, scale, SPARGE_PRECISION_BF16, None, events, topk_per_head, theta_per_head,
+                order=token_order)
     dq, dk = _desc(q), _desc(k)
     _check(lib().sparge_predict_mask_ex(ctypes.byref(dq), ctypes.byref(dk), float(topk), int(causal), ctypes.byref(p),
                                         mask.data_ptr(), ws.data_ptr(), ws.numel(), _stream()))
@@ -275,10 +279,21 @@ def _head_array(x, name):
     return x.data_ptr()
 
 
-def _params(theta, lam, scale, precision, stats, events, topk_h=None, theta_h=None, lam_h=None):
+def _order_ptr(order):
+    """A token order as a device pointer (0 for None); order is an int32 CUDA tensor of N entries."""
+    if order is None:
+        return 0
+    torch = _torch()
+    if not (isinstance(order, torch.Tensor) and order.is_cuda and order.dtype == torch.int32 and order.dim() == 1
+            and order.is_contiguous()):
+        raise TypeError("token_order must be a contiguous int32 CUDA tensor of N entries")
+    return order.data_ptr()
+
+
+def _params(theta, lam, scale, precision, stats, events, topk_h=None, theta_h=None, lam_h=None, order=None):
     """A sparge_params; `events` (6 torch.cuda.Event or None) are passed as cudaEvent_t handles.
     The handle array is kept on the returned struct so it outlives the call.  topk_h, theta_h and
-    lam_h are optional per-query-head float32 CUDA tensors."""
+    lam_h are optional per-query-head float32 CUDA tensors; order an optional int32 token order."""
     evp = None
     if events is not None:
         assert len(events) == 6
@@ -290,25 +305,27 @@ def _params(theta, lam, scale, precision, stats, events, topk_h=None, theta_h=No
                       0 if stats is None else stats.data_ptr(),
                       ctypes.cast(evp, ctypes.c_void_p) if evp is not None else None,
                       _head_array(topk_h, "topk_per_head"), _head_array(theta_h, "theta_per_head"),
-                      _head_array(lam_h, "lambda_per_head"))
+                      _head_array(lam_h, "lambda_per_head"), _order_ptr(order))
     p._evp = evp
-    p._arrays = (topk_h, theta_h, lam_h)
+    p._arrays = (topk_h, theta_h, lam_h, order)
     return p
 
 
 def block_sparse_attn_ex(q, k, v, mask=None, causal: bool = False, lam: float = -math.inf, scale: float = 0.0,
                          precision: int = SPARGE_PRECISION_BF16, stats=None, out=None, ws=None, events=None,
-                         lambda_per_head=None):
+                         lambda_per_head=None, token_order=None):
     """block_sparse_attn with an explicit scale, optional timing events (6 torch.cuda.Event:
     [0] before the V copy or quantisation, [4] after it, [5] after the attention kernel) and an
-    optional per-query-head lambda (float32 CUDA tensor of Hq entries)."""
+    optional per-query-head lambda (float32 CUDA tensor of Hq entries) and an optional token order
+    (int32 CUDA tensor of N entries; the mask then refers to the reordered sequence and the output
+    comes back in the original order)."""
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
     op = SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 if precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV) \
         else SPARGE_OP_BLOCK_SPARSE_ATTN
-    ws = _workspace(op, q, k, ws)
-    p = _params(0.5, lam, scale, precision, stats, events, lam_h=lambda_per_head)
+    ws = _workspace(op | (SPARGE_OP_TOKEN_ORDER if token_order is not None else 0), q, k, ws)
+    p = _params(0.5, lam, scale, precision, stats, events, lam_h=lambda_per_head, order=token_order)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     mp = 0 if mask is None else mask.data_ptr()
     _check(lib().sparge_block_sparse_attn_ex(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), mp, int(causal),
@@ -318,16 +335,21 @@ def block_sparse_attn_ex(q, k, v, mask=None, causal: bool = False, lam: float = 
 
 def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: float = -math.inf,
                    scale: float = 0.0, precision: int = SPARGE_PRECISION_BF16, stats=None, mask_out=None,
-                   out=None, ws=None, events=None, topk_per_head=None, theta_per_head=None, lambda_per_head=None):
+                   out=None, ws=None, events=None, topk_per_head=None, theta_per_head=None, lambda_per_head=None,
+                   token_order=None):
     """sparge_attn with explicit theta, lambda, scale, counters, an optional mask output,
-    optional timing events (6 torch.cuda.Event, recorded around the five kernels) and optional
-    per-query-head topk, theta and lambda (float32 CUDA tensors of Hq entries)."""
+    optional timing events (6 torch.cuda.Event, recorded around the five kernels), optional
+    per-query-head topk, theta and lambda (float32 CUDA tensors of Hq entries) and an optional
+    token order (int32 CUDA tensor of N entries: blocks and mask_out refer to the reordered
+    sequence, the output comes back in the original order)."""
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
     q8 = precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV)
-    ws = _workspace(SPARGE_OP_ATTN_Q8 if q8 else SPARGE_OP_ATTN, q, k, ws)
-    p = _params(theta, lam, scale, precision, stats, events, topk_per_head, theta_per_head, lambda_per_head)
+    ws = _workspace((SPARGE_OP_ATTN_Q8 if q8 else SPARGE_OP_ATTN) | (SPARGE_OP_TOKEN_ORDER if token_order is not None else 0),
+                    q, k, ws)
+    p = _params(theta, lam, scale, precision, stats, events, topk_per_head, theta_per_head, lambda_per_head,
+                token_order)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     mp = 0 if mask_out is None else mask_out.data_ptr()
     _check(lib().sparge_attn_ex(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), float(topk), int(causal),

@@ -183,6 +183,30 @@ int record_event(void *const *ev, int idx, cudaStream_t s) {
   return e == cudaSuccess ? SPARGE_OK : cuda_fail(e, "timing event record");
 }
 
+size_t order_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
+  return align256((size_t)2 * B * Hq * N * d) + align256((size_t)2 * B * Hkv * N * d);
+}
+
+// Calls with a token order: copies q and k into the front of the workspace in that order
+// (contiguous (B, H, N, d) bf16), replaces q and k by the copies and moves ws past them.
+int order_qk(View &q, View &k, const int32_t *perm, void *&ws, size_t &ws_bytes, cudaStream_t s) {
+  const size_t need = order_bytes(q.B, q.H, k.H, q.N, q.d);
+  if (!ws || ws_bytes < need)
+    return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu for the token-ordered copies", ws_bytes,
+                need);
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(SPARGE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  uint8_t *base = static_cast<uint8_t *>(ws);
+  void *qc = base, *kc = base + align256((size_t)2 * q.B * q.H * q.N * q.d);
+  cudaError_t e = launch_permute(q, perm, qc, q.H * q.N * q.d, q.N * q.d, q.d, false, status_ptr(), s, true);
+  if (e == cudaSuccess) e = launch_permute(k, perm, kc, k.H * k.N * k.d, k.N * k.d, k.d, false, status_ptr(), s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "token-order copy launch");
+  q = View{qc, q.B, q.H, q.N, q.d, q.H * q.N * q.d, q.N * q.d, q.d};
+  k = View{kc, k.B, k.H, k.N, k.d, k.H * k.N * k.d, k.N * k.d, k.d};
+  ws = base + need;
+  ws_bytes -= need;
+  return SPARGE_OK;
+}
+
 // Per-query-head parameter arrays of a sparge_params (device pointers, each may be null).
 struct HeadParams {
   const float *topk = nullptr, *theta = nullptr, *lambda = nullptr;
@@ -239,7 +263,7 @@ size_t attn_ws_bytes(int precision, int64_t B, int64_t Hq, int64_t Hkv, int64_t 
 
 int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, float lambda, int causal, float scale,
               int precision, sparge_tensor *o, unsigned long long *stats, void *ws, size_t ws_bytes,
-              cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {}) {
+              cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {}, const int32_t *perm = nullptr) {
   if (precision != SPARGE_PRECISION_BF16 && !is_q8(precision))
     return fail(SPARGE_ERR_UNSUPPORTED, "precision %d not supported", precision);
   const bool q8 = is_q8(precision), pv8 = precision == SPARGE_PRECISION_Q8_FP8PV;
@@ -259,9 +283,10 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   memset(&l, 0, sizeof(l));
   if (q8) {
     const Q8Ws w = q8_ws_carve(ws, q.B, q.H, k.H, q.N, q.d);
-    cudaError_t e = launch_q8_prep(q, k, v, w, pv8, s);
+    cudaError_t e = launch_q8_prep(q, k, v, w, pv8, perm, status_ptr(), s);
     if (e != cudaSuccess) return cuda_fail(e, "8-bit quantisation launch");
-    if (!pv8 && (e = launch_convert_v_f16(v, w.v8, s)) != cudaSuccess) return cuda_fail(e, "convert_v launch");
+    if (!pv8 && (e = launch_convert_v_f16(v, w.v8, perm, status_ptr(), s)) != cudaSuccess)
+      return cuda_fail(e, "convert_v launch");
     if ((rc = record_event(ev, 4, s))) return rc;
     const int64_t d = q.d, N = q.N, npad = cdiv(N, 64) * 64;
     const int64_t qd[4] = {d, N, q.H, q.B}, qs[3] = {d, N * d, q.H * N * d};
@@ -280,7 +305,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
     l.sk = w.sk;
     l.sv = w.sv;
   } else {
-    cudaError_t e = launch_convert_v_f16(v, ws, s);
+    cudaError_t e = launch_convert_v_f16(v, ws, perm, status_ptr(), s);
     if (e != cudaSuccess) return cuda_fail(e, "convert_v launch");
     if ((rc = record_event(ev, 4, s))) return rc;
     View v16{ws, v.B, v.H, v.N, v.d, v.H * v.N * v.d, v.N * v.d, v.d};
@@ -296,6 +321,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   l.scale = scale;
   l.lambda = lambda;
   l.lambda_h = hp.lambda;
+  l.perm = perm;
   l.stats = stats;
   l.status = status_ptr();
   cudaError_t e = launch_bsattn(l, s);
@@ -365,6 +391,10 @@ extern "C" {
 
 size_t sparge_workspace_bytes(int op, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || (d != 64 && d != 128)) return 0;
+  if (op & SPARGE_OP_TOKEN_ORDER) {
+    const size_t base = sparge_workspace_bytes(op & ~SPARGE_OP_TOKEN_ORDER, B, Hq, Hkv, N, d);
+    return base ? base + order_bytes(B, Hq, Hkv, N, d) : 0;
+  }
   switch (op) {
     case SPARGE_OP_PREDICT_MASK:
       return predict_ws_bytes(B, Hq, Hkv, N, d);
@@ -411,8 +441,14 @@ int sparge_predict_mask_ex(const sparge_tensor *q, const sparge_tensor *k, float
   HeadParams hp;
   hp.topk = p->topk_per_head;
   hp.theta = p->theta_per_head;
-  return predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, ws_bytes,
-                      reinterpret_cast<cudaStream_t>(stream), p->timing_events, hp);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->token_order) {
+    const size_t need = order_bytes(qv.B, qv.H, kv.H, qv.N, qv.d) + predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, qv.d);
+    if (!mask) return fail(SPARGE_ERR_INVALID_ARG, "mask is NULL");
+    if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
+    if (qv.B * qv.N > 0 && (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s))) return rc;
+  }
+  return predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, ws_bytes, s, p->timing_events, hp);
 }
 
 int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v,
@@ -444,11 +480,16 @@ int sparge_block_sparse_attn_ex(const sparge_tensor *q, const sparge_tensor *k, 
     return fail(SPARGE_ERR_INVALID_ARG, "scale must be finite and >= 0");
   const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)qv.d);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->token_order) {
+    const size_t need = order_bytes(qv.B, qv.H, kv.H, qv.N, qv.d) + attn_ws_bytes(p->precision, qv.B, qv.H, kv.H, qv.N, qv.d);
+    if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
+  }
   if ((rc = record_event(p->timing_events, 0, s))) return rc;
+  if (p->token_order && qv.B * qv.N > 0 && (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s))) return rc;
   HeadParams hp;
   hp.lambda = p->lambda_per_head;
   return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws, ws_bytes, s,
-                   p->timing_events, hp);
+                   p->timing_events, hp, p->token_order);
 }
 
 int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,
@@ -470,11 +511,13 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   if (is_q8(p->precision) && qv.d != 128)
     return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path needs d = 128 (got %lld)", (long long)qv.d);
   const size_t need_v = attn_ws_bytes(p->precision, qv.B, qv.H, kv.H, qv.N, qv.d);
-  const size_t need = need_pred + mask_bytes + need_v;
+  const size_t need_order = p->token_order ? order_bytes(qv.B, qv.H, kv.H, qv.N, qv.d) : 0;
+  const size_t need = need_order + need_pred + mask_bytes + need_v;
   if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->token_order && qv.B * qv.N > 0 && (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s))) return rc;
   uint8_t *mask = mask_out ? mask_out : static_cast<uint8_t *>(ws) + need_pred;
   void *ws_v = static_cast<uint8_t *>(ws) + need_pred + mask_bytes;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   HeadParams hp;
   hp.topk = p->topk_per_head;
   hp.theta = p->theta_per_head;
@@ -482,7 +525,7 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s, p->timing_events, hp)))
     return rc;
   return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws_v, need_v, s,
-                   p->timing_events, hp);
+                   p->timing_events, hp, p->token_order);
 }
 
 int sparge_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,

@@ -47,6 +47,7 @@ struct AttnArgs {
   int B, Hq, Hkv, G, N, nqb, nkb, causal;
   float scale_log2, lam_log2;
   const float *lam_h;  // lambda per query head (natural-log units), or nullptr
+  const int32_t *perm; // token order or nullptr: output row t is token perm[t] of o
   unsigned long long *stats;
   int *status;
   const float *sq, *sk, *sv;  // 8-bit path: scales of the Q blocks, K blocks and V channels
@@ -509,7 +510,19 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
     const float *svrow = PV8 ? a.sv + (static_cast<int64_t>(b) * a.Hkv + kvh) * D : nullptr;
-    __nv_bfloat16 *orow = a.o + b * a.o_sb + h * a.o_sh + static_cast<int64_t>(row_g) * a.o_sn;
+    // the output row: token row_g, or token perm[row_g] of o under a token order (an entry outside
+    // 0..N-1 is reported and its row left unwritten)
+    int orow_t = row_g;
+    bool write_row = row_ok;
+    if (a.perm && row_ok) {
+      orow_t = __ldg(a.perm + row_g);
+      if (static_cast<unsigned>(orow_t) >= static_cast<unsigned>(a.N)) {
+        record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
+        write_row = false;
+        orow_t = 0;
+      }
+    }
+    __nv_bfloat16 *orow = a.o + b * a.o_sb + h * a.o_sh + static_cast<int64_t>(orow_t) * a.o_sn;
 #pragma unroll 1
     for (int q = 0; q < D / 16; ++q) {
       uint32_t rr[16];
@@ -539,7 +552,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       o1.y = pack_bf16x2(__uint_as_float(rr[10]) * inv_l, __uint_as_float(rr[11]) * inv_l);
       o1.z = pack_bf16x2(__uint_as_float(rr[12]) * inv_l, __uint_as_float(rr[13]) * inv_l);
       o1.w = pack_bf16x2(__uint_as_float(rr[14]) * inv_l, __uint_as_float(rr[15]) * inv_l);
-      if (row_ok) {
+      if (write_row) {
         *reinterpret_cast<uint4 *>(orow + 16 * q) = o0;
         *reinterpret_cast<uint4 *>(orow + 16 * q + 8) = o1;
       }
@@ -578,6 +591,7 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
   a.scale_log2 = l.scale * LOG2E;
   a.lam_log2 = (l.lambda == -INFINITY) ? -INFINITY : l.lambda * LOG2E;
   a.lam_h = l.lambda_h;
+  a.perm = l.perm;
   a.stats = l.stats;
   a.status = l.status;
   a.sq = l.sq;

@@ -80,11 +80,13 @@ struct AttnLaunch {
   int q8;                  // 0: bf16 Q.K^T, f16 P.V; 1: e4m3 Q.K^T (maps over the e4m3 copies, scales sq, sk),
                            // f16 P.V; 2: as 1 with e4m3 P.V (channel-major e4m3 V, scales sv)
   const float *sq, *sk, *sv;
+  const int32_t *perm;     // token order or nullptr: output row t goes to token perm[t] of o
 };
 
 cudaError_t launch_bsattn(const AttnLaunch &a, cudaStream_t st);
 
-cudaError_t launch_convert_v_f16(const View &v, void *v16, cudaStream_t st);
+// perm (or nullptr): row t of the copy is token perm[t] of v; bad entries are reported in *status.
+cudaError_t launch_convert_v_f16(const View &v, void *v16, const int32_t *perm, int *status, cudaStream_t st);
 
 // 8-bit path: e4m3 copies of Q, K - mean(K) and V with their scales (all contiguous).
 struct Q8Ws {
@@ -101,10 +103,12 @@ struct Q8Ws {
 size_t q8_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
 Q8Ws q8_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
 // K mean, V channel scales, e4m3 Q and K - mean with their block scales; with quant_v also the
-// channel-major e4m3 V (otherwise v8 is left to the caller).
-cudaError_t launch_q8_prep(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v, cudaStream_t st);
+// channel-major e4m3 V (otherwise v8 is left to the caller), whose key t is token perm[t] of v
+// when perm is given (Q and K are used in the order they come in).
+cudaError_t launch_q8_prep(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v,
+                           const int32_t *perm, int *status, cudaStream_t st);
 
 cudaError_t launch_permute(const View &x, const int32_t *perm, void *y, int64_t ysb, int64_t ysh, int64_t ysn,
-                           bool inverse, int *status, cudaStream_t st);
+                           bool inverse, int *status, cudaStream_t st, bool zero_bad = false);
 
 }  // namespace sparge

@@ -19,13 +19,15 @@ struct PermArgs {
   int64_t xsb, xsh, xsn, ysb, ysh, ysn;
   int B, H, N;
   int inverse;
+  int zero_bad;  // gather: a bad entry writes a zero row instead of leaving the row alone
   int *status;
 };
 
 // Grid (token chunks, H, B), 256 threads; each thread moves U 16-byte pieces of token rows, all
 // U loads issued before the first store, so each SM keeps many bytes in flight; 32-bit index
 // arithmetic within a head.  A perm entry outside 0..N-1 is never used as an address: its row is
-// skipped and the device status word records SPARGE_ERR_INVALID_ARG.
+// skipped (or, for the library's own ordered copies, written as zeros) and the device status word
+// records SPARGE_ERR_INVALID_ARG.
 constexpr int PERM_U = 4;
 
 template <int D>
@@ -48,6 +50,10 @@ __global__ void __launch_bounds__(256) permute_kernel(PermArgs a) {
       const int p = __ldg(a.perm + t);
       if (static_cast<unsigned>(p) >= static_cast<unsigned>(a.N)) {  // not a token index: skip the row
         if (part[u] == 0) record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
+        if (a.zero_bad && !a.inverse) {
+          dst[u] = t;
+          v[u] = make_uint4(0, 0, 0, 0);
+        }
         continue;
       }
       const int src = a.inverse ? t : p;
@@ -63,10 +69,12 @@ __global__ void __launch_bounds__(256) permute_kernel(PermArgs a) {
 // V (bf16, any legal strides) -> contiguous f16 copy for the P.V product of the attention kernel.
 // cvt.rn.satfinite: exact for |v| <= 65504 (every bf16 value in f16 range keeps its 8 significant
 // bits), larger magnitudes saturate.  Grid (token chunks, H, B); each thread moves 16 bytes per
-// step with streaming loads, two independent vectors in flight.
+// step with streaming loads, two independent vectors in flight.  With a token order, row t of
+// the copy is token perm[t] of V (an entry outside 0..N-1 gives a zero row and is reported).
 template <int D>
 __global__ void __launch_bounds__(256) convert_v_f16_kernel(const __nv_bfloat16 *x, int64_t sb, int64_t sh,
-                                                             int64_t sn, __half *y, int N) {
+                                                             int64_t sn, __half *y, int N, const int32_t *perm,
+                                                             int *status) {
   constexpr int VPR = D / 8;                 // 16-byte vectors per token row
   constexpr int ROWS = 2 * 256 / VPR;        // token rows per CTA
   const int h = blockIdx.y, b = blockIdx.z, H = gridDim.y;
@@ -80,7 +88,18 @@ __global__ void __launch_bounds__(256) convert_v_f16_kernel(const __nv_bfloat16 
     const int e = threadIdx.x + u * 256;
     t[u] = t0 + e / VPR;
     part[u] = e % VPR;
-    if (t[u] < N) v[u] = ld_stream_v4(xb + static_cast<int64_t>(t[u]) * sn + part[u] * 8);
+    if (t[u] < N) {
+      int src = t[u];
+      if (perm) {
+        src = __ldg(perm + t[u]);
+        if (static_cast<unsigned>(src) >= static_cast<unsigned>(N)) {
+          if (part[u] == 0) record_status(status, -1 /* SPARGE_ERR_INVALID_ARG */);
+          v[u] = make_uint4(0, 0, 0, 0);
+          continue;
+        }
+      }
+      v[u] = ld_stream_v4(xb + static_cast<int64_t>(src) * sn + part[u] * 8);
+    }
   }
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
@@ -97,20 +116,22 @@ __global__ void __launch_bounds__(256) convert_v_f16_kernel(const __nv_bfloat16 
 
 }  // namespace
 
-cudaError_t launch_convert_v_f16(const View &v, void *v16, cudaStream_t st) {
+cudaError_t launch_convert_v_f16(const View &v, void *v16, const int32_t *perm, int *status, cudaStream_t st) {
   if (v.B * v.H * v.N == 0) return cudaSuccess;
   const int rows = 2 * 256 / static_cast<int>(v.d / 8);
   dim3 grid(static_cast<unsigned>((v.N + rows - 1) / rows), static_cast<unsigned>(v.H), static_cast<unsigned>(v.B));
   const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(v.data);
   if (v.d == 128)
-    convert_v_f16_kernel<128><<<grid, 256, 0, st>>>(x, v.sb, v.sh, v.sn, static_cast<__half *>(v16), (int)v.N);
+    convert_v_f16_kernel<128><<<grid, 256, 0, st>>>(x, v.sb, v.sh, v.sn, static_cast<__half *>(v16), (int)v.N, perm,
+                                                    status);
   else
-    convert_v_f16_kernel<64><<<grid, 256, 0, st>>>(x, v.sb, v.sh, v.sn, static_cast<__half *>(v16), (int)v.N);
+    convert_v_f16_kernel<64><<<grid, 256, 0, st>>>(x, v.sb, v.sh, v.sn, static_cast<__half *>(v16), (int)v.N, perm,
+                                                   status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_permute(const View &x, const int32_t *perm, void *y, int64_t ysb, int64_t ysh, int64_t ysn,
-                           bool inverse, int *status, cudaStream_t st) {
+                           bool inverse, int *status, cudaStream_t st, bool zero_bad) {
   PermArgs a;
   a.x = static_cast<const __nv_bfloat16 *>(x.data);
   a.y = static_cast<__nv_bfloat16 *>(y);
@@ -119,6 +140,7 @@ cudaError_t launch_permute(const View &x, const int32_t *perm, void *y, int64_t 
   a.ysb = ysb; a.ysh = ysh; a.ysn = ysn;
   a.B = static_cast<int>(x.B); a.H = static_cast<int>(x.H); a.N = static_cast<int>(x.N);
   a.inverse = inverse ? 1 : 0;
+  a.zero_bad = zero_bad ? 1 : 0;
   a.status = status;
   if (x.B * x.H * x.N == 0) return cudaSuccess;
   const int rows = PERM_U * 256 / static_cast<int>(x.d / 8);

@@ -172,13 +172,15 @@ __global__ void __launch_bounds__(256) quant_block_kernel(const __nv_bfloat16 *x
 
 // V -> e4m3 with a scale per (batch, KV head, channel), written channel-major: out is
 // [B][Hkv][D][npad] bytes (npad = N rounded up to 64, the tail zero), so that a 64-key tile is a
-// K-major operand of P.V.  grid (B*Hkv, npad / 64), 256 threads.  Each CTA quantises one tile of
+// K-major operand of P.V; with a token order, key t of the copy is token perm[t] of V (an entry
+// outside 0..N-1 gives zero codes and is reported).  grid (B*Hkv, npad / 64), 256 threads.  Each CTA quantises one tile of
 // 64 keys into shared memory token-major (coalesced 16-byte loads, all issued first; 8-byte
 // stores), then each of D * 2 threads gathers 32 keys of one channel and writes them as two
 // 16-byte pieces (one whole 32-byte sector).
 template <int D>
 __global__ void __launch_bounds__(256) quant_vt_kernel(const __nv_bfloat16 *v, int64_t sb, int64_t sh, int64_t sn,
-                                                       int H, int N, int npad, const float *sv, uint8_t *out) {
+                                                       int H, int N, int npad, const float *sv, uint8_t *out,
+                                                       const int32_t *perm, int *status) {
   constexpr int VPR = D / 8;           // 16-byte input pieces per token
   constexpr int TPC = 256 / VPR;       // tokens per CTA-wide load
   constexpr int STEPS = 64 / TPC;
@@ -194,7 +196,15 @@ __global__ void __launch_bounds__(256) quant_vt_kernel(const __nv_bfloat16 *v, i
 #pragma unroll
   for (int s = 0; s < STEPS; ++s) {
     const int t = t0 + s * TPC + tok;
-    xv[s] = t < N ? ld_stream_v4(base + static_cast<int64_t>(t) * sn) : make_uint4(0, 0, 0, 0);
+    int src = t;
+    if (perm && t < N) {
+      src = __ldg(perm + t);
+      if (static_cast<unsigned>(src) >= static_cast<unsigned>(N)) {
+        if (p == 0) record_status(status, -1 /* SPARGE_ERR_INVALID_ARG */);
+        src = N;  // read nothing: zero codes
+      }
+    }
+    xv[s] = (t < N && src < N) ? ld_stream_v4(base + static_cast<int64_t>(src) * sn) : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
   for (int s = 0; s < STEPS; ++s) {
@@ -222,7 +232,8 @@ __global__ void __launch_bounds__(256) quant_vt_kernel(const __nv_bfloat16 *v, i
 }
 
 template <int D>
-cudaError_t run(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v, cudaStream_t st) {
+cudaError_t run(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v, const int32_t *perm,
+                int *status, cudaStream_t st) {
   const int B = static_cast<int>(q.B), Hq = static_cast<int>(q.H), Hkv = static_cast<int>(k.H);
   const int N = static_cast<int>(q.N);
   const int nchunks = (N + CHUNK - 1) / CHUNK;
@@ -241,7 +252,8 @@ cudaError_t run(const View &q, const View &k, const View &v, const Q8Ws &w, bool
                                                                           w.k8, w.sk);
   const int npad = (N + 63) / 64 * 64;
   if (quant_v)
-    quant_vt_kernel<D><<<dim3(B * Hkv, npad / 64), 256, 0, st>>>(vp, v.sb, v.sh, v.sn, Hkv, N, npad, w.sv, w.v8);
+    quant_vt_kernel<D><<<dim3(B * Hkv, npad / 64), 256, 0, st>>>(vp, v.sb, v.sh, v.sn, Hkv, N, npad, w.sv, w.v8, perm,
+                                                              status);
   return cudaGetLastError();
 }
 
@@ -273,9 +285,10 @@ Q8Ws q8_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_
   return w;
 }
 
-cudaError_t launch_q8_prep(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v, cudaStream_t st) {
+cudaError_t launch_q8_prep(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v,
+                           const int32_t *perm, int *status, cudaStream_t st) {
   if (q.B * q.N == 0) return cudaSuccess;
-  return q.d == 128 ? run<128>(q, k, v, w, quant_v, st) : run<64>(q, k, v, w, quant_v, st);
+  return q.d == 128 ? run<128>(q, k, v, w, quant_v, perm, status, st) : run<64>(q, k, v, w, quant_v, perm, status, st);
 }
 
 }  // namespace sparge

@@ -62,7 +62,9 @@ enum sparge_op {
   SPARGE_OP_BLOCK_SPARSE_ATTN = 2,
   SPARGE_OP_ATTN = 3,
   SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 = 4, /* sparge_block_sparse_attn with an 8-bit precision */
-  SPARGE_OP_ATTN_Q8 = 5               /* sparge_attn_ex with an 8-bit precision */
+  SPARGE_OP_ATTN_Q8 = 5,              /* sparge_attn_ex with an 8-bit precision */
+  SPARGE_OP_TOKEN_ORDER = 0x100       /* flag OR-ed into an op: room for the token-ordered copies of
+                                         Q and K that a call with sparge_params.token_order makes */
 };
 
 /* A strided bf16 tensor of logical shape (B, H, N, d); data is a device pointer. */
@@ -101,6 +103,19 @@ typedef struct sparge_params {
   const float *topk_per_head;
   const float *theta_per_head;
   const float *lambda_per_head;
+  /* Optional token order (device, N int32, or NULL), e.g. the Hilbert order of image or video
+   * tokens (SpargeAttention summary page: reordering by a space-filling curve raises the
+   * similarity inside blocks).  The call then works on the sequence whose token t is token
+   * token_order[t] of q, k and v: blocks, mask (and mask_out) refer to that sequence, and o is
+   * written back in the original order (o token token_order[t] receives row t).  The result is
+   * that of sparge_permute_tokens on q, k and v, the call, and sparge_unpermute_tokens on the
+   * output, without the separate V and output passes: the call copies Q and K into the
+   * workspace in the new order (sparge_workspace_bytes(op | SPARGE_OP_TOKEN_ORDER, ...)), gathers
+   * V while it converts or quantises it, and the attention kernel writes each output row
+   * straight to its original position.  token_order should be a permutation of 0..N-1; an entry
+   * outside that range is never used as an address (its row is skipped or zero) and records
+   * SPARGE_ERR_INVALID_ARG in the device status word. */
+  const int32_t *token_order;
 } sparge_params;
 
 /*
@@ -112,6 +127,8 @@ typedef struct sparge_params {
  *   or e4m3 channel-major with the keys padded to a multiple of 64) and the fp32 scales;
  *   SPARGE_OP_ATTN_Q8: that plus the mask-prediction workspace and the mask.  Both return 0
  *   unless d = 128.
+ * op | SPARGE_OP_TOKEN_ORDER: the op's bytes plus the bf16 copies of Q and K in a given token
+ *   order (at the front of the workspace), for calls whose sparge_params.token_order is set.
  * Returns 0 for an unknown op or an unsupported shape.
  */
 size_t sparge_workspace_bytes(int op, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
@@ -137,10 +154,10 @@ int sparge_predict_mask(const sparge_tensor *q, const sparge_tensor *k, float to
 
 /*
  * sparge_predict_mask with its parameters in a sparge_params: theta, scale (0 means 1/sqrt(d);
- * the pooled scores are scale * muQ . muK), topk_per_head and theta_per_head, and timing events
- * [0]-[3] (before pooling, after pooling, after the pooled scores, after the selection).  lambda,
- * precision, stats and lambda_per_head are unused.  Same workspace and errors as
- * sparge_predict_mask.
+ * the pooled scores are scale * muQ . muK), topk_per_head and theta_per_head, token_order, and
+ * timing events [0]-[3] (before pooling, after pooling, after the pooled scores, after the
+ * selection).  lambda, precision, stats and lambda_per_head are unused.  Same workspace and
+ * errors as sparge_predict_mask (with SPARGE_OP_TOKEN_ORDER when token_order is set).
  */
 int sparge_predict_mask_ex(const sparge_tensor *q, const sparge_tensor *k, float topk, int is_causal,
                            const sparge_params *params, uint8_t *mask, void *ws, size_t ws_bytes,

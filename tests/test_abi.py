@@ -53,9 +53,10 @@ def test_struct_layouts_match_the_header(tmp_path):
     src.write_text(
         "#include <stdio.h>\n#include <stddef.h>\n#include \"sparge.h\"\n"
         "int main(void) {\n"
-        "  printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(sparge_params), offsetof(sparge_params, stats),\n"
+        "  printf(\"%zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(sparge_params), offsetof(sparge_params, stats),\n"
         "         offsetof(sparge_params, timing_events), offsetof(sparge_params, topk_per_head),\n"
-        "         offsetof(sparge_params, theta_per_head), offsetof(sparge_params, lambda_per_head));\n"
+        "         offsetof(sparge_params, theta_per_head), offsetof(sparge_params, lambda_per_head),\n"
+        "         offsetof(sparge_params, token_order));\n"
         "  printf(\"%zu %zu %zu\\n\", sizeof(sparge_tensor), offsetof(sparge_tensor, B),\n"
         "         offsetof(sparge_tensor, stride_n));\n"
         "  return 0;\n}\n")
@@ -64,7 +65,8 @@ def test_struct_layouts_match_the_header(tmp_path):
     got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     P, T = fbs.sparge_params, fbs.sparge_tensor
     want = [ctypes.sizeof(P), P.stats.offset, P.timing_events.offset, P.topk_per_head.offset,
-            P.theta_per_head.offset, P.lambda_per_head.offset, ctypes.sizeof(T), T.B.offset, T.stride_n.offset]
+            P.theta_per_head.offset, P.lambda_per_head.offset, P.token_order.offset, ctypes.sizeof(T), T.B.offset,
+            T.stride_n.offset]
     assert got == want
 
 
@@ -100,6 +102,13 @@ def test_workspace_bytes(lib):
     assert fbs.workspace_bytes(fbs.SPARGE_OP_ATTN_Q8, B, Hq, Hkv, N, d) >= pred + Hq * nqb * nkb + q8
     assert fbs.workspace_bytes(fbs.SPARGE_OP_BLOCK_SPARSE_ATTN_Q8, B, Hq, Hkv, N, 64) == 0
     assert fbs.workspace_bytes(fbs.SPARGE_OP_ATTN_Q8, B, Hq, Hkv, N, 64) == 0
+    # with a token order: the op's bytes plus bf16 copies of Q and K
+    for op in (fbs.SPARGE_OP_PREDICT_MASK, fbs.SPARGE_OP_BLOCK_SPARSE_ATTN, fbs.SPARGE_OP_ATTN,
+               fbs.SPARGE_OP_BLOCK_SPARSE_ATTN_Q8, fbs.SPARGE_OP_ATTN_Q8):
+        base = fbs.workspace_bytes(op, B, Hq, Hkv, N, d)
+        assert fbs.workspace_bytes(op | fbs.SPARGE_OP_TOKEN_ORDER, B, Hq, Hkv, N, d) == base + 2 * B * (Hq + Hkv) * N * d
+    assert fbs.workspace_bytes(fbs.SPARGE_OP_ATTN_Q8 | fbs.SPARGE_OP_TOKEN_ORDER, B, Hq, Hkv, N, 64) == 0
+    assert fbs.workspace_bytes(0x200 | fbs.SPARGE_OP_ATTN, B, Hq, Hkv, N, d) == 0
 
 
 def _t(ptr=0x1000, B=1, H=2, N=256, d=64, dtype=fbs.SPARGE_BF16, sb=None, sh=None, sn=None):
