@@ -115,13 +115,23 @@ def row_softmax(S: np.ndarray) -> np.ndarray:
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def topk_select(p: np.ndarray, valid: np.ndarray, topk: float) -> np.ndarray:
+def count_target(topk: float, n: int) -> int:
+    """Blocks kept by the count reading of topk for a row of n valid blocks: ceil(topk * n),
+    taken with topk as the float32 the library receives and a 1e-3 allowance below each integer
+    (so 0.3 of 10 blocks is 3, not 4 through rounding), at least 1 and at most n."""
+    t = float(np.float32(topk)) * n - 1e-3
+    return int(min(n, max(1, math.ceil(t))))
+
+
+def topk_select(p: np.ndarray, valid: np.ndarray, topk: float, mode: str = "cdf") -> np.ndarray:
     """Keep set of one row of block probabilities.
 
     [overview, FAQ] topk lies in (0, 1]; lower means sparser.  [readme-cn, quick start]
-    topk = 0.5 keeps the top 50% of the attention weights.  Reading: order the valid blocks by
-    (probability descending, index ascending) and keep the shortest prefix whose cumulative
-    probability reaches topk; topk >= 1 keeps every valid block; at least one block is kept.
+    topk = 0.5 keeps the top 50% of the attention weights.  Reading ("cdf", the library's
+    default): order the valid blocks by (probability descending, index ascending) and keep the
+    shortest prefix whose cumulative probability reaches topk; topk >= 1 keeps every valid
+    block; at least one block is kept.  The other reading of the knob ("count"): keep the first
+    count_target(topk, n_valid) blocks of that order.
 
     p: (nkb,) probabilities, valid: (nkb,) bool with at least one True.  Returns bool (nkb,)."""
     keep = np.zeros(p.shape[0], dtype=bool)
@@ -130,6 +140,10 @@ def topk_select(p: np.ndarray, valid: np.ndarray, topk: float) -> np.ndarray:
         return keep
     vj = np.nonzero(valid)[0]
     order = vj[np.lexsort((vj, -p[vj]))]
+    if mode == "count":
+        keep[order[:count_target(topk, order.size)]] = True
+        return keep
+    assert mode == "cdf", mode
     c = np.cumsum(p[order])
     hit = np.nonzero(c >= topk)[0]
     kstar = (hit[0] + 1) if hit.size else order.size
@@ -138,7 +152,7 @@ def topk_select(p: np.ndarray, valid: np.ndarray, topk: float) -> np.ndarray:
 
 
 def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal: bool,
-                 scale: float = None) -> Dict[str, np.ndarray]:
+                 scale: float = None, mode: str = "cdf") -> Dict[str, np.ndarray]:
     """Stage 1 of SpargeAttn: the (B, Hq, ceil(N/128), ceil(N/64)) uint8 block mask.
 
     [overview, "Strengths"] mask shape and 128x64 granularity; [readme-cn, custom mask] 1 = keep.
@@ -148,7 +162,7 @@ def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal
     key/value head.  The softmax is taken over all valid blocks, similar or not.  Comparisons
     with theta are strict.
 
-    q: (B, Hq, N, d), k: (B, Hkv, N, d) float64."""
+    q: (B, Hq, N, d), k: (B, Hkv, N, d) float64.  mode: the reading of topk (topk_select)."""
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
     G = Hq // Hkv
@@ -165,7 +179,7 @@ def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal
         for h in range(Hq):
             colkeep = sK[b, h // G] < theta
             for i in range(nqb):
-                keep = topk_select(P[b, h, i], valid[i], topk)
+                keep = topk_select(P[b, h, i], valid[i], topk, mode)
                 if sQ[b, h, i] < theta:
                     keep |= valid[i]
                 keep |= colkeep & valid[i]
@@ -174,13 +188,14 @@ def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal
 
 
 def row_decisive(p: np.ndarray, valid: np.ndarray, sq: float, sk: np.ndarray, topk: float, theta: float,
-                 eps: float = 1e-3) -> bool:
+                 eps: float = 1e-3, mode: str = "cdf") -> bool:
     """Whether no rounding within ``eps`` can change one mask row (the bit-exact comparison set).
 
     A row is decisive when its query similarity is farther than eps from theta and either it
     keeps every block because s_Q < theta, or (i) the cumulative sum at the cut and the one
     before it are farther than eps from topk, (ii) the probability gap at the cut exceeds eps,
-    and (iii) every valid key block similarity is farther than eps from theta.
+    and (iii) every valid key block similarity is farther than eps from theta.  In the count
+    reading only (ii) and (iii) apply (the number kept does not depend on rounding).
     p: row probabilities (nkb,), valid: bool (nkb,), sq: s_Q of the row, sk: s_K (nkb,)."""
     if abs(sq - theta) <= eps:
         return False
@@ -193,6 +208,9 @@ def row_decisive(p: np.ndarray, valid: np.ndarray, sq: float, sk: np.ndarray, to
     vj = np.nonzero(valid)[0]
     order = vj[np.lexsort((vj, -p[vj]))]
     ps = p[order]
+    if mode == "count":
+        kc = count_target(topk, order.size)
+        return bool(kc >= ps.size or ps[kc - 1] - ps[kc] > eps)
     c = np.cumsum(ps)
     hit = np.nonzero(c >= topk)[0]
     kstar = (hit[0] + 1) if hit.size else order.size
@@ -203,7 +221,7 @@ def row_decisive(p: np.ndarray, valid: np.ndarray, sq: float, sk: np.ndarray, to
 
 
 def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal: bool,
-                  eps: float = 1e-3) -> np.ndarray:
+                  eps: float = 1e-3, mode: str = "cdf") -> np.ndarray:
     """row_decisive for every row of a predict_mask result: bool (B, Hq, nqb)."""
     P, sQ, sK = pred["P"], pred["sQ"], pred["sK"]
     B, Hq, nqb, nkb = P.shape
@@ -213,12 +231,13 @@ def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal
     for b in range(B):
         for h in range(Hq):
             for i in range(nqb):
-                out[b, h, i] = row_decisive(P[b, h, i], valid[i], sQ[b, h, i], sK[b, h // G], topk, theta, eps)
+                out[b, h, i] = row_decisive(P[b, h, i], valid[i], sQ[b, h, i], sK[b, h // G], topk, theta, eps,
+                                            mode)
     return out
 
 
 def predict_mask_row(q_block: np.ndarray, k_head: np.ndarray, i: int, topk: float, theta: float,
-                     causal: bool, scale: float = None) -> Dict[str, np.ndarray]:
+                     causal: bool, scale: float = None, mode: str = "cdf") -> Dict[str, np.ndarray]:
     """predict_mask for a single query block: q_block (n_i, d) the tokens of query block i,
     k_head (N, d) every key of its key/value head.  Same steps as predict_mask, for checking
     rows of workloads too large to run whole.  Returns mask (nkb,) uint8, P (nkb,), sQ (float),
@@ -233,7 +252,7 @@ def predict_mask_row(q_block: np.ndarray, k_head: np.ndarray, i: int, topk: floa
     s = scale * (muk[0, 0] @ muq[0, 0, 0])
     s[~valid] = -np.inf
     p = row_softmax(s)
-    keep = topk_select(p, valid, topk)
+    keep = topk_select(p, valid, topk, mode)
     if sq[0, 0, 0] < theta:
         keep |= valid
     keep |= (sk[0, 0] < theta) & valid

@@ -177,6 +177,63 @@ def test_mask_brute_force_causal_with_ties():
         assert not pred["mask"][0, 0, i][~valid[i]].any()
 
 
+# ----------------------------------------------------------------------------------------------
+# the count reading of topk: keep ceil(topk * n_valid) blocks
+# ----------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("topk,n,k", [(0.3, 10, 3), (0.5, 16, 8), (0.3, 16, 5), (0.25, 8, 2), (1e-9, 100, 1),
+                                      (1.0, 7, 7), (0.999, 7, 7), (0.5, 7, 4), (0.1, 2048, 205)])
+def test_count_target_values(topk, n, k):
+    assert oracle.count_target(topk, n) == k
+
+
+def brute_force_count_keep(p, valid, kc):
+    """Over all subsets of kc valid blocks: the largest probability sum; among those the
+    lexicographically smallest list of indices."""
+    vj = np.nonzero(valid)[0]
+    best, best_sum = None, -1.0
+    for sub in itertools.combinations(range(vj.size), kc):
+        ssum = float(p[vj[list(sub)]].sum())
+        if ssum > best_sum:
+            best, best_sum = sub, ssum
+    keep = np.zeros(p.size, bool)
+    keep[vj[list(best)]] = True
+    return keep
+
+
+def test_count_mode_matches_brute_force_tiny():
+    w = W.make_config("tiny")
+    q, k = f64(w.q), f64(w.k)
+    topk = 0.3                                     # 5 of the 16 key blocks of every row
+    pred = oracle.predict_mask(q, k, topk, 0.0, w.causal, mode="count")   # theta 0: no always-keep
+    from scipy.special import softmax
+    d = q.shape[-1]
+    mq = q.reshape(1, 2, 8, 128, d).mean(axis=3)
+    mk = k.reshape(1, 2, 16, 64, d).mean(axis=3)
+    P = softmax(np.einsum("bhid,bhjd->bhij", mq, mk) / math.sqrt(d), axis=-1)
+    valid = np.ones(16, bool)
+    for h in range(2):
+        for i in range(8):
+            keep = brute_force_count_keep(P[0, h, i], valid, 5)
+            np.testing.assert_array_equal(pred["mask"][0, h, i].astype(bool), keep)
+    assert (pred["mask"].sum(axis=-1) == 5).all()
+
+
+def test_count_mode_ties_keep_lowest_indices_and_is_monotone():
+    p = np.full(12, 1.0 / 12)
+    valid = np.ones(12, bool)
+    keep = oracle.topk_select(p, valid, 0.25, mode="count")
+    np.testing.assert_array_equal(np.nonzero(keep)[0], [0, 1, 2])
+    w = W.make_config("tiny")
+    q, k = f64(w.q), f64(w.k)
+    prev = None
+    for t in (0.05, 0.2, 0.5, 0.8, 1.0):
+        m = oracle.predict_mask(q, k, t, 0.0, False, mode="count")["mask"]
+        assert (m.sum(axis=-1) == oracle.count_target(t, 16)).all()
+        if prev is not None:
+            assert np.all(m >= prev)
+        prev = m
+
+
 def test_topk_one_keeps_all_valid_and_monotone():
     w = W.make_config("tiny")
     q, k = f64(w.q), f64(w.k)
