@@ -33,6 +33,8 @@ SPARGE_OP_ATTN = 3
 SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 = 4
 SPARGE_OP_ATTN_Q8 = 5
 SPARGE_OP_TOKEN_ORDER = 0x100  # flag OR-ed into an op: room for token-ordered copies of Q and K
+SPARGE_TOPK_CUMULATIVE = 0      # topk is a cumulative probability fraction (default)
+SPARGE_TOPK_COUNT = 1           # topk is a fraction of the valid blocks to keep
 QBLK, KBLK = 128, 64
 
 
@@ -52,7 +54,7 @@ class sparge_params(ctypes.Structure):
     _fields_ = [("theta", ctypes.c_float), ("lambda_", ctypes.c_float), ("scale", ctypes.c_float),
                 ("precision", ctypes.c_int32), ("stats", ctypes.c_void_p), ("timing_events", ctypes.c_void_p),
                 ("topk_per_head", ctypes.c_void_p), ("theta_per_head", ctypes.c_void_p),
-                ("lambda_per_head", ctypes.c_void_p), ("token_order", ctypes.c_void_p)]
+                ("lambda_per_head", ctypes.c_void_p), ("token_order", ctypes.c_void_p), ("topk_mode", ctypes.c_int32)]
 
 
 _lib = None
@@ -161,7 +163,8 @@ def predict_mask(q, k, topk: float, theta: float = 0.5, causal: bool = False, ws
 
 
 def predict_mask_ex(q, k, topk: float, causal: bool = False, theta: float = 0.5, scale: float = 0.0,
-                    topk_per_head=None, theta_per_head=None, ws=None, mask=None, events=None, token_order=None):
+                    topk_per_head=None, theta_per_head=None, ws=None, mask=None, events=None, token_order=None,
+                    topk_mode: int = SPARGE_TOPK_CUMULATIVE):
     """predict_mask with an explicit pooled-score scale, optional per-query-head topk and theta
     (float32 CUDA tensors of Hq entries), optional timing events ([0]-[3] are recorded) and an
     optional token order (int32 CUDA tensor of N entries; the mask refers to the reordered
@@ -172,7 +175,7 @@ def predict_mask_ex(q, k, topk: float, causal: bool = False, theta: float = 0.5,
         mask = torch.empty((B, Hq, -(-N // 128), -(-N // 64)), dtype=torch.uint8, device=q.device)
     ws = _workspace(SPARGE_OP_PREDICT_MASK | (SPARGE_OP_TOKEN_ORDER if token_order is not None else 0), q, k, ws)
     p = _params(theta, -math.inf, scale, SPARGE_PRECISION_BF16, None, events, topk_per_head, theta_per_head,
-                order=token_order)
+                order=token_order, topk_mode=topk_mode)
     dq, dk = _desc(q), _desc(k)
     _check(lib().sparge_predict_mask_ex(ctypes.byref(dq), ctypes.byref(dk), float(topk), int(causal), ctypes.byref(p),
                                         mask.data_ptr(), ws.data_ptr(), ws.numel(), _stream()))
@@ -290,7 +293,8 @@ def _order_ptr(order):
     return order.data_ptr()
 
 
-def _params(theta, lam, scale, precision, stats, events, topk_h=None, theta_h=None, lam_h=None, order=None):
+def _params(theta, lam, scale, precision, stats, events, topk_h=None, theta_h=None, lam_h=None, order=None,
+            topk_mode=0):
     """A sparge_params; `events` (6 torch.cuda.Event or None) are passed as cudaEvent_t handles.
     The handle array is kept on the returned struct so it outlives the call.  topk_h, theta_h and
     lam_h are optional per-query-head float32 CUDA tensors; order an optional int32 token order."""
@@ -305,7 +309,7 @@ def _params(theta, lam, scale, precision, stats, events, topk_h=None, theta_h=No
                       0 if stats is None else stats.data_ptr(),
                       ctypes.cast(evp, ctypes.c_void_p) if evp is not None else None,
                       _head_array(topk_h, "topk_per_head"), _head_array(theta_h, "theta_per_head"),
-                      _head_array(lam_h, "lambda_per_head"), _order_ptr(order))
+                      _head_array(lam_h, "lambda_per_head"), _order_ptr(order), int(topk_mode))
     p._evp = evp
     p._arrays = (topk_h, theta_h, lam_h, order)
     return p
@@ -336,7 +340,7 @@ def block_sparse_attn_ex(q, k, v, mask=None, causal: bool = False, lam: float = 
 def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: float = -math.inf,
                    scale: float = 0.0, precision: int = SPARGE_PRECISION_BF16, stats=None, mask_out=None,
                    out=None, ws=None, events=None, topk_per_head=None, theta_per_head=None, lambda_per_head=None,
-                   token_order=None):
+                   token_order=None, topk_mode: int = SPARGE_TOPK_CUMULATIVE):
     """sparge_attn with explicit theta, lambda, scale, counters, an optional mask output,
     optional timing events (6 torch.cuda.Event, recorded around the five kernels), optional
     per-query-head topk, theta and lambda (float32 CUDA tensors of Hq entries) and an optional
@@ -349,7 +353,7 @@ def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: 
     ws = _workspace((SPARGE_OP_ATTN_Q8 if q8 else SPARGE_OP_ATTN) | (SPARGE_OP_TOKEN_ORDER if token_order is not None else 0),
                     q, k, ws)
     p = _params(theta, lam, scale, precision, stats, events, topk_per_head, theta_per_head, lambda_per_head,
-                token_order)
+                token_order, topk_mode)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     mp = 0 if mask_out is None else mask_out.data_ptr()
     _check(lib().sparge_attn_ex(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), float(topk), int(causal),

@@ -210,6 +210,7 @@ int order_qk(View &q, View &k, const int32_t *perm, void *&ws, size_t &ws_bytes,
 // Per-query-head parameter arrays of a sparge_params (device pointers, each may be null).
 struct HeadParams {
   const float *topk = nullptr, *theta = nullptr, *lambda = nullptr;
+  int topk_mode = SPARGE_TOPK_CUMULATIVE;  // how topk selects blocks (enum sparge_topk_mode)
 };
 
 int predict_impl(const View &q, const View &k, float topk, float theta, int causal, float scale, uint8_t *mask,
@@ -246,7 +247,7 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
     if ((rc = record_event(ev, 2, s))) return rc;
   }
   e = launch_score_select(pw, (int)q.B, (int)q.H, (int)k.H, (int)q.N, (int)q.d, topk, theta, causal, mask, hp.topk,
-                          hp.theta, status_ptr(), s);
+                          hp.theta, status_ptr(), hp.topk_mode == SPARGE_TOPK_COUNT ? 1 : 0, s);
   if (e != cudaSuccess) return cuda_fail(e, "score_select launch");
   return record_event(ev, 3, s);
 }
@@ -438,9 +439,12 @@ int sparge_predict_mask_ex(const sparge_tensor *q, const sparge_tensor *k, float
   if (std::isnan(p->scale) || p->scale < 0.f || std::isinf(p->scale))
     return fail(SPARGE_ERR_INVALID_ARG, "scale must be finite and >= 0");
   const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)qv.d);
+  if (p->topk_mode != SPARGE_TOPK_CUMULATIVE && p->topk_mode != SPARGE_TOPK_COUNT)
+    return fail(SPARGE_ERR_INVALID_ARG, "topk_mode %d unknown", p->topk_mode);
   HeadParams hp;
   hp.topk = p->topk_per_head;
   hp.theta = p->theta_per_head;
+  hp.topk_mode = p->topk_mode;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (p->token_order) {
     const size_t need = order_bytes(qv.B, qv.H, kv.H, qv.N, qv.d) + predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, qv.d);
@@ -518,10 +522,13 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   if (p->token_order && qv.B * qv.N > 0 && (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s))) return rc;
   uint8_t *mask = mask_out ? mask_out : static_cast<uint8_t *>(ws) + need_pred;
   void *ws_v = static_cast<uint8_t *>(ws) + need_pred + mask_bytes;
+  if (p->topk_mode != SPARGE_TOPK_CUMULATIVE && p->topk_mode != SPARGE_TOPK_COUNT)
+    return fail(SPARGE_ERR_INVALID_ARG, "topk_mode %d unknown", p->topk_mode);
   HeadParams hp;
   hp.topk = p->topk_per_head;
   hp.theta = p->theta_per_head;
   hp.lambda = p->lambda_per_head;
+  hp.topk_mode = p->topk_mode;
   if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s, p->timing_events, hp)))
     return rc;
   return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws_v, need_v, s,

@@ -62,7 +62,7 @@ cudaError_t launch_score_gemm(const ScoreGemmLaunch &l, cudaStream_t st);
 // recorded in *status and its head keeps every valid block.
 cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int N, int d, float topk,
                                 float theta, int causal, uint8_t *mask, const float *topk_h, const float *theta_h,
-                                int *status, cudaStream_t st);
+                                int *status, int count_mode, cudaStream_t st);
 
 struct AttnLaunch {
   CUtensorMap tq, tk, tv;  // 4-D maps (d, N, H, B), 128-byte swizzle, boxes 64 x 128 (Q) / 64 x 64 (K, V);

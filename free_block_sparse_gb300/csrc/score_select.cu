@@ -40,24 +40,26 @@ struct SelArgs {
   float topk, theta;
   const float *topk_h, *theta_h;  // per query head, or nullptr
   int *status;
+  int count_mode;  // 0: keep the shortest prefix reaching topk of the mass; 1: keep ceil(topk * n) blocks
 };
 
 constexpr float LOG2E = 1.4426950408889634f;
 
-// e of the key blocks j0 .. j0 + 3 of a row (0 past the valid blocks); every pass uses this one
-// expression, so the values agree bit for bit between passes.  s - max is exact zero for the
-// maximum, and the hardware exponential is clamped at 1, so e <= 1 always.
-__device__ __forceinline__ float4 load_e(const float *srow, int j0, int nvalid, float negm) {
-  float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+// e of the key blocks j0 .. j0 + 3 of a row (`none` past the valid blocks: 0 for the mass
+// reading, -1 for the count reading, where an e of 0 is still a block to count); every pass uses
+// this one expression, so the values agree bit for bit between passes.  s - max is exact zero
+// for the maximum, and the hardware exponential is clamped at 1, so e <= 1 always.
+__device__ __forceinline__ float4 load_e(const float *srow, int j0, int nvalid, float negm, float none = 0.f) {
+  float4 e = make_float4(none, none, none, none);
   if (j0 < nvalid) {
     const float4 v = __ldg(reinterpret_cast<const float4 *>(srow + j0));
     const float2 l2 = make_float2(LOG2E, LOG2E), nm = make_float2(negm, negm);
     const float2 a = fmul2(fadd2(make_float2(v.x, v.y), nm), l2);
     const float2 b = fmul2(fadd2(make_float2(v.z, v.w), nm), l2);
     e.x = fminf(fast_exp2(a.x), 1.f);
-    e.y = j0 + 1 < nvalid ? fminf(fast_exp2(a.y), 1.f) : 0.f;
-    e.z = j0 + 2 < nvalid ? fminf(fast_exp2(b.x), 1.f) : 0.f;
-    e.w = j0 + 3 < nvalid ? fminf(fast_exp2(b.y), 1.f) : 0.f;
+    e.y = j0 + 1 < nvalid ? fminf(fast_exp2(a.y), 1.f) : none;
+    e.z = j0 + 2 < nvalid ? fminf(fast_exp2(b.x), 1.f) : none;
+    e.w = j0 + 3 < nvalid ? fminf(fast_exp2(b.y), 1.f) : none;
   }
   return e;
 }
@@ -72,7 +74,8 @@ __device__ __forceinline__ int warp_sum_i(int v) {
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   return v;
 }
-// x (>= 0) has a bit pattern in [lo, hi); lo >= 1, so x = 0 is never inside
+// x has a bit pattern in [lo, hi) (patterns of e >= 0 are ordered like the values; -1, the
+// count reading's mark for an invalid block, has the sign bit and is never inside)
 __device__ __forceinline__ bool in_range(float x, uint32_t lo, uint32_t hi) {
   return __float_as_uint(x) - lo < hi - lo;
 }
@@ -93,21 +96,23 @@ __device__ __forceinline__ void hist_zero(float *H, int lane) {
   for (int k = 0; k < NBIN; ++k) H[k * 32 + lane] = 0.f;
   __syncwarp();
 }
-// 32 bins of 2^shift patterns from hi - 1 down, lane-private column.  With d = hi - 1 - bits, x
-// is in [lo, hi) and in one of the 32 bins exactly when d < lim = min(hi - lo, 32 << shift).
+// 32 bins of 2^shift patterns from hi - 1 down, lane-private column; each element adds its mass
+// e (mass reading) or 1 (count reading, cnt).  With d = hi - 1 - bits, x is in [lo, hi) and in
+// one of the 32 bins exactly when d < lim = min(hi - lo, 32 << shift).
 __device__ __forceinline__ uint32_t hist_lim(const Cut &st) {
   const uint32_t w = st.hi - st.lo, b = static_cast<uint32_t>(NBIN) << st.shift;
   return w < b ? w : b;
 }
-__device__ __forceinline__ void hist_add(float *H, int lane, float x, const Cut &st, uint32_t lim) {
+__device__ __forceinline__ void hist_add(float *H, int lane, float x, const Cut &st, uint32_t lim, bool cnt) {
   const uint32_t d = st.hi - 1u - __float_as_uint(x);
-  if (d < lim) H[(d >> st.shift) * 32 + lane] += x;
+  if (d < lim) H[(d >> st.shift) * 32 + lane] += cnt ? 1.f : x;
 }
-__device__ __forceinline__ void hist_add4(float *H, int lane, const float4 &v, const Cut &st, uint32_t lim) {
-  hist_add(H, lane, v.x, st, lim);
-  hist_add(H, lane, v.y, st, lim);
-  hist_add(H, lane, v.z, st, lim);
-  hist_add(H, lane, v.w, st, lim);
+__device__ __forceinline__ void hist_add4(float *H, int lane, const float4 &v, const Cut &st, uint32_t lim,
+                                          bool cnt) {
+  hist_add(H, lane, v.x, st, lim, cnt);
+  hist_add(H, lane, v.y, st, lim, cnt);
+  hist_add(H, lane, v.z, st, lim, cnt);
+  hist_add(H, lane, v.w, st, lim, cnt);
 }
 // Narrows the state to the bin where the cumulative mass first reaches target (st.nc is left for
 // the caller to recount).  Returns false (state unchanged) if rounding left no bin reaching it.
@@ -190,25 +195,36 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
   }
   if (bad && lane == 0) record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
 
-  const bool keep_all = topk >= 1.f || a.sQ[row] < theta;
+  // The count reading keeps kc = ceil(topk * nvalid) blocks (a 1e-3 allowance below each integer
+  // keeps fp32 rounding of the product from adding a block), at least one: the cut is taken on
+  // block counts instead of mass, over every e in [0, 1] (an e that underflows to 0 still counts).
+  const bool cnt = a.count_mode != 0;
+  const float none = cnt ? -1.f : 0.f;
+  int kc = 0;
+  if (cnt) kc = min(nvalid, max(1, static_cast<int>(ceilf(topk * static_cast<float>(nvalid) - 1e-3f))));
+  const bool keep_all = topk >= 1.f || a.sQ[row] < theta || (cnt && kc >= nvalid);
   Cut st;
-  st.lo = 1u;
+  st.lo = cnt ? 0u : 1u;
   st.hi = 0x3F800001u;  // e <= 1: the maximum gives exactly 1
   st.above = 0.f;
   st.nc = 0x7fffffff;
   st.shift = 16;
   if (!keep_all) {
-    const float r2 = log2f(static_cast<float>(nvalid) / (1.f - topk)) + 0.1f;
-    while (static_cast<float>(NBIN) * exp2f(static_cast<float>(st.shift - 23)) < r2) ++st.shift;
+    if (cnt) {
+      st.shift = 25;  // 32 bins of 2^25 patterns cover [0, 1]
+    } else {
+      const float r2 = log2f(static_cast<float>(nvalid) / (1.f - topk)) + 0.1f;
+      while (static_cast<float>(NBIN) * exp2f(static_cast<float>(st.shift - 23)) < r2) ++st.shift;
+    }
     hist_zero(H, lane);
   }
-  // first pass: Z and the first histogram level
+  // first pass: Z (mass reading) and the first histogram level
   float2 z2 = make_float2(0.f, 0.f);
   const uint32_t lim1 = hist_lim(st);
   for (int t = 0; t < nit; ++t) {
-    const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm);
-    z2 = fadd2(z2, fadd2(make_float2(v.x, v.y), make_float2(v.z, v.w)));
-    if (!keep_all) hist_add4(H, lane, v, st, lim1);
+    const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm, none);
+    if (!cnt) z2 = fadd2(z2, fadd2(make_float2(v.x, v.y), make_float2(v.z, v.w)));
+    if (!keep_all) hist_add4(H, lane, v, st, lim1, cnt);
   }
   const float Z = warp_sum(z2.x + z2.y);
 
@@ -216,7 +232,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
   float et = 2.f;
   int jt = -1;
   if (!keep_all) {
-    const float target = topk * Z;
+    const float target = cnt ? static_cast<float>(kc) : topk * Z;
     bool ok = hist_pick(H, lane, target, st);
     bool listed = false;
     // compact the crossing bin; while it does not fit the short list, split it over the row
@@ -224,7 +240,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
       int n = 0;
       for (int t = 0; t < nit; ++t) {
         const int j0 = 128 * t + 4 * lane;
-        n = list_append(load_e(srow, j0, nvalid, negm), j0, st, Lv, Lj, n, lane);
+        n = list_append(load_e(srow, j0, nvalid, negm, none), j0, st, Lv, Lj, n, lane);
       }
       st.nc = n;
       if (n <= CMAX) {
@@ -234,7 +250,8 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
       if (st.shift < 0) break;
       hist_zero(H, lane);
       const uint32_t lim = hist_lim(st);
-      for (int t = 0; t < nit; ++t) hist_add4(H, lane, load_e(srow, 128 * t + 4 * lane, nvalid, negm), st, lim);
+      for (int t = 0; t < nit; ++t)
+        hist_add4(H, lane, load_e(srow, 128 * t + 4 * lane, nvalid, negm, none), st, lim, cnt);
       ok = hist_pick(H, lane, target, st);
     }
     bool sorted = false;
@@ -245,7 +262,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
 #pragma unroll
       for (int k = 0; k < CMAX / 32; ++k) {
         const int idx = lane + 32 * k;
-        ce[k] = idx < st.nc ? Lv[idx] : 0.f;
+        ce[k] = idx < st.nc ? Lv[idx] : none;
         cj[k] = idx < st.nc ? Lj[idx] : 0x7fffffff;
       }
       __syncwarp();
@@ -254,7 +271,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
         hist_zero(H, lane);
         const uint32_t lim = hist_lim(st);
 #pragma unroll
-        for (int k = 0; k < CMAX / 32; ++k) hist_add(H, lane, ce[k], st, lim);
+        for (int k = 0; k < CMAX / 32; ++k) hist_add(H, lane, ce[k], st, lim, cnt);
         ok = hist_pick(H, lane, target, st);
         if (ok) {
           int cnt = 0;
@@ -299,7 +316,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
             }
           }
         }
-        float ps = x > 0.f ? x : 0.f;
+        float ps = cnt ? (lane < st.nc ? 1.f : 0.f) : (x > 0.f ? x : 0.f);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const float v = __shfl_up_sync(0xffffffffu, ps, o);
@@ -316,15 +333,16 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
     }
     if (!sorted) {
       // bisection over the whole row for v* = the largest value with mass(e >= v*) >= target
-      uint32_t lo = 1u, hi = 0x3F800001u;
+      // each element weighs its mass, or 1 in the count reading (tv >= 0 leaves out the -1 marks)
+      auto wt = [&](float x, bool in) { return in ? (cnt ? 1.f : x) : 0.f; };
+      uint32_t lo = cnt ? 0u : 1u, hi = 0x3F800001u;
       while (hi - lo > 1u) {
         const uint32_t mid = lo + ((hi - lo) >> 1);
         const float tv = __uint_as_float(mid);
         float part = 0.f;
         for (int t = 0; t < nit; ++t) {
-          const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm);
-          part += (v.x >= tv ? v.x : 0.f) + (v.y >= tv ? v.y : 0.f) + (v.z >= tv ? v.z : 0.f) +
-                  (v.w >= tv ? v.w : 0.f);
+          const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm, none);
+          part += wt(v.x, v.x >= tv) + wt(v.y, v.y >= tv) + wt(v.z, v.z >= tv) + wt(v.w, v.w >= tv);
         }
         if (warp_sum(part) >= target)
           lo = mid;
@@ -335,14 +353,14 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
       // elements equal to v* are kept in ascending key-block order until the mass reaches target
       float above = 0.f;
       for (int t = 0; t < nit; ++t) {
-        const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm);
-        above += (v.x > et ? v.x : 0.f) + (v.y > et ? v.y : 0.f) + (v.z > et ? v.z : 0.f) + (v.w > et ? v.w : 0.f);
+        const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm, none);
+        above += wt(v.x, v.x > et) + wt(v.y, v.y > et) + wt(v.z, v.z > et) + wt(v.w, v.w > et);
       }
       float cum = warp_sum(above);
       jt = -1;
       for (int t = 0; t < nit && cum < target; ++t) {
         const int j0 = 128 * t + 4 * lane;
-        const float4 v = load_e(srow, j0, nvalid, negm);
+        const float4 v = load_e(srow, j0, nvalid, negm, none);
         int mine = 0;  // ties held by this lane
 #pragma unroll
         for (int u = 0; u < 4; ++u) mine += (comp(v, u) == et && j0 + u < nvalid) ? 1 : 0;
@@ -354,7 +372,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
         }
         const int total = __shfl_sync(0xffffffffu, upto, 31);
         // ties still needed to bring the mass to target
-        const int take = max(1, static_cast<int>(ceilf((target - cum) / et)));
+        const int take = cnt ? static_cast<int>(target - cum) : max(1, static_cast<int>(ceilf((target - cum) / et)));
         if (take <= total) {
           const int first = upto - mine;  // ties before this lane
           int jsel = -1;
@@ -367,7 +385,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
           jt = __reduce_max_sync(0xffffffffu, jsel);
           cum = target;
         } else {
-          cum += et * static_cast<float>(total);
+          cum += (cnt ? 1.f : et) * static_cast<float>(total);
           jt = 128 * t + 127;  // every tie of this stretch is kept
         }
       }
@@ -382,7 +400,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
     const int j0 = 128 * t + 4 * lane;
     uint32_t word = 0u;
     if (j0 < nvalid) {
-      const float4 v = load_e(srow, j0, nvalid, negm);
+      const float4 v = load_e(srow, j0, nvalid, negm, none);
       const float4 sk = __ldg(reinterpret_cast<const float4 *>(sKrow + j0));
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -419,7 +437,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
 
 cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int N, int d, float topk,
                                 float theta, int causal, uint8_t *mask, const float *topk_h, const float *theta_h,
-                                int *status, cudaStream_t st) {
+                                int *status, int count_mode, cudaStream_t st) {
   (void)d;
   SelArgs a;
   a.S = ws.S;
@@ -438,6 +456,7 @@ cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int
   a.topk_h = topk_h;
   a.theta_h = theta_h;
   a.status = status;
+  a.count_mode = count_mode;
   if (a.rows == 0) return cudaSuccess;
   if (a.rows > 0x7fffffffLL) return cudaErrorInvalidValue;  // the kernel indexes rows in 32 bits
   const int64_t grid = (a.rows + WARPS - 1) / WARPS;

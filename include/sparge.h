@@ -57,6 +57,16 @@ enum sparge_precision {
   SPARGE_PRECISION_Q8_FP8PV = 2       /* 8-bit Q.K^T and P.V (both e4m3); d = 128 */
 };
 
+/* How topk picks a mask row's blocks (sparge_params.topk_mode). */
+enum sparge_topk_mode {
+  SPARGE_TOPK_CUMULATIVE = 0,  /* the shortest prefix, in (probability desc, index asc) order, whose
+                                  cumulative probability reaches topk (the pages' "top 50% of the
+                                  attention weights"; the default) */
+  SPARGE_TOPK_COUNT = 1        /* the first ceil(topk * n_valid) blocks of that order (at least one;
+                                  the product is taken in fp32 with topk as given, less 1e-3, so
+                                  that rounding never adds a block) */
+};
+
 enum sparge_op {
   SPARGE_OP_PREDICT_MASK = 1,
   SPARGE_OP_BLOCK_SPARSE_ATTN = 2,
@@ -116,6 +126,9 @@ typedef struct sparge_params {
    * outside that range is never used as an address (its row is skipped or zero) and records
    * SPARGE_ERR_INVALID_ARG in the device status word. */
   const int32_t *token_order;
+  /* How topk (and topk_per_head) picks blocks: enum sparge_topk_mode (0, the cumulative reading,
+   * when the struct is zeroed).  Used by sparge_predict_mask_ex and sparge_attn_ex. */
+  int32_t topk_mode;
 } sparge_params;
 
 /*

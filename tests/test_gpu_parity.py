@@ -101,6 +101,55 @@ def test_mask_equal_scores_keep_lowest_indices(causal):
         assert gm[..., :math.ceil(topk * nvalid)].all()
 
 
+@pytest.mark.parametrize("key,topk", [("tiny", 0.3), ("llama", 0.5), ("flux", 0.25), ("cogvideox", 0.1)])
+def test_count_mode_mask_matches_oracle(key, topk):
+    """The count reading of topk (ceil(topk * n_valid) blocks per row): bit-exact on the rows whose
+    probability gap at the cut and similarity margins exceed 1e-3."""
+    w = make(key)
+    q, k = dev_bf16(w.q), dev_bf16(w.k)
+    gm = fbs.predict_mask_ex(q, k, topk, w.causal, theta=w.theta, topk_mode=fbs.SPARGE_TOPK_COUNT).cpu().numpy()
+    pred = oracle.predict_mask(f64(w.q), f64(w.k), topk, w.theta, w.causal, mode="count")
+    dec = oracle.decisive_rows(pred, topk, w.theta, w.causal, mode="count")
+    assert dec.mean() > 0.2
+    bad = np.nonzero((gm != pred["mask"]).any(axis=-1) & dec)
+    assert bad[0].size == 0, "count-mode mask differs on decisive rows %s" % (list(zip(*bad))[:5],)
+    # rows that no similarity rule touches keep exactly the count
+    valid = oracle.block_valid(w.nqb, w.nkb, w.causal)
+    G = w.Hq // w.Hkv
+    for b, h, i in zip(*np.nonzero(dec)):
+        if pred["sQ"][b, h, i] >= w.theta and (pred["sK"][b, h // G][valid[i]] >= w.theta).all():
+            assert gm[b, h, i].sum() == oracle.count_target(topk, int(valid[i].sum()))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_count_mode_equal_scores_keep_lowest_indices(causal):
+    """All pooled scores of a row equal: the count reading keeps the lowest indices, through the
+    same tie paths as the cumulative reading (up to 300 tied candidates per row), and rows where
+    exp underflows are not an issue because every e is 1."""
+    B, Hq, Hkv, N, d = 1, 2, 1, 300 * 64, 64
+    qu, ku, _ = W.random_qkv(26, B, Hq, Hkv, N, d)
+    ku = np.broadcast_to(ku[:, :, :1, :], ku.shape).copy()
+    topk, theta = 0.331, 0.0
+    gm = fbs.predict_mask_ex(dev_bf16(qu), dev_bf16(ku), topk, causal, theta=theta,
+                             topk_mode=fbs.SPARGE_TOPK_COUNT).cpu().numpy()
+    pred = oracle.predict_mask(f64(qu), f64(ku), topk, theta, causal, mode="count")
+    assert np.array_equal(gm, pred["mask"])
+
+
+def test_count_mode_through_sparge_attn_ex():
+    """sparge_attn_ex with the count reading: its mask is predict_mask_ex's, its output the
+    oracle's attention on that mask."""
+    w = make("llama")
+    q, k, v = dev_bf16(w.q), dev_bf16(w.k), dev_bf16(w.v)
+    mask = torch.empty((w.B, w.Hq, w.nqb, w.nkb), dtype=torch.uint8, device="cuda")
+    out = fbs.sparge_attn_ex(q, k, v, 0.4, w.causal, theta=w.theta, mask_out=mask, topk_mode=fbs.SPARGE_TOPK_COUNT)
+    m2 = fbs.predict_mask_ex(q, k, 0.4, w.causal, theta=w.theta, topk_mode=fbs.SPARGE_TOPK_COUNT)
+    assert torch.equal(mask, m2)
+    ref = oracle.block_sparse_attn(f64(w.q), f64(w.k), f64(w.v), mask.cpu().numpy(), -math.inf, w.causal)
+    cos, err = cos_maxabs(host_f64(out), ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
+
+
 @pytest.mark.parametrize("topk,theta", [(0.05, 0.5), (0.3, 0.3), (0.9, 0.0), (1.0, 0.5), (0.5, 2.0)])
 def test_mask_topk_theta_sweep(topk, theta):
     w = make("llama")
