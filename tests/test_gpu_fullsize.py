@@ -100,7 +100,8 @@ def _check_block(w, gm, got, b, h, i, lam, predicted, cos_min=COS_MIN, maxabs=MA
     return decisive
 
 
-@pytest.mark.parametrize("name,nsamp", [("llama128k", 12), ("llama32k", 12), ("flux", 8), ("cogvideox", 8)])
+@pytest.mark.parametrize("name,nsamp", [("llama128k", 12), ("llama32k", 12), ("flux", 8), ("cogvideox", 8),
+                                         ("vit", 8)])
 def test_full_size_predicted_mask_and_attention(name, nsamp):
     w = _workload(name)
     q, k, v = dev_bf16(w.q), dev_bf16(w.k), dev_bf16(w.v)

@@ -20,6 +20,7 @@ SMALL = {
     "llama": dict(name="llama32k", N=4096 + 200, Hq=8, Hkv=2),
     "flux": dict(name="flux", Hq=4, Hkv=4),
     "cogvideox": dict(name="cogvideox", Hq=2, Hkv=2, grid=(5, 30, 45)),
+    "vit": dict(name="vit", Hq=2, Hkv=2, grid=(32, 32)),
 }
 
 
@@ -246,7 +247,7 @@ def test_sparge_attn_end_to_end(key):
         assert torch.equal(out, out2)
 
 
-@pytest.mark.parametrize("key", ["flux", "cogvideox"])
+@pytest.mark.parametrize("key", ["flux", "cogvideox", "vit"])
 def test_hilbert_pipeline(key):
     w = make(key)
     perm_np = (fbs.hilbert_perm_2d(w.n_prefix, *w.grid) if len(w.grid) == 2

@@ -187,7 +187,7 @@ def _bernoulli_mask(rng, B, H, N, p=0.25):
 # --------------------------------------------------------------------------
 # named workloads
 # --------------------------------------------------------------------------
-CONFIG_NAMES = ("tiny", "flux", "cogvideox", "llama32k", "llama128k", "custom")
+CONFIG_NAMES = ("tiny", "flux", "cogvideox", "llama32k", "llama128k", "custom", "vit")
 
 # one line per workload on how its tokens are drawn (for reports)
 DATA_DESCRIPTIONS = {
@@ -197,6 +197,7 @@ DATA_DESCRIPTIONS = {
     "llama32k": "Llama-like rotary structure with attention sink",
     "llama128k": "Llama-like rotary structure with attention sink",
     "custom": "i.i.d. N(0,1) Q/K/V with a Bernoulli(0.25) tile mask, diagonal tiles on",
+    "vit": "a 64 x 64 patch grid, 2-D Gaussian random field (correlation length 4 patches) with N(0,0.2) noise",
 }
 
 
@@ -216,6 +217,9 @@ def describe(name: str, **over) -> Workload:
         w = Workload(name, 1, 32, 8, 131072, 128, True, 0.5, 0.5, -8.0)
     elif name == "custom":
         w = Workload(name, 2, 16, 16, 65536, 128, False, 1.0, 0.5, -math.inf)
+    elif name == "vit":
+        # ViT-like image encoder: small batch, non-causal, 64 x 64 patches, no text prefix
+        w = Workload(name, 2, 12, 12, 64 * 64, 64, False, 0.5, 0.5, -math.inf, n_prefix=0, grid=(64, 64))
     else:
         raise KeyError(name)
     for key, val in over.items():
@@ -240,6 +244,11 @@ def make_config(name: str, seed: int = 0, **over) -> Workload:
         w.v = _block_mean_tokens(rng, B, Hkv, N, d)
     elif name == "flux":
         sig = (6.0, 6.0)
+        w.q = _smooth_field_tokens(rng, B, Hq, d, w.n_prefix, w.grid, sig)
+        w.k = _smooth_field_tokens(rng, B, Hkv, d, w.n_prefix, w.grid, sig)
+        w.v = _smooth_field_tokens(rng, B, Hkv, d, w.n_prefix, w.grid, sig)
+    elif name == "vit":
+        sig = (4.0, 4.0)
         w.q = _smooth_field_tokens(rng, B, Hq, d, w.n_prefix, w.grid, sig)
         w.k = _smooth_field_tokens(rng, B, Hkv, d, w.n_prefix, w.grid, sig)
         w.v = _smooth_field_tokens(rng, B, Hkv, d, w.n_prefix, w.grid, sig)
