@@ -395,16 +395,19 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       tc_fence_after();
       const uint32_t sc = tl + SCOL0 + buf * 64;
       float x[64];  // raw scores Q.K^T of this row; hidden columns become -inf
+      float mhw;    // their maximum, from the loads' max reduction
       {
         uint32_t r0[32], r1[32];
-        tmem_ld32(sc, r0);
-        tmem_ld32(sc + 32, r1);
+        float m0, m1;
+        tmem_ld32_max(sc, r0, m0);
+        tmem_ld32_max(sc + 32, r1, m1);
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           x[c] = __uint_as_float(r0[c]);
           x[32 + c] = __uint_as_float(r1[c]);
         }
+        mhw = fmaxf(m0, m1);
       }
       const bool edge = (a.causal && KBLK * j + KBLK - 1 > QBLK * i) || (KBLK * j + KBLK > a.N);
       if (!row_ok) {
@@ -416,10 +419,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
       }
-      float mraw = fmax3(x[0], x[1], x[2]);
+      // a tile with hidden columns needs the maximum of what stays visible
+      float mraw = mhw;
+      if (!row_ok || edge) {
+        mraw = fmax3(x[0], x[1], x[2]);
 #pragma unroll
-      for (int c = 3; c < 63; c += 2) mraw = fmax3(mraw, x[c], x[c + 1]);
-      mraw = fmaxf(mraw, x[63]);
+        for (int c = 3; c < 63; c += 2) mraw = fmax3(mraw, x[c], x[c + 1]);
+        mraw = fmaxf(mraw, x[63]);
+      }
       // score multiplier of this tile (8-bit path: times the Q block and K block scales)
       const float tsc = QK8 ? a.scale_log2 * sq_blk * __ldg(skrow + j) : a.scale_log2;
       const float mloc = mraw * tsc;  // the multiplier is positive: max commutes with it
