@@ -81,17 +81,20 @@ def pool_sim(x: np.ndarray, blk: int) -> Tuple[np.ndarray, np.ndarray]:
 # ---------------------------------------------------------------------------------------------
 # Stage 1b: pooled score map, row softmax, cumulative top-k, always-keep
 # ---------------------------------------------------------------------------------------------
-def block_valid(nqb: int, nkb: int, causal: bool) -> np.ndarray:
+def block_valid(nqb: int, nkb: int, causal: bool, off: int = 0) -> np.ndarray:
     """(nqb, nkb) bool: a 128x64 tile is valid unless causal attention hides all of it.
-    Tile (i, j) holds some visible element iff 64*j <= 128*i + 127."""
+    Query row r sees key column c when c <= off + r, where off = Nk - Nq puts the last query on
+    the last key (a short query block continues the key sequence; reading for Nq < Nk, the
+    pages only treat Nq = Nk, off = 0).  Tile (i, j) holds some visible element iff
+    64*j <= off + 128*i + 127."""
     i = np.arange(nqb)[:, None]
     j = np.arange(nkb)[None, :]
     if not causal:
         return np.ones((nqb, nkb), dtype=bool)
-    return KBLK * j <= QBLK * i + (QBLK - 1)
+    return KBLK * j <= off + QBLK * i + (QBLK - 1)
 
 
-def pooled_scores(muQ: np.ndarray, muK: np.ndarray, causal: bool, scale: float) -> np.ndarray:
+def pooled_scores(muQ: np.ndarray, muK: np.ndarray, causal: bool, scale: float, off: int = 0) -> np.ndarray:
     """S_hat[b, h, i, j] = scale * muQ[b, h, i] . muK[b, h // G, j], -inf on invalid tiles.
 
     [abstract] stage 1 predicts the attention map from a compressed form of Q and K; the
@@ -104,7 +107,7 @@ def pooled_scores(muQ: np.ndarray, muK: np.ndarray, causal: bool, scale: float) 
     for b in range(B):
         for h in range(Hq):
             S[b, h] = scale * (muQ[b, h] @ muK[b, h // G].T)
-    S[:, :, ~block_valid(nqb, nkb, causal)] = -np.inf
+    S[:, :, ~block_valid(nqb, nkb, causal, off)] = -np.inf
     return S
 
 
@@ -162,18 +165,20 @@ def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal
     key/value head.  The softmax is taken over all valid blocks, similar or not.  Comparisons
     with theta are strict.
 
-    q: (B, Hq, N, d), k: (B, Hkv, N, d) float64.  mode: the reading of topk (topk_select)."""
+    q: (B, Hq, Nq, d), k: (B, Hkv, Nk, d) float64 (Nq <= Nk when causal; off = Nk - Nq as in
+    block_valid).  mode: the reading of topk (topk_select)."""
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
+    off = k.shape[2] - N
     G = Hq // Hkv
     if scale is None:
         scale = default_scale(d)
     muQ, sQ = pool_sim(q, QBLK)
     muK, sK = pool_sim(k, KBLK)
-    S = pooled_scores(muQ, muK, causal, scale)
+    S = pooled_scores(muQ, muK, causal, scale, off)
     P = row_softmax(S)
     nqb, nkb = S.shape[2], S.shape[3]
-    valid = block_valid(nqb, nkb, causal)
+    valid = block_valid(nqb, nkb, causal, off)
     mask = np.zeros((B, Hq, nqb, nkb), dtype=np.uint8)
     for b in range(B):
         for h in range(Hq):
@@ -184,7 +189,7 @@ def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal
                     keep |= valid[i]
                 keep |= colkeep & valid[i]
                 mask[b, h, i] = keep
-    return dict(mask=mask, muQ=muQ, sQ=sQ, muK=muK, sK=sK, S=S, P=P)
+    return dict(mask=mask, muQ=muQ, sQ=sQ, muK=muK, sK=sK, S=S, P=P, off=off)
 
 
 def row_decisive(p: np.ndarray, valid: np.ndarray, sq: float, sk: np.ndarray, topk: float, theta: float,
@@ -226,7 +231,7 @@ def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal
     P, sQ, sK = pred["P"], pred["sQ"], pred["sK"]
     B, Hq, nqb, nkb = P.shape
     G = Hq // sK.shape[1]
-    valid = block_valid(nqb, nkb, causal)
+    valid = block_valid(nqb, nkb, causal, pred.get("off", 0))
     out = np.zeros((B, Hq, nqb), dtype=bool)
     for b in range(B):
         for h in range(Hq):
@@ -237,7 +242,7 @@ def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal
 
 
 def predict_mask_row(q_block: np.ndarray, k_head: np.ndarray, i: int, topk: float, theta: float,
-                     causal: bool, scale: float = None, mode: str = "cdf") -> Dict[str, np.ndarray]:
+                     causal: bool, scale: float = None, mode: str = "cdf", off: int = 0) -> Dict[str, np.ndarray]:
     """predict_mask for a single query block: q_block (n_i, d) the tokens of query block i,
     k_head (N, d) every key of its key/value head.  Same steps as predict_mask, for checking
     rows of workloads too large to run whole.  Returns mask (nkb,) uint8, P (nkb,), sQ (float),
@@ -248,7 +253,7 @@ def predict_mask_row(q_block: np.ndarray, k_head: np.ndarray, i: int, topk: floa
     muq, sq = pool_sim(q_block[None, None], QBLK)
     muk, sk = pool_sim(k_head[None, None], KBLK)
     nkb = muk.shape[2]
-    valid = block_valid(i + 1, nkb, causal)[i]
+    valid = block_valid(i + 1, nkb, causal, off)[i]
     s = scale * (muk[0, 0] @ muq[0, 0, 0])
     s[~valid] = -np.inf
     p = row_softmax(s)
@@ -263,10 +268,11 @@ def predict_mask_row(q_block: np.ndarray, k_head: np.ndarray, i: int, topk: floa
 # Stage 2: block-sparse flash attention with the lambda warp filter
 # ---------------------------------------------------------------------------------------------
 def attn_qblock(Qi: np.ndarray, Kh: np.ndarray, Vh: np.ndarray, i: int, kept, lam: float, causal: bool,
-                scale: float, group: int = WARP_ROWS):
-    """The rows of one query block: Qi (n_i, d), Kh/Vh (N, d) of its key/value head, kept the
-    ascending key-block indices to visit (already restricted to valid tiles).  Returns the
-    output rows (n_i, d) and (kept tiles, skipped group-tiles, tiles with a P.V update)."""
+                scale: float, group: int = WARP_ROWS, off: int = 0):
+    """The rows of one query block: Qi (n_i, d), Kh/Vh (Nk, d) of its key/value head, kept the
+    ascending key-block indices to visit (already restricted to valid tiles); causal rows see
+    the columns c <= off + row (block_valid).  Returns the output rows (n_i, d) and (kept tiles,
+    skipped group-tiles, tiles with a P.V update)."""
     N, d = Kh.shape
     r0 = i * QBLK
     nr = Qi.shape[0]
@@ -282,7 +288,7 @@ def attn_qblock(Qi: np.ndarray, Kh: np.ndarray, Vh: np.ndarray, i: int, kept, la
         n_tiles += 1
         S = scale * (Qi @ Kh[c0:c1].T)
         if causal:
-            S = np.where(np.arange(c0, c1)[None, :] > rows[:, None], -np.inf, S)
+            S = np.where(np.arange(c0, c1)[None, :] > off + rows[:, None], -np.inf, S)
         m_loc = S.max(axis=1)
         m_new = np.maximum(m, m_loc)
         with np.errstate(invalid="ignore"):
@@ -320,14 +326,16 @@ def block_sparse_attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask, lam: fl
 
     mask: (B, Hq, nqb, nkb) uint8 or None (all ones).  Tiles above the causal diagonal are never
     visited.  ``qblocks`` optionally restricts the work to a list of (b, h, i) query blocks (the
-    other rows of O stay 0).  Returns O (B, Hq, N, d) float64 (and statistics when asked)."""
+    other rows of O stay 0).  q may be shorter than k and v (Nq <= Nk when causal, off = Nk - Nq
+    as in block_valid).  Returns O (B, Hq, Nq, d) float64 (and statistics when asked)."""
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
+    off = k.shape[2] - N
     G = Hq // Hkv
     if scale is None:
         scale = default_scale(d)
-    nqb, nkb = n_blocks(N, QBLK), n_blocks(N, KBLK)
-    valid = block_valid(nqb, nkb, causal)
+    nqb, nkb = n_blocks(N, QBLK), n_blocks(k.shape[2], KBLK)
+    valid = block_valid(nqb, nkb, causal, off)
     O = np.zeros((B, Hq, N, d))
     tot = np.zeros(3, dtype=np.int64)
     if qblocks is None:
@@ -337,7 +345,7 @@ def block_sparse_attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask, lam: fl
         kept = np.ones(nkb, bool) if mask is None else (mask[b, h, i] != 0)
         js = np.nonzero(kept & valid[i])[0]
         O[b, h, r0:r1], st = attn_qblock(q[b, h, r0:r1], k[b, h // G], v[b, h // G], i, js, lam, causal,
-                                         scale, group)
+                                         scale, group, off)
         tot += st
     if return_stats:
         return O, dict(kept_tiles=int(tot[0]), skipped_group_tiles=int(tot[1]), pv_tiles=int(tot[2]))

@@ -77,6 +77,62 @@ def test_topk_one_equals_dense(causal, N, Hq, Hkv, d):
     np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
 
 
+# ----------------------------------------------------------------------------------------------
+# short queries (Nq < Nk): the last query sits on the last key
+# ----------------------------------------------------------------------------------------------
+def sdpa_f64_offset(q, k, v, causal):
+    """float64 SDPA with an explicit boolean mask: query r sees key c when c <= (Nk - Nq) + r."""
+    G = q.shape[1] // k.shape[1]
+    Nq, Nk = q.shape[2], k.shape[2]
+    tq, tk = torch.from_numpy(q), torch.from_numpy(np.repeat(k, G, axis=1))
+    tv = torch.from_numpy(np.repeat(v, G, axis=1))
+    m = None
+    if causal:
+        m = torch.from_numpy(np.arange(Nk)[None, :] <= (Nk - Nq) + np.arange(Nq)[:, None])
+    return torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=m).numpy()
+
+
+@pytest.mark.parametrize("Nq,Nk", [(128, 1024), (300, 700), (1, 513), (700, 700)])
+def test_block_valid_with_offset_brute_force(Nq, Nk):
+    nqb, nkb, off = -(-Nq // 128), -(-Nk // 64), Nk - Nq
+    got = oracle.block_valid(nqb, nkb, True, off)
+    for i in range(nqb):
+        for j in range(nkb):
+            rows = np.arange(128 * i, min(Nq, 128 * i + 128))
+            cols = np.arange(64 * j, min(Nk, 64 * j + 64))
+            vis = (cols[None, :] <= off + rows[:, None]).any()
+            assert got[i, j] == vis, (i, j)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk,Hq,Hkv,d", [(256, 1024, 2, 1, 64), (130, 700, 2, 2, 32), (1, 300, 1, 1, 64)])
+def test_short_query_dense_equals_sdpa(causal, Nq, Nk, Hq, Hkv, d):
+    rng = np.random.Generator(np.random.PCG64(Nq + Nk))
+    q = f64(W.bf16_bits(rng.standard_normal((1, Hq, Nq, d)).astype(np.float32)))
+    _, k, v = (f64(t) for t in W.random_qkv(5, 1, Hq, Hkv, Nk, d))
+    ref = sdpa_f64_offset(q, k, v, causal)
+    out = oracle.sparge_attn(q, k, v, topk=1.0, causal=causal, theta=0.5, lam=-math.inf)
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    if causal:   # and it is the tail of the full causal attention over a sequence ending in q
+        qf = np.concatenate([f64(W.random_qkv(6, 1, Hq, Hkv, Nk - Nq, d)[0]), q], axis=2) if Nk > Nq else q
+        full = oracle.block_sparse_attn(qf, k, v, None, -math.inf, True)
+        np.testing.assert_allclose(out, full[:, :, Nk - Nq:], rtol=1e-10, atol=1e-12)
+
+
+def test_short_query_mask_brute_force():
+    rng = np.random.Generator(np.random.PCG64(11))
+    Nq, Nk, d = 384, 1280, 32
+    q = rng.standard_normal((1, 1, 1, d)) + 0.3 * rng.standard_normal((1, 1, Nq, d))
+    k = rng.standard_normal((1, 1, 20, d)).repeat(64, axis=2) + 0.3 * rng.standard_normal((1, 1, Nk, d))
+    for causal in (False, True):
+        pred = oracle.predict_mask(q, k, topk=0.6, theta=0.0, causal=causal)
+        valid = oracle.block_valid(3, 20, causal, Nk - Nq)
+        for i in range(3):
+            keep = brute_force_keep(pred["P"][0, 0, i], valid[i], 0.6)
+            np.testing.assert_array_equal(pred["mask"][0, 0, i].astype(bool), keep)
+            assert not pred["mask"][0, 0, i][~valid[i]].any()
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_all_ones_mask_equals_dense(causal):
     q, k, v = (f64(t) for t in W.random_qkv(4, 2, 4, 2, 700, 64))
