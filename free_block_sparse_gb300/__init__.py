@@ -141,18 +141,18 @@ def n_blocks(N: int):
 
 def _workspace(op, q, k, ws):
     torch = _torch()
-    B, Hq, N, d = q.shape
-    need = workspace_bytes(op, B, Hq, k.shape[1], N, d)
+    B, Hq, Nq, d = q.shape
+    need = workspace_bytes(op, B, Hq, k.shape[1], max(Nq, k.shape[2]), d)   # N: an upper bound of both
     if ws is None:
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     return ws
 
 
 def predict_mask(q, k, topk: float, theta: float = 0.5, causal: bool = False, ws=None, mask=None):
-    """Stage 1: the (B, Hq, ceil(N/128), ceil(N/64)) uint8 block mask."""
+    """Stage 1: the (B, Hq, ceil(Nq/128), ceil(Nk/64)) uint8 block mask."""
     torch = _torch()
-    B, Hq, N, d = q.shape
-    nqb, nkb = n_blocks(N)
+    B, Hq, Nq, d = q.shape
+    nqb, nkb = -(-Nq // 128), -(-k.shape[2] // 64)
     if mask is None:
         mask = torch.empty((B, Hq, nqb, nkb), dtype=torch.uint8, device=q.device)
     ws = _workspace(SPARGE_OP_PREDICT_MASK, q, k, ws)
@@ -170,9 +170,9 @@ def predict_mask_ex(q, k, topk: float, causal: bool = False, theta: float = 0.5,
     optional token order (int32 CUDA tensor of N entries; the mask refers to the reordered
     sequence)."""
     torch = _torch()
-    B, Hq, N, _ = q.shape
+    B, Hq, Nq, _ = q.shape
     if mask is None:
-        mask = torch.empty((B, Hq, -(-N // 128), -(-N // 64)), dtype=torch.uint8, device=q.device)
+        mask = torch.empty((B, Hq, -(-Nq // 128), -(-k.shape[2] // 64)), dtype=torch.uint8, device=q.device)
     ws = _workspace(SPARGE_OP_PREDICT_MASK | (SPARGE_OP_TOKEN_ORDER if token_order is not None else 0), q, k, ws)
     p = _params(theta, -math.inf, scale, SPARGE_PRECISION_BF16, None, events, topk_per_head, theta_per_head,
                 order=token_order, topk_mode=topk_mode)

@@ -80,10 +80,22 @@ int check_tensor(const sparge_tensor *t, const char *name, View *v) {
   return SPARGE_OK;
 }
 
+// q may be shorter (or, without the causal mask, longer) than k; the causal case is checked where
+// the mask kind is known (check_lengths).
 int check_qk(const View &q, const View &k) {
-  if (k.B != q.B || k.N != q.N || k.d != q.d)
-    return fail(SPARGE_ERR_INVALID_ARG, "q and k disagree in B, N or d");
+  if (k.B != q.B || k.d != q.d)
+    return fail(SPARGE_ERR_INVALID_ARG, "q and k disagree in B or d");
   if (q.H % k.H != 0) return fail(SPARGE_ERR_UNSUPPORTED, "Hq=%lld not a multiple of Hkv=%lld", (long long)q.H, (long long)k.H);
+  return SPARGE_OK;
+}
+
+// Causal attention with Nq != Nk puts the last query on the last key, so it needs Nq <= Nk; a
+// call with queries needs keys.
+int check_lengths(const View &q, const View &k, int causal) {
+  if (causal && q.N > k.N)
+    return fail(SPARGE_ERR_INVALID_ARG, "causal attention needs Nq <= Nk (got %lld > %lld)", (long long)q.N,
+                (long long)k.N);
+  if (q.N > 0 && k.N == 0) return fail(SPARGE_ERR_INVALID_ARG, "k and v have no tokens");
   return SPARGE_OK;
 }
 
@@ -216,15 +228,16 @@ struct HeadParams {
 int predict_impl(const View &q, const View &k, float topk, float theta, int causal, float scale, uint8_t *mask,
                  void *ws, size_t ws_bytes, cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {}) {
   if (!mask) return fail(SPARGE_ERR_INVALID_ARG, "mask is NULL");
-  if (q.N > 131072) return fail(SPARGE_ERR_UNSUPPORTED, "mask prediction supports N <= 131072 (got %lld)", (long long)q.N);
+  int rc;
+  if ((rc = check_lengths(q, k, causal))) return rc;
+  if (k.N > 131072) return fail(SPARGE_ERR_UNSUPPORTED, "mask prediction supports Nk <= 131072 (got %lld)", (long long)k.N);
   if (q.B * q.H * cdiv(q.N, QBLK) > 0x7fffffffLL)
     return fail(SPARGE_ERR_UNSUPPORTED, "mask prediction supports at most 2^31 - 1 mask rows");
-  const size_t need = predict_ws_bytes(q.B, q.H, k.H, q.N, q.d);
+  const size_t need = predict_ws_bytes(q.B, q.H, k.H, q.N, k.N, q.d);
   if (need && (!ws || ws_bytes < need))
     return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   if (q.B == 0 || q.N == 0) return SPARGE_OK;
-  PredictWs pw = predict_ws_carve(ws, q.B, q.H, k.H, q.N, q.d);
-  int rc;
+  PredictWs pw = predict_ws_carve(ws, q.B, q.H, k.H, q.N, k.N, q.d);
   if ((rc = record_event(ev, 0, s))) return rc;
   cudaError_t e = launch_pool_sim(q, k, pw, s);
   if (e != cudaSuccess) return cuda_fail(e, "pool_sim launch");
@@ -232,21 +245,22 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
   {
     ScoreGemmLaunch g;
     memset(&g, 0, sizeof(g));
-    const int64_t nqb = cdiv(q.N, QBLK), nkb = cdiv(q.N, KBLK);
+    const int64_t nqb = cdiv(q.N, QBLK), nkb = cdiv(k.N, KBLK);
     if ((rc = make_map3(&g.qhi, pw.qhi, q.d, nqb, q.B * q.H, "qhi")) || (rc = make_map3(&g.qlo, pw.qlo, q.d, nqb, q.B * q.H, "qlo")) ||
         (rc = make_map3(&g.khi, pw.khi, q.d, nkb, q.B * k.H, "khi")) || (rc = make_map3(&g.klo, pw.klo, q.d, nkb, q.B * k.H, "klo")) ||
         (rc = make_map_s(&g.ts, pw.S, pw.nkb_pad, nqb, q.B * q.H)))
       return rc;
     g.Smax = pw.Smax;
     g.nkb_pad = pw.nkb_pad;
-    g.B = (int)q.B; g.Hq = (int)q.H; g.Hkv = (int)k.H; g.N = (int)q.N; g.d = (int)q.d; g.causal = causal;
+    g.B = (int)q.B; g.Hq = (int)q.H; g.Hkv = (int)k.H; g.Nq = (int)q.N; g.Nk = (int)k.N; g.d = (int)q.d;
+    g.causal = causal;
     g.scale = scale;
     g.status = status_ptr();
     e = launch_score_gemm(g, s);
     if (e != cudaSuccess) return cuda_fail(e, "score_gemm launch");
     if ((rc = record_event(ev, 2, s))) return rc;
   }
-  e = launch_score_select(pw, (int)q.B, (int)q.H, (int)k.H, (int)q.N, (int)q.d, topk, theta, causal, mask, hp.topk,
+  e = launch_score_select(pw, (int)q.B, (int)q.H, (int)k.H, (int)q.N, (int)k.N, (int)q.d, topk, theta, causal, mask, hp.topk,
                           hp.theta, status_ptr(), hp.topk_mode == SPARGE_TOPK_COUNT ? 1 : 0, s);
   if (e != cudaSuccess) return cuda_fail(e, "score_select launch");
   return record_event(ev, 3, s);
@@ -257,9 +271,9 @@ size_t v16_bytes(int64_t B, int64_t Hkv, int64_t N, int64_t d) { return align256
 // Attention workspace for a precision: the f16 copy of V, or the 8-bit copies and scales.
 bool is_q8(int precision) { return precision == SPARGE_PRECISION_Q8 || precision == SPARGE_PRECISION_Q8_FP8PV; }
 
-size_t attn_ws_bytes(int precision, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
-  if (is_q8(precision)) return d == 128 ? q8_ws_bytes(B, Hq, Hkv, N, d) : 0;
-  return v16_bytes(B, Hkv, N, d);
+size_t attn_ws_bytes(int precision, int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d) {
+  if (is_q8(precision)) return d == 128 ? q8_ws_bytes(B, Hq, Hkv, Nq, Nk, d) : 0;
+  return v16_bytes(B, Hkv, Nk, d);
 }
 
 int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, float lambda, int causal, float scale,
@@ -269,13 +283,14 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
     return fail(SPARGE_ERR_UNSUPPORTED, "precision %d not supported", precision);
   const bool q8 = is_q8(precision), pv8 = precision == SPARGE_PRECISION_Q8_FP8PV;
   if (q8 && q.d != 128) return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path needs d = 128 (got %lld)", (long long)q.d);
-  if (q8 && q.N > 65535LL * 64) return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path supports N <= %lld", 65535LL * 64);
+  if (q8 && k.N > 65535LL * 64) return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path supports Nk <= %lld", 65535LL * 64);
   View ov;
   int rc = check_tensor(o, "o", &ov);
   if (rc) return rc;
-  if (v.B != q.B || v.N != q.N || v.d != q.d || v.H != k.H) return fail(SPARGE_ERR_INVALID_ARG, "v disagrees with q/k");
+  if ((rc = check_lengths(q, k, causal))) return rc;
+  if (v.B != q.B || v.N != k.N || v.d != q.d || v.H != k.H) return fail(SPARGE_ERR_INVALID_ARG, "v disagrees with q/k");
   if (ov.B != q.B || ov.N != q.N || ov.d != q.d || ov.H != q.H) return fail(SPARGE_ERR_INVALID_ARG, "o disagrees with q");
-  const size_t need = attn_ws_bytes(precision, q.B, q.H, k.H, q.N, q.d);
+  const size_t need = attn_ws_bytes(precision, q.B, q.H, k.H, q.N, k.N, q.d);
   if (ws_bytes < need || (need && !ws))
     return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(SPARGE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
@@ -283,14 +298,14 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   AttnLaunch l;
   memset(&l, 0, sizeof(l));
   if (q8) {
-    const Q8Ws w = q8_ws_carve(ws, q.B, q.H, k.H, q.N, q.d);
+    const Q8Ws w = q8_ws_carve(ws, q.B, q.H, k.H, q.N, k.N, q.d);
     cudaError_t e = launch_q8_prep(q, k, v, w, pv8, perm, status_ptr(), s);
     if (e != cudaSuccess) return cuda_fail(e, "8-bit quantisation launch");
     if (!pv8 && (e = launch_convert_v_f16(v, w.v8, perm, status_ptr(), s)) != cudaSuccess)
       return cuda_fail(e, "convert_v launch");
     if ((rc = record_event(ev, 4, s))) return rc;
-    const int64_t d = q.d, N = q.N, npad = cdiv(N, 64) * 64;
-    const int64_t qd[4] = {d, N, q.H, q.B}, qs[3] = {d, N * d, q.H * N * d};
+    const int64_t d = q.d, Nq = q.N, N = k.N, npad = cdiv(N, 64) * 64;
+    const int64_t qd[4] = {d, Nq, q.H, q.B}, qs[3] = {d, Nq * d, q.H * Nq * d};
     const int64_t kd[4] = {d, N, k.H, k.B}, ks[3] = {d, N * d, k.H * N * d};
     const int64_t vd[4] = {npad, d, k.H, k.B}, vs[3] = {npad, d * npad, k.H * d * npad};
     if ((rc = make_map_u8(&l.tq, w.q8, qd, qs, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, "q8")) ||
@@ -317,7 +332,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   l.mask = mask;
   l.o = o->data;
   l.o_sb = ov.sb; l.o_sh = ov.sh; l.o_sn = ov.sn;
-  l.B = (int)q.B; l.Hq = (int)q.H; l.Hkv = (int)k.H; l.N = (int)q.N; l.d = (int)q.d;
+  l.B = (int)q.B; l.Hq = (int)q.H; l.Hkv = (int)k.H; l.Nq = (int)q.N; l.Nk = (int)k.N; l.d = (int)q.d;
   l.causal = causal ? 1 : 0;
   l.scale = scale;
   l.lambda = lambda;
@@ -349,8 +364,8 @@ int run_predict(const View &q, const View &k, float topk, float theta, int causa
 
 int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
 
-size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
-  const int64_t nqb = cdiv(N, QBLK), nkb = cdiv(N, KBLK), nkb_pad = cdiv(nkb, 4) * 4;
+size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d) {
+  const int64_t nqb = cdiv(Nq, QBLK), nkb = cdiv(Nk, KBLK), nkb_pad = cdiv(nkb, 4) * 4;
   size_t s = 0;
   s += align256(sizeof(float) * B * Hq * nqb * d);      // muQ
   s += align256(sizeof(float) * B * Hq * nqb);          // sQ
@@ -363,8 +378,8 @@ size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d
   return s;
 }
 
-PredictWs predict_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
-  const int64_t nqb = cdiv(N, QBLK), nkb = cdiv(N, KBLK), nkb_pad = cdiv(nkb, 4) * 4;
+PredictWs predict_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d) {
+  const int64_t nqb = cdiv(Nq, QBLK), nkb = cdiv(Nk, KBLK), nkb_pad = cdiv(nkb, 4) * 4;
   char *p = static_cast<char *>(ws);
   PredictWs w;
   auto take = [&](size_t bytes) {
@@ -398,18 +413,18 @@ size_t sparge_workspace_bytes(int op, int64_t B, int64_t Hq, int64_t Hkv, int64_
   }
   switch (op) {
     case SPARGE_OP_PREDICT_MASK:
-      return predict_ws_bytes(B, Hq, Hkv, N, d);
+      return predict_ws_bytes(B, Hq, Hkv, N, N, d);
     case SPARGE_OP_BLOCK_SPARSE_ATTN:
       return v16_bytes(B, Hkv, N, d);
     case SPARGE_OP_ATTN:
-      return predict_ws_bytes(B, Hq, Hkv, N, d) + align256((size_t)B * Hq * cdiv(N, QBLK) * cdiv(N, KBLK)) +
+      return predict_ws_bytes(B, Hq, Hkv, N, N, d) + align256((size_t)B * Hq * cdiv(N, QBLK) * cdiv(N, KBLK)) +
              v16_bytes(B, Hkv, N, d);
     case SPARGE_OP_BLOCK_SPARSE_ATTN_Q8:
-      return attn_ws_bytes(SPARGE_PRECISION_Q8, B, Hq, Hkv, N, d);
+      return attn_ws_bytes(SPARGE_PRECISION_Q8, B, Hq, Hkv, N, N, d);
     case SPARGE_OP_ATTN_Q8:
       if (d != 128) return 0;
-      return predict_ws_bytes(B, Hq, Hkv, N, d) + align256((size_t)B * Hq * cdiv(N, QBLK) * cdiv(N, KBLK)) +
-             attn_ws_bytes(SPARGE_PRECISION_Q8, B, Hq, Hkv, N, d);
+      return predict_ws_bytes(B, Hq, Hkv, N, N, d) + align256((size_t)B * Hq * cdiv(N, QBLK) * cdiv(N, KBLK)) +
+             attn_ws_bytes(SPARGE_PRECISION_Q8, B, Hq, Hkv, N, N, d);
     default:
       return 0;
   }
@@ -447,7 +462,8 @@ int sparge_predict_mask_ex(const sparge_tensor *q, const sparge_tensor *k, float
   hp.topk_mode = p->topk_mode;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (p->token_order) {
-    const size_t need = order_bytes(qv.B, qv.H, kv.H, qv.N, qv.d) + predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, qv.d);
+    if (qv.N != kv.N) return fail(SPARGE_ERR_UNSUPPORTED, "a token order needs Nq = Nk");
+    const size_t need = order_bytes(qv.B, qv.H, kv.H, qv.N, qv.d) + predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, kv.N, qv.d);
     if (!mask) return fail(SPARGE_ERR_INVALID_ARG, "mask is NULL");
     if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
     if (qv.B * qv.N > 0 && (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s))) return rc;
@@ -485,7 +501,9 @@ int sparge_block_sparse_attn_ex(const sparge_tensor *q, const sparge_tensor *k, 
   const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)qv.d);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (p->token_order) {
-    const size_t need = order_bytes(qv.B, qv.H, kv.H, qv.N, qv.d) + attn_ws_bytes(p->precision, qv.B, qv.H, kv.H, qv.N, qv.d);
+    if (qv.N != kv.N) return fail(SPARGE_ERR_UNSUPPORTED, "a token order needs Nq = Nk");
+    const size_t need =
+        order_bytes(qv.B, qv.H, kv.H, qv.N, qv.d) + attn_ws_bytes(p->precision, qv.B, qv.H, kv.H, qv.N, kv.N, qv.d);
     if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   }
   if ((rc = record_event(p->timing_events, 0, s))) return rc;
@@ -510,11 +528,12 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   if (std::isnan(p->scale) || p->scale < 0.f || std::isinf(p->scale))
     return fail(SPARGE_ERR_INVALID_ARG, "scale must be finite and >= 0");
   const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)qv.d);
-  const size_t need_pred = predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, qv.d);
-  const size_t mask_bytes = mask_out ? 0 : align256((size_t)qv.B * qv.H * cdiv(qv.N, QBLK) * cdiv(qv.N, KBLK));
+  if (p->token_order && qv.N != kv.N) return fail(SPARGE_ERR_UNSUPPORTED, "a token order needs Nq = Nk");
+  const size_t need_pred = predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, kv.N, qv.d);
+  const size_t mask_bytes = mask_out ? 0 : align256((size_t)qv.B * qv.H * cdiv(qv.N, QBLK) * cdiv(kv.N, KBLK));
   if (is_q8(p->precision) && qv.d != 128)
     return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path needs d = 128 (got %lld)", (long long)qv.d);
-  const size_t need_v = attn_ws_bytes(p->precision, qv.B, qv.H, kv.H, qv.N, qv.d);
+  const size_t need_v = attn_ws_bytes(p->precision, qv.B, qv.H, kv.H, qv.N, kv.N, qv.d);
   const size_t need_order = p->token_order ? order_bytes(qv.B, qv.H, kv.H, qv.N, qv.d) : 0;
   const size_t need = need_order + need_pred + mask_bytes + need_v;
   if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);

@@ -44,7 +44,7 @@ struct AttnArgs {
   const uint8_t *mask;
   __nv_bfloat16 *o;
   int64_t o_sb, o_sh, o_sn;
-  int B, Hq, Hkv, G, N, nqb, nkb, causal;
+  int B, Hq, Hkv, G, Nq, Nk, nqb, nkb, causal, off;  // query and key lengths; off = Nk - Nq
   float scale_log2, lam_log2;
   const float *lam_h;  // lambda per query head (natural-log units), or nullptr
   const int32_t *perm; // token order or nullptr: output row t is token perm[t] of o
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   const int b = bk / a.Hkv, kvh = bk % a.Hkv;
   const int i = a.nqb - 1 - rem / a.G;
   const int h = kvh * a.G + rem % a.G;
-  const int n_valid = a.causal ? min(a.nkb, 2 * i + 2) : a.nkb;
+  const int n_valid = a.causal ? min(a.nkb, causal_key_blocks(i, a.off)) : a.nkb;
   const uint8_t *mrow = a.mask ? a.mask + ((static_cast<int64_t>(b) * a.Hq + h) * a.nqb + i) * a.nkb : nullptr;
 
   constexpr int SCOL0 = (D == 128) ? 128 : 64;
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     // ------------------------------------ softmax warps ------------------------------------
     const int r = warp * 32 + lane;
     const int row_g = QBLK * i + r;
-    const bool row_ok = row_g < a.N;
+    const bool row_ok = row_g < a.Nq;
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
     int nskip = 0, T = 0;
@@ -409,13 +409,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         }
         mhw = fmaxf(m0, m1);
       }
-      const bool edge = (a.causal && KBLK * j + KBLK - 1 > QBLK * i) || (KBLK * j + KBLK > a.N);
+      const bool edge = (a.causal && KBLK * j + KBLK - 1 > a.off + QBLK * i) || (KBLK * j + KBLK > a.Nk);
       if (!row_ok) {
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = -INFINITY;
       } else if (edge) {
-        const int lim_causal = a.causal ? row_g - KBLK * j : 1 << 30;  // cols c > lim are hidden
-        const int lim = min(lim_causal, a.N - 1 - KBLK * j);
+        const int lim_causal = a.causal ? a.off + row_g - KBLK * j : 1 << 30;  // cols c > lim are hidden
+        const int lim = min(lim_causal, a.Nk - 1 - KBLK * j);
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
       }
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
       tmem_st_wait();
       if (lane == 0) cs.skip[buf][warp] = wskip ? 1 : 0;
-      nskip += (wskip && QBLK * i + warp * 32 < a.N) ? 1 : 0;
+      nskip += (wskip && QBLK * i + warp * 32 < a.Nq) ? 1 : 0;
       tc_fence_before();
       mbar_arrive(&cs.p_full[buf]);
     }
@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     bool write_row = row_ok;
     if (a.perm && row_ok) {
       orow_t = __ldg(a.perm + row_g);
-      if (static_cast<unsigned>(orow_t) >= static_cast<unsigned>(a.N)) {
+      if (static_cast<unsigned>(orow_t) >= static_cast<unsigned>(a.Nq)) {
         record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
         write_row = false;
         orow_t = 0;
@@ -590,9 +590,12 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
   a.mask = l.mask;
   a.o = static_cast<__nv_bfloat16 *>(l.o);
   a.o_sb = l.o_sb; a.o_sh = l.o_sh; a.o_sn = l.o_sn;
-  a.B = l.B; a.Hq = l.Hq; a.Hkv = l.Hkv; a.G = l.Hq / l.Hkv; a.N = l.N;
-  a.nqb = (l.N + QBLK - 1) / QBLK;
-  a.nkb = (l.N + KBLK - 1) / KBLK;
+  a.B = l.B; a.Hq = l.Hq; a.Hkv = l.Hkv; a.G = l.Hq / l.Hkv;
+  a.Nq = l.Nq;
+  a.Nk = l.Nk;
+  a.off = l.Nk - l.Nq;
+  a.nqb = (l.Nq + QBLK - 1) / QBLK;
+  a.nkb = (l.Nk + KBLK - 1) / KBLK;
   a.causal = l.causal;
   const float LOG2E = 1.4426950408889634f;
   a.scale_log2 = l.scale * LOG2E;

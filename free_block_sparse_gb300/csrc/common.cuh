@@ -13,6 +13,13 @@ namespace sparge {
 constexpr int QBLK = 128;  // query tokens per mask block
 constexpr int KBLK = 64;   // key tokens per mask block
 
+// Causal attention lets query row r see key column c <= off + r, where off = Nk - Nq >= 0 puts
+// the last query on the last key (off = 0 when the lengths agree).  Query block i then has a
+// visible element in key blocks 0 .. causal_key_blocks(i, off) - 1 (before clamping to nkb).
+__host__ __device__ __forceinline__ int causal_key_blocks(int i, int off) {
+  return (off + QBLK * i + QBLK - 1) / KBLK + 1;
+}
+
 // Device status word (one int in device memory owned by the library's host layer): 0, or a
 // negative sparge_status recorded by a kernel whose bounded wait ran out.
 __device__ __forceinline__ void record_status(int *status, int code) {

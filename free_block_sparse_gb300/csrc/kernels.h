@@ -28,8 +28,9 @@ struct PredictWs {
   int64_t nkb_pad;
 };
 
-size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
-PredictWs predict_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
+// Nq: query length, Nk: key length
+size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d);
+PredictWs predict_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d);
 
 }  // namespace sparge
 struct sparge_tensor;
@@ -51,7 +52,7 @@ struct ScoreGemmLaunch {
   CUtensorMap ts;  // 3-D map over S (nkb_pad, nqb, B*Hq) fp32, box 32 x 128, 128-byte swizzle
   float *Smax;     // [B][Hq][nqb] row maxima over the valid key blocks
   int64_t nkb_pad;
-  int B, Hq, Hkv, N, d, causal;
+  int B, Hq, Hkv, Nq, Nk, d, causal;  // query and key lengths (causal: Nq <= Nk, the last query on the last key)
   float scale;
   int *status;
 };
@@ -60,7 +61,7 @@ cudaError_t launch_score_gemm(const ScoreGemmLaunch &l, cudaStream_t st);
 // Row softmax, cumulative top-k and the always-keep rule on S: writes the uint8 mask.  topk_h and
 // theta_h (device, Hq floats, or nullptr) override topk and theta per query head; a bad entry is
 // recorded in *status and its head keeps every valid block.
-cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int N, int d, float topk,
+cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int Nq, int Nk, int d, float topk,
                                 float theta, int causal, uint8_t *mask, const float *topk_h, const float *theta_h,
                                 int *status, int count_mode, cudaStream_t st);
 
@@ -70,7 +71,7 @@ struct AttnLaunch {
   const uint8_t *mask;     // (B, Hq, nqb, nkb) or nullptr
   void *o;
   int64_t o_sb, o_sh, o_sn;
-  int B, Hq, Hkv, N, d;
+  int B, Hq, Hkv, Nq, Nk, d;  // query and key lengths (causal: Nq <= Nk, the last query on the last key)
   int causal;
   float scale;
   float lambda;
@@ -100,8 +101,9 @@ struct Q8Ws {
   float *sv;        // [B][Hkv][d]    per channel
   float *partial;   // [B*Hkv][chunks][2][d]
 };
-size_t q8_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
-Q8Ws q8_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
+// Nq: query length, N: key / value length
+size_t q8_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t N, int64_t d);
+Q8Ws q8_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t N, int64_t d);
 // K mean, V channel scales, e4m3 Q and K - mean with their block scales; with quant_v also the
 // channel-major e4m3 V (otherwise v8 is left to the caller), whose key t is token perm[t] of v
 // when perm is given (Q and K are used in the order they come in).

@@ -31,7 +31,7 @@ extern "C" int sparge_predict_mask_noalloc(const sparge_tensor *q, const sparge_
   sparge::View qv, kv;
   int rc = sparge::validate_predict_args(q, k, topk, theta, &qv, &kv);
   if (rc) return rc;
-  const size_t need = sparge::predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, qv.d);
+  const size_t need = sparge::predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, kv.N, qv.d);
   if (need > kScratchBytes) {
     char msg[200];
     snprintf(msg, sizeof(msg), "shape needs %zu bytes of scratch; the allocation-free call holds %zu", need,

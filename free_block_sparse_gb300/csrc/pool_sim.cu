@@ -17,7 +17,7 @@ namespace {
 struct PoolArgs {
   const __nv_bfloat16 *q, *k;
   int64_t q_sb, q_sh, q_sn, k_sb, k_sh, k_sn;
-  int B, Hq, Hkv, N, nqb, nkb;
+  int B, Hq, Hkv, Nq, Nk, nqb, nkb;  // query and key lengths may differ
   int64_t nq_total, total;
   PredictWs ws;
 };
@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(128, 5) pool_sim_kernel(PoolArgs a) {
       base = a.k + b * a.k_sb + h * a.k_sh + static_cast<int64_t>(idx) * KBLK * sn;
       row = (static_cast<int64_t>(b) * a.Hkv + h) * a.nkb + idx;
     }
-    n = min(rows, a.N - idx * rows);
+    n = min(rows, (isQ ? a.Nq : a.Nk) - idx * rows);
     const int steps = rows / TPW;  // warp-wide loads covering the block (a multiple of INFLIGHT)
     const __nv_bfloat16 *p = base + sub * sn + part * 8;
     auto load = [&](int s) {
@@ -152,9 +152,10 @@ cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, c
   a.q_sb = q.sb; a.q_sh = q.sh; a.q_sn = q.sn;
   a.k_sb = k.sb; a.k_sh = k.sh; a.k_sn = k.sn;
   a.B = static_cast<int>(q.B); a.Hq = static_cast<int>(q.H); a.Hkv = static_cast<int>(k.H);
-  a.N = static_cast<int>(q.N);
-  a.nqb = (a.N + QBLK - 1) / QBLK;
-  a.nkb = (a.N + KBLK - 1) / KBLK;
+  a.Nq = static_cast<int>(q.N);
+  a.Nk = static_cast<int>(k.N);
+  a.nqb = (a.Nq + QBLK - 1) / QBLK;
+  a.nkb = (a.Nk + KBLK - 1) / KBLK;
   a.nq_total = static_cast<int64_t>(a.B) * a.Hq * a.nqb;
   a.total = a.nq_total + static_cast<int64_t>(a.B) * a.Hkv * a.nkb;
   a.ws = ws;

@@ -235,7 +235,7 @@ template <int D>
 cudaError_t run(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v, const int32_t *perm,
                 int *status, cudaStream_t st) {
   const int B = static_cast<int>(q.B), Hq = static_cast<int>(q.H), Hkv = static_cast<int>(k.H);
-  const int N = static_cast<int>(q.N);
+  const int Nq = static_cast<int>(q.N), N = static_cast<int>(k.N);  // N: keys and values
   const int nchunks = (N + CHUNK - 1) / CHUNK;
   const dim3 pgrid(B * Hkv, nchunks);
   const __nv_bfloat16 *kp = static_cast<const __nv_bfloat16 *>(k.data), *vp = static_cast<const __nv_bfloat16 *>(v.data);
@@ -244,10 +244,10 @@ cudaError_t run(const View &q, const View &k, const View &v, const Q8Ws &w, bool
   else
     kv_partials_kernel<D, false><<<pgrid, 256, 0, st>>>(kp, k.sb, k.sh, k.sn, vp, v.sb, v.sh, v.sn, Hkv, N, w.partial);
   kv_finish_kernel<D><<<B * Hkv, D, 0, st>>>(w.partial, nchunks, N, quant_v ? 1 : 0, w.kmean, w.sv);
-  const int nqb = (N + QBLK - 1) / QBLK, nkb = (N + KBLK - 1) / KBLK;
+  const int nqb = (Nq + QBLK - 1) / QBLK, nkb = (N + KBLK - 1) / KBLK;
   const int64_t nq = static_cast<int64_t>(B) * Hq * nqb, nk = static_cast<int64_t>(B) * Hkv * nkb;
   quant_block_kernel<D, QBLK><<<static_cast<unsigned>(nq), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16 *>(q.data), q.sb, q.sh, q.sn, Hq, N, nqb, nullptr, w.q8, w.sq);
+      static_cast<const __nv_bfloat16 *>(q.data), q.sb, q.sh, q.sn, Hq, Nq, nqb, nullptr, w.q8, w.sq);
   quant_block_kernel<D, KBLK><<<static_cast<unsigned>(nk), 256, 0, st>>>(kp, k.sb, k.sh, k.sn, Hkv, N, nkb, w.kmean,
                                                                           w.k8, w.sk);
   const int npad = (N + 63) / 64 * 64;
@@ -259,22 +259,22 @@ cudaError_t run(const View &q, const View &k, const View &v, const Q8Ws &w, bool
 
 }  // namespace
 
-size_t q8_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
+size_t q8_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t N, int64_t d) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const int64_t nqb = (N + QBLK - 1) / QBLK, nkb = (N + KBLK - 1) / KBLK, nch = (N + CHUNK - 1) / CHUNK;
+  const int64_t nqb = (Nq + QBLK - 1) / QBLK, nkb = (N + KBLK - 1) / KBLK, nch = (N + CHUNK - 1) / CHUNK;
   const int64_t npad = (N + 63) / 64 * 64;
   const int64_t vbytes = std::max(B * Hkv * d * npad, 2 * B * Hkv * N * d);  // e4m3 V^T or the f16 copy
-  return al(B * Hq * N * d) + al(B * Hkv * N * d) + al(vbytes) + al(4 * B * Hq * nqb) + al(4 * B * Hkv * nkb) +
+  return al(B * Hq * Nq * d) + al(B * Hkv * N * d) + al(vbytes) + al(4 * B * Hq * nqb) + al(4 * B * Hkv * nkb) +
          2 * al(4 * B * Hkv * d) + al(4 * B * Hkv * nch * 2 * d);
 }
 
-Q8Ws q8_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
+Q8Ws q8_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t N, int64_t d) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const int64_t nqb = (N + QBLK - 1) / QBLK, nkb = (N + KBLK - 1) / KBLK;
+  const int64_t nqb = (Nq + QBLK - 1) / QBLK, nkb = (N + KBLK - 1) / KBLK;
   const int64_t npad = (N + 63) / 64 * 64;
   char *p = static_cast<char *>(ws);
   Q8Ws w;
-  w.q8 = reinterpret_cast<uint8_t *>(p); p += al(B * Hq * N * d);
+  w.q8 = reinterpret_cast<uint8_t *>(p); p += al(B * Hq * Nq * d);
   w.k8 = reinterpret_cast<uint8_t *>(p); p += al(B * Hkv * N * d);
   w.v8 = reinterpret_cast<uint8_t *>(p); p += al(std::max(B * Hkv * d * npad, 2 * B * Hkv * N * d));
   w.sq = reinterpret_cast<float *>(p); p += al(4 * B * Hq * nqb);

@@ -23,7 +23,7 @@ constexpr int GCOLS = 128;  // key blocks per chunk (MMA N)
 struct GemmArgs {
   float *Smax;
   int64_t nkb_pad;
-  int B, Hq, Hkv, G, nqb, nkb, causal, ngroups;
+  int B, Hq, Hkv, G, nqb, nkb, causal, off, ngroups;  // off = Nk - Nq (causal alignment)
   float scale;
   int *status;
 };
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(192, 1)
   const int bh = blockIdx.x, b = bh / a.Hq, h = bh % a.Hq, kvh = h / a.G;
   const int i0 = group * GROWS;
   const int ilast = min(i0 + GROWS - 1, a.nqb - 1);
-  const int ncols = a.causal ? min(a.nkb, 2 * ilast + 2) : a.nkb;
+  const int ncols = a.causal ? min(a.nkb, causal_key_blocks(ilast, a.off)) : a.nkb;
   const int nch = (ncols + GCOLS - 1) / GCOLS;
   constexpr uint32_t IDESC = idesc_f32acc(128, GCOLS, FMT_BF16, false);
 
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     const int r = warp * 32 + lane;
     const int i = i0 + r;
-    const int nv = (i < a.nqb) ? (a.causal ? min(a.nkb, 2 * i + 2) : a.nkb) : 0;  // valid key blocks
+    const int nv = (i < a.nqb) ? (a.causal ? min(a.nkb, causal_key_blocks(i, a.off)) : a.nkb) : 0;  // valid key blocks
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float rmax = -3.402823466e38f;
     for (int ch = 0; ch < nch; ++ch) {
@@ -232,9 +232,10 @@ cudaError_t launch_score_gemm(const ScoreGemmLaunch &l, cudaStream_t st) {
   a.Smax = l.Smax;
   a.nkb_pad = l.nkb_pad;
   a.B = l.B; a.Hq = l.Hq; a.Hkv = l.Hkv; a.G = l.Hq / l.Hkv;
-  a.nqb = (l.N + QBLK - 1) / QBLK;
-  a.nkb = (l.N + KBLK - 1) / KBLK;
+  a.nqb = (l.Nq + QBLK - 1) / QBLK;
+  a.nkb = (l.Nk + KBLK - 1) / KBLK;
   a.causal = l.causal;
+  a.off = l.Nk - l.Nq;
   a.ngroups = (a.nqb + GROWS - 1) / GROWS;
   a.scale = l.scale;
   a.status = l.status;

@@ -36,7 +36,7 @@ struct SelArgs {
   const float *sQ, *sK;
   uint8_t *mask;
   int64_t nkb_pad, rows;
-  int Hq, Hkv, G, nqb, nkb, causal;
+  int Hq, Hkv, G, nqb, nkb, causal, off;  // off = Nk - Nq (causal alignment)
   float topk, theta;
   const float *topk_h, *theta_h;  // per query head, or nullptr
   int *status;
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
   const uint32_t b = bh / static_cast<uint32_t>(a.Hq);
   const int h = static_cast<int>(bh - b * static_cast<uint32_t>(a.Hq));
   const int kvh = h / a.G;
-  const int nvalid = a.causal ? min(a.nkb, 2 * i + 2) : a.nkb;
+  const int nvalid = a.causal ? min(a.nkb, causal_key_blocks(i, a.off)) : a.nkb;
   const int nit = (nvalid + 127) >> 7;
   const float *srow = a.S + static_cast<int64_t>(row) * a.nkb_pad;
   const float *sKrow = a.sK + (static_cast<int64_t>(b) * a.Hkv + kvh) * a.nkb_pad;
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
 
 }  // namespace
 
-cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int N, int d, float topk,
+cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int Nq, int Nk, int d, float topk,
                                 float theta, int causal, uint8_t *mask, const float *topk_h, const float *theta_h,
                                 int *status, int count_mode, cudaStream_t st) {
   (void)d;
@@ -447,9 +447,10 @@ cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int
   a.mask = mask;
   a.nkb_pad = ws.nkb_pad;
   a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv;
-  a.nqb = (N + QBLK - 1) / QBLK;
-  a.nkb = (N + KBLK - 1) / KBLK;
+  a.nqb = (Nq + QBLK - 1) / QBLK;
+  a.nkb = (Nk + KBLK - 1) / KBLK;
   a.causal = causal;
+  a.off = Nk - Nq;
   a.rows = static_cast<int64_t>(B) * Hq * a.nqb;
   a.topk = topk;
   a.theta = theta;

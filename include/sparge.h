@@ -16,7 +16,13 @@
  *     multiples of 8 (16 bytes); data must be 16-byte aligned.  d is 64 or 128.
  *   - K and V may have fewer heads than Q (grouped-query attention): Hq % Hkv == 0 and query
  *     head h reads key/value head h / (Hq / Hkv).
- *   - The block mask is uint8, contiguous, shape (B, Hq, ceil(N/128), ceil(N/64)); 1 keeps
+ *   - Q may have a different length Nq from K and V (Nk): a chunk of queries continuing a longer
+ *     key sequence (prefill in chunks, decoding).  With the causal mask Nq <= Nk and the last
+ *     query sits on the last key: query row r sees key c when c <= (Nk - Nq) + r (Nq = Nk is
+ *     the usual square case).  Without it any Nq and Nk > 0.  Blocks and masks then have
+ *     ceil(Nq/128) query rows and ceil(Nk/64) key columns, and sparge_workspace_bytes is
+ *     called with N = max(Nq, Nk).  A token order (sparge_params.token_order) needs Nq = Nk.
+ *   - The block mask is uint8, contiguous, shape (B, Hq, ceil(Nq/128), ceil(Nk/64)); 1 keeps
  *     the 128x64 tile, 0 drops it (SpargeAttention Chinese README, custom block-sparse mask).
  *   - Every pointer except the *_host ones is a device pointer.  The caller owns every buffer
  *     (inputs, outputs, mask, workspace); the library allocates no device memory.  All work

@@ -200,6 +200,19 @@ def test_block_sparse_ex_rejects_bad_parameters(lib, case):
     assert rc == code, lib.sparge_last_error()
 
 
+def test_short_query_checks(lib):
+    """Causal attention needs Nq <= Nk; a token order needs Nq = Nk (checked before any CUDA call)."""
+    q, k = _t(N=512), _t(N=256)
+    rc = lib.sparge_predict_mask(ctypes.byref(q), ctypes.byref(k), 0.5, 0.5, 1, ctypes.c_void_p(0x2000), None, 0, None)
+    assert rc == fbs.SPARGE_ERR_INVALID_ARG and b"Nq <= Nk" in lib.sparge_last_error()
+    p = fbs.sparge_params(0.5, -math.inf, 0.0, fbs.SPARGE_PRECISION_BF16, 0, None)
+    p.token_order = 0x3000
+    q2 = _t(N=128)
+    rc = lib.sparge_attn_ex(ctypes.byref(q2), ctypes.byref(k), ctypes.byref(k), 0.5, 1, ctypes.byref(p),
+                            ctypes.byref(q2), None, None, 0, None)
+    assert rc == fbs.SPARGE_ERR_UNSUPPORTED and b"token order" in lib.sparge_last_error()
+
+
 def test_attention_rejects_mismatched_output(lib):
     q, o = _t(), _t(H=4)
     rc = lib.sparge_block_sparse_attn(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), None, -math.inf, 0, 0,
