@@ -218,29 +218,59 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
     }
     hist_zero(H, lane);
   }
-  // first pass: Z (mass reading) and the first histogram level
+  // the mask row: 4 key blocks per lane, 32-bit stores when the rows are 4-byte aligned
+  uint8_t *mrow = a.mask + static_cast<int64_t>(row) * a.nkb;
+  const bool words = (a.nkb & 3) == 0 && (reinterpret_cast<uintptr_t>(a.mask) & 3u) == 0;
+  auto put_word = [&](int j0, uint32_t word) {
+    if (j0 >= a.nkb) return;
+    if (words) {
+      *reinterpret_cast<uint32_t *>(mrow + j0) = word;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (j0 + u < a.nkb) mrow[j0 + u] = static_cast<uint8_t>(word >> (8 * u));
+    }
+  };
+  // first pass (rows not kept whole): Z (mass reading) and the first histogram level
   float2 z2 = make_float2(0.f, 0.f);
-  const uint32_t lim1 = hist_lim(st);
-  for (int t = 0; t < nit; ++t) {
-    const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm, none);
-    if (!cnt) z2 = fadd2(z2, fadd2(make_float2(v.x, v.y), make_float2(v.z, v.w)));
-    if (!keep_all) hist_add4(H, lane, v, st, lim1, cnt);
+  if (!keep_all) {
+    const uint32_t lim1 = hist_lim(st);
+    for (int t = 0; t < nit; ++t) {
+      const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm, none);
+      if (!cnt) z2 = fadd2(z2, fadd2(make_float2(v.x, v.y), make_float2(v.z, v.w)));
+      hist_add4(H, lane, v, st, lim1, cnt);
+    }
   }
   const float Z = warp_sum(z2.x + z2.y);
 
   // the cut: keep e > et, or e == et with index <= jt
   float et = 2.f;
   int jt = -1;
+  bool mask_done = false;  // the row was written by the last compaction pass and patched
   if (!keep_all) {
     const float target = cnt ? static_cast<float>(kc) : topk * Z;
     bool ok = hist_pick(H, lane, target, st);
     bool listed = false;
-    // compact the crossing bin; while it does not fit the short list, split it over the row
+    // compact the crossing bin; while it does not fit the short list, split it over the row.
+    // Each compaction pass also writes the mask row as far as the range decides it: blocks above
+    // [lo, hi) are kept, blocks below it dropped, blocks inside it kept only by the s_K rule
+    // until the cut among them is known (patched below).
     while (ok) {
       int n = 0;
       for (int t = 0; t < nit; ++t) {
         const int j0 = 128 * t + 4 * lane;
-        n = list_append(load_e(srow, j0, nvalid, negm, none), j0, st, Lv, Lj, n, lane);
+        const float4 v = load_e(srow, j0, nvalid, negm, none);
+        n = list_append(v, j0, st, Lv, Lj, n, lane);
+        uint32_t word = 0u;
+        if (j0 < nvalid) {
+          const float4 sk = __ldg(reinterpret_cast<const float4 *>(sKrow + j0));
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const bool keep = j0 + u < nvalid && (__float_as_uint(comp(v, u)) >= st.hi || comp(sk, u) < theta);
+            word |= (keep ? 1u : 0u) << (8 * u);
+          }
+        }
+        put_word(j0, word);
       }
       st.nc = n;
       if (n <= CMAX) {
@@ -328,6 +358,12 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
           et = __shfl_sync(0xffffffffu, x, kstar);
           jt = __shfl_sync(0xffffffffu, xj, kstar);
           sorted = true;
+          // the listed blocks the cut keeps (the compaction pass left them to the s_K rule)
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < CMAX / 32; ++k)
+            if (cj[k] != 0x7fffffff && (ce[k] > et || (ce[k] == et && cj[k] <= jt))) mrow[cj[k]] = 1;
+          mask_done = true;
         }
       }
     }
@@ -392,16 +428,14 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
     }
   }
 
-  // the mask row: 4 key blocks per lane, 32-bit stores when the rows are 4-byte aligned; the
+  // the mask row where no compaction pass wrote it (rows kept whole, the bisection path); the
   // causally hidden part of the row is zero-filled
-  uint8_t *mrow = a.mask + static_cast<int64_t>(row) * a.nkb;
-  const bool words = (a.nkb & 3) == 0 && (reinterpret_cast<uintptr_t>(a.mask) & 3u) == 0;
-  for (int t = 0; t < nit; ++t) {
+  for (int t = 0; t < nit && !mask_done; ++t) {
     const int j0 = 128 * t + 4 * lane;
     uint32_t word = 0u;
     if (j0 < nvalid) {
-      const float4 v = load_e(srow, j0, nvalid, negm, none);
-      const float4 sk = __ldg(reinterpret_cast<const float4 *>(sKrow + j0));
+      const float4 v = keep_all ? make_float4(0.f, 0.f, 0.f, 0.f) : load_e(srow, j0, nvalid, negm, none);
+      const float4 sk = keep_all ? v : __ldg(reinterpret_cast<const float4 *>(sKrow + j0));
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int j = j0 + u;
@@ -410,14 +444,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
         word |= (keep ? 1u : 0u) << (8 * u);
       }
     }
-    if (j0 >= a.nkb) continue;
-    if (words) {
-      *reinterpret_cast<uint32_t *>(mrow + j0) = word;
-    } else {
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (j0 + u < a.nkb) mrow[j0 + u] = static_cast<uint8_t>(word >> (8 * u));
-    }
+    put_word(j0, word);
   }
   const int nall = (a.nkb + 127) >> 7;
   for (int t = nit; t < nall; ++t) {
