@@ -409,19 +409,18 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         }
         mhw = fmaxf(m0, m1);
       }
-      const bool edge = (a.causal && KBLK * j + KBLK - 1 > a.off + QBLK * i) || (KBLK * j + KBLK > a.Nk);
-      if (!row_ok) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = -INFINITY;
-      } else if (edge) {
-        const int lim_causal = a.causal ? a.off + row_g - KBLK * j : 1 << 30;  // cols c > lim are hidden
-        const int lim = min(lim_causal, a.Nk - 1 - KBLK * j);
+      // a tile with hidden columns (causal diagonal, ragged key tail) or rows past the query length;
+      // the vote makes the branch warp-uniform, so interior tiles skip the masking code entirely
+      const bool edge = (a.causal && KBLK * j + KBLK - 1 > a.off + QBLK * i) || (KBLK * j + KBLK > a.Nk) ||
+                        (QBLK * i + QBLK > a.Nq);
+      float mraw = mhw;
+      if (__any_sync(0xffffffffu, edge)) {
+        int lim = a.causal ? a.off + row_g - KBLK * j : 1 << 30;  // cols c > lim are hidden
+        lim = min(lim, a.Nk - 1 - KBLK * j);
+        if (!row_ok) lim = -1;
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
-      }
-      // a tile with hidden columns needs the maximum of what stays visible
-      float mraw = mhw;
-      if (!row_ok || edge) {
+        // the maximum of what stays visible
         mraw = fmax3(x[0], x[1], x[2]);
 #pragma unroll
         for (int c = 3; c < 63; c += 2) mraw = fmax3(mraw, x[c], x[c + 1]);
@@ -470,37 +469,33 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       // P = 2^(x * scale_log2 - m_ref); a row whose reference is still -inf has only hidden columns
       const float nref = (m_ref == -INFINITY) ? 0.f : POFF - m_ref;
       const float2 sc2 = make_float2(tsc, tsc), nr2 = make_float2(nref, nref);
-      float2 rs2 = make_float2(0.f, 0.f);
-      uint32_t pk[32];
+      float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      uint32_t pk[32];  // P of columns 2c, 2c + 1 (two f16, or two e4m3 in the low half)
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float2 e2 = ffma2(make_float2(x[2 * c], x[2 * c + 1]), sc2, nr2);
         // every EXP_POLY_EVERY-th pair goes to the FMA pipe so the MUFU unit is not the bottleneck
         const float2 p2 = (c % EXP_POLY_EVERY == EXP_POLY_EVERY - 1) ? exp2_poly2(e2)
                                                                       : make_float2(fast_exp2(e2.x), fast_exp2(e2.y));
-        rs2 = fadd2(rs2, p2);
+        rs2[c & 3] = fadd2(rs2[c & 3], p2);  // four independent chains
         pk[c] = PV8 ? pack_e4m3x2(p2.x, p2.y) : pack_f16x2(p2.x, p2.y);
       }
-      l += rs2.x + rs2.y;
+      {
+        const float2 rs = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
+        l += rs.x + rs.y;
+      }
       if constexpr (PV8) {
         uint32_t w[16];  // 4 e4m3 per column, keys in order
 #pragma unroll
         for (int c = 0; c < 16; ++c) w[c] = wskip ? 0u : (pk[2 * c] | (pk[2 * c + 1] << 16));
         tmem_st16(sc, w);
+      } else if (wskip) {
+        uint32_t z[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) z[c] = 0u;
+        tmem_st32(sc, z);
       } else {
-        uint32_t lo[16], hi[16];
-        if (wskip) {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) lo[c] = hi[c] = 0u;
-        } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            lo[c] = pk[c];
-            hi[c] = pk[16 + c];
-          }
-        }
-        tmem_st16(sc, lo);
-        tmem_st16(sc + 16, hi);
+        tmem_st32(sc, pk);
       }
       tmem_st_wait();
       if (lane == 0) cs.skip[buf][warp] = wskip ? 1 : 0;
