@@ -325,7 +325,9 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
     if (e != cudaSuccess) return cuda_fail(e, "convert_v launch");
     if ((rc = record_event(ev, 4, s))) return rc;
     View v16{ws, v.B, v.H, v.N, v.d, v.H * v.N * v.d, v.N * v.d, v.d};
-    if ((rc = make_map(&l.tq, q, 128, "q"))) return rc;
+    if ((rc = make_map(&l.tq, q, 128, "q"))) return rc;  // checks the alignment the row reads rely on
+    l.q = q.data;
+    l.q_sb = q.sb; l.q_sh = q.sh; l.q_sn = q.sn;
     if ((rc = make_map(&l.tk, k, 64, "k"))) return rc;
     if ((rc = make_map(&l.tv, v16, 64, "v", CU_TENSOR_MAP_DATA_TYPE_FLOAT16))) return rc;
   }

@@ -17,7 +17,10 @@
 // the kernel): P lies in [0, 256] and f16 keeps 3 more mantissa bits than bf16, so the P.V
 // rounding error is 8x smaller at the same tensor-core rate.
 // TMEM columns: O at [0, D), score buffers at [128, 192) and [192, 256) (D = 128) or [64, 128)
-// and [128, 192) (D = 64); 256 columns are allocated, so two CTAs can share an SM.
+// and [128, 192) (D = 64, where Q also moves into TMEM at [192, 224) as the A operand of Q.K^T);
+// 256 columns are allocated, so two CTAs share an SM.  The tensor core reads the shared-memory
+// operands of one 128 x 64 x 16 product at about 128 bytes per clock, so with Q in shared memory
+// the score product takes 48 cycles instead of 32 and the operand reads bound the kernel.
 //
 // Online softmax per row in the log2 domain.  The exponent reference m_ref is moved only when
 // the running maximum exceeds it by more than 8 (P <= 2^8 before the move), so O is rescaled
@@ -51,6 +54,8 @@ struct AttnArgs {
   unsigned long long *stats;
   int *status;
   const float *sq, *sk, *sv;  // 8-bit path: scales of the Q blocks, K blocks and V channels
+  const __nv_bfloat16 *q;     // bf16 path: Q rows, copied into TMEM by the softmax warps
+  int64_t q_sb, q_sh, q_sn;
 };
 
 // Warp-collective walk over the kept, valid key blocks of one mask row in ascending order, run
@@ -100,7 +105,8 @@ struct Smem {
   static constexpr int EB = QK8 ? 1 : 2;                 // bytes per element of Q and K
   static constexpr int QCH = D * EB / 128;               // 128-byte chunks of a Q or K row
   static constexpr int VCH = D * (PV8 ? 1 : 2) / 128;    // 128 bytes of V row data per chunk
-  static constexpr uint32_t Q_BYTES = QCH * 128 * 128;   // 128 rows x 128 B per chunk
+  static constexpr bool QTM = !QK8 && D == 64;           // bf16 d = 64: Q sits in TMEM, not shared memory
+  static constexpr uint32_t Q_BYTES = QTM ? 0u : QCH * 128 * 128;  // 128 rows x 128 B per chunk
   static constexpr uint32_t KV_CHUNK = 64 * 128;         // 64 rows x 128 B
   static constexpr uint32_t K_BYTES = QCH * KV_CHUNK;    // one K tile
   static constexpr uint32_t V_BYTES = VCH * KV_CHUNK;    // one V tile
@@ -160,14 +166,22 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   const int n_valid = a.causal ? min(a.nkb, causal_key_blocks(i, a.off)) : a.nkb;
   const uint8_t *mrow = a.mask ? a.mask + ((static_cast<int64_t>(b) * a.Hq + h) * a.nqb + i) * a.nkb : nullptr;
 
-  constexpr int SCOL0 = (D == 128) ? 128 : 64;
+  // TMEM columns: d = 128: O [0, 128), score buffers [128, 192) and [192, 256), Q in shared memory;
+  // d = 64 (bf16): O [0, 64), score buffers [64, 128) and [128, 192), and Q [192, 224) as the TMEM
+  // A operand of Q.K^T, so the tensor core reads only K from shared memory.  (Q in TMEM at d = 128
+  // leaves room for one score buffer only; measured slower, as Q.K^T of the next tile can then not
+  // run during the softmax of this one.)
+  constexpr bool QTM = L::QTM;
+  constexpr int NSB = (QTM && D == 128) ? 1 : 2;  // score buffers
+  constexpr int SCOL0 = (D == 128) ? (QTM ? 192 : 128) : 64;
+  constexpr int QCOL = (D == 128) ? 128 : 192;
   constexpr uint32_t TMEM_COLS = 256;
   constexpr uint32_t IDESC_S = QK8 ? idesc_f32acc(128, 64, FMT_E4M3, false) : idesc_f32acc(128, 64, FMT_BF16, false);
   constexpr uint32_t IDESC_PV = PV8 ? idesc_f32acc(128, D, FMT_E4M3, false) : idesc_f32acc(128, D, FMT_F16, true);
   constexpr int KSTEPS = D * L::EB / 32;  // 32 bytes of the contraction per MMA: K = 16 (bf16) or 32 (e4m3)
 
   if (threadIdx.x == 0) {
-    mbar_init(&cs.q_full, 1);
+    mbar_init(&cs.q_full, QTM ? 128 : 1);  // bf16: the 128 softmax threads after their Q rows are in TMEM
     for (int s = 0; s < KST; ++s) {
       mbar_init(&cs.k_full[s], 1);
       mbar_init(&cs.k_empty[s], 1);
@@ -228,7 +242,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         mbar_arrive(&cs.j_full[js]);
         cs.jk[kst] = j;
         if (j >= 0) {
-          if (t == 0) {
+          if (!QTM && t == 0) {
             mbar_arrive_expect_tx(&cs.q_full, L::Q_BYTES);
             for (int c = 0; c < L::QCH; ++c)
               tma_load_4d(smem + L::OFF_Q + c * 16384, &tq, &cs.q_full, (128 / L::EB) * c, QBLK * i, h, b);
@@ -275,20 +289,28 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       tc_fence_after();
       return cs.jk[st];
     };
+    // Descriptors: the start address is the low field (address / 16), so a tile's descriptor for an
+    // operand offset is the base descriptor plus offset / 16; only these adds remain per MMA.
+    const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
     auto issue_s = [&](int u) {
       if (lane == 0) {
-        const uint32_t kaddr = sK + (u % KST) * L::K_BYTES;
-        const uint32_t dS = tmem + SCOL0 + (u & 1) * 64;
+        const uint64_t dk = dk0 + static_cast<uint64_t>(((u % KST) * L::K_BYTES) >> 4);
+        const uint32_t dS = tmem + SCOL0 + (NSB == 2 ? (u & 1) * 64 : 0);
 #pragma unroll
         for (int s = 0; s < KSTEPS; ++s) {
-          const uint64_t da = smem_desc_sw128(sQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
-          const uint64_t db = smem_desc_sw128(kaddr + (s >> 2) * L::KV_CHUNK + (s & 3) * 32, 16, 1024);
-          if constexpr (QK8)
-            mma_f8_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
-          else
-            mma_bf16_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
+          const uint64_t db = dk + static_cast<uint64_t>(((s >> 2) * L::KV_CHUNK + (s & 3) * 32) >> 4);
+          if constexpr (QTM) {
+            mma_bf16_ts(dS, tmem + QCOL + s * 8, db, IDESC_S, s > 0 ? 1u : 0u);  // 16 bf16 of Q = 8 columns
+          } else {
+            const uint64_t da = dq0 + static_cast<uint64_t>(((s >> 2) * 16384 + (s & 3) * 32) >> 4);
+            if constexpr (QK8)
+              mma_f8_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
+            else
+              mma_bf16_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
+          }
         }
-        mma_commit(&cs.s_full[u & 1]);
+        mma_commit(&cs.s_full[NSB == 2 ? (u & 1) : 0]);
         mma_commit(&cs.k_empty[u % KST]);  // the K stage is free once this product completes
       }
       __syncwarp();
@@ -299,30 +321,35 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       issue_s(0);
       uint32_t pv_issued = 0;
       for (int t = 0;; ++t) {
-        jn = next_tile(t + 1);
-        if (jn >= 0) issue_s(t + 1);
-        if (jn == -2 || !mbar_wait(&cs.p_full[t & 1], (t >> 1) & 1, abort, a.status)) break;
+        // two score buffers: Q.K^T of tile t + 1 runs while the softmax works on tile t; one buffer:
+        // it follows P.V of tile t (the tensor core runs them in issue order), and the other CTA on
+        // the SM keeps the tensor core busy meanwhile
+        if constexpr (NSB == 2) {
+          jn = next_tile(t + 1);
+          if (jn >= 0) issue_s(t + 1);
+          if (jn == -2) break;
+        }
+        if (!mbar_wait(&cs.p_full[NSB == 2 ? (t & 1) : 0], NSB == 2 ? ((t >> 1) & 1) : (t & 1), abort, a.status)) break;
         const int vst = t % VST;
         if (!mbar_wait(&cs.v_full[vst], (t / VST) & 1, abort, a.status)) break;
         tc_fence_after();
-        const bool all_skip = cs.skip[t & 1][0] && cs.skip[t & 1][1] && cs.skip[t & 1][2] && cs.skip[t & 1][3];
+        const int sb = NSB == 2 ? (t & 1) : 0;
+        const bool all_skip = cs.skip[sb][0] && cs.skip[sb][1] && cs.skip[sb][2] && cs.skip[sb][3];
         if (lane == 0) {
           if (!all_skip) {
             const uint32_t vaddr = sV + vst * L::V_BYTES;
-            const uint32_t aP = tmem + SCOL0 + (t & 1) * 64;
+            const uint32_t aP = tmem + SCOL0 + sb * 64;
             if constexpr (PV8) {
               // P: 4 e4m3 per TMEM column, 8 columns per 32 keys; V tile rows of 64 keys
+              const uint64_t dv = smem_desc_sw64(vaddr, 512);
 #pragma unroll
-              for (int s = 0; s < 2; ++s) {
-                const uint64_t db = smem_desc_sw64(vaddr + s * 32, 512);
-                mma_f8_ts(tmem, aP + s * 8, db, IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
-              }
+              for (int s = 0; s < 2; ++s)
+                mma_f8_ts(tmem, aP + s * 8, dv + static_cast<uint64_t>((s * 32) >> 4), IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
             } else {
+              const uint64_t dv = smem_desc_sw128(vaddr, L::KV_CHUNK, 1024);
 #pragma unroll
-              for (int s = 0; s < 4; ++s) {
-                const uint64_t db = smem_desc_sw128(vaddr + s * 2048, L::KV_CHUNK, 1024);
-                mma_bf16_ts(tmem, aP + s * 8, db, IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
-              }
+              for (int s = 0; s < 4; ++s)
+                mma_bf16_ts(tmem, aP + s * 8, dv + static_cast<uint64_t>((s * 2048) >> 4), IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
             }
             pv_issued = 1;
             ++pv_count;
@@ -331,6 +358,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           mma_commit(&cs.o_done);
         }
         __syncwarp();
+        if constexpr (NSB == 1) {
+          jn = next_tile(t + 1);
+          if (jn >= 0) issue_s(t + 1);
+        }
         T = t + 1;
         if (jn < 0) break;
       }
@@ -370,6 +401,26 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       lam_log2 = (!good || lh == -INFINITY) ? -INFINITY : lh * 1.4426950408889634f;
       if (!good && r == 0) record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
     }
+    if constexpr (QTM) {
+      // this thread's Q row (zeros past the query length) into TMEM columns QCOL.., two bf16 per column
+      const uint4 *qsrc = reinterpret_cast<const uint4 *>(a.q + b * a.q_sb + h * a.q_sh + static_cast<int64_t>(row_ok ? row_g : 0) * a.q_sn);
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = row_ok ? __ldg(qsrc + 8 * half + c) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
+        }
+        tmem_st32(tl + QCOL + 32 * half, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&cs.q_full);
+    }
     float sq_blk = 1.f;
     const float *skrow = nullptr;
     if constexpr (QK8) {
@@ -387,8 +438,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       if (lane == 0) mbar_arrive(&cs.j_empty[js]);
       if (j < 0) break;
       T = t + 1;
-      const int buf = t & 1;
-      if (!mbar_wait(&cs.s_full[buf], (t >> 1) & 1, abort, a.status)) {
+      const int buf = NSB == 2 ? (t & 1) : 0;
+      if (!mbar_wait(&cs.s_full[buf], NSB == 2 ? ((t >> 1) & 1) : (t & 1), abort, a.status)) {
         ok = false;
         break;
       }
@@ -570,7 +621,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 
 template <int D, int KST, int VST, bool QK8, bool PV8>
 cudaError_t launch_t(const AttnLaunch &l, const AttnArgs &a, cudaStream_t st) {
-  const uint32_t smem = Smem<D, KST, VST, QK8, PV8>::TOTAL;
+  // each CTA allocates 256 TMEM columns, half of the SM's: at least 77 KB of shared memory keeps a
+  // third CTA off the SM (it would only wait in tcgen05.alloc)
+  constexpr uint32_t MIN_SMEM = 77u * 1024u;
+  const uint32_t smem = Smem<D, KST, VST, QK8, PV8>::TOTAL > MIN_SMEM ? Smem<D, KST, VST, QK8, PV8>::TOTAL : MIN_SMEM;
   static std::atomic<unsigned long long> smem_set{0};
   if (cudaError_t e = set_smem_limit_once(bsattn_kernel<D, KST, VST, QK8, PV8>, static_cast<int>(smem), smem_set); e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(a.B) * a.Hq * a.nqb;
@@ -602,6 +656,8 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
   a.sq = l.sq;
   a.sk = l.sk;
   a.sv = l.sv;
+  a.q = static_cast<const __nv_bfloat16 *>(l.q);
+  a.q_sb = l.q_sb; a.q_sh = l.q_sh; a.q_sn = l.q_sn;
   if (static_cast<int64_t>(a.B) * a.Hq * a.nqb == 0) return cudaSuccess;
   if (l.q8 != 0 && l.d != 128) return cudaErrorInvalidValue;
   if (l.q8 == 2) return launch_t<128, 4, 3, true, true>(l, a, st);

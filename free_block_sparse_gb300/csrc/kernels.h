@@ -82,6 +82,8 @@ struct AttnLaunch {
                            // f16 P.V; 2: as 1 with e4m3 P.V (channel-major e4m3 V, scales sv)
   const float *sq, *sk, *sv;
   const int32_t *perm;     // token order or nullptr: output row t goes to token perm[t] of o
+  const void *q;           // bf16 Q (the ordered copy under a token order), read row by row into TMEM
+  int64_t q_sb, q_sh, q_sn;
 };
 
 cudaError_t launch_bsattn(const AttnLaunch &a, cudaStream_t st);
