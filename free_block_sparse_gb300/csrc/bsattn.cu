@@ -4,15 +4,19 @@
 // online softmax-aware filter skips further updates; summary page: that filter works at GPU
 // warp level; Chinese README: arbitrary per-head block masks of 128x64 tiles.
 //
-// One CTA computes one 128-row query block of one head.  Warp roles (192 threads):
+// One CTA computes one 128-row query block of one head.  Warp roles (224 threads):
 //   warps 0-3  softmax + epilogue; warp w owns TMEM lanes 32w..32w+31, i.e. rows 32w.. of the
 //              block, one row per thread (the 32-row group of the lambda filter).
 //   warp 4     producer: TMA loads of the Q block once, then of only the kept tiles: K into a
 //              KST-deep ring that is freed as soon as Q.K^T of a tile completes (so K runs well
 //              ahead), V into a VST-deep ring freed when P.V completes; the key-block index of
 //              each tile goes to the softmax warps through a small ring of its own.
-//   warp 5     MMA issuer: S_t = Q K_t^T (bf16) into one of two TMEM score buffers, O += P_t V_t
-//              (f16) with P_t read back from TMEM (written over S_t) and V_t from shared memory.
+//   warp 5     score issuer: S_t = Q K_t^T (bf16) into one of two TMEM score buffers, as soon as
+//              K_t has landed and P.V of tile t - 2 (the buffer's last P) has completed.
+//   warp 6     P.V issuer: O += P_t V_t (f16) with P_t read back from TMEM (written over S_t) and
+//              V_t from shared memory.  A tcgen05.mma issue returns only once the tensor unit
+//              has taken the product, about 150 cycles per product here, so one thread issuing
+//              both kinds serialised them; two issuers overlap them.
 // P and V enter the second product as f16 (V converted once from bf16 by convert_v_f16 before
 // the kernel): P lies in [0, 256] and f16 keeps 3 more mantissa bits than bf16, so the P.V
 // rounding error is 8x smaller at the same tensor-core rate.
@@ -36,7 +40,7 @@
 namespace sparge {
 namespace {
 
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 224;
 constexpr int RESCALE_LOG2 = 8;   // bf16 path: O is rescaled when the running max passes m_ref + 8
 constexpr int RESCALE_LOG2_P8 = 4;  // e4m3 P: P = 2^(x - m_ref + 4) <= 256 < 448 (e4m3 maximum)
 #ifndef EXP_POLY_EVERY
@@ -129,12 +133,14 @@ struct Ctrl {
   uint64_t p_full[2];
   uint64_t o_done;
   uint64_t mma_done;
-  uint64_t final_bar;
+  uint64_t final_bar, final_bar2;  // completions of each issuer's products
+  uint64_t pv_done[2];             // P.V of the score buffer's last tile completed (buffer free)
   uint32_t tmem_base;
   int jring[JRING];  // key block of tile t at t % JRING; -1 marks the end of the row
   int jk[4];         // key block of the tile in each K stage (-1: end of the row)
   int abort;
   int pv_any;
+  int row_end;  // the row's tile count T, set by the softmax warps with their p_full arrival of phase T
   uint8_t skip[2][4];
 };
 static_assert(sizeof(Ctrl) <= 512, "control block");
@@ -172,7 +178,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   // leaves room for one score buffer only; measured slower, as Q.K^T of the next tile can then not
   // run during the softmax of this one.)
   constexpr bool QTM = L::QTM;
-  constexpr int NSB = (QTM && D == 128) ? 1 : 2;  // score buffers
+  constexpr int NSB = 2;  // score buffers (Q in TMEM only where two of them still fit)
+  static_assert(!QTM || D == 64, "Q in TMEM at d = 64 only");
   constexpr int SCOL0 = (D == 128) ? (QTM ? 192 : 128) : 64;
   constexpr int QCOL = (D == 128) ? 128 : 192;
   constexpr uint32_t TMEM_COLS = 256;
@@ -201,6 +208,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     mbar_init(&cs.o_done, 1);
     mbar_init(&cs.mma_done, 1);
     mbar_init(&cs.final_bar, 1);
+    mbar_init(&cs.final_bar2, 1);
+    mbar_init(&cs.pv_done[0], 1);
+    mbar_init(&cs.pv_done[1], 1);
+    cs.row_end = -1;
     cs.abort = 0;
     cs.pv_any = 0;
     fence_barrier_init();
@@ -280,8 +291,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
     }
   } else if (warp == 5) {
-    // ------------------------------------ MMA issuer ------------------------------------
-    int pv_count = 0, T = 0;
+    // ------------------------------ score-product issuer ------------------------------
+    // Q.K^T of tile u as soon as K_u has landed and the score buffer is free: it last held P of
+    // tile u - 2, so that P.V must have completed.  A second warp issues the P.V products, so
+    // neither kind of product waits behind the other's issue.
     // next_tile(u): waits for K stage u % KST and returns its key block (-1 = end of row)
     auto next_tile = [&](int u) -> int {
       const int st = u % KST;
@@ -315,71 +328,78 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
       __syncwarp();
     };
-    int jn = next_tile(0);
-    if (jn >= 0 && mbar_wait(&cs.q_full, 0, abort, a.status)) {
-      tc_fence_after();
-      issue_s(0);
-      uint32_t pv_issued = 0;
-      for (int t = 0;; ++t) {
-        // two score buffers: Q.K^T of tile t + 1 runs while the softmax works on tile t; one buffer:
-        // it follows P.V of tile t (the tensor core runs them in issue order), and the other CTA on
-        // the SM keeps the tensor core busy meanwhile
-        if constexpr (NSB == 2) {
-          jn = next_tile(t + 1);
-          if (jn >= 0) issue_s(t + 1);
-          if (jn == -2) break;
-        }
-        if (!mbar_wait(&cs.p_full[NSB == 2 ? (t & 1) : 0], NSB == 2 ? ((t >> 1) & 1) : (t & 1), abort, a.status)) break;
-        const int vst = t % VST;
-        if (!mbar_wait(&cs.v_full[vst], (t / VST) & 1, abort, a.status)) break;
+    int u = 0;
+    for (;; ++u) {
+      const int jn = next_tile(u);
+      if (jn < 0) break;  // -1: end of the row, -2: timeout
+      if (u == 0) {
+        if (!mbar_wait(&cs.q_full, 0, abort, a.status)) break;
         tc_fence_after();
-        const int sb = NSB == 2 ? (t & 1) : 0;
-        const bool all_skip = cs.skip[sb][0] && cs.skip[sb][1] && cs.skip[sb][2] && cs.skip[sb][3];
-        if (lane == 0) {
-          if (!all_skip) {
-            const uint32_t vaddr = sV + vst * L::V_BYTES;
-            const uint32_t aP = tmem + SCOL0 + sb * 64;
-            if constexpr (PV8) {
-              // P: 4 e4m3 per TMEM column, 8 columns per 32 keys; V tile rows of 64 keys
-              const uint64_t dv = smem_desc_sw64(vaddr, 512);
-#pragma unroll
-              for (int s = 0; s < 2; ++s)
-                mma_f8_ts(tmem, aP + s * 8, dv + static_cast<uint64_t>((s * 32) >> 4), IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
-            } else {
-              const uint64_t dv = smem_desc_sw128(vaddr, L::KV_CHUNK, 1024);
-#pragma unroll
-              for (int s = 0; s < 4; ++s)
-                mma_bf16_ts(tmem, aP + s * 8, dv + static_cast<uint64_t>((s * 2048) >> 4), IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
-            }
-            pv_issued = 1;
-            ++pv_count;
-          }
-          mma_commit(&cs.v_empty[vst]);
-          mma_commit(&cs.o_done);
-        }
-        __syncwarp();
-        if constexpr (NSB == 1) {
-          jn = next_tile(t + 1);
-          if (jn >= 0) issue_s(t + 1);
-        }
-        T = t + 1;
-        if (jn < 0) break;
+      } else if (u >= 2) {
+        if (!mbar_wait(&cs.pv_done[u & 1], ((u - 2) >> 1) & 1, abort, a.status)) break;
+        tc_fence_after();
       }
-      if (lane == 0) {
-        cs.pv_any = static_cast<int>(pv_issued);
-        mbar_arrive(&cs.mma_done);
-      }
+      issue_s(u);
     }
     if (lane == 0) {
-      if (T > 0) {
-        mma_commit(&cs.final_bar);  // completes once every MMA above has finished
+      if (u > 0) {
+        mma_commit(&cs.final_bar);  // completes once every product this thread issued has finished
         mbar_wait(&cs.final_bar, 0, abort, a.status);
       }
       if (a.stats) {
-        atomicAdd(a.stats + 0, static_cast<unsigned long long>(T));
-        atomicAdd(a.stats + 1, static_cast<unsigned long long>(pv_count));
+        atomicAdd(a.stats + 0, static_cast<unsigned long long>(u));
         atomicAdd(a.stats + 3, static_cast<unsigned long long>(n_valid));
       }
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------ P.V issuer ------------------------------
+    // O += P_t V_t once the softmax has written P_t and V_t has landed; the softmax warps mark the
+    // end of the row with one more p_full arrival, phase T, after storing T in row_end (the flag may
+    // already hold T while earlier phases are still being consumed, hence the comparison with t).
+    int pv_count = 0, t = 0;
+    uint32_t pv_issued = 0;
+    for (;; ++t) {
+      if (!mbar_wait(&cs.p_full[t & 1], (t >> 1) & 1, abort, a.status)) break;
+      if (*reinterpret_cast<volatile int *>(&cs.row_end) == t) break;  // set before phase t's arrival
+      const int vst = t % VST;
+      if (!mbar_wait(&cs.v_full[vst], (t / VST) & 1, abort, a.status)) break;
+      tc_fence_after();
+      const int sb = t & 1;
+      const bool all_skip = cs.skip[sb][0] && cs.skip[sb][1] && cs.skip[sb][2] && cs.skip[sb][3];
+      if (lane == 0) {
+        if (!all_skip) {
+          const uint32_t vaddr = sV + vst * L::V_BYTES;
+          const uint32_t aP = tmem + SCOL0 + sb * 64;
+          if constexpr (PV8) {
+            // P: 4 e4m3 per TMEM column, 8 columns per 32 keys; V tile rows of 64 keys
+            const uint64_t dv = smem_desc_sw64(vaddr, 512);
+#pragma unroll
+            for (int s = 0; s < 2; ++s)
+              mma_f8_ts(tmem, aP + s * 8, dv + static_cast<uint64_t>((s * 32) >> 4), IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
+          } else {
+            const uint64_t dv = smem_desc_sw128(vaddr, L::KV_CHUNK, 1024);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              mma_bf16_ts(tmem, aP + s * 8, dv + static_cast<uint64_t>((s * 2048) >> 4), IDESC_PV, (pv_issued | (s > 0 ? 1u : 0u)));
+          }
+          pv_issued = 1;
+          ++pv_count;
+        }
+        mma_commit(&cs.v_empty[vst]);
+        mma_commit(&cs.o_done);
+        mma_commit(&cs.pv_done[sb]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      cs.pv_any = static_cast<int>(pv_issued);
+      mbar_arrive(&cs.mma_done);
+      if (t > 0) {
+        mma_commit(&cs.final_bar2);
+        mbar_wait(&cs.final_bar2, 0, abort, a.status);
+      }
+      if (a.stats) atomicAdd(a.stats + 1, static_cast<unsigned long long>(pv_count));
     }
     __syncwarp();
   } else {
@@ -436,7 +456,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       const int j = cs.jring[js];
       __syncwarp();
       if (lane == 0) mbar_arrive(&cs.j_empty[js]);
-      if (j < 0) break;
+      if (j < 0) {  // tell the P.V issuer: phase t of p_full carries no tile (t = T, the tile count)
+        if (r == 0) cs.row_end = t;
+        mbar_arrive(&cs.p_full[t & 1]);
+        break;
+      }
       T = t + 1;
       const int buf = NSB == 2 ? (t & 1) : 0;
       if (!mbar_wait(&cs.s_full[buf], NSB == 2 ? ((t >> 1) & 1) : (t & 1), abort, a.status)) {
