@@ -109,7 +109,10 @@ struct Smem {
   static constexpr int EB = QK8 ? 1 : 2;                 // bytes per element of Q and K
   static constexpr int QCH = D * EB / 128;               // 128-byte chunks of a Q or K row
   static constexpr int VCH = D * (PV8 ? 1 : 2) / 128;    // 128 bytes of V row data per chunk
-  static constexpr bool QTM = !QK8 && D == 64;           // bf16 d = 64: Q sits in TMEM, not shared memory
+  // TMEM score buffers.  At d = 64 a third buffer fits if Q leaves TMEM (O 64 + 3 x 64 columns);
+  // measured no faster than two buffers with Q in TMEM (video-like 0.516 vs 0.506 ms).
+  static constexpr int NSB = 2;
+  static constexpr bool QTM = !QK8 && D == 64;  // Q in TMEM where two score buffers still fit
   static constexpr uint32_t Q_BYTES = QTM ? 0u : QCH * 128 * 128;  // 128 rows x 128 B per chunk
   static constexpr uint32_t KV_CHUNK = 64 * 128;         // 64 rows x 128 B
   static constexpr uint32_t K_BYTES = QCH * KV_CHUNK;    // one K tile
@@ -129,19 +132,18 @@ struct Ctrl {
   uint64_t k_full[4], k_empty[4];    // K ring: filled by TMA, freed when Q.K^T of the tile completes
   uint64_t v_full[4], v_empty[4];    // V ring: filled by TMA, freed when P.V of the tile completes
   uint64_t j_full[JRING], j_empty[JRING];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_done;
+  uint64_t s_full[4];
+  uint64_t p_full[4];
   uint64_t mma_done;
   uint64_t final_bar, final_bar2;  // completions of each issuer's products
-  uint64_t pv_done[2];             // P.V of the score buffer's last tile completed (buffer free)
+  uint64_t pv_done[4];             // P.V of the score buffer's last tile completed (buffer free)
   uint32_t tmem_base;
   int jring[JRING];  // key block of tile t at t % JRING; -1 marks the end of the row
   int jk[4];         // key block of the tile in each K stage (-1: end of the row)
   int abort;
   int pv_any;
   int row_end;  // the row's tile count T, set by the softmax warps with their p_full arrival of phase T
-  uint8_t skip[2][4];
+  uint8_t skip[4][4];
 };
 static_assert(sizeof(Ctrl) <= 512, "control block");
 
@@ -178,9 +180,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   // leaves room for one score buffer only; measured slower, as Q.K^T of the next tile can then not
   // run during the softmax of this one.)
   constexpr bool QTM = L::QTM;
-  constexpr int NSB = 2;  // score buffers (Q in TMEM only where two of them still fit)
+  constexpr int NSB = L::NSB;  // score buffers
   static_assert(!QTM || D == 64, "Q in TMEM at d = 64 only");
-  constexpr int SCOL0 = (D == 128) ? (QTM ? 192 : 128) : 64;
+  constexpr int SCOL0 = (D == 128) ? 128 : 64;
   constexpr int QCOL = (D == 128) ? 128 : 192;
   constexpr uint32_t TMEM_COLS = 256;
   constexpr uint32_t IDESC_S = QK8 ? idesc_f32acc(128, 64, FMT_E4M3, false) : idesc_f32acc(128, 64, FMT_BF16, false);
@@ -201,16 +203,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       mbar_init(&cs.j_full[s], 1);
       mbar_init(&cs.j_empty[s], 4);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < L::NSB; ++s) {
       mbar_init(&cs.s_full[s], 1);
       mbar_init(&cs.p_full[s], 128);
+      mbar_init(&cs.pv_done[s], 1);
     }
-    mbar_init(&cs.o_done, 1);
     mbar_init(&cs.mma_done, 1);
     mbar_init(&cs.final_bar, 1);
     mbar_init(&cs.final_bar2, 1);
-    mbar_init(&cs.pv_done[0], 1);
-    mbar_init(&cs.pv_done[1], 1);
     cs.row_end = -1;
     cs.abort = 0;
     cs.pv_any = 0;
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     auto issue_s = [&](int u) {
       if (lane == 0) {
         const uint64_t dk = dk0 + static_cast<uint64_t>(((u % KST) * L::K_BYTES) >> 4);
-        const uint32_t dS = tmem + SCOL0 + (NSB == 2 ? (u & 1) * 64 : 0);
+        const uint32_t dS = tmem + SCOL0 + (u % NSB) * 64;
 #pragma unroll
         for (int s = 0; s < KSTEPS; ++s) {
           const uint64_t db = dk + static_cast<uint64_t>(((s >> 2) * L::KV_CHUNK + (s & 3) * 32) >> 4);
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
               mma_bf16_ss(dS, da, db, IDESC_S, s > 0 ? 1u : 0u);
           }
         }
-        mma_commit(&cs.s_full[NSB == 2 ? (u & 1) : 0]);
+        mma_commit(&cs.s_full[u % NSB]);
         mma_commit(&cs.k_empty[u % KST]);  // the K stage is free once this product completes
       }
       __syncwarp();
@@ -335,8 +335,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       if (u == 0) {
         if (!mbar_wait(&cs.q_full, 0, abort, a.status)) break;
         tc_fence_after();
-      } else if (u >= 2) {
-        if (!mbar_wait(&cs.pv_done[u & 1], ((u - 2) >> 1) & 1, abort, a.status)) break;
+      } else if (u >= NSB) {
+        if (!mbar_wait(&cs.pv_done[u % NSB], ((u - NSB) / NSB) & 1, abort, a.status)) break;
         tc_fence_after();
       }
       issue_s(u);
@@ -360,12 +360,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     int pv_count = 0, t = 0;
     uint32_t pv_issued = 0;
     for (;; ++t) {
-      if (!mbar_wait(&cs.p_full[t & 1], (t >> 1) & 1, abort, a.status)) break;
+      if (!mbar_wait(&cs.p_full[t % NSB], (t / NSB) & 1, abort, a.status)) break;
       if (*reinterpret_cast<volatile int *>(&cs.row_end) == t) break;  // set before phase t's arrival
       const int vst = t % VST;
       if (!mbar_wait(&cs.v_full[vst], (t / VST) & 1, abort, a.status)) break;
       tc_fence_after();
-      const int sb = t & 1;
+      const int sb = t % NSB;
       const bool all_skip = cs.skip[sb][0] && cs.skip[sb][1] && cs.skip[sb][2] && cs.skip[sb][3];
       if (lane == 0) {
         if (!all_skip) {
@@ -387,18 +387,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           ++pv_count;
         }
         mma_commit(&cs.v_empty[vst]);
-        mma_commit(&cs.o_done);
         mma_commit(&cs.pv_done[sb]);
       }
       __syncwarp();
     }
     if (lane == 0) {
-      cs.pv_any = static_cast<int>(pv_issued);
-      mbar_arrive(&cs.mma_done);
       if (t > 0) {
-        mma_commit(&cs.final_bar2);
+        mma_commit(&cs.final_bar2);  // completes once every P.V product has finished
         mbar_wait(&cs.final_bar2, 0, abort, a.status);
       }
+      cs.pv_any = static_cast<int>(pv_issued);
+      mbar_arrive(&cs.mma_done);  // the epilogue may read O
       if (a.stats) atomicAdd(a.stats + 1, static_cast<unsigned long long>(pv_count));
     }
     __syncwarp();
@@ -458,12 +457,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       if (lane == 0) mbar_arrive(&cs.j_empty[js]);
       if (j < 0) {  // tell the P.V issuer: phase t of p_full carries no tile (t = T, the tile count)
         if (r == 0) cs.row_end = t;
-        mbar_arrive(&cs.p_full[t & 1]);
+        mbar_arrive(&cs.p_full[t % NSB]);
         break;
       }
       T = t + 1;
-      const int buf = NSB == 2 ? (t & 1) : 0;
-      if (!mbar_wait(&cs.s_full[buf], NSB == 2 ? ((t >> 1) & 1) : (t & 1), abort, a.status)) {
+      const int buf = t % NSB;
+      if (!mbar_wait(&cs.s_full[buf], (t / NSB) & 1, abort, a.status)) {
         ok = false;
         break;
       }
@@ -511,7 +510,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       const float alpha = resc ? fast_exp2(m_ref - m_new) : 1.f;
       if (__any_sync(0xffffffffu, resc) && t > 0) {
         // O must hold P_{t-1} V_{t-1} before it is rescaled
-        if (!mbar_wait(&cs.o_done, (t - 1) & 1, abort, a.status)) {
+        // P.V of tile t - 1 completed: phase (t - 1) / NSB of its buffer's barrier (that barrier's
+        // phases are NSB tiles apart, so a pending P.V of tile t - 2 cannot alias the wait)
+        if (!mbar_wait(&cs.pv_done[(t - 1) % NSB], ((t - 1) / NSB) & 1, abort, a.status)) {
           ok = false;
           break;
         }
@@ -581,7 +582,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     // ------------------------------------ epilogue ------------------------------------
     bool have_o = false;
     if (T > 0 && ok) {
-      ok = mbar_wait(&cs.o_done, (T - 1) & 1, abort, a.status) && mbar_wait(&cs.mma_done, 0, abort, a.status);
+      ok = mbar_wait(&cs.mma_done, 0, abort, a.status);  // every P.V product has completed
       tc_fence_after();
       have_o = ok && cs.pv_any != 0;
     }
