@@ -278,6 +278,25 @@ def random_qkv(seed, B, Hq, Hkv, N, d, std=1.0):
     return q, k, v
 
 
+def climbing_qkv(seed, B, Hq, Hkv, N, d, step_log2=9.0, alpha=4.0):
+    """Q/K whose scores climb from each 64-key block to the next (edge-case tests of the O rescale).
+
+    Every query is alpha * u plus N(0, 0.1) noise and every key of key block b is beta_b * u plus
+    N(0, 0.1) noise, for one random unit vector u per head, with beta_b chosen so that the score
+    q.k / sqrt(d) grows by step_log2 (in log2 units) per key block; V is iid N(0, 1)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    u = _normal(rng, (B, Hkv, 1, d), 1.0)
+    u /= np.linalg.norm(u, axis=-1, keepdims=True)
+    G = Hq // Hkv
+    uq = np.repeat(u, G, axis=1)
+    dbeta = step_log2 * math.log(2.0) * math.sqrt(d) / alpha
+    beta = (np.arange(N) // KBLK).astype(np.float32) * np.float32(dbeta)
+    q = alpha * uq + _normal(rng, (B, Hq, N, d), 0.1)
+    k = beta[None, None, :, None] * u + _normal(rng, (B, Hkv, N, d), 0.1)
+    v = _normal(rng, (B, Hkv, N, d), 1.0)
+    return bf16_bits(q), bf16_bits(k), bf16_bits(v)
+
+
 def random_mask(seed, B, H, N, p=0.25, force_diag=True):
     """Bernoulli(p) tile mask, optionally with the diagonal tiles (2i, 2i+1) forced on."""
     rng = np.random.Generator(np.random.PCG64(seed))
