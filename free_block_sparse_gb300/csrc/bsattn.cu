@@ -43,9 +43,6 @@ namespace {
 constexpr int NTHREADS = 224;
 constexpr int RESCALE_LOG2 = 8;   // bf16 path: O is rescaled when the running max passes m_ref + 8
 constexpr int RESCALE_LOG2_P8 = 4;  // e4m3 P: P = 2^(x - m_ref + 4) <= 256 < 448 (e4m3 maximum)
-#ifndef EXP_POLY_EVERY
-#define EXP_POLY_EVERY 1000  // pairs c with c % EXP_POLY_EVERY == EXP_POLY_EVERY - 1 use the FMA-pipe exp2 (off: MUFU is not the limit)
-#endif
 
 struct AttnArgs {
   const uint8_t *mask;
@@ -550,9 +547,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float2 e2 = ffma2(make_float2(x[2 * c], x[2 * c + 1]), sc2, nr2);
-        // every EXP_POLY_EVERY-th pair goes to the FMA pipe so the MUFU unit is not the bottleneck
-        const float2 p2 = (c % EXP_POLY_EVERY == EXP_POLY_EVERY - 1) ? exp2_poly2(e2)
-                                                                      : make_float2(fast_exp2(e2.x), fast_exp2(e2.y));
+        const float2 p2 = make_float2(fast_exp2(e2.x), fast_exp2(e2.y));
         rs2[c & 3] = fadd2(rs2[c & 3], p2);  // four independent chains
         pk[c] = PV8 ? pack_e4m3x2(p2.x, p2.y) : pack_f16x2(p2.x, p2.y);
       }

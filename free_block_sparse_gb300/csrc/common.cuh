@@ -385,30 +385,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// 2^x for a pair of floats on the FMA and integer pipes instead of the MUFU unit.  Range
-// reduction to the nearest integer n (adding and subtracting 1.5 * 2^23 rounds x to an integer
-// in fp32), a degree-3 polynomial p(f) = 1 + f (c1 + f (c2 + f c3)) for 2^f on f in [-1/2, 1/2]
-// (coefficients fitted here by iteratively reweighted least squares toward the minimax relative
-// error; max relative error 1.0e-4 in fp32), then n added to the exponent field.  x is clamped
-// to [-127, inf): x = -127 (and -inf) gives exactly +0.  Valid for x <= 127.
-constexpr float EXP2_C1 = 0.6932829022407532f;
-constexpr float EXP2_C2 = 0.2422104775905609f;
-constexpr float EXP2_C3 = 0.05500867962837219f;
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  constexpr float RND = 12582912.f;  // 1.5 * 2^23
-  x.x = fmaxf(x.x, -127.f);
-  x.y = fmaxf(x.y, -127.f);
-  const float2 t = fadd2(x, make_float2(RND, RND));
-  const float2 n = fadd2(t, make_float2(-RND, -RND));
-  const float2 f = ffma2(n, make_float2(-1.f, -1.f), x);
-  float2 p = ffma2(f, make_float2(EXP2_C3, EXP2_C3), make_float2(EXP2_C2, EXP2_C2));
-  p = ffma2(p, f, make_float2(EXP2_C1, EXP2_C1));
-  p = ffma2(p, f, make_float2(1.f, 1.f));
-  // the low mantissa bits of t hold n; shifting them into the exponent field drops the offset
-  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
-}
-
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
