@@ -199,9 +199,12 @@ size_t order_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
   return align256((size_t)2 * B * Hq * N * d) + align256((size_t)2 * B * Hkv * N * d);
 }
 
-// Calls with a token order: copies q and k into the front of the workspace in that order
-// (contiguous (B, H, N, d) bf16), replaces q and k by the copies and moves ws past them.
-int order_qk(View &q, View &k, const int32_t *perm, void *&ws, size_t &ws_bytes, cudaStream_t s) {
+// Calls with a token order: copies q and/or k into the front of the workspace in that order
+// (contiguous (B, H, N, d) bf16), replaces them by the copies and moves ws past the space of both
+// (the space is reserved whether or not a copy is made).  A tensor that is not copied is read
+// through the permutation by the kernels instead (pooling, and the d = 64 attention's Q rows).
+int order_qk(View &q, View &k, const int32_t *perm, void *&ws, size_t &ws_bytes, cudaStream_t s, bool copy_q = true,
+             bool copy_k = true) {
   const size_t need = order_bytes(q.B, q.H, k.H, q.N, q.d);
   if (!ws || ws_bytes < need)
     return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu for the token-ordered copies", ws_bytes,
@@ -209,15 +212,22 @@ int order_qk(View &q, View &k, const int32_t *perm, void *&ws, size_t &ws_bytes,
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(SPARGE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   uint8_t *base = static_cast<uint8_t *>(ws);
   void *qc = base, *kc = base + align256((size_t)2 * q.B * q.H * q.N * q.d);
-  cudaError_t e = launch_permute(q, perm, qc, q.H * q.N * q.d, q.N * q.d, q.d, false, status_ptr(), s, true);
-  if (e == cudaSuccess) e = launch_permute(k, perm, kc, k.H * k.N * k.d, k.N * k.d, k.d, false, status_ptr(), s, true);
+  cudaError_t e = cudaSuccess;
+  if (copy_q) e = launch_permute(q, perm, qc, q.H * q.N * q.d, q.N * q.d, q.d, false, status_ptr(), s, true);
+  if (e == cudaSuccess && copy_k)
+    e = launch_permute(k, perm, kc, k.H * k.N * k.d, k.N * k.d, k.d, false, status_ptr(), s, true);
   if (e != cudaSuccess) return cuda_fail(e, "token-order copy launch");
-  q = View{qc, q.B, q.H, q.N, q.d, q.H * q.N * q.d, q.N * q.d, q.d};
-  k = View{kc, k.B, k.H, k.N, k.d, k.H * k.N * k.d, k.N * k.d, k.d};
+  if (copy_q) q = View{qc, q.B, q.H, q.N, q.d, q.H * q.N * q.d, q.N * q.d, q.d};
+  if (copy_k) k = View{kc, k.B, k.H, k.N, k.d, k.H * k.N * k.d, k.N * k.d, k.d};
   ws = base + need;
   ws_bytes -= need;
   return SPARGE_OK;
 }
+
+bool is_q8(int precision);
+// Under a token order Q gets an ordered copy only where TMA (d = 128) or the 8-bit quantiser reads
+// it; at d = 64 the attention loads Q rows itself and gathers them through the permutation.
+bool order_copies_q(int64_t d, int precision) { return d != 64 || is_q8(precision); }
 
 // Per-query-head parameter arrays of a sparge_params (device pointers, each may be null).
 struct HeadParams {
@@ -226,7 +236,8 @@ struct HeadParams {
 };
 
 int predict_impl(const View &q, const View &k, float topk, float theta, int causal, float scale, uint8_t *mask,
-                 void *ws, size_t ws_bytes, cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {}) {
+                 void *ws, size_t ws_bytes, cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {},
+                 const int32_t *qperm = nullptr, const int32_t *kperm = nullptr) {
   if (!mask) return fail(SPARGE_ERR_INVALID_ARG, "mask is NULL");
   int rc;
   if ((rc = check_lengths(q, k, causal))) return rc;
@@ -239,7 +250,7 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
   if (q.B == 0 || q.N == 0) return SPARGE_OK;
   PredictWs pw = predict_ws_carve(ws, q.B, q.H, k.H, q.N, k.N, q.d);
   if ((rc = record_event(ev, 0, s))) return rc;
-  cudaError_t e = launch_pool_sim(q, k, pw, s);
+  cudaError_t e = launch_pool_sim(q, k, pw, s, qperm, kperm, status_ptr());
   if (e != cudaSuccess) return cuda_fail(e, "pool_sim launch");
   if ((rc = record_event(ev, 1, s))) return rc;
   {
@@ -278,7 +289,8 @@ size_t attn_ws_bytes(int precision, int64_t B, int64_t Hq, int64_t Hkv, int64_t 
 
 int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, float lambda, int causal, float scale,
               int precision, sparge_tensor *o, unsigned long long *stats, void *ws, size_t ws_bytes,
-              cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {}, const int32_t *perm = nullptr) {
+              cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {}, const int32_t *perm = nullptr,
+              const int32_t *qperm = nullptr) {
   if (precision != SPARGE_PRECISION_BF16 && !is_q8(precision))
     return fail(SPARGE_ERR_UNSUPPORTED, "precision %d not supported", precision);
   const bool q8 = is_q8(precision), pv8 = precision == SPARGE_PRECISION_Q8_FP8PV;
@@ -327,6 +339,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
     View v16{ws, v.B, v.H, v.N, v.d, v.H * v.N * v.d, v.N * v.d, v.d};
     if ((rc = make_map(&l.tq, q, 128, "q"))) return rc;  // checks the alignment the row reads rely on
     l.q = q.data;
+    l.qperm = qperm;  // d = 64 under a token order: q is the caller's tensor, gathered by row
     l.q_sb = q.sb; l.q_sh = q.sh; l.q_sn = q.sn;
     if ((rc = make_map(&l.tk, k, 64, "k"))) return rc;
     if ((rc = make_map(&l.tv, v16, 64, "v", CU_TENSOR_MAP_DATA_TYPE_FLOAT16))) return rc;
@@ -468,9 +481,11 @@ int sparge_predict_mask_ex(const sparge_tensor *q, const sparge_tensor *k, float
     const size_t need = order_bytes(qv.B, qv.H, kv.H, qv.N, qv.d) + predict_ws_bytes(qv.B, qv.H, kv.H, qv.N, kv.N, qv.d);
     if (!mask) return fail(SPARGE_ERR_INVALID_ARG, "mask is NULL");
     if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
-    if (qv.B * qv.N > 0 && (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s))) return rc;
+    // pooling reads q and k through the permutation: no ordered copies (the space stays reserved)
+    if (qv.B * qv.N > 0 && (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s, false, false))) return rc;
   }
-  return predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, ws_bytes, s, p->timing_events, hp);
+  return predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, ws_bytes, s, p->timing_events, hp,
+                      p->token_order, p->token_order);
 }
 
 int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v,
@@ -509,11 +524,14 @@ int sparge_block_sparse_attn_ex(const sparge_tensor *q, const sparge_tensor *k, 
     if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   }
   if ((rc = record_event(p->timing_events, 0, s))) return rc;
-  if (p->token_order && qv.B * qv.N > 0 && (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s))) return rc;
+  const bool copy_q = order_copies_q(qv.d, p->precision);
+  if (p->token_order && qv.B * qv.N > 0 &&
+      (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s, copy_q, true)))
+    return rc;
   HeadParams hp;
   hp.lambda = p->lambda_per_head;
   return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws, ws_bytes, s,
-                   p->timing_events, hp, p->token_order);
+                   p->timing_events, hp, p->token_order, (p->token_order && !copy_q) ? p->token_order : nullptr);
 }
 
 int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,
@@ -540,7 +558,11 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   const size_t need = need_order + need_pred + mask_bytes + need_v;
   if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (p->token_order && qv.B * qv.N > 0 && (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s))) return rc;
+  const bool copy_q = order_copies_q(qv.d, p->precision);
+  if (p->token_order && qv.B * qv.N > 0 &&
+      (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s, copy_q, true)))
+    return rc;
+  const int32_t *qperm = (p->token_order && !copy_q) ? p->token_order : nullptr;  // q not copied: gathered
   uint8_t *mask = mask_out ? mask_out : static_cast<uint8_t *>(ws) + need_pred;
   void *ws_v = static_cast<uint8_t *>(ws) + need_pred + mask_bytes;
   if (p->topk_mode != SPARGE_TOPK_CUMULATIVE && p->topk_mode != SPARGE_TOPK_COUNT)
@@ -550,10 +572,10 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   hp.theta = p->theta_per_head;
   hp.lambda = p->lambda_per_head;
   hp.topk_mode = p->topk_mode;
-  if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s, p->timing_events, hp)))
+  if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s, p->timing_events, hp, qperm)))
     return rc;
   return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws_v, need_v, s,
-                   p->timing_events, hp, p->token_order);
+                   p->timing_events, hp, p->token_order, qperm);
 }
 
 int sparge_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,

@@ -56,6 +56,7 @@ struct AttnArgs {
   int *status;
   const float *sq, *sk, *sv;  // 8-bit path: scales of the Q blocks, K blocks and V channels
   const __nv_bfloat16 *q;     // bf16 path: Q rows, copied into TMEM by the softmax warps
+  const int32_t *qperm;       // token order of those rows (or nullptr)
   int64_t q_sb, q_sh, q_sn;
 };
 
@@ -419,13 +420,25 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
     if constexpr (QTM) {
       // this thread's Q row (zeros past the query length) into TMEM columns QCOL.., two bf16 per column
-      const uint4 *qsrc = reinterpret_cast<const uint4 *>(a.q + b * a.q_sb + h * a.q_sh + static_cast<int64_t>(row_ok ? row_g : 0) * a.q_sn);
+      // under a token order the row is token qperm[row] of q (an entry outside 0..Nq-1 is
+      // reported and read as a zero row)
+      int qrow = row_ok ? row_g : 0;
+      bool qok = row_ok;
+      if (a.qperm != nullptr && row_ok) {
+        qrow = __ldg(a.qperm + row_g);
+        if (static_cast<unsigned>(qrow) >= static_cast<unsigned>(a.Nq)) {
+          record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
+          qrow = 0;
+          qok = false;
+        }
+      }
+      const uint4 *qsrc = reinterpret_cast<const uint4 *>(a.q + b * a.q_sb + h * a.q_sh + static_cast<int64_t>(qrow) * a.q_sn);
 #pragma unroll
       for (int half = 0; half < D / 64; ++half) {
         uint32_t w[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 v = row_ok ? __ldg(qsrc + 8 * half + c) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 v = qok ? __ldg(qsrc + 8 * half + c) : make_uint4(0u, 0u, 0u, 0u);
           w[4 * c] = v.x;
           w[4 * c + 1] = v.y;
           w[4 * c + 2] = v.z;
@@ -678,6 +691,7 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
   a.sv = l.sv;
   a.q = static_cast<const __nv_bfloat16 *>(l.q);
   a.q_sb = l.q_sb; a.q_sh = l.q_sh; a.q_sn = l.q_sn;
+  a.qperm = l.qperm;
   if (static_cast<int64_t>(a.B) * a.Hq * a.nqb == 0) return cudaSuccess;
   if (l.q8 != 0 && l.d != 128) return cudaErrorInvalidValue;
   if (l.q8 == 2) return launch_t<128, 4, 3, true, true>(l, a, st);

@@ -42,7 +42,10 @@ int run_predict(const View &q, const View &k, float topk, float theta, int causa
                 size_t ws_bytes, cudaStream_t s);
 int report_error(int code, const char *msg);
 
-cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, cudaStream_t st);
+// qperm / kperm (or nullptr): token order of q / k; block row t of the pooling is token perm[t] (an
+// entry outside 0..N-1 is reported in *status and read as a zero token).
+cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, cudaStream_t st,
+                            const int32_t *qperm = nullptr, const int32_t *kperm = nullptr, int *status = nullptr);
 
 // Pooled scores S = scale * muQ . muK^T on tcgen05 (bf16 hi/lo split, three products), for the
 // valid (causal) key blocks of every query block.  The four maps cover qhi, qlo (3-D: d, nqb,
@@ -82,7 +85,9 @@ struct AttnLaunch {
                            // f16 P.V; 2: as 1 with e4m3 P.V (channel-major e4m3 V, scales sv)
   const float *sq, *sk, *sv;
   const int32_t *perm;     // token order or nullptr: output row t goes to token perm[t] of o
-  const void *q;           // bf16 Q (the ordered copy under a token order), read row by row into TMEM
+  const void *q;           // bf16 Q, read row by row into TMEM at d = 64 (the ordered copy under a token order
+                           // at d = 128, where the rows come by TMA)
+  const int32_t *qperm;    // d = 64 under a token order: Q row t of the block is token qperm[t] of q
   int64_t q_sb, q_sh, q_sn;
 };
 

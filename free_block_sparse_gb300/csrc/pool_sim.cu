@@ -7,7 +7,9 @@
 // zero unit vector.  Memory-bound: one pass over Q and K.  One warp per block, no block-level
 // barriers: each lane keeps eight 16-byte loads in flight in a rolling register buffer while it
 // accumulates, so many warps per SM keep enough bytes in flight to hold HBM busy; fp32 (packed
-// pair) arithmetic, warp-shuffle reductions, vector stores of the results.
+// pair) arithmetic, warp-shuffle reductions, vector stores of the results.  Under a token order
+// (Hilbert order of image or video tokens) a block's rows are gathered whole through the order
+// (its indices read once into shared memory), so the pooling needs no ordered copy of Q or K.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -20,12 +22,18 @@ struct PoolArgs {
   int B, Hq, Hkv, Nq, Nk, nqb, nkb;  // query and key lengths may differ
   int64_t nq_total, total;
   PredictWs ws;
+  const int32_t *qperm, *kperm;  // token orders (or nullptr): block row t is token perm[t]
+  int *status;
 };
 
 constexpr int INFLIGHT = 8;  // 16-byte loads in flight per lane
 
-template <int D>
-__global__ void __launch_bounds__(128, 5) pool_sim_kernel(PoolArgs a) {
+// GATHER: rows come through the token orders (a separate instantiation, so the plain streaming
+// kernel keeps its registers).
+template <int D, bool GATHER>
+__global__ void __launch_bounds__(128, GATHER ? 4 : 5) pool_sim_kernel(PoolArgs a) {
+  constexpr int IFL = INFLIGHT;
+  __shared__ int sperm[GATHER ? 4 : 1][GATHER ? QBLK : 1];  // the block's token indices, per warp
   constexpr int LPT = D / 8;     // lanes per token, 8 bf16 (16 bytes) per lane
   constexpr int TPW = 32 / LPT;  // tokens per warp-wide load
   const int lane = threadIdx.x & 31;
@@ -58,24 +66,44 @@ __global__ void __launch_bounds__(128, 5) pool_sim_kernel(PoolArgs a) {
       base = a.k + b * a.k_sb + h * a.k_sh + static_cast<int64_t>(idx) * KBLK * sn;
       row = (static_cast<int64_t>(b) * a.Hkv + h) * a.nkb + idx;
     }
-    n = min(rows, (isQ ? a.Nq : a.Nk) - idx * rows);
-    const int steps = rows / TPW;  // warp-wide loads covering the block (a multiple of INFLIGHT)
+    const int ntok = isQ ? a.Nq : a.Nk;
+    n = min(rows, ntok - idx * rows);
+    const int steps = rows / TPW;  // warp-wide loads covering the block (a multiple of IFL)
     const __nv_bfloat16 *p = base + sub * sn + part * 8;
+    // under a token order the block's row t is token perm[t] of the head (gathered whole rows)
+    const int32_t *perm = isQ ? a.qperm : a.kperm;
+    const __nv_bfloat16 *hbase = base - static_cast<int64_t>(idx) * rows * sn + part * 8;
+    int *wperm = GATHER ? sperm[(threadIdx.x >> 5) & 3] : nullptr;
+    if constexpr (GATHER) {
+      if (perm != nullptr) {  // one coalesced read of the block's indices; bad ones become -1
+        __syncwarp();  // every lane is done with the previous block's indices
+        for (int u = lane; u < n; u += 32) {
+          const int src = __ldg(perm + idx * rows + u);
+          const bool good = static_cast<unsigned>(src) < static_cast<unsigned>(ntok);
+          if (!good) record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
+          wperm[u] = good ? src : -1;
+        }
+        __syncwarp();
+      }
+    }
     auto load = [&](int s) {
       const int t = s * TPW + sub;
-      return (t < n) ? ld_stream_v4(p + static_cast<int64_t>(s) * TPW * sn) : make_uint4(0, 0, 0, 0);
+      if (t >= n) return make_uint4(0, 0, 0, 0);
+      if (!GATHER || perm == nullptr) return ld_stream_v4(p + static_cast<int64_t>(s) * TPW * sn);
+      const int src = wperm[t];
+      return src >= 0 ? ld_stream_v4(hbase + static_cast<int64_t>(src) * sn) : make_uint4(0, 0, 0, 0);
     };
-    uint4 buf[INFLIGHT];
+    uint4 buf[IFL];
 #pragma unroll
-    for (int u = 0; u < INFLIGHT; ++u) buf[u] = load(u);
+    for (int u = 0; u < IFL; ++u) buf[u] = load(u);
     float2 sx2[4], sh2[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) sx2[c] = sh2[c] = make_float2(0.f, 0.f);
-    for (int s0 = 0; s0 < steps; s0 += INFLIGHT) {
+    for (int s0 = 0; s0 < steps; s0 += IFL) {
 #pragma unroll
-      for (int u = 0; u < INFLIGHT; ++u) {
+      for (int u = 0; u < IFL; ++u) {
         const uint4 v = buf[u];
-        if (s0 + INFLIGHT + u < steps) buf[u] = load(s0 + INFLIGHT + u);
+        if (s0 + IFL + u < steps) buf[u] = load(s0 + IFL + u);
         const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
         float2 x2[4];
 #pragma unroll
@@ -145,7 +173,8 @@ __global__ void __launch_bounds__(128, 5) pool_sim_kernel(PoolArgs a) {
 
 }  // namespace
 
-cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, cudaStream_t st) {
+cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, cudaStream_t st, const int32_t *qperm,
+                            const int32_t *kperm, int *status) {
   PoolArgs a;
   a.q = static_cast<const __nv_bfloat16 *>(q.data);
   a.k = static_cast<const __nv_bfloat16 *>(k.data);
@@ -159,17 +188,29 @@ cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, c
   a.nq_total = static_cast<int64_t>(a.B) * a.Hq * a.nqb;
   a.total = a.nq_total + static_cast<int64_t>(a.B) * a.Hkv * a.nkb;
   a.ws = ws;
+  a.qperm = qperm;
+  a.kperm = kperm;
+  a.status = status;
   if (a.total == 0) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t want = (a.total + 3) / 4;
-  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 5;  // 5 resident CTAs of 4 warps per SM
+  const bool gather = qperm != nullptr || kperm != nullptr;
+  // 5 resident CTAs of 4 warps per SM (4 when gathering through a token order: more registers)
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * (gather ? 4 : 5);
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  if (q.d == 128)
-    pool_sim_kernel<128><<<grid, 128, 0, st>>>(a);
-  else
-    pool_sim_kernel<64><<<grid, 128, 0, st>>>(a);
+  if (q.d == 128) {
+    if (gather)
+      pool_sim_kernel<128, true><<<grid, 128, 0, st>>>(a);
+    else
+      pool_sim_kernel<128, false><<<grid, 128, 0, st>>>(a);
+  } else {
+    if (gather)
+      pool_sim_kernel<64, true><<<grid, 128, 0, st>>>(a);
+    else
+      pool_sim_kernel<64, false><<<grid, 128, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

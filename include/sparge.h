@@ -125,10 +125,12 @@ typedef struct sparge_params {
    * token_order[t] of q, k and v: blocks, mask (and mask_out) refer to that sequence, and o is
    * written back in the original order (o token token_order[t] receives row t).  The result is
    * that of sparge_permute_tokens on q, k and v, the call, and sparge_unpermute_tokens on the
-   * output, without the separate V and output passes: the call copies Q and K into the
-   * workspace in the new order (sparge_workspace_bytes(op | SPARGE_OP_TOKEN_ORDER, ...)), gathers
-   * V while it converts or quantises it, and the attention kernel writes each output row
-   * straight to its original position.  token_order should be a permutation of 0..N-1; an entry
+   * output, without the separate V and output passes: the call copies K, and Q where d = 128 or
+   * an 8-bit precision needs it, into the workspace in the new order (the space is
+   * sparge_workspace_bytes(op | SPARGE_OP_TOKEN_ORDER, ...) either way); pooling and the d = 64
+   * attention read Q rows through the order instead, mask prediction alone copies nothing;
+   * V is gathered while it is converted or quantised, and the attention kernel writes each
+   * output row straight to its original position.  token_order should be a permutation of 0..N-1; an entry
    * outside that range is never used as an address (its row is skipped or zero) and records
    * SPARGE_ERR_INVALID_ARG in the device status word. */
   const int32_t *token_order;
@@ -146,8 +148,9 @@ typedef struct sparge_params {
  *   or e4m3 channel-major with the keys padded to a multiple of 64) and the fp32 scales;
  *   SPARGE_OP_ATTN_Q8: that plus the mask-prediction workspace and the mask.  Both return 0
  *   unless d = 128.
- * op | SPARGE_OP_TOKEN_ORDER: the op's bytes plus the bf16 copies of Q and K in a given token
- *   order (at the front of the workspace), for calls whose sparge_params.token_order is set.
+ * op | SPARGE_OP_TOKEN_ORDER: the op's bytes plus room for bf16 copies of Q and K in a given
+ *   token order (at the front of the workspace), for calls whose sparge_params.token_order is set
+ *   (a call uses only the copies it needs; the room is reserved in full).
  * Returns 0 for an unknown op or an unsupported shape.
  */
 size_t sparge_workspace_bytes(int op, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d);
