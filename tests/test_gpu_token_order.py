@@ -86,11 +86,14 @@ def test_token_order_matches_oracle():
     assert cos >= COS_MIN and err <= MAXABS, (cos, err)
 
 
-def test_token_order_entries_out_of_range_are_reported():
+@pytest.mark.parametrize("key", ["flux", "cogvideox"])
+def test_token_order_entries_out_of_range_are_reported(key):
     """Entries outside 0..N-1 are never used as addresses: the call finishes, the status word
     reports SPARGE_ERR_INVALID_ARG, output rows that no valid entry targets keep their old
-    contents, and every written row is finite (the ordered copies hold zero rows there)."""
-    w, perm_np = _make("flux")
+    contents, and every written row is finite (the ordered copies and the gathers read zero rows
+    there; at d = 64 Q is gathered, not copied).  Mask prediction alone (rows gathered by the
+    pooling, no copies) reports the same."""
+    w, perm_np = _make(key)
     bad = [0, 700, w.N - 1]
     perm_np = perm_np.copy()
     lost = perm_np[bad].copy()              # tokens no entry points at any more
@@ -108,3 +111,7 @@ def test_token_order_entries_out_of_range_are_reported():
     assert (o[:, :, lost] == 5.0).all()
     written = np.setdiff1d(np.arange(w.N), lost)
     assert np.isfinite(o[:, :, written]).all() and not (o[:, :, written] == 5.0).all()
+    m = fbs.predict_mask_ex(q, k, w.topk, w.causal, theta=w.theta, token_order=perm)
+    torch.cuda.synchronize()
+    assert fbs.device_status() == fbs.SPARGE_ERR_INVALID_ARG
+    assert m.shape == (w.B, w.Hq, w.nqb, w.nkb)
