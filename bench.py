@@ -21,6 +21,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -105,7 +106,8 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+        # the raw samples (nvidia-smi CSV); SPARGE_CLOCKS_CSV picks where they go
+        self.path = os.environ.get("SPARGE_CLOCKS_CSV") or os.path.join(tempfile.gettempdir(), "sparge_clocks_bench.csv")
 
     def start(self):
         try:
