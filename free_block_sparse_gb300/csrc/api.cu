@@ -296,7 +296,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   const bool q8 = is_q8(precision), pv8 = precision == SPARGE_PRECISION_Q8_FP8PV;
   if (q8 && q.d != 128) return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path needs d = 128 (got %lld)", (long long)q.d);
   if (q8 && k.N > 65535LL * 64) return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path supports Nk <= %lld", 65535LL * 64);
-  View ov;
+  View ov{};
   int rc = check_tensor(o, "o", &ov);
   if (rc) return rc;
   if ((rc = check_lengths(q, k, causal))) return rc;
