@@ -466,6 +466,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(&cs.j_empty[js]);
       if (j < 0) {  // tell the P.V issuer: phase t of p_full carries no tile (t = T, the tile count)
+        // That is one more phase of p_full[t % NSB], with no score product before it: its previous
+        // phase (tile t - NSB) must have been taken by the P.V issuer first, or both complete
+        // before the issuer's parity wait for the earlier one, which then never passes.
+        if (t >= NSB && !mbar_wait(&cs.pv_done[t % NSB], ((t - NSB) / NSB) & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
         if (r == 0) cs.row_end = t;
         mbar_arrive(&cs.p_full[t % NSB]);
         break;
