@@ -230,3 +230,127 @@ def test_checker_catches_the_former_o_done_aliasing():
     assert caught > 0
     for seed in range(200):   # the per-buffer barrier the kernel waits on instead
         Model(12, 4, 3, NSB=3, rescale_on="buffer", seed=seed).run()
+
+
+class GemmModel:
+    """The pooled-score GEMM's protocol (free_block_sparse_gb300/csrc/score_gemm.cu) for one CTA of
+    nch chunks: a producer loading K chunks into a 2-stage ring, an MMA issuer writing two TMEM
+    accumulators in turn, and the epilogue warps that read an accumulator, stage the scores in the
+    K stage whose products have completed and store them by TMA.  A stage returns to the producer
+    only after both the chunk's products and the stores out of it are done (k_empty counts 2)."""
+
+    def __init__(self, nch, seed=0, KST=2):
+        self.nch, self.KST = nch, KST
+        self.rng = random.Random(seed)
+        B = Barrier
+        self.q_full = B(1)
+        self.k_full = [B(1) for _ in range(KST)]
+        self.k_empty = [B(2) for _ in range(KST)]
+        self.acc_full = [B(1) for _ in range(2)]
+        self.acc_empty = [B(128) for _ in range(2)]
+        self.order = {"mma": [], "tma": [], "store": []}
+        self.stage_users = [set() for _ in range(KST)]  # who still reads or writes each K stage
+        self.acc_users = [set() for _ in range(2)]
+        self.wait = Model.wait.__get__(self)
+
+    def complete_one(self):
+        live = [t for t, q in self.order.items() if q]
+        if not live:
+            return False
+        t = self.rng.choice(live)
+        i = self.rng.randrange(len(self.order[t])) if t == "tma" else 0
+        for f in self.order[t].pop(i):
+            f()
+        return True
+
+    def producer(self):
+        self.q_full.arrive()
+        yield
+        for ch in range(self.nch):
+            st = ch % self.KST
+            while ch >= self.KST and not self.wait(self.k_empty[st], ch // self.KST - 1):
+                yield
+            assert not self.stage_users[st], ("stage reloaded while in use", ch, self.stage_users[st])
+            self.stage_users[st].add(("load", ch))
+
+            def landed(st=st, ch=ch):
+                self.stage_users[st].discard(("load", ch))
+                self.k_full[st].arrive()
+            self.order["tma"].append([landed])
+            yield
+
+    def mma(self):
+        while not self.wait(self.q_full, 0):
+            yield
+        for ch in range(self.nch):
+            st, ab = ch % self.KST, ch & 1
+            while not self.wait(self.k_full[st], ch // self.KST):
+                yield
+            while ch >= 2 and not self.wait(self.acc_empty[ab], ch // 2 - 1):
+                yield
+            assert not self.acc_users[ab], ("accumulator overwritten while read", ch)
+            self.stage_users[st].add(("mma", ch))
+
+            def done(st=st, ab=ab, ch=ch):
+                self.stage_users[st].discard(("mma", ch))
+                self.k_empty[st].arrive()
+                self.acc_users[ab].add(("epi", ch))
+                self.acc_full[ab].arrive()
+            self.order["mma"].append([done])
+            yield
+
+    def epilogue(self):
+        for ch in range(self.nch):
+            st, ab = ch % self.KST, ch & 1
+            while not self.wait(self.acc_full[ab], ch // 2):
+                yield
+            yield  # reads the accumulator, writes the scores into the stage
+            assert not any(u[0] != "store" for u in self.stage_users[st]), ("stage still in use", ch)
+            self.acc_users[ab].discard(("epi", ch))
+            for _ in range(128):
+                self.acc_empty[ab].arrive()
+            self.stage_users[st].add(("store", ch))
+
+            def stored(st=st, ch=ch):
+                self.stage_users[st].discard(("store", ch))
+            self.order["store"].append([stored])
+            while self.order["store"]:  # the stores have read the stage
+                yield
+            self.k_empty[st].arrive()
+
+    def run(self, max_steps=100000):
+        live = [self.producer(), self.mma(), self.epilogue()]
+        for _ in range(max_steps):
+            if not live and not any(self.order.values()):
+                return
+            if any(self.order.values()) and (not live or self.rng.random() < 0.4):
+                self.complete_one()
+                continue
+            r = self.rng.choice(live)
+            try:
+                next(r)
+            except StopIteration:
+                live.remove(r)
+        raise AssertionError("no progress: the protocol did not finish")
+
+
+@pytest.mark.parametrize("nch", [1, 2, 3, 4, 7, 16])
+def test_score_gemm_protocol(nch):
+    for seed in range(80):
+        GemmModel(nch, seed=100 * nch + seed).run()
+
+
+def test_gemm_checker_catches_a_stage_returned_early():
+    """With k_empty counting one arrival instead of two, the products' arrival alone returns a K
+    stage to the producer while the previous chunk's scores may still be stored out of it (and
+    the epilogue's own arrival then completes an extra phase): the model reports a stage reloaded
+    in use or a parity wait off by a phase."""
+    caught = 0
+    for seed in range(300):
+        m = GemmModel(8, seed=seed)
+        m.k_empty = [Barrier(1) for _ in range(m.KST)]
+        try:
+            m.run()
+        except AssertionError:
+            caught += 1
+    assert caught > 0
