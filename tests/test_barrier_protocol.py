@@ -34,8 +34,9 @@ class Aliased(AssertionError):
 class Model:
     """The kernel's protocol for one CTA and a row of T kept tiles."""
 
-    def __init__(self, T, KST, VST, NSB=2, JRING=8, rescale_on="buffer", seed=0):
+    def __init__(self, T, KST, VST, NSB=2, JRING=8, rescale_on="buffer", seed=0, s_waits_pv=True):
         self.T, self.KST, self.VST, self.NSB, self.J = T, KST, VST, NSB, JRING
+        self.s_waits_pv = s_waits_pv
         self.rescale_on = rescale_on
         self.rng = random.Random(seed)
         B = Barrier
@@ -52,8 +53,12 @@ class Model:
         self.q_full = B(128)
         self.mma_done = B(1)
         self.row_end = -1
-        self.async_ops = []    # pending completions: (thread, list of barriers to arrive on)
-        self.order = {"s": [], "pv": [], "tma": []}
+        self.order = {"s": [], "pv": [], "tma": []}  # pending completions per issuing thread
+        # data hazards: pending users of each score buffer, K and V stage, and pending P.V products
+        self.sbuf = [set() for _ in range(NSB)]
+        self.kst_busy = [set() for _ in range(KST)]
+        self.vst_busy = [set() for _ in range(VST)]
+        self.pv_pending = set()
 
     # a parity wait for phase k: returns True when done, False to keep waiting; raises on aliasing
     def wait(self, bar, k):
@@ -77,7 +82,7 @@ class Model:
         # each issuer's products complete in its issue order; TMA copies in any order
         i = self.rng.randrange(len(self.order[t])) if t == "tma" else 0
         for b in self.order[t].pop(i):
-            b.arrive()
+            b() if callable(b) else b.arrive()
         return True
 
     # ---- roles as generators: each yield is one step; a wait yields until it passes
@@ -97,6 +102,7 @@ class Model:
             self.jk = getattr(self, "jk", {})
             self.jk[t % KST] = j
             if j >= 0:
+                assert not self.kst_busy[t % KST], ("K stage reloaded under a score product", t)
                 self.issue("tma", [self.k_full[t % KST]])
             else:
                 self.k_full[t % KST].arrive()
@@ -105,6 +111,7 @@ class Model:
                 u = t - 1
                 while u >= VST and not self.wait(self.v_empty[u % VST], u // VST - 1):
                     yield
+                assert not self.vst_busy[u % VST], ("V stage reloaded under a P.V product", u)
                 self.issue("tma", [self.v_full[u % VST]])
                 yield
             jprev = j
@@ -122,10 +129,13 @@ class Model:
             if u == 0:
                 while not self.wait(self.q_full, 0):
                     yield
-            elif u >= NSB:
+            elif u >= NSB and self.s_waits_pv:
                 while not self.wait(self.pv_done[u % NSB], (u - NSB) // NSB):
                     yield
-            self.issue("s", [self.s_full[u % NSB], self.k_empty[u % KST]])
+            assert not self.sbuf[u % NSB], ("score buffer overwritten in use", u, self.sbuf[u % NSB])
+            self.kst_busy[u % KST].add(u)
+            self.issue("s", [lambda u=u: self.kst_busy[u % KST].discard(u), self.s_full[u % NSB],
+                             self.k_empty[u % KST]])
             yield
             u += 1
         self.s_count = u
@@ -140,7 +150,15 @@ class Model:
                 break
             while not self.wait(self.v_full[t % VST], t // VST):
                 yield
-            self.issue("pv", [self.v_empty[t % VST], self.o_done, self.pv_done[t % NSB]])
+            self.sbuf[t % NSB].add(("pv", t))
+            self.vst_busy[t % VST].add(t)
+            self.pv_pending.add(t)
+
+            def pv_complete(t=t):
+                self.sbuf[t % NSB].discard(("pv", t))
+                self.vst_busy[t % VST].discard(t)
+                self.pv_pending.discard(t)
+            self.issue("pv", [pv_complete, self.v_empty[t % VST], self.o_done, self.pv_done[t % NSB]])
             yield
             t += 1
         # the final completion, then the epilogue may read O
@@ -172,6 +190,7 @@ class Model:
                 break
             while not self.wait(self.s_full[t % NSB], t // NSB):
                 yield
+            self.sbuf[t % NSB].add(("softmax", t))
             if t > 0 and self.rng.random() < 0.3:  # a rescale of O needs P.V of tile t - 1 complete
                 if self.rescale_on == "buffer":
                     while not self.wait(self.pv_done[(t - 1) % NSB], (t - 1) // NSB):
@@ -179,7 +198,9 @@ class Model:
                 else:
                     while not self.wait(self.o_done, t - 1):
                         yield
+                assert not any(x < t for x in self.pv_pending), ("O rescaled under a P.V product", t)
             yield
+            self.sbuf[t % NSB].discard(("softmax", t))
             for _ in range(128):
                 self.p_full[t % NSB].arrive()
             yield
@@ -187,6 +208,7 @@ class Model:
         if t > 0:
             while not self.wait(self.mma_done, 0):
                 yield
+            assert not self.pv_pending, "epilogue reads O under a P.V product"
         self.tiles = t
 
     def run(self, max_steps=200000):
@@ -353,4 +375,16 @@ def test_gemm_checker_catches_a_stage_returned_early():
             m.run()
         except AssertionError:
             caught += 1
+    assert caught > 0
+
+
+def test_checker_catches_a_score_product_over_a_pending_p():
+    """A score issuer that did not wait for P.V of tile u - 2 would overwrite P while that product
+    may still read it; the model's buffer bookkeeping reports it."""
+    caught = 0
+    for seed in range(300):
+        try:
+            Model(10, 3, 2, seed=seed, s_waits_pv=False).run()
+        except AssertionError as e:
+            caught += "overwritten" in str(e)
     assert caught > 0
