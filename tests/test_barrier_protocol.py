@@ -1,14 +1,16 @@
-"""Host model of the attention kernel's barrier protocol (free_block_sparse_gb300/csrc/bsattn.cu).
+"""Host models of the barrier protocols of the two tcgen05 kernels (free_block_sparse_gb300/csrc/
+bsattn.cu and score_gemm.cu).
 
 A parity wait on an mbarrier (try_wait.parity with the parity of phase k) is only right when the
 barrier has completed either exactly k phases (not yet: keep waiting) or k + 1 (done).  With k - 1
-completed phases the parities alias and the wait passes early; with k + 2 it never passes.  This
-model runs the kernel's roles - producer, score issuer, P.V issuer and the softmax warps - against
-counters of completed phases, with the tensor-core products and TMA copies completing
-asynchronously (each issuing thread's products in its own issue order, no order between the two
-issuers), under random schedules, and checks that invariant at every wait and that every schedule
-finishes.  A second model puts back the single P.V-completion barrier that the O rescale once
-waited on and shows that with three score buffers the checker catches the aliasing."""
+completed phases the parities alias and the wait passes early; with k + 2 it never passes.  The
+models run each kernel's roles against counters of completed phases, with the tensor-core
+products completing asynchronously in each issuing thread's order (no order between two issuers)
+and TMA copies in any order, under random schedules.  They check that invariant at every wait,
+that every schedule finishes, and the data hazards themselves (a buffer or stage overwritten while
+a product or the softmax still uses it).  Planted mistakes - the former single P.V-completion
+barrier with three score buffers, a score issuer that skips its wait, a GEMM stage released by one
+arrival - show that the checks fire."""
 import random
 
 import pytest
