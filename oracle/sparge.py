@@ -210,19 +210,34 @@ def row_decisive(p: np.ndarray, valid: np.ndarray, sq: float, sk: np.ndarray, to
         return False
     if topk >= 1.0:
         return True
+    m = cut_margins(p, valid, topk, mode)
+    if mode == "count":
+        return bool(m["kstar"] >= m["n"] or m["gap"] > eps)
+    return bool(abs(m["c_at"] - topk) > eps and abs(topk - m["c_before"]) > eps and m["gap"] > eps)
+
+
+def cut_margins(p: np.ndarray, valid: np.ndarray, topk: float, mode: str = "cdf") -> Dict[str, float]:
+    """Where the top-k cut of one row falls and how far it is from moving (topk < 1).
+
+    Returns the valid blocks in (probability desc, index asc) order ("order"), their count n,
+    the number kept by the cut ("kstar", as topk_select), the probability of the last kept block
+    ("p_cut") and of the first dropped one ("p_next", 0 if none), their difference ("gap"), and
+    the cumulative probability through the cut ("c_at") and through the block before it
+    ("c_before", 0 if none)."""
     vj = np.nonzero(valid)[0]
     order = vj[np.lexsort((vj, -p[vj]))]
     ps = p[order]
-    if mode == "count":
-        kc = count_target(topk, order.size)
-        return bool(kc >= ps.size or ps[kc - 1] - ps[kc] > eps)
     c = np.cumsum(ps)
-    hit = np.nonzero(c >= topk)[0]
-    kstar = (hit[0] + 1) if hit.size else order.size
-    c_at = c[kstar - 1]
-    c_before = c[kstar - 2] if kstar >= 2 else 0.0
-    gap = ps[kstar - 1] - (ps[kstar] if kstar < ps.size else 0.0)
-    return bool(abs(c_at - topk) > eps and abs(topk - c_before) > eps and gap > eps)
+    if mode == "count":
+        kstar = count_target(topk, order.size)
+    else:
+        assert mode == "cdf", mode
+        hit = np.nonzero(c >= topk)[0]
+        kstar = int(hit[0] + 1) if hit.size else order.size
+    p_next = float(ps[kstar]) if kstar < ps.size else 0.0
+    return dict(order=order, n=int(order.size), kstar=int(kstar), p_cut=float(ps[kstar - 1]), p_next=p_next,
+                gap=float(ps[kstar - 1]) - p_next, c_at=float(c[kstar - 1]),
+                c_before=float(c[kstar - 2]) if kstar >= 2 else 0.0)
 
 
 def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal: bool,
@@ -241,27 +256,37 @@ def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal
     return out
 
 
+def pool_key_head(k_head: np.ndarray):
+    """Pooled means and similarities of every 64-key block of one key/value head, (nkb, d) and
+    (nkb,): the key half of stage 1, computed once and shared by the rows of that head."""
+    muk, sk = pool_sim(k_head[None, None], KBLK)
+    return muk[0, 0], sk[0, 0]
+
+
 def predict_mask_row(q_block: np.ndarray, k_head: np.ndarray, i: int, topk: float, theta: float,
-                     causal: bool, scale: float = None, mode: str = "cdf", off: int = 0) -> Dict[str, np.ndarray]:
+                     causal: bool, scale: float = None, mode: str = "cdf", off: int = 0,
+                     k_pool=None) -> Dict[str, np.ndarray]:
     """predict_mask for a single query block: q_block (n_i, d) the tokens of query block i,
     k_head (N, d) every key of its key/value head.  Same steps as predict_mask, for checking
-    rows of workloads too large to run whole.  Returns mask (nkb,) uint8, P (nkb,), sQ (float),
-    sK (nkb,), valid (nkb,) bool."""
+    rows of workloads too large to run whole.  k_pool, if given, is pool_key_head(k_head),
+    so that many rows of one head pool its keys once.  Returns mask (nkb,) uint8, P (nkb,),
+    S (nkb,) the scaled pooled scores (-inf on invalid blocks), muQ (d,) and sQ (float) of the
+    query block, sK (nkb,), valid (nkb,) bool."""
     N, d = k_head.shape
     if scale is None:
         scale = default_scale(d)
     muq, sq = pool_sim(q_block[None, None], QBLK)
-    muk, sk = pool_sim(k_head[None, None], KBLK)
-    nkb = muk.shape[2]
+    muk, sk = pool_key_head(k_head) if k_pool is None else k_pool
+    nkb = muk.shape[0]
     valid = block_valid(i + 1, nkb, causal, off)[i]
-    s = scale * (muk[0, 0] @ muq[0, 0, 0])
+    s = scale * (muk @ muq[0, 0, 0])
     s[~valid] = -np.inf
     p = row_softmax(s)
     keep = topk_select(p, valid, topk, mode)
     if sq[0, 0, 0] < theta:
         keep |= valid
-    keep |= (sk[0, 0] < theta) & valid
-    return dict(mask=keep.astype(np.uint8), P=p, sQ=float(sq[0, 0, 0]), sK=sk[0, 0], valid=valid)
+    keep |= (sk < theta) & valid
+    return dict(mask=keep.astype(np.uint8), P=p, S=s, muQ=muq[0, 0, 0], sQ=float(sq[0, 0, 0]), sK=sk, valid=valid)
 
 
 # ---------------------------------------------------------------------------------------------

@@ -16,6 +16,7 @@ import free_block_sparse_gb300 as fbs
 import oracle
 import workloads as W
 from gpu_util import COS_MIN, MAXABS, cos_maxabs, dev_bf16, f64
+from mask_checks import EPS_SIM, cut_violations, decisive, score_error_bound, slack
 
 pytestmark = pytest.mark.gpu
 
@@ -54,55 +55,59 @@ def _check_whole_mask(w, gm):
     assert (gm.sum(axis=-1) >= 1).all(), "a row keeps no block"
 
 
-def _check_cut_properties(w, pr, row, where, eps=1e-3):
-    """What any correct cut satisfies on a row whose cut rounding may move: the always-keep
-    blocks are kept, the kept mass reaches topk (within eps), no kept top-k block is more than
-    eps below the oracle's cut probability and no dropped block more than eps above it."""
-    valid, p, sk = pr["valid"], pr["P"], pr["sK"]
-    kept = row.astype(bool)
-    assert not (kept & ~valid).any(), where
-    if pr["sQ"] < w.theta - eps:
-        assert kept[valid].all(), where
-        return
-    assert kept[valid & (sk < w.theta - eps)].all(), where
-    assert p[kept].sum() >= min(1.0, w.topk) - eps, where
-    if w.topk >= 1.0:
-        return
-    order = np.nonzero(valid)[0]
-    order = order[np.lexsort((order, -p[order]))]
-    c = np.cumsum(p[order])
-    kstar = int(np.nonzero(c >= w.topk)[0][0]) + 1 if (c >= w.topk).any() else order.size
-    p_cut = p[order[kstar - 1]]
-    topk_part = kept & valid & ~(sk < w.theta + eps)  # blocks kept for their probability
-    assert (p[topk_part] >= p_cut - eps).all(), where
-    assert (p[valid & ~kept] <= p_cut + eps).all(), where
-
-
-def _check_block(w, gm, got, b, h, i, lam, predicted, cos_min=COS_MIN, maxabs=MAXABS):
-    kvh = h // (w.Hq // w.Hkv)
-    kh, vh = f64(w.k[b, kvh]), f64(w.v[b, kvh])
+def _check_attention(w, gm, got, b, h, i, lam, kh, vh, cos_min=COS_MIN, maxabs=MAXABS):
+    """The output rows of query block (b, h, i) against the oracle's single-block attention over
+    the GPU's mask row."""
     qi = _block(w.q, b, h, i)
-    row = gm[b, h, i]
-    decisive = False
-    if predicted:
-        pr = oracle.predict_mask_row(qi, kh, i, w.topk, w.theta, w.causal)
-        decisive = oracle.row_decisive(pr["P"], pr["valid"], pr["sQ"], pr["sK"], w.topk, w.theta)
-        if decisive:
-            assert np.array_equal(row, pr["mask"]), (b, h, i)
-        else:
-            _check_cut_properties(w, pr, row, (b, h, i))
     valid = oracle.block_valid(w.nqb, w.nkb, w.causal)[i]
-    kept = np.nonzero(row.astype(bool) & valid)[0]
+    kept = np.nonzero(gm[b, h, i].astype(bool) & valid)[0]
     ref, _ = oracle.attn_qblock(qi, kh, vh, i, kept, lam, w.causal, oracle.default_scale(w.d))
     g = got[b, h, i * 128:i * 128 + qi.shape[0]].float().cpu().numpy().astype(np.float64)
     cos, err = cos_maxabs(g, ref)
     assert cos >= cos_min and err <= maxabs, ((b, h, i), cos, err)
-    return decisive
 
 
-@pytest.mark.parametrize("name,nsamp", [("llama128k", 12), ("llama32k", 12), ("flux", 8), ("cogvideox", 8),
-                                         ("vit", 8)])
-def test_full_size_predicted_mask_and_attention(name, nsamp):
+def _check_mask_rows(w, gm, ws, rows, kh, kvh_pool, b):
+    """Mask rows (b, h, i) of one key/value head against the oracle's single-row prediction.
+
+    The library's pooled scores, s_Q and s_K (read from its workspace) are first held to the
+    bounds the slack is derived from (mask_checks).  Rows that no rounding within the slack can
+    change are compared bit for bit; the others must satisfy what a correct cut satisfies
+    (cut_violations).  Returns (rows decisive under the derived slack, rows decisive under the
+    absolute 1e-3 margins)."""
+    S_v, sQ_v, sK_v = ws
+    scale = oracle.default_scale(w.d)
+    n_rel = n_abs = 0
+    for h, i in rows:
+        pr = oracle.predict_mask_row(_block(w.q, b, h, i), kh, i, w.topk, w.theta, w.causal, k_pool=kvh_pool)
+        valid = pr["valid"]
+        E = score_error_bound(pr["muQ"], kvh_pool[0], pr["S"], valid, scale)
+        s_gpu = S_v[(b, h, i)]
+        err = np.abs(s_gpu[valid] - pr["S"][valid])
+        assert (err <= E[valid]).all(), ("pooled scores outside their bound", (b, h, i), float((err - E[valid]).max()))
+        assert abs(sQ_v[(b, h, i)] - pr["sQ"]) <= EPS_SIM, (b, h, i)
+        assert np.abs(sK_v[b][valid] - pr["sK"][valid]).max(initial=0.0) <= EPS_SIM, (b, h, i)
+        eps_rel, eps_mass = slack(E)
+        row = gm[b, h, i]
+        if decisive(pr, w.topk, w.theta, eps_rel, eps_mass):
+            assert np.array_equal(row, pr["mask"]), ("decisive row differs", (b, h, i))
+            n_rel += 1
+        else:
+            bad = cut_violations(pr, row, w.topk, w.theta, eps_rel, eps_mass)
+            assert not bad, ((b, h, i), bad)
+        n_abs += oracle.row_decisive(pr["P"], valid, pr["sQ"], pr["sK"], w.topk, w.theta)
+    return n_rel, n_abs
+
+
+# mask rows and attention blocks checked per workload, and the mask rows that must be compared
+# bit for bit (decisive under the derived slack)
+FULL_SIZE = {"llama128k": (320, 12, 100), "llama32k": (160, 12, 60), "flux": (96, 8, 20),
+             "cogvideox": (96, 8, 20), "vit": (96, 8, 20)}
+
+
+@pytest.mark.parametrize("name", list(FULL_SIZE))
+def test_full_size_predicted_mask_and_attention(name):
+    n_mask, n_attn, n_dec_min = FULL_SIZE[name]
     w = _workload(name)
     q, k, v = dev_bf16(w.q), dev_bf16(w.k), dev_bf16(w.v)
     perm = None
@@ -123,13 +128,37 @@ def test_full_size_predicted_mask_and_attention(name, nsamp):
     if perm is not None:
         natural = fbs.unpermute_tokens(out, perm)
         assert torch.equal(fbs.permute_tokens(natural, perm), out)
+    # the prediction alone, with its workspace kept for the pooled scores and similarities
+    ws = torch.empty(fbs.workspace_bytes(fbs.SPARGE_OP_PREDICT_MASK, w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8,
+                     device="cuda")
+    mask2 = fbs.predict_mask(q, k, w.topk, w.theta, w.causal, ws=ws)
     torch.cuda.synchronize()
+    assert torch.equal(mask, mask2)
     gm = mask.cpu().numpy()
     _check_whole_mask(w, gm)
-    n_dec = sum(_check_block(w, gm, out, b, h, i, w.lam, predicted=True) for b, h, i in _samples(w, nsamp))
-    # at least one sampled row compared bit for bit (rows of many nearly equal block
-    # probabilities, as at 128K or in Hilbert order, are often not decisive)
-    assert n_dec >= 1, n_dec
+    muQ, sQ, muK, sK, S = fbs.predict_ws_views(ws, w.B, w.Hq, w.Hkv, w.N, w.d)
+    samples = _samples(w, n_mask)
+    S_v = {s: S[s].double().cpu().numpy() for s in set(samples)}
+    sQ_v = {s: float(sQ[s]) for s in set(samples)}
+    sK_h = sK.double().cpu().numpy()
+    G = w.Hq // w.Hkv
+    n_rel = n_abs = 0
+    attn_set = set(samples[:n_attn])
+    for b in range(w.B):
+        for kvh in range(w.Hkv):
+            rows = [(h, i) for (bb, h, i) in samples if bb == b and h // G == kvh]
+            if not rows:
+                continue
+            kh, vh = f64(w.k[b, kvh]), f64(w.v[b, kvh])
+            kp = oracle.pool_key_head(kh)
+            r, a = _check_mask_rows(w, gm, (S_v, sQ_v, {b: sK_h[b, kvh]}), rows, kh, kp, b)
+            n_rel += r
+            n_abs += a
+            for h, i in rows:
+                if (b, h, i) in attn_set:
+                    _check_attention(w, gm, out, b, h, i, w.lam, kh, vh)
+    print("%s: %d mask rows, %d bit-exact (derived slack), %d decisive at 1e-3" % (name, len(samples), n_rel, n_abs))
+    assert n_rel >= n_dec_min, (n_rel, n_dec_min)
 
 
 @pytest.mark.parametrize("prec,cos_min", [(fbs.SPARGE_PRECISION_BF16, COS_MIN), (fbs.SPARGE_PRECISION_Q8, 0.999),
@@ -143,4 +172,5 @@ def test_full_size_custom_mask(prec, cos_min):
     torch.cuda.synchronize()
     maxabs = MAXABS if prec == fbs.SPARGE_PRECISION_BF16 else math.inf
     for b, h, i in _samples(w, 6):
-        _check_block(w, w.mask, out, b, h, i, w.lam, predicted=False, cos_min=cos_min, maxabs=maxabs)
+        _check_attention(w, w.mask, out, b, h, i, w.lam, f64(w.k[b, h]), f64(w.v[b, h]), cos_min=cos_min,
+                         maxabs=maxabs)

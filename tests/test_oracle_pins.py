@@ -459,3 +459,59 @@ def test_decisive_rows_flag_near_ties():
     t = float(np.cumsum(np.sort(p)[::-1])[1])
     pred2 = oracle.predict_mask(q, k, t, 0.3, False)
     assert not oracle.decisive_rows(pred2, t, 0.3, False)[0, 0, 0]
+
+
+# ----------------------------------------------------------------------------------------------
+# single-row mask prediction (used on workloads too large to predict whole)
+# ----------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("mode", ["cdf", "count"])
+@pytest.mark.parametrize("causal,Nq,Nk,Hq,Hkv,topk,theta", [
+    (True, 1000, 1000, 4, 2, 0.5, 0.5),     # causal GQA, ragged tails of both block sizes
+    (False, 700, 700, 2, 2, 0.3, 0.6),      # non-causal
+    (True, 300, 1100, 4, 1, 0.6, 0.4),      # a short query chunk continuing a longer key sequence
+    (False, 900, 513, 2, 1, 0.9, 0.5),      # more queries than keys, non-causal
+])
+def test_predict_mask_row_equals_predict_mask(mode, causal, Nq, Nk, Hq, Hkv, topk, theta):
+    """predict_mask_row (one query block against one pooled key head) gives, on every row, the
+    mask, probabilities, scores and similarities of the pinned whole-tensor predict_mask, with the
+    key head pooled per call or once (k_pool)."""
+    w = W.make_config("tiny", B=1, Hq=Hq, Hkv=Hkv, N=max(Nq, Nk), d=64)
+    q = f64(w.q)[:, :, :Nq]
+    k = f64(w.k)[:, :, :Nk]
+    pred = oracle.predict_mask(q, k, topk, theta, causal, mode=mode)
+    off = Nk - Nq
+    G = Hq // Hkv
+    for h in range(Hq):
+        kp = oracle.pool_key_head(k[0, h // G])
+        for i in range(pred["mask"].shape[2]):
+            qb = q[0, h, i * 128:min(Nq, (i + 1) * 128)]
+            for pool in (None, kp):
+                r = oracle.predict_mask_row(qb, k[0, h // G], i, topk, theta, causal, mode=mode, off=off, k_pool=pool)
+                assert np.array_equal(r["mask"], pred["mask"][0, h, i]), (h, i)
+                np.testing.assert_allclose(r["P"], pred["P"][0, h, i], rtol=1e-12, atol=1e-15)
+                np.testing.assert_array_equal(np.isneginf(r["S"]), np.isneginf(pred["S"][0, h, i]))
+                fin = ~np.isneginf(r["S"])
+                np.testing.assert_allclose(r["S"][fin], pred["S"][0, h, i][fin], rtol=1e-12, atol=1e-12)
+                assert r["sQ"] == pytest.approx(pred["sQ"][0, h, i], abs=1e-14)
+                np.testing.assert_allclose(r["sK"], pred["sK"][0, h // G], rtol=0, atol=1e-14)
+                np.testing.assert_array_equal(r["valid"], oracle.block_valid(i + 1, r["valid"].size, causal, off)[i])
+
+
+def test_cut_margins_agree_with_topk_select():
+    """cut_margins places the cut where topk_select does, in both readings of topk."""
+    rng = np.random.default_rng(5)
+    for trial in range(200):
+        n = int(rng.integers(1, 40))
+        p = rng.dirichlet(np.full(n, 0.3))
+        valid = rng.random(n) < 0.8
+        valid[int(rng.integers(n))] = True
+        p = np.where(valid, p, 0.0)
+        p /= p.sum()
+        topk = float(rng.uniform(0.05, 0.95))
+        for mode in ("cdf", "count"):
+            keep = oracle.topk_select(p, valid, topk, mode)
+            m = oracle.cut_margins(p, valid, topk, mode)
+            assert keep.sum() == m["kstar"]
+            assert set(np.nonzero(keep)[0]) == set(m["order"][:m["kstar"]])
+            assert m["p_cut"] == p[keep].min()
+            assert m["c_at"] == pytest.approx(p[keep].sum(), abs=1e-12)
