@@ -27,6 +27,9 @@ SPARGE_BF16 = 1
 SPARGE_PRECISION_BF16 = 0
 SPARGE_PRECISION_Q8 = 1
 SPARGE_PRECISION_Q8_FP8PV = 2
+SPARGE_PRECISION_BF16_FP8PV = 3
+# precisions with an 8-bit product: d = 128 and the 8-bit workspace (SPARGE_OP_*_Q8)
+PRECISIONS_8BIT = (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV, SPARGE_PRECISION_BF16_FP8PV)
 SPARGE_OP_PREDICT_MASK = 1
 SPARGE_OP_BLOCK_SPARSE_ATTN = 2
 SPARGE_OP_ATTN = 3
@@ -35,6 +38,7 @@ SPARGE_OP_ATTN_Q8 = 5
 SPARGE_OP_TOKEN_ORDER = 0x100  # flag OR-ed into an op: room for token-ordered copies of Q and K
 SPARGE_TOPK_CUMULATIVE = 0      # topk is a cumulative probability fraction (default)
 SPARGE_TOPK_COUNT = 1           # topk is a fraction of the valid blocks to keep
+SPARGE_TOPK_HYBRID = 2          # the count set of topk united with the cumulative set of topp
 QBLK, KBLK = 128, 64
 
 
@@ -54,7 +58,8 @@ class sparge_params(ctypes.Structure):
     _fields_ = [("theta", ctypes.c_float), ("lambda_", ctypes.c_float), ("scale", ctypes.c_float),
                 ("precision", ctypes.c_int32), ("stats", ctypes.c_void_p), ("timing_events", ctypes.c_void_p),
                 ("topk_per_head", ctypes.c_void_p), ("theta_per_head", ctypes.c_void_p),
-                ("lambda_per_head", ctypes.c_void_p), ("token_order", ctypes.c_void_p), ("topk_mode", ctypes.c_int32)]
+                ("lambda_per_head", ctypes.c_void_p), ("token_order", ctypes.c_void_p), ("topk_mode", ctypes.c_int32),
+                ("topp", ctypes.c_float)]
 
 
 _lib = None
@@ -164,18 +169,18 @@ def predict_mask(q, k, topk: float, theta: float = 0.5, causal: bool = False, ws
 
 def predict_mask_ex(q, k, topk: float, causal: bool = False, theta: float = 0.5, scale: float = 0.0,
                     topk_per_head=None, theta_per_head=None, ws=None, mask=None, events=None, token_order=None,
-                    topk_mode: int = SPARGE_TOPK_CUMULATIVE):
+                    topk_mode: int = SPARGE_TOPK_CUMULATIVE, topp: float = 1.0):
     """predict_mask with an explicit pooled-score scale, optional per-query-head topk and theta
-    (float32 CUDA tensors of Hq entries), optional timing events ([0]-[3] are recorded) and an
+    (float32 CUDA tensors of Hq entries), optional timing events ([0]-[3] are recorded), an
     optional token order (int32 CUDA tensor of N entries; the mask refers to the reordered
-    sequence)."""
+    sequence) and the reading of topk (topk_mode; topp is the top-p mass of the hybrid rule)."""
     torch = _torch()
     B, Hq, Nq, _ = q.shape
     if mask is None:
         mask = torch.empty((B, Hq, -(-Nq // 128), -(-k.shape[2] // 64)), dtype=torch.uint8, device=q.device)
     ws = _workspace(SPARGE_OP_PREDICT_MASK | (SPARGE_OP_TOKEN_ORDER if token_order is not None else 0), q, k, ws)
     p = _params(theta, -math.inf, scale, SPARGE_PRECISION_BF16, None, events, topk_per_head, theta_per_head,
-                order=token_order, topk_mode=topk_mode)
+                order=token_order, topk_mode=topk_mode, topp=topp)
     dq, dk = _desc(q), _desc(k)
     _check(lib().sparge_predict_mask_ex(ctypes.byref(dq), ctypes.byref(dk), float(topk), int(causal), ctypes.byref(p),
                                         mask.data_ptr(), ws.data_ptr(), ws.numel(), _stream()))
@@ -241,13 +246,13 @@ def q8_ws_views(ws, B, Hq, Hkv, N, d):
 def block_sparse_attn(q, k, v, mask=None, lam: float = -math.inf, causal: bool = False, out=None, stats=None,
                       precision: int = SPARGE_PRECISION_BF16, ws=None):
     """Stage 2: attention over the kept 128x64 tiles with the lambda warp filter.
-    precision SPARGE_PRECISION_Q8 (e4m3 Q.K^T, f16 P.V) or SPARGE_PRECISION_Q8_FP8PV (both
-    products e4m3) runs the 8-bit path (d = 128); its workspace then holds the quantised copies
-    and scales (see q8_ws_views)."""
+    precision SPARGE_PRECISION_Q8 (e4m3 Q.K^T, f16 P.V), SPARGE_PRECISION_Q8_FP8PV (both
+    products e4m3) or SPARGE_PRECISION_BF16_FP8PV (bf16 Q.K^T, e4m3 P.V) runs an 8-bit path
+    (d = 128); its workspace then holds the quantised copies and scales (see q8_ws_views)."""
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
-    op = SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 if precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV) \
+    op = SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 if precision in PRECISIONS_8BIT \
         else SPARGE_OP_BLOCK_SPARSE_ATTN
     ws = _workspace(op, q, k, ws)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
@@ -294,7 +299,7 @@ def _order_ptr(order):
 
 
 def _params(theta, lam, scale, precision, stats, events, topk_h=None, theta_h=None, lam_h=None, order=None,
-            topk_mode=0):
+            topk_mode=0, topp=1.0):
     """A sparge_params; `events` (6 torch.cuda.Event or None) are passed as cudaEvent_t handles.
     The handle array is kept on the returned struct so it outlives the call.  topk_h, theta_h and
     lam_h are optional per-query-head float32 CUDA tensors; order an optional int32 token order."""
@@ -309,7 +314,7 @@ def _params(theta, lam, scale, precision, stats, events, topk_h=None, theta_h=No
                       0 if stats is None else stats.data_ptr(),
                       ctypes.cast(evp, ctypes.c_void_p) if evp is not None else None,
                       _head_array(topk_h, "topk_per_head"), _head_array(theta_h, "theta_per_head"),
-                      _head_array(lam_h, "lambda_per_head"), _order_ptr(order), int(topk_mode))
+                      _head_array(lam_h, "lambda_per_head"), _order_ptr(order), int(topk_mode), float(topp))
     p._evp = evp
     p._arrays = (topk_h, theta_h, lam_h, order)
     return p
@@ -326,7 +331,7 @@ def block_sparse_attn_ex(q, k, v, mask=None, causal: bool = False, lam: float = 
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
-    op = SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 if precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV) \
+    op = SPARGE_OP_BLOCK_SPARSE_ATTN_Q8 if precision in PRECISIONS_8BIT \
         else SPARGE_OP_BLOCK_SPARSE_ATTN
     ws = _workspace(op | (SPARGE_OP_TOKEN_ORDER if token_order is not None else 0), q, k, ws)
     p = _params(0.5, lam, scale, precision, stats, events, lam_h=lambda_per_head, order=token_order)
@@ -340,7 +345,7 @@ def block_sparse_attn_ex(q, k, v, mask=None, causal: bool = False, lam: float = 
 def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: float = -math.inf,
                    scale: float = 0.0, precision: int = SPARGE_PRECISION_BF16, stats=None, mask_out=None,
                    out=None, ws=None, events=None, topk_per_head=None, theta_per_head=None, lambda_per_head=None,
-                   token_order=None, topk_mode: int = SPARGE_TOPK_CUMULATIVE):
+                   token_order=None, topk_mode: int = SPARGE_TOPK_CUMULATIVE, topp: float = 1.0):
     """sparge_attn with explicit theta, lambda, scale, counters, an optional mask output,
     optional timing events (6 torch.cuda.Event, recorded around the five kernels), optional
     per-query-head topk, theta and lambda (float32 CUDA tensors of Hq entries) and an optional
@@ -349,11 +354,11 @@ def sparge_attn_ex(q, k, v, topk: float, causal: bool, theta: float = 0.5, lam: 
     torch = _torch()
     if out is None:
         out = torch.empty_like(q)
-    q8 = precision in (SPARGE_PRECISION_Q8, SPARGE_PRECISION_Q8_FP8PV)
+    q8 = precision in PRECISIONS_8BIT
     ws = _workspace((SPARGE_OP_ATTN_Q8 if q8 else SPARGE_OP_ATTN) | (SPARGE_OP_TOKEN_ORDER if token_order is not None else 0),
                     q, k, ws)
     p = _params(theta, lam, scale, precision, stats, events, topk_per_head, theta_per_head, lambda_per_head,
-                token_order, topk_mode)
+                token_order, topk_mode, topp)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     mp = 0 if mask_out is None else mask_out.data_ptr()
     _check(lib().sparge_attn_ex(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), float(topk), int(causal),

@@ -226,14 +226,25 @@ int order_qk(View &q, View &k, const int32_t *perm, void *&ws, size_t &ws_bytes,
 
 bool is_q8(int precision);
 // Under a token order Q gets an ordered copy only where TMA (d = 128) or the 8-bit quantiser reads
-// it; at d = 64 the attention loads Q rows itself and gathers them through the permutation.
+// it; at d = 64 the attention loads Q rows itself and gathers them through the permutation (the
+// 8-bit precisions need d = 128).
 bool order_copies_q(int64_t d, int precision) { return d != 64 || is_q8(precision); }
 
 // Per-query-head parameter arrays of a sparge_params (device pointers, each may be null).
 struct HeadParams {
   const float *topk = nullptr, *theta = nullptr, *lambda = nullptr;
   int topk_mode = SPARGE_TOPK_CUMULATIVE;  // how topk selects blocks (enum sparge_topk_mode)
+  float topp = 1.f;                        // the top-p mass of SPARGE_TOPK_HYBRID
 };
+
+// topk_mode and, for the hybrid rule, topp
+int check_topk_mode(const sparge_params *p) {
+  if (p->topk_mode != SPARGE_TOPK_CUMULATIVE && p->topk_mode != SPARGE_TOPK_COUNT && p->topk_mode != SPARGE_TOPK_HYBRID)
+    return fail(SPARGE_ERR_INVALID_ARG, "topk_mode %d unknown", p->topk_mode);
+  if (p->topk_mode == SPARGE_TOPK_HYBRID && !(p->topp > 0.f && p->topp <= 1.f))
+    return fail(SPARGE_ERR_INVALID_ARG, "topp=%g not in (0, 1]", (double)p->topp);
+  return SPARGE_OK;
+}
 
 int predict_impl(const View &q, const View &k, float topk, float theta, int causal, float scale, uint8_t *mask,
                  void *ws, size_t ws_bytes, cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {},
@@ -271,16 +282,26 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
     if (e != cudaSuccess) return cuda_fail(e, "score_gemm launch");
     if ((rc = record_event(ev, 2, s))) return rc;
   }
+  // the hybrid rule: the count reading with topk, then the cumulative reading with topp OR-ed into
+  // the same mask rows (the union of the two sets)
+  const bool hybrid = hp.topk_mode == SPARGE_TOPK_HYBRID;
   e = launch_score_select(pw, (int)q.B, (int)q.H, (int)k.H, (int)q.N, (int)k.N, (int)q.d, topk, theta, causal, mask, hp.topk,
-                          hp.theta, status_ptr(), hp.topk_mode == SPARGE_TOPK_COUNT ? 1 : 0, s);
+                          hp.theta, status_ptr(), hp.topk_mode != SPARGE_TOPK_CUMULATIVE ? 1 : 0, false, s);
+  if (e == cudaSuccess && hybrid)
+    e = launch_score_select(pw, (int)q.B, (int)q.H, (int)k.H, (int)q.N, (int)k.N, (int)q.d, hp.topp, theta, causal, mask,
+                            nullptr, hp.theta, status_ptr(), 0, true, s);
   if (e != cudaSuccess) return cuda_fail(e, "score_select launch");
   return record_event(ev, 3, s);
 }
 
 size_t v16_bytes(int64_t B, int64_t Hkv, int64_t N, int64_t d) { return align256((size_t)B * Hkv * N * d * 2); }
 
-// Attention workspace for a precision: the f16 copy of V, or the 8-bit copies and scales.
-bool is_q8(int precision) { return precision == SPARGE_PRECISION_Q8 || precision == SPARGE_PRECISION_Q8_FP8PV; }
+// Attention workspace for a precision: the f16 copy of V, or the 8-bit copies and scales (every
+// precision with an 8-bit product uses the 8-bit layout).
+bool is_q8(int precision) {
+  return precision == SPARGE_PRECISION_Q8 || precision == SPARGE_PRECISION_Q8_FP8PV ||
+         precision == SPARGE_PRECISION_BF16_FP8PV;
+}
 
 size_t attn_ws_bytes(int precision, int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d) {
   if (is_q8(precision)) return d == 128 ? q8_ws_bytes(B, Hq, Hkv, Nq, Nk, d) : 0;
@@ -293,7 +314,9 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
               const int32_t *qperm = nullptr) {
   if (precision != SPARGE_PRECISION_BF16 && !is_q8(precision))
     return fail(SPARGE_ERR_UNSUPPORTED, "precision %d not supported", precision);
-  const bool q8 = is_q8(precision), pv8 = precision == SPARGE_PRECISION_Q8_FP8PV;
+  const bool q8 = is_q8(precision);  // an 8-bit product: d = 128, the 8-bit workspace
+  const bool qk8 = precision == SPARGE_PRECISION_Q8 || precision == SPARGE_PRECISION_Q8_FP8PV;
+  const bool pv8 = precision == SPARGE_PRECISION_Q8_FP8PV || precision == SPARGE_PRECISION_BF16_FP8PV;
   if (q8 && q.d != 128) return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path needs d = 128 (got %lld)", (long long)q.d);
   if (q8 && k.N > 65535LL * 64) return fail(SPARGE_ERR_UNSUPPORTED, "the 8-bit path supports Nk <= %lld", 65535LL * 64);
   View ov{};
@@ -311,7 +334,7 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
   memset(&l, 0, sizeof(l));
   if (q8) {
     const Q8Ws w = q8_ws_carve(ws, q.B, q.H, k.H, q.N, k.N, q.d);
-    cudaError_t e = launch_q8_prep(q, k, v, w, pv8, perm, status_ptr(), s);
+    cudaError_t e = launch_q8_prep(q, k, v, w, qk8, pv8, perm, status_ptr(), s);
     if (e != cudaSuccess) return cuda_fail(e, "8-bit quantisation launch");
     if (!pv8 && (e = launch_convert_v_f16(v, w.v8, perm, status_ptr(), s)) != cudaSuccess)
       return cuda_fail(e, "convert_v launch");
@@ -320,15 +343,20 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
     const int64_t qd[4] = {d, Nq, q.H, q.B}, qs[3] = {d, Nq * d, q.H * Nq * d};
     const int64_t kd[4] = {d, N, k.H, k.B}, ks[3] = {d, N * d, k.H * N * d};
     const int64_t vd[4] = {npad, d, k.H, k.B}, vs[3] = {npad, d * npad, k.H * d * npad};
-    if ((rc = make_map_u8(&l.tq, w.q8, qd, qs, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, "q8")) ||
-        (rc = make_map_u8(&l.tk, w.k8, kd, ks, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B, "k8")) ||
-        (pv8 && (rc = make_map_u8(&l.tv, w.v8, vd, vs, 64, (int)d, CU_TENSOR_MAP_SWIZZLE_64B, "v8"))))
-      return rc;
-    if (!pv8) {
+    if (qk8) {
+      if ((rc = make_map_u8(&l.tq, w.q8, qd, qs, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, "q8")) ||
+          (rc = make_map_u8(&l.tk, w.k8, kd, ks, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B, "k8")))
+        return rc;
+    } else if ((rc = make_map(&l.tq, q, 128, "q")) || (rc = make_map(&l.tk, k, 64, "k"))) {
+      return rc;  // bf16 Q.K^T reads the (ordered) bf16 inputs as the bf16 path does
+    }
+    if (pv8) {
+      if ((rc = make_map_u8(&l.tv, w.v8, vd, vs, 64, (int)d, CU_TENSOR_MAP_SWIZZLE_64B, "v8"))) return rc;
+    } else {
       View v16{w.v8, v.B, v.H, v.N, v.d, v.H * v.N * v.d, v.N * v.d, v.d};
       if ((rc = make_map(&l.tv, v16, 64, "v", CU_TENSOR_MAP_DATA_TYPE_FLOAT16))) return rc;
     }
-    l.q8 = pv8 ? 2 : 1;
+    l.q8 = qk8 ? (pv8 ? 2 : 1) : 3;
     l.sq = w.sq;
     l.sk = w.sk;
     l.sv = w.sv;
@@ -469,12 +497,12 @@ int sparge_predict_mask_ex(const sparge_tensor *q, const sparge_tensor *k, float
   if (std::isnan(p->scale) || p->scale < 0.f || std::isinf(p->scale))
     return fail(SPARGE_ERR_INVALID_ARG, "scale must be finite and >= 0");
   const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)qv.d);
-  if (p->topk_mode != SPARGE_TOPK_CUMULATIVE && p->topk_mode != SPARGE_TOPK_COUNT)
-    return fail(SPARGE_ERR_INVALID_ARG, "topk_mode %d unknown", p->topk_mode);
+  if ((rc = check_topk_mode(p))) return rc;
   HeadParams hp;
   hp.topk = p->topk_per_head;
   hp.theta = p->theta_per_head;
   hp.topk_mode = p->topk_mode;
+  hp.topp = p->topp;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (p->token_order) {
     if (qv.N != kv.N) return fail(SPARGE_ERR_UNSUPPORTED, "a token order needs Nq = Nk");
@@ -565,13 +593,13 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   const int32_t *qperm = (p->token_order && !copy_q) ? p->token_order : nullptr;  // q not copied: gathered
   uint8_t *mask = mask_out ? mask_out : static_cast<uint8_t *>(ws) + need_pred;
   void *ws_v = static_cast<uint8_t *>(ws) + need_pred + mask_bytes;
-  if (p->topk_mode != SPARGE_TOPK_CUMULATIVE && p->topk_mode != SPARGE_TOPK_COUNT)
-    return fail(SPARGE_ERR_INVALID_ARG, "topk_mode %d unknown", p->topk_mode);
+  if ((rc = check_topk_mode(p))) return rc;
   HeadParams hp;
   hp.topk = p->topk_per_head;
   hp.theta = p->theta_per_head;
   hp.lambda = p->lambda_per_head;
   hp.topk_mode = p->topk_mode;
+  hp.topp = p->topp;
   if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s, p->timing_events, hp, qperm)))
     return rc;
   return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws_v, need_v, s,

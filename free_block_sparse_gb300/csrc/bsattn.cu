@@ -701,6 +701,7 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
   a.qperm = l.qperm;
   if (static_cast<int64_t>(a.B) * a.Hq * a.nqb == 0) return cudaSuccess;
   if (l.q8 != 0 && l.d != 128) return cudaErrorInvalidValue;
+  if (l.q8 == 3) return launch_t<128, 3, 3, false, true>(l, a, st);  // bf16 Q.K^T, e4m3 P.V
   if (l.q8 == 2) return launch_t<128, 4, 3, true, true>(l, a, st);
   if (l.q8 == 1) return launch_t<128, 4, 2, true, false>(l, a, st);
   return l.d == 128 ? launch_t<128, 3, 2, false, false>(l, a, st) : launch_t<64, 4, 3, false, false>(l, a, st);

@@ -63,10 +63,12 @@ cudaError_t launch_score_gemm(const ScoreGemmLaunch &l, cudaStream_t st);
 
 // Row softmax, cumulative top-k and the always-keep rule on S: writes the uint8 mask.  topk_h and
 // theta_h (device, Hq floats, or nullptr) override topk and theta per query head; a bad entry is
-// recorded in *status and its head keeps every valid block.
+// recorded in *status and its head keeps every valid block.  count_mode: topk is a fraction of the
+// valid blocks instead of the mass; or_into: the kept blocks are OR-ed into the mask rows already
+// there instead of replacing them.
 cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int Nq, int Nk, int d, float topk,
                                 float theta, int causal, uint8_t *mask, const float *topk_h, const float *theta_h,
-                                int *status, int count_mode, cudaStream_t st);
+                                int *status, int count_mode, bool or_into, cudaStream_t st);
 
 struct AttnLaunch {
   CUtensorMap tq, tk, tv;  // 4-D maps (d, N, H, B), 128-byte swizzle, boxes 64 x 128 (Q) / 64 x 64 (K, V);
@@ -82,7 +84,8 @@ struct AttnLaunch {
   unsigned long long *stats;
   int *status;
   int q8;                  // 0: bf16 Q.K^T, f16 P.V; 1: e4m3 Q.K^T (maps over the e4m3 copies, scales sq, sk),
-                           // f16 P.V; 2: as 1 with e4m3 P.V (channel-major e4m3 V, scales sv)
+                           // f16 P.V; 2: as 1 with e4m3 P.V (channel-major e4m3 V, scales sv); 3: bf16
+                           // Q.K^T (maps over the bf16 inputs) with e4m3 P.V as in 2
   const float *sq, *sk, *sv;
   const int32_t *perm;     // token order or nullptr: output row t goes to token perm[t] of o
   const void *q;           // bf16 Q, read row by row into TMEM at d = 64 (the ordered copy under a token order
@@ -111,10 +114,10 @@ struct Q8Ws {
 // Nq: query length, N: key / value length
 size_t q8_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t N, int64_t d);
 Q8Ws q8_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t N, int64_t d);
-// K mean, V channel scales, e4m3 Q and K - mean with their block scales; with quant_v also the
-// channel-major e4m3 V (otherwise v8 is left to the caller), whose key t is token perm[t] of v
-// when perm is given (Q and K are used in the order they come in).
-cudaError_t launch_q8_prep(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v,
+// With quant_qk: the K mean and e4m3 Q and K - mean with their block scales.  With quant_v: the V
+// channel scales and the channel-major e4m3 V (otherwise v8 is left to the caller), whose key t is
+// token perm[t] of v when perm is given (Q and K are used in the order they come in).
+cudaError_t launch_q8_prep(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_qk, bool quant_v,
                            const int32_t *perm, int *status, cudaStream_t st);
 
 cudaError_t launch_permute(const View &x, const int32_t *perm, void *y, int64_t ysb, int64_t ysh, int64_t ysn,

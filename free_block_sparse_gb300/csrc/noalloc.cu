@@ -23,6 +23,22 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void *g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};  // the context each address was looked up in
+
+// cuCtxGetCurrent through the runtime's driver entry point (no link-time dependency on libcuda).
+typedef CUresult (*ctx_get_fn_t)(CUcontext *);
+ctx_get_fn_t ctx_get_fn() {
+  static ctx_get_fn_t fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r) == cudaSuccess &&
+        r == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<ctx_get_fn_t>(p);
+  });
+  return fn;
+}
 
 }  // namespace
 
@@ -42,15 +58,22 @@ extern "C" int sparge_predict_mask_noalloc(const sparge_tensor *q, const sparge_
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return sparge::report_error(SPARGE_ERR_CUDA, cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return sparge::report_error(SPARGE_ERR_UNSUPPORTED, "device ordinal too large");
+  // the device's current context: a new one (after cudaDeviceReset, say) holds a new copy of the array
+  CUcontext ctx = nullptr;
+  ctx_get_fn_t get = ctx_get_fn();
+  if (!get || get(&ctx) != CUDA_SUCCESS || !ctx)
+    return sparge::report_error(SPARGE_ERR_CUDA, "no current CUDA context for the allocation-free call");
   void *scratch = nullptr;
   {
-    // First call on a device: look up the device address of the array with that device current.
+    // First call on a device (or in a new context of it): look up the device address of the
+    // array with that device current.
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
       void *p = nullptr;
       e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess) return sparge::report_error(SPARGE_ERR_CUDA, cudaGetErrorString(e));
       g_scratch_addr[dev] = p;
+      g_scratch_ctx[dev] = ctx;
     }
     scratch = g_scratch_addr[dev];
   }

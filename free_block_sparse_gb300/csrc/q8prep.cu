@@ -27,7 +27,7 @@ constexpr float E4M3_MAX = 448.f;
 // each lane loads U tokens (of K, and of V when its scales are wanted) before it accumulates.
 constexpr int U = 4;
 
-template <int D, bool WITH_V>
+template <int D, bool WITH_K, bool WITH_V>
 __global__ void __launch_bounds__(256) kv_partials_kernel(const __nv_bfloat16 *k, int64_t ksb, int64_t ksh,
                                                           int64_t ksn, const __nv_bfloat16 *v, int64_t vsb,
                                                           int64_t vsh, int64_t vsn, int Hkv, int N,
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(256) kv_partials_kernel(const __nv_bfloat16 *k
       const int tt = t + u * TPS;
       kx[u] = vx[u] = make_uint4(0, 0, 0, 0);  // zeros add nothing to the sum or the maximum
       if (tt < t1) {
-        kx[u] = ld_stream_v4(kb + static_cast<int64_t>(tt) * ksn);
+        if (WITH_K) kx[u] = ld_stream_v4(kb + static_cast<int64_t>(tt) * ksn);
         if (WITH_V) vx[u] = ld_stream_v4(vb + static_cast<int64_t>(tt) * vsn);
       }
     }
@@ -232,24 +232,30 @@ __global__ void __launch_bounds__(256) quant_vt_kernel(const __nv_bfloat16 *v, i
 }
 
 template <int D>
-cudaError_t run(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v, const int32_t *perm,
-                int *status, cudaStream_t st) {
+cudaError_t run(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_qk, bool quant_v,
+                const int32_t *perm, int *status, cudaStream_t st) {
   const int B = static_cast<int>(q.B), Hq = static_cast<int>(q.H), Hkv = static_cast<int>(k.H);
   const int Nq = static_cast<int>(q.N), N = static_cast<int>(k.N);  // N: keys and values
   const int nchunks = (N + CHUNK - 1) / CHUNK;
   const dim3 pgrid(B * Hkv, nchunks);
   const __nv_bfloat16 *kp = static_cast<const __nv_bfloat16 *>(k.data), *vp = static_cast<const __nv_bfloat16 *>(v.data);
-  if (quant_v)
-    kv_partials_kernel<D, true><<<pgrid, 256, 0, st>>>(kp, k.sb, k.sh, k.sn, vp, v.sb, v.sh, v.sn, Hkv, N, w.partial);
+  if (quant_qk && quant_v)
+    kv_partials_kernel<D, true, true><<<pgrid, 256, 0, st>>>(kp, k.sb, k.sh, k.sn, vp, v.sb, v.sh, v.sn, Hkv, N, w.partial);
+  else if (quant_qk)
+    kv_partials_kernel<D, true, false><<<pgrid, 256, 0, st>>>(kp, k.sb, k.sh, k.sn, vp, v.sb, v.sh, v.sn, Hkv, N, w.partial);
+  else if (quant_v)  // V scales only (bf16 Q.K^T): K is not read, its mean comes out 0 and is unused
+    kv_partials_kernel<D, false, true><<<pgrid, 256, 0, st>>>(kp, k.sb, k.sh, k.sn, vp, v.sb, v.sh, v.sn, Hkv, N, w.partial);
   else
-    kv_partials_kernel<D, false><<<pgrid, 256, 0, st>>>(kp, k.sb, k.sh, k.sn, vp, v.sb, v.sh, v.sn, Hkv, N, w.partial);
+    return cudaSuccess;
   kv_finish_kernel<D><<<B * Hkv, D, 0, st>>>(w.partial, nchunks, N, quant_v ? 1 : 0, w.kmean, w.sv);
   const int nqb = (Nq + QBLK - 1) / QBLK, nkb = (N + KBLK - 1) / KBLK;
   const int64_t nq = static_cast<int64_t>(B) * Hq * nqb, nk = static_cast<int64_t>(B) * Hkv * nkb;
-  quant_block_kernel<D, QBLK><<<static_cast<unsigned>(nq), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16 *>(q.data), q.sb, q.sh, q.sn, Hq, Nq, nqb, nullptr, w.q8, w.sq);
-  quant_block_kernel<D, KBLK><<<static_cast<unsigned>(nk), 256, 0, st>>>(kp, k.sb, k.sh, k.sn, Hkv, N, nkb, w.kmean,
-                                                                          w.k8, w.sk);
+  if (quant_qk) {
+    quant_block_kernel<D, QBLK><<<static_cast<unsigned>(nq), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(q.data), q.sb, q.sh, q.sn, Hq, Nq, nqb, nullptr, w.q8, w.sq);
+    quant_block_kernel<D, KBLK><<<static_cast<unsigned>(nk), 256, 0, st>>>(kp, k.sb, k.sh, k.sn, Hkv, N, nkb, w.kmean,
+                                                                            w.k8, w.sk);
+  }
   const int npad = (N + 63) / 64 * 64;
   if (quant_v)
     quant_vt_kernel<D><<<dim3(B * Hkv, npad / 64), 256, 0, st>>>(vp, v.sb, v.sh, v.sn, Hkv, N, npad, w.sv, w.v8, perm,
@@ -285,10 +291,11 @@ Q8Ws q8_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64
   return w;
 }
 
-cudaError_t launch_q8_prep(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_v,
+cudaError_t launch_q8_prep(const View &q, const View &k, const View &v, const Q8Ws &w, bool quant_qk, bool quant_v,
                            const int32_t *perm, int *status, cudaStream_t st) {
   if (q.B * q.N == 0) return cudaSuccess;
-  return q.d == 128 ? run<128>(q, k, v, w, quant_v, perm, status, st) : run<64>(q, k, v, w, quant_v, perm, status, st);
+  return q.d == 128 ? run<128>(q, k, v, w, quant_qk, quant_v, perm, status, st)
+                    : run<64>(q, k, v, w, quant_qk, quant_v, perm, status, st);
 }
 
 }  // namespace sparge

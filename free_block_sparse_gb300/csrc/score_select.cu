@@ -41,6 +41,7 @@ struct SelArgs {
   const float *topk_h, *theta_h;  // per query head, or nullptr
   int *status;
   int count_mode;  // 0: keep the shortest prefix reaching topk of the mass; 1: keep ceil(topk * n) blocks
+  int or_into;     // OR the row into the mask already written (the second half of the hybrid rule)
 };
 
 constexpr float LOG2E = 1.4426950408889634f;
@@ -224,11 +225,15 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
   auto put_word = [&](int j0, uint32_t word) {
     if (j0 >= a.nkb) return;
     if (words) {
-      *reinterpret_cast<uint32_t *>(mrow + j0) = word;
+      uint32_t *dst = reinterpret_cast<uint32_t *>(mrow + j0);
+      *dst = a.or_into ? (*dst | word) : word;
     } else {
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (j0 + u < a.nkb) mrow[j0 + u] = static_cast<uint8_t>(word >> (8 * u));
+        if (j0 + u < a.nkb) {
+          const uint8_t bt = static_cast<uint8_t>(word >> (8 * u));
+          mrow[j0 + u] = a.or_into ? static_cast<uint8_t>(mrow[j0 + u] | bt) : bt;
+        }
     }
   };
   // first pass (rows not kept whole): Z (mass reading) and the first histogram level
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
     }
     put_word(j0, word);
   }
-  const int nall = (a.nkb + 127) >> 7;
+  const int nall = a.or_into ? 0 : (a.nkb + 127) >> 7;  // OR-ed rows: that part is zero already
   for (int t = nit; t < nall; ++t) {
     const int j0 = 128 * t + 4 * lane;
     if (j0 >= a.nkb) continue;
@@ -464,7 +469,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
 
 cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int Nq, int Nk, int d, float topk,
                                 float theta, int causal, uint8_t *mask, const float *topk_h, const float *theta_h,
-                                int *status, int count_mode, cudaStream_t st) {
+                                int *status, int count_mode, bool or_into, cudaStream_t st) {
   (void)d;
   SelArgs a;
   a.S = ws.S;
@@ -485,6 +490,7 @@ cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int
   a.theta_h = theta_h;
   a.status = status;
   a.count_mode = count_mode;
+  a.or_into = or_into ? 1 : 0;
   if (a.rows == 0) return cudaSuccess;
   if (a.rows > 0x7fffffffLL) return cudaErrorInvalidValue;  // the kernel indexes rows in 32 bits
   const int64_t grid = (a.rows + WARPS - 1) / WARPS;

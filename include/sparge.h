@@ -60,7 +60,8 @@ enum sparge_dtype { SPARGE_BF16 = 1 };
 enum sparge_precision {
   SPARGE_PRECISION_BF16 = 0,          /* bf16 tensor-core products, fp32 accumulation */
   SPARGE_PRECISION_Q8 = 1,            /* 8-bit Q.K^T (e4m3, K smoothed), f16 P.V; d = 128 */
-  SPARGE_PRECISION_Q8_FP8PV = 2       /* 8-bit Q.K^T and P.V (both e4m3); d = 128 */
+  SPARGE_PRECISION_Q8_FP8PV = 2,      /* 8-bit Q.K^T and P.V (both e4m3); d = 128 */
+  SPARGE_PRECISION_BF16_FP8PV = 3     /* bf16 Q.K^T, 8-bit P.V (e4m3); d = 128 */
 };
 
 /* How topk picks a mask row's blocks (sparge_params.topk_mode). */
@@ -68,9 +69,14 @@ enum sparge_topk_mode {
   SPARGE_TOPK_CUMULATIVE = 0,  /* the shortest prefix, in (probability desc, index asc) order, whose
                                   cumulative probability reaches topk (the pages' "top 50% of the
                                   attention weights"; the default) */
-  SPARGE_TOPK_COUNT = 1        /* the first ceil(topk * n_valid) blocks of that order (at least one;
+  SPARGE_TOPK_COUNT = 1,       /* the first ceil(topk * n_valid) blocks of that order (at least one;
                                   the product is taken in fp32 with topk as given, less 1e-3, so
                                   that rounding never adds a block) */
+  SPARGE_TOPK_HYBRID = 2       /* a block is kept when SPARGE_TOPK_COUNT with topk keeps it or
+                                  SPARGE_TOPK_CUMULATIVE with sparge_params.topp keeps it (the
+                                  union of a top-k and a top-p set: the longer of the two prefixes;
+                                  reading of the hybrid Top-k + Top-p mask that the Chinese README's
+                                  citation list names for SpargeAttention2 without a rule) */
 };
 
 enum sparge_op {
@@ -137,6 +143,10 @@ typedef struct sparge_params {
   /* How topk (and topk_per_head) picks blocks: enum sparge_topk_mode (0, the cumulative reading,
    * when the struct is zeroed).  Used by sparge_predict_mask_ex and sparge_attn_ex. */
   int32_t topk_mode;
+  /* SPARGE_TOPK_HYBRID only: the cumulative probability of the top-p set, in (0, 1] (else
+   * SPARGE_ERR_INVALID_ARG); topk (or topk_per_head) is then the count fraction of the top-k set.
+   * Unused by the other modes. */
+  float topp;
 } sparge_params;
 
 /*
@@ -209,8 +219,12 @@ int sparge_predict_mask_ex(const sparge_tensor *q, const sparge_tensor *k, float
  * leaves a larger score error than INT8 would.  SPARGE_PRECISION_Q8 keeps P.V on f16 operands
  * as above; SPARGE_PRECISION_Q8_FP8PV also quantises V to e4m3 with one scale per channel and
  * P to e4m3 (P <= 256) and runs P.V as e4m3 x e4m3 (faster tensor work, about twice the output
- * error).  ws: 256-byte aligned, at least sparge_workspace_bytes(SPARGE_OP_BLOCK_SPARSE_ATTN_Q8,
- * ...) bytes (both 8-bit precisions); it holds the quantised copies after the call.
+ * error).  SPARGE_PRECISION_BF16_FP8PV (d = 128 only) keeps Q.K^T on the bf16 inputs and runs
+ * P.V in e4m3 as SPARGE_PRECISION_Q8_FP8PV does: e4m3 Q.K^T moves peaked softmax rows (large,
+ * aligned scores) much more than INT8 would, while e4m3 P.V alone stays within cosine 0.999 of
+ * the exact output on every workload measured.  ws: 256-byte aligned, at least
+ * sparge_workspace_bytes(SPARGE_OP_BLOCK_SPARSE_ATTN_Q8, ...) bytes (every precision with an
+ * 8-bit product); it holds the quantised copies after the call.
  * stats: optional counters (see sparge_params), may be NULL.
  */
 int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k,
@@ -284,8 +298,9 @@ int sparge_hilbert_perm_3d(int n_prefix, int T, int H, int W, int32_t *perm_host
  * GPU loading the library holds until the process exits; a shape whose scratch
  * (sparge_workspace_bytes(SPARGE_OP_PREDICT_MASK, ...)) exceeds 8 MiB is rejected with
  * SPARGE_ERR_UNSUPPORTED before anything is enqueued.  The first call on a device looks up the
- * array's device address with that device current; make that first call before any stream
- * capture.  All calls on a device share the array and it keeps the last call's contents (no
+ * array's device address with that device current (and so does the first call in a new context of
+ * the device, e.g. after cudaDeviceReset, which gives the array a new home); make that first call
+ * before any stream capture.  All calls on a device share the array and it keeps the last call's contents (no
  * part of it needs to start at zero): calls that can overlap on the GPU (different streams, no
  * ordering between them) race on it and must be serialised by the caller.
  */

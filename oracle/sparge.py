@@ -126,7 +126,7 @@ def count_target(topk: float, n: int) -> int:
     return int(min(n, max(1, math.ceil(t))))
 
 
-def topk_select(p: np.ndarray, valid: np.ndarray, topk: float, mode: str = "cdf") -> np.ndarray:
+def topk_select(p: np.ndarray, valid: np.ndarray, topk: float, mode: str = "cdf", topp: float = None) -> np.ndarray:
     """Keep set of one row of block probabilities.
 
     [overview, FAQ] topk lies in (0, 1]; lower means sparser.  [readme-cn, quick start]
@@ -136,7 +136,13 @@ def topk_select(p: np.ndarray, valid: np.ndarray, topk: float, mode: str = "cdf"
     block; at least one block is kept.  The other reading of the knob ("count"): keep the first
     count_target(topk, n_valid) blocks of that order.
 
+    "hybrid": [readme-cn, citation list] names a hybrid Top-k + Top-p mask (SpargeAttention2)
+    without a rule.  Reading: a block is kept when the count reading with topk keeps it or the
+    cumulative reading with topp keeps it (the union of a top-k set and a top-p set).
+
     p: (nkb,) probabilities, valid: (nkb,) bool with at least one True.  Returns bool (nkb,)."""
+    if mode == "hybrid":
+        return topk_select(p, valid, topk, "count") | topk_select(p, valid, topp, "cdf")
     keep = np.zeros(p.shape[0], dtype=bool)
     if topk >= 1.0:
         keep[valid] = True
@@ -155,7 +161,7 @@ def topk_select(p: np.ndarray, valid: np.ndarray, topk: float, mode: str = "cdf"
 
 
 def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal: bool,
-                 scale: float = None, mode: str = "cdf") -> Dict[str, np.ndarray]:
+                 scale: float = None, mode: str = "cdf", topp: float = None) -> Dict[str, np.ndarray]:
     """Stage 1 of SpargeAttn: the (B, Hq, ceil(N/128), ceil(N/64)) uint8 block mask.
 
     [overview, "Strengths"] mask shape and 128x64 granularity; [readme-cn, custom mask] 1 = keep.
@@ -166,7 +172,7 @@ def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal
     with theta are strict.
 
     q: (B, Hq, Nq, d), k: (B, Hkv, Nk, d) float64 (Nq <= Nk when causal; off = Nk - Nq as in
-    block_valid).  mode: the reading of topk (topk_select)."""
+    block_valid).  mode: the reading of topk (topk_select; topp is the top-p mass of "hybrid")."""
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
     off = k.shape[2] - N
@@ -184,7 +190,7 @@ def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal
         for h in range(Hq):
             colkeep = sK[b, h // G] < theta
             for i in range(nqb):
-                keep = topk_select(P[b, h, i], valid[i], topk, mode)
+                keep = topk_select(P[b, h, i], valid[i], topk, mode, topp)
                 if sQ[b, h, i] < theta:
                     keep |= valid[i]
                 keep |= colkeep & valid[i]
@@ -193,14 +199,15 @@ def predict_mask(q: np.ndarray, k: np.ndarray, topk: float, theta: float, causal
 
 
 def row_decisive(p: np.ndarray, valid: np.ndarray, sq: float, sk: np.ndarray, topk: float, theta: float,
-                 eps: float = 1e-3, mode: str = "cdf") -> bool:
+                 eps: float = 1e-3, mode: str = "cdf", topp: float = None) -> bool:
     """Whether no rounding within ``eps`` can change one mask row (the bit-exact comparison set).
 
     A row is decisive when its query similarity is farther than eps from theta and either it
     keeps every block because s_Q < theta, or (i) the cumulative sum at the cut and the one
     before it are farther than eps from topk, (ii) the probability gap at the cut exceeds eps,
     and (iii) every valid key block similarity is farther than eps from theta.  In the count
-    reading only (ii) and (iii) apply (the number kept does not depend on rounding).
+    reading only (ii) and (iii) apply (the number kept does not depend on rounding); in the
+    hybrid reading both cuts (count with topk, cumulative with topp) must be decisive.
     p: row probabilities (nkb,), valid: bool (nkb,), sq: s_Q of the row, sk: s_K (nkb,)."""
     if abs(sq - theta) <= eps:
         return False
@@ -208,6 +215,9 @@ def row_decisive(p: np.ndarray, valid: np.ndarray, sq: float, sk: np.ndarray, to
         return True
     if not np.all(np.abs(sk[valid] - theta) > eps):
         return False
+    if mode == "hybrid":
+        return (row_decisive(p, valid, sq, sk, topk, theta, eps, "count") and
+                row_decisive(p, valid, sq, sk, topp, theta, eps, "cdf"))
     if topk >= 1.0:
         return True
     m = cut_margins(p, valid, topk, mode)
@@ -241,7 +251,7 @@ def cut_margins(p: np.ndarray, valid: np.ndarray, topk: float, mode: str = "cdf"
 
 
 def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal: bool,
-                  eps: float = 1e-3, mode: str = "cdf") -> np.ndarray:
+                  eps: float = 1e-3, mode: str = "cdf", topp: float = None) -> np.ndarray:
     """row_decisive for every row of a predict_mask result: bool (B, Hq, nqb)."""
     P, sQ, sK = pred["P"], pred["sQ"], pred["sK"]
     B, Hq, nqb, nkb = P.shape
@@ -252,7 +262,7 @@ def decisive_rows(pred: Dict[str, np.ndarray], topk: float, theta: float, causal
         for h in range(Hq):
             for i in range(nqb):
                 out[b, h, i] = row_decisive(P[b, h, i], valid[i], sQ[b, h, i], sK[b, h // G], topk, theta, eps,
-                                            mode)
+                                            mode, topp)
     return out
 
 
@@ -265,7 +275,7 @@ def pool_key_head(k_head: np.ndarray):
 
 def predict_mask_row(q_block: np.ndarray, k_head: np.ndarray, i: int, topk: float, theta: float,
                      causal: bool, scale: float = None, mode: str = "cdf", off: int = 0,
-                     k_pool=None) -> Dict[str, np.ndarray]:
+                     k_pool=None, topp: float = None) -> Dict[str, np.ndarray]:
     """predict_mask for a single query block: q_block (n_i, d) the tokens of query block i,
     k_head (N, d) every key of its key/value head.  Same steps as predict_mask, for checking
     rows of workloads too large to run whole.  k_pool, if given, is pool_key_head(k_head),
@@ -282,7 +292,7 @@ def predict_mask_row(q_block: np.ndarray, k_head: np.ndarray, i: int, topk: floa
     s = scale * (muk @ muq[0, 0, 0])
     s[~valid] = -np.inf
     p = row_softmax(s)
-    keep = topk_select(p, valid, topk, mode)
+    keep = topk_select(p, valid, topk, mode, topp)
     if sq[0, 0, 0] < theta:
         keep |= valid
     keep |= (sk < theta) & valid

@@ -57,6 +57,7 @@ def test_struct_layouts_match_the_header(tmp_path):
         "         offsetof(sparge_params, timing_events), offsetof(sparge_params, topk_per_head),\n"
         "         offsetof(sparge_params, theta_per_head), offsetof(sparge_params, lambda_per_head),\n"
         "         offsetof(sparge_params, token_order), offsetof(sparge_params, topk_mode));\n"
+        "  printf(\"%zu\\n\", offsetof(sparge_params, topp));\n"
         "  printf(\"%zu %zu %zu\\n\", sizeof(sparge_tensor), offsetof(sparge_tensor, B),\n"
         "         offsetof(sparge_tensor, stride_n));\n"
         "  return 0;\n}\n")
@@ -66,18 +67,22 @@ def test_struct_layouts_match_the_header(tmp_path):
     P, T = fbs.sparge_params, fbs.sparge_tensor
     want = [ctypes.sizeof(P), P.stats.offset, P.timing_events.offset, P.topk_per_head.offset,
             P.theta_per_head.offset, P.lambda_per_head.offset, P.token_order.offset, P.topk_mode.offset,
-            ctypes.sizeof(T), T.B.offset,
+            P.topp.offset, ctypes.sizeof(T), T.B.offset,
             T.stride_n.offset]
     assert got == want
 
 
-@pytest.mark.parametrize("case", ["null_params", "bad_topk", "bad_theta", "neg_scale", "bad_mode"])
+@pytest.mark.parametrize("case", ["null_params", "bad_topk", "bad_theta", "neg_scale", "bad_mode", "bad_topp",
+                                  "nan_topp"])
 def test_predict_mask_ex_rejects_bad_parameters(lib, case):
     q = _t()
     p = fbs.sparge_params(0.5, -math.inf, 0.0, fbs.SPARGE_PRECISION_BF16, 0, None)
     topk = 0.5
     if case == "bad_mode":
         p.topk_mode = 7
+    if case in ("bad_topp", "nan_topp"):
+        p.topk_mode = fbs.SPARGE_TOPK_HYBRID
+        p.topp = 0.0 if case == "bad_topp" else math.nan
     if case == "bad_topk":
         topk = 1.5
     elif case == "bad_theta":

@@ -161,11 +161,13 @@ def test_full_size_predicted_mask_and_attention(name):
     assert n_rel >= n_dec_min, (n_rel, n_dec_min)
 
 
-@pytest.mark.parametrize("prec,cos_min", [(fbs.SPARGE_PRECISION_BF16, COS_MIN), (fbs.SPARGE_PRECISION_Q8, 0.999),
-                                          (fbs.SPARGE_PRECISION_Q8_FP8PV, 0.998)])
+@pytest.mark.parametrize("prec,cos_min", [
+    (fbs.SPARGE_PRECISION_BF16, COS_MIN), (fbs.SPARGE_PRECISION_Q8, 0.999), (fbs.SPARGE_PRECISION_BF16_FP8PV, 0.999),
+    pytest.param(fbs.SPARGE_PRECISION_Q8_FP8PV, 0.999,
+                 marks=pytest.mark.xfail(strict=True, reason="e4m3 scores, P and V: measured cosine 0.9986 < 0.999"))])
 def test_full_size_custom_mask(prec, cos_min):
     """The custom-mask workload at full size (B 2, 16 heads, N 65536) through the block-sparse
-    call on its own mask, in each precision; the 8-bit ones at their cosine bounds only."""
+    call on its own mask, in each precision; the 8-bit ones at the cosine bound only."""
     w = _workload("custom")
     q, k, v = dev_bf16(w.q), dev_bf16(w.k), dev_bf16(w.v)
     out = fbs.block_sparse_attn_ex(q, k, v, torch.from_numpy(w.mask).cuda(), w.causal, lam=w.lam, precision=prec)

@@ -151,6 +151,45 @@ def test_count_mode_through_sparge_attn_ex():
     assert cos >= COS_MIN and err <= MAXABS, (cos, err)
 
 
+@pytest.mark.parametrize("key,topk,topp", [("tiny", 0.1, 0.3), ("tiny", 0.2, 0.5), ("llama", 0.15, 0.4),
+                                           ("llama", 0.12, 0.45)])
+def test_hybrid_mode_mask_matches_oracle(key, topk, topp):
+    """The hybrid reading (blocks kept by the count reading with topk or by the cumulative reading
+    with topp): bit-exact on the rows where both cuts are decisive, and on every row at least
+    the blocks each reading keeps alone."""
+    w = make(key)
+    q, k = dev_bf16(w.q), dev_bf16(w.k)
+    gm = fbs.predict_mask_ex(q, k, topk, w.causal, theta=w.theta, topk_mode=fbs.SPARGE_TOPK_HYBRID,
+                             topp=topp).cpu().numpy()
+    pred = oracle.predict_mask(f64(w.q), f64(w.k), topk, w.theta, w.causal, mode="hybrid", topp=topp)
+    dec = oracle.decisive_rows(pred, topk, w.theta, w.causal, mode="hybrid", topp=topp)
+    assert dec.mean() > 0.2
+    bad = np.nonzero((gm != pred["mask"]).any(axis=-1) & dec)
+    assert bad[0].size == 0, "hybrid mask differs on decisive rows %s" % (list(zip(*bad))[:5],)
+    # the GPU's own count-mode and cumulative-mode masks are subsets of its hybrid mask, and
+    # together they make it up
+    gc = fbs.predict_mask_ex(q, k, topk, w.causal, theta=w.theta, topk_mode=fbs.SPARGE_TOPK_COUNT).cpu().numpy()
+    gp = fbs.predict_mask_ex(q, k, topp, w.causal, theta=w.theta).cpu().numpy()
+    assert np.array_equal(gm, gc | gp)
+    # both readings decide some rows (the union is not just one of them)
+    assert (gm != gc).any() and (gm != gp).any()
+
+
+def test_hybrid_mode_through_sparge_attn_ex():
+    """sparge_attn_ex with the hybrid reading: its mask is predict_mask_ex's, its output the
+    oracle's attention on that mask."""
+    w = make("llama")
+    q, k, v = dev_bf16(w.q), dev_bf16(w.k), dev_bf16(w.v)
+    mask = torch.empty((w.B, w.Hq, w.nqb, w.nkb), dtype=torch.uint8, device="cuda")
+    out = fbs.sparge_attn_ex(q, k, v, 0.1, w.causal, theta=w.theta, mask_out=mask, topk_mode=fbs.SPARGE_TOPK_HYBRID,
+                             topp=0.4)
+    m2 = fbs.predict_mask_ex(q, k, 0.1, w.causal, theta=w.theta, topk_mode=fbs.SPARGE_TOPK_HYBRID, topp=0.4)
+    assert torch.equal(mask, m2)
+    ref = oracle.block_sparse_attn(f64(w.q), f64(w.k), f64(w.v), mask.cpu().numpy(), -math.inf, w.causal)
+    cos, err = cos_maxabs(host_f64(out), ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
+
+
 @pytest.mark.parametrize("topk,theta", [(0.05, 0.5), (0.3, 0.3), (0.9, 0.0), (1.0, 0.5), (0.5, 2.0)])
 def test_mask_topk_theta_sweep(topk, theta):
     w = make("llama")

@@ -274,6 +274,50 @@ def test_count_mode_matches_brute_force_tiny():
     assert (pred["mask"].sum(axis=-1) == 5).all()
 
 
+def brute_force_hybrid_keep(p, valid, kc, topp):
+    """Over all subsets of the valid blocks with at least kc blocks and a probability sum of at
+    least topp: the fewest blocks; among those the largest sum; among those the lexicographically
+    smallest list of indices."""
+    vj = np.nonzero(valid)[0]
+    n = vj.size
+    subsets = np.array(list(itertools.product([0, 1], repeat=n)), dtype=bool)
+    sums = subsets.astype(np.float64) @ p[vj]
+    card = subsets.sum(axis=1)
+    ok = (sums >= topp) & (card >= kc)
+    cmin = card[ok].min()
+    cand = ok & (card == cmin)
+    cand &= sums == sums[cand].max()
+    idx = sorted(tuple(vj[s]) for s in subsets[cand])
+    keep = np.zeros(p.size, bool)
+    keep[np.array(idx[0], dtype=int)] = True
+    return keep
+
+
+@pytest.mark.parametrize("topk,topp", [(0.2, 0.5), (0.35, 0.7), (0.1, 0.3)])
+def test_hybrid_mode_matches_brute_force_tiny(topk, topp):
+    """The hybrid reading (count topk or cumulative topp) against subset enumeration of its
+    defining property, on every row of the tiny workload; both the count side and the mass side
+    decide some rows."""
+    w = W.make_config("tiny")
+    q, k = f64(w.q), f64(w.k)
+    pred = oracle.predict_mask(q, k, topk, 0.0, w.causal, mode="hybrid", topp=topp)
+    from scipy.special import softmax
+    d = q.shape[-1]
+    mq = q.reshape(1, 2, 8, 128, d).mean(axis=3)
+    mk = k.reshape(1, 2, 16, 64, d).mean(axis=3)
+    P = softmax(np.einsum("bhid,bhjd->bhij", mq, mk) / math.sqrt(d), axis=-1)
+    valid = np.ones(16, bool)
+    kc = oracle.count_target(topk, 16)
+    sides = set()
+    for h in range(2):
+        for i in range(8):
+            keep = brute_force_hybrid_keep(P[0, h, i], valid, kc, topp)
+            np.testing.assert_array_equal(pred["mask"][0, h, i].astype(bool), keep)
+            by_mass = brute_force_keep(P[0, h, i], valid, topp).sum()
+            sides.add("count" if kc > by_mass else "mass" if by_mass > kc else "tie")
+    assert {"count", "mass"} <= sides, sides
+
+
 def test_count_mode_ties_keep_lowest_indices_and_is_monotone():
     p = np.full(12, 1.0 / 12)
     valid = np.ones(12, bool)
