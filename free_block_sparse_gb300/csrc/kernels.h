@@ -91,6 +91,9 @@ struct AttnLaunch {
   const void *q;           // bf16 Q, read row by row into TMEM at d = 64 (the ordered copy under a token order
                            // at d = 128, where the rows come by TMA)
   const int32_t *qperm;    // d = 64 under a token order: Q row t of the block is token qperm[t] of q
+  // Token order gathered by TMA (or nullptr): tk (and tq when qg is set) are then 2-D maps over
+  // all rows of k (q), box 64 columns x 1 row, and tile row t is row token_order[t] of its head
+  const int32_t *kg, *qg;
   int64_t q_sb, q_sh, q_sn;
 };
 

@@ -21,6 +21,7 @@ SMALL = {
     "cogvideox": dict(name="cogvideox", Hq=2, Hkv=2, grid=(5, 30, 45)),
 }
 BF16, Q8, FP8PV = fbs.SPARGE_PRECISION_BF16, fbs.SPARGE_PRECISION_Q8, fbs.SPARGE_PRECISION_Q8_FP8PV
+BF16PV = fbs.SPARGE_PRECISION_BF16_FP8PV
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,8 +45,11 @@ def _empty_mask(w):
     return torch.empty((w.B, w.Hq, w.nqb, w.nkb), dtype=torch.uint8, device="cuda")
 
 
-@pytest.mark.parametrize("key,prec", [("flux", BF16), ("flux", Q8), ("flux", FP8PV), ("cogvideox", BF16)])
+@pytest.mark.parametrize("key,prec", [("flux", BF16), ("flux", Q8), ("flux", FP8PV), ("flux", BF16PV),
+                                      ("cogvideox", BF16)])
 def test_token_order_equals_explicit_permutes(key, prec):
+    """With contiguous inputs the bf16 Q.K^T paths read Q and K in place (pooling through the order,
+    the attention's tiles by TMA gathers, Q rows into TMEM at d = 64): no ordered copies."""
     w, perm_np = _make(key)
     perm = torch.from_numpy(perm_np).cuda()
     q, k, v = dev_bf16(w.q), dev_bf16(w.k), dev_bf16(w.v)
@@ -115,3 +119,26 @@ def test_token_order_entries_out_of_range_are_reported(key):
     torch.cuda.synchronize()
     assert fbs.device_status() == fbs.SPARGE_ERR_INVALID_ARG
     assert m.shape == (w.B, w.Hq, w.nqb, w.nkb)
+
+
+@pytest.mark.parametrize("key", ["flux", "cogvideox"])
+def test_token_order_with_strided_rows_falls_back_to_copies(key):
+    """Q and K views whose heads are not packed back to back (a slice of longer sequences) cannot be
+    gathered through one row map: the call copies them in order instead, with the same result."""
+    w, perm_np = _make(key)
+    perm = torch.from_numpy(perm_np).cuda()
+    pad = 256
+    big = [torch.zeros((t.shape[0], t.shape[1], w.N + pad, w.d), dtype=torch.bfloat16, device="cuda")
+           for t in (w.q, w.k)]
+    big[0][:, :, :w.N] = dev_bf16(w.q)
+    big[1][:, :, :w.N] = dev_bf16(w.k)
+    q, k = big[0][:, :, :w.N], big[1][:, :, :w.N]
+    v = dev_bf16(w.v)
+    assert q.stride(1) != w.N * w.d
+    m1, m2 = _empty_mask(w), _empty_mask(w)
+    o1 = fbs.sparge_attn_ex(q.contiguous(), k.contiguous(), v, w.topk, w.causal, theta=w.theta, mask_out=m1,
+                            token_order=perm)
+    o2 = fbs.sparge_attn_ex(q, k, v, w.topk, w.causal, theta=w.theta, mask_out=m2, token_order=perm)
+    assert torch.equal(m1, m2)
+    assert torch.equal(o1, o2)
+    assert fbs.device_status() == fbs.SPARGE_OK
