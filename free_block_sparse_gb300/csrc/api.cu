@@ -131,29 +131,6 @@ int make_map(CUtensorMap *m, const View &v, int box_rows, const char *name,
   return SPARGE_OK;
 }
 
-// Whether a tensor's rows are uniformly strided (stride_h = N stride_n, stride_b = H stride_h), so
-// that one 2-D map over all B H N rows addresses them, with row indices that fit the TMA's 32-bit
-// coordinates.
-bool rows_uniform(const View &v) {
-  return v.sh == v.N * v.sn && v.sb == v.H * v.sh && v.B * v.H * v.N <= 0x7fffffffLL;
-}
-
-// 2-D map over all rows of a uniformly strided bf16 tensor, box 64 columns x 1 row, 128-byte
-// swizzle: the map of the attention kernel's TMA gathers.
-int make_map_rows(CUtensorMap *m, const View &v, const char *name) {
-  encode_fn_t enc = get_encode();
-  if (!enc) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  cuuint64_t dims[2] = {(cuuint64_t)v.d, (cuuint64_t)(v.B * v.H * v.N)};
-  cuuint64_t strides[1] = {(cuuint64_t)v.sn * 2};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(v.data), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(SPARGE_ERR_CUDA, "cuTensorMapEncodeTiled(%s rows) failed with %d", name, (int)r);
-  return SPARGE_OK;
-}
-
 // 3-D map over a contiguous bf16 array [planes][rows][d], box 64 columns x 128 rows, 128-byte swizzle.
 int make_map3(CUtensorMap *m, void *base, int64_t d, int64_t rows, int64_t planes, const char *name) {
   encode_fn_t enc = get_encode();
@@ -222,12 +199,15 @@ size_t order_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
   return align256((size_t)2 * B * Hq * N * d) + align256((size_t)2 * B * Hkv * N * d);
 }
 
-// Calls with a token order: copies q and/or k into the front of the workspace in that order
-// (contiguous (B, H, N, d) bf16), replaces them by the copies and moves ws past the space of both
-// (the space is reserved whether or not a copy is made).  A tensor that is not copied is read
-// through the permutation by the kernels instead (pooling, and the d = 64 attention's Q rows).
+// Calls with a token order: places copies of q and/or k in that order at the front of the
+// workspace (contiguous (B, H, N, d) bf16), replaces them by the copies and moves ws past the space
+// of both (the space is reserved whether or not a copy is made).  With launch the copies are made
+// here by permute kernels; without it the caller has them written by another kernel (the pooling
+// of mask prediction, which reads every row through the order anyway).  A tensor that is not
+// copied is read through the permutation by the kernels instead (pooling, and the d = 64
+// attention's Q rows).
 int order_qk(View &q, View &k, const int32_t *perm, void *&ws, size_t &ws_bytes, cudaStream_t s, bool copy_q = true,
-             bool copy_k = true) {
+             bool copy_k = true, bool launch = true) {
   const size_t need = order_bytes(q.B, q.H, k.H, q.N, q.d);
   if (!ws || ws_bytes < need)
     return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu for the token-ordered copies", ws_bytes,
@@ -236,8 +216,8 @@ int order_qk(View &q, View &k, const int32_t *perm, void *&ws, size_t &ws_bytes,
   uint8_t *base = static_cast<uint8_t *>(ws);
   void *qc = base, *kc = base + align256((size_t)2 * q.B * q.H * q.N * q.d);
   cudaError_t e = cudaSuccess;
-  if (copy_q) e = launch_permute(q, perm, qc, q.H * q.N * q.d, q.N * q.d, q.d, false, status_ptr(), s, true);
-  if (e == cudaSuccess && copy_k)
+  if (launch && copy_q) e = launch_permute(q, perm, qc, q.H * q.N * q.d, q.N * q.d, q.d, false, status_ptr(), s, true);
+  if (launch && e == cudaSuccess && copy_k)
     e = launch_permute(k, perm, kc, k.H * k.N * k.d, k.N * k.d, k.d, false, status_ptr(), s, true);
   if (e != cudaSuccess) return cuda_fail(e, "token-order copy launch");
   if (copy_q) q = View{qc, q.B, q.H, q.N, q.d, q.H * q.N * q.d, q.N * q.d, q.d};
@@ -247,25 +227,11 @@ int order_qk(View &q, View &k, const int32_t *perm, void *&ws, size_t &ws_bytes,
   return SPARGE_OK;
 }
 
-// How a call with a token order reads Q and K.  The 8-bit quantiser of Q and K reads ordered
-// copies in the workspace.  Otherwise nothing is copied where the rows can be read in place:
-// the pooling gathers Q and K rows through the order by plain loads, the d = 64 attention gathers
-// its Q rows into TMEM itself, and the attention's K tiles (and Q tiles at d = 128) come by TMA
-// gathers through one 2-D row map, which needs uniformly strided rows; a tensor that is not
-// gets an ordered copy.
-struct OrderPlan {
-  bool copy_q, copy_k;          // ordered copies in the workspace
-  bool gather_q, gather_k;      // attention tiles by TMA gathers through the order
-};
-OrderPlan order_plan(const View &q, const View &k, int precision) {
-  const bool qk8 = precision == SPARGE_PRECISION_Q8 || precision == SPARGE_PRECISION_Q8_FP8PV;
-  OrderPlan p;
-  p.gather_k = !qk8 && rows_uniform(k);
-  p.gather_q = !qk8 && q.d == 128 && rows_uniform(q);
-  p.copy_k = !p.gather_k;
-  p.copy_q = qk8 || (q.d == 128 && !p.gather_q);
-  return p;
-}
+bool is_q8(int precision);
+// Under a token order Q gets an ordered copy only where TMA (d = 128) or the 8-bit quantiser reads
+// it; at d = 64 the attention loads Q rows itself and gathers them through the permutation (the
+// 8-bit precisions need d = 128).
+bool order_copies_q(int64_t d, int precision) { return d != 64 || is_q8(precision); }
 
 // Per-query-head parameter arrays of a sparge_params (device pointers, each may be null).
 struct HeadParams {
@@ -285,7 +251,8 @@ int check_topk_mode(const sparge_params *p) {
 
 int predict_impl(const View &q, const View &k, float topk, float theta, int causal, float scale, uint8_t *mask,
                  void *ws, size_t ws_bytes, cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {},
-                 const int32_t *qperm = nullptr, const int32_t *kperm = nullptr) {
+                 const int32_t *qperm = nullptr, const int32_t *kperm = nullptr, void *qcopy = nullptr,
+                 void *kcopy = nullptr) {
   if (!mask) return fail(SPARGE_ERR_INVALID_ARG, "mask is NULL");
   int rc;
   if ((rc = check_lengths(q, k, causal))) return rc;
@@ -298,7 +265,7 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
   if (q.B == 0 || q.N == 0) return SPARGE_OK;
   PredictWs pw = predict_ws_carve(ws, q.B, q.H, k.H, q.N, k.N, q.d);
   if ((rc = record_event(ev, 0, s))) return rc;
-  cudaError_t e = launch_pool_sim(q, k, pw, s, qperm, kperm, status_ptr());
+  cudaError_t e = launch_pool_sim(q, k, pw, s, qperm, kperm, status_ptr(), qcopy, kcopy);
   if (e != cudaSuccess) return cuda_fail(e, "pool_sim launch");
   if ((rc = record_event(ev, 1, s))) return rc;
   {
@@ -348,7 +315,7 @@ size_t attn_ws_bytes(int precision, int64_t B, int64_t Hq, int64_t Hkv, int64_t 
 int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, float lambda, int causal, float scale,
               int precision, sparge_tensor *o, unsigned long long *stats, void *ws, size_t ws_bytes,
               cudaStream_t s, void *const *ev = nullptr, const HeadParams &hp = {}, const int32_t *perm = nullptr,
-              const int32_t *qperm = nullptr, const int32_t *kg = nullptr, const int32_t *qg = nullptr) {
+              const int32_t *qperm = nullptr) {
   if (precision != SPARGE_PRECISION_BF16 && !is_q8(precision))
     return fail(SPARGE_ERR_UNSUPPORTED, "precision %d not supported", precision);
   const bool q8 = is_q8(precision);  // an 8-bit product: d = 128, the 8-bit workspace
@@ -384,12 +351,8 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
       if ((rc = make_map_u8(&l.tq, w.q8, qd, qs, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, "q8")) ||
           (rc = make_map_u8(&l.tk, w.k8, kd, ks, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B, "k8")))
         return rc;
-    } else {  // bf16 Q.K^T reads the bf16 inputs as the bf16 path does
-      if ((rc = qg ? make_map_rows(&l.tq, q, "q") : make_map(&l.tq, q, 128, "q")) ||
-          (rc = kg ? make_map_rows(&l.tk, k, "k") : make_map(&l.tk, k, 64, "k")))
-        return rc;
-      l.kg = kg;
-      l.qg = qg;
+    } else if ((rc = make_map(&l.tq, q, 128, "q")) || (rc = make_map(&l.tk, k, 64, "k"))) {
+      return rc;  // bf16 Q.K^T reads the (ordered) bf16 inputs as the bf16 path does
     }
     if (pv8) {
       if ((rc = make_map_u8(&l.tv, w.v8, vd, vs, 64, (int)d, CU_TENSOR_MAP_SWIZZLE_64B, "v8"))) return rc;
@@ -406,14 +369,11 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
     if (e != cudaSuccess) return cuda_fail(e, "convert_v launch");
     if ((rc = record_event(ev, 4, s))) return rc;
     View v16{ws, v.B, v.H, v.N, v.d, v.H * v.N * v.d, v.N * v.d, v.d};
-    // (the Q map also checks the alignment the d = 64 row reads rely on)
-    if ((rc = qg ? make_map_rows(&l.tq, q, "q") : make_map(&l.tq, q, 128, "q"))) return rc;
+    if ((rc = make_map(&l.tq, q, 128, "q"))) return rc;  // checks the alignment the row reads rely on
     l.q = q.data;
     l.qperm = qperm;  // d = 64 under a token order: q is the caller's tensor, gathered by row
     l.q_sb = q.sb; l.q_sh = q.sh; l.q_sn = q.sn;
-    if ((rc = kg ? make_map_rows(&l.tk, k, "k") : make_map(&l.tk, k, 64, "k"))) return rc;
-    l.kg = kg;
-    l.qg = qg;
+    if ((rc = make_map(&l.tk, k, 64, "k"))) return rc;
     if ((rc = make_map(&l.tv, v16, 64, "v", CU_TENSOR_MAP_DATA_TYPE_FLOAT16))) return rc;
   }
   l.mask = mask;
@@ -596,14 +556,14 @@ int sparge_block_sparse_attn_ex(const sparge_tensor *q, const sparge_tensor *k, 
     if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   }
   if ((rc = record_event(p->timing_events, 0, s))) return rc;
-  const int32_t *ord = p->token_order;
-  const OrderPlan op = order_plan(qv, kv, p->precision);
-  if (ord && qv.B * qv.N > 0 && (rc = order_qk(qv, kv, ord, ws, ws_bytes, s, op.copy_q, op.copy_k))) return rc;
+  const bool copy_q = order_copies_q(qv.d, p->precision);
+  if (p->token_order && qv.B * qv.N > 0 &&
+      (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s, copy_q, true)))
+    return rc;
   HeadParams hp;
   hp.lambda = p->lambda_per_head;
   return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws, ws_bytes, s,
-                   p->timing_events, hp, ord, (ord && !op.copy_q) ? ord : nullptr, (ord && op.gather_k) ? ord : nullptr,
-                   (ord && op.gather_q) ? ord : nullptr);
+                   p->timing_events, hp, p->token_order, (p->token_order && !copy_q) ? p->token_order : nullptr);
 }
 
 int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,
@@ -630,11 +590,15 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   const size_t need = need_order + need_pred + mask_bytes + need_v;
   if (!ws || ws_bytes < need) return fail(SPARGE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, need);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool copy_q = order_copies_q(qv.d, p->precision);
+  // Under a token order the pooling reads Q and K through it and writes the ordered copies the
+  // attention (or the 8-bit quantiser) reads, so no separate copy pass runs.
+  const View q_in = qv, k_in = kv;
+  if (p->token_order && qv.B * qv.N > 0 &&
+      (rc = order_qk(qv, kv, p->token_order, ws, ws_bytes, s, copy_q, true, false)))
+    return rc;
   const int32_t *ord = p->token_order;
-  const OrderPlan op = order_plan(qv, kv, p->precision);
-  if (ord && qv.B * qv.N > 0 && (rc = order_qk(qv, kv, ord, ws, ws_bytes, s, op.copy_q, op.copy_k))) return rc;
-  const int32_t *qperm = (ord && !op.copy_q) ? ord : nullptr;  // q not copied: read through the order
-  const int32_t *kperm = (ord && !op.copy_k) ? ord : nullptr;  // k likewise
+  const int32_t *qperm = (ord && !copy_q) ? ord : nullptr;  // q not copied: the attention gathers its rows
   uint8_t *mask = mask_out ? mask_out : static_cast<uint8_t *>(ws) + need_pred;
   void *ws_v = static_cast<uint8_t *>(ws) + need_pred + mask_bytes;
   if ((rc = check_topk_mode(p))) return rc;
@@ -644,12 +608,16 @@ int sparge_attn_ex(const sparge_tensor *q, const sparge_tensor *k, const sparge_
   hp.lambda = p->lambda_per_head;
   hp.topk_mode = p->topk_mode;
   hp.topp = p->topp;
-  if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s, p->timing_events, hp, qperm,
-                         kperm)))
+  if (ord) {
+    if ((rc = predict_impl(q_in, k_in, topk, p->theta, is_causal, scale, mask, ws, need_pred, s, p->timing_events, hp,
+                           ord, ord, copy_q ? const_cast<void *>(qv.data) : nullptr, const_cast<void *>(kv.data))))
+      return rc;
+  } else if ((rc = predict_impl(qv, kv, topk, p->theta, is_causal, scale, mask, ws, need_pred, s, p->timing_events,
+                                hp))) {
     return rc;
+  }
   return attn_impl(qv, kv, vv, mask, p->lambda, is_causal, scale, p->precision, o, p->stats, ws_v, need_v, s,
-                   p->timing_events, hp, ord, qperm, (ord && op.gather_k) ? ord : nullptr,
-                   (ord && op.gather_q) ? ord : nullptr);
+                   p->timing_events, hp, p->token_order, qperm);
 }
 
 int sparge_attn(const sparge_tensor *q, const sparge_tensor *k, const sparge_tensor *v, float topk, int is_causal,

@@ -58,37 +58,7 @@ struct AttnArgs {
   const __nv_bfloat16 *q;     // bf16 path: Q rows, copied into TMEM by the softmax warps
   const int32_t *qperm;       // token order of those rows (or nullptr)
   int64_t q_sb, q_sh, q_sn;
-  const int32_t *kg, *qg;     // token orders gathered by TMA (2-D row maps), or nullptr
 };
-
-// TMA gathers of `nrows` rows (64 or 128) of one head into a tile of nch 64-column chunks
-// (chunk stride nrows x 128 bytes): tile row r is row rbase + ord[t0 + r] of the map.  Rows past
-// ntok, and entries outside 0..ntok-1 (reported in *status), read the head's first row instead,
-// so no address outside the head is formed.  Run by the 32 lanes of the producer warp after the
-// barrier's expected bytes are set.
-__device__ __forceinline__ void gather_rows(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, const int32_t *ord,
-                                            int t0, int ntok, int64_t rbase, int nrows, int nch, int lane,
-                                            int *status) {
-  const int per = nrows / 4;  // gathers per chunk
-  for (int g = lane; g < per * nch; g += 32) {
-    const int c = g / per, r = 4 * (g % per);
-    int y[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int t = t0 + r + u;
-      int src = 0;
-      if (t < ntok) {
-        src = __ldg(ord + t);
-        if (static_cast<unsigned>(src) >= static_cast<unsigned>(ntok)) {
-          record_status(status, -1 /* SPARGE_ERR_INVALID_ARG */);
-          src = 0;
-        }
-      }
-      y[u] = static_cast<int>(rbase + src);
-    }
-    tma_gather4(dst + c * (nrows * 128) + r * 128, map, bar, 64 * c, y[0], y[1], y[2], y[3]);
-  }
-}
 
 // Warp-collective walk over the kept, valid key blocks of one mask row in ascending order, run
 // by the producer warp only: windows of 512 candidates, 16 per lane loaded as independent bytes,
@@ -276,7 +246,6 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       const int kst = t % KST, js = t % JRING;
       if (!mbar_wait(&cs.k_empty[kst], ((t / KST) & 1) ^ 1, abort, a.status)) break;
       if (!mbar_wait(&cs.j_empty[js], ((t / JRING) & 1) ^ 1, abort, a.status)) break;
-      uint8_t *kdst = smem + L::OFF_K + kst * L::K_BYTES;
       if (lane == 0) {
         cs.jring[js] = j;
         mbar_arrive(&cs.j_full[js]);
@@ -284,28 +253,18 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         if (j >= 0) {
           if (!QTM && t == 0) {
             mbar_arrive_expect_tx(&cs.q_full, L::Q_BYTES);
-            if (a.qg == nullptr)
-              for (int c = 0; c < L::QCH; ++c)
-                tma_load_4d(smem + L::OFF_Q + c * 16384, &tq, &cs.q_full, (128 / L::EB) * c, QBLK * i, h, b);
-          }
-          mbar_arrive_expect_tx(&cs.k_full[kst], L::K_BYTES);
-          if (a.kg == nullptr)
             for (int c = 0; c < L::QCH; ++c)
-              tma_load_4d(kdst + c * L::KV_CHUNK, &tk, &cs.k_full[kst], (128 / L::EB) * c, KBLK * j, kvh, b);
+              tma_load_4d(smem + L::OFF_Q + c * 16384, &tq, &cs.q_full, (128 / L::EB) * c, QBLK * i, h, b);
+          }
+          uint8_t *kdst = smem + L::OFF_K + kst * L::K_BYTES;
+          mbar_arrive_expect_tx(&cs.k_full[kst], L::K_BYTES);
+          for (int c = 0; c < L::QCH; ++c)
+            tma_load_4d(kdst + c * L::KV_CHUNK, &tk, &cs.k_full[kst], (128 / L::EB) * c, KBLK * j, kvh, b);
         } else {
           mbar_arrive(&cs.k_full[kst]);
         }
       }
       __syncwarp();
-      if constexpr (!QK8) {
-        // under a token order the rows come through it, four per TMA gather, from every lane
-        if (j >= 0 && !QTM && t == 0 && a.qg != nullptr)
-          gather_rows(smem + L::OFF_Q, &tq, &cs.q_full, a.qg, QBLK * i, a.Nq,
-                      (static_cast<int64_t>(b) * a.Hq + h) * a.Nq, QBLK, L::QCH, lane, a.status);
-        if (j >= 0 && a.kg != nullptr)
-          gather_rows(kdst, &tk, &cs.k_full[kst], a.kg, KBLK * j, a.Nk,
-                      (static_cast<int64_t>(b) * a.Hkv + kvh) * a.Nk, KBLK, L::QCH, lane, a.status);
-      }
       if (jprev >= 0) {
         const int u = t - 1, vst = u % VST;
         if (!mbar_wait(&cs.v_empty[vst], ((u / VST) & 1) ^ 1, abort, a.status)) break;
@@ -740,10 +699,7 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
   a.q = static_cast<const __nv_bfloat16 *>(l.q);
   a.q_sb = l.q_sb; a.q_sh = l.q_sh; a.q_sn = l.q_sn;
   a.qperm = l.qperm;
-  a.kg = l.kg;
-  a.qg = l.qg;
   if (static_cast<int64_t>(a.B) * a.Hq * a.nqb == 0) return cudaSuccess;
-  if ((l.kg || l.qg) && l.q8 != 0 && l.q8 != 3) return cudaErrorInvalidValue;  // gathers read bf16 rows
   if (l.q8 != 0 && l.d != 128) return cudaErrorInvalidValue;
   if (l.q8 == 3) return launch_t<128, 3, 3, false, true>(l, a, st);  // bf16 Q.K^T, e4m3 P.V
   if (l.q8 == 2) return launch_t<128, 4, 3, true, true>(l, a, st);

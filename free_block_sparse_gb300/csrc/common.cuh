@@ -124,19 +124,6 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
-// TMA gather of four rows: rows r0..r3 of a 2-D tensor map whose box is one row of 128 bytes, at
-// column x, into four consecutive 128-byte rows at dst (the 128-byte swizzle follows the
-// destination address, so a 1024-byte aligned tile filled 512 bytes at a time is laid out as one
-// tiled load would lay it out).
-__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int r0, int r1,
-                                            int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // TMA tensor store shared -> global (bulk-group completion; rows or columns outside the tensor are
 // not written).  The smem source must have been written before a fence_proxy_async_smem() by
 // every writing thread and a barrier.

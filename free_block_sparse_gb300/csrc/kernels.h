@@ -43,9 +43,12 @@ int run_predict(const View &q, const View &k, float topk, float theta, int causa
 int report_error(int code, const char *msg);
 
 // qperm / kperm (or nullptr): token order of q / k; block row t of the pooling is token perm[t] (an
-// entry outside 0..N-1 is reported in *status and read as a zero token).
+// entry outside 0..N-1 is reported in *status and read as a zero token).  qcopy / kcopy (or
+// nullptr; used only with the order): contiguous (B, H, N, d) bf16 buffers that receive the rows
+// in that order as they are read (zero rows for bad entries).
 cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, cudaStream_t st,
-                            const int32_t *qperm = nullptr, const int32_t *kperm = nullptr, int *status = nullptr);
+                            const int32_t *qperm = nullptr, const int32_t *kperm = nullptr, int *status = nullptr,
+                            void *qcopy = nullptr, void *kcopy = nullptr);
 
 // Pooled scores S = scale * muQ . muK^T on tcgen05 (bf16 hi/lo split, three products), for the
 // valid (causal) key blocks of every query block.  The four maps cover qhi, qlo (3-D: d, nqb,
@@ -91,9 +94,6 @@ struct AttnLaunch {
   const void *q;           // bf16 Q, read row by row into TMEM at d = 64 (the ordered copy under a token order
                            // at d = 128, where the rows come by TMA)
   const int32_t *qperm;    // d = 64 under a token order: Q row t of the block is token qperm[t] of q
-  // Token order gathered by TMA (or nullptr): tk (and tq when qg is set) are then 2-D maps over
-  // all rows of k (q), box 64 columns x 1 row, and tile row t is row token_order[t] of its head
-  const int32_t *kg, *qg;
   int64_t q_sb, q_sh, q_sn;
 };
 

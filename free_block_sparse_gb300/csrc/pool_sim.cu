@@ -9,7 +9,8 @@
 // accumulates, so many warps per SM keep enough bytes in flight to hold HBM busy; fp32 (packed
 // pair) arithmetic, warp-shuffle reductions, vector stores of the results.  Under a token order
 // (Hilbert order of image or video tokens) a block's rows are gathered whole through the order
-// (its indices read once into shared memory), so the pooling needs no ordered copy of Q or K.
+// (its indices read once into shared memory), so the pooling needs no ordered copy of Q or K; it
+// writes the ordered copies the later kernels read as it goes (the rows are in its registers).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -24,6 +25,8 @@ struct PoolArgs {
   PredictWs ws;
   const int32_t *qperm, *kperm;  // token orders (or nullptr): block row t is token perm[t]
   int *status;
+  __nv_bfloat16 *qcopy, *kcopy;  // with a token order: contiguous (B, H, N, d) copies in that order
+                                 // that the pooling writes as it reads the rows (or nullptr)
 };
 
 constexpr int INFLIGHT = 8;  // 16-byte loads in flight per lane
@@ -74,6 +77,14 @@ __global__ void __launch_bounds__(128, GATHER ? 4 : 5) pool_sim_kernel(PoolArgs 
     const int32_t *perm = isQ ? a.qperm : a.kperm;
     const __nv_bfloat16 *hbase = base - static_cast<int64_t>(idx) * rows * sn + part * 8;
     int *wperm = GATHER ? sperm[(threadIdx.x >> 5) & 3] : nullptr;
+    // the block's rows of the ordered copy (this lane's 16 bytes of row 0), when one is wanted
+    __nv_bfloat16 *cpy = nullptr;
+    if constexpr (GATHER) {
+      __nv_bfloat16 *cbase = isQ ? a.qcopy : a.kcopy;
+      if (cbase != nullptr)
+        cpy = cbase + ((static_cast<int64_t>(b) * (isQ ? a.Hq : a.Hkv) + h) * ntok + static_cast<int64_t>(idx) * rows) * D +
+              part * 8;
+    }
     if constexpr (GATHER) {
       if (perm != nullptr) {  // one coalesced read of the block's indices; bad ones become -1
         __syncwarp();  // every lane is done with the previous block's indices
@@ -104,6 +115,10 @@ __global__ void __launch_bounds__(128, GATHER ? 4 : 5) pool_sim_kernel(PoolArgs 
       for (int u = 0; u < IFL; ++u) {
         const uint4 v = buf[u];
         if (s0 + IFL + u < steps) buf[u] = load(s0 + IFL + u);
+        if constexpr (GATHER) {
+          const int t = (s0 + u) * TPW + sub;
+          if (cpy != nullptr && t < n) *reinterpret_cast<uint4 *>(cpy + static_cast<int64_t>(t) * D) = v;
+        }
         const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
         float2 x2[4];
 #pragma unroll
@@ -174,7 +189,7 @@ __global__ void __launch_bounds__(128, GATHER ? 4 : 5) pool_sim_kernel(PoolArgs 
 }  // namespace
 
 cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, cudaStream_t st, const int32_t *qperm,
-                            const int32_t *kperm, int *status) {
+                            const int32_t *kperm, int *status, void *qcopy, void *kcopy) {
   PoolArgs a;
   a.q = static_cast<const __nv_bfloat16 *>(q.data);
   a.k = static_cast<const __nv_bfloat16 *>(k.data);
@@ -191,6 +206,8 @@ cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, c
   a.qperm = qperm;
   a.kperm = kperm;
   a.status = status;
+  a.qcopy = qperm ? static_cast<__nv_bfloat16 *>(qcopy) : nullptr;
+  a.kcopy = kperm ? static_cast<__nv_bfloat16 *>(kcopy) : nullptr;
   if (a.total == 0) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);

@@ -131,14 +131,17 @@ typedef struct sparge_params {
    * token_order[t] of q, k and v: blocks, mask (and mask_out) refer to that sequence, and o is
    * written back in the original order (o token token_order[t] receives row t).  The result is
    * that of sparge_permute_tokens on q, k and v, the call, and sparge_unpermute_tokens on the
-   * output, without the separate V and output passes: the call copies K, and Q where d = 128 or
-   * an 8-bit precision needs it, into the workspace in the new order (the space is
-   * sparge_workspace_bytes(op | SPARGE_OP_TOKEN_ORDER, ...) either way); pooling and the d = 64
-   * attention read Q rows through the order instead, mask prediction alone copies nothing;
-   * V is gathered while it is converted or quantised, and the attention kernel writes each
-   * output row straight to its original position.  token_order should be a permutation of 0..N-1; an entry
-   * outside that range is never used as an address (its row is skipped or zero) and records
-   * SPARGE_ERR_INVALID_ARG in the device status word. */
+   * output, without the separate V and output passes: the attention reads K, and Q where d = 128
+   * or an 8-bit precision needs it, from copies in the new order in the workspace (the space is
+   * sparge_workspace_bytes(op | SPARGE_OP_TOKEN_ORDER, ...) either way).  In sparge_attn_ex the
+   * mask prediction's pooling, which reads every row through the order, writes those copies as
+   * it goes (no separate copy pass); sparge_block_sparse_attn_ex, which has no pooling, copies
+   * them in a pass of its own.  The d = 64 attention reads Q rows through the order itself,
+   * mask prediction alone copies nothing, V is gathered while it is converted or quantised, and
+   * the attention kernel writes each output row straight to its original position.
+   * token_order should be a permutation of 0..N-1; an entry outside that range is never used as
+   * an address (its row is skipped or zero) and records SPARGE_ERR_INVALID_ARG in the device
+   * status word. */
   const int32_t *token_order;
   /* How topk (and topk_per_head) picks blocks: enum sparge_topk_mode (0, the cumulative reading,
    * when the struct is zeroed).  Used by sparge_predict_mask_ex and sparge_attn_ex. */
