@@ -307,9 +307,20 @@ bool is_q8(int precision) {
          precision == SPARGE_PRECISION_BF16_FP8PV;
 }
 
+// bf16: the f16 copy of V, or (decoding calls) the chunks' partial rows, whichever is larger
 size_t attn_ws_bytes(int precision, int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d) {
   if (is_q8(precision)) return d == 128 ? q8_ws_bytes(B, Hq, Hkv, Nq, Nk, d) : 0;
-  return v16_bytes(B, Hkv, Nk, d);
+  const size_t v16 = v16_bytes(B, Hkv, Nk, d), part = decode_part_bytes(B, Hkv, Nk, d);
+  return v16 > part ? v16 : part;
+}
+
+// Few queries per head against many keys (decoding, short chunks): the G Nq rows of a KV head's
+// heads share one tile and the key blocks are split over CTAs (bf16, lambda off, no token order;
+// the split needs the order of visiting tiles not to matter, which holds without the filter).
+bool use_decode(const View &q, const View &k, int precision, float lambda, const HeadParams &hp, const int32_t *perm) {
+  const int64_t G = q.H / k.H;
+  return precision == SPARGE_PRECISION_BF16 && lambda == -INFINITY && hp.lambda == nullptr && perm == nullptr &&
+         G * q.N <= 128 && cdiv(k.N, KBLK) >= 32;
 }
 
 int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, float lambda, int causal, float scale,
@@ -364,6 +375,20 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
     l.sq = w.sq;
     l.sk = w.sk;
     l.sv = w.sv;
+  } else if (use_decode(q, k, precision, lambda, hp, perm)) {
+    // decoding tiles read Q rows, K and V (bf16) in place; the workspace holds the partial rows
+    if ((rc = record_event(ev, 4, s))) return rc;
+    const DecodeSplit sp = decode_split(k.B, k.H, k.N);
+    const size_t rows = static_cast<size_t>(k.B * k.H) * sp.nchunk * 128;
+    l.decode = 1;
+    l.nchunk = sp.nchunk;
+    l.chunk_blocks = sp.chunk_blocks;
+    l.part_o = static_cast<float *>(ws);
+    l.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + align256(rows * q.d * 4));
+    if ((rc = make_map(&l.tq, q, 128, "q"))) return rc;  // checks the alignment the row reads rely on
+    l.q = q.data;
+    l.q_sb = q.sb; l.q_sh = q.sh; l.q_sn = q.sn;
+    if ((rc = make_map(&l.tk, k, 64, "k")) || (rc = make_map(&l.tv, v, 64, "v"))) return rc;
   } else {
     cudaError_t e = launch_convert_v_f16(v, ws, perm, status_ptr(), s);
     if (e != cudaSuccess) return cuda_fail(e, "convert_v launch");
@@ -462,10 +487,10 @@ size_t sparge_workspace_bytes(int op, int64_t B, int64_t Hq, int64_t Hkv, int64_
     case SPARGE_OP_PREDICT_MASK:
       return predict_ws_bytes(B, Hq, Hkv, N, N, d);
     case SPARGE_OP_BLOCK_SPARSE_ATTN:
-      return v16_bytes(B, Hkv, N, d);
+      return attn_ws_bytes(SPARGE_PRECISION_BF16, B, Hq, Hkv, N, N, d);
     case SPARGE_OP_ATTN:
       return predict_ws_bytes(B, Hq, Hkv, N, N, d) + align256((size_t)B * Hq * cdiv(N, QBLK) * cdiv(N, KBLK)) +
-             v16_bytes(B, Hkv, N, d);
+             attn_ws_bytes(SPARGE_PRECISION_BF16, B, Hq, Hkv, N, N, d);
     case SPARGE_OP_BLOCK_SPARSE_ATTN_Q8:
       return attn_ws_bytes(SPARGE_PRECISION_Q8, B, Hq, Hkv, N, N, d);
     case SPARGE_OP_ATTN_Q8:

@@ -58,20 +58,29 @@ struct AttnArgs {
   const __nv_bfloat16 *q;     // bf16 path: Q rows, copied into TMEM by the softmax warps
   const int32_t *qperm;       // token order of those rows (or nullptr)
   int64_t q_sb, q_sh, q_sn;
+  // decoding tiles: the key blocks of a (batch, KV head) are split into nchunk chunks of
+  // chunk_blocks; partial results go to part_o [B Hkv][nchunk][128][D] and part_ml (m, l) per row
+  int nchunk, chunk_blocks;
+  float *part_o, *part_ml;
 };
 
 // Warp-collective walk over the kept, valid key blocks of one mask row in ascending order, run
 // by the producer warp only: windows of 512 candidates, 16 per lane loaded as independent bytes,
 // then lowest lane / lowest bit first.  Returns -1 after the last kept block.
+// A decoding tile walks the union of the mask rows of its G heads (gstride bytes apart) from block
+// lo on.
 struct KeptScan {
   const uint8_t *row;
-  int n, base, t;
+  int n, base, t, G;
+  int64_t gstride;
   uint32_t bits;  // this lane's 16 flags of the current window
-  __device__ void init(const uint8_t *r, int n_valid) {
+  __device__ void init(const uint8_t *r, int n_valid, int lo = 0, int g = 1, int64_t gs = 0) {
     row = r;
     n = n_valid;
-    base = -512;
-    t = 0;
+    base = lo - 512;
+    t = lo;
+    G = g;
+    gstride = gs;
     bits = 0u;
   }
   __device__ int next(int lane) {
@@ -90,7 +99,11 @@ struct KeptScan {
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const int j = base + 16 * lane + c;
-        if (j < n && __ldg(row + j) != 0) f |= 1u << c;
+        if (j < n) {
+          bool keep = false;
+          for (int g = 0; g < G; ++g) keep = keep || __ldg(row + g * gstride + j) != 0;
+          if (keep) f |= 1u << c;
+        }
       }
       bits = f;
     }
@@ -145,7 +158,7 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= 512, "control block");
 
-template <int D, int KST, int VST, bool QK8, bool PV8>
+template <int D, int KST, int VST, bool QK8, bool PV8, bool DEC>
 __global__ void __launch_bounds__(NTHREADS, 2)
     bsattn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const AttnArgs a) {
@@ -164,12 +177,26 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 
   // work item: (b, kvh) outermost so concurrently resident CTAs share K/V in L2; within it the
   // query blocks go from last to first (most causal work first), heads of a group adjacent.
-  const int per_bk = a.nqb * a.G;
-  const int bk = blockIdx.x / per_bk, rem = blockIdx.x % per_bk;
-  const int b = bk / a.Hkv, kvh = bk % a.Hkv;
-  const int i = a.nqb - 1 - rem / a.G;
-  const int h = kvh * a.G + rem % a.G;
-  const int n_valid = a.causal ? min(a.nkb, causal_key_blocks(i, a.off)) : a.nkb;
+  // A decoding tile (DEC) holds the Nq query rows of all G heads of one KV head (row g Nq + qi is
+  // query qi of head kvh G + g) against one chunk of the key blocks.
+  int b, kvh, i, h, lo = 0, n_valid;
+  if constexpr (DEC) {
+    const int chunk = blockIdx.x % a.nchunk, bk = blockIdx.x / a.nchunk;
+    b = bk / a.Hkv;
+    kvh = bk % a.Hkv;
+    i = 0;
+    h = kvh * a.G;  // the group's first head
+    lo = chunk * a.chunk_blocks;
+    n_valid = min(a.nkb, lo + a.chunk_blocks);  // causal visibility is row by row in the softmax
+  } else {
+    const int per_bk = a.nqb * a.G;
+    const int bk = blockIdx.x / per_bk, rem = blockIdx.x % per_bk;
+    b = bk / a.Hkv;
+    kvh = bk % a.Hkv;
+    i = a.nqb - 1 - rem / a.G;
+    h = kvh * a.G + rem % a.G;
+    n_valid = a.causal ? min(a.nkb, causal_key_blocks(i, a.off)) : a.nkb;
+  }
   const uint8_t *mrow = a.mask ? a.mask + ((static_cast<int64_t>(b) * a.Hq + h) * a.nqb + i) * a.nkb : nullptr;
 
   // TMEM columns: d = 128: O [0, 128), score buffers [128, 192) and [192, 256), Q in shared memory;
@@ -184,11 +211,15 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   constexpr int QCOL = (D == 128) ? 128 : 192;
   constexpr uint32_t TMEM_COLS = 256;
   constexpr uint32_t IDESC_S = QK8 ? idesc_f32acc(128, 64, FMT_E4M3, false) : idesc_f32acc(128, 64, FMT_BF16, false);
-  constexpr uint32_t IDESC_PV = PV8 ? idesc_f32acc(128, D, FMT_E4M3, false) : idesc_f32acc(128, D, FMT_F16, true);
+  // P.V: e4m3, f16 (V copied to f16), or bf16 for decoding tiles, which read V in place
+  constexpr uint32_t IDESC_PV = PV8 ? idesc_f32acc(128, D, FMT_E4M3, false)
+                                    : idesc_f32acc(128, D, DEC ? FMT_BF16 : FMT_F16, true);
   constexpr int KSTEPS = D * L::EB / 32;  // 32 bytes of the contraction per MMA: K = 16 (bf16) or 32 (e4m3)
 
   if (threadIdx.x == 0) {
-    mbar_init(&cs.q_full, QTM ? 128 : 1);  // bf16: the 128 softmax threads after their Q rows are in TMEM
+    // the 128 softmax threads after their Q rows are in TMEM (d = 64 bf16) or in shared memory
+    // (decoding tiles); else the producer's TMA load
+    mbar_init(&cs.q_full, (QTM || DEC) ? 128 : 1);
     for (int s = 0; s < KST; ++s) {
       mbar_init(&cs.k_full[s], 1);
       mbar_init(&cs.k_empty[s], 1);
@@ -234,7 +265,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     // follows P.V.  After the last tile the next K stage and j slot get the end mark (-1, a plain
     // arrive without data).
     KeptScan ks;
-    ks.init(mrow, n_valid);
+    if constexpr (DEC)
+      ks.init(mrow, n_valid, lo, a.G, static_cast<int64_t>(a.nqb) * a.nkb);
+    else
+      ks.init(mrow, n_valid);
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
@@ -251,7 +285,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         mbar_arrive(&cs.j_full[js]);
         cs.jk[kst] = j;
         if (j >= 0) {
-          if (!QTM && t == 0) {
+          if (!QTM && !DEC && t == 0) {
             mbar_arrive_expect_tx(&cs.q_full, L::Q_BYTES);
             for (int c = 0; c < L::QCH; ++c)
               tma_load_4d(smem + L::OFF_Q + c * 16384, &tq, &cs.q_full, (128 / L::EB) * c, QBLK * i, h, b);
@@ -346,7 +380,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
       if (a.stats) {
         atomicAdd(a.stats + 0, static_cast<unsigned long long>(u));
-        atomicAdd(a.stats + 3, static_cast<unsigned long long>(n_valid));
+        atomicAdd(a.stats + 3, static_cast<unsigned long long>(n_valid - lo));
       }
     }
     __syncwarp();
@@ -402,8 +436,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   } else {
     // ------------------------------------ softmax warps ------------------------------------
     const int r = warp * 32 + lane;
-    const int row_g = QBLK * i + r;
-    const bool row_ok = row_g < a.Nq;
+    // the row's query index and head: row r of query block i of head h, or (decoding tile) query
+    // r % Nq of head h + r / Nq, rows past G Nq empty
+    int row_g = QBLK * i + r, hrow = h;
+    bool row_ok = row_g < a.Nq;
+    const uint8_t *hmask = nullptr;  // decoding tile: this row's head's mask row
+    if constexpr (DEC) {
+      row_ok = r < a.G * a.Nq;
+      row_g = row_ok ? r % a.Nq : 0;
+      hrow = h + (row_ok ? r / a.Nq : 0);
+      if (a.mask) hmask = a.mask + (static_cast<int64_t>(b) * a.Hq + hrow) * a.nqb * a.nkb;
+    }
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
     int nskip = 0, T = 0;
@@ -432,7 +475,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           qok = false;
         }
       }
-      const uint4 *qsrc = reinterpret_cast<const uint4 *>(a.q + b * a.q_sb + h * a.q_sh + static_cast<int64_t>(qrow) * a.q_sn);
+      const uint4 *qsrc = reinterpret_cast<const uint4 *>(a.q + b * a.q_sb + hrow * a.q_sh + static_cast<int64_t>(qrow) * a.q_sn);
 #pragma unroll
       for (int half = 0; half < D / 64; ++half) {
         uint32_t w[32];
@@ -448,6 +491,19 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
       tmem_st_wait();
       tc_fence_before();
+      mbar_arrive(&cs.q_full);
+    } else if constexpr (DEC) {
+      // this thread's Q row (zeros for the empty rows) into the shared-memory Q tile, 16-byte pieces
+      // in the 128-byte swizzle the score product's descriptor expects
+      const uint4 *qsrc = reinterpret_cast<const uint4 *>(a.q + b * a.q_sb + hrow * a.q_sh + static_cast<int64_t>(row_g) * a.q_sn);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const uint4 v = row_ok ? __ldg(qsrc + 8 * c + p) : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4 *>(smem + L::OFF_Q + c * 16384 + r * 128 + ((p ^ (r & 7)) << 4)) = v;
+        }
+      fence_proxy_async_smem();  // generic writes read by the tensor core
       mbar_arrive(&cs.q_full);
     }
     float sq_blk = 1.f;
@@ -502,13 +558,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
       // a tile with hidden columns (causal diagonal, ragged key tail) or rows past the query length;
       // the vote makes the branch warp-uniform, so interior tiles skip the masking code entirely
-      const bool edge = (a.causal && KBLK * j + KBLK - 1 > a.off + QBLK * i) || (KBLK * j + KBLK > a.Nk) ||
+      // (decoding tiles always take it: their rows have their own heads' masks)
+      const bool edge = DEC || (a.causal && KBLK * j + KBLK - 1 > a.off + QBLK * i) || (KBLK * j + KBLK > a.Nk) ||
                         (QBLK * i + QBLK > a.Nq);
       float mraw = mhw;
       if (__any_sync(0xffffffffu, edge)) {
         int lim = a.causal ? a.off + row_g - KBLK * j : 1 << 30;  // cols c > lim are hidden
         lim = min(lim, a.Nk - 1 - KBLK * j);
         if (!row_ok) lim = -1;
+        if constexpr (DEC) {
+          if (hmask != nullptr && __ldg(hmask + j) == 0) lim = -1;  // not kept by this row's head
+        }
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
         // the maximum of what stays visible
@@ -569,7 +629,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         const float2 e2 = ffma2(make_float2(x[2 * c], x[2 * c + 1]), sc2, nr2);
         const float2 p2 = make_float2(fast_exp2(e2.x), fast_exp2(e2.y));
         rs2[c & 3] = fadd2(rs2[c & 3], p2);  // four independent chains
-        pk[c] = PV8 ? pack_e4m3x2(p2.x, p2.y) : pack_f16x2(p2.x, p2.y);
+        pk[c] = PV8 ? pack_e4m3x2(p2.x, p2.y) : (DEC ? pack_bf16x2(p2.x, p2.y) : pack_f16x2(p2.x, p2.y));
       }
       {
         const float2 rs = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
@@ -590,7 +650,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
       tmem_st_wait();
       if (lane == 0) cs.skip[buf][warp] = wskip ? 1 : 0;
-      nskip += (wskip && QBLK * i + warp * 32 < a.Nq) ? 1 : 0;
+      nskip += (wskip && (DEC ? warp * 32 < a.G * a.Nq : QBLK * i + warp * 32 < a.Nq)) ? 1 : 0;
       tc_fence_before();
       mbar_arrive(&cs.p_full[buf]);
     }
@@ -601,53 +661,79 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       tc_fence_after();
       have_o = ok && cs.pv_any != 0;
     }
-    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-    const float *svrow = PV8 ? a.sv + (static_cast<int64_t>(b) * a.Hkv + kvh) * D : nullptr;
-    // the output row: token row_g, or token perm[row_g] of o under a token order (an entry outside
-    // 0..N-1 is reported and its row left unwritten)
-    int orow_t = row_g;
-    bool write_row = row_ok;
-    if (a.perm && row_ok) {
-      orow_t = __ldg(a.perm + row_g);
-      if (static_cast<unsigned>(orow_t) >= static_cast<unsigned>(a.Nq)) {
-        record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
-        write_row = false;
-        orow_t = 0;
-      }
-    }
-    __nv_bfloat16 *orow = a.o + b * a.o_sb + h * a.o_sh + static_cast<int64_t>(orow_t) * a.o_sn;
+    if constexpr (DEC) {
+      // decoding tile: this row's partial result over the chunk, relative to 2^m_ref (O and l share
+      // the exponent reference), for the combining kernel; rows that saw no visible key give l = 0
+      const int chunk = blockIdx.x % a.nchunk, bk = blockIdx.x / a.nchunk;
+      const int64_t prow = (static_cast<int64_t>(bk) * a.nchunk + chunk) * 128 + r;
+      float4 *po = reinterpret_cast<float4 *>(a.part_o + prow * D);
 #pragma unroll 1
-    for (int q = 0; q < D / 16; ++q) {
-      uint32_t rr[16];
-      if (have_o) {
-        tmem_ld16(tl + 16 * q, rr);
-        tmem_ld_wait();
-      } else {
+      for (int q = 0; q < D / 16; ++q) {
+        uint32_t rr[16];
+        if (have_o) {
+          tmem_ld16(tl + 16 * q, rr);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) rr[c] = 0u;
+          for (int c = 0; c < 16; ++c) rr[c] = 0u;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          po[4 * q + c] = make_float4(__uint_as_float(rr[4 * c]), __uint_as_float(rr[4 * c + 1]),
+                                      __uint_as_float(rr[4 * c + 2]), __uint_as_float(rr[4 * c + 3]));
       }
-      if constexpr (PV8) {  // undo the per-channel V scale
-#pragma unroll
-        for (int c = 0; c < 16; c += 4) {
-          const float4 s4 = __ldg(reinterpret_cast<const float4 *>(svrow + 16 * q + c));
-          rr[c] = __float_as_uint(__uint_as_float(rr[c]) * s4.x);
-          rr[c + 1] = __float_as_uint(__uint_as_float(rr[c + 1]) * s4.y);
-          rr[c + 2] = __float_as_uint(__uint_as_float(rr[c + 2]) * s4.z);
-          rr[c + 3] = __float_as_uint(__uint_as_float(rr[c + 3]) * s4.w);
+      const bool any = have_o && l > 0.f;
+      a.part_ml[2 * prow] = any ? m_ref : -INFINITY;
+      a.part_ml[2 * prow + 1] = any ? l : 0.f;
+    } else {
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const float *svrow = PV8 ? a.sv + (static_cast<int64_t>(b) * a.Hkv + kvh) * D : nullptr;
+      // the output row: token row_g, or token perm[row_g] of o under a token order (an entry outside
+      // 0..N-1 is reported and its row left unwritten)
+      int orow_t = row_g;
+      bool write_row = row_ok;
+      if (a.perm && row_ok) {
+        orow_t = __ldg(a.perm + row_g);
+        if (static_cast<unsigned>(orow_t) >= static_cast<unsigned>(a.Nq)) {
+          record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
+          write_row = false;
+          orow_t = 0;
         }
       }
-      uint4 o0, o1;
-      o0.x = pack_bf16x2(__uint_as_float(rr[0]) * inv_l, __uint_as_float(rr[1]) * inv_l);
-      o0.y = pack_bf16x2(__uint_as_float(rr[2]) * inv_l, __uint_as_float(rr[3]) * inv_l);
-      o0.z = pack_bf16x2(__uint_as_float(rr[4]) * inv_l, __uint_as_float(rr[5]) * inv_l);
-      o0.w = pack_bf16x2(__uint_as_float(rr[6]) * inv_l, __uint_as_float(rr[7]) * inv_l);
-      o1.x = pack_bf16x2(__uint_as_float(rr[8]) * inv_l, __uint_as_float(rr[9]) * inv_l);
-      o1.y = pack_bf16x2(__uint_as_float(rr[10]) * inv_l, __uint_as_float(rr[11]) * inv_l);
-      o1.z = pack_bf16x2(__uint_as_float(rr[12]) * inv_l, __uint_as_float(rr[13]) * inv_l);
-      o1.w = pack_bf16x2(__uint_as_float(rr[14]) * inv_l, __uint_as_float(rr[15]) * inv_l);
-      if (write_row) {
-        *reinterpret_cast<uint4 *>(orow + 16 * q) = o0;
-        *reinterpret_cast<uint4 *>(orow + 16 * q + 8) = o1;
+      __nv_bfloat16 *orow = a.o + b * a.o_sb + h * a.o_sh + static_cast<int64_t>(orow_t) * a.o_sn;
+  #pragma unroll 1
+      for (int q = 0; q < D / 16; ++q) {
+        uint32_t rr[16];
+        if (have_o) {
+          tmem_ld16(tl + 16 * q, rr);
+          tmem_ld_wait();
+        } else {
+  #pragma unroll
+          for (int c = 0; c < 16; ++c) rr[c] = 0u;
+        }
+        if constexpr (PV8) {  // undo the per-channel V scale
+  #pragma unroll
+          for (int c = 0; c < 16; c += 4) {
+            const float4 s4 = __ldg(reinterpret_cast<const float4 *>(svrow + 16 * q + c));
+            rr[c] = __float_as_uint(__uint_as_float(rr[c]) * s4.x);
+            rr[c + 1] = __float_as_uint(__uint_as_float(rr[c + 1]) * s4.y);
+            rr[c + 2] = __float_as_uint(__uint_as_float(rr[c + 2]) * s4.z);
+            rr[c + 3] = __float_as_uint(__uint_as_float(rr[c + 3]) * s4.w);
+          }
+        }
+        uint4 o0, o1;
+        o0.x = pack_bf16x2(__uint_as_float(rr[0]) * inv_l, __uint_as_float(rr[1]) * inv_l);
+        o0.y = pack_bf16x2(__uint_as_float(rr[2]) * inv_l, __uint_as_float(rr[3]) * inv_l);
+        o0.z = pack_bf16x2(__uint_as_float(rr[4]) * inv_l, __uint_as_float(rr[5]) * inv_l);
+        o0.w = pack_bf16x2(__uint_as_float(rr[6]) * inv_l, __uint_as_float(rr[7]) * inv_l);
+        o1.x = pack_bf16x2(__uint_as_float(rr[8]) * inv_l, __uint_as_float(rr[9]) * inv_l);
+        o1.y = pack_bf16x2(__uint_as_float(rr[10]) * inv_l, __uint_as_float(rr[11]) * inv_l);
+        o1.z = pack_bf16x2(__uint_as_float(rr[12]) * inv_l, __uint_as_float(rr[13]) * inv_l);
+        o1.w = pack_bf16x2(__uint_as_float(rr[14]) * inv_l, __uint_as_float(rr[15]) * inv_l);
+        if (write_row) {
+          *reinterpret_cast<uint4 *>(orow + 16 * q) = o0;
+          *reinterpret_cast<uint4 *>(orow + 16 * q + 8) = o1;
+        }
       }
     }
     if (a.stats && lane == 0 && nskip) atomicAdd(a.stats + 2, static_cast<unsigned long long>(nskip));
@@ -659,17 +745,63 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int D, int KST, int VST, bool QK8, bool PV8>
+template <int D, int KST, int VST, bool QK8, bool PV8, bool DEC = false>
 cudaError_t launch_t(const AttnLaunch &l, const AttnArgs &a, cudaStream_t st) {
   // each CTA allocates 256 TMEM columns, half of the SM's: at least 77 KB of shared memory keeps a
   // third CTA off the SM (it would only wait in tcgen05.alloc)
   constexpr uint32_t MIN_SMEM = 77u * 1024u;
   const uint32_t smem = Smem<D, KST, VST, QK8, PV8>::TOTAL > MIN_SMEM ? Smem<D, KST, VST, QK8, PV8>::TOTAL : MIN_SMEM;
   static std::atomic<unsigned long long> smem_set{0};
-  if (cudaError_t e = set_smem_limit_once(bsattn_kernel<D, KST, VST, QK8, PV8>, static_cast<int>(smem), smem_set); e != cudaSuccess) return e;
-  const int64_t grid = static_cast<int64_t>(a.B) * a.Hq * a.nqb;
-  bsattn_kernel<D, KST, VST, QK8, PV8><<<static_cast<unsigned>(grid), NTHREADS, smem, st>>>(l.tq, l.tk, l.tv, a);
+  if (cudaError_t e = set_smem_limit_once(bsattn_kernel<D, KST, VST, QK8, PV8, DEC>, static_cast<int>(smem), smem_set);
+      e != cudaSuccess)
+    return e;
+  const int64_t grid = DEC ? static_cast<int64_t>(a.B) * a.Hkv * a.nchunk : static_cast<int64_t>(a.B) * a.Hq * a.nqb;
+  bsattn_kernel<D, KST, VST, QK8, PV8, DEC><<<static_cast<unsigned>(grid), NTHREADS, smem, st>>>(l.tq, l.tk, l.tv, a);
   return cudaGetLastError();
+}
+
+// The partial rows of a decoding call's chunks combined into the output: one warp per output row
+// (b, h, qi), lanes across the channels.  With M the largest exponent reference over the chunks,
+// O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c (0 where no chunk saw a visible key).
+template <int D>
+__global__ void __launch_bounds__(256) decode_combine_kernel(const float *part_o, const float *part_ml, int nchunk,
+                                                             int B, int Hq, int Hkv, int Nq, __nv_bfloat16 *o,
+                                                             int64_t o_sb, int64_t o_sh, int64_t o_sn) {
+  constexpr int PER = D / 32;
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= static_cast<int64_t>(B) * Hq * Nq) return;
+  const int qi = static_cast<int>(wid % Nq);
+  const int64_t bh = wid / Nq;
+  const int h = static_cast<int>(bh % Hq), b = static_cast<int>(bh / Hq);
+  const int G = Hq / Hkv, kvh = h / G, r = (h % G) * Nq + qi;
+  const int64_t base = (static_cast<int64_t>(b) * Hkv + kvh) * nchunk;
+  float M = -INFINITY;
+  for (int c = lane; c < nchunk; c += 32) {
+    const int64_t pr = (base + c) * 128 + r;
+    if (part_ml[2 * pr + 1] > 0.f) M = fmaxf(M, part_ml[2 * pr]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float L = 0.f, acc[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+  if (M != -INFINITY) {
+    for (int c = 0; c < nchunk; ++c) {
+      const int64_t pr = (base + c) * 128 + r;
+      const float lc = part_ml[2 * pr + 1];
+      if (!(lc > 0.f)) continue;
+      const float w = exp2f(part_ml[2 * pr] - M);
+      L = fmaf(w, lc, L);
+      const float *oc = part_o + pr * D;
+#pragma unroll
+      for (int k = 0; k < PER; ++k) acc[k] = fmaf(w, oc[lane + 32 * k], acc[k]);
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16 *orow = o + b * o_sb + h * o_sh + static_cast<int64_t>(qi) * o_sn;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) orow[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
 }
 
 }  // namespace
@@ -701,6 +833,25 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
   a.qperm = l.qperm;
   if (static_cast<int64_t>(a.B) * a.Hq * a.nqb == 0) return cudaSuccess;
   if (l.q8 != 0 && l.d != 128) return cudaErrorInvalidValue;
+  if (l.decode) {  // bf16 only: the host picks this path for few queries per head, lambda off
+    if (l.q8 != 0 || a.G * a.Nq > 128 || l.nchunk <= 0) return cudaErrorInvalidValue;
+    a.nchunk = l.nchunk;
+    a.chunk_blocks = l.chunk_blocks;
+    a.part_o = l.part_o;
+    a.part_ml = l.part_ml;
+    cudaError_t e = l.d == 128 ? launch_t<128, 3, 2, false, false, true>(l, a, st)
+                               : launch_t<64, 4, 3, false, false, true>(l, a, st);
+    if (e != cudaSuccess) return e;
+    const int64_t rows = static_cast<int64_t>(a.B) * a.Hq * a.Nq;
+    const unsigned cgrid = static_cast<unsigned>((rows * 32 + 255) / 256);
+    if (l.d == 128)
+      decode_combine_kernel<128><<<cgrid, 256, 0, st>>>(l.part_o, l.part_ml, l.nchunk, a.B, a.Hq, a.Hkv, a.Nq, a.o,
+                                                        a.o_sb, a.o_sh, a.o_sn);
+    else
+      decode_combine_kernel<64><<<cgrid, 256, 0, st>>>(l.part_o, l.part_ml, l.nchunk, a.B, a.Hq, a.Hkv, a.Nq, a.o,
+                                                       a.o_sb, a.o_sh, a.o_sn);
+    return cudaGetLastError();
+  }
   if (l.q8 == 3) return launch_t<128, 3, 3, false, true>(l, a, st);  // bf16 Q.K^T, e4m3 P.V
   if (l.q8 == 2) return launch_t<128, 4, 3, true, true>(l, a, st);
   if (l.q8 == 1) return launch_t<128, 4, 2, true, false>(l, a, st);

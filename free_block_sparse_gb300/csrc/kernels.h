@@ -95,7 +95,36 @@ struct AttnLaunch {
                            // at d = 128, where the rows come by TMA)
   const int32_t *qperm;    // d = 64 under a token order: Q row t of the block is token qperm[t] of q
   int64_t q_sb, q_sh, q_sn;
+  // decoding tiles (decode != 0, bf16): the G Nq <= 128 query rows of a KV head's heads in one
+  // tile, the key blocks split into nchunk chunks of chunk_blocks (decode_split), the chunks'
+  // partial rows in part_o / part_ml, then combined; V is read in place as bf16
+  int decode, nchunk, chunk_blocks;
+  float *part_o, *part_ml;
 };
+
+// How a decoding call splits the key blocks of each (batch, KV head): about two CTAs per SM of a
+// 152-SM part, at least 16 key blocks per chunk.  Sizes both the workspace and the launch.
+struct DecodeSplit {
+  int nchunk, chunk_blocks;
+};
+inline DecodeSplit decode_split(int64_t B, int64_t Hkv, int64_t Nk) {
+  const int64_t nkb = (Nk + 63) / 64, units = B * Hkv > 0 ? B * Hkv : 1;
+  int64_t nchunk = (304 + units - 1) / units;
+  const int64_t most = nkb >= 16 ? nkb / 16 : 1;
+  if (nchunk > most) nchunk = most;
+  if (nchunk < 1) nchunk = 1;
+  const int64_t cb = (nkb + nchunk - 1) / nchunk;
+  DecodeSplit s;
+  s.chunk_blocks = static_cast<int>(cb > 0 ? cb : 1);
+  s.nchunk = static_cast<int>((nkb + s.chunk_blocks - 1) / s.chunk_blocks);
+  return s;
+}
+// Workspace of a decoding call's partial rows: [B Hkv][nchunk][128][d] fp32, then (m, l) per row.
+inline size_t decode_part_bytes(int64_t B, int64_t Hkv, int64_t Nk, int64_t d) {
+  const DecodeSplit s = decode_split(B, Hkv, Nk);
+  const size_t rows = static_cast<size_t>(B * Hkv) * s.nchunk * 128;
+  return ((rows * d * 4 + 255) & ~size_t(255)) + ((rows * 2 * 4 + 255) & ~size_t(255));
+}
 
 cudaError_t launch_bsattn(const AttnLaunch &a, cudaStream_t st);
 

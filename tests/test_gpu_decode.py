@@ -1,0 +1,94 @@
+"""Decoding tiles (few queries per head against many keys): the G Nq query rows of the heads that
+share a KV head are packed into one 128-row tile, the key blocks are split over CTAs and the
+chunks' partial rows combined.  The library takes this path by itself for bf16 calls with the
+lambda filter off, no token order and G Nq <= 128 against at least 32 key blocks; these tests hold
+it to the float64 oracle (given mask: masks that differ per head, heads with nothing kept,
+causal alignment of the last query on the last key, ragged key tails, d = 64 and 128) and to the
+regular kernel."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import free_block_sparse_gb300 as fbs
+import oracle
+import workloads as W
+from gpu_util import COS_MIN, MAXABS, cos_maxabs, dev_bf16, f64, host_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fbs.lib()
+    assert torch.cuda.is_available()
+    yield
+    torch.cuda.synchronize()
+    assert fbs.device_status() == 0
+
+
+def _qkv(seed, B, Hq, Hkv, Nq, Nk, d):
+    qu, _, _ = W.random_qkv(seed, B, Hq, Hkv, Nq, d)
+    _, ku, vu = W.random_qkv(seed + 1, B, Hq, Hkv, Nk, d)
+    return qu, ku, vu
+
+
+def _mask(seed, B, Hq, Nq, Nk, p):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    nqb, nkb = -(-Nq // 128), -(-Nk // 64)
+    m = (rng.random((B, Hq, nqb, nkb)) < p).astype(np.uint8)
+    m[..., -1] = 1  # the last key block (holding the last keys the causal queries see)
+    return m
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal,p", [
+    (1, 32, 8, 1, 4096 + 77, 128, True, 0.3),     # single-token decoding, GQA 4, ragged key tail
+    (1, 8, 2, 4, 3000, 64, False, 0.5),           # a few queries, d = 64, non-causal
+    (2, 16, 2, 16, 8192, 128, True, 0.2),         # G Nq = 128 rows, two batches
+    (1, 4, 4, 1, 2048, 128, False, 1.0),          # no GQA, every block kept
+    (1, 8, 1, 12, 5000, 64, True, 0.25),          # G = 8, d = 64, causal
+])
+def test_decode_matches_oracle(B, Hq, Hkv, Nq, Nk, d, causal, p):
+    qu, ku, vu = _qkv(40, B, Hq, Hkv, Nq, Nk, d)
+    m = _mask(41, B, Hq, Nq, Nk, p)
+    if Hq > 1:
+        m[0, 1] = 0                      # a head that keeps nothing: zero rows
+    out = fbs.block_sparse_attn(dev_bf16(qu), dev_bf16(ku), dev_bf16(vu), torch.from_numpy(m).cuda(), -math.inf,
+                                causal)
+    ref = oracle.block_sparse_attn(f64(qu), f64(ku), f64(vu), m, -math.inf, causal)
+    got = host_f64(out)
+    cos, err = cos_maxabs(got, ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
+    if Hq > 1:
+        assert (got[0, 1] == 0).all()
+
+
+def test_decode_equals_regular_kernel_closely():
+    """The split over key chunks against the regular kernel (taken when the lambda filter is on; a
+    lambda of -1e30 never skips) on the same mask."""
+    B, Hq, Hkv, Nq, Nk, d = 1, 16, 4, 2, 6000, 128
+    qu, ku, vu = _qkv(42, B, Hq, Hkv, Nq, Nk, d)
+    m = torch.from_numpy(_mask(43, B, Hq, Nq, Nk, 0.4)).cuda()
+    q, k, v = dev_bf16(qu), dev_bf16(ku), dev_bf16(vu)
+    a = fbs.block_sparse_attn(q, k, v, m, -math.inf, True)
+    b = fbs.block_sparse_attn(q, k, v, m, -1e30, True)
+    cos, err = cos_maxabs(host_f64(a), host_f64(b))
+    assert cos >= 0.99999 and err <= 1e-2, (cos, err)
+
+
+def test_decode_through_sparge_attn_ex():
+    """A decoding step with the predicted mask: one query token per head continuing a Llama-like
+    sequence of 4296 keys (8 query heads, 2 KV heads)."""
+    w = W.make_config("llama32k", N=4096 + 200, Hq=8, Hkv=2)
+    q = w.q[:, :, -1:]
+    qd, k, v = dev_bf16(np.ascontiguousarray(q)), dev_bf16(w.k), dev_bf16(w.v)
+    mask = torch.empty((1, 8, 1, w.nkb), dtype=torch.uint8, device="cuda")
+    out = fbs.sparge_attn_ex(qd, k, v, w.topk, True, theta=w.theta, mask_out=mask)
+    gm = mask.cpu().numpy()
+    pred = oracle.predict_mask(f64(q), f64(w.k), w.topk, w.theta, True)
+    dec = oracle.decisive_rows(pred, w.topk, w.theta, True)
+    assert not ((gm != pred["mask"]).any(axis=-1) & dec).any()
+    ref = oracle.block_sparse_attn(f64(q), f64(w.k), f64(w.v), gm, -math.inf, True)
+    cos, err = cos_maxabs(host_f64(out), ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
