@@ -236,6 +236,52 @@ def measure_permute(steps, warmup, dev, peaks):
             "pct_hbm": round(100 * gbs / float(peaks["hbm_gbs"]), 2)}
 
 
+def measure_decode(q, k, w, steps, warmup, dev, peaks, v):
+    """One decoding step of a causal workload: the last query token of every head against all the
+    keys (mask prediction of that token, then the decoding tiles that pack the G query rows of a
+    KV head into one tile and split the keys over CTAs), on the bench's own device tensors.  The
+    lambda filter is off (the split over key chunks needs it off).  Algorithmic bytes of the
+    attention: a K and a V tile per key block that any head of a KV head keeps (counted by the
+    kernel), the token's Q and O rows and the mask."""
+    import torch
+    import free_block_sparse_gb300 as fbs
+    B, Hq, _, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    nkb = -(-Nk // 64)
+    qd = q[:, :, -1:]
+    mask = torch.empty((B, Hq, 1, nkb), dtype=torch.uint8, device=dev)
+    ws = torch.empty(fbs.workspace_bytes(fbs.SPARGE_OP_ATTN, B, Hq, Hkv, Nk, d), dtype=torch.uint8, device=dev)
+    o = torch.empty((B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
+    stats = torch.zeros(4, dtype=torch.int64, device=dev)
+
+    def step(events=None, counters=None):
+        fbs.sparge_attn_ex(qd, k, v, w.topk, True, theta=w.theta, lam=-math.inf, mask_out=mask, out=o, ws=ws,
+                           events=events, stats=counters)
+
+    step(counters=stats)
+    torch.cuda.synchronize()
+    tiles = int(stats[0].item())
+    for _ in range(max(warmup, 3)):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for e in evs:
+        step(events=e)
+    torch.cuda.synchronize()
+    assert fbs.device_status() == 0
+    t_step = statistics.median(e[0].elapsed_time(e[5]) for e in evs) / 1e3
+    t_pred = statistics.median(e[0].elapsed_time(e[3]) for e in evs) / 1e3
+    t_attn = statistics.median(e[4].elapsed_time(e[5]) for e in evs) / 1e3
+    nbytes = tiles * 64 * d * 2 * 2 + 2 * 2 * B * Hq * d + mask.numel()
+    gbs = nbytes / t_attn / 1e9
+    return {"workload": "%s decoding step: the last query token of each of the %d heads against the %d keys, "
+                        "predicted mask, lambda off" % (w.name, Hq, Nk),
+            "ms": round(t_step * 1e3, 4), "mask_pred_ms": round(t_pred * 1e3, 4), "attn_ms": round(t_attn * 1e3, 4),
+            "kv_tiles": tiles, "attn_bytes": nbytes, "attn_gbs": round(gbs, 1),
+            "attn_pct_hbm": round(100 * gbs / float(peaks["hbm_gbs"]), 2),
+            "tokens_per_s": round(B / t_step, 1)}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import free_block_sparse_gb300 as fbs
@@ -480,6 +526,8 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
     }
     line["permute"] = measure_permute(max(args.steps, 10), args.warmup, dev, peaks)
+    if w.causal and w.mask is None and w.N // 64 >= 32:
+        line["decode"] = measure_decode(q, k, w, max(args.steps, 10), args.warmup, dev, peaks, v)
     if rank == 0 and not args.no_cpu_baseline:
         tops, wall, desc, ncores = oracle_sample(w, args.cpu_blocks, min(args.cpu_workers, os.cpu_count() or 1))
         line["cpu_baseline"] = {"value": round(tops, 6), "unit": "dense-equiv TOPS", "cores": ncores,

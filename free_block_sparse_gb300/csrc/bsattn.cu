@@ -760,48 +760,47 @@ cudaError_t launch_t(const AttnLaunch &l, const AttnArgs &a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// The partial rows of a decoding call's chunks combined into the output: one warp per output row
-// (b, h, qi), lanes across the channels.  With M the largest exponent reference over the chunks,
+// The partial rows of a decoding call's chunks combined into the output: one CTA of D threads per
+// output row (b, h, qi).  The chunks' exponent references and row sums are staged in shared
+// memory, the largest reference M and the weights 2^(m_c - M) found by the first warp, then
+// thread t sums channel t over the chunks (coalesced rows of the partial outputs):
 // O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c (0 where no chunk saw a visible key).
+constexpr int MAX_DECODE_CHUNKS = 1024;
 template <int D>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const float *part_o, const float *part_ml, int nchunk,
-                                                             int B, int Hq, int Hkv, int Nq, __nv_bfloat16 *o,
-                                                             int64_t o_sb, int64_t o_sh, int64_t o_sn) {
-  constexpr int PER = D / 32;
-  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= static_cast<int64_t>(B) * Hq * Nq) return;
-  const int qi = static_cast<int>(wid % Nq);
-  const int64_t bh = wid / Nq;
-  const int h = static_cast<int>(bh % Hq), b = static_cast<int>(bh / Hq);
+__global__ void __launch_bounds__(D) decode_combine_kernel(const float *part_o, const float *part_ml, int nchunk,
+                                                           int Hq, int Hkv, int Nq, __nv_bfloat16 *o, int64_t o_sb,
+                                                           int64_t o_sh, int64_t o_sn) {
+  __shared__ float wgt[MAX_DECODE_CHUNKS];
+  __shared__ float inv_sum;
+  const int row = blockIdx.x, t = threadIdx.x;
+  const int qi = row % Nq, bh = row / Nq, h = bh % Hq, b = bh / Hq;
   const int G = Hq / Hkv, kvh = h / G, r = (h % G) * Nq + qi;
   const int64_t base = (static_cast<int64_t>(b) * Hkv + kvh) * nchunk;
-  float M = -INFINITY;
-  for (int c = lane; c < nchunk; c += 32) {
+  for (int c = t; c < nchunk; c += D) {  // m_c where the chunk saw a visible key, else -inf
     const int64_t pr = (base + c) * 128 + r;
-    if (part_ml[2 * pr + 1] > 0.f) M = fmaxf(M, part_ml[2 * pr]);
+    wgt[c] = part_ml[2 * pr + 1] > 0.f ? part_ml[2 * pr] : -INFINITY;
   }
+  __syncthreads();
+  if (t < 32) {
+    float M = -INFINITY;
+    for (int c = t; c < nchunk; c += 32) M = fmaxf(M, wgt[c]);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float L = 0.f, acc[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-  if (M != -INFINITY) {
-    for (int c = 0; c < nchunk; ++c) {
-      const int64_t pr = (base + c) * 128 + r;
-      const float lc = part_ml[2 * pr + 1];
-      if (!(lc > 0.f)) continue;
-      const float w = exp2f(part_ml[2 * pr] - M);
-      L = fmaf(w, lc, L);
-      const float *oc = part_o + pr * D;
-#pragma unroll
-      for (int k = 0; k < PER; ++k) acc[k] = fmaf(w, oc[lane + 32 * k], acc[k]);
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int c = t; c < nchunk; c += 32) {
+      const float w = (M == -INFINITY || wgt[c] == -INFINITY) ? 0.f : exp2f(wgt[c] - M);
+      wgt[c] = w;
+      L = fmaf(w, part_ml[2 * ((base + c) * 128 + r) + 1], L);
     }
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  __nv_bfloat16 *orow = o + b * o_sb + h * o_sh + static_cast<int64_t>(qi) * o_sn;
 #pragma unroll
-  for (int k = 0; k < PER; ++k) orow[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (t == 0) inv_sum = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  float acc = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < nchunk; ++c) acc = fmaf(wgt[c], part_o[((base + c) * 128 + r) * D + t], acc);
+  o[b * o_sb + h * o_sh + static_cast<int64_t>(qi) * o_sn + t] = __float2bfloat16_rn(acc * inv_sum);
 }
 
 }  // namespace
@@ -842,14 +841,14 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
     cudaError_t e = l.d == 128 ? launch_t<128, 3, 2, false, false, true>(l, a, st)
                                : launch_t<64, 4, 3, false, false, true>(l, a, st);
     if (e != cudaSuccess) return e;
-    const int64_t rows = static_cast<int64_t>(a.B) * a.Hq * a.Nq;
-    const unsigned cgrid = static_cast<unsigned>((rows * 32 + 255) / 256);
+    if (l.nchunk > MAX_DECODE_CHUNKS) return cudaErrorInvalidValue;
+    const unsigned rows = static_cast<unsigned>(static_cast<int64_t>(a.B) * a.Hq * a.Nq);
     if (l.d == 128)
-      decode_combine_kernel<128><<<cgrid, 256, 0, st>>>(l.part_o, l.part_ml, l.nchunk, a.B, a.Hq, a.Hkv, a.Nq, a.o,
-                                                        a.o_sb, a.o_sh, a.o_sn);
+      decode_combine_kernel<128><<<rows, 128, 0, st>>>(l.part_o, l.part_ml, l.nchunk, a.Hq, a.Hkv, a.Nq, a.o, a.o_sb,
+                                                       a.o_sh, a.o_sn);
     else
-      decode_combine_kernel<64><<<cgrid, 256, 0, st>>>(l.part_o, l.part_ml, l.nchunk, a.B, a.Hq, a.Hkv, a.Nq, a.o,
-                                                       a.o_sb, a.o_sh, a.o_sn);
+      decode_combine_kernel<64><<<rows, 64, 0, st>>>(l.part_o, l.part_ml, l.nchunk, a.Hq, a.Hkv, a.Nq, a.o, a.o_sb,
+                                                     a.o_sh, a.o_sn);
     return cudaGetLastError();
   }
   if (l.q8 == 3) return launch_t<128, 3, 3, false, true>(l, a, st);  // bf16 Q.K^T, e4m3 P.V
