@@ -667,8 +667,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       const int chunk = blockIdx.x % a.nchunk, bk = blockIdx.x / a.nchunk;
       const int64_t prow = (static_cast<int64_t>(bk) * a.nchunk + chunk) * 128 + r;
       float4 *po = reinterpret_cast<float4 *>(a.part_o + prow * D);
+      // only the G Nq rows the combining kernel reads (a warp of empty rows skips it all)
+      const bool warp_rows = __any_sync(0xffffffffu, row_ok);
 #pragma unroll 1
-      for (int q = 0; q < D / 16; ++q) {
+      for (int q = 0; q < (warp_rows ? D / 16 : 0); ++q) {
         uint32_t rr[16];
         if (have_o) {
           tmem_ld16(tl + 16 * q, rr);
@@ -677,14 +679,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
           for (int c = 0; c < 16; ++c) rr[c] = 0u;
         }
+        if (row_ok)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          po[4 * q + c] = make_float4(__uint_as_float(rr[4 * c]), __uint_as_float(rr[4 * c + 1]),
-                                      __uint_as_float(rr[4 * c + 2]), __uint_as_float(rr[4 * c + 3]));
+          for (int c = 0; c < 4; ++c)
+            po[4 * q + c] = make_float4(__uint_as_float(rr[4 * c]), __uint_as_float(rr[4 * c + 1]),
+                                        __uint_as_float(rr[4 * c + 2]), __uint_as_float(rr[4 * c + 3]));
       }
-      const bool any = have_o && l > 0.f;
-      a.part_ml[2 * prow] = any ? m_ref : -INFINITY;
-      a.part_ml[2 * prow + 1] = any ? l : 0.f;
+      if (row_ok) {
+        const bool any = have_o && l > 0.f;
+        a.part_ml[2 * prow] = any ? m_ref : -INFINITY;
+        a.part_ml[2 * prow + 1] = any ? l : 0.f;
+      }
     } else {
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const float *svrow = PV8 ? a.sv + (static_cast<int64_t>(b) * a.Hkv + kvh) * D : nullptr;

@@ -360,6 +360,20 @@ def test_mask_invariant_to_constant_shift_of_keys():
     np.testing.assert_array_equal(m0["mask"][dec], m1["mask"][dec])
 
 
+@pytest.mark.parametrize("causal,lam", [(False, -math.inf), (True, -math.inf), (True, -8.0)])
+def test_output_invariant_to_key_mean_smoothing(causal, lam):
+    """Subtracting the token mean of K (per batch and key/value head) shifts every score of a row
+    by the same q . mean, which the softmax and the lambda filter (differences of maxima) ignore:
+    the attention output is unchanged in float64 (the smoothing the 8-bit path applies)."""
+    qu, ku, vu = W.random_qkv(12, 1, 4, 2, 700, 32)
+    q, k, v = f64(qu), f64(ku) + 3.0, f64(vu)
+    mask = W.random_mask(13, 1, 4, 700, p=0.5)
+    ks = k - k.mean(axis=2, keepdims=True)
+    o0 = oracle.block_sparse_attn(q, k, v, mask, lam, causal)
+    o1 = oracle.block_sparse_attn(q, ks, v, mask, lam, causal)
+    np.testing.assert_allclose(o1, o0, rtol=1e-9, atol=1e-11)
+
+
 def test_always_keep_rows_and_columns():
     rng = np.random.default_rng(9)
     N, d = 512, 32
