@@ -50,6 +50,24 @@ constexpr float LOG2E = 1.4426950408889634f;
 // reading, -1 for the count reading, where an e of 0 is still a block to count); every pass uses
 // this one expression, so the values agree bit for bit between passes.  s - max is exact zero
 // for the maximum, and the hardware exponential is clamped at 1, so e <= 1 always.
+// The loads and the exponentials are split (load_s, to_e) so that the row passes can load the
+// next 4 blocks while they work on these; load_e is the two together.
+__device__ __forceinline__ float4 load_s(const float *srow, int j0, int nvalid) {
+  return j0 < nvalid ? __ldg(reinterpret_cast<const float4 *>(srow + j0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+__device__ __forceinline__ float4 to_e(const float4 v, int j0, int nvalid, float negm, float none) {
+  float4 e = make_float4(none, none, none, none);
+  if (j0 < nvalid) {
+    const float2 l2 = make_float2(LOG2E, LOG2E), nm = make_float2(negm, negm);
+    const float2 a = fmul2(fadd2(make_float2(v.x, v.y), nm), l2);
+    const float2 b = fmul2(fadd2(make_float2(v.z, v.w), nm), l2);
+    e.x = fminf(fast_exp2(a.x), 1.f);
+    e.y = j0 + 1 < nvalid ? fminf(fast_exp2(a.y), 1.f) : none;
+    e.z = j0 + 2 < nvalid ? fminf(fast_exp2(b.x), 1.f) : none;
+    e.w = j0 + 3 < nvalid ? fminf(fast_exp2(b.y), 1.f) : none;
+  }
+  return e;
+}
 __device__ __forceinline__ float4 load_e(const float *srow, int j0, int nvalid, float negm, float none = 0.f) {
   float4 e = make_float4(none, none, none, none);
   if (j0 < nvalid) {
@@ -240,8 +258,12 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
   float2 z2 = make_float2(0.f, 0.f);
   if (!keep_all) {
     const uint32_t lim1 = hist_lim(st);
+    float4 sn = load_s(srow, 4 * lane, nvalid);  // one stretch of 128 blocks loaded ahead
     for (int t = 0; t < nit; ++t) {
-      const float4 v = load_e(srow, 128 * t + 4 * lane, nvalid, negm, none);
+      const int j0 = 128 * t + 4 * lane;
+      const float4 sv = sn;
+      if (t + 1 < nit) sn = load_s(srow, j0 + 128, nvalid);
+      const float4 v = to_e(sv, j0, nvalid, negm, none);
       if (!cnt) z2 = fadd2(z2, fadd2(make_float2(v.x, v.y), make_float2(v.z, v.w)));
       hist_add4(H, lane, v, st, lim1, cnt);
     }
@@ -262,9 +284,12 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
     // until the cut among them is known (patched below).
     while (ok) {
       int n = 0;
+      float4 sn = load_s(srow, 4 * lane, nvalid);  // loaded one stretch ahead
       for (int t = 0; t < nit; ++t) {
         const int j0 = 128 * t + 4 * lane;
-        const float4 v = load_e(srow, j0, nvalid, negm, none);
+        const float4 sv = sn;
+        if (t + 1 < nit) sn = load_s(srow, j0 + 128, nvalid);
+        const float4 v = to_e(sv, j0, nvalid, negm, none);
         n = list_append(v, j0, st, Lv, Lj, n, lane);
         uint32_t word = 0u;
         if (j0 < nvalid) {
