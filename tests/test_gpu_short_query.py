@@ -83,8 +83,15 @@ def test_short_query_dense_is_tail_of_full_causal():
     assert cos >= COS_MIN and err <= MAXABS, (cos, err)
 
 
-@pytest.mark.parametrize("prec,cos_min", [(fbs.SPARGE_PRECISION_Q8, 0.999), (fbs.SPARGE_PRECISION_Q8_FP8PV, 0.998)])
-def test_short_query_8bit(prec, cos_min):
+@pytest.mark.parametrize("prec", [
+    fbs.SPARGE_PRECISION_Q8,            # measured 0.99926
+    pytest.param(fbs.SPARGE_PRECISION_Q8_FP8PV,
+                 marks=pytest.mark.xfail(strict=True, reason="e4m3 scores, P and V: measured cosine 0.99861 < 0.999")),
+    fbs.SPARGE_PRECISION_BF16_FP8PV,    # measured 0.99935
+])
+def test_short_query_8bit(prec):
+    """A short causal query chunk (Nq < Nk, ragged tails) on every 8-bit precision, held to the
+    8-bit bound (cosine >= 0.999 against the float64 oracle)."""
     Nq, Nk, Hq, Hkv, d = 384 + 5, 2048 + 33, 4, 2, 128
     qu, ku, vu = W.random_qkv(79, 1, Hq, Hkv, Nk, d)
     qu = qu[:, :, :Nq].copy()
@@ -92,4 +99,5 @@ def test_short_query_8bit(prec, cos_min):
     out = fbs.block_sparse_attn(q, k, v, None, -math.inf, True, precision=prec)
     ref = oracle.block_sparse_attn(f64(qu), f64(ku), f64(vu), None, -math.inf, True)
     cos, _ = cos_maxabs(host_f64(out), ref)
-    assert cos >= cos_min, cos
+    print("short query 8-bit precision %d: cosine %.6f" % (prec, cos))
+    assert cos >= 0.999, cos
