@@ -277,6 +277,8 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
         (rc = make_map_s(&g.ts, pw.S, pw.nkb_pad, nqb, q.B * q.H)))
       return rc;
     g.Smax = pw.Smax;
+    g.splits = pw.smax_splits;
+    g.smax_stride = pw.smax_stride;
     g.nkb_pad = pw.nkb_pad;
     g.B = (int)q.B; g.Hq = (int)q.H; g.Hkv = (int)k.H; g.Nq = (int)q.N; g.Nk = (int)k.N; g.d = (int)q.d;
     g.causal = causal;
@@ -446,7 +448,7 @@ size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t 
   s += 2 * align256(2 * B * Hq * nqb * d);              // qhi, qlo
   s += 2 * align256(2 * B * Hkv * nkb * d);             // khi, klo
   s += align256(sizeof(float) * B * Hq * nqb * nkb_pad);  // S
-  s += align256(sizeof(float) * B * Hq * nqb);          // Smax
+  s += align256(sizeof(float) * score_gemm_slices(Nk) * B * Hq * nqb);  // Smax slices
   return s;
 }
 
@@ -468,7 +470,9 @@ PredictWs predict_ws_carve(void *ws, int64_t B, int64_t Hq, int64_t Hkv, int64_t
   w.khi = reinterpret_cast<uint16_t *>(take(2 * B * Hkv * nkb * d));
   w.klo = reinterpret_cast<uint16_t *>(take(2 * B * Hkv * nkb * d));
   w.S = reinterpret_cast<float *>(take(sizeof(float) * B * Hq * nqb * nkb_pad));
-  w.Smax = reinterpret_cast<float *>(take(sizeof(float) * B * Hq * nqb));
+  w.smax_splits = score_gemm_splits(B, Hq, Nq, Nk);
+  w.smax_stride = B * Hq * nqb;
+  w.Smax = reinterpret_cast<float *>(take(sizeof(float) * score_gemm_slices(Nk) * B * Hq * nqb));
   w.nkb_pad = nkb_pad;
   return w;
 }

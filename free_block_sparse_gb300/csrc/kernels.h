@@ -24,9 +24,33 @@ struct PredictWs {
   uint16_t *qhi, *qlo;  // bf16 [B][Hq][nqb][d]
   uint16_t *khi, *klo;  // bf16 [B][Hkv][nkb][d]
   float *S;         // [B][Hq][nqb][nkb_pad]
-  float *Smax;      // [B][Hq][nqb] maximum of each S row over its valid key blocks
+  float *Smax;      // [smax_splits][B][Hq][nqb] maximum of each S row over its valid key blocks, one
+                    // slice per key-chunk split of the score product (the row maximum is theirs)
   int64_t nkb_pad;
+  int smax_splits;
+  int64_t smax_stride;  // B Hq nqb: floats between two slices
 };
+
+// Key-chunk splits of the pooled-score product.  One CTA per (head, group of 128 query blocks)
+// leaves most of a 152-SM part idle when there are few such tiles (decoding, short queries): the
+// key chunks of 128 blocks are then divided among up to about two CTAs per SM (at most 8 splits),
+// each writing the maxima of its chunks to its own Smax slice.  The workspace holds
+// score_gemm_slices(Nk) slices, a bound that grows with Nk alone, so a workspace sized for the
+// longer of the two lengths covers every shorter query.
+constexpr int SCORE_GEMM_MAX_SPLITS = 8;
+inline int score_gemm_slices(int64_t Nk) {
+  const int64_t nch = ((Nk + 63) / 64 + 127) / 128;
+  return static_cast<int>(nch < 1 ? 1 : (nch < SCORE_GEMM_MAX_SPLITS ? nch : SCORE_GEMM_MAX_SPLITS));
+}
+inline int score_gemm_splits(int64_t B, int64_t Hq, int64_t Nq, int64_t Nk) {
+  const int64_t nqb = (Nq + 127) / 128, nkb = (Nk + 63) / 64;
+  const int64_t tiles = B * Hq * ((nqb + 127) / 128), nch = (nkb + 127) / 128;
+  if (tiles <= 0 || nch <= 1 || tiles >= 152) return 1;
+  int64_t s = (2 * 152 + tiles - 1) / tiles;
+  if (s > score_gemm_slices(Nk)) s = score_gemm_slices(Nk);
+  const int64_t per = (nch + s - 1) / s;  // chunks per split
+  return static_cast<int>((nch + per - 1) / per);
+}
 
 // Nq: query length, Nk: key length
 size_t predict_ws_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d);
@@ -56,8 +80,10 @@ cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, c
 struct ScoreGemmLaunch {
   CUtensorMap qhi, qlo, khi, klo;
   CUtensorMap ts;  // 3-D map over S (nkb_pad, nqb, B*Hq) fp32, box 32 x 128, 128-byte swizzle
-  float *Smax;     // [B][Hq][nqb] row maxima over the valid key blocks
+  float *Smax;     // [splits][B][Hq][nqb] row maxima over the valid key blocks of each split's chunks
   int64_t nkb_pad;
+  int splits;      // score_gemm_splits of the shape
+  int64_t smax_stride;
   int B, Hq, Hkv, Nq, Nk, d, causal;  // query and key lengths (causal: Nq <= Nk, the last query on the last key)
   float scale;
   int *status;

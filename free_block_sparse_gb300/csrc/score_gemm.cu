@@ -22,8 +22,9 @@ constexpr int GCOLS = 128;  // key blocks per chunk (MMA N)
 
 struct GemmArgs {
   float *Smax;
-  int64_t nkb_pad;
+  int64_t nkb_pad, smax_stride;
   int B, Hq, Hkv, G, nqb, nkb, causal, off, ngroups;  // off = Nk - Nq (causal alignment)
+  int per_split;  // key chunks per split (blockIdx.z): split z takes chunks [z per_split, ...)
   float scale;
   int *status;
 };
@@ -72,7 +73,9 @@ __global__ void __launch_bounds__(192, 1)
   const int i0 = group * GROWS;
   const int ilast = min(i0 + GROWS - 1, a.nqb - 1);
   const int ncols = a.causal ? min(a.nkb, causal_key_blocks(ilast, a.off)) : a.nkb;
-  const int nch = (ncols + GCOLS - 1) / GCOLS;
+  // this CTA's key chunks [ch0, ch0 + nch) of the group's (ncols + 127) / 128
+  const int ch0 = static_cast<int>(blockIdx.z) * a.per_split;
+  const int nch = max(0, min((ncols + GCOLS - 1) / GCOLS - ch0, a.per_split));
   constexpr uint32_t IDESC = idesc_f32acc(128, GCOLS, FMT_BF16, false);
 
   if (threadIdx.x == 0) {
@@ -97,7 +100,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = cs.tmem_base;
 
   if (warp == 4) {
-    if (lane == 0) {
+    if (lane == 0 && nch > 0) {
       mbar_arrive_expect_tx(&cs.q_full, 2 * L::OP_BYTES);
       for (int c = 0; c < L::KCH; ++c) {
         tma_load_3d(smem + L::OFF_QHI + c * 16384, &tqh, &cs.q_full, 64 * c, i0, bh);
@@ -110,8 +113,8 @@ __global__ void __launch_bounds__(192, 1)
         uint8_t *kl = kh + L::OP_BYTES;
         mbar_arrive_expect_tx(&cs.k_full[st], 2 * L::OP_BYTES);
         for (int c = 0; c < L::KCH; ++c) {
-          tma_load_3d(kh + c * 16384, &tkh, &cs.k_full[st], 64 * c, GCOLS * ch, b * a.Hkv + kvh);
-          tma_load_3d(kl + c * 16384, &tkl, &cs.k_full[st], 64 * c, GCOLS * ch, b * a.Hkv + kvh);
+          tma_load_3d(kh + c * 16384, &tkh, &cs.k_full[st], 64 * c, GCOLS * (ch0 + ch), b * a.Hkv + kvh);
+          tma_load_3d(kl + c * 16384, &tkl, &cs.k_full[st], 64 * c, GCOLS * (ch0 + ch), b * a.Hkv + kvh);
         }
       }
       if (*abort) {
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(192, 1)
           uint32_t v[32];
           tmem_ld32(tl + ab * GCOLS + 32 * q, v);
           tmem_ld_wait();
-          const int j0 = GCOLS * ch + 32 * q;
+          const int j0 = GCOLS * (ch0 + ch) + 32 * q;
           uint8_t *row = stage + qq * 16384 + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -197,7 +200,7 @@ __global__ void __launch_bounds__(192, 1)
         bar_sync(1, 128);
         if (threadIdx.x == 0) {
           for (int qq = 0; qq < L::QPR; ++qq)
-            tma_store_3d(&ts, stage + qq * 16384, GCOLS * ch + 32 * (rd * L::QPR + qq), i0, bh);
+            tma_store_3d(&ts, stage + qq * 16384, GCOLS * (ch0 + ch) + 32 * (rd * L::QPR + qq), i0, bh);
           bulk_commit();
         }
       }
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     if (threadIdx.x == 0) bulk_wait_all();
-    if (i < a.nqb) a.Smax[static_cast<int64_t>(bh) * a.nqb + i] = rmax;
+    if (i < a.nqb) a.Smax[blockIdx.z * a.smax_stride + static_cast<int64_t>(bh) * a.nqb + i] = rmax;
   }
   tc_fence_before();
   __syncthreads();
@@ -220,7 +223,9 @@ cudaError_t launch_d(const ScoreGemmLaunch &l, const GemmArgs &a, cudaStream_t s
   const uint32_t smem = GL<D>::TOTAL;
   static std::atomic<unsigned long long> smem_set{0};
   if (cudaError_t e = set_smem_limit_once(score_gemm_kernel<D>, static_cast<int>(smem), smem_set); e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(a.B * a.Hq), static_cast<unsigned>(a.ngroups));
+  const int nch_all = (a.nkb + GCOLS - 1) / GCOLS;
+  dim3 grid(static_cast<unsigned>(a.B * a.Hq), static_cast<unsigned>(a.ngroups),
+            static_cast<unsigned>((nch_all + a.per_split - 1) / a.per_split));
   score_gemm_kernel<D><<<grid, 192, smem, st>>>(l.qhi, l.qlo, l.khi, l.klo, l.ts, a);
   return cudaGetLastError();
 }
@@ -231,6 +236,7 @@ cudaError_t launch_score_gemm(const ScoreGemmLaunch &l, cudaStream_t st) {
   GemmArgs a;
   a.Smax = l.Smax;
   a.nkb_pad = l.nkb_pad;
+  a.smax_stride = l.smax_stride;
   a.B = l.B; a.Hq = l.Hq; a.Hkv = l.Hkv; a.G = l.Hq / l.Hkv;
   a.nqb = (l.Nq + QBLK - 1) / QBLK;
   a.nkb = (l.Nk + KBLK - 1) / KBLK;
@@ -239,6 +245,12 @@ cudaError_t launch_score_gemm(const ScoreGemmLaunch &l, cudaStream_t st) {
   a.ngroups = (a.nqb + GROWS - 1) / GROWS;
   a.scale = l.scale;
   a.status = l.status;
+  {
+    const int nch_all = (a.nkb + GCOLS - 1) / GCOLS, sp = l.splits > 0 ? l.splits : 1;
+    a.per_split = (nch_all + sp - 1) / sp;
+    if (a.per_split < 1) a.per_split = 1;
+    if ((nch_all + a.per_split - 1) / a.per_split > sp) return cudaErrorInvalidValue;  // more slices than Smax has
+  }
   if (static_cast<int64_t>(a.B) * a.Hq * a.ngroups == 0) return cudaSuccess;
   return l.d == 128 ? launch_d<128>(l, a, st) : launch_d<64>(l, a, st);
 }

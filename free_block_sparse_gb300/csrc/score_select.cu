@@ -32,7 +32,9 @@ constexpr int NBIN = 32;
 constexpr int CMAX = 256;  // crossing-bin elements compacted into the short list (8 per lane)
 
 struct SelArgs {
-  const float *S, *Smax;
+  const float *S, *Smax;  // Smax: smax_splits slices of `rows` row maxima
+  int smax_splits;
+  int64_t smax_stride;
   const float *sQ, *sK;
   uint8_t *mask;
   int64_t nkb_pad, rows;
@@ -200,7 +202,9 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
   const int nit = (nvalid + 127) >> 7;
   const float *srow = a.S + static_cast<int64_t>(row) * a.nkb_pad;
   const float *sKrow = a.sK + (static_cast<int64_t>(b) * a.Hkv + kvh) * a.nkb_pad;
-  const float negm = -a.Smax[row];
+  float smax = a.Smax[row];
+  for (int z = 1; z < a.smax_splits; ++z) smax = fmaxf(smax, a.Smax[z * a.smax_stride + row]);
+  const float negm = -smax;
   // this head's parameters; an entry out of range keeps every valid block of the head
   float topk = a.topk, theta = a.theta;
   bool bad = false;
@@ -499,6 +503,8 @@ cudaError_t launch_score_select(const PredictWs &ws, int B, int Hq, int Hkv, int
   SelArgs a;
   a.S = ws.S;
   a.Smax = ws.Smax;
+  a.smax_splits = ws.smax_splits;
+  a.smax_stride = ws.smax_stride;
   a.sQ = ws.sQ;
   a.sK = ws.sK;
   a.mask = mask;
