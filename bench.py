@@ -240,9 +240,11 @@ def measure_decode(q, k, w, steps, warmup, dev, peaks, v):
     """One decoding step of a causal workload: the last query token of every head against all the
     keys (mask prediction of that token, then the decoding tiles that pack the G query rows of a
     KV head into one tile and split the keys over CTAs), on the bench's own device tensors.  The
-    lambda filter is off (the split over key chunks needs it off).  Algorithmic bytes of the
-    attention: a K and a V tile per key block that any head of a KV head keeps (counted by the
-    kernel), the token's Q and O rows and the mask."""
+    lambda filter is off (the split over key chunks needs it off).  A decoding loop replays its
+    step as a CUDA graph, so the step, the prediction alone and the attention alone are each timed
+    as graph replays (device time without the host's launch work); `eager_ms` is the same step
+    called directly.  Algorithmic bytes of the attention: a K and a V tile per key block that any
+    head of a KV head keeps (counted by the kernel), the token's Q and O rows and the mask."""
     import torch
     import free_block_sparse_gb300 as fbs
     B, Hq, _, d = q.shape
@@ -253,31 +255,61 @@ def measure_decode(q, k, w, steps, warmup, dev, peaks, v):
     ws = torch.empty(fbs.workspace_bytes(fbs.SPARGE_OP_ATTN, B, Hq, Hkv, Nk, d), dtype=torch.uint8, device=dev)
     o = torch.empty((B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
     stats = torch.zeros(4, dtype=torch.int64, device=dev)
+    s = torch.cuda.Stream(device=dev)
 
-    def step(events=None, counters=None):
+    def step(counters=None):
         fbs.sparge_attn_ex(qd, k, v, w.topk, True, theta=w.theta, lam=-math.inf, mask_out=mask, out=o, ws=ws,
-                           events=events, stats=counters)
+                           stats=counters)
 
-    step(counters=stats)
+    def predict():
+        fbs.predict_mask(qd, k, w.topk, w.theta, True, ws=ws, mask=mask)
+
+    def attend():
+        fbs.block_sparse_attn(qd, k, v, mask, -math.inf, True, out=o, ws=ws)
+
+    def per_replay(fn):
+        """Device time of one call of fn, replayed from a CUDA graph (median of `steps` replays)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        for _ in range(max(warmup, 3)):
+            g.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
+
+    with torch.cuda.stream(s):
+        step(counters=stats)
+        torch.cuda.synchronize()
+        tiles = int(stats[0].item())
+        ref = o.clone()
+        for _ in range(max(warmup, 3)):
+            step()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            e0.record(s)
+            step()
+            e1.record(s)
+        torch.cuda.synchronize()
+        t_eager = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3
+        t_step = per_replay(step)
+        t_pred = per_replay(predict)
+        t_attn = per_replay(attend)
     torch.cuda.synchronize()
-    tiles = int(stats[0].item())
-    for _ in range(max(warmup, 3)):
-        step()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
-    torch.cuda.synchronize()
-    for e in evs:
-        step(events=e)
-    torch.cuda.synchronize()
+    assert torch.equal(o, ref)
     assert fbs.device_status() == 0
-    t_step = statistics.median(e[0].elapsed_time(e[5]) for e in evs) / 1e3
-    t_pred = statistics.median(e[0].elapsed_time(e[3]) for e in evs) / 1e3
-    t_attn = statistics.median(e[4].elapsed_time(e[5]) for e in evs) / 1e3
     nbytes = tiles * 64 * d * 2 * 2 + 2 * 2 * B * Hq * d + mask.numel()
     gbs = nbytes / t_attn / 1e9
     return {"workload": "%s decoding step: the last query token of each of the %d heads against the %d keys, "
-                        "predicted mask, lambda off" % (w.name, Hq, Nk),
-            "ms": round(t_step * 1e3, 4), "mask_pred_ms": round(t_pred * 1e3, 4), "attn_ms": round(t_attn * 1e3, 4),
-            "kv_tiles": tiles, "attn_bytes": nbytes, "attn_gbs": round(gbs, 1),
+                        "predicted mask, lambda off; device times of CUDA-graph replays" % (w.name, Hq, Nk),
+            "ms": round(t_step * 1e3, 4), "eager_ms": round(t_eager * 1e3, 4), "mask_pred_ms": round(t_pred * 1e3, 4),
+            "attn_ms": round(t_attn * 1e3, 4), "kv_tiles": tiles, "attn_bytes": nbytes, "attn_gbs": round(gbs, 1),
             "attn_pct_hbm": round(100 * gbs / float(peaks["hbm_gbs"]), 2),
             "tokens_per_s": round(B / t_step, 1)}
 

@@ -775,15 +775,24 @@ template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const float *part_o, const float *part_ml, int nchunk,
                                                            int Hq, int Hkv, int Nq, __nv_bfloat16 *o, int64_t o_sb,
                                                            int64_t o_sh, int64_t o_sn) {
+  constexpr int PREG = 64;  // chunks whose partial outputs a thread holds in registers
   __shared__ float wgt[MAX_DECODE_CHUNKS];
+  __shared__ float lsum[MAX_DECODE_CHUNKS];
   __shared__ float inv_sum;
   const int row = blockIdx.x, t = threadIdx.x;
   const int qi = row % Nq, bh = row / Nq, h = bh % Hq, b = bh / Hq;
   const int G = Hq / Hkv, kvh = h / G, r = (h % G) * Nq + qi;
   const int64_t base = (static_cast<int64_t>(b) * Hkv + kvh) * nchunk;
-  for (int c = t; c < nchunk; c += D) {  // m_c where the chunk saw a visible key, else -inf
+  // this thread's channel of every chunk's partial output, loaded first: none of these loads
+  // waits for the weights
+  float po[PREG];
+#pragma unroll
+  for (int c = 0; c < PREG; ++c) po[c] = c < nchunk ? part_o[((base + c) * 128 + r) * D + t] : 0.f;
+  for (int c = t; c < nchunk; c += D) {  // m_c where the chunk saw a visible key, else -inf; l_c
     const int64_t pr = (base + c) * 128 + r;
-    wgt[c] = part_ml[2 * pr + 1] > 0.f ? part_ml[2 * pr] : -INFINITY;
+    const float l = part_ml[2 * pr + 1];
+    wgt[c] = l > 0.f ? part_ml[2 * pr] : -INFINITY;
+    lsum[c] = l;
   }
   __syncthreads();
   if (t < 32) {
@@ -795,7 +804,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *part_o, 
     for (int c = t; c < nchunk; c += 32) {
       const float w = (M == -INFINITY || wgt[c] == -INFINITY) ? 0.f : exp2f(wgt[c] - M);
       wgt[c] = w;
-      L = fmaf(w, part_ml[2 * ((base + c) * 128 + r) + 1], L);
+      L = fmaf(w, lsum[c], L);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
@@ -803,8 +812,10 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *part_o, 
   }
   __syncthreads();
   float acc = 0.f;
+#pragma unroll
+  for (int c = 0; c < PREG; ++c) acc = fmaf(wgt[c < nchunk ? c : 0], po[c], acc);  // po is 0 past nchunk
 #pragma unroll 4
-  for (int c = 0; c < nchunk; ++c) acc = fmaf(wgt[c], part_o[((base + c) * 128 + r) * D + t], acc);
+  for (int c = PREG; c < nchunk; ++c) acc = fmaf(wgt[c], part_o[((base + c) * 128 + r) * D + t], acc);
   o[b * o_sb + h * o_sh + static_cast<int64_t>(qi) * o_sn + t] = __float2bfloat16_rn(acc * inv_sum);
 }
 
