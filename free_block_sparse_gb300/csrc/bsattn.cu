@@ -95,15 +95,19 @@ struct KeptScan {
       }
       base += 512;
       if (base >= n) return -1;
+      // per row of the group: the lane's 16 flags are all loaded before any is used, so the loads
+      // of a window are in flight together (one memory latency per row, not one per flag)
       uint32_t f = 0u;
+      for (int g = 0; g < G; ++g) {
+        const uint8_t *rg = row + g * gstride;
+        uint32_t m[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int j = base + 16 * lane + c;
-        if (j < n) {
-          bool keep = false;
-          for (int g = 0; g < G; ++g) keep = keep || __ldg(row + g * gstride + j) != 0;
-          if (keep) f |= 1u << c;
+        for (int c = 0; c < 16; ++c) {
+          const int j = base + 16 * lane + c;
+          m[c] = j < n ? __ldg(rg + j) : 0u;
         }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) f |= (m[c] != 0u ? 1u : 0u) << c;
       }
       bits = f;
     }
