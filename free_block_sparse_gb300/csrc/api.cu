@@ -387,6 +387,10 @@ int attn_impl(const View &q, const View &k, const View &v, const uint8_t *mask, 
     l.chunk_blocks = sp.chunk_blocks;
     l.part_o = static_cast<float *>(ws);
     l.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + align256(rows * q.d * 4));
+    const size_t lists_off = align256(rows * q.d * 4) + align256(rows * 2 * 4);
+    l.dlist = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) + lists_off);
+    l.dcount = reinterpret_cast<int *>(static_cast<uint8_t *>(ws) + lists_off +
+                                       align256(static_cast<size_t>(k.B * k.H) * cdiv(k.N, KBLK) * 4));
     if ((rc = make_map(&l.tq, q, 128, "q"))) return rc;  // checks the alignment the row reads rely on
     l.q = q.data;
     l.q_sb = q.sb; l.q_sh = q.sh; l.q_sn = q.sn;

@@ -58,10 +58,13 @@ struct AttnArgs {
   const __nv_bfloat16 *q;     // bf16 path: Q rows, copied into TMEM by the softmax warps
   const int32_t *qperm;       // token order of those rows (or nullptr)
   int64_t q_sb, q_sh, q_sn;
-  // decoding tiles: the key blocks of a (batch, KV head) are split into nchunk chunks of
-  // chunk_blocks; partial results go to part_o [B Hkv][nchunk][128][D] and part_ml (m, l) per row
+  // decoding tiles: the key blocks that any head of a (batch, KV head) keeps, listed in dlist
+  // ([B Hkv][nkb], count in dcount; without a mask every block), are split into nchunk equal
+  // shares; partial results go to part_o [B Hkv][nchunk][128][D] and part_ml (m, l) per row
   int nchunk, chunk_blocks;
   float *part_o, *part_ml;
+  const int32_t *dlist;
+  const int *dcount;
 };
 
 // Warp-collective walk over the kept, valid key blocks of one mask row in ascending order, run
@@ -269,10 +272,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     // follows P.V.  After the last tile the next K stage and j slot get the end mark (-1, a plain
     // arrive without data).
     KeptScan ks;
-    if constexpr (DEC)
-      ks.init(mrow, n_valid, lo, a.G, static_cast<int64_t>(a.nqb) * a.nkb);
-    else
-      ks.init(mrow, n_valid);
+    ks.init(mrow, n_valid);
+    // decoding tile: share `chunk` of the (batch, KV head)'s kept-block list, [d_lo, d_hi)
+    int d_lo = 0, d_hi = 0;
+    const int32_t *dl = nullptr;
+    if constexpr (DEC) {
+      const int chunk = blockIdx.x % a.nchunk, bk = blockIdx.x / a.nchunk;
+      const int cnt = a.mask ? __ldg(a.dcount + bk) : a.nkb;
+      d_lo = static_cast<int>(static_cast<int64_t>(chunk) * cnt / a.nchunk);
+      d_hi = static_cast<int>(static_cast<int64_t>(chunk + 1) * cnt / a.nchunk);
+      if (a.mask) dl = a.dlist + static_cast<int64_t>(bk) * a.nkb;
+    }
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
@@ -280,7 +290,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
     int jprev = -1;
     for (int t = 0;; ++t) {
-      const int j = ks.next(lane);
+      int j;
+      if constexpr (DEC)
+        j = d_lo + t < d_hi ? (dl ? __ldg(dl + d_lo + t) : d_lo + t) : -1;
+      else
+        j = ks.next(lane);
       const int kst = t % KST, js = t % JRING;
       if (!mbar_wait(&cs.k_empty[kst], ((t / KST) & 1) ^ 1, abort, a.status)) break;
       if (!mbar_wait(&cs.j_empty[js], ((t / JRING) & 1) ^ 1, abort, a.status)) break;
@@ -775,6 +789,39 @@ cudaError_t launch_t(const AttnLaunch &l, const AttnArgs &a, cudaStream_t st) {
 // thread t sums channel t over the chunks (coalesced rows of the partial outputs):
 // O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c (0 where no chunk saw a visible key).
 constexpr int MAX_DECODE_CHUNKS = 1024;
+// The key blocks that any of the G heads of a (batch, KV head) keeps, in ascending order, for the
+// decoding tiles to share out evenly (one CTA of 256 threads per (batch, KV head); query block 0
+// of each head's mask, the only one a decoding call has).
+__global__ void __launch_bounds__(256) decode_union_kernel(const uint8_t *mask, int Hq, int Hkv, int nqb, int nkb,
+                                                           int32_t *list, int *count) {
+  __shared__ int wcount[8];
+  const int bk = blockIdx.x, b = bk / Hkv, kvh = bk % Hkv, G = Hq / Hkv;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint8_t *m0 = mask + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(kvh) * G) * nqb * nkb;
+  const int64_t gstride = static_cast<int64_t>(nqb) * nkb;
+  int32_t *out = list + static_cast<int64_t>(bk) * nkb;
+  int base = 0;
+  for (int j0 = 0; j0 < nkb; j0 += 256) {
+    const int j = j0 + static_cast<int>(threadIdx.x);
+    uint32_t f = 0u;
+    if (j < nkb)
+      for (int g = 0; g < G; ++g) f |= __ldg(m0 + g * gstride + j);
+    const uint32_t bal = __ballot_sync(0xffffffffu, f != 0u);
+    if (lane == 0) wcount[w] = __popc(bal);
+    __syncthreads();
+    int off = base, tot = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      off += u < w ? wcount[u] : 0;
+      tot += wcount[u];
+    }
+    if (f != 0u) out[off + __popc(bal & ((1u << lane) - 1u))] = j;
+    base += tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) count[bk] = base;
+}
+
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const float *part_o, const float *part_ml, int nchunk,
                                                            int Hq, int Hkv, int Nq, __nv_bfloat16 *o, int64_t o_sb,
@@ -858,6 +905,14 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
     a.chunk_blocks = l.chunk_blocks;
     a.part_o = l.part_o;
     a.part_ml = l.part_ml;
+    a.dlist = l.dlist;
+    a.dcount = l.dcount;
+    if (a.mask) {
+      if (!l.dlist || !l.dcount) return cudaErrorInvalidValue;
+      decode_union_kernel<<<static_cast<unsigned>(static_cast<int64_t>(a.B) * a.Hkv), 256, 0, st>>>(
+          a.mask, a.Hq, a.Hkv, a.nqb, a.nkb, l.dlist, l.dcount);
+      if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+    }
     cudaError_t e = l.d == 128 ? launch_t<128, 3, 2, false, false, true>(l, a, st)
                                : launch_t<64, 4, 3, false, false, true>(l, a, st);
     if (e != cudaSuccess) return e;

@@ -122,10 +122,14 @@ struct AttnLaunch {
   const int32_t *qperm;    // d = 64 under a token order: Q row t of the block is token qperm[t] of q
   int64_t q_sb, q_sh, q_sn;
   // decoding tiles (decode != 0, bf16): the G Nq <= 128 query rows of a KV head's heads in one
-  // tile, the key blocks split into nchunk chunks of chunk_blocks (decode_split), the chunks'
-  // partial rows in part_o / part_ml, then combined; V is read in place as bf16
+  // tile; the key blocks that any of the G heads keeps are listed in ascending order (dlist,
+  // [B Hkv][nkb], with their count in dcount) and split into nchunk equal shares, one per CTA
+  // (decode_split); the shares' partial rows go to part_o / part_ml, then are combined; V is read in
+  // place as bf16
   int decode, nchunk, chunk_blocks;
   float *part_o, *part_ml;
+  int32_t *dlist;
+  int *dcount;
 };
 
 // How a decoding call splits the key blocks of each (batch, KV head): about two CTAs per SM of a
@@ -145,11 +149,14 @@ inline DecodeSplit decode_split(int64_t B, int64_t Hkv, int64_t Nk) {
   s.nchunk = static_cast<int>((nkb + s.chunk_blocks - 1) / s.chunk_blocks);
   return s;
 }
-// Workspace of a decoding call's partial rows: [B Hkv][nchunk][128][d] fp32, then (m, l) per row.
+// Workspace of a decoding call: the partial rows [B Hkv][nchunk][128][d] fp32, then (m, l) per
+// row, then the kept-block lists [B Hkv][nkb] int32 and their counts [B Hkv].
 inline size_t decode_part_bytes(int64_t B, int64_t Hkv, int64_t Nk, int64_t d) {
   const DecodeSplit s = decode_split(B, Hkv, Nk);
   const size_t rows = static_cast<size_t>(B * Hkv) * s.nchunk * 128;
-  return ((rows * d * 4 + 255) & ~size_t(255)) + ((rows * 2 * 4 + 255) & ~size_t(255));
+  const size_t units = static_cast<size_t>(B * Hkv), nkb = static_cast<size_t>((Nk + 63) / 64);
+  return ((rows * d * 4 + 255) & ~size_t(255)) + ((rows * 2 * 4 + 255) & ~size_t(255)) +
+         ((units * nkb * 4 + 255) & ~size_t(255)) + ((units * 4 + 255) & ~size_t(255));
 }
 
 cudaError_t launch_bsattn(const AttnLaunch &a, cudaStream_t st);
