@@ -231,12 +231,12 @@ int sparge_predict_mask_ex(const sparge_tensor *q, const sparge_tensor *k, float
  * Few queries against many keys (decoding, short chunks): with precision SPARGE_PRECISION_BF16,
  * lambda = -INFINITY (and no per-head lambda), no token order, G Nq <= 128 (G = Hq / Hkv) and at
  * least 32 key blocks, the call packs the Nq query rows of the G heads of each KV head into one
- * tile, splits the key blocks over CTAs (each CTA visits the blocks any of the G heads keeps in
- * its chunk, each row masking the blocks its own head does not keep) and combines the chunks'
- * partial rows in a second kernel; P.V then runs on bf16 P and V read in place (no f16 copy of
+ * tile, lists the key blocks any of the G heads keeps and splits that list into equal shares over
+ * CTAs (each row masking the blocks its own head does not keep), and combines the shares' partial
+ * rows in a last kernel; P.V then runs on bf16 P and V read in place (no f16 copy of
  * V; the workspace holds the partial rows instead).  The result is the same computation within
  * the bf16 tolerances; the lambda filter needs the tiles visited in order, so calls with it keep
- * one tile per query block and head.  Counters then count a tile once per chunk visit.
+ * one tile per query block and head.  Counters then count a tile once per (batch, KV head).
  * stats: optional counters (see sparge_params), may be NULL.
  */
 int sparge_block_sparse_attn(const sparge_tensor *q, const sparge_tensor *k,
