@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsparge.so")
 
-CUDA_SOURCES = ["api.cu", "pool_sim.cu", "score_gemm.cu", "score_select.cu", "bsattn.cu", "permute.cu", "noalloc.cu", "q8prep.cu"]
+CUDA_SOURCES = ["api.cu", "pool_sim.cu", "score_gemm.cu", "score_select.cu", "bsattn.cu", "decode.cu", "permute.cu", "noalloc.cu", "q8prep.cu"]
 CXX_SOURCES = ["hilbert.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

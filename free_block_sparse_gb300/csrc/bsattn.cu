@@ -783,93 +783,6 @@ cudaError_t launch_t(const AttnLaunch &l, const AttnArgs &a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// The partial rows of a decoding call's chunks combined into the output: one CTA of D threads per
-// output row (b, h, qi).  The chunks' exponent references and row sums are staged in shared
-// memory, the largest reference M and the weights 2^(m_c - M) found by the first warp, then
-// thread t sums channel t over the chunks (coalesced rows of the partial outputs):
-// O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c (0 where no chunk saw a visible key).
-constexpr int MAX_DECODE_CHUNKS = 1024;
-// The key blocks that any of the G heads of a (batch, KV head) keeps, in ascending order, for the
-// decoding tiles to share out evenly (one CTA of 256 threads per (batch, KV head); query block 0
-// of each head's mask, the only one a decoding call has).
-__global__ void __launch_bounds__(256) decode_union_kernel(const uint8_t *mask, int Hq, int Hkv, int nqb, int nkb,
-                                                           int32_t *list, int *count) {
-  __shared__ int wcount[8];
-  const int bk = blockIdx.x, b = bk / Hkv, kvh = bk % Hkv, G = Hq / Hkv;
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint8_t *m0 = mask + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(kvh) * G) * nqb * nkb;
-  const int64_t gstride = static_cast<int64_t>(nqb) * nkb;
-  int32_t *out = list + static_cast<int64_t>(bk) * nkb;
-  int base = 0;
-  for (int j0 = 0; j0 < nkb; j0 += 256) {
-    const int j = j0 + static_cast<int>(threadIdx.x);
-    uint32_t f = 0u;
-    if (j < nkb)
-      for (int g = 0; g < G; ++g) f |= __ldg(m0 + g * gstride + j);
-    const uint32_t bal = __ballot_sync(0xffffffffu, f != 0u);
-    if (lane == 0) wcount[w] = __popc(bal);
-    __syncthreads();
-    int off = base, tot = 0;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      off += u < w ? wcount[u] : 0;
-      tot += wcount[u];
-    }
-    if (f != 0u) out[off + __popc(bal & ((1u << lane) - 1u))] = j;
-    base += tot;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) count[bk] = base;
-}
-
-template <int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const float *part_o, const float *part_ml, int nchunk,
-                                                           int Hq, int Hkv, int Nq, __nv_bfloat16 *o, int64_t o_sb,
-                                                           int64_t o_sh, int64_t o_sn) {
-  constexpr int PREG = 64;  // chunks whose partial outputs a thread holds in registers
-  __shared__ float wgt[MAX_DECODE_CHUNKS];
-  __shared__ float lsum[MAX_DECODE_CHUNKS];
-  __shared__ float inv_sum;
-  const int row = blockIdx.x, t = threadIdx.x;
-  const int qi = row % Nq, bh = row / Nq, h = bh % Hq, b = bh / Hq;
-  const int G = Hq / Hkv, kvh = h / G, r = (h % G) * Nq + qi;
-  const int64_t base = (static_cast<int64_t>(b) * Hkv + kvh) * nchunk;
-  // this thread's channel of every chunk's partial output, loaded first: none of these loads
-  // waits for the weights
-  float po[PREG];
-#pragma unroll
-  for (int c = 0; c < PREG; ++c) po[c] = c < nchunk ? part_o[((base + c) * 128 + r) * D + t] : 0.f;
-  for (int c = t; c < nchunk; c += D) {  // m_c where the chunk saw a visible key, else -inf; l_c
-    const int64_t pr = (base + c) * 128 + r;
-    const float l = part_ml[2 * pr + 1];
-    wgt[c] = l > 0.f ? part_ml[2 * pr] : -INFINITY;
-    lsum[c] = l;
-  }
-  __syncthreads();
-  if (t < 32) {
-    float M = -INFINITY;
-    for (int c = t; c < nchunk; c += 32) M = fmaxf(M, wgt[c]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float L = 0.f;
-    for (int c = t; c < nchunk; c += 32) {
-      const float w = (M == -INFINITY || wgt[c] == -INFINITY) ? 0.f : exp2f(wgt[c] - M);
-      wgt[c] = w;
-      L = fmaf(w, lsum[c], L);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (t == 0) inv_sum = L > 0.f ? 1.f / L : 0.f;
-  }
-  __syncthreads();
-  float acc = 0.f;
-#pragma unroll
-  for (int c = 0; c < PREG; ++c) acc = fmaf(wgt[c < nchunk ? c : 0], po[c], acc);  // po is 0 past nchunk
-#pragma unroll 4
-  for (int c = PREG; c < nchunk; ++c) acc = fmaf(wgt[c], part_o[((base + c) * 128 + r) * D + t], acc);
-  o[b * o_sb + h * o_sh + static_cast<int64_t>(qi) * o_sn + t] = __float2bfloat16_rn(acc * inv_sum);
-}
-
 }  // namespace
 
 cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
@@ -909,22 +822,15 @@ cudaError_t launch_bsattn(const AttnLaunch &l, cudaStream_t st) {
     a.dcount = l.dcount;
     if (a.mask) {
       if (!l.dlist || !l.dcount) return cudaErrorInvalidValue;
-      decode_union_kernel<<<static_cast<unsigned>(static_cast<int64_t>(a.B) * a.Hkv), 256, 0, st>>>(
-          a.mask, a.Hq, a.Hkv, a.nqb, a.nkb, l.dlist, l.dcount);
-      if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+      if (cudaError_t e = launch_decode_union(a.mask, a.B, a.Hq, a.Hkv, a.nqb, a.nkb, l.dlist, l.dcount, st);
+          e != cudaSuccess)
+        return e;
     }
     cudaError_t e = l.d == 128 ? launch_t<128, 3, 2, false, false, true>(l, a, st)
                                : launch_t<64, 4, 3, false, false, true>(l, a, st);
     if (e != cudaSuccess) return e;
-    if (l.nchunk > MAX_DECODE_CHUNKS) return cudaErrorInvalidValue;
-    const unsigned rows = static_cast<unsigned>(static_cast<int64_t>(a.B) * a.Hq * a.Nq);
-    if (l.d == 128)
-      decode_combine_kernel<128><<<rows, 128, 0, st>>>(l.part_o, l.part_ml, l.nchunk, a.Hq, a.Hkv, a.Nq, a.o, a.o_sb,
-                                                       a.o_sh, a.o_sn);
-    else
-      decode_combine_kernel<64><<<rows, 64, 0, st>>>(l.part_o, l.part_ml, l.nchunk, a.Hq, a.Hkv, a.Nq, a.o, a.o_sb,
-                                                     a.o_sh, a.o_sn);
-    return cudaGetLastError();
+    return launch_decode_combine(l.part_o, l.part_ml, l.nchunk, a.B, a.Hq, a.Hkv, a.Nq, l.d, a.o, a.o_sb, a.o_sh, a.o_sn,
+                                 st);
   }
   if (l.q8 == 3) return launch_t<128, 3, 3, false, true>(l, a, st);  // bf16 Q.K^T, e4m3 P.V
   if (l.q8 == 2) return launch_t<128, 4, 3, true, true>(l, a, st);

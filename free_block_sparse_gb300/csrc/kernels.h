@@ -161,6 +161,14 @@ inline size_t decode_part_bytes(int64_t B, int64_t Hkv, int64_t Nk, int64_t d) {
 
 cudaError_t launch_bsattn(const AttnLaunch &a, cudaStream_t st);
 
+// Decoding tiles (decode.cu): before the attention, the ascending list of key blocks that any of
+// the G heads of each (batch, KV head) keeps in query block 0 (list [B Hkv][nkb], count [B Hkv]);
+// after it, the shares' partial rows combined into o (bf16, strides in elements).
+cudaError_t launch_decode_union(const uint8_t *mask, int B, int Hq, int Hkv, int nqb, int nkb, int32_t *list, int *count,
+                                cudaStream_t st);
+cudaError_t launch_decode_combine(const float *part_o, const float *part_ml, int nchunk, int B, int Hq, int Hkv, int Nq,
+                                  int d, void *o, int64_t o_sb, int64_t o_sh, int64_t o_sn, cudaStream_t st);
+
 // perm (or nullptr): row t of the copy is token perm[t] of v; bad entries are reported in *status.
 cudaError_t launch_convert_v_f16(const View &v, void *v16, const int32_t *perm, int *status, cudaStream_t st);
 
