@@ -92,3 +92,35 @@ def test_decode_through_sparge_attn_ex():
     ref = oracle.block_sparse_attn(f64(q), f64(w.k), f64(w.v), gm, -math.inf, True)
     cos, err = cos_maxabs(host_f64(out), ref)
     assert cos >= COS_MIN and err <= MAXABS, (cos, err)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_decode_without_mask_is_dense(causal):
+    """No mask: every key block is shared out over the CTAs (no listing pass), against dense
+    attention from the oracle."""
+    B, Hq, Hkv, Nq, Nk, d = 1, 8, 2, 3, 5000 + 11, 128
+    qu, ku, vu = _qkv(44, B, Hq, Hkv, Nq, Nk, d)
+    out = fbs.block_sparse_attn(dev_bf16(qu), dev_bf16(ku), dev_bf16(vu), None, -math.inf, causal)
+    ref = oracle.block_sparse_attn(f64(qu), f64(ku), f64(vu), None, -math.inf, causal)
+    cos, err = cos_maxabs(host_f64(out), ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
+
+
+def test_decode_bunched_mask_matches_oracle():
+    """Kept blocks bunched into a few stretches of the key range (the shape of real decoding masks:
+    the first blocks, a few recent stretches, the last block), so that equal key ranges would give
+    some CTAs most of the work; each head keeps its own subset of the stretches."""
+    B, Hq, Hkv, Nq, Nk, d = 1, 16, 4, 1, 40000, 128
+    qu, ku, vu = _qkv(45, B, Hq, Hkv, Nq, Nk, d)
+    nkb = -(-Nk // 64)
+    rng = np.random.Generator(np.random.PCG64(46))
+    m = np.zeros((B, Hq, 1, nkb), dtype=np.uint8)
+    for h in range(Hq):
+        m[0, h, 0, :4] = 1
+        for s in rng.choice(np.arange(0, nkb - 40, 40), size=3, replace=False):
+            m[0, h, 0, s:s + int(rng.integers(5, 40))] = 1
+        m[0, h, 0, -1] = 1
+    out = fbs.block_sparse_attn(dev_bf16(qu), dev_bf16(ku), dev_bf16(vu), torch.from_numpy(m).cuda(), -math.inf, True)
+    ref = oracle.block_sparse_attn(f64(qu), f64(ku), f64(vu), m, -math.inf, True)
+    cos, err = cos_maxabs(host_f64(out), ref)
+    assert cos >= COS_MIN and err <= MAXABS, (cos, err)
