@@ -177,15 +177,26 @@ PRECISIONS = {  # name: (C enum, dtype label, Q.K^T peak ratio to bf16, P.V peak
 }
 
 
+def code_digest(paths) -> str:
+    """sha256 (first 16 hex digits) of C++/CUDA sources with their comments and whitespace removed,
+    so that a capture stays attached to the code it measured across edits of comments alone."""
+    import re
+    text = ""
+    for p in paths:
+        s = open(p).read()
+        s = re.sub(r"/\*.*?\*/", " ", s, flags=re.S)
+        s = re.sub(r"//[^\n]*", " ", s)
+        text += " ".join(s.split()) + "\n"
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
 def profile_traffic(w, precision):
     """DRAM bytes of one full attention launch from the committed ncu capture of the same kernel
     (4 of the 32 query heads, scaled by 8), or None when the workload differs or the kernel source
     has changed since the capture."""
     if w.name != "llama128k" or precision != "bf16" or (w.Hq, w.Hkv) != (32, 8):
         return None
-    src = b"".join(open(os.path.join(ROOT, "free_block_sparse_gb300", "csrc", f), "rb").read()
-                   for f in ("bsattn.cu", "common.cuh"))
-    sha = hashlib.sha256(src).hexdigest()[:16]
+    sha = code_digest(os.path.join(ROOT, "free_block_sparse_gb300", "csrc", f) for f in ("bsattn.cu", "common.cuh"))
     path = os.path.join(ROOT, "profiles", "bsattn_llama128k_h4.md")
     if not os.path.exists(path):
         return None
@@ -194,7 +205,7 @@ def profile_traffic(w, precision):
         if ":" in line and line.startswith("- "):
             k, v = line[2:].split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
-    if fields.get("source sha256 (bsattn.cu + common.cuh)") != sha:
+    if fields.get("code sha256 (bsattn.cu + common.cuh)") != sha:
         return None
     return int(fields["traffic per full launch (bytes)"])
 

@@ -185,7 +185,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   // work item: (b, kvh) outermost so concurrently resident CTAs share K/V in L2; within it the
   // query blocks go from last to first (most causal work first), heads of a group adjacent.
   // A decoding tile (DEC) holds the Nq query rows of all G heads of one KV head (row g Nq + qi is
-  // query qi of head kvh G + g) against one chunk of the key blocks.
+  // query qi of head kvh G + g) against one share of the key blocks those heads keep (lo and
+  // n_valid only count the chunk's key range for the counters).
   int b, kvh, i, h, lo = 0, n_valid;
   if constexpr (DEC) {
     const int chunk = blockIdx.x % a.nchunk, bk = blockIdx.x / a.nchunk;
