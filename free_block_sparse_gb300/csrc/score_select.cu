@@ -288,16 +288,21 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
     // until the cut among them is known (patched below).
     while (ok) {
       int n = 0;
-      float4 sn = load_s(srow, 4 * lane, nvalid);  // loaded one stretch ahead
+      // the scores and the key blocks' similarities, both loaded one stretch ahead (s_K has
+      // nkb_pad >= j0 + 4 entries per row)
+      float4 sn = load_s(srow, 4 * lane, nvalid);
+      float4 kn = load_s(sKrow, 4 * lane, nvalid);
       for (int t = 0; t < nit; ++t) {
         const int j0 = 128 * t + 4 * lane;
-        const float4 sv = sn;
-        if (t + 1 < nit) sn = load_s(srow, j0 + 128, nvalid);
+        const float4 sv = sn, sk = kn;
+        if (t + 1 < nit) {
+          sn = load_s(srow, j0 + 128, nvalid);
+          kn = load_s(sKrow, j0 + 128, nvalid);
+        }
         const float4 v = to_e(sv, j0, nvalid, negm, none);
         n = list_append(v, j0, st, Lv, Lj, n, lane);
         uint32_t word = 0u;
         if (j0 < nvalid) {
-          const float4 sk = __ldg(reinterpret_cast<const float4 *>(sKrow + j0));
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const bool keep = j0 + u < nvalid && (__float_as_uint(comp(v, u)) >= st.hi || comp(sk, u) < theta);
