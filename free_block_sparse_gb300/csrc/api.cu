@@ -277,6 +277,9 @@ int predict_impl(const View &q, const View &k, float topk, float theta, int caus
         (rc = make_map_s(&g.ts, pw.S, pw.nkb_pad, nqb, q.B * q.H)))
       return rc;
     g.Smax = pw.Smax;
+    g.muQ = pw.muQ;
+    g.muK = pw.muK;
+    g.S = pw.S;
     g.splits = pw.smax_splits;
     g.smax_stride = pw.smax_stride;
     g.nkb_pad = pw.nkb_pad;

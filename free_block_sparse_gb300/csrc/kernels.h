@@ -42,8 +42,20 @@ inline int score_gemm_slices(int64_t Nk) {
   const int64_t nch = ((Nk + 63) / 64 + 127) / 128;
   return static_cast<int>(nch < 1 ? 1 : (nch < SCORE_GEMM_MAX_SPLITS ? nch : SCORE_GEMM_MAX_SPLITS));
 }
+// With at most SCORE_ROW_KERNEL_ROWS query-block rows in all (decoding steps, short chunks) the
+// pooled scores come from a row kernel instead of the tensor-core product (a 128-row MMA tile
+// would be almost empty): one CTA per (row, 256 key blocks), fp32 dot products of the fp32 means,
+// each CTA's row maximum in its own Smax slice (at most 8, as 2048 key blocks is the longest row).
+constexpr int64_t SCORE_ROW_KERNEL_ROWS = 256;
+inline bool score_use_rows(int64_t B, int64_t Hq, int64_t Nq) {
+  return B * Hq * ((Nq + 127) / 128) <= SCORE_ROW_KERNEL_ROWS;
+}
 inline int score_gemm_splits(int64_t B, int64_t Hq, int64_t Nq, int64_t Nk) {
   const int64_t nqb = (Nq + 127) / 128, nkb = (Nk + 63) / 64;
+  if (score_use_rows(B, Hq, Nq)) {
+    const int64_t s = (nkb + 255) / 256;
+    return static_cast<int>(s < 1 ? 1 : s);
+  }
   const int64_t tiles = B * Hq * ((nqb + 127) / 128), nch = (nkb + 127) / 128;
   if (tiles <= 0 || nch <= 1 || tiles >= 152) return 1;
   int64_t s = (2 * 152 + tiles - 1) / tiles;
@@ -84,6 +96,8 @@ struct ScoreGemmLaunch {
   int64_t nkb_pad;
   int splits;      // score_gemm_splits of the shape
   int64_t smax_stride;
+  const float *muQ, *muK;  // the fp32 means and S itself, for the row kernel of few-row shapes
+  float *S;
   int B, Hq, Hkv, Nq, Nk, d, causal;  // query and key lengths (causal: Nq <= Nk, the last query on the last key)
   float scale;
   int *status;

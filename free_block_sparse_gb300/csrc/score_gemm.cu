@@ -218,6 +218,53 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 5) tmem_dealloc(tmem, 256);
 }
 
+// The few-row path: S[row][j] = scale * muQ[row] . muK[j] in fp32 for the valid key blocks of
+// each row, one CTA per (row, 256 key blocks) and one key block per thread: the row's mean is
+// staged in shared memory (read as a broadcast), each thread streams its block's mean as D / 4
+// independent 16-byte loads into four FMA chains, and the threads' scores go out as one
+// coalesced row; the CTA's maximum over its valid blocks goes to its own Smax slice.
+template <int D>
+__global__ void __launch_bounds__(256) score_rows_kernel(const float *__restrict__ muQ, const float *__restrict__ muK,
+                                                         float *S, float *Smax, int64_t smax_stride, int64_t nkb_pad,
+                                                         int Hq, int Hkv, int nqb, int nkb, int causal, int off,
+                                                         float scale) {
+  __shared__ float4 qs[D / 4];
+  __shared__ float wmax[8];
+  const int row = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = row / nqb, i = row - bh * nqb, b = bh / Hq, h = bh - b * Hq, kvh = h / (Hq / Hkv);
+  const int nvalid = causal ? min(nkb, causal_key_blocks(i, off)) : nkb;
+  if (threadIdx.x < D / 4) qs[threadIdx.x] = __ldg(reinterpret_cast<const float4 *>(muQ + static_cast<int64_t>(row) * D) + threadIdx.x);
+  __syncthreads();
+  const int j = static_cast<int>(blockIdx.y) * 256 + static_cast<int>(threadIdx.x);
+  float m = -3.402823466e38f;
+  if (j < nvalid) {
+    const float4 *kr = reinterpret_cast<const float4 *>(muK + ((static_cast<int64_t>(b) * Hkv + kvh) * nkb + j) * D);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < D / 4; ++u) {
+      const float4 kv = __ldg(kr + u), qv = qs[u];
+      float a = acc[u & 3];
+      a = fmaf(qv.x, kv.x, a);
+      a = fmaf(qv.y, kv.y, a);
+      a = fmaf(qv.z, kv.z, a);
+      a = fmaf(qv.w, kv.w, a);
+      acc[u & 3] = a;
+    }
+    const float sc = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * scale;
+    S[static_cast<int64_t>(row) * nkb_pad + j] = sc;
+    m = sc;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) wmax[w] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mm = wmax[0];
+    for (int u = 1; u < 8; ++u) mm = fmaxf(mm, wmax[u]);
+    Smax[blockIdx.y * smax_stride + row] = mm;
+  }
+}
+
 template <int D>
 cudaError_t launch_d(const ScoreGemmLaunch &l, const GemmArgs &a, cudaStream_t st) {
   const uint32_t smem = GL<D>::TOTAL;
@@ -252,6 +299,19 @@ cudaError_t launch_score_gemm(const ScoreGemmLaunch &l, cudaStream_t st) {
     if ((nch_all + a.per_split - 1) / a.per_split > sp) return cudaErrorInvalidValue;  // more slices than Smax has
   }
   if (static_cast<int64_t>(a.B) * a.Hq * a.ngroups == 0) return cudaSuccess;
+  if (score_use_rows(l.B, l.Hq, l.Nq)) {
+    const int64_t rows = static_cast<int64_t>(a.B) * a.Hq * a.nqb;
+    const unsigned zs = static_cast<unsigned>((a.nkb + 255) / 256);
+    if (static_cast<int>(zs) != l.splits || !l.muQ || !l.muK || !l.S) return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>(rows), zs);
+    if (l.d == 128)
+      score_rows_kernel<128><<<grid, 256, 0, st>>>(l.muQ, l.muK, l.S, a.Smax, a.smax_stride, a.nkb_pad, a.Hq, a.Hkv,
+                                                   a.nqb, a.nkb, a.causal, a.off, a.scale);
+    else
+      score_rows_kernel<64><<<grid, 256, 0, st>>>(l.muQ, l.muK, l.S, a.Smax, a.smax_stride, a.nkb_pad, a.Hq, a.Hkv,
+                                                  a.nqb, a.nkb, a.causal, a.off, a.scale);
+    return cudaGetLastError();
+  }
   return l.d == 128 ? launch_d<128>(l, a, st) : launch_d<64>(l, a, st);
 }
 
