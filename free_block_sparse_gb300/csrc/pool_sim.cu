@@ -45,25 +45,28 @@ __global__ void __launch_bounds__(128, GATHER ? 4 : 5) pool_sim_kernel(PoolArgs 
   for (int64_t bid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; bid < a.total;
        bid += nwarps) {
     // ---- which block ----
-    const bool isQ = bid < a.nq_total;
+    // 32-bit block arithmetic (the host keeps the block count below 2^31): 64-bit divisions
+    // would sit between one block's last loads and the next block's first
+    const uint32_t ub = static_cast<uint32_t>(bid), nqt = static_cast<uint32_t>(a.nq_total);
+    const bool isQ = ub < nqt;
     int b, h, idx, n, rows;
     const __nv_bfloat16 *base;
     int64_t sn, row;
     if (isQ) {
-      idx = static_cast<int>(bid % a.nqb);
-      const int64_t bh = bid / a.nqb;
-      h = static_cast<int>(bh % a.Hq);
-      b = static_cast<int>(bh / a.Hq);
+      const uint32_t bh = ub / static_cast<uint32_t>(a.nqb);
+      idx = static_cast<int>(ub - bh * static_cast<uint32_t>(a.nqb));
+      h = static_cast<int>(bh % static_cast<uint32_t>(a.Hq));
+      b = static_cast<int>(bh / static_cast<uint32_t>(a.Hq));
       rows = QBLK;
       sn = a.q_sn;
       base = a.q + b * a.q_sb + h * a.q_sh + static_cast<int64_t>(idx) * QBLK * sn;
       row = (static_cast<int64_t>(b) * a.Hq + h) * a.nqb + idx;
     } else {
-      const int64_t kb = bid - a.nq_total;
-      idx = static_cast<int>(kb % a.nkb);
-      const int64_t bh = kb / a.nkb;
-      h = static_cast<int>(bh % a.Hkv);
-      b = static_cast<int>(bh / a.Hkv);
+      const uint32_t kb = ub - nqt;
+      const uint32_t bh = kb / static_cast<uint32_t>(a.nkb);
+      idx = static_cast<int>(kb - bh * static_cast<uint32_t>(a.nkb));
+      h = static_cast<int>(bh % static_cast<uint32_t>(a.Hkv));
+      b = static_cast<int>(bh / static_cast<uint32_t>(a.Hkv));
       rows = KBLK;
       sn = a.k_sn;
       base = a.k + b * a.k_sb + h * a.k_sh + static_cast<int64_t>(idx) * KBLK * sn;
@@ -209,6 +212,7 @@ cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, c
   a.qcopy = qperm ? static_cast<__nv_bfloat16 *>(qcopy) : nullptr;
   a.kcopy = kperm ? static_cast<__nv_bfloat16 *>(kcopy) : nullptr;
   if (a.total == 0) return cudaSuccess;
+  if (a.total > 0x7fffffffLL) return cudaErrorInvalidValue;  // the kernel's block arithmetic is 32-bit
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
