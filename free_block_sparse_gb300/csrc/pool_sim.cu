@@ -5,11 +5,11 @@
 // the valid tokens and s = ||(1/n) sum_a x_a / ||x_a|| ||^2, the mean cosine similarity over
 // all ordered token pairs of the block (pairs a == b included).  A zero token contributes a
 // zero unit vector.  Memory-bound: one pass over Q and K.  One warp per block, no block-level
-// barriers: each lane keeps eight 16-byte loads in flight in a rolling register buffer while it
-// accumulates, so many warps per SM keep enough bytes in flight to hold HBM busy; fp32 (packed
-// pair) arithmetic, warp-shuffle reductions, vector stores of the results.  Under a token order
-// (Hilbert order of image or video tokens) a block's rows are gathered whole through the order
-// (its indices read once into shared memory), so the pooling needs no ordered copy of Q or K; it
+// barriers, fp32 (packed pair) arithmetic, warp-shuffle reductions, vector stores of the results.
+// The plain pooling streams each block's rows through a per-lane ring of shared-memory slots
+// filled by cp.async well ahead of the arithmetic, so the bytes in flight cost no registers.  Under a token order (Hilbert order of image or video tokens) a
+// block's rows are gathered whole through the order (its indices read once into shared memory)
+// into a rolling register window of loads, so the pooling needs no ordered copy of Q or K; it
 // writes the ordered copies the later kernels read as it goes (the rows are in its registers).
 #include "common.cuh"
 #include "kernels.h"
@@ -31,12 +31,178 @@ struct PoolArgs {
 
 constexpr int INFLIGHT = 8;  // 16-byte loads in flight per lane
 
-// GATHER: rows come through the token orders (a separate instantiation, so the plain streaming
-// kernel keeps its registers).
-template <int D, bool GATHER>
-__global__ void __launch_bounds__(128, GATHER ? 4 : 5) pool_sim_kernel(PoolArgs a) {
+// One block's place in the inputs and outputs: block ub of the Q blocks then the K blocks
+// (32-bit arithmetic: the host keeps the block count below 2^31).
+struct BlockRef {
+  const __nv_bfloat16 *base;  // the block's first row
+  int64_t sn, row;            // row stride; the block's index in the pooled outputs
+  int b, h, idx, n, rows, ntok;
+  bool isQ;
+};
+__device__ __forceinline__ BlockRef block_ref(const PoolArgs &a, uint32_t ub) {
+  BlockRef r;
+  const uint32_t nqt = static_cast<uint32_t>(a.nq_total);
+  r.isQ = ub < nqt;
+  if (r.isQ) {
+    const uint32_t bh = ub / static_cast<uint32_t>(a.nqb);
+    r.idx = static_cast<int>(ub - bh * static_cast<uint32_t>(a.nqb));
+    r.h = static_cast<int>(bh % static_cast<uint32_t>(a.Hq));
+    r.b = static_cast<int>(bh / static_cast<uint32_t>(a.Hq));
+    r.rows = QBLK;
+    r.sn = a.q_sn;
+    r.base = a.q + r.b * a.q_sb + r.h * a.q_sh + static_cast<int64_t>(r.idx) * QBLK * r.sn;
+    r.row = (static_cast<int64_t>(r.b) * a.Hq + r.h) * a.nqb + r.idx;
+    r.ntok = a.Nq;
+  } else {
+    const uint32_t kb = ub - nqt;
+    const uint32_t bh = kb / static_cast<uint32_t>(a.nkb);
+    r.idx = static_cast<int>(kb - bh * static_cast<uint32_t>(a.nkb));
+    r.h = static_cast<int>(bh % static_cast<uint32_t>(a.Hkv));
+    r.b = static_cast<int>(bh / static_cast<uint32_t>(a.Hkv));
+    r.rows = KBLK;
+    r.sn = a.k_sn;
+    r.base = a.k + r.b * a.k_sb + r.h * a.k_sh + static_cast<int64_t>(r.idx) * KBLK * r.sn;
+    r.row = (static_cast<int64_t>(r.b) * a.Hkv + r.h) * a.nkb + r.idx;
+    r.ntok = a.Nk;
+  }
+  r.n = min(r.rows, r.ntok - r.idx * r.rows);
+  return r;
+}
+
+// One token's 8 coordinates held by this lane (LPT lanes per token): adds them to the running
+// sum and their share of the unit vector x / ||x|| (the norm from a shuffle over the LPT lanes).
+template <int LPT>
+__device__ __forceinline__ void pool_accumulate(const uint4 v, float2 (&sx2)[4], float2 (&sh2)[4]) {
+  const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+  float2 x2[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) x2[c] = make_float2(bf16lo(wd[c]), bf16hi(wd[c]));
+  float2 n2 = fmul2(x2[0], x2[0]);
+#pragma unroll
+  for (int c = 1; c < 4; ++c) n2 = ffma2(x2[c], x2[c], n2);
+  float nn = n2.x + n2.y;
+#pragma unroll
+  for (int off = LPT / 2; off > 0; off >>= 1) nn += __shfl_xor_sync(0xffffffffu, nn, off);
+  const float inv = nn > 0.f ? rsqrtf(nn) : 0.f;
+  const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    sx2[c] = fadd2(sx2[c], x2[c]);
+    sh2[c] = ffma2(x2[c], inv2, sh2[c]);
+  }
+}
+
+// The block's results from the lanes' sums: the mean, its bf16 hi/lo split and s.
+template <int D>
+__device__ __forceinline__ void pool_finish(const PoolArgs &a, const BlockRef &r, int lane, float2 (&sx2)[4],
+                                            float2 (&sh2)[4]) {
+  constexpr int LPT = D / 8;
+  const int sub = lane / LPT, part = lane % LPT;
+  // sum over the token slots of the warp (lanes with the same part)
+#pragma unroll
+  for (int off = LPT; off < 32; off <<= 1) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      sx2[c].x += __shfl_xor_sync(0xffffffffu, sx2[c].x, off);
+      sx2[c].y += __shfl_xor_sync(0xffffffffu, sx2[c].y, off);
+      sh2[c].x += __shfl_xor_sync(0xffffffffu, sh2[c].x, off);
+      sh2[c].y += __shfl_xor_sync(0xffffffffu, sh2[c].y, off);
+    }
+  }
+  const float invn = 1.f / static_cast<float>(r.n);
+  float hsq = 0.f;
+  if (sub == 0) {  // lanes 0..LPT-1 own dims 8 part .. 8 part + 7
+    float mean[8];
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      mean[2 * c] = sx2[c].x * invn;
+      mean[2 * c + 1] = sx2[c].y * invn;
+      const float h0 = sh2[c].x * invn, h1 = sh2[c].y * invn;
+      hsq = fmaf(h0, h0, fmaf(h1, h1, hsq));
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const __nv_bfloat16 a0 = __float2bfloat16_rn(mean[2 * c]), a1 = __float2bfloat16_rn(mean[2 * c + 1]);
+      const __nv_bfloat16 b0 = __float2bfloat16_rn(mean[2 * c] - __bfloat162float(a0));
+      const __nv_bfloat16 b1 = __float2bfloat16_rn(mean[2 * c + 1] - __bfloat162float(a1));
+      hi[c] = static_cast<uint32_t>(__bfloat16_as_ushort(a0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(a1)) << 16);
+      lo[c] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b1)) << 16);
+    }
+    float *mu = (r.isQ ? a.ws.muQ : a.ws.muK) + r.row * D + part * 8;
+    *reinterpret_cast<float4 *>(mu) = make_float4(mean[0], mean[1], mean[2], mean[3]);
+    *reinterpret_cast<float4 *>(mu + 4) = make_float4(mean[4], mean[5], mean[6], mean[7]);
+    *reinterpret_cast<uint4 *>((r.isQ ? a.ws.qhi : a.ws.khi) + r.row * D + part * 8) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4 *>((r.isQ ? a.ws.qlo : a.ws.klo) + r.row * D + part * 8) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) hsq += __shfl_xor_sync(0xffffffffu, hsq, off);
+  if (lane == 0) {
+    if (r.isQ)
+      a.ws.sQ[r.row] = hsq;
+    else
+      a.ws.sK[(static_cast<int64_t>(r.b) * a.Hkv + r.h) * a.ws.nkb_pad + r.idx] = hsq;
+  }
+}
+
+// The plain (unordered) pooling: each warp takes its blocks one after another and streams a
+// block's rows through a ring of RING 16-byte slots per lane in shared memory, filled by cp.async
+// RING warp-wide steps ahead of the arithmetic (rows past the block's valid tokens zero-filled),
+// so the bytes in flight cost no registers; each lane reads back only the slots it filled.
+// (Letting the ring run on into the warp's next block, with no drain at block ends, measured
+// slower: 0.28 against 0.235 ms at 128K.)
+constexpr int RING = 16;
+template <int D>
+__global__ void __launch_bounds__(128, 5) pool_stream_kernel(PoolArgs a) {
+  __shared__ __align__(16) uint8_t ring_smem[4][RING * 512];
+  constexpr int LPT = D / 8;     // lanes per token, 8 bf16 (16 bytes) per lane
+  constexpr int TPW = 32 / LPT;  // tokens per warp-wide step
+  const int lane = threadIdx.x & 31, sub = lane / LPT, part = lane % LPT;
+  const uint32_t ring = smem_u32(ring_smem[threadIdx.x >> 5]) + lane * 16;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t bid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; bid < a.total;
+       bid += nwarps) {
+    const BlockRef r = block_ref(a, static_cast<uint32_t>(bid));
+    const int steps = r.rows / TPW;
+    const __nv_bfloat16 *p = r.base + sub * r.sn + part * 8;
+    auto issue = [&](int s) {
+      const int t = s * TPW + sub;
+      const bool in = t < r.n;
+      const __nv_bfloat16 *src = in ? p + static_cast<int64_t>(s) * TPW * r.sn : p;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ring + (s % RING) * 512), "l"(src),
+                   "r"(in ? 16u : 0u)
+                   : "memory");
+    };
+#pragma unroll
+    for (int s = 0; s < RING; ++s) {
+      if (s < steps) issue(s);
+      asm volatile("cp.async.commit_group;" ::: "memory");  // one group per step, empty or not
+    }
+    float2 sx2[4], sh2[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) sx2[c] = sh2[c] = make_float2(0.f, 0.f);
+    for (int s = 0; s < steps; ++s) {
+      asm volatile("cp.async.wait_group %0;" ::"n"(RING - 1) : "memory");  // step s has landed
+      uint4 v;
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(ring + (s % RING) * 512)
+                   : "memory");
+      pool_accumulate<LPT>(v, sx2, sh2);
+      if (s + RING < steps) issue(s + RING);  // into the slot just read (v is used above)
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    pool_finish<D>(a, r, lane, sx2, sh2);
+  }
+}
+
+// Under a token order: each lane keeps INFLIGHT 16-byte loads of gathered rows in flight in a
+// rolling register window (the token indices of a block read once into shared memory).
+template <int D>
+__global__ void __launch_bounds__(128, 4) pool_gather_kernel(PoolArgs a) {
   constexpr int IFL = INFLIGHT;
-  __shared__ int sperm[GATHER ? 4 : 1][GATHER ? QBLK : 1];  // the block's token indices, per warp
+  __shared__ int sperm[4][QBLK];  // the block's token indices, per warp
   constexpr int LPT = D / 8;     // lanes per token, 8 bf16 (16 bytes) per lane
   constexpr int TPW = 32 / LPT;  // tokens per warp-wide load
   const int lane = threadIdx.x & 31;
@@ -44,68 +210,35 @@ __global__ void __launch_bounds__(128, GATHER ? 4 : 5) pool_sim_kernel(PoolArgs 
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t bid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; bid < a.total;
        bid += nwarps) {
-    // ---- which block ----
-    // 32-bit block arithmetic (the host keeps the block count below 2^31): 64-bit divisions
-    // would sit between one block's last loads and the next block's first
-    const uint32_t ub = static_cast<uint32_t>(bid), nqt = static_cast<uint32_t>(a.nq_total);
-    const bool isQ = ub < nqt;
-    int b, h, idx, n, rows;
-    const __nv_bfloat16 *base;
-    int64_t sn, row;
-    if (isQ) {
-      const uint32_t bh = ub / static_cast<uint32_t>(a.nqb);
-      idx = static_cast<int>(ub - bh * static_cast<uint32_t>(a.nqb));
-      h = static_cast<int>(bh % static_cast<uint32_t>(a.Hq));
-      b = static_cast<int>(bh / static_cast<uint32_t>(a.Hq));
-      rows = QBLK;
-      sn = a.q_sn;
-      base = a.q + b * a.q_sb + h * a.q_sh + static_cast<int64_t>(idx) * QBLK * sn;
-      row = (static_cast<int64_t>(b) * a.Hq + h) * a.nqb + idx;
-    } else {
-      const uint32_t kb = ub - nqt;
-      const uint32_t bh = kb / static_cast<uint32_t>(a.nkb);
-      idx = static_cast<int>(kb - bh * static_cast<uint32_t>(a.nkb));
-      h = static_cast<int>(bh % static_cast<uint32_t>(a.Hkv));
-      b = static_cast<int>(bh / static_cast<uint32_t>(a.Hkv));
-      rows = KBLK;
-      sn = a.k_sn;
-      base = a.k + b * a.k_sb + h * a.k_sh + static_cast<int64_t>(idx) * KBLK * sn;
-      row = (static_cast<int64_t>(b) * a.Hkv + h) * a.nkb + idx;
-    }
-    const int ntok = isQ ? a.Nq : a.Nk;
-    n = min(rows, ntok - idx * rows);
-    const int steps = rows / TPW;  // warp-wide loads covering the block (a multiple of IFL)
-    const __nv_bfloat16 *p = base + sub * sn + part * 8;
-    // under a token order the block's row t is token perm[t] of the head (gathered whole rows)
-    const int32_t *perm = isQ ? a.qperm : a.kperm;
-    const __nv_bfloat16 *hbase = base - static_cast<int64_t>(idx) * rows * sn + part * 8;
-    int *wperm = GATHER ? sperm[(threadIdx.x >> 5) & 3] : nullptr;
+    const BlockRef r = block_ref(a, static_cast<uint32_t>(bid));
+    const int n = r.n, steps = r.rows / TPW;  // warp-wide loads covering the block (a multiple of IFL)
+    const __nv_bfloat16 *p = r.base + sub * r.sn + part * 8;
+    // the block's row t is token perm[t] of the head (gathered whole rows)
+    const int32_t *perm = r.isQ ? a.qperm : a.kperm;
+    const __nv_bfloat16 *hbase = r.base - static_cast<int64_t>(r.idx) * r.rows * r.sn + part * 8;
+    int *wperm = sperm[(threadIdx.x >> 5) & 3];
     // the block's rows of the ordered copy (this lane's 16 bytes of row 0), when one is wanted
     __nv_bfloat16 *cpy = nullptr;
-    if constexpr (GATHER) {
-      __nv_bfloat16 *cbase = isQ ? a.qcopy : a.kcopy;
-      if (cbase != nullptr)
-        cpy = cbase + ((static_cast<int64_t>(b) * (isQ ? a.Hq : a.Hkv) + h) * ntok + static_cast<int64_t>(idx) * rows) * D +
-              part * 8;
-    }
-    if constexpr (GATHER) {
-      if (perm != nullptr) {  // one coalesced read of the block's indices; bad ones become -1
-        __syncwarp();  // every lane is done with the previous block's indices
-        for (int u = lane; u < n; u += 32) {
-          const int src = __ldg(perm + idx * rows + u);
-          const bool good = static_cast<unsigned>(src) < static_cast<unsigned>(ntok);
-          if (!good) record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
-          wperm[u] = good ? src : -1;
-        }
-        __syncwarp();
+    __nv_bfloat16 *cbase = r.isQ ? a.qcopy : a.kcopy;
+    if (cbase != nullptr)
+      cpy = cbase + ((static_cast<int64_t>(r.b) * (r.isQ ? a.Hq : a.Hkv) + r.h) * r.ntok +
+                     static_cast<int64_t>(r.idx) * r.rows) * D + part * 8;
+    if (perm != nullptr) {  // one coalesced read of the block's indices; bad ones become -1
+      __syncwarp();  // every lane is done with the previous block's indices
+      for (int u = lane; u < n; u += 32) {
+        const int src = __ldg(perm + r.idx * r.rows + u);
+        const bool good = static_cast<unsigned>(src) < static_cast<unsigned>(r.ntok);
+        if (!good) record_status(a.status, -1 /* SPARGE_ERR_INVALID_ARG */);
+        wperm[u] = good ? src : -1;
       }
+      __syncwarp();
     }
     auto load = [&](int s) {
       const int t = s * TPW + sub;
       if (t >= n) return make_uint4(0, 0, 0, 0);
-      if (!GATHER || perm == nullptr) return ld_stream_v4(p + static_cast<int64_t>(s) * TPW * sn);
+      if (perm == nullptr) return ld_stream_v4(p + static_cast<int64_t>(s) * TPW * r.sn);
       const int src = wperm[t];
-      return src >= 0 ? ld_stream_v4(hbase + static_cast<int64_t>(src) * sn) : make_uint4(0, 0, 0, 0);
+      return src >= 0 ? ld_stream_v4(hbase + static_cast<int64_t>(src) * r.sn) : make_uint4(0, 0, 0, 0);
     };
     uint4 buf[IFL];
 #pragma unroll
@@ -118,74 +251,12 @@ __global__ void __launch_bounds__(128, GATHER ? 4 : 5) pool_sim_kernel(PoolArgs 
       for (int u = 0; u < IFL; ++u) {
         const uint4 v = buf[u];
         if (s0 + IFL + u < steps) buf[u] = load(s0 + IFL + u);
-        if constexpr (GATHER) {
-          const int t = (s0 + u) * TPW + sub;
-          if (cpy != nullptr && t < n) *reinterpret_cast<uint4 *>(cpy + static_cast<int64_t>(t) * D) = v;
-        }
-        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-        float2 x2[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) x2[c] = make_float2(bf16lo(wd[c]), bf16hi(wd[c]));
-        float2 n2 = fmul2(x2[0], x2[0]);
-#pragma unroll
-        for (int c = 1; c < 4; ++c) n2 = ffma2(x2[c], x2[c], n2);
-        float nn = n2.x + n2.y;
-#pragma unroll
-        for (int off = LPT / 2; off > 0; off >>= 1) nn += __shfl_xor_sync(0xffffffffu, nn, off);
-        const float inv = nn > 0.f ? rsqrtf(nn) : 0.f;
-        const float2 inv2 = make_float2(inv, inv);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          sx2[c] = fadd2(sx2[c], x2[c]);
-          sh2[c] = ffma2(x2[c], inv2, sh2[c]);
-        }
+        const int t = (s0 + u) * TPW + sub;
+        if (cpy != nullptr && t < n) *reinterpret_cast<uint4 *>(cpy + static_cast<int64_t>(t) * D) = v;
+        pool_accumulate<LPT>(v, sx2, sh2);
       }
     }
-    // sum over the token slots of the warp (lanes with the same part)
-#pragma unroll
-    for (int off = LPT; off < 32; off <<= 1) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        sx2[c].x += __shfl_xor_sync(0xffffffffu, sx2[c].x, off);
-        sx2[c].y += __shfl_xor_sync(0xffffffffu, sx2[c].y, off);
-        sh2[c].x += __shfl_xor_sync(0xffffffffu, sh2[c].x, off);
-        sh2[c].y += __shfl_xor_sync(0xffffffffu, sh2[c].y, off);
-      }
-    }
-    const float invn = 1.f / static_cast<float>(n);
-    float hsq = 0.f;
-    if (sub == 0) {  // lanes 0..LPT-1 own dims 8 part .. 8 part + 7
-      float mean[8];
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        mean[2 * c] = sx2[c].x * invn;
-        mean[2 * c + 1] = sx2[c].y * invn;
-        const float h0 = sh2[c].x * invn, h1 = sh2[c].y * invn;
-        hsq = fmaf(h0, h0, fmaf(h1, h1, hsq));
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const __nv_bfloat16 a0 = __float2bfloat16_rn(mean[2 * c]), a1 = __float2bfloat16_rn(mean[2 * c + 1]);
-        const __nv_bfloat16 b0 = __float2bfloat16_rn(mean[2 * c] - __bfloat162float(a0));
-        const __nv_bfloat16 b1 = __float2bfloat16_rn(mean[2 * c + 1] - __bfloat162float(a1));
-        hi[c] = static_cast<uint32_t>(__bfloat16_as_ushort(a0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(a1)) << 16);
-        lo[c] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b1)) << 16);
-      }
-      float *mu = (isQ ? a.ws.muQ : a.ws.muK) + row * D + part * 8;
-      *reinterpret_cast<float4 *>(mu) = make_float4(mean[0], mean[1], mean[2], mean[3]);
-      *reinterpret_cast<float4 *>(mu + 4) = make_float4(mean[4], mean[5], mean[6], mean[7]);
-      *reinterpret_cast<uint4 *>((isQ ? a.ws.qhi : a.ws.khi) + row * D + part * 8) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4 *>((isQ ? a.ws.qlo : a.ws.klo) + row * D + part * 8) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) hsq += __shfl_xor_sync(0xffffffffu, hsq, off);
-    if (lane == 0) {
-      if (isQ)
-        a.ws.sQ[row] = hsq;
-      else
-        a.ws.sK[(static_cast<int64_t>(b) * a.Hkv + h) * a.ws.nkb_pad + idx] = hsq;
-    }
+    pool_finish<D>(a, r, lane, sx2, sh2);
   }
 }
 
@@ -223,14 +294,14 @@ cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, c
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
   if (q.d == 128) {
     if (gather)
-      pool_sim_kernel<128, true><<<grid, 128, 0, st>>>(a);
+      pool_gather_kernel<128><<<grid, 128, 0, st>>>(a);
     else
-      pool_sim_kernel<128, false><<<grid, 128, 0, st>>>(a);
+      pool_stream_kernel<128><<<grid, 128, 0, st>>>(a);
   } else {
     if (gather)
-      pool_sim_kernel<64, true><<<grid, 128, 0, st>>>(a);
+      pool_gather_kernel<64><<<grid, 128, 0, st>>>(a);
     else
-      pool_sim_kernel<64, false><<<grid, 128, 0, st>>>(a);
+      pool_stream_kernel<64><<<grid, 128, 0, st>>>(a);
   }
   return cudaGetLastError();
 }
