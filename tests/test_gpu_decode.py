@@ -77,10 +77,12 @@ def test_decode_equals_regular_kernel_closely():
     assert cos >= 0.99999 and err <= 1e-2, (cos, err)
 
 
-def test_decode_through_sparge_attn_ex():
+@pytest.mark.parametrize("N", [4096 + 200, 40000 + 37])
+def test_decode_through_sparge_attn_ex(N):
     """A decoding step with the predicted mask: one query token per head continuing a Llama-like
-    sequence of 4296 keys (8 query heads, 2 KV heads)."""
-    w = W.make_config("llama32k", N=4096 + 200, Hq=8, Hkv=2)
+    sequence (8 query heads, 2 KV heads); at 40037 keys the pooled scores of the few query rows
+    come in three slices of 256 key blocks with their own row maxima."""
+    w = W.make_config("llama32k", N=N, Hq=8, Hkv=2)
     q = w.q[:, :, -1:]
     qd, k, v = dev_bf16(np.ascontiguousarray(q)), dev_bf16(w.k), dev_bf16(w.v)
     mask = torch.empty((1, 8, 1, w.nkb), dtype=torch.uint8, device="cuda")
