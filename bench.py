@@ -474,6 +474,9 @@ def run_ours(args, rank, world, local_rank):
     e2e_step(0)
     e2e_step(1)
     torch.cuda.synchronize()
+    e2e_clocks = ClockSampler(local_rank)   # the clocks of this region too (copies and compute together)
+    e2e_clocks.start()
+    time.sleep(0.5)
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(s_in)              # before the first copy in
     s_in.wait_event(a0)
@@ -482,6 +485,7 @@ def run_ours(args, rank, world, local_rank):
     stream.wait_stream(s_out)
     a1.record(stream)            # after the last copy back
     torch.cuda.synchronize()
+    e2e_clk = e2e_clocks.stop()
     e2e_t = a0.elapsed_time(a1) / 1e3 / e2e_steps
     for b in range(2):
         assert torch.equal(ho[b], o.cpu())
@@ -564,7 +568,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": profile_traffic(w, args.precision)},
         "e2e": {"value": round(world * dense / e2e_t / 1e12, 2), "unit": "dense-equiv TOPS",
                 "h2d_bytes_per_step": int(w.q.nbytes + w.k.nbytes + w.v.nbytes),
-                "d2h_bytes_per_step": int(o.numel() * 2)},
+                "d2h_bytes_per_step": int(o.numel() * 2), "clocks": e2e_clk},
         "gpu_launches": (LAUNCHES_PER_STEP[(args.precision, given_mask)] + order_copies) * args.steps,
         "clocks": clk,
     }
