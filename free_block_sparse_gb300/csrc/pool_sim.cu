@@ -6,11 +6,11 @@
 // all ordered token pairs of the block (pairs a == b included).  A zero token contributes a
 // zero unit vector.  Memory-bound: one pass over Q and K.  One warp per block, no block-level
 // barriers, fp32 (packed pair) arithmetic, warp-shuffle reductions, vector stores of the results.
-// The plain pooling streams each block's rows through a per-lane ring of shared-memory slots
-// filled by cp.async well ahead of the arithmetic, so the bytes in flight cost no registers.  Under a token order (Hilbert order of image or video tokens) a
-// block's rows are gathered whole through the order (its indices read once into shared memory)
-// into a rolling register window of loads, so the pooling needs no ordered copy of Q or K; it
-// writes the ordered copies the later kernels read as it goes (the rows are in its registers).
+// A block's rows stream through a per-lane ring of shared-memory slots filled by cp.async well
+// ahead of the arithmetic, so the bytes in flight cost no registers.  Under a token order (Hilbert
+// order of image or video tokens) the rows are gathered whole through the order (the block's
+// indices read once into shared memory), so the pooling needs no ordered copy of Q or K; it writes
+// the ordered copies the later kernels read as it goes (the rows pass through its registers).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -28,8 +28,6 @@ struct PoolArgs {
   __nv_bfloat16 *qcopy, *kcopy;  // with a token order: contiguous (B, H, N, d) copies in that order
                                  // that the pooling writes as it reads the rows (or nullptr)
 };
-
-constexpr int INFLIGHT = 8;  // 16-byte loads in flight per lane
 
 // One block's place in the inputs and outputs: block ub of the Q blocks then the K blocks
 // (32-bit arithmetic: the host keeps the block count below 2^31).
@@ -197,21 +195,23 @@ __global__ void __launch_bounds__(128, 5) pool_stream_kernel(PoolArgs a) {
   }
 }
 
-// Under a token order: each lane keeps INFLIGHT 16-byte loads of gathered rows in flight in a
-// rolling register window (the token indices of a block read once into shared memory).
+// Under a token order: a block's token indices are read once into shared memory and its rows
+// gathered through them into the warp's cp.async ring; the rows also go out, from registers, to
+// the ordered copies the later kernels read.
 template <int D>
-__global__ void __launch_bounds__(128, 4) pool_gather_kernel(PoolArgs a) {
-  constexpr int IFL = INFLIGHT;
+__global__ void __launch_bounds__(128, 5) pool_gather_kernel(PoolArgs a) {
+  __shared__ __align__(16) uint8_t ring_smem[4][RING * 512];
   __shared__ int sperm[4][QBLK];  // the block's token indices, per warp
   constexpr int LPT = D / 8;     // lanes per token, 8 bf16 (16 bytes) per lane
   constexpr int TPW = 32 / LPT;  // tokens per warp-wide load
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPT, part = lane % LPT;
+  const uint32_t ring = smem_u32(ring_smem[threadIdx.x >> 5]) + lane * 16;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t bid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; bid < a.total;
        bid += nwarps) {
     const BlockRef r = block_ref(a, static_cast<uint32_t>(bid));
-    const int n = r.n, steps = r.rows / TPW;  // warp-wide loads covering the block (a multiple of IFL)
+    const int n = r.n, steps = r.rows / TPW;  // warp-wide steps covering the block
     const __nv_bfloat16 *p = r.base + sub * r.sn + part * 8;
     // the block's row t is token perm[t] of the head (gathered whole rows)
     const int32_t *perm = r.isQ ? a.qperm : a.kperm;
@@ -233,29 +233,47 @@ __global__ void __launch_bounds__(128, 4) pool_gather_kernel(PoolArgs a) {
       }
       __syncwarp();
     }
-    auto load = [&](int s) {
+    // the rows (gathered through the order, or in place) through the warp's cp.async ring, as in
+    // pool_stream_kernel; entries outside the order's range read as zero rows
+    auto issue = [&](int s) {
       const int t = s * TPW + sub;
-      if (t >= n) return make_uint4(0, 0, 0, 0);
-      if (perm == nullptr) return ld_stream_v4(p + static_cast<int64_t>(s) * TPW * r.sn);
-      const int src = wperm[t];
-      return src >= 0 ? ld_stream_v4(hbase + static_cast<int64_t>(src) * r.sn) : make_uint4(0, 0, 0, 0);
+      const __nv_bfloat16 *src = p;
+      bool in = t < n;
+      if (in) {
+        if (perm == nullptr) {
+          src = p + static_cast<int64_t>(s) * TPW * r.sn;
+        } else {
+          const int g = wperm[t];
+          in = g >= 0;
+          src = in ? hbase + static_cast<int64_t>(g) * r.sn : p;
+        }
+      }
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ring + (s % RING) * 512), "l"(src),
+                   "r"(in ? 16u : 0u)
+                   : "memory");
     };
-    uint4 buf[IFL];
 #pragma unroll
-    for (int u = 0; u < IFL; ++u) buf[u] = load(u);
+    for (int s = 0; s < RING; ++s) {
+      if (s < steps) issue(s);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
     float2 sx2[4], sh2[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) sx2[c] = sh2[c] = make_float2(0.f, 0.f);
-    for (int s0 = 0; s0 < steps; s0 += IFL) {
-#pragma unroll
-      for (int u = 0; u < IFL; ++u) {
-        const uint4 v = buf[u];
-        if (s0 + IFL + u < steps) buf[u] = load(s0 + IFL + u);
-        const int t = (s0 + u) * TPW + sub;
-        if (cpy != nullptr && t < n) *reinterpret_cast<uint4 *>(cpy + static_cast<int64_t>(t) * D) = v;
-        pool_accumulate<LPT>(v, sx2, sh2);
-      }
+    for (int s = 0; s < steps; ++s) {
+      asm volatile("cp.async.wait_group %0;" ::"n"(RING - 1) : "memory");
+      uint4 v;
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(ring + (s % RING) * 512)
+                   : "memory");
+      const int t = s * TPW + sub;
+      if (cpy != nullptr && t < n) *reinterpret_cast<uint4 *>(cpy + static_cast<int64_t>(t) * D) = v;
+      pool_accumulate<LPT>(v, sx2, sh2);
+      if (s + RING < steps) issue(s + RING);
+      asm volatile("cp.async.commit_group;" ::: "memory");
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     pool_finish<D>(a, r, lane, sx2, sh2);
   }
 }
@@ -289,8 +307,8 @@ cudaError_t launch_pool_sim(const View &q, const View &k, const PredictWs &ws, c
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t want = (a.total + 3) / 4;
   const bool gather = qperm != nullptr || kperm != nullptr;
-  // 5 resident CTAs of 4 warps per SM (4 when gathering through a token order: more registers)
-  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * (gather ? 4 : 5);
+  // 5 resident CTAs of 4 warps per SM (33-35 KB of ring and indices each)
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * 5;
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
   if (q.d == 128) {
     if (gather)
