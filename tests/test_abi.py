@@ -249,3 +249,55 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         fbs.sparge_attn(x, x, x)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal,precision", [
+    (1, 32, 8, 1, 131072, 128, 1, fbs.SPARGE_PRECISION_BF16),       # a decoding step: row scores, lists
+    (1, 32, 8, 131072, 131072, 128, 1, fbs.SPARGE_PRECISION_BF16),  # the 128K prefill
+    (2, 16, 4, 16, 40000, 64, 1, fbs.SPARGE_PRECISION_BF16),
+    (1, 76, 76, 16384, 16385, 64, 0, fbs.SPARGE_PRECISION_BF16),   # score splits on one side of a group
+    (1, 76, 76, 16385, 16384, 64, 0, fbs.SPARGE_PRECISION_BF16),
+    (3, 8, 2, 300, 20000, 128, 1, fbs.SPARGE_PRECISION_BF16_FP8PV),
+    (1, 4, 1, 7000, 900, 128, 0, fbs.SPARGE_PRECISION_Q8),
+    (8, 32, 8, 1, 32768, 128, 1, fbs.SPARGE_PRECISION_BF16),
+])
+def test_public_workspace_size_covers_every_shorter_query(lib, B, Hq, Hkv, Nq, Nk, d, causal, precision):
+    """sparge_workspace_bytes for N = max(Nq, Nk) is enough for sparge_attn_ex on (Nq, Nk): the
+    call passes its workspace check and stops at the next check (an unknown topk_mode), before
+    anything is enqueued; 16 bytes fail the workspace check."""
+    q8 = precision in fbs.PRECISIONS_8BIT
+    op = fbs.SPARGE_OP_ATTN_Q8 if q8 else fbs.SPARGE_OP_ATTN
+    wsb = fbs.workspace_bytes(op, B, Hq, Hkv, max(Nq, Nk), d)
+    assert wsb > 0
+    q, o = _t(B=B, H=Hq, N=Nq, d=d), _t(B=B, H=Hq, N=Nq, d=d)
+    k = _t(B=B, H=Hkv, N=Nk, d=d)
+    p = fbs.sparge_params(0.5, -math.inf, 0.0, precision, 0, None)
+    p.topk_mode = 99
+    for size, code in ((wsb, fbs.SPARGE_ERR_INVALID_ARG), (16, fbs.SPARGE_ERR_WORKSPACE_TOO_SMALL)):
+        rc = lib.sparge_attn_ex(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k), 0.5, causal, ctypes.byref(p),
+                                ctypes.byref(o), None, 0x100000, size, None)
+        err = lib.sparge_last_error()
+        assert rc == code, (size, err)
+        if code == fbs.SPARGE_ERR_INVALID_ARG:
+            assert b"topk_mode" in err, err
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (1, 32, 8, 1, 131072, 128, 1),     # decoding tiles: partial rows, lists and counts
+    (2, 16, 2, 16, 8192, 128, 1),
+    (1, 8, 1, 12, 5000, 64, 1),
+    (1, 24, 24, 4608, 4608, 128, 0),
+])
+def test_public_workspace_size_covers_block_sparse_attention(lib, B, Hq, Hkv, Nq, Nk, d, causal):
+    """The same for the block-sparse call alone (the decoding tiles' workspace included): with the
+    public size the call passes its workspace-size check and stops at the workspace alignment
+    check (a deliberately misaligned pointer), before anything is enqueued."""
+    wsb = fbs.workspace_bytes(fbs.SPARGE_OP_BLOCK_SPARSE_ATTN, B, Hq, Hkv, max(Nq, Nk), d)
+    q, o = _t(B=B, H=Hq, N=Nq, d=d), _t(B=B, H=Hq, N=Nq, d=d)
+    k = _t(B=B, H=Hkv, N=Nk, d=d)
+    p = fbs.sparge_params(0.5, -math.inf, 0.0, fbs.SPARGE_PRECISION_BF16, 0, None)
+    for size, code, word in ((wsb, fbs.SPARGE_ERR_INVALID_ARG, b"aligned"), (16, fbs.SPARGE_ERR_WORKSPACE_TOO_SMALL, b"need")):
+        rc = lib.sparge_block_sparse_attn_ex(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k), 0x2000, causal,
+                                             ctypes.byref(p), ctypes.byref(o), 0x100010, size, None)
+        err = lib.sparge_last_error()
+        assert rc == code and word in err, (size, err)
