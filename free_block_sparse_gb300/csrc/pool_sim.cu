@@ -171,23 +171,35 @@ __global__ void __launch_bounds__(128, 5) pool_stream_kernel(PoolArgs a) {
                    "r"(in ? 16u : 0u)
                    : "memory");
     };
+    // steps go in pairs (a block has an even number of steps): one group per pair
 #pragma unroll
-    for (int s = 0; s < RING; ++s) {
-      if (s < steps) issue(s);
-      asm volatile("cp.async.commit_group;" ::: "memory");  // one group per step, empty or not
+    for (int s = 0; s < RING; s += 2) {
+      if (s < steps) {
+        issue(s);
+        issue(s + 1);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");  // one group per pair, empty or not
     }
     float2 sx2[4], sh2[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) sx2[c] = sh2[c] = make_float2(0.f, 0.f);
-    for (int s = 0; s < steps; ++s) {
-      asm volatile("cp.async.wait_group %0;" ::"n"(RING - 1) : "memory");  // step s has landed
-      uint4 v;
+    for (int s = 0; s < steps; s += 2) {
+      asm volatile("cp.async.wait_group %0;" ::"n"(RING / 2 - 1) : "memory");  // pair s has landed
+      uint4 v0, v1;
       asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "=r"(v0.x), "=r"(v0.y), "=r"(v0.z), "=r"(v0.w)
                    : "r"(ring + (s % RING) * 512)
                    : "memory");
-      pool_accumulate<LPT>(v, sx2, sh2);
-      if (s + RING < steps) issue(s + RING);  // into the slot just read (v is used above)
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(v1.x), "=r"(v1.y), "=r"(v1.z), "=r"(v1.w)
+                   : "r"(ring + ((s + 1) % RING) * 512)
+                   : "memory");
+      pool_accumulate<LPT>(v0, sx2, sh2);
+      pool_accumulate<LPT>(v1, sx2, sh2);
+      if (s + RING < steps) {  // into the slots just read (v0, v1 are used above)
+        issue(s + RING);
+        issue(s + RING + 1);
+      }
       asm volatile("cp.async.commit_group;" ::: "memory");
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
