@@ -70,6 +70,15 @@ __device__ __forceinline__ float4 to_e(const float4 v, int j0, int nvalid, float
   }
   return e;
 }
+// to_e for a stretch that lies wholly inside the valid blocks (a warp-uniform case: no per-block
+// range checks; the same expression, so the same values)
+__device__ __forceinline__ float4 to_e_full(const float4 v, float negm) {
+  const float2 l2 = make_float2(LOG2E, LOG2E), nm = make_float2(negm, negm);
+  const float2 a = fmul2(fadd2(make_float2(v.x, v.y), nm), l2);
+  const float2 b = fmul2(fadd2(make_float2(v.z, v.w), nm), l2);
+  return make_float4(fminf(fast_exp2(a.x), 1.f), fminf(fast_exp2(a.y), 1.f), fminf(fast_exp2(b.x), 1.f),
+                     fminf(fast_exp2(b.y), 1.f));
+}
 __device__ __forceinline__ float4 load_e(const float *srow, int j0, int nvalid, float negm, float none = 0.f) {
   float4 e = make_float4(none, none, none, none);
   if (j0 < nvalid) {
@@ -267,7 +276,8 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
       const int j0 = 128 * t + 4 * lane;
       const float4 sv = sn;
       if (t + 1 < nit) sn = load_s(srow, j0 + 128, nvalid);
-      const float4 v = to_e(sv, j0, nvalid, negm, none);
+      const bool full = 128 * t + 128 <= nvalid;  // the whole stretch is valid (warp-uniform)
+      const float4 v = full ? to_e_full(sv, negm) : to_e(sv, j0, nvalid, negm, none);
       if (!cnt) z2 = fadd2(z2, fadd2(make_float2(v.x, v.y), make_float2(v.z, v.w)));
       hist_add4(H, lane, v, st, lim1, cnt);
     }
@@ -299,10 +309,17 @@ __global__ void __launch_bounds__(WARPS * 32, 4) score_select_kernel(SelArgs a) 
           sn = load_s(srow, j0 + 128, nvalid);
           kn = load_s(sKrow, j0 + 128, nvalid);
         }
-        const float4 v = to_e(sv, j0, nvalid, negm, none);
+        const bool full = 128 * t + 128 <= nvalid;  // the whole stretch is valid (warp-uniform)
+        const float4 v = full ? to_e_full(sv, negm) : to_e(sv, j0, nvalid, negm, none);
         n = list_append(v, j0, st, Lv, Lj, n, lane);
         uint32_t word = 0u;
-        if (j0 < nvalid) {
+        if (full) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const bool keep = __float_as_uint(comp(v, u)) >= st.hi || comp(sk, u) < theta;
+            word |= (keep ? 1u : 0u) << (8 * u);
+          }
+        } else if (j0 < nvalid) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const bool keep = j0 + u < nvalid && (__float_as_uint(comp(v, u)) >= st.hi || comp(sk, u) < theta);
