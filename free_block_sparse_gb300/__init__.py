@@ -187,13 +187,14 @@ def predict_mask_ex(q, k, topk: float, causal: bool = False, theta: float = 0.5,
     return mask
 
 
-def predict_ws_views(ws, B, Hq, Hkv, N, d):
+def predict_ws_views(ws, B, Hq, Hkv, N, d, Nk=None):
     """Views of the stage-1 workspace after predict_mask: muQ (B,Hq,nqb,d), sQ (B,Hq,nqb),
     muK (B,Hkv,nkb,d), sK (B,Hkv,nkb) and the scaled pooled scores S (B,Hq,nqb,nkb), following
     the layout the library writes (regions 256-byte aligned; fp32 except the bf16 hi/lo copies of
-    the means, which are skipped here)."""
+    the means, which are skipped here).  N is the query length, Nk the key length (default N)."""
     torch = _torch()
-    nqb, nkb = n_blocks(N)
+    nqb = n_blocks(N)[0]
+    nkb = n_blocks(N if Nk is None else Nk)[1]
     nkb_pad = -(-nkb // 4) * 4
     u8 = ws if ws.dtype == torch.uint8 else ws.view(torch.uint8)
 

@@ -77,12 +77,23 @@ def test_decode_equals_regular_kernel_closely():
     assert cos >= 0.99999 and err <= 1e-2, (cos, err)
 
 
-@pytest.mark.parametrize("N", [4096 + 200, 40000 + 37])
-def test_decode_through_sparge_attn_ex(N):
+@pytest.mark.parametrize("N,d", [(4096 + 200, 128), (40000 + 37, 128), (40000 + 37, 64)])
+def test_decode_through_sparge_attn_ex(N, d):
     """A decoding step with the predicted mask: one query token per head continuing a Llama-like
     sequence (8 query heads, 2 KV heads); at 40037 keys the pooled scores of the few query rows
     come in three slices of 256 key blocks with their own row maxima."""
-    w = W.make_config("llama32k", N=N, Hq=8, Hkv=2)
+    w = W.make_config("llama32k", N=N, Hq=8, Hkv=2, d=d)
+    # the pooled scores of the single query block (a row kernel at this shape) against the oracle's
+    qs, kd = dev_bf16(np.ascontiguousarray(w.q[:, :, -1:])), dev_bf16(w.k)
+    ws = torch.zeros(fbs.workspace_bytes(fbs.SPARGE_OP_PREDICT_MASK, 1, 8, 2, N, d), dtype=torch.uint8, device="cuda")
+    fbs.predict_mask(qs, kd, w.topk, w.theta, True, ws=ws)
+    torch.cuda.synchronize()
+    S = fbs.predict_ws_views(ws, 1, 8, 2, 1, d, Nk=N)[4].cpu().numpy().astype(np.float64)
+    rmuQ, _ = oracle.pool_sim(f64(w.q[:, :, -1:]), 128)
+    rmuK, _ = oracle.pool_sim(f64(w.k), 64)
+    rS = oracle.pooled_scores(rmuQ, rmuK, True, oracle.default_scale(d), off=N - 1)
+    valid = np.isfinite(rS)
+    np.testing.assert_allclose(S[valid], rS[valid], rtol=1e-4, atol=2e-4)
     q = w.q[:, :, -1:]
     qd, k, v = dev_bf16(np.ascontiguousarray(q)), dev_bf16(w.k), dev_bf16(w.v)
     mask = torch.empty((1, 8, 1, w.nkb), dtype=torch.uint8, device="cuda")
