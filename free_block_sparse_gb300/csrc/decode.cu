@@ -48,7 +48,8 @@ __global__ void __launch_bounds__(UNION_THREADS) decode_union_kernel(const uint8
 // The partial rows of a decoding call's chunks combined into the output: one CTA of D threads per
 // output row (b, h, qi).  The chunks' exponent references and row sums are staged in shared
 // memory, the largest reference M and the weights 2^(m_c - M) found by the first warp, then
-// thread t sums channel t over the chunks (coalesced rows of the partial outputs):
+// thread t sums channel t over the chunks (coalesced rows of the partial outputs, the first 64
+// chunks' values loaded into registers before the weights are known):
 // O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c (0 where no chunk saw a visible key).
 constexpr int MAX_DECODE_CHUNKS = 1024;
 template <int D>
