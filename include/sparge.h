@@ -234,7 +234,7 @@ int sparge_predict_mask_ex(const sparge_tensor *q, const sparge_tensor *k, float
  * tile, lists the key blocks any of the G heads keeps and splits that list into equal shares over
  * CTAs (each row masking the blocks its own head does not keep), and combines the shares' partial
  * rows in a last kernel; P.V then runs on bf16 P and V read in place (no f16 copy of
- * V; the workspace holds the partial rows instead).  The result is the same computation within
+ * V; the workspace holds the partial rows and the block lists instead).  The result is the same computation within
  * the bf16 tolerances; the lambda filter needs the tiles visited in order, so calls with it keep
  * one tile per query block and head.  Counters then count a tile once per (batch, KV head).
  * stats: optional counters (see sparge_params), may be NULL.
